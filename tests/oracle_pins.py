@@ -1,0 +1,261 @@
+"""Pins for the fp64 oracle: checks against what the pages and the mathematics fix.
+
+Each ``pin_*`` function takes an oracle front end (``oracle.Oracle``) and raises
+AssertionError when the oracle disagrees with a closed form, an invariant, a
+library routine, brute-force finite differences or a hand-worked fixture.  The
+pins are chosen so that a plausible slip anywhere in the oracle (a dropped term,
+a wrong sign or index, a transposed operand) fails at least one of them; the
+mutation test plants such slips in a copy of the oracle and checks exactly that.
+"""
+from __future__ import annotations
+
+import os
+
+import numpy as np
+import torch
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def rel(x, y):
+    """max|x - y| / max|y| (max-normalised relative error)."""
+    x, y = np.asarray(x, np.float64), np.asarray(y, np.float64)
+    den = np.max(np.abs(y))
+    return float(np.max(np.abs(x - y)) / (den if den > 0 else 1.0))
+
+
+def rnd(seed, *shape, scale=1.0):
+    return np.random.default_rng(seed).standard_normal(shape) * scale
+
+
+def case(seed, B=2, H=1, N=50, Dk=16, Dv=32, scale=1.0):
+    r = np.random.default_rng(seed)
+    q = r.standard_normal((B, H, N, Dk)) * scale
+    k = r.standard_normal((B, H, N, Dk)) * scale
+    v = r.standard_normal((B, H, N, Dv))
+    dO = r.standard_normal((B, H, N, Dv))
+    return q, k, v, dO
+
+
+def lib_phi(x):
+    """phi through the library ELU (torch, fp64), independent of the oracle."""
+    t = torch.as_tensor(np.asarray(x, np.float64))
+    return (torch.nn.functional.elu(t, alpha=1.0) + 1.0).numpy()
+
+
+# ---------------------------------------------------------------- feature map
+def pin_phi_library(orc):
+    x = np.concatenate([rnd(1, 1000, scale=3.0), np.array([0.0, -0.0, 1e-12, -1e-12, 30.0, -30.0])])
+    # the library evaluates (exp(x) - 1) + 1, exact to ~1 ulp of 1 in absolute terms
+    assert np.max(np.abs(orc.phi(x) - lib_phi(x)) / np.maximum(1.0, lib_phi(x))) < 1e-15
+    xt = torch.as_tensor(x, dtype=torch.float64).requires_grad_(True)
+    (torch.nn.functional.elu(xt) + 1.0).sum().backward()
+    assert rel(orc.dphi(x), xt.grad.numpy()) < 1e-15
+
+
+def pin_phi_golden(orc):
+    rows = [l.split() for l in open(os.path.join(GOLDEN, "phi_points.txt")) if l.strip() and not l.startswith("#")]
+    x = np.array([float(r[0]) for r in rows])
+    assert np.allclose(orc.phi(x), [float(r[1]) for r in rows], rtol=1e-15, atol=0)
+    assert np.allclose(orc.dphi(x), [float(r[2]) for r in rows], rtol=1e-15, atol=0)
+
+
+# ---------------------------------------------------------------- forward forms
+def pin_forms_agree(orc):
+    # Shapes of the itwiki "구현" check (B=2, T=50, d_k=16, d_v=32: T is not a multiple of C).
+    for seed, shp in ((3, dict(B=2, H=1, N=50, Dk=16, Dv=32)), (4, dict(B=1, H=3, N=37, Dk=8, Dv=5))):
+        q, k, v, _ = case(seed, **shp)
+        ref = orc.causal_direct(q, k, v)
+        assert rel(orc.causal_recurrent(q, k, v), ref) < 1e-12
+        for C in (1, 7, 16, 64):
+            assert rel(orc.causal_chunked(q, k, v, C), ref) < 1e-12
+        assert rel(orc.noncausal_assoc(q, k, v), orc.noncausal_direct(q, k, v)) < 1e-12
+
+
+def pin_single_position(orc):
+    q, k, v, _ = case(5, B=1, H=2, N=1, Dk=4, Dv=3)
+    for f in (orc.causal_direct, orc.causal_recurrent, orc.noncausal_direct, orc.noncausal_assoc):
+        assert np.array_equal(f(q, k, v), v) or rel(f(q, k, v), v) < 1e-15
+    assert rel(orc.causal_chunked(q, k, v, 4), v) < 1e-15
+
+
+def pin_constant_values(orc):
+    q, k, _, _ = case(6, B=1, H=1, N=40, Dk=6, Dv=3)
+    c = np.array([1.5, -2.0, 0.25])
+    v = np.broadcast_to(c, (1, 1, 40, 3)).copy()
+    for o in (orc.causal_direct(q, k, v), orc.causal_recurrent(q, k, v), orc.causal_chunked(q, k, v, 16),
+              orc.noncausal_direct(q, k, v), orc.noncausal_assoc(q, k, v)):
+        assert np.max(np.abs(o - c)) < 1e-13
+
+
+def pin_identical_keys(orc):
+    # k_j = k for every j: weights are equal, so causal o_i is the running mean of v.
+    q, _, v, _ = case(7, B=1, H=1, N=30, Dk=5, Dv=4)
+    k = np.broadcast_to(rnd(8, 5), (1, 1, 30, 5)).copy()
+    run_mean = np.cumsum(v, axis=2) / np.arange(1, 31)[None, None, :, None]
+    for o in (orc.causal_direct(q, k, v), orc.causal_recurrent(q, k, v), orc.causal_chunked(q, k, v, 8)):
+        assert rel(o, run_mean) < 1e-13
+    gm = v.mean(axis=2, keepdims=True)
+    for o in (orc.noncausal_direct(q, k, v), orc.noncausal_assoc(q, k, v)):
+        assert rel(o, np.broadcast_to(gm, o.shape)) < 1e-13
+
+
+def pin_dk1_ignores_q(orc):
+    q, k, v, _ = case(9, B=1, H=2, N=20, Dk=1, Dv=3)
+    q2 = rnd(10, *q.shape)
+    for f in (orc.causal_direct, orc.causal_recurrent, orc.noncausal_assoc):
+        assert rel(f(q2, k, v), f(q, k, v)) < 1e-13
+    # and the output is the phi(k)-weighted running mean of v
+    w = lib_phi(k)[..., 0]
+    ref = np.cumsum(w[..., None] * v, axis=2) / np.cumsum(w, axis=2)[..., None]
+    assert rel(orc.causal_direct(q, k, v), ref) < 1e-13
+
+
+def pin_noncausal_is_causal_last(orc):
+    q, k, v, _ = case(11, B=1, H=2, N=25, Dk=7, Dv=5)
+    oc = orc.causal_direct(q, k, v)
+    # every query sees all N keys in the non-causal form, as position N does in the causal one
+    for i in range(25):
+        qi = np.broadcast_to(q[:, :, i:i + 1, :], q.shape).copy()
+        onc = orc.noncausal_assoc(qi, k, v)
+        assert rel(onc[:, :, 0], orc.causal_direct(qi, k, v)[:, :, -1]) < 1e-13
+    onc = orc.noncausal_direct(q, k, v)
+    assert rel(onc[:, :, -1], oc[:, :, -1]) < 1e-13
+
+
+def pin_convex_hull(orc):
+    q, k, v, _ = case(12, B=1, H=1, N=60, Dk=4, Dv=6, scale=2.0)
+    o = orc.causal_direct(q, k, v)
+    lo = np.minimum.accumulate(v, axis=2)
+    hi = np.maximum.accumulate(v, axis=2)
+    assert np.all(o >= lo - 1e-12) and np.all(o <= hi + 1e-12)
+    o = orc.noncausal_assoc(q, k, v)
+    assert np.all(o >= v.min(axis=2, keepdims=True) - 1e-12) and np.all(o <= v.max(axis=2, keepdims=True) + 1e-12)
+
+
+def pin_affine_covariance(orc):
+    q, k, v, _ = case(13, B=1, H=1, N=33, Dk=5, Dv=7)
+    b = rnd(14, 7)
+    for f in (orc.causal_direct, orc.causal_recurrent, orc.noncausal_assoc):
+        assert rel(f(q, k, -2.5 * v + b), -2.5 * f(q, k, v) + b) < 1e-12
+
+
+def pin_noncausal_permutation(orc):
+    q, k, v, _ = case(15, B=1, H=1, N=21, Dk=6, Dv=4)
+    p = np.random.default_rng(16).permutation(21)
+    o = orc.noncausal_assoc(q, k, v)
+    assert rel(orc.noncausal_assoc(q, k[:, :, p], v[:, :, p]), o) < 1e-13
+    assert rel(orc.noncausal_direct(q[:, :, p], k, v), o[:, :, p]) < 1e-13
+
+
+def _golden_two_token():
+    rows = {}
+    for l in open(os.path.join(GOLDEN, "two_token_case.txt")):
+        if l.strip() and not l.startswith("#"):
+            key, *vals = l.split()
+            rows[key] = np.array([float(x) for x in vals])
+    sh_k, sh_v = (1, 1, 2, 1), (1, 1, 2, 2)
+    return {n: rows[n].reshape(sh_k if n in ("q", "k", "dq", "dk") else sh_v) for n in rows}
+
+
+def pin_two_token_golden(orc):
+    g = _golden_two_token()
+    for f in (orc.causal_direct, orc.causal_recurrent):
+        assert np.allclose(f(g["q"], g["k"], g["v"]), g["o"], rtol=0, atol=1e-15)
+    for f in (orc.causal_bwd_direct, orc.causal_bwd_recurrent):
+        dq, dk, dv = f(g["q"], g["k"], g["v"], g["dO"])
+        assert np.allclose(dq, g["dq"], atol=1e-15)
+        assert np.allclose(dk, g["dk"], atol=1e-15)
+        assert np.allclose(dv, g["dv"], atol=1e-15)
+
+
+# ---------------------------------------------------------------- decode
+def pin_decode_reproduces_causal(orc):
+    q, k, v, _ = case(17, B=2, H=3, N=12, Dk=4, Dv=5)
+    S = np.zeros((2, 3, 4, 5))
+    z = np.zeros((2, 3, 4))
+    outs = []
+    for t in range(12):
+        o, S, z = orc.recurrent_step(q[:, :, t], k[:, :, t], v[:, :, t], S, z)
+        outs.append(o)
+    assert rel(np.stack(outs, axis=2), orc.causal_direct(q, k, v)) < 1e-12
+    kt = lib_phi(k)
+    assert rel(S, np.einsum("bhnd,bhnm->bhdm", kt, v)) < 1e-12   # S_N = phi(K)^T V
+    assert rel(z, kt.sum(axis=2)) < 1e-12                       # z_N = phi(K)^T 1
+
+
+def pin_decode_resume(orc):
+    q, k, v, _ = case(18, B=1, H=2, N=10, Dk=3, Dv=4)
+    S, z = np.zeros((1, 2, 3, 4)), np.zeros((1, 2, 3))
+    full = []
+    for t in range(10):
+        o, S, z = orc.recurrent_step(q[:, :, t], k[:, :, t], v[:, :, t], S, z)
+        full.append(o)
+    S2, z2 = np.zeros((1, 2, 3, 4)), np.zeros((1, 2, 3))
+    for t in range(6):
+        _, S2, z2 = orc.recurrent_step(q[:, :, t], k[:, :, t], v[:, :, t], S2, z2)
+    saved = (S2.copy(), z2.copy())
+    for t in range(6, 10):
+        o, S2, z2 = orc.recurrent_step(q[:, :, t], k[:, :, t], v[:, :, t], *saved)
+        saved = (S2, z2)
+        assert np.array_equal(o, full[t])
+
+
+# ---------------------------------------------------------------- backward
+def _fd_grads(f, q, k, v, dO, h=1e-6):
+    """Central finite differences of L = sum(dO * f(q, k, v)) for every input element."""
+    grads = []
+    for which in range(3):
+        args = [q.copy(), k.copy(), v.copy()]
+        g = np.zeros_like(args[which])
+        flat = args[which].reshape(-1)
+        for t in range(flat.size):
+            x0 = flat[t]
+            flat[t] = x0 + h
+            lp = np.sum(dO * f(*args))
+            flat[t] = x0 - h
+            lm = np.sum(dO * f(*args))
+            flat[t] = x0
+            g.reshape(-1)[t] = (lp - lm) / (2 * h)
+        grads.append(g)
+    return grads
+
+
+def pin_bwd_finite_differences(orc):
+    for seed, (N, Dk, Dv) in ((19, (6, 3, 4)), (20, (8, 4, 2)), (21, (1, 2, 3))):
+        q, k, v, dO = case(seed, B=1, H=1, N=N, Dk=Dk, Dv=Dv)
+        fd = _fd_grads(orc.causal_direct, q, k, v, dO)
+        for bwd in (orc.causal_bwd_direct, orc.causal_bwd_recurrent):
+            for a, b in zip(bwd(q, k, v, dO), fd):
+                assert np.max(np.abs(a - b)) <= 1e-6 * max(1.0, np.max(np.abs(b)))
+        fdn = _fd_grads(orc.noncausal_direct, q, k, v, dO)
+        for a, b in zip(orc.noncausal_bwd_direct(q, k, v, dO), fdn):
+            assert np.max(np.abs(a - b)) <= 1e-6 * max(1.0, np.max(np.abs(b)))
+
+
+def pin_bwd_forms_agree(orc):
+    q, k, v, dO = case(22, B=2, H=1, N=50, Dk=16, Dv=32)
+    for a, b in zip(orc.causal_bwd_recurrent(q, k, v, dO), orc.causal_bwd_direct(q, k, v, dO)):
+        assert rel(a, b) < 1e-11
+
+
+def pin_bwd_invariants(orc):
+    q, k, v, dO = case(23, B=1, H=2, N=24, Dk=5, Dv=3)
+    for bwd in (orc.causal_bwd_direct, orc.causal_bwd_recurrent, orc.noncausal_bwd_direct):
+        # sum_j dv_j = sum_i dO_i (the weights of each output sum to one)
+        _, _, dv = bwd(q, k, v, dO)
+        assert rel(dv.sum(axis=2), dO.sum(axis=2)) < 1e-12
+        # constant V: the output does not depend on q or k
+        vc = np.broadcast_to(rnd(24, 3), v.shape).copy()
+        dq, dk, _ = bwd(q, k, vc, dO)
+        assert np.max(np.abs(dq)) < 1e-12 and np.max(np.abs(dk)) < 1e-12
+    # identical keys: causal o_i is the running mean, so dq = 0 and dv_j = sum_{i>=j} dO_i / i
+    kc = np.broadcast_to(rnd(25, 5), k.shape).copy()
+    ref_dv = np.flip(np.cumsum(np.flip(dO / np.arange(1, 25)[None, None, :, None], axis=2), axis=2), axis=2)
+    for bwd in (orc.causal_bwd_direct, orc.causal_bwd_recurrent):
+        dq, _, dv = bwd(q, kc, v, dO)
+        assert np.max(np.abs(dq)) < 1e-12
+        assert rel(dv, ref_dv) < 1e-12
+
+
+ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
