@@ -1,0 +1,228 @@
+"""Causal linear attention with phi(x) = elu(x) + 1 on GB300 (sm_103a).
+
+A thin ctypes binding over the C ABI of ``libla.so`` (declared in
+``include/la.h``).  It only marshals arguments: every step of the computation
+runs in the library's CUDA kernels.  PyTorch supplies device memory (outputs
+and the workspace come from its caching allocator) and the current stream.
+There is no CPU fallback: if the library is not built, importing works but
+every call raises ``RuntimeError``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+__all__ = [
+    "LaError", "noncausal_fwd", "causal_fwd", "causal_bwd", "recurrent_step", "workspace_bytes",
+    "last_error", "clear_error", "timing_enable", "timing_reset", "timing_read", "library", "version",
+    "OP_NONCAUSAL_FWD", "OP_CAUSAL_FWD", "OP_CAUSAL_BWD", "OP_NONCAUSAL_BWD",
+]
+
+OP_NONCAUSAL_FWD, OP_CAUSAL_FWD, OP_CAUSAL_BWD, OP_NONCAUSAL_BWD = 0, 1, 2, 3
+LA_F32, LA_BF16 = 0, 1
+_STATUS = {0: "LA_OK", 1: "LA_ERR_INVALID_ARG", 2: "LA_ERR_UNSUPPORTED", 3: "LA_ERR_WORKSPACE",
+           4: "LA_ERR_CUDA", 5: "LA_ERR_TIMEOUT"}
+
+
+class LaError(RuntimeError):
+    def __init__(self, status: int, where: str, detail: str = ""):
+        self.status = status
+        super().__init__("%s failed: %s%s" % (where, _STATUS.get(status, str(status)),
+                                               (" (%s)" % detail) if detail else ""))
+
+
+class Shape(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("H", ctypes.c_int), ("N", ctypes.c_int), ("Dk", ctypes.c_int),
+                ("Dv", ctypes.c_int), ("dtype", ctypes.c_int)]
+
+
+class KernelTime(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char_p), ("launches", ctypes.c_int), ("total_ms", ctypes.c_double)]
+
+
+_lib = None
+_lock = threading.Lock()
+_vp = ctypes.c_void_p
+
+
+def _declare(lib):
+    lib.la_workspace_bytes.argtypes = [ctypes.c_int, Shape]
+    lib.la_workspace_bytes.restype = ctypes.c_size_t
+    lib.la_noncausal_fwd.argtypes = [_vp, _vp, _vp, _vp, Shape, _vp, ctypes.c_size_t, _vp]
+    lib.la_causal_fwd.argtypes = [_vp, _vp, _vp, _vp, Shape, _vp, ctypes.c_size_t, _vp]
+    lib.la_causal_bwd.argtypes = [_vp] * 7 + [Shape, _vp, ctypes.c_size_t, _vp]
+    lib.la_recurrent_step.argtypes = [_vp] * 6 + [Shape, _vp]
+    for f in ("la_noncausal_fwd", "la_causal_fwd", "la_causal_bwd", "la_recurrent_step", "la_last_error",
+              "la_clear_error", "la_timing_enable", "la_timing_reset"):
+        getattr(lib, f).restype = ctypes.c_int
+    lib.la_last_error.argtypes = []
+    lib.la_clear_error.argtypes = []
+    lib.la_status_string.argtypes = [ctypes.c_int]
+    lib.la_status_string.restype = ctypes.c_char_p
+    lib.la_error_detail.argtypes = []
+    lib.la_error_detail.restype = ctypes.c_char_p
+    lib.la_version.argtypes = []
+    lib.la_version.restype = ctypes.c_char_p
+    lib.la_timing_enable.argtypes = [ctypes.c_int]
+    lib.la_timing_reset.argtypes = []
+    lib.la_timing_read.argtypes = [ctypes.POINTER(KernelTime), ctypes.c_int]
+    lib.la_timing_read.restype = ctypes.c_int
+    return lib
+
+
+def library(path: str | None = None):
+    """The loaded libla (ctypes.CDLL).  Raises RuntimeError if it is not built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            p = path or _build.LIB_PATH
+            if not os.path.exists(p):
+                raise RuntimeError("libla.so is not built (%s); run causal_linear_attention_phi_gb300.build."
+                                   "build_library() or __graft_entry__.build()" % p)
+            _lib = _declare(ctypes.CDLL(p))
+    return _lib
+
+
+def version() -> str:
+    return library().la_version().decode()
+
+
+def _check(st: int, where: str):
+    if st != 0:
+        raise LaError(st, where, library().la_error_detail().decode(errors="replace"))
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return LA_F32
+    if t.dtype == torch.bfloat16:
+        return LA_BF16
+    raise TypeError("unsupported dtype %s (float32 or bfloat16)" % t.dtype)
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise TypeError("expected CUDA tensors")
+        if not t.is_contiguous():
+            raise ValueError("expected contiguous tensors")
+
+
+def _stream_ptr(stream=None) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None and t.numel() > 0 else ctypes.c_void_p(0)
+
+
+def _shape4(q, k, v):
+    if q.dim() != 4 or k.shape != q.shape or v.dim() != 4 or v.shape[:3] != q.shape[:3]:
+        raise ValueError("expected q, k [B,H,N,Dk] and v [B,H,N,Dv]; got %s %s %s" %
+                         (tuple(q.shape), tuple(k.shape), tuple(v.shape)))
+    if not (q.dtype == k.dtype == v.dtype):
+        raise TypeError("q, k, v must share a dtype")
+    B, H, N, Dk = q.shape
+    return Shape(B, H, N, Dk, v.shape[3], _dtype_code(q))
+
+
+def workspace_bytes(op: int, B: int, H: int, N: int, Dk: int, Dv: int, dtype: torch.dtype) -> int:
+    code = LA_BF16 if dtype == torch.bfloat16 else LA_F32
+    return int(library().la_workspace_bytes(op, Shape(B, H, N, Dk, Dv, code)))
+
+
+def _workspace(op, s: Shape, device, workspace):
+    need = int(library().la_workspace_bytes(op, s))
+    if workspace is not None:
+        return workspace, max(need, workspace.numel())
+    if need == 0:
+        return None, 0
+    return torch.empty(need, dtype=torch.uint8, device=device), need
+
+
+def noncausal_fwd(q, k, v, out=None, workspace=None, stream=None):
+    """o_i = phi(q_i)^T S / phi(q_i)^T z with S = phi(K)^T V, z = phi(K)^T 1 over all positions."""
+    _need_cuda(q, k, v)
+    s = _shape4(q, k, v)
+    if out is None:
+        out = torch.empty_like(v)
+    ws, nb = _workspace(OP_NONCAUSAL_FWD, s, q.device, workspace)
+    _check(library().la_noncausal_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), s, _ptr(ws), nb, _stream_ptr(stream)),
+           "la_noncausal_fwd")
+    return out
+
+
+def causal_fwd(q, k, v, out=None, workspace=None, stream=None):
+    """Causal linear attention (j <= i) in the chunked form; returns o [B,H,N,Dv]."""
+    _need_cuda(q, k, v)
+    s = _shape4(q, k, v)
+    if out is None:
+        out = torch.empty_like(v)
+    ws, nb = _workspace(OP_CAUSAL_FWD, s, q.device, workspace)
+    _check(library().la_causal_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), s, _ptr(ws), nb, _stream_ptr(stream)),
+           "la_causal_fwd")
+    return out
+
+
+def causal_bwd(q, k, v, dout, dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """Gradients (dq, dk, dv) of the causal form for upstream gradient dout; states are recomputed."""
+    _need_cuda(q, k, v, dout)
+    s = _shape4(q, k, v)
+    if dout.shape != v.shape or dout.dtype != v.dtype:
+        raise ValueError("dout must match v in shape and dtype")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    ws, nb = _workspace(OP_CAUSAL_BWD, s, q.device, workspace)
+    _check(library().la_causal_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), s, _ptr(ws),
+                                   nb, _stream_ptr(stream)), "la_causal_bwd")
+    return dq, dk, dv
+
+
+def recurrent_step(q, k, v, S, z, out=None, stream=None):
+    """One decode step: S += phi(k) v^T, z += phi(k) (in place), out = phi(q)^T S / phi(q)^T z."""
+    _need_cuda(q, k, v, S, z)
+    if q.dim() != 3 or k.shape != q.shape or v.shape[:2] != q.shape[:2]:
+        raise ValueError("expected q, k [B,H,Dk] and v [B,H,Dv]")
+    B, H, Dk = q.shape
+    Dv = v.shape[2]
+    if S.dtype != torch.float32 or z.dtype != torch.float32 or S.shape != (B, H, Dk, Dv) or z.shape != (B, H, Dk):
+        raise ValueError("S must be fp32 [B,H,Dk,Dv] and z fp32 [B,H,Dk]")
+    if out is None:
+        out = torch.empty_like(v)
+    s = Shape(B, H, 1, Dk, Dv, _dtype_code(q))
+    _check(library().la_recurrent_step(_ptr(q), _ptr(k), _ptr(v), _ptr(S), _ptr(z), _ptr(out), s, _stream_ptr(stream)),
+           "la_recurrent_step")
+    return out
+
+
+def last_error() -> int:
+    """Sticky device-side status (0 = LA_OK); synchronises the device."""
+    return int(library().la_last_error())
+
+
+def clear_error():
+    _check(library().la_clear_error(), "la_clear_error")
+
+
+def timing_enable(on: bool = True):
+    _check(library().la_timing_enable(1 if on else 0), "la_timing_enable")
+
+
+def timing_reset():
+    _check(library().la_timing_reset(), "la_timing_reset")
+
+
+def timing_read() -> dict:
+    """{kernel name: (launches, total_ms)} since the last reset."""
+    lib = library()
+    n = lib.la_timing_read(None, 0)
+    buf = (KernelTime * max(n, 1))()
+    n = lib.la_timing_read(buf, n)
+    return {buf[i].name.decode(): (buf[i].launches, buf[i].total_ms) for i in range(n)}

@@ -1,0 +1,410 @@
+// api.cu -- the extern "C" entry points of libla: argument checks, work
+// planning, workspace carving and kernel dispatch, plus the sticky device
+// error word and the optional per-kernel timing.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "la_internal.cuh"
+
+namespace la {
+
+// ------------------------------------------------------------------ sticky error word
+__device__ int g_error_word = 0;
+
+namespace {
+thread_local std::string t_detail;
+
+la_status fail(la_status st, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    t_detail = buf;
+    return st;
+}
+
+constexpr int kMaxDevices = 64;
+int* g_err_ptr[kMaxDevices] = {};
+int g_cc_ok[kMaxDevices] = {};  // 0 unknown, 1 sm_103, -1 other
+std::mutex g_dev_mu;
+
+int current_device() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    return dev;
+}
+}  // namespace
+
+int* device_error_word() {
+    int dev = current_device();
+    if (dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> g(g_dev_mu);
+    if (!g_err_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return nullptr;
+        g_err_ptr[dev] = static_cast<int*>(p);
+    }
+    return g_err_ptr[dev];
+}
+
+// ------------------------------------------------------------------ timing
+namespace {
+struct Pending {
+    const char* name;
+    cudaEvent_t a, b;
+};
+struct Total {
+    const char* name;
+    int launches;
+    double ms;
+};
+std::mutex g_t_mu;
+bool g_timing = false;
+std::vector<Pending> g_pending;
+std::vector<Total> g_totals;
+std::vector<cudaEvent_t> g_event_pool;
+thread_local cudaEvent_t t_open = nullptr;
+
+cudaEvent_t take_event() {
+    if (!g_event_pool.empty()) {
+        cudaEvent_t e = g_event_pool.back();
+        g_event_pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    cudaEventCreate(&e);
+    return e;
+}
+
+void drain_locked() {
+    for (auto& p : g_pending) {
+        float ms = 0.f;
+        cudaEventSynchronize(p.b);
+        cudaEventElapsedTime(&ms, p.a, p.b);
+        Total* t = nullptr;
+        for (auto& x : g_totals)
+            if (strcmp(x.name, p.name) == 0) t = &x;
+        if (!t) {
+            g_totals.push_back({p.name, 0, 0.0});
+            t = &g_totals.back();
+        }
+        t->launches += 1;
+        t->ms += ms;
+        g_event_pool.push_back(p.a);
+        g_event_pool.push_back(p.b);
+    }
+    g_pending.clear();
+}
+}  // namespace
+
+void launch_begin(const char* /*name*/, cudaStream_t st) {
+    if (!g_timing) return;
+    std::lock_guard<std::mutex> g(g_t_mu);
+    t_open = take_event();
+    cudaEventRecord(t_open, st);
+}
+
+cudaError_t launch_end(const char* name, cudaStream_t st) {
+    cudaError_t err = cudaGetLastError();
+    if (g_timing && t_open) {
+        std::lock_guard<std::mutex> g(g_t_mu);
+        cudaEvent_t b = take_event();
+        cudaEventRecord(b, st);
+        g_pending.push_back({name, t_open, b});
+        t_open = nullptr;
+        if (g_pending.size() > 4096) drain_locked();
+    }
+    return err;
+}
+
+// ------------------------------------------------------------------ planning
+// CUDA-core kernels: one CTA per SM (about 215 KB of shared memory at D = 128),
+// so aim for a few hundred CTAs; the count is a fixed function of the shape so
+// la_workspace_bytes stays device independent.
+static constexpr int kSimtChunk = 64;
+static constexpr int kTargetCtas = 304;
+
+Plan make_plan(const la_shape& s, int /*op*/) {
+    Plan p{};
+    p.tc = false;
+    p.C = kSimtChunk;
+    p.nchunks = (s.N + p.C - 1) / p.C;
+    const int BH = s.B * s.H;
+    int P = (kTargetCtas + BH - 1) / BH;
+    if (P < 1) P = 1;
+    if (P > p.nchunks) P = p.nchunks;
+    if (P < 1) P = 1;
+    p.cps = (p.nchunks + P - 1) / P;
+    p.P = (p.nchunks + p.cps - 1) / p.cps;
+    if (p.P < 1) p.P = 1;
+    return p;
+}
+
+static size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+WsLayout make_ws_layout(const la_shape& s, int op, const Plan& p) {
+    WsLayout w{};
+    const size_t BH = (size_t)s.B * s.H;
+    const size_t E = state_elems(s.Dk, s.Dv);
+    const size_t seg = align256(BH * p.P * E * sizeof(float));
+    size_t off = 0;
+    w.seg_states = off;
+    off += seg;
+    if (op == LA_OP_CAUSAL_BWD || op == LA_OP_NONCAUSAL_BWD) {
+        w.seg_states2 = off;
+        off += seg;
+        w.den_g = off;
+        off += align256(BH * (size_t)s.N * 2 * sizeof(float));
+    }
+    if (op == LA_OP_NONCAUSAL_FWD || op == LA_OP_NONCAUSAL_BWD) {
+        w.totals = off;
+        off += align256(BH * E * sizeof(float));
+    }
+    w.bytes = off;
+    return w;
+}
+
+// ------------------------------------------------------------------ argument checks
+namespace {
+
+bool pow2_head(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
+
+la_status check_shape(const la_shape& s) {
+    if (s.B < 0 || s.H < 0 || s.N < 0) return fail(LA_ERR_INVALID_ARG, "negative size B=%d H=%d N=%d", s.B, s.H, s.N);
+    if (s.dtype != LA_F32 && s.dtype != LA_BF16) return fail(LA_ERR_INVALID_ARG, "bad dtype %d", s.dtype);
+    if (s.Dk <= 0 || s.Dv <= 0) return fail(LA_ERR_INVALID_ARG, "bad head size Dk=%d Dv=%d", s.Dk, s.Dv);
+    if (!pow2_head(s.Dk) || !pow2_head(s.Dv))
+        return fail(LA_ERR_UNSUPPORTED, "head sizes must be 16, 32, 64 or 128 (Dk=%d Dv=%d)", s.Dk, s.Dv);
+    if ((long long)s.B * s.H > 65535) return fail(LA_ERR_UNSUPPORTED, "B*H=%lld exceeds 65535", (long long)s.B * s.H);
+    const double elems = (double)s.B * s.H * (double)s.N * (s.Dk > s.Dv ? s.Dk : s.Dv);
+    if (elems >= 1099511627776.0) return fail(LA_ERR_INVALID_ARG, "problem too large");
+    return LA_OK;
+}
+
+bool empty(const la_shape& s) { return s.B == 0 || s.H == 0 || s.N == 0; }
+
+la_status check_device() {
+    const int dev = current_device();
+    if (dev < 0 || dev >= kMaxDevices) return fail(LA_ERR_CUDA, "no current CUDA device");
+    int ok = g_cc_ok[dev];
+    if (ok == 0) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+            return fail(LA_ERR_CUDA, "cannot query device %d", dev);
+        ok = (major == 10 && minor == 3) ? 1 : -1;
+        g_cc_ok[dev] = ok;
+        if (ok < 0) return fail(LA_ERR_UNSUPPORTED, "device %d is sm_%d%d; this build targets sm_103a", dev, major, minor);
+    }
+    return ok > 0 ? LA_OK : fail(LA_ERR_UNSUPPORTED, "device is not sm_103");
+}
+
+// A tensor argument must be a 16-byte aligned pointer to device (or managed)
+// memory of the current device.  Host pointers are refused here, before any
+// kernel could dereference them.
+la_status check_ptr(const void* p, const char* what) {
+    if (!p) return fail(LA_ERR_INVALID_ARG, "%s is NULL", what);
+    if (reinterpret_cast<uintptr_t>(p) & 15) return fail(LA_ERR_INVALID_ARG, "%s is not 16-byte aligned", what);
+    cudaPointerAttributes attr;
+    cudaError_t e = cudaPointerGetAttributes(&attr, p);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(LA_ERR_INVALID_ARG, "%s: not a CUDA pointer", what);
+    }
+    if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged)
+        return fail(LA_ERR_INVALID_ARG, "%s is not device memory", what);
+    if (attr.type == cudaMemoryTypeDevice && attr.device != current_device())
+        return fail(LA_ERR_INVALID_ARG, "%s lives on device %d, not the current device", what, attr.device);
+    return LA_OK;
+}
+
+la_status check_ws(void* ws, size_t ws_bytes, size_t need) {
+    if (need == 0) return LA_OK;
+    if (!ws) return fail(LA_ERR_WORKSPACE, "workspace is NULL (%zu bytes needed)", need);
+    if (ws_bytes < need) return fail(LA_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", ws_bytes, need);
+    return check_ptr(ws, "workspace") == LA_OK ? LA_OK : LA_ERR_INVALID_ARG;
+}
+
+la_status cuda_status(cudaError_t e, const char* where) {
+    if (e == cudaSuccess) return LA_OK;
+    return fail(LA_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+#define LA_TRY(expr)                        \
+    do {                                    \
+        la_status _st = (expr);             \
+        if (_st != LA_OK) return _st;       \
+    } while (0)
+
+}  // namespace
+}  // namespace la
+
+using namespace la;
+
+extern "C" {
+
+size_t la_workspace_bytes(int op, la_shape s) {
+    if (op < LA_OP_NONCAUSAL_FWD || op > LA_OP_NONCAUSAL_BWD) return 0;
+    if (check_shape(s) != LA_OK || empty(s)) return 0;
+    const Plan p = make_plan(s, op);
+    return make_ws_layout(s, op, p).bytes;
+}
+
+la_status la_noncausal_fwd(const void* q, const void* k, const void* v, void* o, la_shape s, void* ws,
+                           size_t ws_bytes, la_stream_t stream) {
+    t_detail.clear();
+    LA_TRY(check_shape(s));
+    if (empty(s)) return LA_OK;
+    LA_TRY(check_device());
+    LA_TRY(check_ptr(q, "q"));
+    LA_TRY(check_ptr(k, "k"));
+    LA_TRY(check_ptr(v, "v"));
+    LA_TRY(check_ptr(o, "o"));
+    const Plan p = make_plan(s, LA_OP_NONCAUSAL_FWD);
+    const WsLayout w = make_ws_layout(s, LA_OP_NONCAUSAL_FWD, p);
+    LA_TRY(check_ws(ws, ws_bytes, w.bytes));
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    float* seg = reinterpret_cast<float*>(static_cast<char*>(ws) + w.seg_states);
+    float* tot = reinterpret_cast<float*>(static_cast<char*>(ws) + w.totals);
+    LA_TRY(cuda_status(simt_segment_sums(k, v, seg, s, p, st), "noncausal segment sums"));
+    LA_TRY(cuda_status(scan_segments(seg, tot, s, p, SCAN_TOTAL, st), "noncausal totals"));
+    LA_TRY(cuda_status(simt_noncausal_apply(q, o, tot, s, st), "noncausal apply"));
+    return LA_OK;
+}
+
+la_status la_causal_fwd(const void* q, const void* k, const void* v, void* o, la_shape s, void* ws, size_t ws_bytes,
+                        la_stream_t stream) {
+    t_detail.clear();
+    LA_TRY(check_shape(s));
+    if (empty(s)) return LA_OK;
+    LA_TRY(check_device());
+    LA_TRY(check_ptr(q, "q"));
+    LA_TRY(check_ptr(k, "k"));
+    LA_TRY(check_ptr(v, "v"));
+    LA_TRY(check_ptr(o, "o"));
+    const Plan p = make_plan(s, LA_OP_CAUSAL_FWD);
+    const WsLayout w = make_ws_layout(s, LA_OP_CAUSAL_FWD, p);
+    LA_TRY(check_ws(ws, ws_bytes, w.bytes));
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    float* seg = reinterpret_cast<float*>(static_cast<char*>(ws) + w.seg_states);
+    if (p.P > 1) {
+        LA_TRY(cuda_status(simt_segment_sums(k, v, seg, s, p, st), "segment sums"));
+        LA_TRY(cuda_status(scan_segments(seg, nullptr, s, p, SCAN_EXCLUSIVE_PREFIX, st), "segment scan"));
+    } else {
+        LA_TRY(cuda_status(cudaMemsetAsync(seg, 0, (size_t)s.B * s.H * state_elems(s.Dk, s.Dv) * sizeof(float), st),
+                           "state clear"));
+    }
+    LA_TRY(cuda_status(simt_causal_fwd_out(q, k, v, o, seg, s, p, st), "causal forward"));
+    return LA_OK;
+}
+
+la_status la_causal_bwd(const void* q, const void* k, const void* v, const void* dout, void* dq, void* dk, void* dv,
+                        la_shape s, void* ws, size_t ws_bytes, la_stream_t stream) {
+    t_detail.clear();
+    LA_TRY(check_shape(s));
+    if (empty(s)) return LA_OK;
+    LA_TRY(check_device());
+    LA_TRY(check_ptr(q, "q"));
+    LA_TRY(check_ptr(k, "k"));
+    LA_TRY(check_ptr(v, "v"));
+    LA_TRY(check_ptr(dout, "dout"));
+    LA_TRY(check_ptr(dq, "dq"));
+    LA_TRY(check_ptr(dk, "dk"));
+    LA_TRY(check_ptr(dv, "dv"));
+    const Plan p = make_plan(s, LA_OP_CAUSAL_BWD);
+    const WsLayout w = make_ws_layout(s, LA_OP_CAUSAL_BWD, p);
+    LA_TRY(check_ws(ws, ws_bytes, w.bytes));
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    char* base = static_cast<char*>(ws);
+    float* segS = reinterpret_cast<float*>(base + w.seg_states);
+    float* segR = reinterpret_cast<float*>(base + w.seg_states2);
+    float* den_g = reinterpret_cast<float*>(base + w.den_g);
+    if (p.P > 1) {
+        LA_TRY(cuda_status(simt_segment_sums(k, v, segS, s, p, st), "segment sums"));
+        LA_TRY(cuda_status(scan_segments(segS, nullptr, s, p, SCAN_EXCLUSIVE_PREFIX, st), "segment scan"));
+    } else {
+        LA_TRY(cuda_status(cudaMemsetAsync(segS, 0, (size_t)s.B * s.H * state_elems(s.Dk, s.Dv) * sizeof(float), st),
+                           "state clear"));
+    }
+    LA_TRY(cuda_status(simt_bwd_forward_sweep(q, k, v, dout, dq, segS, segR, den_g, s, p, st), "backward forward sweep"));
+    LA_TRY(cuda_status(scan_segments(segR, nullptr, s, p, SCAN_EXCLUSIVE_SUFFIX, st), "reverse scan"));
+    LA_TRY(cuda_status(simt_bwd_reverse_sweep(q, k, v, dout, dk, dv, segR, den_g, s, p, st), "backward reverse sweep"));
+    return LA_OK;
+}
+
+la_status la_recurrent_step(const void* q, const void* k, const void* v, float* S, float* z, void* out, la_shape s,
+                            la_stream_t stream) {
+    t_detail.clear();
+    la_shape s1 = s;
+    s1.N = 1;  // N is ignored by the step
+    LA_TRY(check_shape(s1));
+    if (empty(s1)) return LA_OK;
+    LA_TRY(check_device());
+    LA_TRY(check_ptr(q, "q"));
+    LA_TRY(check_ptr(k, "k"));
+    LA_TRY(check_ptr(v, "v"));
+    LA_TRY(check_ptr(S, "S"));
+    LA_TRY(check_ptr(z, "z"));
+    LA_TRY(check_ptr(out, "out"));
+    LA_TRY(cuda_status(la::recurrent_step(q, k, v, S, z, out, s1, reinterpret_cast<cudaStream_t>(stream)),
+                       "recurrent step"));
+    return LA_OK;
+}
+
+la_status la_last_error(void) {
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_error_word, sizeof(int)) != cudaSuccess)
+        return fail(LA_ERR_CUDA, "cannot read the device error word");
+    return static_cast<la_status>(v);
+}
+
+la_status la_clear_error(void) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_error_word, &zero, sizeof(int)) != cudaSuccess)
+        return fail(LA_ERR_CUDA, "cannot clear the device error word");
+    return LA_OK;
+}
+
+const char* la_status_string(la_status st) {
+    switch (st) {
+        case LA_OK: return "LA_OK";
+        case LA_ERR_INVALID_ARG: return "LA_ERR_INVALID_ARG: invalid argument";
+        case LA_ERR_UNSUPPORTED: return "LA_ERR_UNSUPPORTED: unsupported size or device";
+        case LA_ERR_WORKSPACE: return "LA_ERR_WORKSPACE: workspace missing or too small";
+        case LA_ERR_CUDA: return "LA_ERR_CUDA: CUDA runtime or launch failure";
+        case LA_ERR_TIMEOUT: return "LA_ERR_TIMEOUT: a bounded device wait ran out";
+    }
+    return "unknown la_status";
+}
+
+const char* la_error_detail(void) { return t_detail.c_str(); }
+
+const char* la_version(void) { return "0.1.0"; }
+
+la_status la_timing_enable(int on) {
+    std::lock_guard<std::mutex> g(g_t_mu);
+    g_timing = on != 0;
+    return LA_OK;
+}
+
+la_status la_timing_reset(void) {
+    std::lock_guard<std::mutex> g(g_t_mu);
+    drain_locked();
+    g_totals.clear();
+    return LA_OK;
+}
+
+int la_timing_read(la_kernel_time* out, int max) {
+    std::lock_guard<std::mutex> g(g_t_mu);
+    drain_locked();
+    const int n = (int)g_totals.size();
+    for (int i = 0; i < n && i < max && out; ++i) out[i] = {g_totals[i].name, g_totals[i].launches, g_totals[i].ms};
+    return n;
+}
+
+}  // extern "C"

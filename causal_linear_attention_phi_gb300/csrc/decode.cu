@@ -1,0 +1,131 @@
+// decode.cu -- one recurrent step for every head:
+//   S <- S + phi(k) v^T,  z <- z + phi(k),  out = phi(q)^T S / phi(q)^T z
+// (state updated first, then read: the diagonal term j = i is included).
+// "Transformers은 RNN이다" digest, 핵심 구성요소 4 (RNN view); velog review 3.6;
+// itwiki 인과 마스킹과 순환형.
+//
+// The step is bound by memory traffic: S (fp32, Dk x Dv per head) is read and
+// written once, everything else is O(Dk + Dv) per head.  One warp owns one head.
+// S rows are moved as float4: a row of Dv floats is Dv/4 vectors, so a warp
+// instruction covers (32 / (Dv/4)) consecutive rows when Dv < 128, i.e. one
+// contiguous, fully coalesced span of S per instruction.  Each lane keeps its
+// four v values and four partial numerators in registers; the partial
+// numerators of lanes that share a column group are combined with shuffles.
+#include "la_internal.cuh"
+
+namespace la {
+namespace {
+
+constexpr int kWarpsPerBlock = 2;
+
+template <typename T>
+__device__ __forceinline__ float4 load4(const T* p);
+template <>
+__device__ __forceinline__ float4 load4<float>(const float* p) {
+    return *reinterpret_cast<const float4*>(p);
+}
+template <>
+__device__ __forceinline__ float4 load4<__nv_bfloat16>(const __nv_bfloat16* p) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(p);
+    float2 a = __bfloat1622float2(h[0]), b = __bfloat1622float2(h[1]);
+    return make_float4(a.x, a.y, b.x, b.y);
+}
+
+template <typename T>
+__device__ __forceinline__ void store4(T* p, float4 x);
+template <>
+__device__ __forceinline__ void store4<float>(float* p, float4 x) {
+    *reinterpret_cast<float4*>(p) = x;
+}
+template <>
+__device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* p, float4 x) {
+    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(p);
+    h[0] = __floats2bfloat162_rn(x.x, x.y);
+    h[1] = __floats2bfloat162_rn(x.z, x.w);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(32 * kWarpsPerBlock)
+recurrent_step_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
+                      float* __restrict__ S, float* __restrict__ z, T* __restrict__ out, int BH, int Dk, int Dv) {
+    __shared__ float qk_s[kWarpsPerBlock][2][128];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int h = blockIdx.x * kWarpsPerBlock + warp;
+    if (h >= BH) return;  // whole warp leaves together
+
+    const T* qh = q + (size_t)h * Dk;
+    const T* kh = k + (size_t)h * Dk;
+    float* zh = z + (size_t)h * Dk;
+    // phi(q), phi(k) into shared memory; z update and phi(q).z on the way
+    float den = 0.f;
+    for (int d = lane; d < Dk; d += 32) {
+        const float qt = phi_f(to_f32(qh[d]));
+        const float kt = phi_f(to_f32(kh[d]));
+        qk_s[warp][0][d] = qt;
+        qk_s[warp][1][d] = kt;
+        const float zn = zh[d] + kt;
+        zh[d] = zn;
+        den = fmaf(qt, zn, den);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+    __syncwarp();
+
+    const int ncol4 = Dv >> 2;                    // float4 columns per row (4..32)
+    const int cols = ncol4 < 32 ? ncol4 : 32;     // lanes across a row
+    const int rows_per_iter = 32 / cols;          // rows covered by one warp instruction
+    const int c4 = lane % cols, rsub = lane / cols;
+    const int npass = ncol4 / cols;               // column passes (1 unless Dv > 128)
+    float* Sh = S + (size_t)h * Dk * Dv;
+
+    for (int pass = 0; pass < npass; ++pass) {
+        const int col = (pass * cols + c4) * 4;
+        const float4 vv = load4<T>(v + (size_t)h * Dv + col);
+        float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+        for (int d = rsub; d < Dk; d += rows_per_iter) {
+            float4* sp = reinterpret_cast<float4*>(Sh + (size_t)d * Dv + col);
+            float4 s = *sp;
+            const float kt = qk_s[warp][1][d], qt = qk_s[warp][0][d];
+            s.x = fmaf(kt, vv.x, s.x);
+            s.y = fmaf(kt, vv.y, s.y);
+            s.z = fmaf(kt, vv.z, s.z);
+            s.w = fmaf(kt, vv.w, s.w);
+            *sp = s;
+            num.x = fmaf(qt, s.x, num.x);
+            num.y = fmaf(qt, s.y, num.y);
+            num.z = fmaf(qt, s.z, num.z);
+            num.w = fmaf(qt, s.w, num.w);
+        }
+        // combine lanes with the same column group (they differ in the row bits)
+        for (int o = cols; o < 32; o <<= 1) {
+            num.x += __shfl_xor_sync(0xffffffffu, num.x, o);
+            num.y += __shfl_xor_sync(0xffffffffu, num.y, o);
+            num.z += __shfl_xor_sync(0xffffffffu, num.z, o);
+            num.w += __shfl_xor_sync(0xffffffffu, num.w, o);
+        }
+        if (rsub == 0) {
+            const float inv = 1.f / den;
+            store4<T>(out + (size_t)h * Dv + col, make_float4(num.x * inv, num.y * inv, num.z * inv, num.w * inv));
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t recurrent_step(const void* q, const void* k, const void* v, float* S, float* z, void* out,
+                           const la_shape& s, cudaStream_t st) {
+    const int BH = s.B * s.H;
+    const unsigned blocks = (unsigned)((BH + kWarpsPerBlock - 1) / kWarpsPerBlock);
+    launch_begin("recurrent_step", st);
+    if (s.dtype == LA_BF16)
+        recurrent_step_kernel<__nv_bfloat16><<<blocks, 32 * kWarpsPerBlock, 0, st>>>(
+            (const __nv_bfloat16*)q, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, S, z, (__nv_bfloat16*)out, BH,
+            s.Dk, s.Dv);
+    else
+        recurrent_step_kernel<float><<<blocks, 32 * kWarpsPerBlock, 0, st>>>(
+            (const float*)q, (const float*)k, (const float*)v, S, z, (float*)out, BH, s.Dk, s.Dv);
+    return launch_end("recurrent_step", st);
+}
+
+}  // namespace la

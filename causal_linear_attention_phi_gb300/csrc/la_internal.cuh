@@ -1,0 +1,88 @@
+// la_internal.cuh -- definitions shared by the libla translation units.
+//
+// Work decomposition used by every chunked kernel.  A head's N positions are
+// cut into chunks of C positions (the last one may be short and is masked);
+// consecutive chunks are grouped into P segments of `cps` chunks.  One CTA owns
+// one (segment, head) pair and walks its chunks in order, carrying the state
+// (S, z) chunk to chunk on chip.  The states that cross segment boundaries are
+// produced by a per-segment reduction kernel and an exclusive scan over the P
+// segments (the prefix-sum structure of the causal form: "Transformers은 RNN이다"
+// digest, Insights / Prefix-sum 병렬성; itwiki 계산 형태 비교, chunked row).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "la.h"
+
+namespace la {
+
+// Elements of one (S, z) state record in the workspace: Dk*Dv for S then Dk for z.
+inline __host__ __device__ size_t state_elems(int Dk, int Dv) { return (size_t)Dk * Dv + Dk; }
+
+struct Plan {
+    int C;        // chunk length (positions)
+    int nchunks;  // ceil(N / C)
+    int P;        // segments per head
+    int cps;      // chunks per segment
+    bool tc;      // tensor-core (tcgen05) kernels, else CUDA-core kernels
+};
+
+// Byte offsets of the workspace regions of one call (all 256-byte aligned).
+struct WsLayout {
+    size_t seg_states;   // [BH][P][E] fp32: per-segment S/z sums, then scanned in place
+    size_t seg_states2;  // [BH][P][E] fp32: backward reverse-state sums (R, r)
+    size_t totals;       // [BH][E] fp32: non-causal totals
+    size_t den_g;        // [BH][N][2] fp32: backward per-position den and g
+    size_t bytes;        // total
+};
+
+Plan make_plan(const la_shape& s, int op);
+WsLayout make_ws_layout(const la_shape& s, int op, const Plan& p);
+
+// ------------------------------------------------------------------ device helpers
+template <typename T> __device__ __forceinline__ float to_f32(T x);
+template <> __device__ __forceinline__ float to_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+
+// phi(x) = elu(x) + 1 (alpha = 1): x + 1 for x > 0, exp(x) for x <= 0.
+__device__ __forceinline__ float phi_f(float x) { return x > 0.f ? x + 1.f : expf(x); }
+// phi'(x) = 1 for x > 0, exp(x) otherwise; equal to min(1, phi(x)).
+__device__ __forceinline__ float dphi_from_phi(float p) { return fminf(p, 1.f); }
+
+// ------------------------------------------------------------------ launch bookkeeping
+// Every launch goes through launch_begin/launch_end so the optional per-kernel
+// timing (la_timing_enable) can bracket it with events on the launch stream.
+void launch_begin(const char* name, cudaStream_t st);
+cudaError_t launch_end(const char* name, cudaStream_t st);
+
+// Device address of the sticky error word (set once per device).
+int* device_error_word();
+
+// ------------------------------------------------------------------ host launchers
+// CUDA-core (SIMT) kernels, any dtype, Dk/Dv multiples of 16 up to 128.
+cudaError_t simt_segment_sums(const void* k, const void* v, float* seg, const la_shape& s, const Plan& p,
+                              cudaStream_t st);
+cudaError_t scan_segments(float* seg, float* totals, const la_shape& s, const Plan& p, int mode,
+                          cudaStream_t st);
+cudaError_t simt_causal_fwd_out(const void* q, const void* k, const void* v, void* o, const float* seg,
+                                const la_shape& s, const Plan& p, cudaStream_t st);
+cudaError_t simt_noncausal_apply(const void* q, void* o, const float* totals, const la_shape& s,
+                                 cudaStream_t st);
+cudaError_t simt_bwd_forward_sweep(const void* q, const void* k, const void* v, const void* dout,
+                                   void* dq, const float* seg_S, float* seg_R, float* den_g,
+                                   const la_shape& s, const Plan& p, cudaStream_t st);
+cudaError_t simt_bwd_reverse_sweep(const void* q, const void* k, const void* v, const void* dout,
+                                   void* dk, void* dv, const float* seg_R, const float* den_g,
+                                   const la_shape& s, const Plan& p, cudaStream_t st);
+cudaError_t recurrent_step(const void* q, const void* k, const void* v, float* S, float* z, void* out,
+                           const la_shape& s, cudaStream_t st);
+
+enum ScanMode { SCAN_EXCLUSIVE_PREFIX = 0, SCAN_EXCLUSIVE_SUFFIX = 1, SCAN_TOTAL = 2 };
+
+}  // namespace la

@@ -1,0 +1,180 @@
+/*
+ * la.h -- C ABI of the GB300 (sm_103a) causal linear attention library (libla).
+ *
+ * The library computes attention with the kernel feature map phi(x) = elu(x) + 1
+ * (alpha = 1):
+ *
+ *   o_i = phi(q_i)^T S_i / (phi(q_i)^T z_i),
+ *   S_i = sum_{j in J(i)} phi(k_j) v_j^T   (Dk x Dv),   z_i = sum_{j in J(i)} phi(k_j)   (Dk),
+ *
+ * with J(i) = {j <= i} for the causal forms and all j for the non-causal form.
+ * No 1/sqrt(D) scale and no epsilon are applied.
+ *
+ * Sources, by page title and section:
+ *   "Transformers은 RNN이다 — 선형 어텐션으로 빠른 Autoregressive Transformer
+ *    만들기" (irregular6612 digest): Methods; 핵심 구성요소 1-4.
+ *   "[논문 리뷰] Transformers are RNNs: Fast Autoregressive Transformers with
+ *    Linear Attention" (velog review): 3.2 Linearized Attention, 3.3 Feature
+ *    Maps, 3.4 Causal Masking, 3.5 Gradient Computation, 3.6 Transformers and RNNs.
+ *   "선형 어텐션" (itwiki): 결합 법칙으로 순서 바꾸기; 인과 마스킹과 순환형;
+ *    계산 형태 비교 (chunked form); 구현.
+ *
+ * Conventions shared by every entry point
+ * ----------------------------------------
+ * Layout.   q, k: [B, H, N, Dk]; v, o, dout: [B, H, N, Dv]; dense row-major
+ *           (innermost dimension contiguous), one dtype per call (la_shape.dtype).
+ *           Decode state S: [B, H, Dk, Dv] fp32; z: [B, H, Dk] fp32.
+ * Memory.   Every tensor pointer is a DEVICE pointer on the current CUDA device,
+ *           16-byte aligned.  The caller owns and allocates every buffer,
+ *           including the workspace; the library allocates no device memory and
+ *           keeps no per-call state.  The workspace is scratch for one call: its
+ *           contents on entry are ignored and on exit are unspecified.
+ * Sizes.    B, H, N >= 0 (any zero makes the call a no-op returning LA_OK; the
+ *           pointers may then be NULL).  Dk and Dv are each one of 16, 32, 64,
+ *           128.  B*H <= 65535 and B*H*N*max(Dk,Dv) < 2^40.
+ * Streams.  `stream` is a cudaStream_t (NULL = the legacy default stream).  All
+ *           work is enqueued asynchronously on it; the call returns once the
+ *           launches are queued.
+ * Errors.   Invalid arguments return LA_ERR_INVALID_ARG, unsupported sizes
+ *           LA_ERR_UNSUPPORTED and a short workspace LA_ERR_WORKSPACE, all before
+ *           anything is launched.  A failed launch returns LA_ERR_CUDA.  Faults
+ *           detected on the device (a bounded wait that ran out) are recorded in
+ *           a sticky device word that la_last_error() reads after the stream has
+ *           been synchronised.  No C++ exception crosses this interface.
+ * Precision. Accumulation is fp32 throughout; inputs and outputs are fp32 or
+ *           bf16 (la_shape.dtype); the decode state is always fp32.
+ */
+#ifndef LA_H_
+#define LA_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    LA_OK = 0,
+    LA_ERR_INVALID_ARG = 1,  /* null / misaligned pointer, negative size, bad dtype or op */
+    LA_ERR_UNSUPPORTED = 2,  /* Dk or Dv not in {16, 32, 64, 128}, B*H > 65535, or not an sm_103 device */
+    LA_ERR_WORKSPACE = 3,    /* ws_bytes smaller than la_workspace_bytes(), or ws NULL */
+    LA_ERR_CUDA = 4,         /* a CUDA runtime call or kernel launch failed */
+    LA_ERR_TIMEOUT = 5       /* a bounded device-side wait ran out (read via la_last_error) */
+} la_status;
+
+typedef enum { LA_F32 = 0, LA_BF16 = 1 } la_dtype;
+
+typedef enum {
+    LA_OP_NONCAUSAL_FWD = 0,
+    LA_OP_CAUSAL_FWD = 1,
+    LA_OP_CAUSAL_BWD = 2,
+    LA_OP_NONCAUSAL_BWD = 3
+} la_op;
+
+/* Problem shape.  dtype is an la_dtype value. */
+typedef struct {
+    int B, H, N, Dk, Dv;
+    int dtype;
+} la_shape;
+
+/* A cudaStream_t, declared opaquely so this header needs no CUDA headers. */
+typedef struct CUstream_st* la_stream_t;
+
+/*
+ * Workspace bytes the call `op` needs for shape `s` (0 when none).  A pure
+ * function of (op, s): it does not touch the device.  Returns 0 for invalid
+ * arguments as well; the call itself then reports the error.
+ */
+size_t la_workspace_bytes(int op, la_shape s);
+
+/*
+ * Non-causal linear attention, o_i = phi(q_i)^T S / phi(q_i)^T z with
+ * S = phi(K)^T V and z = phi(K)^T 1 summed over all N positions of the head.
+ * ("Transformers은 RNN이다" digest, 핵심 구성요소 2; velog review 3.2;
+ * itwiki 결합 법칙으로 순서 바꾸기.)
+ * q, k: [B,H,N,Dk]; v: [B,H,N,Dv]; o: [B,H,N,Dv] (written).
+ */
+la_status la_noncausal_fwd(const void* q, const void* k, const void* v, void* o, la_shape s,
+                           void* ws, size_t ws_bytes, la_stream_t stream);
+
+/*
+ * Causal linear attention (j <= i, diagonal included), computed in the chunked
+ * form: inside a chunk the masked product phi(Q_c) phi(K_c)^T is formed, and the
+ * state (S, z) is carried between chunks by a prefix sum.  A final chunk shorter
+ * than the chunk size is masked.  (Digest, 핵심 구성요소 3; velog review 3.4;
+ * itwiki 계산 형태 비교, chunked row, and 구현.)
+ * q, k: [B,H,N,Dk]; v: [B,H,N,Dv]; o: [B,H,N,Dv] (written).
+ */
+la_status la_causal_fwd(const void* q, const void* k, const void* v, void* o, la_shape s,
+                        void* ws, size_t ws_bytes, la_stream_t stream);
+
+/*
+ * Gradient of the causal form for an upstream gradient dout = dL/do.  States
+ * are recomputed from q, k, v (nothing from the forward call is needed), and
+ * no per-position state is stored, so memory stays linear in N ("velog review"
+ * 3.5 Gradient Computation: the gradient is itself a cumulative sum).  With
+ * den_i = phi(q_i)^T z_i, P_i = dout_i / den_i, g_i = -(dout_i . o_i) / den_i,
+ * R_j = sum_{i>=j} phi(q_i) P_i^T and r_j = sum_{i>=j} g_i phi(q_i):
+ *   dq_i = (S_i P_i + g_i z_i) * phi'(q_i),
+ *   dk_j = (R_j v_j + r_j) * phi'(k_j),
+ *   dv_j = R_j^T phi(k_j).
+ * q, k, dq, dk: [B,H,N,Dk]; v, dout, dv: [B,H,N,Dv]; dq, dk, dv written.
+ */
+la_status la_causal_bwd(const void* q, const void* k, const void* v, const void* dout,
+                        void* dq, void* dk, void* dv, la_shape s,
+                        void* ws, size_t ws_bytes, la_stream_t stream);
+
+/*
+ * One recurrent (decode) step for every head, the state updated first and then
+ * read:  S <- S + phi(k) v^T,  z <- z + phi(k),  out = phi(q)^T S / phi(q)^T z.
+ * ("Transformers은 RNN이다" digest, 핵심 구성요소 4; velog review 3.6; itwiki
+ * 인과 마스킹과 순환형.)
+ * q, k: [B,H,Dk]; v, out: [B,H,Dv] in s.dtype; S: [B,H,Dk,Dv] fp32 and
+ * z: [B,H,Dk] fp32, both read and updated in place.  s.N is ignored.  The
+ * caller zeroes S and z before the first step of a sequence; passing saved
+ * (S, z) back in resumes it exactly.  No workspace.
+ */
+la_status la_recurrent_step(const void* q, const void* k, const void* v, float* S, float* z,
+                            void* out, la_shape s, la_stream_t stream);
+
+/*
+ * Sticky device-side status: LA_OK, or the first error a kernel recorded since
+ * the last la_clear_error() (LA_ERR_TIMEOUT for a bounded wait that ran out).
+ * It reads device memory synchronously (the current device is synchronised);
+ * call it after the stream work has finished.  la_clear_error() resets it.
+ */
+la_status la_last_error(void);
+la_status la_clear_error(void);
+
+/* Static description of a status code. */
+const char* la_status_string(la_status st);
+
+/* Text of the most recent host-side failure on the calling thread ("" if none). */
+const char* la_error_detail(void);
+
+/* Library version, e.g. "0.1.0". */
+const char* la_version(void);
+
+/*
+ * Per-kernel timing (for the benchmark).  While enabled, every kernel launch
+ * is bracketed by CUDA events recorded on its launch stream; la_timing_read()
+ * synchronises those events and reports, per kernel name, the number of
+ * launches and their total device time since the last reset.  Off by default;
+ * enabling it adds two event records per launch and nothing else.
+ */
+typedef struct {
+    const char* name;   /* static string owned by the library */
+    int launches;
+    double total_ms;
+} la_kernel_time;
+
+la_status la_timing_enable(int on);
+la_status la_timing_reset(void);
+/* Fills up to `max` entries; returns the number of distinct kernels, or -1 on error. */
+int la_timing_read(la_kernel_time* out, int max);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LA_H_ */

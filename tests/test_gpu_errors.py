@@ -1,0 +1,63 @@
+"""Error behaviour of the C ABI on a GPU: bad pointers and short workspaces are
+refused before anything is launched, and the sticky device word stays clear."""
+import ctypes
+
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module")
+def la():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import causal_linear_attention_phi_gb300 as la
+    la.build.build_library()
+    la.clear_error()
+    return la
+
+
+def _raw_fwd(la, q, k, v, o, ws, nbytes):
+    s = la.Shape(*q.shape, v.shape[-1], la.LA_F32)
+    p = lambda t: ctypes.c_void_p(t.data_ptr()) if isinstance(t, torch.Tensor) else ctypes.c_void_p(t)
+    return la.library().la_causal_fwd(p(q), p(k), p(v), p(o), s, p(ws), nbytes, None)
+
+
+def test_workspace_too_small(la):
+    q = torch.randn(1, 2, 300, 32, device=DEV)
+    need = la.workspace_bytes(la.OP_CAUSAL_FWD, 1, 2, 300, 32, 32, torch.float32)
+    ws = torch.empty(need, dtype=torch.uint8, device=DEV)
+    o = torch.empty_like(q)
+    assert _raw_fwd(la, q, q, q, o, ws, need - 1) == 3
+    assert _raw_fwd(la, q, q, q, o, 0, need) == 3
+    assert _raw_fwd(la, q, q, q, o, ws, need) == 0
+
+
+def test_bad_pointers(la):
+    q = torch.randn(1, 2, 100, 32, device=DEV)
+    o = torch.empty_like(q)
+    need = la.workspace_bytes(la.OP_CAUSAL_FWD, 1, 2, 100, 32, 32, torch.float32)
+    ws = torch.empty(need, dtype=torch.uint8, device=DEV)
+    host = torch.randn(1, 2, 100, 32)
+    assert _raw_fwd(la, host, q, q, o, ws, need) == 1            # host memory refused
+    assert _raw_fwd(la, q, q, q, 0, ws, need) == 1               # NULL output
+    assert _raw_fwd(la, q.data_ptr() + 4, q, q, o, ws, need) == 1  # misaligned
+    with pytest.raises(la.LaError):
+        la.causal_fwd(q, q, torch.randn(1, 2, 100, 48, device=DEV))  # unsupported Dv
+    torch.cuda.synchronize()
+    assert la.last_error() == 0
+
+
+def test_timing_hooks(la):
+    q = torch.randn(1, 2, 640, 64, device=DEV)
+    la.timing_reset()
+    la.timing_enable(True)
+    try:
+        la.causal_fwd(q, q, q)
+        t = la.timing_read()
+    finally:
+        la.timing_enable(False)
+    assert any(n.startswith("simt_causal_fwd") or n.startswith("tc_") for n in t)
+    assert all(v[0] >= 1 and v[1] >= 0 for v in t.values())

@@ -1,0 +1,222 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Every comparison is per (b, h) head slice, max|gpu - oracle| / max|oracle|,
+bounded by 1e-4 for fp32 inputs and 2e-2 for bf16 inputs (fp32 accumulation).
+The oracle consumes the same seeded inputs after the cast to the input dtype.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from causal_linear_attention_phi_gb300 import workloads as W
+from util import rel_per_head, tol_for, to_np
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module")
+def la():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import causal_linear_attention_phi_gb300 as la
+    la.build.build_library()
+    la.library()
+    la.clear_error()
+    yield la
+    assert la.last_error() == 0
+
+
+def dev(*ts):
+    return [t.to(DEV) for t in ts]
+
+
+def check(name, gpu, ref, tol):
+    e = rel_per_head(gpu, ref)
+    assert e <= tol, "%s: max rel err %.3e > %.1e" % (name, e, tol)
+    return e
+
+
+# ---------------------------------------------------------------- forward, small fp32 workload
+def test_small_f32_causal_fwd(la):
+    q, k, v = W.make_inputs(W.SMALL_F32)
+    o = la.causal_fwd(*dev(q, k, v))
+    check("o vs direct", o, oracle.causal_direct(q, k, v), 1e-4)
+    check("o vs recurrent", o, oracle.causal_recurrent(q, k, v), 1e-4)
+
+
+# ---------------------------------------------------------------- forward, bf16 B=4 H=8 N=1024 D=64
+def test_fwd_bf16_noncausal_and_causal(la):
+    q, k, v = W.make_inputs(W.FWD_BF16)
+    qd, kd, vd = dev(q, k, v)
+    onc = la.noncausal_fwd(qd, kd, vd)
+    oc = la.causal_fwd(qd, kd, vd)
+    assert onc.dtype == torch.bfloat16 and oc.dtype == torch.bfloat16
+    check("noncausal", onc, oracle.noncausal_assoc(q, k, v), 2e-2)
+    check("causal", oc, oracle.causal_recurrent(q, k, v), 2e-2)
+
+
+# ---------------------------------------------------------------- edge cases of the forward
+FWD_CASES = [
+    # (B, H, N, Dk, Dv, dtype)
+    (1, 1, 1, 16, 16, torch.float32),      # a single position: o = v
+    (1, 2, 63, 32, 16, torch.float32),     # one short chunk
+    (1, 1, 64, 16, 32, torch.float32),     # exactly one chunk
+    (2, 1, 65, 64, 128, torch.float32),    # one position past a chunk
+    (1, 3, 200, 128, 64, torch.float32),   # several chunks and a ragged tail
+    (1, 2, 1000, 128, 128, torch.float32), # many segments (segment scan in use)
+    (3, 1, 777, 32, 32, torch.bfloat16),
+    (1, 1, 4097, 64, 64, torch.bfloat16),
+    (2, 2, 130, 16, 128, torch.bfloat16),
+]
+
+
+@pytest.mark.parametrize("B,H,N,Dk,Dv,dtype", FWD_CASES)
+def test_causal_fwd_cases(la, B, H, N, Dk, Dv, dtype):
+    scale = 1.0 if dtype == torch.float32 else 0.5
+    q, k, v = W.random_case(100 + N, B, H, N, Dk, Dv, dtype=dtype, scale=scale)
+    o = la.causal_fwd(*dev(q, k, v))
+    ref = oracle.causal_direct(q, k, v) if N <= 1000 else oracle.causal_recurrent(q, k, v)
+    check("causal o", o, ref, tol_for(dtype))
+    onc = la.noncausal_fwd(*dev(q, k, v))
+    check("noncausal o", onc, oracle.noncausal_assoc(q, k, v), tol_for(dtype))
+    if N == 1:
+        assert torch.allclose(o.cpu(), v, rtol=1e-6, atol=0)
+
+
+def test_constant_v_gives_constant_output(la):
+    q, k, _ = W.random_case(5, 1, 2, 333, 64, 32, dtype=torch.float32)
+    c = torch.linspace(-2, 2, 32)
+    v = c.expand(1, 2, 333, 32).contiguous()
+    o = la.causal_fwd(*dev(q, k, v)).cpu()
+    assert torch.max(torch.abs(o - c)) < 1e-5
+
+
+def test_empty_is_noop(la):
+    z = torch.empty(1, 2, 0, 16, device=DEV)
+    o = la.causal_fwd(z, z, z)
+    assert o.shape == (1, 2, 0, 16)
+
+
+# ---------------------------------------------------------------- backward
+BWD_CASES = [
+    (1, 1, 1, 16, 16, torch.float32),
+    (1, 2, 50, 16, 32, torch.float32),     # the itwiki check's shapes
+    (2, 1, 129, 32, 16, torch.float32),
+    (1, 2, 700, 64, 64, torch.float32),    # multiple segments
+    (1, 1, 300, 128, 128, torch.float32),
+    (1, 2, 1000, 64, 64, torch.bfloat16),
+    (2, 1, 515, 128, 128, torch.bfloat16),
+]
+
+
+@pytest.mark.parametrize("B,H,N,Dk,Dv,dtype", BWD_CASES)
+def test_causal_bwd_cases(la, B, H, N, Dk, Dv, dtype):
+    scale = 1.0 if dtype == torch.float32 else 0.5
+    q, k, v, dO = W.random_case(200 + N, B, H, N, Dk, Dv, dtype=dtype, scale=scale, with_grad=True)
+    dq, dk, dv = la.causal_bwd(*dev(q, k, v, dO))
+    ref = oracle.causal_bwd_recurrent(q, k, v, dO)
+    tol = tol_for(dtype)
+    for name, a, b in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
+        check(name, a, b, tol)
+
+
+def test_bwd_invariants(la):
+    q, k, v, dO = W.random_case(31, 1, 2, 257, 32, 32, dtype=torch.float32, with_grad=True)
+    dq, dk, dv = la.causal_bwd(*dev(q, k, v, dO))
+    # sum_j dv_j = sum_i dO_i per head and column
+    assert rel_per_head(dv.sum(2, keepdim=True).cpu(), dO.sum(2, keepdim=True)) < 1e-4
+    # constant v: the output ignores q and k
+    vc = torch.linspace(-1, 1, 32).expand_as(v).contiguous()
+    dq, dk, _ = la.causal_bwd(*dev(q, k, vc, dO))
+    assert float(dq.abs().max()) < 1e-4 and float(dk.abs().max()) < 1e-4
+
+
+# ---------------------------------------------------------------- length sweep, bf16 B=1 H=8 D=64
+@pytest.mark.parametrize("N", [512, 1024, 4096])
+def test_sweep_fwd_bwd_full(la, N):
+    w = W.sweep(N)
+    q, k, v, dO = W.make_inputs(w, with_grad=True)
+    qd, kd, vd, dOd = dev(q, k, v, dO)
+    o = la.causal_fwd(qd, kd, vd)
+    dq, dk, dv = la.causal_bwd(qd, kd, vd, dOd)
+    check("o", o, oracle.causal_recurrent(q, k, v), 2e-2)
+    for name, a, b in zip(("dq", "dk", "dv"), (dq, dk, dv), oracle.causal_bwd_recurrent(q, k, v, dO)):
+        check(name, a, b, 2e-2)
+
+
+def _sampled_heads(la, w, heads):
+    """Full-size run on the GPU, oracle on a few whole heads (heads are independent)."""
+    q, k, v, dO = W.make_inputs(w, with_grad=True)
+    qd, kd, vd, dOd = dev(q, k, v, dO)
+    o = la.causal_fwd(qd, kd, vd)
+    dq, dk, dv = la.causal_bwd(qd, kd, vd, dOd)
+    torch.cuda.synchronize()
+    sel = lambda t: torch.stack([t[b, h] for b, h in heads])[None]
+    qs, ks, vs, dOs = (sel(t) for t in (q, k, v, dO))
+    check("o", sel(o.cpu()), oracle.causal_recurrent(qs, ks, vs), 2e-2)
+    ref = oracle.causal_bwd_recurrent(qs, ks, vs, dOs)
+    for name, a, b in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
+        check(name, sel(a.cpu()), b, 2e-2)
+
+
+def test_sweep_65536_sampled_heads(la):
+    _sampled_heads(la, W.sweep(65536), [(0, 0), (0, 5)])
+
+
+def test_long_bf16_full_size_sampled_heads(la):
+    _sampled_heads(la, W.LONG_BF16, [(0, 0), (1, 15)])
+
+
+# ---------------------------------------------------------------- decode
+def test_decode_mnist_shape_all_steps(la):
+    w = W.DECODE_MNIST
+    q, k, v = W.make_decode_inputs(w)
+    qd, kd, vd = dev(q, k, v)
+    S = torch.zeros(w.B, w.H, w.Dk, w.Dv, device=DEV)
+    z = torch.zeros(w.B, w.H, w.Dk, device=DEV)
+    outs = torch.empty(w.steps, w.B, w.H, w.Dv, device=DEV)
+    for t in range(w.steps):
+        la.recurrent_step(qd[t], kd[t], vd[t], S, z, out=outs[t])
+    torch.cuda.synchronize()
+    # the causal form over the step sequence, computed by the oracle
+    to_seq = lambda x: x.permute(1, 2, 0, 3).contiguous()
+    ref = oracle.causal_recurrent(to_seq(q), to_seq(k), to_seq(v))
+    check("decode outputs", to_seq(outs.cpu()), ref, 1e-4)
+    phk = oracle.phi(to_seq(k))
+    check("final S", S.cpu(), np.einsum("bhnd,bhnm->bhdm", phk, to_np(to_seq(v))), 1e-4)
+    assert rel_per_head(z.cpu()[..., None], phk.sum(axis=2)[..., None]) < 1e-4
+
+
+def test_decode_resume_is_bit_exact(la):
+    q, k, v = (t[:, :4] for t in W.make_decode_inputs(W.DECODE_MNIST, steps=40))
+    qd, kd, vd = dev(q.contiguous(), k.contiguous(), v.contiguous())
+    S = torch.zeros(4, 8, 32, 32, device=DEV)
+    z = torch.zeros(4, 8, 32, device=DEV)
+    full = [la.recurrent_step(qd[t], kd[t], vd[t], S, z).clone() for t in range(40)]
+    S2 = torch.zeros_like(S)
+    z2 = torch.zeros_like(z)
+    for t in range(25):
+        la.recurrent_step(qd[t], kd[t], vd[t], S2, z2)
+    saved_S, saved_z = S2.cpu(), z2.cpu()          # checkpoint to the host and back
+    S3, z3 = saved_S.to(DEV), saved_z.to(DEV)
+    for t in range(25, 40):
+        o = la.recurrent_step(qd[t], kd[t], vd[t], S3, z3)
+        assert torch.equal(o, full[t])
+    assert torch.equal(S3, S) and torch.equal(z3, z)
+
+
+@pytest.mark.parametrize("Dk,Dv,dtype", [(16, 16, torch.float32), (64, 32, torch.float32), (128, 128, torch.float32),
+                                         (32, 64, torch.bfloat16), (128, 16, torch.bfloat16)])
+def test_decode_head_sizes(la, Dk, Dv, dtype):
+    B, H, T = 3, 5, 9
+    q, k, v = W.random_case(41, B, H, T, Dk, Dv, dtype=dtype)
+    S = torch.zeros(B, H, Dk, Dv, device=DEV)
+    z = torch.zeros(B, H, Dk, device=DEV)
+    qd, kd, vd = dev(q, k, v)
+    outs = [la.recurrent_step(qd[:, :, t].contiguous(), kd[:, :, t].contiguous(), vd[:, :, t].contiguous(), S, z)
+            for t in range(T)]
+    o = torch.stack(outs, 2)
+    check("decode", o, oracle.causal_recurrent(q, k, v), tol_for(dtype))
