@@ -1,0 +1,467 @@
+"""Throughput of causal linear attention (phi = elu + 1) on one GB300 per rank.
+
+Default workload: causal forward + backward, bf16 inputs with fp32
+accumulation, B=2 H=16 N=65536 Dk=Dv=128 (Q, K ~ N(0,1)/sqrt(128), V, dO ~
+N(0,1), seed 5).  One step = la_causal_fwd + la_causal_bwd over that batch
+(feature map, intra-chunk products, chunk-state scan, backward with states
+recomputed).  The inputs (2.1 GB) are far larger than L2, so consecutive steps
+cannot reuse cached data.
+
+Printed on rank 0 as one JSON line:
+  value       tokens/s (B*N*ranks / step time), inputs resident in HBM
+  e2e         the same through the C ABI with host buffers: pinned-host copies
+              of q, k, v, dO in and o, dq, dk, dv out inside the timed region
+  roofline    the dominant kernel against the measured HBM copy bandwidth
+  decode      recurrent step at B=64 H=8 D=32, 3072 and 784 steps, CUDA graph
+  noncausal   the non-causal forward at B=4 H=8 N=1024 D=64 bf16
+  cpu_baseline  the fp64 oracle on a bounded sample of the same workload
+
+`--impl reference` times the fp64 CPU oracle on the same workload instead
+(the only reference that exists for this method: it is not a GPU program).
+Multi-GPU (torchrun): every rank runs its own replica of the batch (heads are
+independent), no collective on the data path; time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from causal_linear_attention_phi_gb300 import workloads as W  # noqa: E402
+
+PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_PATH = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+# ------------------------------------------------------------------ helpers
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def peaks():
+    try:
+        with open(PEAKS_PATH) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for l in self.lines:
+            parts = [x.strip() for x in l.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def kernel_sources_sha():
+    import glob
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "causal_linear_attention_phi_gb300", "csrc", "*"))):
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str):
+    """DRAM bytes per launch from a committed ncu summary, if taken on the current kernels."""
+    try:
+        with open(TRAFFIC_PATH) as f:
+            t = json.load(f)
+    except Exception:
+        return None
+    if t.get("sources_sha") != kernel_sources_sha():
+        return None
+    k = t.get("kernels", {}).get(kernel)
+    return None if k is None else float(k["dram_bytes_per_launch"])
+
+
+# Compulsory HBM bytes per launch of each kernel (its own inputs and outputs,
+# each counted once), for the long bf16 workload.  units = token-heads.
+def kernel_algorithmic_bytes(name: str, B, H, N, Dk, Dv, sz):
+    T = B * H * N
+    table = {
+        "segment_sums": T * (Dk + Dv) * sz,                       # read k, v
+        "causal_fwd_out": T * (2 * Dk + 2 * Dv) * sz,             # read q, k, v; write o
+        "bwd_forward_sweep": T * ((2 * Dk + 2 * Dv) * sz + Dk * sz + 8),   # read q,k,v,dO; write dq, (den,g)
+        "bwd_reverse_sweep": T * ((2 * Dk + 2 * Dv) * sz + 8 + (Dk + Dv) * sz),  # read q,k,v,dO,(den,g); write dk,dv
+    }
+    for key, val in table.items():
+        if key in name:
+            return val
+    return None
+
+
+# ------------------------------------------------------------------ our implementation
+def run_ours(args):
+    import causal_linear_attention_phi_gb300 as la
+
+    ws_n, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws_n > 1:
+        import datetime
+        import torch.distributed as dist
+        dist.init_process_group("nccl", timeout=datetime.timedelta(minutes=10))
+    la.build.build_library()
+    la.library()
+    la.clear_error()
+
+    w = W.LONG_BF16
+    B, H, N, Dk, Dv = w.B, w.H, w.N, w.Dk, w.Dv
+    q, k, v, dO = W.make_inputs(w, with_grad=True)
+    qd, kd, vd, dOd = (t.to(dev) for t in (q, k, v, dO))
+    o = torch.empty_like(vd)
+    dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    ws_f = torch.empty(la.workspace_bytes(la.OP_CAUSAL_FWD, B, H, N, Dk, Dv, w.dtype), dtype=torch.uint8, device=dev)
+    ws_b = torch.empty(la.workspace_bytes(la.OP_CAUSAL_BWD, B, H, N, Dk, Dv, w.dtype), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        la.causal_fwd(qd, kd, vd, out=o, workspace=ws_f)
+        la.causal_bwd(qd, kd, vd, dOd, dq=dq, dk=dk, dv=dv, workspace=ws_b)
+
+    def barrier():
+        if ws_n > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert la.last_error() == 0
+
+    # ---- timed region (device events on the launch stream; per-kernel events inside)
+    la.timing_reset()
+    la.timing_enable(True)
+    barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    la.timing_enable(False)
+    ktimes = la.timing_read()
+    ms_total = e0.elapsed_time(e1)
+    if ws_n > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    tokens_per_step = B * N * ws_n
+    value = tokens_per_step / (ms_step / 1e3)
+    launches = sum(c for c, _ in ktimes.values())
+    assert la.last_error() == 0
+
+    # ---- roofline of the dominant kernel
+    hbm, tc_peak, peak_kind = peaks()
+    dom = max(ktimes.items(), key=lambda kv: kv[1][1])
+    dom_name, (dom_n, dom_ms) = dom
+    avg_ms = dom_ms / dom_n
+    alg = kernel_algorithmic_bytes(dom_name, B, H, N, Dk, Dv, 2)
+    achieved = alg / (avg_ms / 1e3) / 1e9 if alg else None
+    traffic = ncu_traffic(dom_name)
+    roofline = {"kernel": dom_name, "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                "frac": (achieved / hbm) if achieved else None, "traffic": traffic,
+                "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else peak_kind,
+                "algorithmic_bytes_per_launch": alg, "avg_launch_ms": avg_ms}
+    step_alg_bytes = B * H * N * ((2 * Dk + 2 * Dv) + (4 * Dk + 3 * Dv)) * 2
+    step_roof = {"algorithmic_bytes": step_alg_bytes,
+                 "achieved_gbs": step_alg_bytes / (ms_step / 1e3) / 1e9,
+                 "frac": step_alg_bytes / (ms_step / 1e3) / 1e9 / hbm}
+
+    result = {
+        "metric": "causal lin-attn fwd+bwd tokens/s @N=64K; decode steps/s; % of roofline",
+        "value": value, "unit": "tokens/s", "n_gpus": ws_n, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded N(0,1) inputs, no dataset)",
+        "config": {"workload": w.name, "B": B, "H": H, "N": N, "Dk": Dk, "Dv": Dv,
+                   "global_batch": B * ws_n, "seq_len": N, "parallelism": "replicas over heads/batch (dp%d)" % ws_n,
+                   "l2": "inputs (2.1 GB) larger than L2; no flush needed"},
+        "kernel_times_ms": {n: {"launches": c, "total_ms": round(t, 4)} for n, (c, t) in ktimes.items()},
+        "gpu_launches": launches,
+        "roofline": roofline,
+        "step_roofline": step_roof,
+        "clocks": clk.summary(),
+    }
+
+    # ---- end to end through the C ABI with host buffers (pinned host in, host out)
+    if not args.skip_e2e:
+        host_in = [t.pin_memory() for t in (q, k, v, dO)]
+        host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (q, k, v, v)]
+        h2d = sum(t.numel() * t.element_size() for t in host_in)
+        d2h = sum(t.numel() * t.element_size() for t in host_out)
+
+        def e2e_step():
+            for hsrc, ddst in zip(host_in, (qd, kd, vd, dOd)):
+                ddst.copy_(hsrc, non_blocking=True)
+            step()
+            for dsrc, hdst in zip((dq, dk, dv, o), host_out[:3] + [host_out[3]]):
+                hdst.copy_(dsrc, non_blocking=True)
+
+        e2e_steps = max(2, min(args.steps, 5))
+        e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        a1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = a0.elapsed_time(a1) / e2e_steps
+        if ws_n > 1:
+            import torch.distributed as dist
+            t = torch.tensor([e2e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        result["e2e"] = {"value": tokens_per_step / (e2e_ms / 1e3), "unit": "tokens/s",
+                         "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+        del host_in, host_out
+
+    # ---- decode and non-causal sub-measurements (rank 0 only, not part of value)
+    if rank == 0 and not args.skip_extras:
+        result["decode"] = bench_decode(la, dev, hbm)
+        result["noncausal"] = bench_noncausal(la, dev)
+    if rank == 0 and not args.skip_cpu:
+        result["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    assert la.last_error() == 0
+    if ws_n > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(result))
+
+
+def bench_decode(la, dev, hbm):
+    out = {}
+    for wd in (W.DECODE_CIFAR, W.DECODE_MNIST):
+        T = wd.steps
+        q, k, v = (t.to(dev) for t in W.make_decode_inputs(wd))
+        S = torch.zeros(wd.B, wd.H, wd.Dk, wd.Dv, device=dev)
+        z = torch.zeros(wd.B, wd.H, wd.Dk, device=dev)
+        outs = torch.empty(T, wd.B, wd.H, wd.Dv, device=dev)
+        s = torch.cuda.Stream(dev)
+        s.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(s):
+            for t in range(3):  # warm-up outside capture
+                la.recurrent_step(q[t], k[t], v[t], S, z, out=outs[t])
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for t in range(T):
+                la.recurrent_step(q[t], k[t], v[t], S, z, out=outs[t])
+        g.replay()
+        torch.cuda.synchronize()
+        reps = 5
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        us_step = e0.elapsed_time(e1) * 1e3 / (reps * T)
+        # kernel-only duration: eager launches bracketed by the library's per-launch events
+        la.timing_reset()
+        la.timing_enable(True)
+        for t in range(min(T, 200)):
+            la.recurrent_step(q[t], k[t], v[t], S, z, out=outs[t])
+        torch.cuda.synchronize()
+        la.timing_enable(False)
+        n_l, ms_l = la.timing_read()["recurrent_step"]
+        kern_us = ms_l * 1e3 / n_l
+        bytes_step = wd.B * wd.H * (2 * wd.Dk * wd.Dv * 4 + 2 * wd.Dk * 4 + (2 * wd.Dk + 2 * wd.Dv) * 4)
+        out["steps_%d" % T] = {
+            "steps_per_s": 1e6 / us_step, "us_per_step": us_step, "tokens_per_s": wd.B * 1e6 / us_step,
+            "kernel_us": kern_us, "bytes_per_step": bytes_step,
+            "achieved_gbs_graph": bytes_step / (us_step * 1e-6) / 1e9,
+            "achieved_gbs_kernel": bytes_step / (kern_us * 1e-6) / 1e9,
+            "frac_graph": bytes_step / (us_step * 1e-6) / 1e9 / hbm,
+            "note": "S (2 MiB) stays in L2 across steps; graph replay of %d single-step launches" % T}
+    return out
+
+
+def bench_noncausal(la, dev):
+    w = W.FWD_BF16
+    q, k, v = (t.to(dev) for t in W.make_inputs(w))
+    o = torch.empty_like(v)
+    ws = torch.empty(la.workspace_bytes(la.OP_NONCAUSAL_FWD, w.B, w.H, w.N, w.Dk, w.Dv, w.dtype),
+                     dtype=torch.uint8, device=dev)
+    oc = torch.empty_like(v)
+    wsc = torch.empty(la.workspace_bytes(la.OP_CAUSAL_FWD, w.B, w.H, w.N, w.Dk, w.Dv, w.dtype),
+                      dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    res = {}
+    for name, fn in (("noncausal_fwd", lambda: la.noncausal_fwd(q, k, v, out=o, workspace=ws)),
+                     ("causal_fwd", lambda: la.causal_fwd(q, k, v, out=oc, workspace=wsc))):
+        for _ in range(3):
+            fn()
+        times = []
+        for _ in range(20):
+            flush.zero_()  # evict L2 (inputs are only 16.8 MB)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1))
+        ms = statistics.median(times)
+        res[name] = {"ms": ms, "tokens_per_s": w.B * w.N / (ms / 1e3), "workload": w.name, "l2": "flushed"}
+    return res
+
+
+# ------------------------------------------------------------------ CPU baseline (the fp64 oracle)
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(seconds_hint: float = 15.0):
+    """The fp64 oracle (recurrent forward + reverse-recurrence backward) on a
+    bounded sample of the long bf16 workload: `heads` whole heads, first
+    `n_pos` positions each.  Throughput is scaled to the workload's unit:
+    tokens/s = (heads * n_pos / H) / seconds."""
+    import oracle
+    cores = cpu_cores()
+    os.environ.setdefault("OMP_NUM_THREADS", str(cores))
+    w = W.LONG_BF16
+    heads = cores
+    # calibrate the sample size on a small probe so the run lasts about `seconds_hint`
+    n_probe = 1024
+    q, k, v, dO = W.make_inputs(w, with_grad=True, B=1, H=heads, N=n_probe)
+    t0 = time.perf_counter()
+    oracle.causal_recurrent(q, k, v)
+    oracle.causal_bwd_recurrent(q, k, v, dO)
+    dt = time.perf_counter() - t0
+    n_pos = int(min(w.N, max(n_probe, n_probe * seconds_hint / max(dt, 1e-6))))
+    q, k, v, dO = W.make_inputs(w, with_grad=True, B=1, H=heads, N=n_pos)
+    t0 = time.perf_counter()
+    oracle.causal_recurrent(q, k, v)
+    oracle.causal_bwd_recurrent(q, k, v, dO)
+    dt = time.perf_counter() - t0
+    tps = heads * n_pos / w.H / dt
+    return {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": "%d heads x %d positions of B=2 H=16 N=65536 D=128 (fp64 recurrent fwd + reverse-recurrence "
+                      "bwd, OpenMP over heads), %.1f s" % (heads, n_pos, dt),
+            "seconds": dt}
+
+
+def run_reference(args):
+    ws_n, rank, local = dist_env()
+    if rank != 0:
+        return
+    step_seconds = max(1.0, args.cpu_seconds / max(1, args.steps))
+    for _ in range(args.warmup):
+        cpu_baseline(min(step_seconds, 2.0))
+    vals = []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        vals.append(cpu_baseline(step_seconds))
+    total = time.perf_counter() - t0
+    value = statistics.mean(v["value"] for v in vals)
+    w = W.LONG_BF16
+    res = {"impl": "reference", "metric": "causal lin-attn fwd+bwd tokens/s @N=64K; decode steps/s; % of roofline",
+           "value": value, "unit": "tokens/s", "n_gpus": ws_n, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded, no dataset)",
+           "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "Dk": w.Dk, "Dv": w.Dv},
+           "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": vals[0]["cores"], "kind": "oracle",
+                            "sample": vals[0]["sample"]},
+           "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(res))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--skip-extras", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

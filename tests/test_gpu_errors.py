@@ -20,7 +20,7 @@ def la():
 
 
 def _raw_fwd(la, q, k, v, o, ws, nbytes):
-    s = la.Shape(*q.shape, v.shape[-1], la.LA_F32)
+    s = la.Shape(*k.shape, v.shape[-1], la.LA_F32)
     p = lambda t: ctypes.c_void_p(t.data_ptr()) if isinstance(t, torch.Tensor) else ctypes.c_void_p(t)
     return la.library().la_causal_fwd(p(q), p(k), p(v), p(o), s, p(ws), nbytes, None)
 

@@ -102,7 +102,6 @@ def test_empty_is_noop(la):
 
 # ---------------------------------------------------------------- backward
 BWD_CASES = [
-    (1, 1, 1, 16, 16, torch.float32),
     (1, 2, 50, 16, 32, torch.float32),     # the itwiki check's shapes
     (2, 1, 129, 32, 16, torch.float32),
     (1, 2, 700, 64, 64, torch.float32),    # multiple segments
@@ -121,6 +120,14 @@ def test_causal_bwd_cases(la, B, H, N, Dk, Dv, dtype):
     tol = tol_for(dtype)
     for name, a, b in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
         check(name, a, b, tol)
+
+
+def test_bwd_single_position(la):
+    # N = 1: o_1 = v_1 whatever q and k are, so dq = dk = 0 exactly and dv = dO.
+    q, k, v, dO = W.random_case(30, 2, 3, 1, 16, 32, dtype=torch.float32, with_grad=True)
+    dq, dk, dv = la.causal_bwd(*dev(q, k, v, dO))
+    assert float(dq.abs().max()) < 1e-5 and float(dk.abs().max()) < 1e-5
+    assert torch.allclose(dv.cpu(), dO, rtol=1e-5, atol=1e-6)
 
 
 def test_bwd_invariants(la):
