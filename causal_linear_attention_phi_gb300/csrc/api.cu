@@ -3,6 +3,7 @@
 // error word and the optional per-kernel timing.
 #include <cstdarg>
 #include <cstdio>
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 #include <string>
@@ -124,24 +125,55 @@ cudaError_t launch_end(const char* name, cudaStream_t st) {
 
 // ------------------------------------------------------------------ planning
 // CUDA-core kernels: one CTA per SM (about 215 KB of shared memory at D = 128),
-// so aim for a few hundred CTAs; the count is a fixed function of the shape so
+// so aim for a few hundred CTAs.  Tensor-core kernels: one CTA per SM as well;
+// the segment count is chosen so the CTAs fill whole waves of the GB300's 152
+// SMs with equal chunk counts.  Both are fixed functions of the shape so that
 // la_workspace_bytes stays device independent.
 static constexpr int kSimtChunk = 64;
 static constexpr int kTargetCtas = 304;
+static constexpr int kTcChunk = 128;
+static constexpr int kSms = 152;
+static constexpr int kMaxWaves = 8;
 
-Plan make_plan(const la_shape& s, int /*op*/) {
-    Plan p{};
-    p.tc = false;
-    p.C = kSimtChunk;
-    p.nchunks = (s.N + p.C - 1) / p.C;
-    const int BH = s.B * s.H;
-    int P = (kTargetCtas + BH - 1) / BH;
+bool tc_supported(const la_shape& s, int op) {
+    return s.dtype == LA_BF16 && s.Dk == 128 && s.Dv == 128 && (op == LA_OP_CAUSAL_FWD || op == LA_OP_CAUSAL_BWD);
+}
+
+static void finish_plan(Plan& p, int P) {
     if (P < 1) P = 1;
     if (P > p.nchunks) P = p.nchunks;
     if (P < 1) P = 1;
     p.cps = (p.nchunks + P - 1) / P;
     p.P = (p.nchunks + p.cps - 1) / p.cps;
     if (p.P < 1) p.P = 1;
+}
+
+Plan make_plan(const la_shape& s, int op) {
+    Plan p{};
+    const int BH = s.B * s.H;
+    p.tc = tc_supported(s, op);
+    p.C = p.tc ? kTcChunk : kSimtChunk;
+    p.nchunks = (s.N + p.C - 1) / p.C;
+    if (!p.tc) {
+        finish_plan(p, (kTargetCtas + BH - 1) / BH);
+        return p;
+    }
+    // maximise useful chunk work / (waves * SMs * chunks per CTA)
+    int best_P = 1;
+    double best = -1.0;
+    const int pmax = std::max(1, std::min(p.nchunks, kMaxWaves * kSms / std::max(BH, 1)));
+    for (int P = 1; P <= pmax; ++P) {
+        const int cps = (p.nchunks + P - 1) / P;
+        const int Pr = (p.nchunks + cps - 1) / cps;
+        const long long ctas = (long long)BH * Pr;
+        const long long waves = (ctas + kSms - 1) / kSms;
+        const double eff = (double)p.nchunks * BH / ((double)waves * kSms * cps);
+        if (eff > best + 1e-9) {
+            best = eff;
+            best_P = P;
+        }
+    }
+    finish_plan(p, best_P);
     return p;
 }
 
@@ -292,14 +324,20 @@ la_status la_causal_fwd(const void* q, const void* k, const void* v, void* o, la
     LA_TRY(check_ws(ws, ws_bytes, w.bytes));
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     float* seg = reinterpret_cast<float*>(static_cast<char*>(ws) + w.seg_states);
+    const size_t seg_bytes = (size_t)s.B * s.H * p.P * state_elems(s.Dk, s.Dv) * sizeof(float);
     if (p.P > 1) {
-        LA_TRY(cuda_status(simt_segment_sums(k, v, seg, s, p, st), "segment sums"));
+        if (p.tc)
+            LA_TRY(cuda_status(tc_causal_fwd(nullptr, k, v, nullptr, seg, s, p, false, st), "segment sums"));
+        else
+            LA_TRY(cuda_status(simt_segment_sums(k, v, seg, s, p, st), "segment sums"));
         LA_TRY(cuda_status(scan_segments(seg, nullptr, s, p, SCAN_EXCLUSIVE_PREFIX, st), "segment scan"));
     } else {
-        LA_TRY(cuda_status(cudaMemsetAsync(seg, 0, (size_t)s.B * s.H * state_elems(s.Dk, s.Dv) * sizeof(float), st),
-                           "state clear"));
+        LA_TRY(cuda_status(cudaMemsetAsync(seg, 0, seg_bytes, st), "state clear"));
     }
-    LA_TRY(cuda_status(simt_causal_fwd_out(q, k, v, o, seg, s, p, st), "causal forward"));
+    if (p.tc)
+        LA_TRY(cuda_status(tc_causal_fwd(q, k, v, o, seg, s, p, true, st), "causal forward"));
+    else
+        LA_TRY(cuda_status(simt_causal_fwd_out(q, k, v, o, seg, s, p, st), "causal forward"));
     return LA_OK;
 }
 
@@ -324,16 +362,29 @@ la_status la_causal_bwd(const void* q, const void* k, const void* v, const void*
     float* segS = reinterpret_cast<float*>(base + w.seg_states);
     float* segR = reinterpret_cast<float*>(base + w.seg_states2);
     float* den_g = reinterpret_cast<float*>(base + w.den_g);
+    const size_t seg_bytes = (size_t)s.B * s.H * p.P * state_elems(s.Dk, s.Dv) * sizeof(float);
     if (p.P > 1) {
-        LA_TRY(cuda_status(simt_segment_sums(k, v, segS, s, p, st), "segment sums"));
+        if (p.tc)
+            LA_TRY(cuda_status(tc_causal_fwd(nullptr, k, v, nullptr, segS, s, p, false, st), "segment sums"));
+        else
+            LA_TRY(cuda_status(simt_segment_sums(k, v, segS, s, p, st), "segment sums"));
         LA_TRY(cuda_status(scan_segments(segS, nullptr, s, p, SCAN_EXCLUSIVE_PREFIX, st), "segment scan"));
     } else {
-        LA_TRY(cuda_status(cudaMemsetAsync(segS, 0, (size_t)s.B * s.H * state_elems(s.Dk, s.Dv) * sizeof(float), st),
-                           "state clear"));
+        LA_TRY(cuda_status(cudaMemsetAsync(segS, 0, seg_bytes, st), "state clear"));
     }
-    LA_TRY(cuda_status(simt_bwd_forward_sweep(q, k, v, dout, dq, segS, segR, den_g, s, p, st), "backward forward sweep"));
-    LA_TRY(cuda_status(scan_segments(segR, nullptr, s, p, SCAN_EXCLUSIVE_SUFFIX, st), "reverse scan"));
-    LA_TRY(cuda_status(simt_bwd_reverse_sweep(q, k, v, dout, dk, dv, segR, den_g, s, p, st), "backward reverse sweep"));
+    if (p.tc) {
+        LA_TRY(cuda_status(tc_bwd_forward_sweep(q, k, v, dout, dq, segS, segR, den_g, s, p, st),
+                           "backward forward sweep"));
+        LA_TRY(cuda_status(scan_segments(segR, nullptr, s, p, SCAN_EXCLUSIVE_SUFFIX, st), "reverse scan"));
+        LA_TRY(cuda_status(tc_bwd_reverse_sweep(q, k, v, dout, dk, dv, segR, den_g, s, p, st),
+                           "backward reverse sweep"));
+    } else {
+        LA_TRY(cuda_status(simt_bwd_forward_sweep(q, k, v, dout, dq, segS, segR, den_g, s, p, st),
+                           "backward forward sweep"));
+        LA_TRY(cuda_status(scan_segments(segR, nullptr, s, p, SCAN_EXCLUSIVE_SUFFIX, st), "reverse scan"));
+        LA_TRY(cuda_status(simt_bwd_reverse_sweep(q, k, v, dout, dk, dv, segR, den_g, s, p, st),
+                           "backward reverse sweep"));
+    }
     return LA_OK;
 }
 

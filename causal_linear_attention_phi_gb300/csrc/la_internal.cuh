@@ -83,6 +83,18 @@ cudaError_t simt_bwd_reverse_sweep(const void* q, const void* k, const void* v, 
 cudaError_t recurrent_step(const void* q, const void* k, const void* v, float* S, float* z, void* out,
                            const la_shape& s, cudaStream_t st);
 
+// Tensor-core (tcgen05) kernels: bf16, Dk = Dv = 128, C = 128.
+// out_pass = false: per-segment sums (S, z) into seg; true: outputs from the scanned prefixes.
+cudaError_t tc_causal_fwd(const void* q, const void* k, const void* v, void* o, float* seg, const la_shape& s,
+                          const Plan& p, bool out_pass, cudaStream_t st);
+cudaError_t tc_bwd_forward_sweep(const void* q, const void* k, const void* v, const void* dout, void* dq,
+                                 const float* seg_S, float* seg_R, float* den_g, const la_shape& s, const Plan& p,
+                                 cudaStream_t st);
+cudaError_t tc_bwd_reverse_sweep(const void* q, const void* k, const void* v, const void* dout, void* dk, void* dv,
+                                 const float* seg_R, const float* den_g, const la_shape& s, const Plan& p,
+                                 cudaStream_t st);
+bool tc_supported(const la_shape& s, int op);
+
 enum ScanMode { SCAN_EXCLUSIVE_PREFIX = 0, SCAN_EXCLUSIVE_SUFFIX = 1, SCAN_TOTAL = 2 };
 
 }  // namespace la

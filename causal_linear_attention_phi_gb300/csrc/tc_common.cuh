@@ -1,0 +1,161 @@
+// tc_common.cuh -- shared pieces of the tcgen05 kernels (bf16, D = 128, C = 128).
+//
+// Tile layout: a 128-row x 128-column bf16 tile is two 64-column blocks of
+// 128 rows x 128 B, each written by TMA with the 128-byte swizzle: inside a
+// block, the 16-byte chunk `lc` of row `row` sits at physical chunk
+// lc ^ (row & 7).  The same physical tile serves as a K-major operand (rows =
+// M or N, contiguous K) and as an MN-major operand (rows = K, contiguous M/N)
+// of tcgen05.mma; see smem_desc_sw128.
+#pragma once
+
+#include "la_internal.cuh"
+#include "sm100.cuh"
+
+namespace la {
+namespace tc {
+using namespace sm100;
+
+constexpr int kC = 128;             // chunk length
+constexpr int kD = 128;             // Dk = Dv
+constexpr int kTileBytes = 32768;   // one 128 x 128 bf16 tile
+constexpr int kBlockBytes = 16384;  // one 64-column block
+
+// K-major operand, K step kk (16 elements): block kk / 4, +32 B inside the 128-B row.
+__device__ __forceinline__ uint64_t desc_kmajor(uint32_t tile, int kk) {
+    return smem_desc_sw128(tile + (kk >> 2) * kBlockBytes + (kk & 3) * 32, 16, 1024);
+}
+// MN-major operand, K step kk (16 rows): +2048 B; the two 64-wide M/N blocks are kBlockBytes apart.
+__device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, int kk) {
+    return smem_desc_sw128(tile + kk * 2048, kBlockBytes, 1024);
+}
+
+// Byte offset of logical 16-byte chunk lc (0..15, 8 columns each) of `row`.
+__device__ __forceinline__ int chunk_off(int row, int lc) {
+    return (lc >> 3) * kBlockBytes + row * 128 + (((lc & 7) ^ (row & 7)) << 4);
+}
+// Byte offset of element (row, col).
+__device__ __forceinline__ int elem_off(int row, int col) { return chunk_off(row, col >> 3) + ((col & 7) << 1); }
+
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ float bf_at(const uint8_t* tile, int row, int col) {
+    const uint16_t h = *reinterpret_cast<const uint16_t*>(tile + elem_off(row, col));
+    return __uint_as_float((uint32_t)h << 16);
+}
+
+// Barrier over the 128-thread compute warpgroup (named barrier 1) that ANDs a
+// predicate across it, so every thread takes the same branch after a bounded wait.
+__device__ __forceinline__ bool wg_all(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, 1, 128, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v)
+        : "memory");
+    return r != 0;
+}
+__device__ __forceinline__ void wg_sync() { named_barrier(1, 128); }
+
+// phi in place on a staged tile, rows >= n set to exactly 0.  Thread t
+// (0..127) handles the 16-byte vectors t + 128 j (block j / 8, row
+// ((t >> 3) + 16 j) & 127); the swizzle only permutes chunks within a row, so
+// an elementwise map ignores it.
+__device__ __forceinline__ void phi_tile(uint8_t* tile, int t, int n) {
+#pragma unroll 4
+    for (int j = 0; j < 16; ++j) {
+        const int row = ((t >> 3) + 16 * j) & 127;
+        uint4* p = reinterpret_cast<uint4*>(tile + (j >> 3) * kBlockBytes + row * 128 + (t & 7) * 16);
+        uint4 w = *p;
+        uint32_t* u = reinterpret_cast<uint32_t*>(&w);
+        const bool valid = row < n;
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            u[e] = valid ? pack_bf16x2(phi_f(bf_lo(u[e])), phi_f(bf_hi(u[e]))) : 0u;
+        *p = w;
+    }
+}
+
+// Row `row` scaled by 1/den[row] in place (rows >= n are left as loaded: zero).
+__device__ __forceinline__ void scale_rows_tile(uint8_t* tile, int t, const float* inv_den) {
+#pragma unroll 4
+    for (int j = 0; j < 16; ++j) {
+        const int row = ((t >> 3) + 16 * j) & 127;
+        uint4* p = reinterpret_cast<uint4*>(tile + (j >> 3) * kBlockBytes + row * 128 + (t & 7) * 16);
+        uint4 w = *p;
+        uint32_t* u = reinterpret_cast<uint32_t*>(&w);
+        const float s = inv_den[row];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) u[e] = pack_bf16x2(bf_lo(u[e]) * s, bf_hi(u[e]) * s);
+        *p = w;
+    }
+}
+
+// Sum over rows 0..n-1 of column `col` of a tile, each row weighted by w[row] (or 1).
+__device__ __forceinline__ float column_sum(const uint8_t* tile, int col, int n, const float* w) {
+    float acc = 0.f;
+    for (int row = 0; row < n; ++row) acc = fmaf(w ? w[row] : 1.f, bf_at(tile, row, col), acc);
+    return acc;
+}
+
+// One TMEM row (32 lanes per warp) of 128 fp32 columns into a bf16 tile row
+// (rows = TMEM lanes), e.g. the fp32 state S -> its bf16 MMA operand copy.
+__device__ __forceinline__ void tmem_row_to_tile(uint32_t taddr, uint8_t* tile, int row) {
+#pragma unroll
+    for (int cb = 0; cb < 4; ++cb) {
+        uint32_t w[32];
+        tmem_ld32(taddr + 32 * cb, w);
+        tmem_ld_wait();
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+            uint4 v4;
+            v4.x = pack_bf16x2(__uint_as_float(w[8 * q4 + 0]), __uint_as_float(w[8 * q4 + 1]));
+            v4.y = pack_bf16x2(__uint_as_float(w[8 * q4 + 2]), __uint_as_float(w[8 * q4 + 3]));
+            v4.z = pack_bf16x2(__uint_as_float(w[8 * q4 + 4]), __uint_as_float(w[8 * q4 + 5]));
+            v4.w = pack_bf16x2(__uint_as_float(w[8 * q4 + 6]), __uint_as_float(w[8 * q4 + 7]));
+            *reinterpret_cast<uint4*>(tile + chunk_off(row, 4 * cb + q4)) = v4;
+        }
+    }
+}
+
+// fp32 row from global memory into TMEM (initial states).
+__device__ __forceinline__ void global_row_to_tmem(const float* src, uint32_t taddr) {
+#pragma unroll
+    for (int cb = 0; cb < 4; ++cb) {
+        uint32_t w[32];
+#pragma unroll
+        for (int x = 0; x < 32; x += 4) {
+            const float4 f = *reinterpret_cast<const float4*>(src + 32 * cb + x);
+            w[x] = __float_as_uint(f.x);
+            w[x + 1] = __float_as_uint(f.y);
+            w[x + 2] = __float_as_uint(f.z);
+            w[x + 3] = __float_as_uint(f.w);
+        }
+        tmem_st32(taddr + 32 * cb, w);
+    }
+    tmem_st_wait();
+}
+
+// fp32 TMEM row to global memory.
+__device__ __forceinline__ void tmem_row_to_global(uint32_t taddr, float* dst) {
+#pragma unroll
+    for (int cb = 0; cb < 4; ++cb) {
+        uint32_t w[32];
+        tmem_ld32(taddr + 32 * cb, w);
+        tmem_ld_wait();
+#pragma unroll
+        for (int x = 0; x < 32; x += 4)
+            *reinterpret_cast<float4*>(dst + 32 * cb + x) = make_float4(
+                __uint_as_float(w[x]), __uint_as_float(w[x + 1]), __uint_as_float(w[x + 2]), __uint_as_float(w[x + 3]));
+    }
+}
+
+}  // namespace tc
+
+// Host: a [BH][N][D] bf16 tensor as a 3-D TMA map with 64 x box_rows x 1 boxes
+// and the 128-byte swizzle; rows past N inside a head read as zeros.
+bool make_tmap_bf16_rows(CUtensorMap* map, const void* ptr, int BH, int N, int D, int box_rows);
+
+}  // namespace la

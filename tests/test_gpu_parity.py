@@ -70,6 +70,12 @@ FWD_CASES = [
     (3, 1, 777, 32, 32, torch.bfloat16),
     (1, 1, 4097, 64, 64, torch.bfloat16),
     (2, 2, 130, 16, 128, torch.bfloat16),
+    # bf16 with Dk = Dv = 128 runs on the tensor-core kernels (chunks of 128)
+    (1, 1, 1, 128, 128, torch.bfloat16),
+    (1, 1, 128, 128, 128, torch.bfloat16),
+    (2, 1, 129, 128, 128, torch.bfloat16),
+    (1, 2, 1000, 128, 128, torch.bfloat16),
+    (1, 3, 4097, 128, 128, torch.bfloat16),
 ]
 
 
@@ -154,9 +160,9 @@ def test_sweep_fwd_bwd_full(la, N):
         check(name, a, b, 2e-2)
 
 
-def _sampled_heads(la, w, heads):
+def _sampled_heads(la, w, heads, tensors=None):
     """Full-size run on the GPU, oracle on a few whole heads (heads are independent)."""
-    q, k, v, dO = W.make_inputs(w, with_grad=True)
+    q, k, v, dO = W.make_inputs(w, with_grad=True) if tensors is None else tensors
     qd, kd, vd, dOd = dev(q, k, v, dO)
     o = la.causal_fwd(qd, kd, vd)
     dq, dk, dv = la.causal_bwd(qd, kd, vd, dOd)
@@ -175,6 +181,23 @@ def test_sweep_65536_sampled_heads(la):
 
 def test_long_bf16_full_size_sampled_heads(la):
     _sampled_heads(la, W.LONG_BF16, [(0, 0), (1, 15)])
+
+
+def test_bf16_d128_many_chunks_and_segments(la):
+    # B*H = 64, N = 20000: 157 chunks of 128 per head, several chunks per segment and
+    # several segments per head, ragged tail (20000 = 156 * 128 + 32)
+    t = W.random_case(77, 4, 16, 20000, 128, 128, dtype=torch.bfloat16, scale=128 ** -0.5, with_grad=True)
+    _sampled_heads(la, None, [(0, 0), (2, 7), (3, 15)], tensors=t)
+
+
+def test_bf16_d128_single_position(la):
+    q, k, v, dO = W.random_case(78, 1, 2, 1, 128, 128, dtype=torch.bfloat16, with_grad=True)
+    qd, kd, vd, dOd = dev(q, k, v, dO)
+    o = la.causal_fwd(qd, kd, vd)
+    assert torch.equal(o.cpu(), v)
+    dq, dk, dv = la.causal_bwd(qd, kd, vd, dOd)
+    assert float(dq.float().abs().max()) < 1e-2 and float(dk.float().abs().max()) < 1e-2
+    assert rel_per_head(dv.cpu(), dO) < 2e-2
 
 
 # ---------------------------------------------------------------- decode
