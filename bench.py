@@ -174,6 +174,10 @@ def run_ours(args):
     la.clear_error()
 
     w = W.LONG_BF16
+    if args.workload == "profile":
+        # same recipe, half the heads and half the length (inputs 0.5 GB, still far above L2)
+        import dataclasses
+        w = dataclasses.replace(w, name="causal fwd+bwd bf16 B=1 H=16 N=32768 Dk=Dv=128", B=1, N=32768)
     B, H, N, Dk, Dv = w.B, w.H, w.N, w.Dk, w.Dv
     q, k, v, dO = W.make_inputs(w, with_grad=True)
     qd, kd, vd, dOd = (t.to(dev) for t in (q, k, v, dO))
@@ -444,6 +448,51 @@ def run_reference(args):
     print(json.dumps(res))
 
 
+def run_sweep(args):
+    """fwd+bwd time and peak device memory per N for the length sweep
+    (bf16, B=1 H=8 D=64, N = 2^9 .. 2^16); one JSON line per N."""
+    import causal_linear_attention_phi_gb300 as la
+    dev = torch.device("cuda", 0)
+    la.build.build_library()
+    for N in W.SWEEP_NS:
+        w = W.sweep(N)
+        q, k, v, dO = W.make_inputs(w, with_grad=True)
+        torch.cuda.empty_cache()
+        torch.cuda.reset_peak_memory_stats(dev)
+        base = torch.cuda.memory_allocated(dev)
+        qd, kd, vd, dOd = (t.to(dev) for t in (q, k, v, dO))
+        o = torch.empty_like(vd)
+        dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+        wsf = torch.empty(la.workspace_bytes(la.OP_CAUSAL_FWD, w.B, w.H, N, w.Dk, w.Dv, w.dtype), dtype=torch.uint8,
+                          device=dev)
+        wsb = torch.empty(la.workspace_bytes(la.OP_CAUSAL_BWD, w.B, w.H, N, w.Dk, w.Dv, w.dtype), dtype=torch.uint8,
+                          device=dev)
+        flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+
+        def step():
+            la.causal_fwd(qd, kd, vd, out=o, workspace=wsf)
+            la.causal_bwd(qd, kd, vd, dOd, dq=dq, dk=dk, dv=dv, workspace=wsb)
+
+        for _ in range(args.warmup):
+            step()
+        times = []
+        for _ in range(args.steps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            step()
+            e1.record()
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1))
+        ms = statistics.median(times)
+        peak = torch.cuda.max_memory_allocated(dev) - base - flush.numel()
+        print(json.dumps({"sweep": "causal fwd+bwd bf16 B=1 H=8 D=64", "N": N, "ms": ms,
+                          "tokens_per_s": w.B * N / (ms / 1e3), "peak_bytes": int(peak),
+                          "workspace_bytes": int(wsf.numel() + wsb.numel()),
+                          "io_bytes": int(8 * w.B * w.H * N * w.Dk * 2), "l2": "flushed between steps"}))
+        del qd, kd, vd, dOd, o, dq, dk, dv, wsf, wsb, flush
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -454,10 +503,15 @@ def main():
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--skip-extras", action="store_true")
+    ap.add_argument("--sweep", action="store_true", help="length sweep N=2^9..2^16 (time, peak memory)")
+    ap.add_argument("--workload", choices=("long", "profile"), default="long",
+                    help="long: B=2 H=16 N=65536 D=128 (the benchmark); profile: B=1 H=16 N=32768 (ncu captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.impl == "reference":
+    if args.sweep:
+        run_sweep(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

@@ -111,13 +111,142 @@ recurrent_step_kernel(const T* __restrict__ q, const T* __restrict__ k, const T*
     }
 }
 
+// Fast path for heads with Dk*Dv <= 64*64: one warp per head, every global
+// load of the step issued before any arithmetic (one memory round trip), S
+// held in registers as float4s.  Lane layout: COLS = Dv/4 lanes across a row,
+// RPI = 32/COLS rows per warp instruction, ROWS = Dk/RPI rows per lane.
+// Launched with programmatic stream serialization: the grid may be scheduled
+// while the previous kernel in the stream drains, and it waits
+// (griddepcontrol.wait) before touching any global memory, so the stream
+// order seen by memory is unchanged.
+template <typename T, int DK, int DV>
+__global__ void __launch_bounds__(32 * kWarpsPerBlock)
+recurrent_step_small_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
+                            float* __restrict__ S, float* __restrict__ z, T* __restrict__ out, int BH) {
+    constexpr int COLS = DV / 4;
+    constexpr int RPI = 32 / COLS;
+    constexpr int ROWS = DK / RPI;
+    constexpr int ZPL = (DK + 31) / 32;  // z entries per lane
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int h = blockIdx.x * kWarpsPerBlock + warp;
+    if (h >= BH) return;
+    const int c4 = lane % COLS, rsub = lane / COLS;
+    const int col = c4 * 4;
+    float* Sh = S + (size_t)h * DK * DV;
+    const T* qh = q + (size_t)h * DK;
+    const T* kh = k + (size_t)h * DK;
+    // ---- all loads first
+    float4 s[ROWS];
+    float kt[ROWS], qt[ROWS];
+#pragma unroll
+    for (int x = 0; x < ROWS; ++x) {
+        const int d = rsub + RPI * x;
+        s[x] = *reinterpret_cast<const float4*>(Sh + (size_t)d * DV + col);
+        kt[x] = to_f32(kh[d]);
+        qt[x] = to_f32(qh[d]);
+    }
+    const float4 vv = load4<T>(v + (size_t)h * DV + col);
+    float zq[ZPL], zk[ZPL], zz[ZPL];
+#pragma unroll
+    for (int y = 0; y < ZPL; ++y) {
+        const int d = lane + 32 * y;
+        const bool in = d < DK;
+        zz[y] = in ? z[(size_t)h * DK + d] : 0.f;
+        zk[y] = in ? to_f32(kh[d]) : 0.f;
+        zq[y] = in ? to_f32(qh[d]) : 0.f;
+    }
+    // ---- z update and phi(q).z
+    float den = 0.f;
+#pragma unroll
+    for (int y = 0; y < ZPL; ++y) {
+        const int d = lane + 32 * y;
+        if (d < DK) {
+            const float zn = zz[y] + phi_f(zk[y]);
+            z[(size_t)h * DK + d] = zn;
+            den = fmaf(phi_f(zq[y]), zn, den);
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+    // ---- S update and phi(q)^T S
+    float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int x = 0; x < ROWS; ++x) {
+        const int d = rsub + RPI * x;
+        const float a = phi_f(kt[x]), b = phi_f(qt[x]);
+        float4 t = s[x];
+        t.x = fmaf(a, vv.x, t.x);
+        t.y = fmaf(a, vv.y, t.y);
+        t.z = fmaf(a, vv.z, t.z);
+        t.w = fmaf(a, vv.w, t.w);
+        *reinterpret_cast<float4*>(Sh + (size_t)d * DV + col) = t;
+        num.x = fmaf(b, t.x, num.x);
+        num.y = fmaf(b, t.y, num.y);
+        num.z = fmaf(b, t.z, num.z);
+        num.w = fmaf(b, t.w, num.w);
+    }
+#pragma unroll
+    for (int o = COLS; o < 32; o <<= 1) {
+        num.x += __shfl_xor_sync(0xffffffffu, num.x, o);
+        num.y += __shfl_xor_sync(0xffffffffu, num.y, o);
+        num.z += __shfl_xor_sync(0xffffffffu, num.z, o);
+        num.w += __shfl_xor_sync(0xffffffffu, num.w, o);
+    }
+    if (rsub == 0) {
+        const float inv = 1.f / den;
+        store4<T>(out + (size_t)h * DV + col, make_float4(num.x * inv, num.y * inv, num.z * inv, num.w * inv));
+    }
+}
+
+template <typename T, int DK, int DV>
+cudaError_t launch_small(const void* q, const void* k, const void* v, float* S, float* z, void* out, int BH,
+                         cudaStream_t st) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((BH + kWarpsPerBlock - 1) / kWarpsPerBlock));
+    cfg.blockDim = dim3(32 * kWarpsPerBlock);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, recurrent_step_small_kernel<T, DK, DV>, (const T*)q, (const T*)k, (const T*)v, S,
+                              z, (T*)out, BH);
+}
+
+template <typename T>
+cudaError_t dispatch_small(const void* q, const void* k, const void* v, float* S, float* z, void* out, int BH,
+                           int Dk, int Dv, cudaStream_t st, bool* handled) {
+    *handled = true;
+#define LA_SMALL(a, b) \
+    if (Dk == a && Dv == b) return launch_small<T, a, b>(q, k, v, S, z, out, BH, st);
+    LA_SMALL(16, 16) LA_SMALL(16, 32) LA_SMALL(16, 64) LA_SMALL(32, 16) LA_SMALL(32, 32) LA_SMALL(32, 64)
+    LA_SMALL(64, 16) LA_SMALL(64, 32) LA_SMALL(64, 64)
+#undef LA_SMALL
+    *handled = false;
+    return cudaSuccess;
+}
+
 }  // namespace
 
 cudaError_t recurrent_step(const void* q, const void* k, const void* v, float* S, float* z, void* out,
                            const la_shape& s, cudaStream_t st) {
     const int BH = s.B * s.H;
-    const unsigned blocks = (unsigned)((BH + kWarpsPerBlock - 1) / kWarpsPerBlock);
+    bool handled = false;
+    cudaError_t e;
     launch_begin("recurrent_step", st);
+    if (s.dtype == LA_BF16)
+        e = dispatch_small<__nv_bfloat16>(q, k, v, S, z, out, BH, s.Dk, s.Dv, st, &handled);
+    else
+        e = dispatch_small<float>(q, k, v, S, z, out, BH, s.Dk, s.Dv, st, &handled);
+    if (handled) {
+        cudaError_t e2 = launch_end("recurrent_step", st);
+        return e != cudaSuccess ? e : e2;
+    }
+    const unsigned blocks = (unsigned)((BH + kWarpsPerBlock - 1) / kWarpsPerBlock);
     if (s.dtype == LA_BF16)
         recurrent_step_kernel<__nv_bfloat16><<<blocks, 32 * kWarpsPerBlock, 0, st>>>(
             (const __nv_bfloat16*)q, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, S, z, (__nv_bfloat16*)out, BH,
