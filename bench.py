@@ -56,6 +56,23 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(x: float) -> float:
+    """Max of a per-rank float over the process group (identity when not distributed).
+    Uses a CUDA tensor under NCCL and a CPU tensor under gloo."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_value(tokens_per_rank_step: int, world: int, ms_per_step_max: float) -> float:
+    """Whole-job throughput: every rank processes its own batch; time is the slowest rank's."""
+    return tokens_per_rank_step * world / (ms_per_step_max / 1e3)
+
+
 def peaks():
     try:
         with open(PEAKS_PATH) as f:
@@ -216,15 +233,10 @@ def run_ours(args):
     barrier()
     la.timing_enable(False)
     ktimes = la.timing_read()
-    ms_total = e0.elapsed_time(e1)
-    if ws_n > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(e0.elapsed_time(e1))
     ms_step = ms_total / args.steps
     tokens_per_step = B * N * ws_n
-    value = tokens_per_step / (ms_step / 1e3)
+    value = weak_scaling_value(B * N, ws_n, ms_step)
     launches = sum(c for c, _ in ktimes.values())
     assert la.last_error() == 0
 
@@ -284,12 +296,7 @@ def run_ours(args):
             e2e_step()
         a1.record(stream)
         torch.cuda.synchronize()
-        e2e_ms = a0.elapsed_time(a1) / e2e_steps
-        if ws_n > 1:
-            import torch.distributed as dist
-            t = torch.tensor([e2e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+        e2e_ms = max_over_ranks(a0.elapsed_time(a1) / e2e_steps)
         result["e2e"] = {"value": tokens_per_step / (e2e_ms / 1e3), "unit": "tokens/s",
                          "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
         del host_in, host_out

@@ -120,6 +120,31 @@ __device__ __forceinline__ void tmem_row_to_tile(uint32_t taddr, uint8_t* tile, 
     }
 }
 
+// The same row as a hi + lo pair of bf16 tiles, hi = bf16(x), lo = bf16(x - hi):
+// a product with (hi + lo) carries the fp32 state to about 2^-17 relative, which
+// the backward needs where two large inter-chunk terms cancel.
+__device__ __forceinline__ void tmem_row_to_tiles_split(uint32_t taddr, uint8_t* hi, uint8_t* lo, int row) {
+#pragma unroll
+    for (int cb = 0; cb < 4; ++cb) {
+        uint32_t w[32];
+        tmem_ld32(taddr + 32 * cb, w);
+        tmem_ld_wait();
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+            uint32_t h4[4], l4[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float x0 = __uint_as_float(w[8 * q4 + 2 * e]), x1 = __uint_as_float(w[8 * q4 + 2 * e + 1]);
+                h4[e] = pack_bf16x2(x0, x1);
+                l4[e] = pack_bf16x2(x0 - bf_lo(h4[e]), x1 - bf_hi(h4[e]));
+            }
+            const int off = chunk_off(row, 4 * cb + q4);
+            *reinterpret_cast<uint4*>(hi + off) = make_uint4(h4[0], h4[1], h4[2], h4[3]);
+            *reinterpret_cast<uint4*>(lo + off) = make_uint4(l4[0], l4[1], l4[2], l4[3]);
+        }
+    }
+}
+
 // fp32 row from global memory into TMEM (initial states).
 __device__ __forceinline__ void global_row_to_tmem(const float* src, uint32_t taddr) {
 #pragma unroll

@@ -16,9 +16,9 @@
 // The same kernel with kOut = false only accumulates the segment's sums
 // (S, z) for the segment scan.
 //
-// Roles (192 threads): warp 0 issues TMA loads, warp 1 owns TMEM and issues
-// tcgen05.mma, warps 2-5 (a warpgroup) transform tiles, mask A, refresh S_prev
-// and write outputs.  Warp w of the warpgroup reads TMEM lanes 32*(w%4)...
+// Roles (320 threads): warp 0 issues TMA loads, warp 1 owns TMEM and issues
+// tcgen05.mma, warps 2-9 (two warpgroups) transform tiles, mask A, refresh
+// S_prev and write outputs.  Warp w reads TMEM lanes 32*(w%4) ..
 // Every wait is bounded: on timeout the kernel records LA_ERR_TIMEOUT in the
 // sticky error word and all roles leave their loops.
 #include <cudaTypedefs.h>
@@ -36,7 +36,7 @@ constexpr int kC = 128;          // chunk length
 constexpr int kD = 128;          // Dk = Dv
 constexpr int kTileBytes = 32768;   // 128 rows x 128 bf16, as two 64-column swizzled blocks
 constexpr int kBlockBytes = 16384;  // one 64-column block (128 rows x 128 B)
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;  // warp 0 TMA, warp 1 MMA, warps 2-9 compute
 
 // TMEM column map (512 columns allocated)
 constexpr uint32_t kTmS = 0, kTmQK = 128, kTmO = 256, kTmA = 384;
@@ -52,62 +52,62 @@ struct __align__(8) Barriers {
 struct SmemLayout {
     // offsets from the 1024-aligned base
     static constexpr int Q = 0;
-    static constexpr int K0 = Q + kTileBytes;
-    static constexpr int K1 = K0 + kTileBytes;
-    static constexpr int V0 = K1 + kTileBytes;
-    static constexpr int V1 = V0 + kTileBytes;
-    static constexpr int Sb = V1 + kTileBytes;
-    static constexpr int zsh = Sb + kTileBytes;       // float[128]: z before the current chunk
-    static constexpr int zchunk = zsh + 512;          // float[128]: this chunk's sum of phi(k)
-    static constexpr int bars = zchunk + 512;
+    static constexpr int K0 = Q + kTileBytes;       // K stages 0, 1
+    static constexpr int V0 = K0 + 2 * kTileBytes;  // V stages 0, 1
+    static constexpr int Sb = V0 + 2 * kTileBytes;
+    static constexpr int zsh = Sb + kTileBytes;     // float[128]
+    static constexpr int zpart = zsh + 512;         // float[2][128]
+    static constexpr int rpart = zpart + 1024;      // float[2][128]
+    static constexpr int dpart = rpart + 1024;      // float[2][128]
+    static constexpr int bars = dpart + 1024;
     static constexpr int tmem_slot = bars + 256;
     static constexpr int total = tmem_slot + 16;
 };
 constexpr size_t kSmemBytes = SmemLayout::total + 1024;  // + alignment slack
 
-__device__ __forceinline__ bool wg_all(bool v) {
-    // barrier over the 128-thread compute warpgroup (id 1) that also ANDs a predicate
+// The compute group is two warpgroups (warps 2-9, 256 threads).  Warp w reads
+// TMEM lanes 32*(w%4) .. +31 (row r of a 128-row tile); warps 2-5 take columns
+// 0-63 of their rows and warps 6-9 columns 64-127, so each row is split
+// between two threads whose partial row reductions meet in shared memory.
+constexpr int kComputeThreads = 256;
+
+__device__ __forceinline__ bool cg_all(bool v) {
+    // barrier over the compute group (named barrier 1) that also ANDs a predicate
     uint32_t r;
     asm volatile(
         "{\n\t.reg .pred p, q;\n\t"
         "setp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.and.pred q, 1, 128, p;\n\t"
+        "bar.red.and.pred q, 1, 256, p;\n\t"
         "selp.u32 %0, 1, 0, q;\n\t}"
         : "=r"(r)
         : "r"((uint32_t)v)
         : "memory");
     return r != 0;
 }
-__device__ __forceinline__ void wg_sync() { named_barrier(1, 128); }
+__device__ __forceinline__ void cg_sync() { named_barrier(1, kComputeThreads); }
 
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-// Apply phi in place to a 128 x 128 bf16 tile (two swizzled 64-column blocks),
-// zeroing rows >= n.  With `zpart`, also accumulate the per-column sums of the
-// rounded phi values.  Thread t (0..127) touches 16-byte vectors t + 128 j:
-// block j / 8, row ((t >> 3) + 16 j) & 127, physical chunk t & 7, whose
-// logical chunk (columns 8*lc .. 8*lc + 7 of the block) is (t & 7) ^ (row & 7).
-template <bool kZ>
-__device__ __forceinline__ void phi_tile(uint8_t* tile, int t, int n, float (&zp)[2][8]) {
+// Byte offset of logical 16-byte chunk lc (0..15) of `row` in a swizzled tile.
+__device__ __forceinline__ int chunk_off(int row, int lc) {
+    return (lc >> 3) * kBlockBytes + row * 128 + (((lc & 7) ^ (row & 7)) << 4);
+}
+
+// phi in place on a staged 128 x 128 bf16 tile, rows >= n set to exactly 0.
+// Compute thread ct (0..255) handles vectors ct + 256 j, j < 8: block j / 4,
+// row ((ct >> 3) + 32 j) & 127, physical chunk ct & 7 (an elementwise map
+// ignores the swizzle, which only permutes chunks within a row).
+__device__ __forceinline__ void phi_tile(uint8_t* tile, int ct, int n) {
 #pragma unroll 4
-    for (int j = 0; j < 16; ++j) {
-        const int blk = j >> 3;
-        const int row = ((t >> 3) + 16 * j) & 127;
-        uint4* p = reinterpret_cast<uint4*>(tile + blk * kBlockBytes + row * 128 + (t & 7) * 16);
+    for (int j = 0; j < 8; ++j) {
+        const int row = ((ct >> 3) + 32 * j) & 127;
+        uint4* p = reinterpret_cast<uint4*>(tile + (j >> 2) * kBlockBytes + row * 128 + (ct & 7) * 16);
         uint4 w = *p;
         uint32_t* u = reinterpret_cast<uint32_t*>(&w);
         const bool valid = row < n;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            float a = valid ? phi_f(bf_lo(u[e])) : 0.f;
-            float b = valid ? phi_f(bf_hi(u[e])) : 0.f;
-            u[e] = pack_bf16x2(a, b);
-            if (kZ) {
-                zp[blk][2 * e] += bf_lo(u[e]);
-                zp[blk][2 * e + 1] += bf_hi(u[e]);
-            }
-        }
+        for (int e = 0; e < 4; ++e) u[e] = valid ? pack_bf16x2(phi_f(bf_lo(u[e])), phi_f(bf_hi(u[e]))) : 0u;
         *p = w;
     }
 }
@@ -120,11 +120,11 @@ tc_causal_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sQ = base + SmemLayout::Q;
-    uint8_t* sK[2] = {base + SmemLayout::K0, base + SmemLayout::K1};
-    uint8_t* sV[2] = {base + SmemLayout::V0, base + SmemLayout::V1};
     uint8_t* sSb = base + SmemLayout::Sb;
-    float* zsh = reinterpret_cast<float*>(base + SmemLayout::zsh);
-    float* zchunk = reinterpret_cast<float*>(base + SmemLayout::zchunk);
+    float* zsh = reinterpret_cast<float*>(base + SmemLayout::zsh);       // [128] z before the chunk
+    float* zpart = reinterpret_cast<float*>(base + SmemLayout::zpart);   // [2][128] this chunk's column sums
+    float* rpart = reinterpret_cast<float*>(base + SmemLayout::rpart);   // [2][128] row partials of A 1
+    float* dpart = reinterpret_cast<float*>(base + SmemLayout::dpart);   // [2][128] row partials of phi(q).z
     Barriers* bar = reinterpret_cast<Barriers*>(base + SmemLayout::bars);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + SmemLayout::tmem_slot);
 
@@ -133,22 +133,13 @@ tc_causal_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     const int cbeg = p * cps, cend = min(nchunks, cbeg + cps), nloc = cend - cbeg;
     const size_t E = state_elems(kD, kD);
     float* segp = seg + ((size_t)bh * P + p) * E;
+    // K and V stage s live at K0 + s * kTileBytes and V0 + s * kTileBytes
+    auto sK = [&](int s) { return base + SmemLayout::K0 + s * kTileBytes; };
+    auto sV = [&](int s) { return base + SmemLayout::V0 + s * kTileBytes; };
 
     if (tid == 0) {
-        mbar_init(&bar->q_full, 1);
-        mbar_init(&bar->q_empty, 1);
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(&bar->kv_full[s], 1);
-            mbar_init(&bar->kv_empty[s], 1);
-        }
-        mbar_init(&bar->qk_ready[0], 1);
-        mbar_init(&bar->qk_ready[1], 1);
-        mbar_init(&bar->sb_ready, 1);
-        mbar_init(&bar->a_ready, 1);
-        mbar_init(&bar->qk_done, 1);
-        mbar_init(&bar->o_done, 1);
-        mbar_init(&bar->s_done, 1);
-        mbar_init(&bar->final_mma, 1);
+        uint64_t* b = reinterpret_cast<uint64_t*>(bar);
+        for (int x = 0; x < (int)(sizeof(Barriers) / 8); ++x) mbar_init(b + x, 1);
         fence_mbar_init();
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
@@ -173,10 +164,10 @@ tc_causal_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                 ok = mbar_wait(&bar->kv_empty[s], ((i >> 1) & 1) ^ 1, err, LA_ERR_TIMEOUT);
                 if (!ok) break;
                 mbar_arrive_expect_tx(&bar->kv_full[s], 2 * kTileBytes);
-                tma_load_3d(sK[s], &tm_k, 0, t0, bh, &bar->kv_full[s]);
-                tma_load_3d(sK[s] + kBlockBytes, &tm_k, 64, t0, bh, &bar->kv_full[s]);
-                tma_load_3d(sV[s], &tm_v, 0, t0, bh, &bar->kv_full[s]);
-                tma_load_3d(sV[s] + kBlockBytes, &tm_v, 64, t0, bh, &bar->kv_full[s]);
+                tma_load_3d(sK(s), &tm_k, 0, t0, bh, &bar->kv_full[s]);
+                tma_load_3d(sK(s) + kBlockBytes, &tm_k, 64, t0, bh, &bar->kv_full[s]);
+                tma_load_3d(sV(s), &tm_v, 0, t0, bh, &bar->kv_full[s]);
+                tma_load_3d(sV(s) + kBlockBytes, &tm_v, 64, t0, bh, &bar->kv_full[s]);
                 armed_kv[s] = i;
                 if (kOut) {
                     ok = mbar_wait(&bar->q_empty, (i & 1) ^ 1, err, LA_ERR_TIMEOUT);
@@ -202,7 +193,7 @@ tc_causal_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             bool ok = true;
             for (int i = 0; i < nloc && ok; ++i) {
                 const int s = i & 1;
-                const uint32_t k_addr = smem_u32(sK[s]), v_addr = smem_u32(sV[s]);
+                const uint32_t k_addr = smem_u32(sK(s)), v_addr = smem_u32(sV(s));
                 if (!(ok = mbar_wait(&bar->qk_ready[s], (i >> 1) & 1, err, LA_ERR_TIMEOUT))) break;
                 tc_fence_after();
                 if (kOut) {
@@ -244,173 +235,158 @@ tc_causal_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             mbar_wait(&bar->final_mma, 0, err, LA_ERR_TIMEOUT);
         }
     } else {
-        // ------------------------------------------------------------ compute warpgroup
-        const int t = tid - 64;                       // 0..127
-        const int r = 32 * (warp & 3) + lane;         // TMEM lane / tile row owned by this thread
+        // ------------------------------------------------------------ compute group (256 threads)
+        const int ct = tid - 64;                       // 0..255
+        const int h = (warp - 2) >> 2;                 // column half of the rows this thread serves
+        const int r = 32 * (warp & 3) + lane;          // TMEM lane / tile row
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-        // initial state: S_prev from the scanned segment prefix (kOut), z likewise
+        const int zc = ct & 127, zh = ct >> 7;         // column-sum assignment: column zc, rows of half zh
+        if (ct < 128) zsh[ct] = kOut ? segp[(size_t)kD * kD + ct] : 0.f;
         if (kOut) {
-            const float* pre = segp + (size_t)r * kD;
+            // S_prev from the scanned segment prefix: row r, this thread's 64 columns
+            const float* pre = segp + (size_t)r * kD + 64 * h;
 #pragma unroll
-            for (int cb = 0; cb < 4; ++cb) {
+            for (int cb = 0; cb < 2; ++cb) {
                 uint32_t w[32];
 #pragma unroll
                 for (int x = 0; x < 32; ++x) w[x] = __float_as_uint(pre[32 * cb + x]);
-                tmem_st32(tmem + lane_base + kTmS + 32 * cb, w);
+                tmem_st32(tmem + lane_base + kTmS + 64 * h + 32 * cb, w);
             }
             tmem_st_wait();
-            zsh[r] = segp[(size_t)kD * kD + r];
-        } else {
-            zsh[r] = 0.f;
         }
-        zchunk[r] = 0.f;
         tc_fence_before();
-        bool ok = wg_all(true);
+        bool ok = cg_all(true);
         for (int i = 0; i < nloc && ok; ++i) {
             const int s = i & 1;
             const int c0 = (cbeg + i) * kC, n = min(kC, N - c0);
-            // (a) phi on the K (and Q) tiles, z partial sums
-            ok = mbar_wait(&bar->kv_full[s], (i >> 1) & 1, err, LA_ERR_TIMEOUT);
-            if (kOut) ok = ok && mbar_wait(&bar->q_full, i & 1, err, LA_ERR_TIMEOUT);
-            if (!wg_all(ok)) { ok = false; break; }
-            float zp[2][8];
-#pragma unroll
-            for (int b = 0; b < 2; ++b)
-#pragma unroll
-                for (int e = 0; e < 8; ++e) zp[b][e] = 0.f;
-            phi_tile<true>(sK[s], t, n, zp);
-            {
-                const int lc = (t & 7) ^ ((t >> 3) & 7);
-#pragma unroll
-                for (int b = 0; b < 2; ++b)
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) atomicAdd(&zchunk[64 * b + 8 * lc + e], zp[b][e]);
-            }
-            float den_inter = 0.f;
-            if (kOut) {
-                float dummy[2][8];
-                phi_tile<false>(sQ, t, kC, dummy);
-            }
+            uint8_t* kt = sK(s);
+            // (a) phi on the K (and Q) tiles
+            bool w = mbar_wait(&bar->kv_full[s], (i >> 1) & 1, err, LA_ERR_TIMEOUT);
+            if (kOut) w = w && mbar_wait(&bar->q_full, i & 1, err, LA_ERR_TIMEOUT);
+            if (!cg_all(w)) { ok = false; break; }
+            phi_tile(kt, ct, n);
+            if (kOut) phi_tile(sQ, ct, n);
             fence_proxy_async_smem();
-            wg_sync();
-            if (t == 0) mbar_arrive(&bar->qk_ready[s]);
+            cg_sync();
+            if (ct == 0) mbar_arrive(&bar->qk_ready[s]);
+            {
+                // this chunk's column sums of phi(K), rows [64 zh, 64 zh + 64) of column zc
+                float acc = 0.f;
+                const int rend = min(64 * zh + 64, n);
+                for (int row = 64 * zh; row < rend; ++row) {
+                    const uint16_t hv =
+                        *reinterpret_cast<const uint16_t*>(kt + chunk_off(row, zc >> 3) + ((zc & 7) << 1));
+                    acc += __uint_as_float((uint32_t)hv << 16);
+                }
+                zpart[zh * 128 + zc] = acc;
+            }
             if (kOut) {
-                // den_inter = phi(q_r) . z_prev from this thread's Q row
+                // den partial: phi(q_r) . z_prev over this thread's 64 columns
+                float di = 0.f;
 #pragma unroll
-                for (int b = 0; b < 2; ++b)
+                for (int lc8 = 0; lc8 < 8; ++lc8) {
+                    const int lc = 8 * h + lc8;
+                    const uint4 qv = *reinterpret_cast<const uint4*>(sQ + chunk_off(r, lc));
+                    const uint32_t* u = reinterpret_cast<const uint32_t*>(&qv);
+                    const float* zz = zsh + 8 * lc;
 #pragma unroll
-                    for (int lc = 0; lc < 8; ++lc) {
-                        const uint4 w = *reinterpret_cast<const uint4*>(sQ + b * kBlockBytes + r * 128 +
-                                                                        ((lc ^ (r & 7)) * 16));
-                        const uint32_t* u = reinterpret_cast<const uint32_t*>(&w);
-                        const float* zz = zsh + 64 * b + 8 * lc;
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            den_inter += bf_lo(u[e]) * zz[2 * e] + bf_hi(u[e]) * zz[2 * e + 1];
-                    }
-                // (b) S_prev -> bf16 B operand (MN-major: row = dk = r, 64-wide dv blocks)
+                    for (int e = 0; e < 4; ++e) di += bf_lo(u[e]) * zz[2 * e] + bf_hi(u[e]) * zz[2 * e + 1];
+                }
+                dpart[h * 128 + r] = di;
+                // (b) S_prev -> bf16 B operand (row = dk = r, this thread's 64 dv columns = block h)
                 if (i > 0) {
-                    ok = mbar_wait(&bar->s_done, (i - 1) & 1, err, LA_ERR_TIMEOUT);
-                    if (!wg_all(ok)) { ok = false; break; }
+                    if (!cg_all(mbar_wait(&bar->s_done, (i - 1) & 1, err, LA_ERR_TIMEOUT))) { ok = false; break; }
                     tc_fence_after();
                 }
 #pragma unroll
-                for (int cb = 0; cb < 4; ++cb) {
-                    uint32_t w[32];
-                    tmem_ld32(tmem + lane_base + kTmS + 32 * cb, w);
+                for (int cb = 0; cb < 2; ++cb) {
+                    uint32_t wv[32];
+                    tmem_ld32(tmem + lane_base + kTmS + 64 * h + 32 * cb, wv);
                     tmem_ld_wait();
-                    // columns 32cb .. 32cb+31 = dv; block cb/2, logical chunks 4*(cb&1) .. +3
 #pragma unroll
                     for (int q4 = 0; q4 < 4; ++q4) {
-                        const int lc = 4 * (cb & 1) + q4;
                         uint4 v4;
-                        v4.x = pack_bf16x2(__uint_as_float(w[8 * q4 + 0]), __uint_as_float(w[8 * q4 + 1]));
-                        v4.y = pack_bf16x2(__uint_as_float(w[8 * q4 + 2]), __uint_as_float(w[8 * q4 + 3]));
-                        v4.z = pack_bf16x2(__uint_as_float(w[8 * q4 + 4]), __uint_as_float(w[8 * q4 + 5]));
-                        v4.w = pack_bf16x2(__uint_as_float(w[8 * q4 + 6]), __uint_as_float(w[8 * q4 + 7]));
-                        *reinterpret_cast<uint4*>(sSb + (cb >> 1) * kBlockBytes + r * 128 + ((lc ^ (r & 7)) * 16)) =
-                            v4;
+                        v4.x = pack_bf16x2(__uint_as_float(wv[8 * q4 + 0]), __uint_as_float(wv[8 * q4 + 1]));
+                        v4.y = pack_bf16x2(__uint_as_float(wv[8 * q4 + 2]), __uint_as_float(wv[8 * q4 + 3]));
+                        v4.z = pack_bf16x2(__uint_as_float(wv[8 * q4 + 4]), __uint_as_float(wv[8 * q4 + 5]));
+                        v4.w = pack_bf16x2(__uint_as_float(wv[8 * q4 + 6]), __uint_as_float(wv[8 * q4 + 7]));
+                        *reinterpret_cast<uint4*>(sSb + chunk_off(r, 8 * h + 4 * cb + q4)) = v4;
                     }
                 }
                 tc_fence_before();
                 fence_proxy_async_smem();
-                wg_sync();
-                if (t == 0) mbar_arrive(&bar->sb_ready);
-                // (c) A = tril(QK) -> bf16 into TMEM; row sums for den
-                ok = mbar_wait(&bar->qk_done, i & 1, err, LA_ERR_TIMEOUT);
-                if (!wg_all(ok)) { ok = false; break; }
+                cg_sync();
+                if (ct == 0) mbar_arrive(&bar->sb_ready);
+                // (c) A = tril(QK^T) on keys [64 h, 64 h + 64) -> bf16 pairs into TMEM; row-sum partial
+                if (!cg_all(mbar_wait(&bar->qk_done, i & 1, err, LA_ERR_TIMEOUT))) { ok = false; break; }
                 tc_fence_after();
                 float rs = 0.f;
 #pragma unroll
-                for (int cb = 0; cb < 4; ++cb) {
-                    uint32_t w[32];
-                    tmem_ld32(tmem + lane_base + kTmQK + 32 * cb, w);
+                for (int cb = 0; cb < 2; ++cb) {
+                    uint32_t wv[32], pk[16];
+                    tmem_ld32(tmem + lane_base + kTmQK + 64 * h + 32 * cb, wv);
                     tmem_ld_wait();
-                    uint32_t pk[16];
 #pragma unroll
                     for (int x = 0; x < 16; ++x) {
-                        const int j0 = 32 * cb + 2 * x;
-                        const float a0 = (j0 <= r) ? __uint_as_float(w[2 * x]) : 0.f;
-                        const float a1 = (j0 + 1 <= r) ? __uint_as_float(w[2 * x + 1]) : 0.f;
-                        pk[x] = pack_bf16x2(a0, a1);
+                        const int j0 = 64 * h + 32 * cb + 2 * x;
+                        pk[x] = pack_bf16x2(j0 <= r ? __uint_as_float(wv[2 * x]) : 0.f,
+                                            j0 + 1 <= r ? __uint_as_float(wv[2 * x + 1]) : 0.f);
                         rs += bf_lo(pk[x]) + bf_hi(pk[x]);
                     }
-                    tmem_st16(tmem + lane_base + kTmA + 16 * cb, pk);
+                    tmem_st16(tmem + lane_base + kTmA + 32 * h + 16 * cb, pk);
                 }
+                rpart[h * 128 + r] = rs;
                 tmem_st_wait();
                 tc_fence_before();
-                wg_sync();
-                if (t == 0) mbar_arrive(&bar->a_ready);
-                // (d) o = O / den
-                ok = mbar_wait(&bar->o_done, i & 1, err, LA_ERR_TIMEOUT);
-                if (!wg_all(ok)) { ok = false; break; }
+                cg_sync();
+                if (ct == 0) mbar_arrive(&bar->a_ready);
+                // (d) o = O / den on this thread's 64 columns
+                if (!cg_all(mbar_wait(&bar->o_done, i & 1, err, LA_ERR_TIMEOUT))) { ok = false; break; }
                 tc_fence_after();
-                const float inv = 1.f / (rs + den_inter);
-                __nv_bfloat16* orow = o + ((size_t)bh * N + c0 + r) * kD;
+                const float inv = 1.f / (rpart[r] + rpart[128 + r] + dpart[r] + dpart[128 + r]);
+                __nv_bfloat16* orow = o + ((size_t)bh * N + c0 + r) * kD + 64 * h;
 #pragma unroll
-                for (int cb = 0; cb < 4; ++cb) {
-                    uint32_t w[32];
-                    tmem_ld32(tmem + lane_base + kTmO + 32 * cb, w);
+                for (int cb = 0; cb < 2; ++cb) {
+                    uint32_t wv[32];
+                    tmem_ld32(tmem + lane_base + kTmO + 64 * h + 32 * cb, wv);
                     tmem_ld_wait();
                     if (r < n) {
 #pragma unroll
                         for (int q4 = 0; q4 < 4; ++q4) {
                             uint4 v4;
-                            v4.x = pack_bf16x2(__uint_as_float(w[8 * q4 + 0]) * inv, __uint_as_float(w[8 * q4 + 1]) * inv);
-                            v4.y = pack_bf16x2(__uint_as_float(w[8 * q4 + 2]) * inv, __uint_as_float(w[8 * q4 + 3]) * inv);
-                            v4.z = pack_bf16x2(__uint_as_float(w[8 * q4 + 4]) * inv, __uint_as_float(w[8 * q4 + 5]) * inv);
-                            v4.w = pack_bf16x2(__uint_as_float(w[8 * q4 + 6]) * inv, __uint_as_float(w[8 * q4 + 7]) * inv);
+                            v4.x = pack_bf16x2(__uint_as_float(wv[8 * q4 + 0]) * inv, __uint_as_float(wv[8 * q4 + 1]) * inv);
+                            v4.y = pack_bf16x2(__uint_as_float(wv[8 * q4 + 2]) * inv, __uint_as_float(wv[8 * q4 + 3]) * inv);
+                            v4.z = pack_bf16x2(__uint_as_float(wv[8 * q4 + 4]) * inv, __uint_as_float(wv[8 * q4 + 5]) * inv);
+                            v4.w = pack_bf16x2(__uint_as_float(wv[8 * q4 + 6]) * inv, __uint_as_float(wv[8 * q4 + 7]) * inv);
                             *reinterpret_cast<uint4*>(orow + 32 * cb + 8 * q4) = v4;
                         }
                     }
                 }
                 tc_fence_before();
             }
-            // z_prev += this chunk's sums (after every thread has used z_prev)
-            wg_sync();
-            zsh[r] += zchunk[r];
-            zchunk[r] = 0.f;
-            wg_sync();
+            // z_prev += this chunk's column sums (after every thread has used z_prev)
+            cg_sync();
+            if (ct < 128) zsh[ct] += zpart[ct] + zpart[128 + ct];
+            cg_sync();
         }
         if (!kOut && ok && nloc > 0) {
-            // segment sums out: S from TMEM (row r = dk), z from shared memory.  The
-            // MMA thread's single-use drain barrier marks the last S update done.
-            ok = mbar_wait(&bar->final_mma, 0, err, LA_ERR_TIMEOUT);
-            if (wg_all(ok)) {
+            // segment sums out: S from TMEM (row r = dk, this thread's 64 columns), z from shared memory.
+            // The MMA thread's single-use drain barrier marks the last S update done.
+            if (cg_all(mbar_wait(&bar->final_mma, 0, err, LA_ERR_TIMEOUT))) {
                 tc_fence_after();
-                float* out = segp + (size_t)r * kD;
+                float* out = segp + (size_t)r * kD + 64 * h;
 #pragma unroll
-                for (int cb = 0; cb < 4; ++cb) {
-                    uint32_t w[32];
-                    tmem_ld32(tmem + lane_base + kTmS + 32 * cb, w);
+                for (int cb = 0; cb < 2; ++cb) {
+                    uint32_t wv[32];
+                    tmem_ld32(tmem + lane_base + kTmS + 64 * h + 32 * cb, wv);
                     tmem_ld_wait();
 #pragma unroll
                     for (int x = 0; x < 32; x += 4)
                         *reinterpret_cast<float4*>(out + 32 * cb + x) =
-                            make_float4(__uint_as_float(w[x]), __uint_as_float(w[x + 1]), __uint_as_float(w[x + 2]),
-                                        __uint_as_float(w[x + 3]));
+                            make_float4(__uint_as_float(wv[x]), __uint_as_float(wv[x + 1]),
+                                        __uint_as_float(wv[x + 2]), __uint_as_float(wv[x + 3]));
                 }
-                segp[(size_t)kD * kD + r] = zsh[r];
+                if (ct < 128) segp[(size_t)kD * kD + ct] = zsh[ct];
             }
         }
         tc_fence_before();
