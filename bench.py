@@ -459,14 +459,15 @@ def run_sweep(args):
     """fwd+bwd time and peak device memory per N for the length sweep
     (bf16, B=1 H=8 D=64, N = 2^9 .. 2^16); one JSON line per N."""
     import causal_linear_attention_phi_gb300 as la
+    torch.cuda.set_device(0)
     dev = torch.device("cuda", 0)
     la.build.build_library()
     for N in W.SWEEP_NS:
         w = W.sweep(N)
         q, k, v, dO = W.make_inputs(w, with_grad=True)
         torch.cuda.empty_cache()
-        torch.cuda.reset_peak_memory_stats(dev)
-        base = torch.cuda.memory_allocated(dev)
+        torch.cuda.reset_peak_memory_stats()
+        base = torch.cuda.memory_allocated()
         qd, kd, vd, dOd = (t.to(dev) for t in (q, k, v, dO))
         o = torch.empty_like(vd)
         dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
@@ -492,7 +493,7 @@ def run_sweep(args):
             torch.cuda.synchronize()
             times.append(e0.elapsed_time(e1))
         ms = statistics.median(times)
-        peak = torch.cuda.max_memory_allocated(dev) - base - flush.numel()
+        peak = torch.cuda.max_memory_allocated() - base - flush.numel()
         print(json.dumps({"sweep": "causal fwd+bwd bf16 B=1 H=8 D=64", "N": N, "ms": ms,
                           "tokens_per_s": w.B * N / (ms / 1e3), "peak_bytes": int(peak),
                           "workspace_bytes": int(wsf.numel() + wsb.numel()),

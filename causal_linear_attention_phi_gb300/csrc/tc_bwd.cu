@@ -43,7 +43,7 @@ struct FwdSweepBars {
 
 struct FwdSweepSmem {
     static constexpr int Q = 0, K = kTileBytes, V = 2 * kTileBytes, P = 3 * kTileBytes, Sb = 4 * kTileBytes;
-    static constexpr int SbLo = 5 * kTileBytes;  // low bf16 half of S_prev
+    static constexpr int KLo = 5 * kTileBytes;   // low bf16 half of phi(K) (hi is the K tile)
     static constexpr int zsh = 6 * kTileBytes;   // float[128] z_prev
     static constexpr int rsh = zsh + 512;        // float[128] segment sum of g phi(q)
     static constexpr int gsh = rsh + 512;        // float[128] g of the chunk's rows
@@ -65,7 +65,7 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
     uint8_t* sV = base + FwdSweepSmem::V;
     uint8_t* sP = base + FwdSweepSmem::P;
     uint8_t* sSb = base + FwdSweepSmem::Sb;
-    uint8_t* sSbLo = base + FwdSweepSmem::SbLo;
+    uint8_t* sKLo = base + FwdSweepSmem::KLo;
     float* zsh = reinterpret_cast<float*>(base + FwdSweepSmem::zsh);
     float* rsh = reinterpret_cast<float*>(base + FwdSweepSmem::rsh);
     float* gsh = reinterpret_cast<float*>(base + FwdSweepSmem::gsh);
@@ -120,7 +120,7 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
             constexpr uint32_t id_kmn = idesc_bf16_f32(128, 128, 0, 1);
             constexpr uint32_t id_mnmn = idesc_bf16_f32(128, 128, 1, 1);
             const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV), aP = smem_u32(sP),
-                           aSb = smem_u32(sSb), aSbLo = smem_u32(sSbLo);
+                           aSb = smem_u32(sSb), aKLo = smem_u32(sKLo);
             for (int i = 0; i < nloc; ++i) {
                 const uint32_t ph = i & 1;
                 if (!mbar_wait(&bar->qk_ready, ph, err, LA_ERR_TIMEOUT)) break;
@@ -132,11 +132,8 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
                 if (!mbar_wait(&bar->sb_ready, ph, err, LA_ERR_TIMEOUT)) break;
                 tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)  // Y = Q~ S_prev (hi + lo)
+                for (int kk = 0; kk < 8; ++kk)  // Y = Q~ S_prev
                     mma_ss(tmem + kFY, desc_kmajor(aQ, kk), desc_mnmajor(aSb, kk), id_kmn, kk > 0);
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_ss(tmem + kFY, desc_kmajor(aQ, kk), desc_mnmajor(aSbLo, kk), id_kmn, 1);
                 if (!mbar_wait(&bar->a_ready, ph, err, LA_ERR_TIMEOUT)) break;
                 tc_fence_after();
 #pragma unroll
@@ -159,17 +156,17 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
                 if (!mbar_wait(&bar->d_ready, ph, err, LA_ERR_TIMEOUT)) break;
                 tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)  // Y = P S_prev^T (hi + lo)
+                for (int kk = 0; kk < 8; ++kk)  // Y = P S_prev^T
                     mma_ss(tmem + kFY, desc_kmajor(aP, kk), desc_kmajor(aSb, kk), id_kk, kk > 0);
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_ss(tmem + kFY, desc_kmajor(aP, kk), desc_kmajor(aSbLo, kk), id_kk, 1);
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)  // Y += D K~ (hi + lo)
+                for (int kk = 0; kk < 8; ++kk)  // Y += D K~ as D_hi K_hi + D_lo K_hi + D_hi K_lo
                     mma_ts(tmem + kFY, tmem + kFX + 8 * kk, desc_mnmajor(aK, kk), id_kmn, 1);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
                     mma_ts(tmem + kFY, tmem + kFX + 64 + 8 * kk, desc_mnmajor(aK, kk), id_kmn, 1);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_ts(tmem + kFY, tmem + kFX + 8 * kk, desc_mnmajor(aKLo, kk), id_kmn, 1);
                 mma_commit(&bar->dq_done);
             }
             mma_commit(&bar->final_mma);
@@ -191,7 +188,7 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
             const int c0 = (cbeg + i) * kC, n = min(kC, N - c0);
             // (a) phi on the Q and K tiles; this chunk's column sums of phi(K); den_inter
             if (!wg_all(mbar_wait(&bar->full, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
-            phi_tile(sK, t, n);
+            phi_tile_split(sK, sKLo, t, n);
             phi_tile(sQ, t, n);
             fence_proxy_async_smem();
             wg_sync();
@@ -213,7 +210,7 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
                 if (!wg_all(w1 && w2)) { ok = false; break; }
                 tc_fence_after();
             }
-            tmem_row_to_tiles_split(tmem + lb + kFS, sSb, sSbLo, r);
+            tmem_row_to_tile(tmem + lb + kFS, sSb, r);
             tc_fence_before();
             fence_proxy_async_smem();
             wg_sync();
@@ -367,25 +364,23 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
 }
 
 // ------------------------------------------------------------------ reverse sweep
-// TMEM: R [0,128) fp32 reverse state R_next; ACC [128,256) first holds D^T fp32,
-// then the dK~ accumulator, then the dV accumulator; AT [256,384) holds A^T
-// fp32, converted in place to bf16 in AT[0,64); X [384,512) holds D^T as a bf16
-// hi / lo pair in X[0,64) / X[64,128).
-constexpr uint32_t kRR = 0, kRACC = 128, kRAT = 256, kRX = 384;
+// TMEM: R [0,128) fp32 reverse state R_next; DK [128,256) and DV [256,384)
+// accumulators (they first hold D^T and A^T in fp32); X [384,512): D^T bf16 in
+// X[0,64), A^T bf16 in X[64,128).
+constexpr uint32_t kRR = 0, kRDK = 128, kRDV = 256, kRX = 384;
 
 struct RevSweepBars {
     uint64_t full, empty;
-    uint64_t ready, rb_ready, masks_ready, dk_read;
-    uint64_t at_dt_done, dk_done, dv_done, chunk_done;
+    uint64_t ready, rb_ready, masks_ready;
+    uint64_t at_done, dt_done, dkv_done;
     uint64_t final_mma;
 };
 
 struct RevSweepSmem {
     static constexpr int Q = 0, K = kTileBytes, V = 2 * kTileBytes, P = 3 * kTileBytes, Rb = 4 * kTileBytes;
-    static constexpr int RbLo = 5 * kTileBytes;  // low bf16 half of R_next
-    static constexpr int rsh = 6 * kTileBytes;   // float[128] r_next
-    static constexpr int gsh = rsh + 512;        // float[128] g of the chunk's rows
-    static constexpr int ish = gsh + 512;        // float[128] 1/den of the chunk's rows
+    static constexpr int rsh = 5 * kTileBytes;  // float[128] r_next
+    static constexpr int gsh = rsh + 512;       // float[128] g of the chunk's rows
+    static constexpr int ish = gsh + 512;       // float[128] 1/den of the chunk's rows
     static constexpr int bars = ish + 512;
     static constexpr int tmem_slot = bars + 256;
     static constexpr int total = tmem_slot + 16;
@@ -404,7 +399,6 @@ tc_bwd_reverse_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
     uint8_t* sV = base + RevSweepSmem::V;
     uint8_t* sP = base + RevSweepSmem::P;
     uint8_t* sRb = base + RevSweepSmem::Rb;
-    uint8_t* sRbLo = base + RevSweepSmem::RbLo;
     float* rsh = reinterpret_cast<float*>(base + RevSweepSmem::rsh);
     float* gsh = reinterpret_cast<float*>(base + RevSweepSmem::gsh);
     float* ish = reinterpret_cast<float*>(base + RevSweepSmem::ish);
@@ -459,51 +453,38 @@ tc_bwd_reverse_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
             constexpr uint32_t id_kmn = idesc_bf16_f32(128, 128, 0, 1);
             constexpr uint32_t id_mnmn = idesc_bf16_f32(128, 128, 1, 1);
             const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV), aP = smem_u32(sP),
-                           aRb = smem_u32(sRb), aRbLo = smem_u32(sRbLo);
+                           aRb = smem_u32(sRb);
             for (int i = 0; i < nloc; ++i) {
                 const uint32_t ph = i & 1;
                 if (!mbar_wait(&bar->ready, ph, err, LA_ERR_TIMEOUT)) break;
                 tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)  // AT = A^T = K~ Q~^T (rows = keys)
-                    mma_ss(tmem + kRAT, desc_kmajor(aK, kk), desc_kmajor(aQ, kk), id_kk, kk > 0);
+                for (int kk = 0; kk < 8; ++kk)  // DV region = A^T = K~ Q~^T (rows = keys)
+                    mma_ss(tmem + kRDV, desc_kmajor(aK, kk), desc_kmajor(aQ, kk), id_kk, kk > 0);
+                mma_commit(&bar->at_done);
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)  // ACC = V P^T (rows = keys)
-                    mma_ss(tmem + kRACC, desc_kmajor(aV, kk), desc_kmajor(aP, kk), id_kk, kk > 0);
-                mma_commit(&bar->at_dt_done);
+                for (int kk = 0; kk < 8; ++kk)  // DK region = V P^T (rows = keys)
+                    mma_ss(tmem + kRDK, desc_kmajor(aV, kk), desc_kmajor(aP, kk), id_kk, kk > 0);
+                mma_commit(&bar->dt_done);
                 if (!mbar_wait(&bar->rb_ready, ph, err, LA_ERR_TIMEOUT)) break;
                 if (!mbar_wait(&bar->masks_ready, ph, err, LA_ERR_TIMEOUT)) break;
                 tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)  // dK~ = V R_next^T (hi + lo)
-                    mma_ss(tmem + kRACC, desc_kmajor(aV, kk), desc_kmajor(aRb, kk), id_kk, kk > 0);
+                for (int kk = 0; kk < 8; ++kk)  // dK~ = V R_next^T
+                    mma_ss(tmem + kRDK, desc_kmajor(aV, kk), desc_kmajor(aRb, kk), id_kk, kk > 0);
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_ss(tmem + kRACC, desc_kmajor(aV, kk), desc_kmajor(aRbLo, kk), id_kk, 1);
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)  // dK~ += D^T Q~ (hi + lo)
-                    mma_ts(tmem + kRACC, tmem + kRX + 8 * kk, desc_mnmajor(aQ, kk), id_kmn, 1);
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_ts(tmem + kRACC, tmem + kRX + 64 + 8 * kk, desc_mnmajor(aQ, kk), id_kmn, 1);
-                mma_commit(&bar->dk_done);
-                if (!mbar_wait(&bar->dk_read, ph, err, LA_ERR_TIMEOUT)) break;
-                tc_fence_after();
+                for (int kk = 0; kk < 8; ++kk)  // dK~ += D^T Q~
+                    mma_ts(tmem + kRDK, tmem + kRX + 8 * kk, desc_mnmajor(aQ, kk), id_kmn, 1);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)  // dV = K~ R_next
-                    mma_ss(tmem + kRACC, desc_kmajor(aK, kk), desc_mnmajor(aRb, kk), id_kmn, kk > 0);
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_ss(tmem + kRACC, desc_kmajor(aK, kk), desc_mnmajor(aRbLo, kk), id_kmn, 1);
+                    mma_ss(tmem + kRDV, desc_kmajor(aK, kk), desc_mnmajor(aRb, kk), id_kmn, kk > 0);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)  // dV += A^T P
-                    mma_ts(tmem + kRACC, tmem + kRAT + 8 * kk, desc_mnmajor(aP, kk), id_kmn, 1);
-                mma_commit(&bar->dv_done);
+                    mma_ts(tmem + kRDV, tmem + kRX + 64 + 8 * kk, desc_mnmajor(aP, kk), id_kmn, 1);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)  // R_next += Q~^T P
                     mma_ss(tmem + kRR, desc_mnmajor(aQ, kk), desc_mnmajor(aP, kk), id_mnmn, 1);
-                mma_commit(&bar->chunk_done);
-                mma_commit(&bar->empty);  // the tiles are free once every product of the chunk is done
+                mma_commit(&bar->dkv_done);
             }
             mma_commit(&bar->final_mma);
             mbar_wait(&bar->final_mma, 0, err, LA_ERR_TIMEOUT);
@@ -536,23 +517,23 @@ tc_bwd_reverse_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
             wg_sync();
             if (t == 0) mbar_arrive(&bar->ready);
             const float rc = column_sum(sQ, t, n, gsh);  // this chunk's sum of g phi(q), column t
-            // (b) R_next -> bf16 hi / lo copies (rows = dk)
+            // (b) R_next -> bf16 copy (rows = dk)
             if (i > 0) {
-                if (!wg_all(mbar_wait(&bar->chunk_done, (i - 1) & 1, err, LA_ERR_TIMEOUT))) { ok = false; break; }
+                if (!wg_all(mbar_wait(&bar->dkv_done, (i - 1) & 1, err, LA_ERR_TIMEOUT))) { ok = false; break; }
                 tc_fence_after();
             }
-            tmem_row_to_tiles_split(tmem + lb + kRR, sRb, sRbLo, r);
+            tmem_row_to_tile(tmem + lb + kRR, sRb, r);
             tc_fence_before();
             fence_proxy_async_smem();
             wg_sync();
             if (t == 0) mbar_arrive(&bar->rb_ready);
-            // (c) masks: row r is key j = r, column x is query i = x; keep j <= i
-            if (!wg_all(mbar_wait(&bar->at_dt_done, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
+            // (c) masks: row r is key j = r; column x is query i = x; keep j <= i
+            if (!wg_all(mbar_wait(&bar->at_done, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
             tc_fence_after();
 #pragma unroll
-            for (int cb = 0; cb < 4; ++cb) {  // A^T -> bf16 in place (block cb writes columns 16cb.., already read)
+            for (int cb = 0; cb < 4; ++cb) {
                 uint32_t w[32], pk[16];
-                tmem_ld32(tmem + lb + kRAT + 32 * cb, w);
+                tmem_ld32(tmem + lb + kRDV + 32 * cb, w);
                 tmem_ld_wait();
 #pragma unroll
                 for (int x = 0; x < 16; ++x) {
@@ -560,30 +541,29 @@ tc_bwd_reverse_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
                     pk[x] = pack_bf16x2(r <= qi ? __uint_as_float(w[2 * x]) : 0.f,
                                         r <= qi + 1 ? __uint_as_float(w[2 * x + 1]) : 0.f);
                 }
-                tmem_st16(tmem + lb + kRAT + 16 * cb, pk);
+                tmem_st16(tmem + lb + kRX + 64 + 16 * cb, pk);
             }
+            if (!wg_all(mbar_wait(&bar->dt_done, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
+            tc_fence_after();
 #pragma unroll
-            for (int cb = 0; cb < 4; ++cb) {  // D^T = V P^T + g, masked -> bf16 hi / lo into X
-                uint32_t w[32], hi[16], lo[16];
-                tmem_ld32(tmem + lb + kRACC + 32 * cb, w);
+            for (int cb = 0; cb < 4; ++cb) {
+                uint32_t w[32], pk[16];
+                tmem_ld32(tmem + lb + kRDK + 32 * cb, w);
                 tmem_ld_wait();
 #pragma unroll
                 for (int x = 0; x < 16; ++x) {
                     const int qi = 32 * cb + 2 * x;
-                    const float d0 = r <= qi ? __uint_as_float(w[2 * x]) + gsh[qi] : 0.f;
-                    const float d1 = r <= qi + 1 ? __uint_as_float(w[2 * x + 1]) + gsh[qi + 1] : 0.f;
-                    hi[x] = pack_bf16x2(d0, d1);
-                    lo[x] = pack_bf16x2(d0 - bf_lo(hi[x]), d1 - bf_hi(hi[x]));
+                    pk[x] = pack_bf16x2(r <= qi ? __uint_as_float(w[2 * x]) + gsh[qi] : 0.f,
+                                        r <= qi + 1 ? __uint_as_float(w[2 * x + 1]) + gsh[qi + 1] : 0.f);
                 }
-                tmem_st16(tmem + lb + kRX + 16 * cb, hi);
-                tmem_st16(tmem + lb + kRX + 64 + 16 * cb, lo);
+                tmem_st16(tmem + lb + kRX + 16 * cb, pk);
             }
             tmem_st_wait();
             tc_fence_before();
             wg_sync();
             if (t == 0) mbar_arrive(&bar->masks_ready);
-            // (d) dk = (dK~ + r_next) * phi'(k)
-            if (!wg_all(mbar_wait(&bar->dk_done, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
+            // (d) dk = (dK~ + r_next) * phi'(k), dv
+            if (!wg_all(mbar_wait(&bar->dkv_done, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
             tc_fence_after();
             const bool valid = r < n;
             __nv_bfloat16* dkrow = dk + ((size_t)bh * N + c0 + r) * kD;
@@ -591,7 +571,7 @@ tc_bwd_reverse_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
 #pragma unroll
             for (int cb = 0; cb < 4; ++cb) {
                 uint32_t w[32];
-                tmem_ld32(tmem + lb + kRACC + 32 * cb, w);
+                tmem_ld32(tmem + lb + kRDK + 32 * cb, w);
                 tmem_ld_wait();
                 if (valid) {
 #pragma unroll
@@ -611,16 +591,10 @@ tc_bwd_reverse_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
                     }
                 }
             }
-            tc_fence_before();
-            wg_sync();
-            if (t == 0) mbar_arrive(&bar->dk_read);
-            // (e) dv
-            if (!wg_all(mbar_wait(&bar->dv_done, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
-            tc_fence_after();
 #pragma unroll
             for (int cb = 0; cb < 4; ++cb) {
                 uint32_t w[32];
-                tmem_ld32(tmem + lb + kRACC + 32 * cb, w);
+                tmem_ld32(tmem + lb + kRDV + 32 * cb, w);
                 tmem_ld_wait();
                 if (valid) {
 #pragma unroll
@@ -635,10 +609,10 @@ tc_bwd_reverse_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
                 }
             }
             tc_fence_before();
-            // (f) r_next += this chunk's sum of g phi(q) (after every thread has used r_next)
             wg_sync();
             rsh[t] += rc;
             wg_sync();
+            if (t == 0) mbar_arrive(&bar->empty);
         }
         tc_fence_before();
     }

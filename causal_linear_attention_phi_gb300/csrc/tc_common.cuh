@@ -78,6 +78,29 @@ __device__ __forceinline__ void phi_tile(uint8_t* tile, int t, int n) {
     }
 }
 
+// phi in place as the bf16 "hi" part, plus lo = bf16(phi - hi) into `lo_tile`
+// (same layout), so that hi + lo carries phi to about 2^-17 relative.
+__device__ __forceinline__ void phi_tile_split(uint8_t* tile, uint8_t* lo_tile, int t, int n) {
+#pragma unroll 4
+    for (int j = 0; j < 16; ++j) {
+        const int row = ((t >> 3) + 16 * j) & 127;
+        const int off = (j >> 3) * kBlockBytes + row * 128 + (t & 7) * 16;
+        uint4 w = *reinterpret_cast<const uint4*>(tile + off);
+        uint32_t* u = reinterpret_cast<uint32_t*>(&w);
+        uint4 l;
+        uint32_t* ul = reinterpret_cast<uint32_t*>(&l);
+        const bool valid = row < n;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float a = valid ? phi_f(bf_lo(u[e])) : 0.f, b = valid ? phi_f(bf_hi(u[e])) : 0.f;
+            u[e] = pack_bf16x2(a, b);
+            ul[e] = pack_bf16x2(a - bf_lo(u[e]), b - bf_hi(u[e]));
+        }
+        *reinterpret_cast<uint4*>(tile + off) = w;
+        *reinterpret_cast<uint4*>(lo_tile + off) = l;
+    }
+}
+
 // Row `row` scaled by 1/den[row] in place (rows >= n are left as loaded: zero).
 __device__ __forceinline__ void scale_rows_tile(uint8_t* tile, int t, const float* inv_den) {
 #pragma unroll 4

@@ -39,6 +39,14 @@ def check(name, gpu, ref, tol):
     return e
 
 
+def check_all(pairs, tol):
+    """Compare several tensors, reporting every error before failing on any."""
+    errs = {name: rel_per_head(a, b) for name, a, b in pairs}
+    bad = {n: e for n, e in errs.items() if not e <= tol}
+    assert not bad, "max rel errs %s (bound %.1e)" % ({n: "%.3e" % e for n, e in errs.items()}, tol)
+    return errs
+
+
 # ---------------------------------------------------------------- forward, small fp32 workload
 def test_small_f32_causal_fwd(la):
     q, k, v = W.make_inputs(W.SMALL_F32)
@@ -123,9 +131,7 @@ def test_causal_bwd_cases(la, B, H, N, Dk, Dv, dtype):
     q, k, v, dO = W.random_case(200 + N, B, H, N, Dk, Dv, dtype=dtype, scale=scale, with_grad=True)
     dq, dk, dv = la.causal_bwd(*dev(q, k, v, dO))
     ref = oracle.causal_bwd_recurrent(q, k, v, dO)
-    tol = tol_for(dtype)
-    for name, a, b in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
-        check(name, a, b, tol)
+    check_all([(n, a, b) for n, a, b in zip(("dq", "dk", "dv"), (dq, dk, dv), ref)], tol_for(dtype))
 
 
 def test_bwd_single_position(la):
@@ -155,9 +161,9 @@ def test_sweep_fwd_bwd_full(la, N):
     qd, kd, vd, dOd = dev(q, k, v, dO)
     o = la.causal_fwd(qd, kd, vd)
     dq, dk, dv = la.causal_bwd(qd, kd, vd, dOd)
-    check("o", o, oracle.causal_recurrent(q, k, v), 2e-2)
-    for name, a, b in zip(("dq", "dk", "dv"), (dq, dk, dv), oracle.causal_bwd_recurrent(q, k, v, dO)):
-        check(name, a, b, 2e-2)
+    check_all([("o", o, oracle.causal_recurrent(q, k, v))] +
+              [(n, a, b) for n, a, b in zip(("dq", "dk", "dv"), (dq, dk, dv), oracle.causal_bwd_recurrent(q, k, v, dO))],
+              2e-2)
 
 
 def _sampled_heads(la, w, heads, tensors=None):
@@ -169,10 +175,9 @@ def _sampled_heads(la, w, heads, tensors=None):
     torch.cuda.synchronize()
     sel = lambda t: torch.stack([t[b, h] for b, h in heads])[None]
     qs, ks, vs, dOs = (sel(t) for t in (q, k, v, dO))
-    check("o", sel(o.cpu()), oracle.causal_recurrent(qs, ks, vs), 2e-2)
     ref = oracle.causal_bwd_recurrent(qs, ks, vs, dOs)
-    for name, a, b in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
-        check(name, sel(a.cpu()), b, 2e-2)
+    check_all([("o", sel(o.cpu()), oracle.causal_recurrent(qs, ks, vs))] +
+              [(n, sel(a.cpu()), b) for n, a, b in zip(("dq", "dk", "dv"), (dq, dk, dv), ref)], 2e-2)
 
 
 def test_sweep_65536_sampled_heads(la):
