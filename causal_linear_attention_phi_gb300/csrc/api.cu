@@ -274,6 +274,14 @@ la_status cuda_status(cudaError_t e, const char* where) {
     } while (0)
 
 }  // namespace
+
+// Argument checks for entry points defined in other translation units.
+la_status checked_shape(const la_shape& s) { return check_shape(s); }
+la_status checked_device() { return check_device(); }
+la_status checked_ptr(const void* p, const char* what) { return check_ptr(p, what); }
+la_status failed(la_status st, const char* msg) { return fail(st, "%s", msg); }
+void clear_detail() { t_detail.clear(); }
+
 }  // namespace la
 
 using namespace la;

@@ -138,6 +138,29 @@ la_status la_recurrent_step(const void* q, const void* k, const void* v, float* 
                             void* out, la_shape s, la_stream_t stream);
 
 /*
+ * la_causal_fwd with no workspace argument: the same causal forward, with its
+ * scratch (the per-segment states) in a 16 MiB device array that the library
+ * owns.  The pages have no counterpart to this call; it exists for callers
+ * that cannot allocate device memory when they call the library, such as a
+ * plugin inside a host framework that owns every device allocation and hands
+ * its plugins no workspace, or a latency-critical loop that may not call
+ * cudaMalloc (which can synchronise the device) after start-up.
+ * Arguments, layouts, dtypes and checks are those of la_causal_fwd.  It calls
+ * no cudaMalloc, cudaFree or other allocating routine.  The array is static:
+ * every GPU that loads the library holds the 16 MiB until the process exits.
+ * The first call on a device looks up the array's address on that device
+ * (that device must be current); make that first call before any stream
+ * capture.  Sizes needing more than the array, i.e. B*H*(Dk*Dv + Dk)*4 bytes
+ * > 16 MiB (at Dk = Dv = 128: B*H > 254), return LA_ERR_WORKSPACE before
+ * anything is launched.  Every call shares the array, so calls whose work
+ * overlaps on the GPU (other streams or host threads) race on it and corrupt
+ * each other's results: serialise them.  Each call rewrites every part of the
+ * array it reads, so what a previous call left there does not matter.
+ */
+la_status la_causal_fwd_noalloc(const void* q, const void* k, const void* v, void* o, la_shape s,
+                                la_stream_t stream);
+
+/*
  * Sticky device-side status: LA_OK, or the first error a kernel recorded since
  * the last la_clear_error() (LA_ERR_TIMEOUT for a bounded wait that ran out).
  * It reads device memory synchronously (the current device is synchronised);
