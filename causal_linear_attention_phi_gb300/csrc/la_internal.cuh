@@ -50,8 +50,14 @@ template <typename T> __device__ __forceinline__ T from_f32(float x);
 template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
 template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
 
-// phi(x) = elu(x) + 1 (alpha = 1): x + 1 for x > 0, exp(x) for x <= 0.
-__device__ __forceinline__ float phi_f(float x) { return x > 0.f ? x + 1.f : expf(x); }
+// 2^x with the ex2.approx instruction (relative error about 2^-22).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+// phi(x) = elu(x) + 1 (alpha = 1): x + 1 for x > 0, exp(x) = 2^(x log2 e) for x <= 0.
+__device__ __forceinline__ float phi_f(float x) { return x > 0.f ? x + 1.f : ex2_approx(x * 1.4426950408889634f); }
 // phi'(x) = 1 for x > 0, exp(x) otherwise; equal to min(1, phi(x)).
 __device__ __forceinline__ float dphi_from_phi(float p) { return fminf(p, 1.f); }
 

@@ -103,29 +103,40 @@ segment_sums_kernel(const T* __restrict__ k, const T* __restrict__ v, float* __r
 
 // ---------------------------------------------------------------- scan over segments
 // mode 0: exclusive prefix over p (in place); 1: exclusive suffix (in place);
-// 2: totals[bh][e] = sum over p (seg unchanged).
+// 2: totals[bh][e] = sum over p (seg unchanged).  Each thread owns four
+// consecutive elements (one float4) of every segment record and walks the P
+// records in batches whose loads are all issued before any of them is used.
+constexpr int kScanBatch = 8;
+
 __global__ void scan_kernel(float* __restrict__ seg, float* __restrict__ totals, int P, size_t E, int mode) {
-    const size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (e >= E) return;
+    const size_t e4 = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
+    if (e4 >= E) return;
     const size_t bh = blockIdx.y;
-    float* base = seg + bh * P * E + e;
-    float run = 0.f;
-    if (mode == SCAN_EXCLUSIVE_PREFIX) {
-        for (int p = 0; p < P; ++p) {
-            float t = base[(size_t)p * E];
-            base[(size_t)p * E] = run;
-            run += t;
+    float* base = seg + bh * P * E + e4;
+    float4 run = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int b0 = 0; b0 < P; b0 += kScanBatch) {
+        const int nb = min(kScanBatch, P - b0);
+        float4 t[kScanBatch];
+#pragma unroll
+        for (int j = 0; j < kScanBatch; ++j) {
+            if (j < nb) {
+                const int p = mode == SCAN_EXCLUSIVE_SUFFIX ? P - 1 - (b0 + j) : b0 + j;
+                t[j] = *reinterpret_cast<const float4*>(base + (size_t)p * E);
+            }
         }
-    } else if (mode == SCAN_EXCLUSIVE_SUFFIX) {
-        for (int p = P - 1; p >= 0; --p) {
-            float t = base[(size_t)p * E];
-            base[(size_t)p * E] = run;
-            run += t;
+#pragma unroll
+        for (int j = 0; j < kScanBatch; ++j) {
+            if (j < nb) {
+                const int p = mode == SCAN_EXCLUSIVE_SUFFIX ? P - 1 - (b0 + j) : b0 + j;
+                if (mode != SCAN_TOTAL) *reinterpret_cast<float4*>(base + (size_t)p * E) = run;
+                run.x += t[j].x;
+                run.y += t[j].y;
+                run.z += t[j].z;
+                run.w += t[j].w;
+            }
         }
-    } else {
-        for (int p = 0; p < P; ++p) run += base[(size_t)p * E];
-        totals[bh * E + e] = run;
     }
+    if (mode == SCAN_TOTAL) *reinterpret_cast<float4*>(totals + bh * E + e4) = run;
 }
 
 // ---------------------------------------------------------------- causal forward
@@ -719,10 +730,10 @@ cudaError_t simt_segment_sums(const void* k, const void* v, float* seg, const la
 }
 
 cudaError_t scan_segments(float* seg, float* totals, const la_shape& s, const Plan& p, int mode, cudaStream_t st) {
-    const size_t E = state_elems(s.Dk, s.Dv);
-    dim3 grid((unsigned)((E + 255) / 256), s.B * s.H);
+    const size_t E = state_elems(s.Dk, s.Dv);  // a multiple of 16 for the supported head sizes
+    dim3 grid((unsigned)((E / 4 + 127) / 128), s.B * s.H);
     launch_begin("scan_segments", st);
-    scan_kernel<<<grid, 256, 0, st>>>(seg, totals, p.P, E, mode);
+    scan_kernel<<<grid, 128, 0, st>>>(seg, totals, p.P, E, mode);
     return launch_end("scan_segments", st);
 }
 

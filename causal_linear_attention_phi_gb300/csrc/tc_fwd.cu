@@ -3,43 +3,44 @@
 //
 // Per chunk c of a segment ("선형 어텐션" (itwiki), 계산 형태 비교: matrix
 // products inside a chunk, the state passed between chunks):
-//   QK   = phi(Q_c) phi(K_c)^T                      tcgen05, TMEM fp32 (128 x 128)
-//   A    = tril(QK)  -> bf16, written back to TMEM   compute warpgroup
-//   O    = phi(Q_c) S_prev + A V_c                   tcgen05, TMEM fp32 (128 x 128)
-//   den  = phi(Q_c) z_prev + A 1                     CUDA cores, fp32
-//   o    = O / den -> bf16 -> global                 compute warpgroup
-//   S   += phi(K_c)^T V_c,  z += phi(K_c)^T 1         tcgen05 (S in TMEM), CUDA cores (z)
-// S_prev enters the O product as a bf16 copy in shared memory, refreshed from
-// the fp32 TMEM state after every chunk.  phi is applied in place to the
-// TMA-staged Q and K tiles (fused into the tile load).
+//   QK   = phi(Q_c) phi(K_c)^T                         tcgen05 -> TMEM fp32 (128 x 128)
+//   A    = tril(QK) -> bf16, written back to TMEM       compute group
+//   O    = phi(Q_c) S_prev + A V_c                      tcgen05 -> TMEM fp32 (128 x 128)
+//   den  = phi(Q_c) z_prev + A 1                        tcgen05, N = 16 -> TMEM (column 0)
+//   o    = O / den -> bf16 -> global                    compute group
+//   S   += phi(K_c)^T V_c,  z += phi(K_c)^T 1           tcgen05 (both accumulate in TMEM)
+// The normaliser products use a constant 16 x 128 operand whose row 0 is ones
+// (the "append a column of ones" form of phi(Q)(phi(K)^T [V | 1]) in the
+// "Transformers은 RNN이다" digest, 핵심 구성요소 2-3).  S_prev and z_prev enter
+// as bf16 copies in shared memory, refreshed from the fp32 TMEM state after
+// every chunk.  phi is applied in place to the TMA-staged Q and K tiles.
 //
 // The same kernel with kOut = false only accumulates the segment's sums
 // (S, z) for the segment scan.
 //
 // Roles (320 threads): warp 0 issues TMA loads, warp 1 owns TMEM and issues
 // tcgen05.mma, warps 2-9 (two warpgroups) transform tiles, mask A, refresh
-// S_prev and write outputs.  Warp w reads TMEM lanes 32*(w%4) ..
-// Every wait is bounded: on timeout the kernel records LA_ERR_TIMEOUT in the
-// sticky error word and all roles leave their loops.
+// S_prev and write outputs.  Warp w reads TMEM lanes 32*(w%4) .. +31 (row r of
+// a 128-row tile); warps 2-5 take columns 0-63 of their rows, warps 6-9 the
+// columns 64-127.  Every wait is bounded: on timeout the kernel records
+// LA_ERR_TIMEOUT in the sticky error word and all roles leave their loops.
 #include <cudaTypedefs.h>
 
 #include <mutex>
 
-#include "la_internal.cuh"
-#include "sm100.cuh"
+#include "tc_common.cuh"
 
 namespace la {
 namespace {
 using namespace sm100;
+using namespace tc;
 
-constexpr int kC = 128;          // chunk length
-constexpr int kD = 128;          // Dk = Dv
-constexpr int kTileBytes = 32768;   // 128 rows x 128 bf16, as two 64-column swizzled blocks
-constexpr int kBlockBytes = 16384;  // one 64-column block (128 rows x 128 B)
 constexpr int kThreads = 320;  // warp 0 TMA, warp 1 MMA, warps 2-9 compute
+constexpr int kComputeThreads = 256;
+constexpr int kSmallBytes = 4096;  // a 16-row x 128-column bf16 K-major operand (two 2 KB blocks)
 
 // TMEM column map (512 columns allocated)
-constexpr uint32_t kTmS = 0, kTmQK = 128, kTmO = 256, kTmA = 384;
+constexpr uint32_t kTmS = 0, kTmQK = 128, kTmO = 256, kTmA = 384, kTmZ = 448, kTmDen = 464;
 
 struct __align__(8) Barriers {
     uint64_t q_full, q_empty;
@@ -54,22 +55,23 @@ struct SmemLayout {
     static constexpr int Q = 0;
     static constexpr int K0 = Q + kTileBytes;       // K stages 0, 1
     static constexpr int V0 = K0 + 2 * kTileBytes;  // V stages 0, 1
-    static constexpr int Sb = V0 + 2 * kTileBytes;
-    static constexpr int zsh = Sb + kTileBytes;     // float[128]
-    static constexpr int zpart = zsh + 512;         // float[2][128]
-    static constexpr int rpart = zpart + 1024;      // float[2][128]
-    static constexpr int dpart = rpart + 1024;      // float[2][128]
-    static constexpr int bars = dpart + 1024;
+    static constexpr int Sb = V0 + 2 * kTileBytes;  // bf16 S_prev, rows = dk
+    static constexpr int Ones = Sb + kTileBytes;    // 16 x 128: row 0 ones, rows 1-15 zero
+    static constexpr int Zb = Ones + kSmallBytes;   // 16 x 128: row 0 bf16 z_prev, rows 1-15 zero
+    static constexpr int bars = Zb + kSmallBytes;
     static constexpr int tmem_slot = bars + 256;
     static constexpr int total = tmem_slot + 16;
 };
 constexpr size_t kSmemBytes = SmemLayout::total + 1024;  // + alignment slack
 
-// The compute group is two warpgroups (warps 2-9, 256 threads).  Warp w reads
-// TMEM lanes 32*(w%4) .. +31 (row r of a 128-row tile); warps 2-5 take columns
-// 0-63 of their rows and warps 6-9 columns 64-127, so each row is split
-// between two threads whose partial row reductions meet in shared memory.
-constexpr int kComputeThreads = 256;
+// K-major 16-row operand, K step kk: block kk / 4 (2 KB apart), +32 B inside the row.
+__device__ __forceinline__ uint64_t desc_small(uint32_t base, int kk) {
+    return smem_desc_sw128(base + (kk >> 2) * 2048 + (kk & 3) * 32, 16, 1024);
+}
+// Byte offset of element (0, col) of a 16-row K-major operand (row 0: chunks unswizzled).
+__device__ __forceinline__ int small_row0_off(int col) {
+    return (col >> 6) * 2048 + (((col & 63) >> 3) << 4) + ((col & 7) << 1);
+}
 
 __device__ __forceinline__ bool cg_all(bool v) {
     // barrier over the compute group (named barrier 1) that also ANDs a predicate
@@ -86,19 +88,11 @@ __device__ __forceinline__ bool cg_all(bool v) {
 }
 __device__ __forceinline__ void cg_sync() { named_barrier(1, kComputeThreads); }
 
-__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
-// Byte offset of logical 16-byte chunk lc (0..15) of `row` in a swizzled tile.
-__device__ __forceinline__ int chunk_off(int row, int lc) {
-    return (lc >> 3) * kBlockBytes + row * 128 + (((lc & 7) ^ (row & 7)) << 4);
-}
-
 // phi in place on a staged 128 x 128 bf16 tile, rows >= n set to exactly 0.
 // Compute thread ct (0..255) handles vectors ct + 256 j, j < 8: block j / 4,
 // row ((ct >> 3) + 32 j) & 127, physical chunk ct & 7 (an elementwise map
 // ignores the swizzle, which only permutes chunks within a row).
-__device__ __forceinline__ void phi_tile(uint8_t* tile, int ct, int n) {
+__device__ __forceinline__ void phi_tile256(uint8_t* tile, int ct, int n) {
 #pragma unroll 4
     for (int j = 0; j < 8; ++j) {
         const int row = ((ct >> 3) + 32 * j) & 127;
@@ -121,10 +115,8 @@ tc_causal_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sQ = base + SmemLayout::Q;
     uint8_t* sSb = base + SmemLayout::Sb;
-    float* zsh = reinterpret_cast<float*>(base + SmemLayout::zsh);       // [128] z before the chunk
-    float* zpart = reinterpret_cast<float*>(base + SmemLayout::zpart);   // [2][128] this chunk's column sums
-    float* rpart = reinterpret_cast<float*>(base + SmemLayout::rpart);   // [2][128] row partials of A 1
-    float* dpart = reinterpret_cast<float*>(base + SmemLayout::dpart);   // [2][128] row partials of phi(q).z
+    uint8_t* sOnes = base + SmemLayout::Ones;
+    uint8_t* sZb = base + SmemLayout::Zb;
     Barriers* bar = reinterpret_cast<Barriers*>(base + SmemLayout::bars);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + SmemLayout::tmem_slot);
 
@@ -148,6 +140,18 @@ tc_causal_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     if (warp == 1) {
         tmem_alloc(tmem_slot, 512);
         tmem_relinquish();
+    }
+    if (warp >= 2) {
+        // constant operand: row 0 ones, rows 1-15 zero (row 0 is unswizzled); Zb rows 1-15 zero
+        const int ct = tid - 64;
+        for (int x = ct; x < kSmallBytes / 16; x += kComputeThreads) {
+            const int row = (x >> 3) & 15;  // 8 chunks of 16 B per 128-B row, 16 rows per 2 KB block
+            const uint32_t one2 = 0x3F803F80u;
+            const uint4 v = row == 0 ? make_uint4(one2, one2, one2, one2) : make_uint4(0u, 0u, 0u, 0u);
+            reinterpret_cast<uint4*>(sOnes)[x] = v;
+            reinterpret_cast<uint4*>(sZb)[x] = make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();
     }
     tc_fence_before();
     __syncthreads();
@@ -186,47 +190,47 @@ tc_causal_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t id_qk = idesc_bf16_f32(128, 128, 0, 0);
+            constexpr uint32_t id_kk = idesc_bf16_f32(128, 128, 0, 0);
             constexpr uint32_t id_kmn = idesc_bf16_f32(128, 128, 0, 1);
             constexpr uint32_t id_mnmn = idesc_bf16_f32(128, 128, 1, 1);
-            const uint32_t q_addr = smem_u32(sQ), sb_addr = smem_u32(sSb);
+            constexpr uint32_t id_k16 = idesc_bf16_f32(128, 16, 0, 0);   // N = 16, both K-major
+            constexpr uint32_t id_mn16 = idesc_bf16_f32(128, 16, 1, 0);  // N = 16, A MN-major
+            const uint32_t aQ = smem_u32(sQ), aSb = smem_u32(sSb), aOnes = smem_u32(sOnes), aZb = smem_u32(sZb);
             bool ok = true;
             for (int i = 0; i < nloc && ok; ++i) {
                 const int s = i & 1;
-                const uint32_t k_addr = smem_u32(sK(s)), v_addr = smem_u32(sV(s));
+                const uint32_t aK = smem_u32(sK(s)), aV = smem_u32(sV(s));
                 if (!(ok = mbar_wait(&bar->qk_ready[s], (i >> 1) & 1, err, LA_ERR_TIMEOUT))) break;
                 tc_fence_after();
                 if (kOut) {
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint32_t off = (kk >> 2) * kBlockBytes + (kk & 3) * 32;
-                        mma_ss(tmem + kTmQK, smem_desc_sw128(q_addr + off, 16, 1024),
-                               smem_desc_sw128(k_addr + off, 16, 1024), id_qk, kk > 0);
-                    }
+                    for (int kk = 0; kk < 8; ++kk)  // QK = Q~ K~^T
+                        mma_ss(tmem + kTmQK, desc_kmajor(aQ, kk), desc_kmajor(aK, kk), id_kk, kk > 0);
                     mma_commit(&bar->qk_done);
                     if (!(ok = mbar_wait(&bar->sb_ready, i & 1, err, LA_ERR_TIMEOUT))) break;
                     tc_fence_after();
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint32_t off = (kk >> 2) * kBlockBytes + (kk & 3) * 32;
-                        mma_ss(tmem + kTmO, smem_desc_sw128(q_addr + off, 16, 1024),
-                               smem_desc_sw128(sb_addr + kk * 2048, kBlockBytes, 1024), id_kmn, kk > 0);
+                    for (int kk = 0; kk < 8; ++kk) {  // O = Q~ S_prev, den = Q~ z_prev
+                        mma_ss(tmem + kTmO, desc_kmajor(aQ, kk), desc_mnmajor(aSb, kk), id_kmn, kk > 0);
+                        mma_ss(tmem + kTmDen, desc_kmajor(aQ, kk), desc_small(aZb, kk), id_k16, kk > 0);
                     }
                     mma_commit(&bar->q_empty);
                     if (!(ok = mbar_wait(&bar->a_ready, i & 1, err, LA_ERR_TIMEOUT))) break;
                     tc_fence_after();
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        mma_ts(tmem + kTmO, tmem + kTmA + 8 * kk,
-                               smem_desc_sw128(v_addr + kk * 2048, kBlockBytes, 1024), id_kmn, 1);
+                    for (int kk = 0; kk < 8; ++kk) {  // O += A V, den += A 1
+                        mma_ts(tmem + kTmO, tmem + kTmA + 8 * kk, desc_mnmajor(aV, kk), id_kmn, 1);
+                        mma_ts(tmem + kTmDen, tmem + kTmA + 8 * kk, desc_small(aOnes, kk), id_k16, 1);
+                    }
                     mma_commit(&bar->o_done);
                 }
-                // S += phi(K)^T V  (K tile read as an MN-major A operand)
+                // S += K~^T V, z += K~^T 1  (K tile read as an MN-major A operand)
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_ss(tmem + kTmS, smem_desc_sw128(k_addr + kk * 2048, kBlockBytes, 1024),
-                           smem_desc_sw128(v_addr + kk * 2048, kBlockBytes, 1024), id_mnmn,
-                           (kOut || i > 0 || kk > 0) ? 1u : 0u);
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t acc = (kOut || i > 0 || kk > 0) ? 1u : 0u;
+                    mma_ss(tmem + kTmS, desc_mnmajor(aK, kk), desc_mnmajor(aV, kk), id_mnmn, acc);
+                    mma_ss(tmem + kTmZ, desc_mnmajor(aK, kk), desc_small(aOnes, kk), id_mn16, acc);
+                }
                 mma_commit(&bar->s_done);
                 mma_commit(&bar->kv_empty[s]);
             }
@@ -240,17 +244,28 @@ tc_causal_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         const int h = (warp - 2) >> 2;                 // column half of the rows this thread serves
         const int r = 32 * (warp & 3) + lane;          // TMEM lane / tile row
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-        const int zc = ct & 127, zh = ct >> 7;         // column-sum assignment: column zc, rows of half zh
-        if (ct < 128) zsh[ct] = kOut ? segp[(size_t)kD * kD + ct] : 0.f;
         if (kOut) {
-            // S_prev from the scanned segment prefix: row r, this thread's 64 columns
+            // initial state from the scanned segment prefix: S row r (this thread's 64 columns), z[r]
             const float* pre = segp + (size_t)r * kD + 64 * h;
 #pragma unroll
             for (int cb = 0; cb < 2; ++cb) {
                 uint32_t w[32];
 #pragma unroll
-                for (int x = 0; x < 32; ++x) w[x] = __float_as_uint(pre[32 * cb + x]);
+                for (int x = 0; x < 32; x += 4) {
+                    const float4 f = *reinterpret_cast<const float4*>(pre + 32 * cb + x);
+                    w[x] = __float_as_uint(f.x);
+                    w[x + 1] = __float_as_uint(f.y);
+                    w[x + 2] = __float_as_uint(f.z);
+                    w[x + 3] = __float_as_uint(f.w);
+                }
                 tmem_st32(tmem + lane_base + kTmS + 64 * h + 32 * cb, w);
+            }
+            if (h == 0) {
+                uint32_t zw[16];
+                const uint32_t zv = __float_as_uint(segp[(size_t)kD * kD + r]);
+#pragma unroll
+                for (int x = 0; x < 16; ++x) zw[x] = zv;
+                tmem_st16(tmem + lane_base + kTmZ, zw);
             }
             tmem_st_wait();
         }
@@ -259,119 +274,107 @@ tc_causal_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         for (int i = 0; i < nloc && ok; ++i) {
             const int s = i & 1;
             const int c0 = (cbeg + i) * kC, n = min(kC, N - c0);
-            uint8_t* kt = sK(s);
             // (a) phi on the K (and Q) tiles
             bool w = mbar_wait(&bar->kv_full[s], (i >> 1) & 1, err, LA_ERR_TIMEOUT);
             if (kOut) w = w && mbar_wait(&bar->q_full, i & 1, err, LA_ERR_TIMEOUT);
             if (!cg_all(w)) { ok = false; break; }
-            phi_tile(kt, ct, n);
-            if (kOut) phi_tile(sQ, ct, n);
+            phi_tile256(sK(s), ct, n);
+            if (kOut) phi_tile256(sQ, ct, n);
             fence_proxy_async_smem();
             cg_sync();
             if (ct == 0) mbar_arrive(&bar->qk_ready[s]);
-            {
-                // this chunk's column sums of phi(K), rows [64 zh, 64 zh + 64) of column zc
-                float acc = 0.f;
-                const int rend = min(64 * zh + 64, n);
-                for (int row = 64 * zh; row < rend; ++row) {
-                    const uint16_t hv =
-                        *reinterpret_cast<const uint16_t*>(kt + chunk_off(row, zc >> 3) + ((zc & 7) << 1));
-                    acc += __uint_as_float((uint32_t)hv << 16);
-                }
-                zpart[zh * 128 + zc] = acc;
+            if (!kOut) continue;
+            // (b) S_prev, z_prev -> bf16 operands (row r = dk, this thread's 64 dv columns = block h)
+            if (i > 0) {
+                if (!cg_all(mbar_wait(&bar->s_done, (i - 1) & 1, err, LA_ERR_TIMEOUT))) { ok = false; break; }
+                tc_fence_after();
             }
-            if (kOut) {
-                // den partial: phi(q_r) . z_prev over this thread's 64 columns
-                float di = 0.f;
 #pragma unroll
-                for (int lc8 = 0; lc8 < 8; ++lc8) {
-                    const int lc = 8 * h + lc8;
-                    const uint4 qv = *reinterpret_cast<const uint4*>(sQ + chunk_off(r, lc));
-                    const uint32_t* u = reinterpret_cast<const uint32_t*>(&qv);
-                    const float* zz = zsh + 8 * lc;
+            for (int cb = 0; cb < 2; ++cb) {
+                uint32_t wv[32];
+                tmem_ld32(tmem + lane_base + kTmS + 64 * h + 32 * cb, wv);
+                tmem_ld_wait();
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) di += bf_lo(u[e]) * zz[2 * e] + bf_hi(u[e]) * zz[2 * e + 1];
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    uint4 v4;
+                    v4.x = pack_bf16x2(__uint_as_float(wv[8 * q4 + 0]), __uint_as_float(wv[8 * q4 + 1]));
+                    v4.y = pack_bf16x2(__uint_as_float(wv[8 * q4 + 2]), __uint_as_float(wv[8 * q4 + 3]));
+                    v4.z = pack_bf16x2(__uint_as_float(wv[8 * q4 + 4]), __uint_as_float(wv[8 * q4 + 5]));
+                    v4.w = pack_bf16x2(__uint_as_float(wv[8 * q4 + 6]), __uint_as_float(wv[8 * q4 + 7]));
+                    *reinterpret_cast<uint4*>(sSb + chunk_off(r, 8 * h + 4 * cb + q4)) = v4;
                 }
-                dpart[h * 128 + r] = di;
-                // (b) S_prev -> bf16 B operand (row = dk = r, this thread's 64 dv columns = block h)
-                if (i > 0) {
-                    if (!cg_all(mbar_wait(&bar->s_done, (i - 1) & 1, err, LA_ERR_TIMEOUT))) { ok = false; break; }
-                    tc_fence_after();
-                }
+            }
+            if (h == 0) {
+                uint32_t zv[16];
+                tmem_ld16(tmem + lane_base + kTmZ, zv);
+                tmem_ld_wait();
+                *reinterpret_cast<__nv_bfloat16*>(sZb + small_row0_off(r)) = __float2bfloat16_rn(__uint_as_float(zv[0]));
+            }
+            tc_fence_before();
+            fence_proxy_async_smem();
+            cg_sync();
+            if (ct == 0) mbar_arrive(&bar->sb_ready);
+            // (c) A = tril(QK^T) on keys [64 h, 64 h + 64) -> bf16 pairs into TMEM columns [32 h, 32 h + 32)
+            if (!cg_all(mbar_wait(&bar->qk_done, i & 1, err, LA_ERR_TIMEOUT))) { ok = false; break; }
+            tc_fence_after();
 #pragma unroll
-                for (int cb = 0; cb < 2; ++cb) {
+            for (int cb = 0; cb < 2; ++cb) {
+                const int j0 = 64 * h + 32 * cb;  // first key of this 32-column block
+                uint32_t pk[16];
+                if (j0 > r) {  // entirely above the diagonal
+#pragma unroll
+                    for (int x = 0; x < 16; ++x) pk[x] = 0u;
+                } else {
                     uint32_t wv[32];
-                    tmem_ld32(tmem + lane_base + kTmS + 64 * h + 32 * cb, wv);
+                    tmem_ld32(tmem + lane_base + kTmQK + j0, wv);
                     tmem_ld_wait();
+                    if (j0 + 31 <= r) {  // entirely on or below the diagonal
+#pragma unroll
+                        for (int x = 0; x < 16; ++x)
+                            pk[x] = pack_bf16x2(__uint_as_float(wv[2 * x]), __uint_as_float(wv[2 * x + 1]));
+                    } else {
+#pragma unroll
+                        for (int x = 0; x < 16; ++x)
+                            pk[x] = pack_bf16x2(j0 + 2 * x <= r ? __uint_as_float(wv[2 * x]) : 0.f,
+                                                j0 + 2 * x + 1 <= r ? __uint_as_float(wv[2 * x + 1]) : 0.f);
+                    }
+                }
+                tmem_st16(tmem + lane_base + kTmA + 32 * h + 16 * cb, pk);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            cg_sync();
+            if (ct == 0) mbar_arrive(&bar->a_ready);
+            // (d) o = O / den on this thread's 64 columns
+            if (!cg_all(mbar_wait(&bar->o_done, i & 1, err, LA_ERR_TIMEOUT))) { ok = false; break; }
+            tc_fence_after();
+            uint32_t dv[16];
+            tmem_ld16(tmem + lane_base + kTmDen, dv);
+            tmem_ld_wait();
+            const float inv = 1.f / __uint_as_float(dv[0]);
+            __nv_bfloat16* orow = o + ((size_t)bh * N + c0 + r) * kD + 64 * h;
+#pragma unroll
+            for (int cb = 0; cb < 2; ++cb) {
+                uint32_t wv[32];
+                tmem_ld32(tmem + lane_base + kTmO + 64 * h + 32 * cb, wv);
+                tmem_ld_wait();
+                if (r < n) {
 #pragma unroll
                     for (int q4 = 0; q4 < 4; ++q4) {
                         uint4 v4;
-                        v4.x = pack_bf16x2(__uint_as_float(wv[8 * q4 + 0]), __uint_as_float(wv[8 * q4 + 1]));
-                        v4.y = pack_bf16x2(__uint_as_float(wv[8 * q4 + 2]), __uint_as_float(wv[8 * q4 + 3]));
-                        v4.z = pack_bf16x2(__uint_as_float(wv[8 * q4 + 4]), __uint_as_float(wv[8 * q4 + 5]));
-                        v4.w = pack_bf16x2(__uint_as_float(wv[8 * q4 + 6]), __uint_as_float(wv[8 * q4 + 7]));
-                        *reinterpret_cast<uint4*>(sSb + chunk_off(r, 8 * h + 4 * cb + q4)) = v4;
+                        v4.x = pack_bf16x2(__uint_as_float(wv[8 * q4 + 0]) * inv, __uint_as_float(wv[8 * q4 + 1]) * inv);
+                        v4.y = pack_bf16x2(__uint_as_float(wv[8 * q4 + 2]) * inv, __uint_as_float(wv[8 * q4 + 3]) * inv);
+                        v4.z = pack_bf16x2(__uint_as_float(wv[8 * q4 + 4]) * inv, __uint_as_float(wv[8 * q4 + 5]) * inv);
+                        v4.w = pack_bf16x2(__uint_as_float(wv[8 * q4 + 6]) * inv, __uint_as_float(wv[8 * q4 + 7]) * inv);
+                        *reinterpret_cast<uint4*>(orow + 32 * cb + 8 * q4) = v4;
                     }
                 }
-                tc_fence_before();
-                fence_proxy_async_smem();
-                cg_sync();
-                if (ct == 0) mbar_arrive(&bar->sb_ready);
-                // (c) A = tril(QK^T) on keys [64 h, 64 h + 64) -> bf16 pairs into TMEM; row-sum partial
-                if (!cg_all(mbar_wait(&bar->qk_done, i & 1, err, LA_ERR_TIMEOUT))) { ok = false; break; }
-                tc_fence_after();
-                float rs = 0.f;
-#pragma unroll
-                for (int cb = 0; cb < 2; ++cb) {
-                    uint32_t wv[32], pk[16];
-                    tmem_ld32(tmem + lane_base + kTmQK + 64 * h + 32 * cb, wv);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int x = 0; x < 16; ++x) {
-                        const int j0 = 64 * h + 32 * cb + 2 * x;
-                        pk[x] = pack_bf16x2(j0 <= r ? __uint_as_float(wv[2 * x]) : 0.f,
-                                            j0 + 1 <= r ? __uint_as_float(wv[2 * x + 1]) : 0.f);
-                        rs += bf_lo(pk[x]) + bf_hi(pk[x]);
-                    }
-                    tmem_st16(tmem + lane_base + kTmA + 32 * h + 16 * cb, pk);
-                }
-                rpart[h * 128 + r] = rs;
-                tmem_st_wait();
-                tc_fence_before();
-                cg_sync();
-                if (ct == 0) mbar_arrive(&bar->a_ready);
-                // (d) o = O / den on this thread's 64 columns
-                if (!cg_all(mbar_wait(&bar->o_done, i & 1, err, LA_ERR_TIMEOUT))) { ok = false; break; }
-                tc_fence_after();
-                const float inv = 1.f / (rpart[r] + rpart[128 + r] + dpart[r] + dpart[128 + r]);
-                __nv_bfloat16* orow = o + ((size_t)bh * N + c0 + r) * kD + 64 * h;
-#pragma unroll
-                for (int cb = 0; cb < 2; ++cb) {
-                    uint32_t wv[32];
-                    tmem_ld32(tmem + lane_base + kTmO + 64 * h + 32 * cb, wv);
-                    tmem_ld_wait();
-                    if (r < n) {
-#pragma unroll
-                        for (int q4 = 0; q4 < 4; ++q4) {
-                            uint4 v4;
-                            v4.x = pack_bf16x2(__uint_as_float(wv[8 * q4 + 0]) * inv, __uint_as_float(wv[8 * q4 + 1]) * inv);
-                            v4.y = pack_bf16x2(__uint_as_float(wv[8 * q4 + 2]) * inv, __uint_as_float(wv[8 * q4 + 3]) * inv);
-                            v4.z = pack_bf16x2(__uint_as_float(wv[8 * q4 + 4]) * inv, __uint_as_float(wv[8 * q4 + 5]) * inv);
-                            v4.w = pack_bf16x2(__uint_as_float(wv[8 * q4 + 6]) * inv, __uint_as_float(wv[8 * q4 + 7]) * inv);
-                            *reinterpret_cast<uint4*>(orow + 32 * cb + 8 * q4) = v4;
-                        }
-                    }
-                }
-                tc_fence_before();
             }
-            // z_prev += this chunk's column sums (after every thread has used z_prev)
-            cg_sync();
-            if (ct < 128) zsh[ct] += zpart[ct] + zpart[128 + ct];
-            cg_sync();
+            tc_fence_before();
         }
         if (!kOut && ok && nloc > 0) {
-            // segment sums out: S from TMEM (row r = dk, this thread's 64 columns), z from shared memory.
-            // The MMA thread's single-use drain barrier marks the last S update done.
+            // segment sums out: S row r (this thread's 64 columns) and z[r] from TMEM.  The MMA
+            // thread's single-use drain barrier marks the last update done.
             if (cg_all(mbar_wait(&bar->final_mma, 0, err, LA_ERR_TIMEOUT))) {
                 tc_fence_after();
                 float* out = segp + (size_t)r * kD + 64 * h;
@@ -386,7 +389,12 @@ tc_causal_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                             make_float4(__uint_as_float(wv[x]), __uint_as_float(wv[x + 1]),
                                         __uint_as_float(wv[x + 2]), __uint_as_float(wv[x + 3]));
                 }
-                if (ct < 128) segp[(size_t)kD * kD + ct] = zsh[ct];
+                if (h == 0) {
+                    uint32_t zv[16];
+                    tmem_ld16(tmem + lane_base + kTmZ, zv);
+                    tmem_ld_wait();
+                    segp[(size_t)kD * kD + r] = __uint_as_float(zv[0]);
+                }
             }
         }
         tc_fence_before();
@@ -415,7 +423,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 }  // namespace
 
-// A [BH][N][128] bf16 tensor as a 3-D TMA map with 64 x 128 x 1 boxes and the
+// A [BH][N][D] bf16 tensor as a 3-D TMA map with 64 x box_rows x 1 boxes and the
 // 128-byte swizzle; rows past N inside a head read as zeros.
 bool make_tmap_bf16_rows(CUtensorMap* map, const void* ptr, int BH, int N, int D, int box_rows) {
     auto fn = encode_fn();
