@@ -4,21 +4,24 @@
 // The gradient is a cumulative sum ("[논문 리뷰] Transformers are RNNs ..."
 // (velog review), 3.5 Gradient Computation): states are recomputed, never
 // stored per position.  With den_i = phi(q_i)^T z_i, P_i = dO_i / den_i,
-// g_i = -(dO_i . o_i) / den_i, per chunk c (A = tril(Q~ K~^T), D = tril(P V^T + g 1^T)):
+// g_i = -P_i . o_i, per chunk c (A = tril(Q~ K~^T), D = tril(P V^T + g 1^T)):
 //   dQ~ = P S_prev^T + g z_prev^T + D K~
 //   dK~ = V R_next^T + 1 r_next^T + D^T Q~
 //   dV  = K~ R_next + A^T P
 // where R_next = sum over later positions of phi(q_i) P_i^T and r_next = sum g_i phi(q_i).
 //
 // Forward sweep kernel: chunks in order, S and the segment's R contribution in
-// TMEM; recomputes num, den (as the forward does), derives P and g, writes dq
-// and the per-position (den, g).
+// TMEM; recomputes num and den as the forward does, derives P and g (g from the
+// bf16 P the products use), writes dq and the per-position (den, g).  dq is the
+// difference of two terms that nearly cancel when phi(k) varies little, so D
+// enters as a hi + lo pair of bf16 operands and phi(K) as hi + lo in D K~.
 // Reverse sweep kernel: chunks in reverse order with R_next in TMEM; every
 // product is taken with the keys as the M (TMEM lane) dimension so dk and dv
 // come out row by row.
 //
-// Roles as in the forward kernel: warp 0 TMA, warp 1 TMEM owner and MMA
-// issuer, warps 2-5 the compute warpgroup.  All waits are bounded.
+// Roles: warp 0 TMA, warp 1 TMEM owner and MMA issuer, warps 2-9 the 256-thread
+// compute group (each row's columns split between two warpgroups).  All waits
+// are bounded.
 #include "tc_common.cuh"
 
 namespace la {
@@ -26,7 +29,7 @@ namespace {
 using namespace sm100;
 using namespace tc;
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
 
 // ------------------------------------------------------------------ forward sweep
 // TMEM: S [0,128) fp32 state; R [128,256) segment sum of phi(q) P^T;
@@ -42,12 +45,16 @@ struct FwdSweepBars {
 };
 
 struct FwdSweepSmem {
-    static constexpr int Q = 0, K = kTileBytes, V = 2 * kTileBytes, P = 3 * kTileBytes, Sb = 4 * kTileBytes;
-    static constexpr int KLo = 5 * kTileBytes;   // low bf16 half of phi(K) (hi is the K tile)
-    static constexpr int zsh = 6 * kTileBytes;   // float[128] z_prev
-    static constexpr int rsh = zsh + 512;        // float[128] segment sum of g phi(q)
-    static constexpr int gsh = rsh + 512;        // float[128] g of the chunk's rows
-    static constexpr int bars = gsh + 512;
+    static constexpr int Q = 0, K = kTileBytes, KLo = 2 * kTileBytes, V = 3 * kTileBytes, P = 4 * kTileBytes;
+    static constexpr int Sb = 5 * kTileBytes;
+    static constexpr int zsh = 6 * kTileBytes;  // float[128] z_prev
+    static constexpr int zacc = zsh + 512;      // float[128] this chunk's column sums of phi(k)
+    static constexpr int racc = zacc + 512;     // float[128] segment sum of g phi(q)
+    static constexpr int gsh = racc + 512;      // float[128] g of the chunk's rows
+    static constexpr int rpart = gsh + 512;     // float[2][128] row-sum halves of A
+    static constexpr int dpart = rpart + 1024;  // float[2][128] halves of phi(q) . z_prev
+    static constexpr int tpart = dpart + 1024;  // float[2][128] halves of P . num
+    static constexpr int bars = tpart + 1024;
     static constexpr int tmem_slot = bars + 256;
     static constexpr int total = tmem_slot + 16;
 };
@@ -62,13 +69,17 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sQ = base + FwdSweepSmem::Q;
     uint8_t* sK = base + FwdSweepSmem::K;
+    uint8_t* sKLo = base + FwdSweepSmem::KLo;
     uint8_t* sV = base + FwdSweepSmem::V;
     uint8_t* sP = base + FwdSweepSmem::P;
     uint8_t* sSb = base + FwdSweepSmem::Sb;
-    uint8_t* sKLo = base + FwdSweepSmem::KLo;
     float* zsh = reinterpret_cast<float*>(base + FwdSweepSmem::zsh);
-    float* rsh = reinterpret_cast<float*>(base + FwdSweepSmem::rsh);
+    float* zacc = reinterpret_cast<float*>(base + FwdSweepSmem::zacc);
+    float* racc = reinterpret_cast<float*>(base + FwdSweepSmem::racc);
     float* gsh = reinterpret_cast<float*>(base + FwdSweepSmem::gsh);
+    float* rpart = reinterpret_cast<float*>(base + FwdSweepSmem::rpart);
+    float* dpart = reinterpret_cast<float*>(base + FwdSweepSmem::dpart);
+    float* tpart = reinterpret_cast<float*>(base + FwdSweepSmem::tpart);
     FwdSweepBars* bar = reinterpret_cast<FwdSweepBars*>(base + FwdSweepSmem::bars);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + FwdSweepSmem::tmem_slot);
 
@@ -119,8 +130,8 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
             constexpr uint32_t id_kk = idesc_bf16_f32(128, 128, 0, 0);
             constexpr uint32_t id_kmn = idesc_bf16_f32(128, 128, 0, 1);
             constexpr uint32_t id_mnmn = idesc_bf16_f32(128, 128, 1, 1);
-            const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV), aP = smem_u32(sP),
-                           aSb = smem_u32(sSb), aKLo = smem_u32(sKLo);
+            const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aKLo = smem_u32(sKLo), aV = smem_u32(sV),
+                           aP = smem_u32(sP), aSb = smem_u32(sSb);
             for (int i = 0; i < nloc; ++i) {
                 const uint32_t ph = i & 1;
                 if (!mbar_wait(&bar->qk_ready, ph, err, LA_ERR_TIMEOUT)) break;
@@ -159,200 +170,262 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
                 for (int kk = 0; kk < 8; ++kk)  // Y = P S_prev^T
                     mma_ss(tmem + kFY, desc_kmajor(aP, kk), desc_kmajor(aSb, kk), id_kk, kk > 0);
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)  // Y += D K~ as D_hi K_hi + D_lo K_hi + D_hi K_lo
+                for (int kk = 0; kk < 8; ++kk) {  // Y += D K~ as D_hi K_hi + D_lo K_hi + D_hi K_lo
                     mma_ts(tmem + kFY, tmem + kFX + 8 * kk, desc_mnmajor(aK, kk), id_kmn, 1);
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
                     mma_ts(tmem + kFY, tmem + kFX + 64 + 8 * kk, desc_mnmajor(aK, kk), id_kmn, 1);
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
                     mma_ts(tmem + kFY, tmem + kFX + 8 * kk, desc_mnmajor(aKLo, kk), id_kmn, 1);
+                }
                 mma_commit(&bar->dq_done);
             }
             mma_commit(&bar->final_mma);
             mbar_wait(&bar->final_mma, 0, err, LA_ERR_TIMEOUT);
         }
     } else {
-        const int t = tid - 64;
+        const int ct = tid - 64;
+        const int h = (warp - 2) >> 2;
         const int r = 32 * (warp & 3) + lane;
-        const uint32_t lb = (uint32_t)(32 * (warp & 3)) << 16;
+        const uint32_t lb = ((uint32_t)(32 * (warp & 3)) << 16) + 64 * h;  // this thread's row half
         const float* pre = seg_S + ((size_t)bh * P + p) * E;
-        global_row_to_tmem(pre + (size_t)r * kD, tmem + lb + kFS);
-        zsh[r] = pre[(size_t)kD * kD + r];
-        rsh[r] = 0.f;
+        {
+            // S_prev row r (this half) into TMEM; z_prev
+            uint32_t w[64];
+#pragma unroll
+            for (int x = 0; x < 64; x += 4) {
+                const float4 f = *reinterpret_cast<const float4*>(pre + (size_t)r * kD + 64 * h + x);
+                w[x] = __float_as_uint(f.x);
+                w[x + 1] = __float_as_uint(f.y);
+                w[x + 2] = __float_as_uint(f.z);
+                w[x + 3] = __float_as_uint(f.w);
+            }
+            tmem_st32(tmem + lb + kFS, *reinterpret_cast<uint32_t(*)[32]>(&w[0]));
+            tmem_st32(tmem + lb + kFS + 32, *reinterpret_cast<uint32_t(*)[32]>(&w[32]));
+            tmem_st_wait();
+        }
+        if (ct < 128) {
+            zsh[ct] = pre[(size_t)kD * kD + ct];
+            zacc[ct] = 0.f;
+            racc[ct] = 0.f;
+        }
         tc_fence_before();
-        bool ok = wg_all(true);
+        bool ok = grp_all(true);
         float* dgh = den_g + (size_t)bh * N * 2;
         for (int i = 0; i < nloc && ok; ++i) {
             const uint32_t ph = i & 1;
             const int c0 = (cbeg + i) * kC, n = min(kC, N - c0);
-            // (a) phi on the Q and K tiles; this chunk's column sums of phi(K); den_inter
-            if (!wg_all(mbar_wait(&bar->full, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
-            phi_tile_split(sK, sKLo, t, n);
-            phi_tile(sQ, t, n);
+            const bool valid = r < n;
+            // (a) phi on K (hi in place, lo beside it; column sums of hi into zacc) and on Q
+            if (!grp_all(mbar_wait(&bar->full, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
+            grp_phi_tile(sK, sKLo, ct, n, nullptr, zacc);
+            grp_phi_tile(sQ, nullptr, ct, n, nullptr, nullptr);
             fence_proxy_async_smem();
-            wg_sync();
-            if (t == 0) mbar_arrive(&bar->qk_ready);
-            const float zc = column_sum(sK, t, n, nullptr);
-            float den_inter = 0.f;
-#pragma unroll 4
-            for (int lc = 0; lc < 16; ++lc) {
-                const uint4 w = *reinterpret_cast<const uint4*>(sQ + chunk_off(r, lc));
-                const uint32_t* u = reinterpret_cast<const uint32_t*>(&w);
+            grp_sync();
+            if (ct == 0) mbar_arrive(&bar->qk_ready);
+            {
+                // phi(q_r) . z_prev over this thread's 64 columns
+                float di = 0.f;
 #pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    den_inter += bf_lo(u[e]) * zsh[8 * lc + 2 * e] + bf_hi(u[e]) * zsh[8 * lc + 2 * e + 1];
+                for (int c8 = 0; c8 < 8; ++c8) {
+                    const int lc = 8 * h + c8;
+                    const uint4 qv = *reinterpret_cast<const uint4*>(sQ + chunk_off(r, lc));
+                    const uint32_t* u = reinterpret_cast<const uint32_t*>(&qv);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        di += bf_lo(u[e]) * zsh[8 * lc + 2 * e] + bf_hi(u[e]) * zsh[8 * lc + 2 * e + 1];
+                }
+                dpart[128 * h + r] = di;
             }
-            // (b) S_prev -> bf16 copy (rows = dk)
+            // (b) S_prev -> bf16 copy (rows = dk; this thread's 64 columns)
             if (i > 0) {
                 const bool w1 = mbar_wait(&bar->s_done, (i - 1) & 1, err, LA_ERR_TIMEOUT);
                 const bool w2 = mbar_wait(&bar->dq_done, (i - 1) & 1, err, LA_ERR_TIMEOUT);
-                if (!wg_all(w1 && w2)) { ok = false; break; }
+                if (!grp_all(w1 && w2)) { ok = false; break; }
                 tc_fence_after();
             }
-            tmem_row_to_tile(tmem + lb + kFS, sSb, r);
+            {
+                uint32_t w[64];
+                tmem_ld64(tmem + lb + kFS, w);
+                row64_to_tile(w, sSb, r, h);
+            }
             tc_fence_before();
             fence_proxy_async_smem();
-            wg_sync();
-            if (t == 0) mbar_arrive(&bar->sb_ready);
-            // (c) A = tril(QK^T) as bf16 pairs into X[0,64) (each thread overwrites only columns it has read)
-            if (!wg_all(mbar_wait(&bar->qk_done, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
+            grp_sync();
+            if (ct == 0) mbar_arrive(&bar->sb_ready);
+            // (c) A = tril(QK^T) on keys [64h, 64h+64) as bf16 pairs into X columns [32h, 32h+32)
+            if (!grp_all(mbar_wait(&bar->qk_done, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
             tc_fence_after();
-            float rs = 0.f;
+            {
+                uint32_t pk[32];
+                float rs = 0.f;
 #pragma unroll
-            for (int cb = 0; cb < 4; ++cb) {
-                uint32_t w[32], pk[16];
-                tmem_ld32(tmem + lb + kFX + 32 * cb, w);
-                tmem_ld_wait();
+                for (int cb = 0; cb < 2; ++cb) {
+                    const int j0 = 64 * h + 32 * cb;
+                    if (j0 > r) {
 #pragma unroll
-                for (int x = 0; x < 16; ++x) {
-                    const int j = 32 * cb + 2 * x;
-                    pk[x] = pack_bf16x2(j <= r ? __uint_as_float(w[2 * x]) : 0.f,
-                                        j + 1 <= r ? __uint_as_float(w[2 * x + 1]) : 0.f);
-                    rs += bf_lo(pk[x]) + bf_hi(pk[x]);
+                        for (int x = 0; x < 16; ++x) pk[16 * cb + x] = 0u;
+                    } else {
+                        uint32_t w[32];
+                        tmem_ld32(tmem + lb + kFX + 32 * cb, w);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int x = 0; x < 16; ++x) {
+                            const int j = j0 + 2 * x;
+                            pk[16 * cb + x] = pack_bf16x2(j <= r ? __uint_as_float(w[2 * x]) : 0.f,
+                                                          j + 1 <= r ? __uint_as_float(w[2 * x + 1]) : 0.f);
+                            rs += bf_lo(pk[16 * cb + x]) + bf_hi(pk[16 * cb + x]);
+                        }
+                    }
                 }
-                tmem_st16(tmem + lb + kFX + 16 * cb, pk);
+                rpart[128 * h + r] = rs;
+                tc_fence_before();
+                grp_sync();  // every thread has read its QK columns before any A column is written
+                tc_fence_after();
+                tmem_st16(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + kFX + 32 * h,
+                          *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
+                tmem_st16(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + kFX + 32 * h + 16,
+                          *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
+                tmem_st_wait();
             }
-            tmem_st_wait();
             tc_fence_before();
-            wg_sync();
-            if (t == 0) mbar_arrive(&bar->a_ready);
-            // (d) den, g, P = dO / den (in place over dO), store (den, g)
-            if (!wg_all(mbar_wait(&bar->o_done, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
+            grp_sync();
+            if (ct == 0) mbar_arrive(&bar->a_ready);
+            // (d) den; P = dO / den (in place, bf16); g = -P . num / den from that bf16 P
+            if (!grp_all(mbar_wait(&bar->o_done, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
             tc_fence_after();
-            const bool valid = r < n;
-            const float den = valid ? rs + den_inter : 1.f;
+            const float den = valid ? rpart[r] + rpart[128 + r] + dpart[r] + dpart[128 + r] : 1.f;
             const float inv = 1.f / den;
-            float dot = 0.f;
+            {
+                uint32_t w[64];
+                tmem_ld64(tmem + lb + kFY, w);
+                float dot = 0.f;
 #pragma unroll
-            for (int cb = 0; cb < 4; ++cb) {
-                uint32_t w[32];
-                tmem_ld32(tmem + lb + kFY + 32 * cb, w);
-                tmem_ld_wait();
-#pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    uint4* pp = reinterpret_cast<uint4*>(sP + chunk_off(r, 4 * cb + q4));
+                for (int c8 = 0; c8 < 8; ++c8) {
+                    uint4* pp = reinterpret_cast<uint4*>(sP + chunk_off(r, 8 * h + c8));
                     uint4 v4 = *pp;
                     uint32_t* u = reinterpret_cast<uint32_t*>(&v4);
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         u[e] = pack_bf16x2(bf_lo(u[e]) * inv, bf_hi(u[e]) * inv);
-                        dot += bf_lo(u[e]) * __uint_as_float(w[8 * q4 + 2 * e]) +
-                               bf_hi(u[e]) * __uint_as_float(w[8 * q4 + 2 * e + 1]);
+                        dot += bf_lo(u[e]) * __uint_as_float(w[8 * c8 + 2 * e]) +
+                               bf_hi(u[e]) * __uint_as_float(w[8 * c8 + 2 * e + 1]);
                     }
                     *pp = v4;
                 }
-            }
-            // g = -P.o with the bf16 P the products use (o = num / den)
-            const float g = valid ? -dot * inv : 0.f;
-            gsh[r] = g;
-            if (valid) {
-                dgh[(size_t)(c0 + r) * 2 + 0] = den;
-                dgh[(size_t)(c0 + r) * 2 + 1] = g;
+                tpart[128 * h + r] = dot;
             }
             fence_proxy_async_smem();
+            grp_sync();
+            const float g = valid ? -(tpart[r] + tpart[128 + r]) * inv : 0.f;
+            if (h == 0) {
+                gsh[r] = g;
+                if (valid) *reinterpret_cast<float2*>(dgh + (size_t)(c0 + r) * 2) = make_float2(den, g);
+            }
             tc_fence_before();
-            wg_sync();
-            if (t == 0) mbar_arrive(&bar->p_ready);
-            rsh[t] += column_sum(sQ, t, n, gsh);  // segment sum of g phi(q)
-            // (e) D = tril(P V^T + g) as a hi + lo pair of bf16 operands: D_hi in X[0,64),
-            // D_lo in X[64,128).  PV block cb (columns 32cb..32cb+31) gives D_hi columns
-            // 16cb.. and D_lo columns 64+16cb..; loading the blocks in the order 0, 2, 1, 3,
-            // each before the writes that land on it, means every column a thread
-            // overwrites has already been read by that thread.
-            if (!wg_all(mbar_wait(&bar->pv_done, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
+            grp_sync();
+            if (ct == 0) mbar_arrive(&bar->p_ready);
+            {
+                // segment sum of g phi(q): weighted column sums of the Q tile
+                float zp[2][8];
+#pragma unroll
+                for (int b = 0; b < 2; ++b)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) zp[b][e] = 0.f;
+#pragma unroll 4
+                for (int j = 0; j < 8; ++j) {
+                    const uint4 qv = *reinterpret_cast<const uint4*>(sQ + grp_vec_off(ct, j));
+                    const uint32_t* u = reinterpret_cast<const uint32_t*>(&qv);
+                    const float wr = gsh[grp_vec_row(ct, j)];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        zp[j >> 2][2 * e] = fmaf(wr, bf_lo(u[e]), zp[j >> 2][2 * e]);
+                        zp[j >> 2][2 * e + 1] = fmaf(wr, bf_hi(u[e]), zp[j >> 2][2 * e + 1]);
+                    }
+                }
+                grp_column_add(zp, racc, ct);
+            }
+            // (e) D = tril(P V^T + g) as hi / lo bf16 pairs into X[32h..] / X[64 + 32h..]
+            if (!grp_all(mbar_wait(&bar->pv_done, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
             tc_fence_after();
             {
-                uint32_t w0[32], w1[32];
-                auto emit = [&](const uint32_t (&w)[32], int cb) {
-                    uint32_t hi[16], lo[16];
+                uint32_t hi[32], lo[32];
 #pragma unroll
-                    for (int x = 0; x < 16; ++x) {
-                        const int j = 32 * cb + 2 * x;
-                        const float d0 = j <= r ? __uint_as_float(w[2 * x]) + g : 0.f;
-                        const float d1 = j + 1 <= r ? __uint_as_float(w[2 * x + 1]) + g : 0.f;
-                        hi[x] = pack_bf16x2(d0, d1);
-                        lo[x] = pack_bf16x2(d0 - bf_lo(hi[x]), d1 - bf_hi(hi[x]));
+                for (int cb = 0; cb < 2; ++cb) {
+                    const int j0 = 64 * h + 32 * cb;
+                    if (j0 > r) {
+#pragma unroll
+                        for (int x = 0; x < 16; ++x) hi[16 * cb + x] = lo[16 * cb + x] = 0u;
+                    } else {
+                        uint32_t w[32];
+                        tmem_ld32(tmem + lb + kFX + 32 * cb, w);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int x = 0; x < 16; ++x) {
+                            const int j = j0 + 2 * x;
+                            const float d0 = j <= r ? __uint_as_float(w[2 * x]) + g : 0.f;
+                            const float d1 = j + 1 <= r ? __uint_as_float(w[2 * x + 1]) + g : 0.f;
+                            hi[16 * cb + x] = pack_bf16x2(d0, d1);
+                            lo[16 * cb + x] = pack_bf16x2(d0 - bf_lo(hi[16 * cb + x]), d1 - bf_hi(hi[16 * cb + x]));
+                        }
                     }
-                    tmem_st16(tmem + lb + kFX + 16 * cb, hi);
-                    tmem_st16(tmem + lb + kFX + 64 + 16 * cb, lo);
-                };
-                tmem_ld32(tmem + lb + kFX + 0, w0);
-                tmem_ld32(tmem + lb + kFX + 64, w1);
-                tmem_ld_wait();
-                emit(w0, 0);                       // writes 0-15, 64-79 (blocks 0, 2 read)
-                tmem_ld32(tmem + lb + kFX + 32, w0);
-                tmem_ld_wait();
-                emit(w0, 1);                       // writes 16-31, 80-95 (block 1 read)
-                tmem_ld32(tmem + lb + kFX + 96, w0);
-                tmem_ld_wait();
-                emit(w1, 2);                       // writes 32-47, 96-111 (block 3 read)
-                emit(w0, 3);                       // writes 48-63, 112-127
+                }
+                tc_fence_before();
+                grp_sync();  // every thread has read its P V^T columns before any D column is written
+                tc_fence_after();
+                const uint32_t row_base = ((uint32_t)(32 * (warp & 3)) << 16) + kFX;
+                tmem_st16(row_base + 32 * h, *reinterpret_cast<uint32_t(*)[16]>(&hi[0]));
+                tmem_st16(row_base + 32 * h + 16, *reinterpret_cast<uint32_t(*)[16]>(&hi[16]));
+                tmem_st16(row_base + 64 + 32 * h, *reinterpret_cast<uint32_t(*)[16]>(&lo[0]));
+                tmem_st16(row_base + 64 + 32 * h + 16, *reinterpret_cast<uint32_t(*)[16]>(&lo[16]));
+                tmem_st_wait();
             }
-            tmem_st_wait();
             tc_fence_before();
-            wg_sync();
-            if (t == 0) mbar_arrive(&bar->d_ready);
-            // (f) dq = (dQ~ + g z_prev) * phi'(q)
-            if (!wg_all(mbar_wait(&bar->dq_done, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
+            grp_sync();
+            if (ct == 0) mbar_arrive(&bar->d_ready);
+            // (f) dq = (dQ~ + g z_prev) * phi'(q), this thread's 64 columns
+            if (!grp_all(mbar_wait(&bar->dq_done, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
             tc_fence_after();
-            __nv_bfloat16* drow = dq + ((size_t)bh * N + c0 + r) * kD;
-#pragma unroll
-            for (int cb = 0; cb < 4; ++cb) {
-                uint32_t w[32];
-                tmem_ld32(tmem + lb + kFY + 32 * cb, w);
-                tmem_ld_wait();
+            {
+                uint32_t w[64];
+                tmem_ld64(tmem + lb + kFY, w);
                 if (valid) {
+                    __nv_bfloat16* drow = dq + ((size_t)bh * N + c0 + r) * kD + 64 * h;
 #pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) {
-                        const uint4 qv = *reinterpret_cast<const uint4*>(sQ + chunk_off(r, 4 * cb + q4));
+                    for (int c8 = 0; c8 < 8; ++c8) {
+                        const uint4 qv = *reinterpret_cast<const uint4*>(sQ + chunk_off(r, 8 * h + c8));
                         const uint32_t* qu = reinterpret_cast<const uint32_t*>(&qv);
                         uint4 o4;
                         uint32_t* ou = reinterpret_cast<uint32_t*>(&o4);
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            const int d = 32 * cb + 8 * q4 + 2 * e;
-                            const float a0 = (__uint_as_float(w[8 * q4 + 2 * e]) + g * zsh[d]) * dphi_from_phi(bf_lo(qu[e]));
+                            const int d = 64 * h + 8 * c8 + 2 * e;
+                            const float a0 = (__uint_as_float(w[8 * c8 + 2 * e]) + g * zsh[d]) * dphi_from_phi(bf_lo(qu[e]));
                             const float a1 =
-                                (__uint_as_float(w[8 * q4 + 2 * e + 1]) + g * zsh[d + 1]) * dphi_from_phi(bf_hi(qu[e]));
+                                (__uint_as_float(w[8 * c8 + 2 * e + 1]) + g * zsh[d + 1]) * dphi_from_phi(bf_hi(qu[e]));
                             ou[e] = pack_bf16x2(a0, a1);
                         }
-                        *reinterpret_cast<uint4*>(drow + 32 * cb + 8 * q4) = o4;
+                        *reinterpret_cast<uint4*>(drow + 8 * c8) = o4;
                     }
                 }
             }
             tc_fence_before();
-            wg_sync();
-            zsh[t] += zc;
-            wg_sync();
-            if (t == 0) mbar_arrive(&bar->empty);
+            grp_sync();
+            if (ct < 128) {
+                zsh[ct] += zacc[ct];
+                zacc[ct] = 0.f;
+            }
+            grp_sync();
+            if (ct == 0) mbar_arrive(&bar->empty);
         }
         // segment sums of the reverse state out: R from TMEM, r from shared memory
-        if (ok && nloc > 0 && wg_all(mbar_wait(&bar->final_mma, 0, err, LA_ERR_TIMEOUT))) {
+        if (ok && nloc > 0 && grp_all(mbar_wait(&bar->final_mma, 0, err, LA_ERR_TIMEOUT))) {
             tc_fence_after();
             float* out = seg_R + ((size_t)bh * P + p) * E;
-            tmem_row_to_global(tmem + lb + kFR, out + (size_t)r * kD);
-            out[(size_t)kD * kD + t] = rsh[t];
+            uint32_t w[64];
+            tmem_ld64(tmem + lb + kFR, w);
+#pragma unroll
+            for (int x = 0; x < 64; x += 4)
+                *reinterpret_cast<float4*>(out + (size_t)r * kD + 64 * h + x) = make_float4(
+                    __uint_as_float(w[x]), __uint_as_float(w[x + 1]), __uint_as_float(w[x + 2]), __uint_as_float(w[x + 3]));
+            if (ct < 128) out[(size_t)kD * kD + ct] = racc[ct];
         }
         tc_fence_before();
     }
@@ -372,14 +445,15 @@ constexpr uint32_t kRR = 0, kRDK = 128, kRDV = 256, kRX = 384;
 struct RevSweepBars {
     uint64_t full, empty;
     uint64_t ready, rb_ready, masks_ready;
-    uint64_t at_done, dt_done, dkv_done;
+    uint64_t at_dt_done, dkv_done;
     uint64_t final_mma;
 };
 
 struct RevSweepSmem {
     static constexpr int Q = 0, K = kTileBytes, V = 2 * kTileBytes, P = 3 * kTileBytes, Rb = 4 * kTileBytes;
     static constexpr int rsh = 5 * kTileBytes;  // float[128] r_next
-    static constexpr int gsh = rsh + 512;       // float[128] g of the chunk's rows
+    static constexpr int racc = rsh + 512;      // float[128] this chunk's sum of g phi(q)
+    static constexpr int gsh = racc + 512;      // float[128] g of the chunk's rows
     static constexpr int ish = gsh + 512;       // float[128] 1/den of the chunk's rows
     static constexpr int bars = ish + 512;
     static constexpr int tmem_slot = bars + 256;
@@ -400,6 +474,7 @@ tc_bwd_reverse_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
     uint8_t* sP = base + RevSweepSmem::P;
     uint8_t* sRb = base + RevSweepSmem::Rb;
     float* rsh = reinterpret_cast<float*>(base + RevSweepSmem::rsh);
+    float* racc = reinterpret_cast<float*>(base + RevSweepSmem::racc);
     float* gsh = reinterpret_cast<float*>(base + RevSweepSmem::gsh);
     float* ish = reinterpret_cast<float*>(base + RevSweepSmem::ish);
     RevSweepBars* bar = reinterpret_cast<RevSweepBars*>(base + RevSweepSmem::bars);
@@ -461,11 +536,10 @@ tc_bwd_reverse_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)  // DV region = A^T = K~ Q~^T (rows = keys)
                     mma_ss(tmem + kRDV, desc_kmajor(aK, kk), desc_kmajor(aQ, kk), id_kk, kk > 0);
-                mma_commit(&bar->at_done);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)  // DK region = V P^T (rows = keys)
                     mma_ss(tmem + kRDK, desc_kmajor(aV, kk), desc_kmajor(aP, kk), id_kk, kk > 0);
-                mma_commit(&bar->dt_done);
+                mma_commit(&bar->at_dt_done);
                 if (!mbar_wait(&bar->rb_ready, ph, err, LA_ERR_TIMEOUT)) break;
                 if (!mbar_wait(&bar->masks_ready, ph, err, LA_ERR_TIMEOUT)) break;
                 tc_fence_after();
@@ -490,129 +564,147 @@ tc_bwd_reverse_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
             mbar_wait(&bar->final_mma, 0, err, LA_ERR_TIMEOUT);
         }
     } else {
-        const int t = tid - 64;
+        const int ct = tid - 64;
+        const int h = (warp - 2) >> 2;
         const int r = 32 * (warp & 3) + lane;
-        const uint32_t lb = (uint32_t)(32 * (warp & 3)) << 16;
+        const uint32_t lane0 = (uint32_t)(32 * (warp & 3)) << 16;
+        const uint32_t lb = lane0 + 64 * h;
         const float* suf = seg_R + ((size_t)bh * P + p) * E;
-        global_row_to_tmem(suf + (size_t)r * kD, tmem + lb + kRR);
-        rsh[r] = suf[(size_t)kD * kD + r];
+        {
+            uint32_t w[64];
+#pragma unroll
+            for (int x = 0; x < 64; x += 4) {
+                const float4 f = *reinterpret_cast<const float4*>(suf + (size_t)r * kD + 64 * h + x);
+                w[x] = __float_as_uint(f.x);
+                w[x + 1] = __float_as_uint(f.y);
+                w[x + 2] = __float_as_uint(f.z);
+                w[x + 3] = __float_as_uint(f.w);
+            }
+            tmem_st32(tmem + lb + kRR, *reinterpret_cast<uint32_t(*)[32]>(&w[0]));
+            tmem_st32(tmem + lb + kRR + 32, *reinterpret_cast<uint32_t(*)[32]>(&w[32]));
+            tmem_st_wait();
+        }
+        if (ct < 128) {
+            rsh[ct] = suf[(size_t)kD * kD + ct];
+            racc[ct] = 0.f;
+        }
         tc_fence_before();
-        bool ok = wg_all(true);
+        bool ok = grp_all(true);
         const float* dgh = den_g + (size_t)bh * N * 2;
         for (int i = 0; i < nloc && ok; ++i) {
             const uint32_t ph = i & 1;
             const int c0 = (cend - 1 - i) * kC, n = min(kC, N - c0);
-            // (a) per-row 1/den and g; phi on Q and K; P = dO / den in place
-            if (!wg_all(mbar_wait(&bar->full, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
-            {
-                const bool valid = t < n;
-                ish[t] = valid ? 1.f / dgh[(size_t)(c0 + t) * 2 + 0] : 0.f;
-                gsh[t] = valid ? dgh[(size_t)(c0 + t) * 2 + 1] : 0.f;
+            // (a) per-row 1/den and g; phi on Q (with the chunk's sum of g phi(q)) and K; P = dO / den
+            if (!grp_all(mbar_wait(&bar->full, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
+            if (ct < 128) {
+                const bool v = ct < n;
+                const float2 dg = v ? *reinterpret_cast<const float2*>(dgh + (size_t)(c0 + ct) * 2) : make_float2(1.f, 0.f);
+                ish[ct] = v ? 1.f / dg.x : 0.f;
+                gsh[ct] = dg.y;
             }
-            wg_sync();
-            phi_tile(sQ, t, n);
-            phi_tile(sK, t, n);
-            scale_rows_tile(sP, t, ish);
+            grp_sync();
+            grp_phi_tile(sQ, nullptr, ct, n, gsh, racc);
+            grp_phi_tile(sK, nullptr, ct, n, nullptr, nullptr);
+            grp_scale_rows(sP, ct, ish);
             fence_proxy_async_smem();
-            wg_sync();
-            if (t == 0) mbar_arrive(&bar->ready);
-            const float rc = column_sum(sQ, t, n, gsh);  // this chunk's sum of g phi(q), column t
-            // (b) R_next -> bf16 copy (rows = dk)
+            grp_sync();
+            if (ct == 0) mbar_arrive(&bar->ready);
+            // (b) R_next -> bf16 copy (rows = dk; this thread's 64 columns)
             if (i > 0) {
-                if (!wg_all(mbar_wait(&bar->dkv_done, (i - 1) & 1, err, LA_ERR_TIMEOUT))) { ok = false; break; }
+                if (!grp_all(mbar_wait(&bar->dkv_done, (i - 1) & 1, err, LA_ERR_TIMEOUT))) { ok = false; break; }
                 tc_fence_after();
             }
-            tmem_row_to_tile(tmem + lb + kRR, sRb, r);
+            {
+                uint32_t w[64];
+                tmem_ld64(tmem + lb + kRR, w);
+                row64_to_tile(w, sRb, r, h);
+            }
             tc_fence_before();
             fence_proxy_async_smem();
-            wg_sync();
-            if (t == 0) mbar_arrive(&bar->rb_ready);
-            // (c) masks: row r is key j = r; column x is query i = x; keep j <= i
-            if (!wg_all(mbar_wait(&bar->at_done, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
+            grp_sync();
+            if (ct == 0) mbar_arrive(&bar->rb_ready);
+            // (c) masks: row r is key j = r; columns [64h, 64h+64) are queries; keep j <= i
+            if (!grp_all(mbar_wait(&bar->at_dt_done, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
             tc_fence_after();
 #pragma unroll
-            for (int cb = 0; cb < 4; ++cb) {
-                uint32_t w[32], pk[16];
-                tmem_ld32(tmem + lb + kRDV + 32 * cb, w);
-                tmem_ld_wait();
+            for (int cb = 0; cb < 2; ++cb) {
+                const int q0 = 64 * h + 32 * cb;  // first query of this block
+                uint32_t pa[16], pd[16];
+                if (q0 + 31 < r) {  // every query here is before key r: all masked
 #pragma unroll
-                for (int x = 0; x < 16; ++x) {
-                    const int qi = 32 * cb + 2 * x;
-                    pk[x] = pack_bf16x2(r <= qi ? __uint_as_float(w[2 * x]) : 0.f,
-                                        r <= qi + 1 ? __uint_as_float(w[2 * x + 1]) : 0.f);
+                    for (int x = 0; x < 16; ++x) pa[x] = pd[x] = 0u;
+                } else {
+                    uint32_t wa[32], wd[32];
+                    tmem_ld32(tmem + lb + kRDV + 32 * cb, wa);
+                    tmem_ld32(tmem + lb + kRDK + 32 * cb, wd);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int x = 0; x < 16; ++x) {
+                        const int qi = q0 + 2 * x;
+                        pa[x] = pack_bf16x2(r <= qi ? __uint_as_float(wa[2 * x]) : 0.f,
+                                            r <= qi + 1 ? __uint_as_float(wa[2 * x + 1]) : 0.f);
+                        pd[x] = pack_bf16x2(r <= qi ? __uint_as_float(wd[2 * x]) + gsh[qi] : 0.f,
+                                            r <= qi + 1 ? __uint_as_float(wd[2 * x + 1]) + gsh[qi + 1] : 0.f);
+                    }
                 }
-                tmem_st16(tmem + lb + kRX + 64 + 16 * cb, pk);
-            }
-            if (!wg_all(mbar_wait(&bar->dt_done, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
-            tc_fence_after();
-#pragma unroll
-            for (int cb = 0; cb < 4; ++cb) {
-                uint32_t w[32], pk[16];
-                tmem_ld32(tmem + lb + kRDK + 32 * cb, w);
-                tmem_ld_wait();
-#pragma unroll
-                for (int x = 0; x < 16; ++x) {
-                    const int qi = 32 * cb + 2 * x;
-                    pk[x] = pack_bf16x2(r <= qi ? __uint_as_float(w[2 * x]) + gsh[qi] : 0.f,
-                                        r <= qi + 1 ? __uint_as_float(w[2 * x + 1]) + gsh[qi + 1] : 0.f);
-                }
-                tmem_st16(tmem + lb + kRX + 16 * cb, pk);
+                tmem_st16(lane0 + tmem + kRX + 64 + 32 * h + 16 * cb, pa);
+                tmem_st16(lane0 + tmem + kRX + 32 * h + 16 * cb, pd);
             }
             tmem_st_wait();
             tc_fence_before();
-            wg_sync();
-            if (t == 0) mbar_arrive(&bar->masks_ready);
-            // (d) dk = (dK~ + r_next) * phi'(k), dv
-            if (!wg_all(mbar_wait(&bar->dkv_done, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
+            grp_sync();
+            if (ct == 0) mbar_arrive(&bar->masks_ready);
+            // (d) dk = (dK~ + r_next) * phi'(k), dv; this thread's 64 columns of key row r
+            if (!grp_all(mbar_wait(&bar->dkv_done, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
             tc_fence_after();
             const bool valid = r < n;
-            __nv_bfloat16* dkrow = dk + ((size_t)bh * N + c0 + r) * kD;
-            __nv_bfloat16* dvrow = dv + ((size_t)bh * N + c0 + r) * kD;
-#pragma unroll
-            for (int cb = 0; cb < 4; ++cb) {
-                uint32_t w[32];
-                tmem_ld32(tmem + lb + kRDK + 32 * cb, w);
-                tmem_ld_wait();
+            {
+                uint32_t w[64];
+                tmem_ld64(tmem + lb + kRDK, w);
                 if (valid) {
+                    __nv_bfloat16* dkrow = dk + ((size_t)bh * N + c0 + r) * kD + 64 * h;
 #pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) {
-                        const uint4 kv = *reinterpret_cast<const uint4*>(sK + chunk_off(r, 4 * cb + q4));
+                    for (int c8 = 0; c8 < 8; ++c8) {
+                        const uint4 kv = *reinterpret_cast<const uint4*>(sK + chunk_off(r, 8 * h + c8));
                         const uint32_t* ku = reinterpret_cast<const uint32_t*>(&kv);
                         uint4 o4;
                         uint32_t* ou = reinterpret_cast<uint32_t*>(&o4);
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            const int d = 32 * cb + 8 * q4 + 2 * e;
-                            ou[e] = pack_bf16x2((__uint_as_float(w[8 * q4 + 2 * e]) + rsh[d]) * dphi_from_phi(bf_lo(ku[e])),
-                                                (__uint_as_float(w[8 * q4 + 2 * e + 1]) + rsh[d + 1]) *
+                            const int d = 64 * h + 8 * c8 + 2 * e;
+                            ou[e] = pack_bf16x2((__uint_as_float(w[8 * c8 + 2 * e]) + rsh[d]) * dphi_from_phi(bf_lo(ku[e])),
+                                                (__uint_as_float(w[8 * c8 + 2 * e + 1]) + rsh[d + 1]) *
                                                     dphi_from_phi(bf_hi(ku[e])));
                         }
-                        *reinterpret_cast<uint4*>(dkrow + 32 * cb + 8 * q4) = o4;
+                        *reinterpret_cast<uint4*>(dkrow + 8 * c8) = o4;
                     }
                 }
             }
-#pragma unroll
-            for (int cb = 0; cb < 4; ++cb) {
-                uint32_t w[32];
-                tmem_ld32(tmem + lb + kRDV + 32 * cb, w);
-                tmem_ld_wait();
+            {
+                uint32_t w[64];
+                tmem_ld64(tmem + lb + kRDV, w);
                 if (valid) {
+                    __nv_bfloat16* dvrow = dv + ((size_t)bh * N + c0 + r) * kD + 64 * h;
 #pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) {
+                    for (int c8 = 0; c8 < 8; ++c8) {
                         uint4 o4;
-                        o4.x = pack_bf16x2(__uint_as_float(w[8 * q4 + 0]), __uint_as_float(w[8 * q4 + 1]));
-                        o4.y = pack_bf16x2(__uint_as_float(w[8 * q4 + 2]), __uint_as_float(w[8 * q4 + 3]));
-                        o4.z = pack_bf16x2(__uint_as_float(w[8 * q4 + 4]), __uint_as_float(w[8 * q4 + 5]));
-                        o4.w = pack_bf16x2(__uint_as_float(w[8 * q4 + 6]), __uint_as_float(w[8 * q4 + 7]));
-                        *reinterpret_cast<uint4*>(dvrow + 32 * cb + 8 * q4) = o4;
+                        o4.x = pack_bf16x2(__uint_as_float(w[8 * c8 + 0]), __uint_as_float(w[8 * c8 + 1]));
+                        o4.y = pack_bf16x2(__uint_as_float(w[8 * c8 + 2]), __uint_as_float(w[8 * c8 + 3]));
+                        o4.z = pack_bf16x2(__uint_as_float(w[8 * c8 + 4]), __uint_as_float(w[8 * c8 + 5]));
+                        o4.w = pack_bf16x2(__uint_as_float(w[8 * c8 + 6]), __uint_as_float(w[8 * c8 + 7]));
+                        *reinterpret_cast<uint4*>(dvrow + 8 * c8) = o4;
                     }
                 }
             }
             tc_fence_before();
-            wg_sync();
-            rsh[t] += rc;
-            wg_sync();
-            if (t == 0) mbar_arrive(&bar->empty);
+            // (e) r_next += this chunk's sum of g phi(q) (after every thread has used r_next)
+            grp_sync();
+            if (ct < 128) {
+                rsh[ct] += racc[ct];
+                racc[ct] = 0.f;
+            }
+            grp_sync();
+            if (ct == 0) mbar_arrive(&bar->empty);
         }
         tc_fence_before();
     }

@@ -200,6 +200,128 @@ __device__ __forceinline__ void tmem_row_to_global(uint32_t taddr, float* dst) {
     }
 }
 
+// ------------------------------------------------------------------ 256-thread compute group
+// Warps 2-9 of a CTA: thread ct = tid - 64.  For row-wise TMEM work, warp w owns
+// TMEM lanes 32*(w%4) .. +31 and column half h = (w - 2) / 4 of those rows.  For
+// whole-tile elementwise work, thread ct owns the 16-byte vectors ct + 256 j
+// (j < 8): block j / 4, row ((ct >> 3) + 32 j) & 127, physical chunk ct & 7,
+// logical chunk lc = (ct & 7) ^ ((ct >> 3) & 7), i.e. columns 64*(j/4) + 8*lc + e.
+constexpr int kGroupThreads = 256;
+
+__device__ __forceinline__ bool grp_all(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, 1, 256, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v)
+        : "memory");
+    return r != 0;
+}
+__device__ __forceinline__ void grp_sync() { named_barrier(1, kGroupThreads); }
+
+__device__ __forceinline__ int grp_vec_row(int ct, int j) { return ((ct >> 3) + 32 * j) & 127; }
+__device__ __forceinline__ int grp_vec_off(int ct, int j) {
+    return (j >> 2) * kBlockBytes + grp_vec_row(ct, j) * 128 + (ct & 7) * 16;
+}
+__device__ __forceinline__ int grp_vec_lc(int ct) { return (ct & 7) ^ ((ct >> 3) & 7); }
+
+// Column partial sums zp[block][e] (for columns 64*block + 8*lc + e of this
+// thread) summed over the four lanes of the warp that share lc (lanes l, l^9,
+// l^18, l^27) and added into dst[128] by lanes 0-7.
+__device__ __forceinline__ void grp_column_add(float (&zp)[2][8], float* dst, int ct) {
+#pragma unroll
+    for (int b = 0; b < 2; ++b)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            float x = zp[b][e];
+            x += __shfl_xor_sync(0xffffffffu, x, 9);
+            x += __shfl_xor_sync(0xffffffffu, x, 18);
+            zp[b][e] = x;
+        }
+    if ((ct & 31) < 8) {
+        const int lc = grp_vec_lc(ct);
+#pragma unroll
+        for (int b = 0; b < 2; ++b)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) atomicAdd(dst + 64 * b + 8 * lc + e, zp[b][e]);
+    }
+}
+
+// phi in place on a staged tile (rows >= n exactly 0) with the column sums of
+// the rounded values (weighted by w[row] when w is given) added into colsum.
+// With lo_tile, also writes lo = bf16(phi - hi) there.
+__device__ __forceinline__ void grp_phi_tile(uint8_t* tile, uint8_t* lo_tile, int ct, int n, const float* w,
+                                             float* colsum) {
+    float zp[2][8];
+#pragma unroll
+    for (int b = 0; b < 2; ++b)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) zp[b][e] = 0.f;
+#pragma unroll 4
+    for (int j = 0; j < 8; ++j) {
+        const int row = grp_vec_row(ct, j);
+        const int off = grp_vec_off(ct, j);
+        uint4 v = *reinterpret_cast<const uint4*>(tile + off);
+        uint32_t* u = reinterpret_cast<uint32_t*>(&v);
+        uint4 l;
+        uint32_t* ul = reinterpret_cast<uint32_t*>(&l);
+        const bool valid = row < n;
+        const float wr = (w && valid) ? w[row] : 1.f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float a = valid ? phi_f(bf_lo(u[e])) : 0.f, b = valid ? phi_f(bf_hi(u[e])) : 0.f;
+            u[e] = pack_bf16x2(a, b);
+            ul[e] = pack_bf16x2(a - bf_lo(u[e]), b - bf_hi(u[e]));
+            if (colsum) {
+                zp[j >> 2][2 * e] = fmaf(wr, bf_lo(u[e]), zp[j >> 2][2 * e]);
+                zp[j >> 2][2 * e + 1] = fmaf(wr, bf_hi(u[e]), zp[j >> 2][2 * e + 1]);
+            }
+        }
+        *reinterpret_cast<uint4*>(tile + off) = v;
+        if (lo_tile) *reinterpret_cast<uint4*>(lo_tile + off) = l;
+    }
+    if (colsum) grp_column_add(zp, colsum, ct);
+}
+
+// Every row of a staged tile scaled by s[row], rounded to bf16, in place.
+__device__ __forceinline__ void grp_scale_rows(uint8_t* tile, int ct, const float* s) {
+#pragma unroll 4
+    for (int j = 0; j < 8; ++j) {
+        const int off = grp_vec_off(ct, j);
+        uint4 v = *reinterpret_cast<const uint4*>(tile + off);
+        uint32_t* u = reinterpret_cast<uint32_t*>(&v);
+        const float f = s[grp_vec_row(ct, j)];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) u[e] = pack_bf16x2(bf_lo(u[e]) * f, bf_hi(u[e]) * f);
+        *reinterpret_cast<uint4*>(tile + off) = v;
+    }
+}
+
+// 64 fp32 TMEM columns (two x32 loads) of this thread's row.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&w)[64]) {
+    uint32_t (&a)[32] = *reinterpret_cast<uint32_t(*)[32]>(&w[0]);
+    uint32_t (&b)[32] = *reinterpret_cast<uint32_t(*)[32]>(&w[32]);
+    tmem_ld32(taddr, a);
+    tmem_ld32(taddr + 32, b);
+    tmem_ld_wait();
+}
+
+// 64 fp32 values -> this row's half (block h, 64 columns) of a bf16 tile.
+__device__ __forceinline__ void row64_to_tile(const uint32_t (&w)[64], uint8_t* tile, int row, int h) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        uint4 v4;
+        v4.x = pack_bf16x2(__uint_as_float(w[8 * q + 0]), __uint_as_float(w[8 * q + 1]));
+        v4.y = pack_bf16x2(__uint_as_float(w[8 * q + 2]), __uint_as_float(w[8 * q + 3]));
+        v4.z = pack_bf16x2(__uint_as_float(w[8 * q + 4]), __uint_as_float(w[8 * q + 5]));
+        v4.w = pack_bf16x2(__uint_as_float(w[8 * q + 6]), __uint_as_float(w[8 * q + 7]));
+        *reinterpret_cast<uint4*>(tile + chunk_off(row, 8 * h + q)) = v4;
+    }
+}
+
 }  // namespace tc
 
 // Host: a [BH][N][D] bf16 tensor as a 3-D TMA map with 64 x box_rows x 1 boxes
