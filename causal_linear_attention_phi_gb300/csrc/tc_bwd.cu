@@ -37,10 +37,13 @@ constexpr int kThreads = 320;
 // Y [384,512): O = phi(Q) S_prev + A V (numerator) -> dQ~.
 constexpr uint32_t kFS = 0, kFR = 128, kFX = 256, kFY = 384;
 
+// Q and V arrive (full_qv) and are released (empty_qv: the MMA's last read of
+// them and the compute group's last read of Q) apart from K and dO (full_kp,
+// empty_kp), so the next chunk's Q and V load during this chunk's D and dq work.
 struct FwdSweepBars {
-    uint64_t full, empty;
+    uint64_t full_qv, empty_qv, full_kp, empty_kp;
     uint64_t qk_ready, sb_ready, a_ready, p_ready, d_ready;
-    uint64_t qk_done, o_done, s_done, pv_done, dq_done;
+    uint64_t qk_done, o_done, pv_done, dq_done;
     uint64_t final_mma;
 };
 
@@ -91,6 +94,7 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
     if (tid == 0) {
         uint64_t* b = reinterpret_cast<uint64_t*>(bar);
         for (int x = 0; x < (int)(sizeof(FwdSweepBars) / 8); ++x) mbar_init(b + x, 1);
+        mbar_init(&bar->empty_qv, 2);  // one MMA commit + one compute-group arrival
         fence_mbar_init();
         tma_prefetch_desc(&tm_q);
         tma_prefetch_desc(&tm_k);
@@ -108,22 +112,27 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
 
     if (warp == 0) {
         if (lane == 0) {
-            int armed = -1;
+            int armed_qv = -1, armed_kp = -1;
             for (int i = 0; i < nloc; ++i) {
                 const int t0 = (cbeg + i) * kC;
-                if (!mbar_wait(&bar->empty, (i & 1) ^ 1, err, LA_ERR_TIMEOUT)) break;
-                mbar_arrive_expect_tx(&bar->full, 4 * kTileBytes);
-                tma_load_3d(sQ, &tm_q, 0, t0, bh, &bar->full);
-                tma_load_3d(sQ + kBlockBytes, &tm_q, 64, t0, bh, &bar->full);
-                tma_load_3d(sK, &tm_k, 0, t0, bh, &bar->full);
-                tma_load_3d(sK + kBlockBytes, &tm_k, 64, t0, bh, &bar->full);
-                tma_load_3d(sV, &tm_v, 0, t0, bh, &bar->full);
-                tma_load_3d(sV + kBlockBytes, &tm_v, 64, t0, bh, &bar->full);
-                tma_load_3d(sP, &tm_do, 0, t0, bh, &bar->full);
-                tma_load_3d(sP + kBlockBytes, &tm_do, 64, t0, bh, &bar->full);
-                armed = i;
+                if (!mbar_wait(&bar->empty_qv, (i & 1) ^ 1, err, LA_ERR_TIMEOUT)) break;
+                mbar_arrive_expect_tx(&bar->full_qv, 2 * kTileBytes);
+                tma_load_3d(sQ, &tm_q, 0, t0, bh, &bar->full_qv);
+                tma_load_3d(sQ + kBlockBytes, &tm_q, 64, t0, bh, &bar->full_qv);
+                tma_load_3d(sV, &tm_v, 0, t0, bh, &bar->full_qv);
+                tma_load_3d(sV + kBlockBytes, &tm_v, 64, t0, bh, &bar->full_qv);
+                armed_qv = i;
+                if (!mbar_wait(&bar->empty_kp, (i & 1) ^ 1, err, LA_ERR_TIMEOUT)) break;
+                mbar_arrive_expect_tx(&bar->full_kp, 2 * kTileBytes);
+                tma_load_3d(sK, &tm_k, 0, t0, bh, &bar->full_kp);
+                tma_load_3d(sK + kBlockBytes, &tm_k, 64, t0, bh, &bar->full_kp);
+                tma_load_3d(sP, &tm_do, 0, t0, bh, &bar->full_kp);
+                tma_load_3d(sP + kBlockBytes, &tm_do, 64, t0, bh, &bar->full_kp);
+                armed_kp = i;
             }
-            if (armed >= 0) mbar_wait(&bar->full, armed & 1, err, LA_ERR_TIMEOUT);
+            // no copy may still be landing when the CTA exits
+            if (armed_qv >= 0) mbar_wait(&bar->full_qv, armed_qv & 1, err, LA_ERR_TIMEOUT);
+            if (armed_kp >= 0) mbar_wait(&bar->full_kp, armed_kp & 1, err, LA_ERR_TIMEOUT);
         }
     } else if (warp == 1) {
         if (lane == 0) {
@@ -134,17 +143,17 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
                            aP = smem_u32(sP), aSb = smem_u32(sSb);
             for (int i = 0; i < nloc; ++i) {
                 const uint32_t ph = i & 1;
+                if (!mbar_wait(&bar->sb_ready, ph, err, LA_ERR_TIMEOUT)) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)  // Y = Q~ S_prev (needs phi(Q) and S_prev only)
+                    mma_ss(tmem + kFY, desc_kmajor(aQ, kk), desc_mnmajor(aSb, kk), id_kmn, kk > 0);
                 if (!mbar_wait(&bar->qk_ready, ph, err, LA_ERR_TIMEOUT)) break;
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)  // X = Q~ K~^T
                     mma_ss(tmem + kFX, desc_kmajor(aQ, kk), desc_kmajor(aK, kk), id_kk, kk > 0);
                 mma_commit(&bar->qk_done);
-                if (!mbar_wait(&bar->sb_ready, ph, err, LA_ERR_TIMEOUT)) break;
-                tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)  // Y = Q~ S_prev
-                    mma_ss(tmem + kFY, desc_kmajor(aQ, kk), desc_mnmajor(aSb, kk), id_kmn, kk > 0);
                 if (!mbar_wait(&bar->a_ready, ph, err, LA_ERR_TIMEOUT)) break;
                 tc_fence_after();
 #pragma unroll
@@ -154,7 +163,6 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)  // S += K~^T V
                     mma_ss(tmem + kFS, desc_mnmajor(aK, kk), desc_mnmajor(aV, kk), id_mnmn, 1);
-                mma_commit(&bar->s_done);
                 if (!mbar_wait(&bar->p_ready, ph, err, LA_ERR_TIMEOUT)) break;
                 tc_fence_after();
 #pragma unroll
@@ -164,6 +172,7 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)  // R += Q~^T P
                     mma_ss(tmem + kFR, desc_mnmajor(aQ, kk), desc_mnmajor(aP, kk), id_mnmn, (i > 0 || kk > 0));
+                mma_commit(&bar->empty_qv);  // last MMA read of Q and V in this chunk
                 if (!mbar_wait(&bar->d_ready, ph, err, LA_ERR_TIMEOUT)) break;
                 tc_fence_after();
 #pragma unroll
@@ -176,6 +185,7 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
                     mma_ts(tmem + kFY, tmem + kFX + 8 * kk, desc_mnmajor(aKLo, kk), id_kmn, 1);
                 }
                 mma_commit(&bar->dq_done);
+                mma_commit(&bar->empty_kp);  // last read of K, K_lo and P
             }
             mma_commit(&bar->final_mma);
             mbar_wait(&bar->final_mma, 0, err, LA_ERR_TIMEOUT);
@@ -186,21 +196,7 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
         const int r = 32 * (warp & 3) + lane;
         const uint32_t lb = ((uint32_t)(32 * (warp & 3)) << 16) + 64 * h;  // this thread's row half
         const float* pre = seg_S + ((size_t)bh * P + p) * E;
-        {
-            // S_prev row r (this half) into TMEM; z_prev
-            uint32_t w[64];
-#pragma unroll
-            for (int x = 0; x < 64; x += 4) {
-                const float4 f = *reinterpret_cast<const float4*>(pre + (size_t)r * kD + 64 * h + x);
-                w[x] = __float_as_uint(f.x);
-                w[x + 1] = __float_as_uint(f.y);
-                w[x + 2] = __float_as_uint(f.z);
-                w[x + 3] = __float_as_uint(f.w);
-            }
-            tmem_st32(tmem + lb + kFS, *reinterpret_cast<uint32_t(*)[32]>(&w[0]));
-            tmem_st32(tmem + lb + kFS + 32, *reinterpret_cast<uint32_t(*)[32]>(&w[32]));
-            tmem_st_wait();
-        }
+        global_row_to_tmem<64>(pre + (size_t)r * kD + 64 * h, tmem + lb + kFS);  // S_prev row r, this half
         if (ct < 128) {
             zsh[ct] = pre[(size_t)kD * kD + ct];
             zacc[ct] = 0.f;
@@ -213,55 +209,54 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
             const uint32_t ph = i & 1;
             const int c0 = (cbeg + i) * kC, n = min(kC, N - c0);
             const bool valid = r < n;
-            // (a) phi on K (hi in place, lo beside it; column sums of hi into zacc) and on Q
-            if (!grp_all(mbar_wait(&bar->full, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
-            grp_phi_tile(sK, sKLo, ct, n, nullptr, zacc);
+            // (a) phi on Q in place; S_prev -> its bf16 copy (rows = dk; this thread's 64
+            // columns).  S and Y are settled: the previous chunk's dq_done, which follows
+            // every earlier MMA, has been awaited.
+            if (!grp_all(mbar_wait(&bar->full_qv, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
+            tc_fence_after();
             grp_phi_tile(sQ, nullptr, ct, n, nullptr, nullptr);
+            tmem_half_row_to_tile(tmem + lb + kFS, sSb, r, h);
+            tc_fence_before();
             fence_proxy_async_smem();
             grp_sync();
-            if (ct == 0) mbar_arrive(&bar->qk_ready);
+            if (ct == 0) mbar_arrive(&bar->sb_ready);
+            // phi(q_r) on this thread's 64 columns stays in registers for phi'(q) in the dq
+            // epilogue (Q is released before it); phi(q_r) . z_prev
+            uint32_t qrow[32];
             {
-                // phi(q_r) . z_prev over this thread's 64 columns
                 float di = 0.f;
 #pragma unroll
                 for (int c8 = 0; c8 < 8; ++c8) {
                     const int lc = 8 * h + c8;
                     const uint4 qv = *reinterpret_cast<const uint4*>(sQ + chunk_off(r, lc));
-                    const uint32_t* u = reinterpret_cast<const uint32_t*>(&qv);
+                    qrow[4 * c8 + 0] = qv.x;
+                    qrow[4 * c8 + 1] = qv.y;
+                    qrow[4 * c8 + 2] = qv.z;
+                    qrow[4 * c8 + 3] = qv.w;
 #pragma unroll
                     for (int e = 0; e < 4; ++e)
-                        di += bf_lo(u[e]) * zsh[8 * lc + 2 * e] + bf_hi(u[e]) * zsh[8 * lc + 2 * e + 1];
+                        di += bf_lo(qrow[4 * c8 + e]) * zsh[8 * lc + 2 * e] + bf_hi(qrow[4 * c8 + e]) * zsh[8 * lc + 2 * e + 1];
                 }
                 dpart[128 * h + r] = di;
             }
-            // (b) S_prev -> bf16 copy (rows = dk; this thread's 64 columns)
-            if (i > 0) {
-                const bool w1 = mbar_wait(&bar->s_done, (i - 1) & 1, err, LA_ERR_TIMEOUT);
-                const bool w2 = mbar_wait(&bar->dq_done, (i - 1) & 1, err, LA_ERR_TIMEOUT);
-                if (!grp_all(w1 && w2)) { ok = false; break; }
-                tc_fence_after();
-            }
-            {
-                uint32_t w[64];
-                tmem_ld64(tmem + lb + kFS, w);
-                row64_to_tile(w, sSb, r, h);
-            }
-            tc_fence_before();
+            // (b) phi on K: hi in place, lo beside it, column sums of hi into zacc
+            if (!grp_all(mbar_wait(&bar->full_kp, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
+            grp_phi_tile(sK, sKLo, ct, n, nullptr, zacc);
             fence_proxy_async_smem();
             grp_sync();
-            if (ct == 0) mbar_arrive(&bar->sb_ready);
+            if (ct == 0) mbar_arrive(&bar->qk_ready);
             // (c) A = tril(QK^T) on keys [64h, 64h+64) as bf16 pairs into X columns [32h, 32h+32)
             if (!grp_all(mbar_wait(&bar->qk_done, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
             tc_fence_after();
             {
-                uint32_t pk[32];
+                uint32_t pk[2][16];
                 float rs = 0.f;
 #pragma unroll
                 for (int cb = 0; cb < 2; ++cb) {
                     const int j0 = 64 * h + 32 * cb;
                     if (j0 > r) {
 #pragma unroll
-                        for (int x = 0; x < 16; ++x) pk[16 * cb + x] = 0u;
+                        for (int x = 0; x < 16; ++x) pk[cb][x] = 0u;
                     } else {
                         uint32_t w[32];
                         tmem_ld32(tmem + lb + kFX + 32 * cb, w);
@@ -269,9 +264,9 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
 #pragma unroll
                         for (int x = 0; x < 16; ++x) {
                             const int j = j0 + 2 * x;
-                            pk[16 * cb + x] = pack_bf16x2(j <= r ? __uint_as_float(w[2 * x]) : 0.f,
-                                                          j + 1 <= r ? __uint_as_float(w[2 * x + 1]) : 0.f);
-                            rs += bf_lo(pk[16 * cb + x]) + bf_hi(pk[16 * cb + x]);
+                            pk[cb][x] = pack_bf16x2(j <= r ? __uint_as_float(w[2 * x]) : 0.f,
+                                                    j + 1 <= r ? __uint_as_float(w[2 * x + 1]) : 0.f);
+                            rs += bf_lo(pk[cb][x]) + bf_hi(pk[cb][x]);
                         }
                     }
                 }
@@ -279,10 +274,8 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
                 tc_fence_before();
                 grp_sync();  // every thread has read its QK columns before any A column is written
                 tc_fence_after();
-                tmem_st16(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + kFX + 32 * h,
-                          *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
-                tmem_st16(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + kFX + 32 * h + 16,
-                          *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
+                tmem_st16(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + kFX + 32 * h, pk[0]);
+                tmem_st16(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + kFX + 32 * h + 16, pk[1]);
                 tmem_st_wait();
             }
             tc_fence_before();
@@ -294,21 +287,25 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
             const float den = valid ? rpart[r] + rpart[128 + r] + dpart[r] + dpart[128 + r] : 1.f;
             const float inv = 1.f / den;
             {
-                uint32_t w[64];
-                tmem_ld64(tmem + lb + kFY, w);
                 float dot = 0.f;
 #pragma unroll
-                for (int c8 = 0; c8 < 8; ++c8) {
-                    uint4* pp = reinterpret_cast<uint4*>(sP + chunk_off(r, 8 * h + c8));
-                    uint4 v4 = *pp;
-                    uint32_t* u = reinterpret_cast<uint32_t*>(&v4);
+                for (int cb = 0; cb < 2; ++cb) {
+                    uint32_t w[32];
+                    tmem_ld32(tmem + lb + kFY + 32 * cb, w);
+                    tmem_ld_wait();
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        u[e] = pack_bf16x2(bf_lo(u[e]) * inv, bf_hi(u[e]) * inv);
-                        dot += bf_lo(u[e]) * __uint_as_float(w[8 * c8 + 2 * e]) +
-                               bf_hi(u[e]) * __uint_as_float(w[8 * c8 + 2 * e + 1]);
+                    for (int c4 = 0; c4 < 4; ++c4) {
+                        uint4* pp = reinterpret_cast<uint4*>(sP + chunk_off(r, 8 * h + 4 * cb + c4));
+                        uint4 v4 = *pp;
+                        uint32_t* u = reinterpret_cast<uint32_t*>(&v4);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            u[e] = pack_bf16x2(bf_lo(u[e]) * inv, bf_hi(u[e]) * inv);
+                            dot += bf_lo(u[e]) * __uint_as_float(w[8 * c4 + 2 * e]) +
+                                   bf_hi(u[e]) * __uint_as_float(w[8 * c4 + 2 * e + 1]);
+                        }
+                        *pp = v4;
                     }
-                    *pp = v4;
                 }
                 tpart[128 * h + r] = dot;
             }
@@ -329,7 +326,7 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
                 for (int b = 0; b < 2; ++b)
 #pragma unroll
                     for (int e = 0; e < 8; ++e) zp[b][e] = 0.f;
-#pragma unroll 4
+#pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     const uint4 qv = *reinterpret_cast<const uint4*>(sQ + grp_vec_off(ct, j));
                     const uint32_t* u = reinterpret_cast<const uint32_t*>(&qv);
@@ -342,17 +339,19 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
                 }
                 grp_column_add(zp, racc, ct);
             }
+            grp_sync();  // every read of Q by the compute group is done
+            if (ct == 0) mbar_arrive(&bar->empty_qv);
             // (e) D = tril(P V^T + g) as hi / lo bf16 pairs into X[32h..] / X[64 + 32h..]
             if (!grp_all(mbar_wait(&bar->pv_done, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
             tc_fence_after();
             {
-                uint32_t hi[32], lo[32];
+                uint32_t hi[2][16], lo[2][16];
 #pragma unroll
                 for (int cb = 0; cb < 2; ++cb) {
                     const int j0 = 64 * h + 32 * cb;
                     if (j0 > r) {
 #pragma unroll
-                        for (int x = 0; x < 16; ++x) hi[16 * cb + x] = lo[16 * cb + x] = 0u;
+                        for (int x = 0; x < 16; ++x) hi[cb][x] = lo[cb][x] = 0u;
                     } else {
                         uint32_t w[32];
                         tmem_ld32(tmem + lb + kFX + 32 * cb, w);
@@ -362,8 +361,8 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
                             const int j = j0 + 2 * x;
                             const float d0 = j <= r ? __uint_as_float(w[2 * x]) + g : 0.f;
                             const float d1 = j + 1 <= r ? __uint_as_float(w[2 * x + 1]) + g : 0.f;
-                            hi[16 * cb + x] = pack_bf16x2(d0, d1);
-                            lo[16 * cb + x] = pack_bf16x2(d0 - bf_lo(hi[16 * cb + x]), d1 - bf_hi(hi[16 * cb + x]));
+                            hi[cb][x] = pack_bf16x2(d0, d1);
+                            lo[cb][x] = pack_bf16x2(d0 - bf_lo(hi[cb][x]), d1 - bf_hi(hi[cb][x]));
                         }
                     }
                 }
@@ -371,10 +370,10 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
                 grp_sync();  // every thread has read its P V^T columns before any D column is written
                 tc_fence_after();
                 const uint32_t row_base = ((uint32_t)(32 * (warp & 3)) << 16) + kFX;
-                tmem_st16(row_base + 32 * h, *reinterpret_cast<uint32_t(*)[16]>(&hi[0]));
-                tmem_st16(row_base + 32 * h + 16, *reinterpret_cast<uint32_t(*)[16]>(&hi[16]));
-                tmem_st16(row_base + 64 + 32 * h, *reinterpret_cast<uint32_t(*)[16]>(&lo[0]));
-                tmem_st16(row_base + 64 + 32 * h + 16, *reinterpret_cast<uint32_t(*)[16]>(&lo[16]));
+                tmem_st16(row_base + 32 * h, hi[0]);
+                tmem_st16(row_base + 32 * h + 16, hi[1]);
+                tmem_st16(row_base + 64 + 32 * h, lo[0]);
+                tmem_st16(row_base + 64 + 32 * h + 16, lo[1]);
                 tmem_st_wait();
             }
             tc_fence_before();
@@ -383,48 +382,42 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
             // (f) dq = (dQ~ + g z_prev) * phi'(q), this thread's 64 columns
             if (!grp_all(mbar_wait(&bar->dq_done, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
             tc_fence_after();
-            {
-                uint32_t w[64];
-                tmem_ld64(tmem + lb + kFY, w);
-                if (valid) {
-                    __nv_bfloat16* drow = dq + ((size_t)bh * N + c0 + r) * kD + 64 * h;
 #pragma unroll
-                    for (int c8 = 0; c8 < 8; ++c8) {
-                        const uint4 qv = *reinterpret_cast<const uint4*>(sQ + chunk_off(r, 8 * h + c8));
-                        const uint32_t* qu = reinterpret_cast<const uint32_t*>(&qv);
+            for (int cb = 0; cb < 2; ++cb) {
+                uint32_t w[32];
+                tmem_ld32(tmem + lb + kFY + 32 * cb, w);
+                tmem_ld_wait();
+                if (valid) {
+                    __nv_bfloat16* drow = dq + ((size_t)bh * N + c0 + r) * kD + 64 * h + 32 * cb;
+#pragma unroll
+                    for (int c4 = 0; c4 < 4; ++c4) {
+                        const uint32_t* qu = &qrow[4 * (4 * cb + c4)];
                         uint4 o4;
                         uint32_t* ou = reinterpret_cast<uint32_t*>(&o4);
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            const int d = 64 * h + 8 * c8 + 2 * e;
-                            const float a0 = (__uint_as_float(w[8 * c8 + 2 * e]) + g * zsh[d]) * dphi_from_phi(bf_lo(qu[e]));
+                            const int d = 64 * h + 32 * cb + 8 * c4 + 2 * e;
+                            const float a0 = (__uint_as_float(w[8 * c4 + 2 * e]) + g * zsh[d]) * dphi_from_phi(bf_lo(qu[e]));
                             const float a1 =
-                                (__uint_as_float(w[8 * c8 + 2 * e + 1]) + g * zsh[d + 1]) * dphi_from_phi(bf_hi(qu[e]));
+                                (__uint_as_float(w[8 * c4 + 2 * e + 1]) + g * zsh[d + 1]) * dphi_from_phi(bf_hi(qu[e]));
                             ou[e] = pack_bf16x2(a0, a1);
                         }
-                        *reinterpret_cast<uint4*>(drow + 8 * c8) = o4;
+                        *reinterpret_cast<uint4*>(drow + 8 * c4) = o4;
                     }
                 }
             }
             tc_fence_before();
-            grp_sync();
+            grp_sync();  // z_prev has been used by every thread
             if (ct < 128) {
                 zsh[ct] += zacc[ct];
                 zacc[ct] = 0.f;
             }
-            grp_sync();
-            if (ct == 0) mbar_arrive(&bar->empty);
         }
         // segment sums of the reverse state out: R from TMEM, r from shared memory
         if (ok && nloc > 0 && grp_all(mbar_wait(&bar->final_mma, 0, err, LA_ERR_TIMEOUT))) {
             tc_fence_after();
             float* out = seg_R + ((size_t)bh * P + p) * E;
-            uint32_t w[64];
-            tmem_ld64(tmem + lb + kFR, w);
-#pragma unroll
-            for (int x = 0; x < 64; x += 4)
-                *reinterpret_cast<float4*>(out + (size_t)r * kD + 64 * h + x) = make_float4(
-                    __uint_as_float(w[x]), __uint_as_float(w[x + 1]), __uint_as_float(w[x + 2]), __uint_as_float(w[x + 3]));
+            tmem_row_to_global<64>(tmem + lb + kFR, out + (size_t)r * kD + 64 * h);
             if (ct < 128) out[(size_t)kD * kD + ct] = racc[ct];
         }
         tc_fence_before();
@@ -449,9 +442,12 @@ struct RevSweepBars {
     uint64_t final_mma;
 };
 
+// Kc: a copy of phi(K) for phi'(k) in the dk epilogue, so that the inputs are
+// released (by the MMA thread, at dkv_done) while the epilogue still runs.
 struct RevSweepSmem {
     static constexpr int Q = 0, K = kTileBytes, V = 2 * kTileBytes, P = 3 * kTileBytes, Rb = 4 * kTileBytes;
-    static constexpr int rsh = 5 * kTileBytes;  // float[128] r_next
+    static constexpr int Kc = 5 * kTileBytes;
+    static constexpr int rsh = 6 * kTileBytes;  // float[128] r_next
     static constexpr int racc = rsh + 512;      // float[128] this chunk's sum of g phi(q)
     static constexpr int gsh = racc + 512;      // float[128] g of the chunk's rows
     static constexpr int ish = gsh + 512;       // float[128] 1/den of the chunk's rows
@@ -473,6 +469,7 @@ tc_bwd_reverse_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
     uint8_t* sV = base + RevSweepSmem::V;
     uint8_t* sP = base + RevSweepSmem::P;
     uint8_t* sRb = base + RevSweepSmem::Rb;
+    uint8_t* sKc = base + RevSweepSmem::Kc;
     float* rsh = reinterpret_cast<float*>(base + RevSweepSmem::rsh);
     float* racc = reinterpret_cast<float*>(base + RevSweepSmem::racc);
     float* gsh = reinterpret_cast<float*>(base + RevSweepSmem::gsh);
@@ -559,6 +556,7 @@ tc_bwd_reverse_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
                 for (int kk = 0; kk < 8; ++kk)  // R_next += Q~^T P
                     mma_ss(tmem + kRR, desc_mnmajor(aQ, kk), desc_mnmajor(aP, kk), id_mnmn, 1);
                 mma_commit(&bar->dkv_done);
+                mma_commit(&bar->empty);  // Q, K, V, P: no further read in this chunk
             }
             mma_commit(&bar->final_mma);
             mbar_wait(&bar->final_mma, 0, err, LA_ERR_TIMEOUT);
@@ -570,20 +568,7 @@ tc_bwd_reverse_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
         const uint32_t lane0 = (uint32_t)(32 * (warp & 3)) << 16;
         const uint32_t lb = lane0 + 64 * h;
         const float* suf = seg_R + ((size_t)bh * P + p) * E;
-        {
-            uint32_t w[64];
-#pragma unroll
-            for (int x = 0; x < 64; x += 4) {
-                const float4 f = *reinterpret_cast<const float4*>(suf + (size_t)r * kD + 64 * h + x);
-                w[x] = __float_as_uint(f.x);
-                w[x + 1] = __float_as_uint(f.y);
-                w[x + 2] = __float_as_uint(f.z);
-                w[x + 3] = __float_as_uint(f.w);
-            }
-            tmem_st32(tmem + lb + kRR, *reinterpret_cast<uint32_t(*)[32]>(&w[0]));
-            tmem_st32(tmem + lb + kRR + 32, *reinterpret_cast<uint32_t(*)[32]>(&w[32]));
-            tmem_st_wait();
-        }
+        global_row_to_tmem<64>(suf + (size_t)r * kD + 64 * h, tmem + lb + kRR);  // R_next row r, this half
         if (ct < 128) {
             rsh[ct] = suf[(size_t)kD * kD + ct];
             racc[ct] = 0.f;
@@ -604,7 +589,7 @@ tc_bwd_reverse_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
             }
             grp_sync();
             grp_phi_tile(sQ, nullptr, ct, n, gsh, racc);
-            grp_phi_tile(sK, nullptr, ct, n, nullptr, nullptr);
+            grp_phi_tile(sK, nullptr, ct, n, nullptr, nullptr, sKc);
             grp_scale_rows(sP, ct, ish);
             fence_proxy_async_smem();
             grp_sync();
@@ -614,11 +599,7 @@ tc_bwd_reverse_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
                 if (!grp_all(mbar_wait(&bar->dkv_done, (i - 1) & 1, err, LA_ERR_TIMEOUT))) { ok = false; break; }
                 tc_fence_after();
             }
-            {
-                uint32_t w[64];
-                tmem_ld64(tmem + lb + kRR, w);
-                row64_to_tile(w, sRb, r, h);
-            }
+            tmem_half_row_to_tile(tmem + lb + kRR, sRb, r, h);
             tc_fence_before();
             fence_proxy_async_smem();
             grp_sync();
@@ -658,41 +639,45 @@ tc_bwd_reverse_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
             if (!grp_all(mbar_wait(&bar->dkv_done, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
             tc_fence_after();
             const bool valid = r < n;
-            {
-                uint32_t w[64];
-                tmem_ld64(tmem + lb + kRDK, w);
-                if (valid) {
-                    __nv_bfloat16* dkrow = dk + ((size_t)bh * N + c0 + r) * kD + 64 * h;
 #pragma unroll
-                    for (int c8 = 0; c8 < 8; ++c8) {
-                        const uint4 kv = *reinterpret_cast<const uint4*>(sK + chunk_off(r, 8 * h + c8));
+            for (int cb = 0; cb < 2; ++cb) {
+                uint32_t w[32];
+                tmem_ld32(tmem + lb + kRDK + 32 * cb, w);
+                tmem_ld_wait();
+                if (valid) {
+                    __nv_bfloat16* dkrow = dk + ((size_t)bh * N + c0 + r) * kD + 64 * h + 32 * cb;
+#pragma unroll
+                    for (int c4 = 0; c4 < 4; ++c4) {
+                        const uint4 kv = *reinterpret_cast<const uint4*>(sKc + chunk_off(r, 8 * h + 4 * cb + c4));
                         const uint32_t* ku = reinterpret_cast<const uint32_t*>(&kv);
                         uint4 o4;
                         uint32_t* ou = reinterpret_cast<uint32_t*>(&o4);
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            const int d = 64 * h + 8 * c8 + 2 * e;
-                            ou[e] = pack_bf16x2((__uint_as_float(w[8 * c8 + 2 * e]) + rsh[d]) * dphi_from_phi(bf_lo(ku[e])),
-                                                (__uint_as_float(w[8 * c8 + 2 * e + 1]) + rsh[d + 1]) *
+                            const int d = 64 * h + 32 * cb + 8 * c4 + 2 * e;
+                            ou[e] = pack_bf16x2((__uint_as_float(w[8 * c4 + 2 * e]) + rsh[d]) * dphi_from_phi(bf_lo(ku[e])),
+                                                (__uint_as_float(w[8 * c4 + 2 * e + 1]) + rsh[d + 1]) *
                                                     dphi_from_phi(bf_hi(ku[e])));
                         }
-                        *reinterpret_cast<uint4*>(dkrow + 8 * c8) = o4;
+                        *reinterpret_cast<uint4*>(dkrow + 8 * c4) = o4;
                     }
                 }
             }
-            {
-                uint32_t w[64];
-                tmem_ld64(tmem + lb + kRDV, w);
-                if (valid) {
-                    __nv_bfloat16* dvrow = dv + ((size_t)bh * N + c0 + r) * kD + 64 * h;
 #pragma unroll
-                    for (int c8 = 0; c8 < 8; ++c8) {
+            for (int cb = 0; cb < 2; ++cb) {
+                uint32_t w[32];
+                tmem_ld32(tmem + lb + kRDV + 32 * cb, w);
+                tmem_ld_wait();
+                if (valid) {
+                    __nv_bfloat16* dvrow = dv + ((size_t)bh * N + c0 + r) * kD + 64 * h + 32 * cb;
+#pragma unroll
+                    for (int c4 = 0; c4 < 4; ++c4) {
                         uint4 o4;
-                        o4.x = pack_bf16x2(__uint_as_float(w[8 * c8 + 0]), __uint_as_float(w[8 * c8 + 1]));
-                        o4.y = pack_bf16x2(__uint_as_float(w[8 * c8 + 2]), __uint_as_float(w[8 * c8 + 3]));
-                        o4.z = pack_bf16x2(__uint_as_float(w[8 * c8 + 4]), __uint_as_float(w[8 * c8 + 5]));
-                        o4.w = pack_bf16x2(__uint_as_float(w[8 * c8 + 6]), __uint_as_float(w[8 * c8 + 7]));
-                        *reinterpret_cast<uint4*>(dvrow + 8 * c8) = o4;
+                        o4.x = pack_bf16x2(__uint_as_float(w[8 * c4 + 0]), __uint_as_float(w[8 * c4 + 1]));
+                        o4.y = pack_bf16x2(__uint_as_float(w[8 * c4 + 2]), __uint_as_float(w[8 * c4 + 3]));
+                        o4.z = pack_bf16x2(__uint_as_float(w[8 * c4 + 4]), __uint_as_float(w[8 * c4 + 5]));
+                        o4.w = pack_bf16x2(__uint_as_float(w[8 * c4 + 6]), __uint_as_float(w[8 * c4 + 7]));
+                        *reinterpret_cast<uint4*>(dvrow + 8 * c4) = o4;
                     }
                 }
             }
@@ -703,8 +688,6 @@ tc_bwd_reverse_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
                 rsh[ct] += racc[ct];
                 racc[ct] = 0.f;
             }
-            grp_sync();
-            if (ct == 0) mbar_arrive(&bar->empty);
         }
         tc_fence_before();
     }

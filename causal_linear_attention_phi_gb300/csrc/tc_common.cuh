@@ -168,10 +168,11 @@ __device__ __forceinline__ void tmem_row_to_tiles_split(uint32_t taddr, uint8_t*
     }
 }
 
-// fp32 row from global memory into TMEM (initial states).
+// kCols fp32 values of a row from global memory into TMEM columns (initial states).
+template <int kCols = 128>
 __device__ __forceinline__ void global_row_to_tmem(const float* src, uint32_t taddr) {
 #pragma unroll
-    for (int cb = 0; cb < 4; ++cb) {
+    for (int cb = 0; cb < kCols / 32; ++cb) {
         uint32_t w[32];
 #pragma unroll
         for (int x = 0; x < 32; x += 4) {
@@ -186,10 +187,11 @@ __device__ __forceinline__ void global_row_to_tmem(const float* src, uint32_t ta
     tmem_st_wait();
 }
 
-// fp32 TMEM row to global memory.
+// kCols fp32 TMEM columns of a row to global memory.
+template <int kCols = 128>
 __device__ __forceinline__ void tmem_row_to_global(uint32_t taddr, float* dst) {
 #pragma unroll
-    for (int cb = 0; cb < 4; ++cb) {
+    for (int cb = 0; cb < kCols / 32; ++cb) {
         uint32_t w[32];
         tmem_ld32(taddr + 32 * cb, w);
         tmem_ld_wait();
@@ -197,6 +199,30 @@ __device__ __forceinline__ void tmem_row_to_global(uint32_t taddr, float* dst) {
         for (int x = 0; x < 32; x += 4)
             *reinterpret_cast<float4*>(dst + 32 * cb + x) = make_float4(
                 __uint_as_float(w[x]), __uint_as_float(w[x + 1]), __uint_as_float(w[x + 2]), __uint_as_float(w[x + 3]));
+    }
+}
+
+// 32 fp32 values -> logical 16-byte chunks lc0 .. lc0 + 3 of `row` of a bf16 tile.
+__device__ __forceinline__ void row32_to_tile(const uint32_t (&w)[32], uint8_t* tile, int row, int lc0) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint4 v4;
+        v4.x = pack_bf16x2(__uint_as_float(w[8 * q + 0]), __uint_as_float(w[8 * q + 1]));
+        v4.y = pack_bf16x2(__uint_as_float(w[8 * q + 2]), __uint_as_float(w[8 * q + 3]));
+        v4.z = pack_bf16x2(__uint_as_float(w[8 * q + 4]), __uint_as_float(w[8 * q + 5]));
+        v4.w = pack_bf16x2(__uint_as_float(w[8 * q + 6]), __uint_as_float(w[8 * q + 7]));
+        *reinterpret_cast<uint4*>(tile + chunk_off(row, lc0 + q)) = v4;
+    }
+}
+
+// 64 fp32 TMEM columns of this thread's row (column half h) -> the same half of a bf16 tile row.
+__device__ __forceinline__ void tmem_half_row_to_tile(uint32_t taddr, uint8_t* tile, int row, int h) {
+#pragma unroll
+    for (int cb = 0; cb < 2; ++cb) {
+        uint32_t w[32];
+        tmem_ld32(taddr + 32 * cb, w);
+        tmem_ld_wait();
+        row32_to_tile(w, tile, row, 8 * h + 4 * cb);
     }
 }
 
@@ -252,20 +278,22 @@ __device__ __forceinline__ void grp_column_add(float (&zp)[2][8], float* dst, in
 
 // phi in place on a staged tile (rows >= n exactly 0) with the column sums of
 // the rounded values (weighted by w[row] when w is given) added into colsum.
-// With lo_tile, also writes lo = bf16(phi - hi) there.
+// With lo_tile, also writes lo = bf16(phi - hi) there; with copy_tile, a second
+// copy of the rounded phi.
 __device__ __forceinline__ void grp_phi_tile(uint8_t* tile, uint8_t* lo_tile, int ct, int n, const float* w,
-                                             float* colsum) {
+                                             float* colsum, uint8_t* copy_tile = nullptr) {
     float zp[2][8];
 #pragma unroll
     for (int b = 0; b < 2; ++b)
 #pragma unroll
         for (int e = 0; e < 8; ++e) zp[b][e] = 0.f;
-#pragma unroll 4
+    uint4 v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = *reinterpret_cast<const uint4*>(tile + grp_vec_off(ct, j));
+#pragma unroll
     for (int j = 0; j < 8; ++j) {
         const int row = grp_vec_row(ct, j);
-        const int off = grp_vec_off(ct, j);
-        uint4 v = *reinterpret_cast<const uint4*>(tile + off);
-        uint32_t* u = reinterpret_cast<uint32_t*>(&v);
+        uint32_t* u = reinterpret_cast<uint32_t*>(&v[j]);
         uint4 l;
         uint32_t* ul = reinterpret_cast<uint32_t*>(&l);
         const bool valid = row < n;
@@ -280,45 +308,25 @@ __device__ __forceinline__ void grp_phi_tile(uint8_t* tile, uint8_t* lo_tile, in
                 zp[j >> 2][2 * e + 1] = fmaf(wr, bf_hi(u[e]), zp[j >> 2][2 * e + 1]);
             }
         }
-        *reinterpret_cast<uint4*>(tile + off) = v;
-        if (lo_tile) *reinterpret_cast<uint4*>(lo_tile + off) = l;
+        *reinterpret_cast<uint4*>(tile + grp_vec_off(ct, j)) = v[j];
+        if (lo_tile) *reinterpret_cast<uint4*>(lo_tile + grp_vec_off(ct, j)) = l;
+        if (copy_tile) *reinterpret_cast<uint4*>(copy_tile + grp_vec_off(ct, j)) = v[j];
     }
     if (colsum) grp_column_add(zp, colsum, ct);
 }
 
 // Every row of a staged tile scaled by s[row], rounded to bf16, in place.
 __device__ __forceinline__ void grp_scale_rows(uint8_t* tile, int ct, const float* s) {
-#pragma unroll 4
+    uint4 v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = *reinterpret_cast<const uint4*>(tile + grp_vec_off(ct, j));
+#pragma unroll
     for (int j = 0; j < 8; ++j) {
-        const int off = grp_vec_off(ct, j);
-        uint4 v = *reinterpret_cast<const uint4*>(tile + off);
-        uint32_t* u = reinterpret_cast<uint32_t*>(&v);
+        uint32_t* u = reinterpret_cast<uint32_t*>(&v[j]);
         const float f = s[grp_vec_row(ct, j)];
 #pragma unroll
         for (int e = 0; e < 4; ++e) u[e] = pack_bf16x2(bf_lo(u[e]) * f, bf_hi(u[e]) * f);
-        *reinterpret_cast<uint4*>(tile + off) = v;
-    }
-}
-
-// 64 fp32 TMEM columns (two x32 loads) of this thread's row.
-__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&w)[64]) {
-    uint32_t (&a)[32] = *reinterpret_cast<uint32_t(*)[32]>(&w[0]);
-    uint32_t (&b)[32] = *reinterpret_cast<uint32_t(*)[32]>(&w[32]);
-    tmem_ld32(taddr, a);
-    tmem_ld32(taddr + 32, b);
-    tmem_ld_wait();
-}
-
-// 64 fp32 values -> this row's half (block h, 64 columns) of a bf16 tile.
-__device__ __forceinline__ void row64_to_tile(const uint32_t (&w)[64], uint8_t* tile, int row, int h) {
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-        uint4 v4;
-        v4.x = pack_bf16x2(__uint_as_float(w[8 * q + 0]), __uint_as_float(w[8 * q + 1]));
-        v4.y = pack_bf16x2(__uint_as_float(w[8 * q + 2]), __uint_as_float(w[8 * q + 3]));
-        v4.z = pack_bf16x2(__uint_as_float(w[8 * q + 4]), __uint_as_float(w[8 * q + 5]));
-        v4.w = pack_bf16x2(__uint_as_float(w[8 * q + 6]), __uint_as_float(w[8 * q + 7]));
-        *reinterpret_cast<uint4*>(tile + chunk_off(row, 8 * h + q)) = v4;
+        *reinterpret_cast<uint4*>(tile + grp_vec_off(ct, j)) = v[j];
     }
 }
 

@@ -36,7 +36,7 @@ using namespace sm100;
 using namespace tc;
 
 constexpr int kThreads = 320;  // warp 0 TMA, warp 1 MMA, warps 2-9 compute
-constexpr int kComputeThreads = 256;
+constexpr int kComputeThreads = kGroupThreads;
 constexpr int kSmallBytes = 4096;  // a 16-row x 128-column bf16 K-major operand (two 2 KB blocks)
 
 // TMEM column map (512 columns allocated)
@@ -71,39 +71,6 @@ __device__ __forceinline__ uint64_t desc_small(uint32_t base, int kk) {
 // Byte offset of element (0, col) of a 16-row K-major operand (row 0: chunks unswizzled).
 __device__ __forceinline__ int small_row0_off(int col) {
     return (col >> 6) * 2048 + (((col & 63) >> 3) << 4) + ((col & 7) << 1);
-}
-
-__device__ __forceinline__ bool cg_all(bool v) {
-    // barrier over the compute group (named barrier 1) that also ANDs a predicate
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.and.pred q, 1, 256, p;\n\t"
-        "selp.u32 %0, 1, 0, q;\n\t}"
-        : "=r"(r)
-        : "r"((uint32_t)v)
-        : "memory");
-    return r != 0;
-}
-__device__ __forceinline__ void cg_sync() { named_barrier(1, kComputeThreads); }
-
-// phi in place on a staged 128 x 128 bf16 tile, rows >= n set to exactly 0.
-// Compute thread ct (0..255) handles vectors ct + 256 j, j < 8: block j / 4,
-// row ((ct >> 3) + 32 j) & 127, physical chunk ct & 7 (an elementwise map
-// ignores the swizzle, which only permutes chunks within a row).
-__device__ __forceinline__ void phi_tile256(uint8_t* tile, int ct, int n) {
-#pragma unroll 4
-    for (int j = 0; j < 8; ++j) {
-        const int row = ((ct >> 3) + 32 * j) & 127;
-        uint4* p = reinterpret_cast<uint4*>(tile + (j >> 2) * kBlockBytes + row * 128 + (ct & 7) * 16);
-        uint4 w = *p;
-        uint32_t* u = reinterpret_cast<uint32_t*>(&w);
-        const bool valid = row < n;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) u[e] = valid ? pack_bf16x2(phi_f(bf_lo(u[e])), phi_f(bf_hi(u[e]))) : 0u;
-        *p = w;
-    }
 }
 
 template <bool kOut>
@@ -270,23 +237,23 @@ tc_causal_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             tmem_st_wait();
         }
         tc_fence_before();
-        bool ok = cg_all(true);
+        bool ok = grp_all(true);
         for (int i = 0; i < nloc && ok; ++i) {
             const int s = i & 1;
             const int c0 = (cbeg + i) * kC, n = min(kC, N - c0);
             // (a) phi on the K (and Q) tiles
             bool w = mbar_wait(&bar->kv_full[s], (i >> 1) & 1, err, LA_ERR_TIMEOUT);
             if (kOut) w = w && mbar_wait(&bar->q_full, i & 1, err, LA_ERR_TIMEOUT);
-            if (!cg_all(w)) { ok = false; break; }
-            phi_tile256(sK(s), ct, n);
-            if (kOut) phi_tile256(sQ, ct, n);
+            if (!grp_all(w)) { ok = false; break; }
+            grp_phi_tile(sK(s), nullptr, ct, n, nullptr, nullptr);
+            if (kOut) grp_phi_tile(sQ, nullptr, ct, n, nullptr, nullptr);
             fence_proxy_async_smem();
-            cg_sync();
+            grp_sync();
             if (ct == 0) mbar_arrive(&bar->qk_ready[s]);
             if (!kOut) continue;
             // (b) S_prev, z_prev -> bf16 operands (row r = dk, this thread's 64 dv columns = block h)
             if (i > 0) {
-                if (!cg_all(mbar_wait(&bar->s_done, (i - 1) & 1, err, LA_ERR_TIMEOUT))) { ok = false; break; }
+                if (!grp_all(mbar_wait(&bar->s_done, (i - 1) & 1, err, LA_ERR_TIMEOUT))) { ok = false; break; }
                 tc_fence_after();
             }
 #pragma unroll
@@ -312,10 +279,10 @@ tc_causal_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             }
             tc_fence_before();
             fence_proxy_async_smem();
-            cg_sync();
+            grp_sync();
             if (ct == 0) mbar_arrive(&bar->sb_ready);
             // (c) A = tril(QK^T) on keys [64 h, 64 h + 64) -> bf16 pairs into TMEM columns [32 h, 32 h + 32)
-            if (!cg_all(mbar_wait(&bar->qk_done, i & 1, err, LA_ERR_TIMEOUT))) { ok = false; break; }
+            if (!grp_all(mbar_wait(&bar->qk_done, i & 1, err, LA_ERR_TIMEOUT))) { ok = false; break; }
             tc_fence_after();
 #pragma unroll
             for (int cb = 0; cb < 2; ++cb) {
@@ -343,10 +310,10 @@ tc_causal_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             }
             tmem_st_wait();
             tc_fence_before();
-            cg_sync();
+            grp_sync();
             if (ct == 0) mbar_arrive(&bar->a_ready);
             // (d) o = O / den on this thread's 64 columns
-            if (!cg_all(mbar_wait(&bar->o_done, i & 1, err, LA_ERR_TIMEOUT))) { ok = false; break; }
+            if (!grp_all(mbar_wait(&bar->o_done, i & 1, err, LA_ERR_TIMEOUT))) { ok = false; break; }
             tc_fence_after();
             uint32_t dv[16];
             tmem_ld16(tmem + lane_base + kTmDen, dv);
@@ -375,7 +342,7 @@ tc_causal_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         if (!kOut && ok && nloc > 0) {
             // segment sums out: S row r (this thread's 64 columns) and z[r] from TMEM.  The MMA
             // thread's single-use drain barrier marks the last update done.
-            if (cg_all(mbar_wait(&bar->final_mma, 0, err, LA_ERR_TIMEOUT))) {
+            if (grp_all(mbar_wait(&bar->final_mma, 0, err, LA_ERR_TIMEOUT))) {
                 tc_fence_after();
                 float* out = segp + (size_t)r * kD + 64 * h;
 #pragma unroll
