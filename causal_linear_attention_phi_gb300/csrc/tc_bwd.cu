@@ -33,9 +33,14 @@ constexpr int kThreads = 320;
 
 // ------------------------------------------------------------------ forward sweep
 // TMEM: S [0,128) fp32 state; R [128,256) segment sum of phi(q) P^T;
-// X [256,384): QK^T fp32 -> A bf16 in X[0,64) -> P V^T fp32 -> D as bf16 hi / lo in X[0,64) / X[64,128);
+// X [256,384): QK^T fp32 -> A bf16 -> P V^T fp32 -> D as bf16 hi + lo.  Each 32-key
+// block b of fp32 columns X[32b, 32b+32) is rewritten in place by the thread that
+// read it: A (bf16 pairs) in X[32b, 32b+16), D_hi there and D_lo in X[32b+16, 32b+32);
+// so the MMA's A operand for K step kk (keys 16kk..16kk+15) sits at column
+// 32 (kk / 2) + 8 (kk % 2) (+16 for D_lo).
 // Y [384,512): O = phi(Q) S_prev + A V (numerator) -> dQ~.
 constexpr uint32_t kFS = 0, kFR = 128, kFX = 256, kFY = 384;
+__device__ __forceinline__ uint32_t xcol(int kk) { return 32 * (kk >> 1) + 8 * (kk & 1); }
 
 // Q and V arrive (full_qv) and are released (empty_qv: the MMA's last read of
 // them and the compute group's last read of Q) apart from K and dO (full_kp,
@@ -49,11 +54,12 @@ struct FwdSweepBars {
 
 struct FwdSweepSmem {
     static constexpr int Q = 0, K = kTileBytes, KLo = 2 * kTileBytes, V = 3 * kTileBytes, P = 4 * kTileBytes;
-    static constexpr int Sb = 5 * kTileBytes;
+    static constexpr int Sb = 5 * kTileBytes;   // bf16 S_prev; after the dq products, the dq tile for the TMA store
     static constexpr int zsh = 6 * kTileBytes;  // float[128] z_prev
-    static constexpr int zacc = zsh + 512;      // float[128] this chunk's column sums of phi(k)
-    static constexpr int racc = zacc + 512;     // float[128] segment sum of g phi(q)
-    static constexpr int gsh = racc + 512;      // float[128] g of the chunk's rows
+    static constexpr int zpart = zsh + 512;     // float[8][128] per-warp column sums of this chunk's phi(k)
+    static constexpr int racc = zpart + 4096;   // float[128] segment sum of g phi(q)
+    static constexpr int drpart = racc + 512;   // float[8][128] per-warp column sums of this chunk's g phi(q)
+    static constexpr int gsh = drpart + 4096;   // float[128] g of the chunk's rows
     static constexpr int rpart = gsh + 512;     // float[2][128] row-sum halves of A
     static constexpr int dpart = rpart + 1024;  // float[2][128] halves of phi(q) . z_prev
     static constexpr int tpart = dpart + 1024;  // float[2][128] halves of P . num
@@ -65,7 +71,7 @@ struct FwdSweepSmem {
 __global__ void __launch_bounds__(kThreads, 1)
 tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                             const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                            __nv_bfloat16* __restrict__ dq, const float* __restrict__ seg_S,
+                            const __grid_constant__ CUtensorMap tm_dq, const float* __restrict__ seg_S,
                             float* __restrict__ seg_R, float* __restrict__ den_g, int N, int nchunks, int cps, int P,
                             int* err) {
     extern __shared__ uint8_t smem_raw[];
@@ -77,8 +83,9 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
     uint8_t* sP = base + FwdSweepSmem::P;
     uint8_t* sSb = base + FwdSweepSmem::Sb;
     float* zsh = reinterpret_cast<float*>(base + FwdSweepSmem::zsh);
-    float* zacc = reinterpret_cast<float*>(base + FwdSweepSmem::zacc);
+    float* zpart = reinterpret_cast<float*>(base + FwdSweepSmem::zpart);
     float* racc = reinterpret_cast<float*>(base + FwdSweepSmem::racc);
+    float* drpart = reinterpret_cast<float*>(base + FwdSweepSmem::drpart);
     float* gsh = reinterpret_cast<float*>(base + FwdSweepSmem::gsh);
     float* rpart = reinterpret_cast<float*>(base + FwdSweepSmem::rpart);
     float* dpart = reinterpret_cast<float*>(base + FwdSweepSmem::dpart);
@@ -100,6 +107,7 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
         tma_prefetch_desc(&tm_do);
+        tma_prefetch_desc(&tm_dq);
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, 512);
@@ -158,7 +166,7 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)  // Y += A V
-                    mma_ts(tmem + kFY, tmem + kFX + 8 * kk, desc_mnmajor(aV, kk), id_kmn, 1);
+                    mma_ts(tmem + kFY, tmem + kFX + xcol(kk), desc_mnmajor(aV, kk), id_kmn, 1);
                 mma_commit(&bar->o_done);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)  // S += K~^T V
@@ -180,9 +188,9 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
                     mma_ss(tmem + kFY, desc_kmajor(aP, kk), desc_kmajor(aSb, kk), id_kk, kk > 0);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {  // Y += D K~ as D_hi K_hi + D_lo K_hi + D_hi K_lo
-                    mma_ts(tmem + kFY, tmem + kFX + 8 * kk, desc_mnmajor(aK, kk), id_kmn, 1);
-                    mma_ts(tmem + kFY, tmem + kFX + 64 + 8 * kk, desc_mnmajor(aK, kk), id_kmn, 1);
-                    mma_ts(tmem + kFY, tmem + kFX + 8 * kk, desc_mnmajor(aKLo, kk), id_kmn, 1);
+                    mma_ts(tmem + kFY, tmem + kFX + xcol(kk), desc_mnmajor(aK, kk), id_kmn, 1);
+                    mma_ts(tmem + kFY, tmem + kFX + xcol(kk) + 16, desc_mnmajor(aK, kk), id_kmn, 1);
+                    mma_ts(tmem + kFY, tmem + kFX + xcol(kk), desc_mnmajor(aKLo, kk), id_kmn, 1);
                 }
                 mma_commit(&bar->dq_done);
                 mma_commit(&bar->empty_kp);  // last read of K, K_lo and P
@@ -199,7 +207,6 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
         global_row_to_tmem<64>(pre + (size_t)r * kD + 64 * h, tmem + lb + kFS);  // S_prev row r, this half
         if (ct < 128) {
             zsh[ct] = pre[(size_t)kD * kD + ct];
-            zacc[ct] = 0.f;
             racc[ct] = 0.f;
         }
         tc_fence_before();
@@ -212,6 +219,7 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
             // (a) phi on Q in place; S_prev -> its bf16 copy (rows = dk; this thread's 64
             // columns).  S and Y are settled: the previous chunk's dq_done, which follows
             // every earlier MMA, has been awaited.
+            if (ct == 0) bulk_wait_read_all();  // the previous dq store has left the Sb tile
             if (!grp_all(mbar_wait(&bar->full_qv, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
             tc_fence_after();
             grp_phi_tile(sQ, nullptr, ct, n, nullptr, nullptr);
@@ -239,24 +247,24 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
                 }
                 dpart[128 * h + r] = di;
             }
-            // (b) phi on K: hi in place, lo beside it, column sums of hi into zacc
+            // (b) phi on K: hi in place, lo beside it, per-warp column sums of hi into zpart
             if (!grp_all(mbar_wait(&bar->full_kp, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
-            grp_phi_tile(sK, sKLo, ct, n, nullptr, zacc);
+            grp_phi_tile(sK, sKLo, ct, n, nullptr, zpart);
             fence_proxy_async_smem();
             grp_sync();
             if (ct == 0) mbar_arrive(&bar->qk_ready);
-            // (c) A = tril(QK^T) on keys [64h, 64h+64) as bf16 pairs into X columns [32h, 32h+32)
+            // (c) A = tril(QK^T) on this thread's keys [64h, 64h+64), in place (see the X layout)
             if (!grp_all(mbar_wait(&bar->qk_done, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
             tc_fence_after();
             {
-                uint32_t pk[2][16];
                 float rs = 0.f;
 #pragma unroll
                 for (int cb = 0; cb < 2; ++cb) {
                     const int j0 = 64 * h + 32 * cb;
+                    uint32_t pk[16];
                     if (j0 > r) {
 #pragma unroll
-                        for (int x = 0; x < 16; ++x) pk[cb][x] = 0u;
+                        for (int x = 0; x < 16; ++x) pk[x] = 0u;
                     } else {
                         uint32_t w[32];
                         tmem_ld32(tmem + lb + kFX + 32 * cb, w);
@@ -264,18 +272,14 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
 #pragma unroll
                         for (int x = 0; x < 16; ++x) {
                             const int j = j0 + 2 * x;
-                            pk[cb][x] = pack_bf16x2(j <= r ? __uint_as_float(w[2 * x]) : 0.f,
-                                                    j + 1 <= r ? __uint_as_float(w[2 * x + 1]) : 0.f);
-                            rs += bf_lo(pk[cb][x]) + bf_hi(pk[cb][x]);
+                            pk[x] = pack_bf16x2(j <= r ? __uint_as_float(w[2 * x]) : 0.f,
+                                                j + 1 <= r ? __uint_as_float(w[2 * x + 1]) : 0.f);
+                            rs += bf_lo(pk[x]) + bf_hi(pk[x]);
                         }
                     }
+                    tmem_st16(tmem + lb + kFX + 32 * cb, pk);
                 }
                 rpart[128 * h + r] = rs;
-                tc_fence_before();
-                grp_sync();  // every thread has read its QK columns before any A column is written
-                tc_fence_after();
-                tmem_st16(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + kFX + 32 * h, pk[0]);
-                tmem_st16(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + kFX + 32 * h + 16, pk[1]);
                 tmem_st_wait();
             }
             tc_fence_before();
@@ -337,49 +341,43 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
                         zp[j >> 2][2 * e + 1] = fmaf(wr, bf_hi(u[e]), zp[j >> 2][2 * e + 1]);
                     }
                 }
-                grp_column_add(zp, racc, ct);
+                grp_column_part(zp, drpart, ct);
             }
             grp_sync();  // every read of Q by the compute group is done
             if (ct == 0) mbar_arrive(&bar->empty_qv);
-            // (e) D = tril(P V^T + g) as hi / lo bf16 pairs into X[32h..] / X[64 + 32h..]
+            // (e) D = tril(P V^T + g) as bf16 hi + lo on this thread's keys, in place (see the X layout)
             if (!grp_all(mbar_wait(&bar->pv_done, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
             tc_fence_after();
-            {
-                uint32_t hi[2][16], lo[2][16];
 #pragma unroll
-                for (int cb = 0; cb < 2; ++cb) {
-                    const int j0 = 64 * h + 32 * cb;
-                    if (j0 > r) {
+            for (int cb = 0; cb < 2; ++cb) {
+                const int j0 = 64 * h + 32 * cb;
+                uint32_t hi[16], lo[16];
+                if (j0 > r) {
 #pragma unroll
-                        for (int x = 0; x < 16; ++x) hi[cb][x] = lo[cb][x] = 0u;
-                    } else {
-                        uint32_t w[32];
-                        tmem_ld32(tmem + lb + kFX + 32 * cb, w);
-                        tmem_ld_wait();
+                    for (int x = 0; x < 16; ++x) hi[x] = lo[x] = 0u;
+                } else {
+                    uint32_t w[32];
+                    tmem_ld32(tmem + lb + kFX + 32 * cb, w);
+                    tmem_ld_wait();
 #pragma unroll
-                        for (int x = 0; x < 16; ++x) {
-                            const int j = j0 + 2 * x;
-                            const float d0 = j <= r ? __uint_as_float(w[2 * x]) + g : 0.f;
-                            const float d1 = j + 1 <= r ? __uint_as_float(w[2 * x + 1]) + g : 0.f;
-                            hi[cb][x] = pack_bf16x2(d0, d1);
-                            lo[cb][x] = pack_bf16x2(d0 - bf_lo(hi[cb][x]), d1 - bf_hi(hi[cb][x]));
-                        }
+                    for (int x = 0; x < 16; ++x) {
+                        const int j = j0 + 2 * x;
+                        const float d0 = j <= r ? __uint_as_float(w[2 * x]) + g : 0.f;
+                        const float d1 = j + 1 <= r ? __uint_as_float(w[2 * x + 1]) + g : 0.f;
+                        hi[x] = pack_bf16x2(d0, d1);
+                        lo[x] = pack_bf16x2(d0 - bf_lo(hi[x]), d1 - bf_hi(hi[x]));
                     }
                 }
-                tc_fence_before();
-                grp_sync();  // every thread has read its P V^T columns before any D column is written
-                tc_fence_after();
-                const uint32_t row_base = ((uint32_t)(32 * (warp & 3)) << 16) + kFX;
-                tmem_st16(row_base + 32 * h, hi[0]);
-                tmem_st16(row_base + 32 * h + 16, hi[1]);
-                tmem_st16(row_base + 64 + 32 * h, lo[0]);
-                tmem_st16(row_base + 64 + 32 * h + 16, lo[1]);
-                tmem_st_wait();
+                tmem_st16(tmem + lb + kFX + 32 * cb, hi);
+                tmem_st16(tmem + lb + kFX + 32 * cb + 16, lo);
             }
+            tmem_st_wait();
             tc_fence_before();
             grp_sync();
             if (ct == 0) mbar_arrive(&bar->d_ready);
-            // (f) dq = (dQ~ + g z_prev) * phi'(q), this thread's 64 columns
+            // (f) dq = (dQ~ + g z_prev) * phi'(q), this thread's 64 columns, staged in the Sb
+            // tile (free once the dq products are done) and written by one TMA store
+            // (rows past N are not written)
             if (!grp_all(mbar_wait(&bar->dq_done, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
             tc_fence_after();
 #pragma unroll
@@ -387,32 +385,36 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
                 uint32_t w[32];
                 tmem_ld32(tmem + lb + kFY + 32 * cb, w);
                 tmem_ld_wait();
-                if (valid) {
-                    __nv_bfloat16* drow = dq + ((size_t)bh * N + c0 + r) * kD + 64 * h + 32 * cb;
 #pragma unroll
-                    for (int c4 = 0; c4 < 4; ++c4) {
-                        const uint32_t* qu = &qrow[4 * (4 * cb + c4)];
-                        uint4 o4;
-                        uint32_t* ou = reinterpret_cast<uint32_t*>(&o4);
+                for (int c4 = 0; c4 < 4; ++c4) {
+                    const uint32_t* qu = &qrow[4 * (4 * cb + c4)];
+                    uint4 o4;
+                    uint32_t* ou = reinterpret_cast<uint32_t*>(&o4);
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int d = 64 * h + 32 * cb + 8 * c4 + 2 * e;
-                            const float a0 = (__uint_as_float(w[8 * c4 + 2 * e]) + g * zsh[d]) * dphi_from_phi(bf_lo(qu[e]));
-                            const float a1 =
-                                (__uint_as_float(w[8 * c4 + 2 * e + 1]) + g * zsh[d + 1]) * dphi_from_phi(bf_hi(qu[e]));
-                            ou[e] = pack_bf16x2(a0, a1);
-                        }
-                        *reinterpret_cast<uint4*>(drow + 8 * c4) = o4;
+                    for (int e = 0; e < 4; ++e) {
+                        const int d = 64 * h + 32 * cb + 8 * c4 + 2 * e;
+                        const float a0 = (__uint_as_float(w[8 * c4 + 2 * e]) + g * zsh[d]) * dphi_from_phi(bf_lo(qu[e]));
+                        const float a1 =
+                            (__uint_as_float(w[8 * c4 + 2 * e + 1]) + g * zsh[d + 1]) * dphi_from_phi(bf_hi(qu[e]));
+                        ou[e] = pack_bf16x2(a0, a1);
                     }
+                    *reinterpret_cast<uint4*>(sSb + chunk_off(r, 8 * h + 4 * cb + c4)) = o4;
                 }
             }
+            fence_proxy_async_smem();
             tc_fence_before();
-            grp_sync();  // z_prev has been used by every thread
+            grp_sync();  // the dq tile is complete and z_prev has been used by every thread
+            if (ct == 0) {
+                tma_store_3d(&tm_dq, sSb, 0, c0, bh);
+                tma_store_3d(&tm_dq, sSb + kBlockBytes, 64, c0, bh);
+                bulk_commit();
+            }
             if (ct < 128) {
-                zsh[ct] += zacc[ct];
-                zacc[ct] = 0.f;
+                zsh[ct] += grp_column_sum(zpart, ct);
+                racc[ct] += grp_column_sum(drpart, ct);
             }
         }
+        if (ct == 0) bulk_wait_all();
         // segment sums of the reverse state out: R from TMEM, r from shared memory
         if (ok && nloc > 0 && grp_all(mbar_wait(&bar->final_mma, 0, err, LA_ERR_TIMEOUT))) {
             tc_fence_after();
@@ -443,13 +445,15 @@ struct RevSweepBars {
 };
 
 // Kc: a copy of phi(K) for phi'(k) in the dk epilogue, so that the inputs are
-// released (by the MMA thread, at dkv_done) while the epilogue still runs.
+// released (by the MMA thread, at dkv_done) while the epilogue still runs; the
+// epilogue then overwrites it with the dk tile, and the Rb tile (free after
+// the products) with the dv tile, for the TMA stores.
 struct RevSweepSmem {
     static constexpr int Q = 0, K = kTileBytes, V = 2 * kTileBytes, P = 3 * kTileBytes, Rb = 4 * kTileBytes;
     static constexpr int Kc = 5 * kTileBytes;
     static constexpr int rsh = 6 * kTileBytes;  // float[128] r_next
-    static constexpr int racc = rsh + 512;      // float[128] this chunk's sum of g phi(q)
-    static constexpr int gsh = racc + 512;      // float[128] g of the chunk's rows
+    static constexpr int rpart = rsh + 512;     // float[8][128] per-warp column sums of this chunk's g phi(q)
+    static constexpr int gsh = rpart + 4096;    // float[128] g of the chunk's rows
     static constexpr int ish = gsh + 512;       // float[128] 1/den of the chunk's rows
     static constexpr int bars = ish + 512;
     static constexpr int tmem_slot = bars + 256;
@@ -459,7 +463,7 @@ struct RevSweepSmem {
 __global__ void __launch_bounds__(kThreads, 1)
 tc_bwd_reverse_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                             const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                            __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv,
+                            const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
                             const float* __restrict__ seg_R, const float* __restrict__ den_g, int N, int nchunks,
                             int cps, int P, int* err) {
     extern __shared__ uint8_t smem_raw[];
@@ -471,7 +475,7 @@ tc_bwd_reverse_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
     uint8_t* sRb = base + RevSweepSmem::Rb;
     uint8_t* sKc = base + RevSweepSmem::Kc;
     float* rsh = reinterpret_cast<float*>(base + RevSweepSmem::rsh);
-    float* racc = reinterpret_cast<float*>(base + RevSweepSmem::racc);
+    float* rpart = reinterpret_cast<float*>(base + RevSweepSmem::rpart);
     float* gsh = reinterpret_cast<float*>(base + RevSweepSmem::gsh);
     float* ish = reinterpret_cast<float*>(base + RevSweepSmem::ish);
     RevSweepBars* bar = reinterpret_cast<RevSweepBars*>(base + RevSweepSmem::bars);
@@ -490,6 +494,8 @@ tc_bwd_reverse_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
         tma_prefetch_desc(&tm_do);
+        tma_prefetch_desc(&tm_dk);
+        tma_prefetch_desc(&tm_dv);
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, 512);
@@ -569,10 +575,7 @@ tc_bwd_reverse_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
         const uint32_t lb = lane0 + 64 * h;
         const float* suf = seg_R + ((size_t)bh * P + p) * E;
         global_row_to_tmem<64>(suf + (size_t)r * kD + 64 * h, tmem + lb + kRR);  // R_next row r, this half
-        if (ct < 128) {
-            rsh[ct] = suf[(size_t)kD * kD + ct];
-            racc[ct] = 0.f;
-        }
+        if (ct < 128) rsh[ct] = suf[(size_t)kD * kD + ct];
         tc_fence_before();
         bool ok = grp_all(true);
         const float* dgh = den_g + (size_t)bh * N * 2;
@@ -580,6 +583,7 @@ tc_bwd_reverse_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
             const uint32_t ph = i & 1;
             const int c0 = (cend - 1 - i) * kC, n = min(kC, N - c0);
             // (a) per-row 1/den and g; phi on Q (with the chunk's sum of g phi(q)) and K; P = dO / den
+            if (ct == 0) bulk_wait_read_all();  // the previous dk / dv stores have left Kc and Rb
             if (!grp_all(mbar_wait(&bar->full, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
             if (ct < 128) {
                 const bool v = ct < n;
@@ -588,7 +592,7 @@ tc_bwd_reverse_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
                 gsh[ct] = dg.y;
             }
             grp_sync();
-            grp_phi_tile(sQ, nullptr, ct, n, gsh, racc);
+            grp_phi_tile(sQ, nullptr, ct, n, gsh, rpart);
             grp_phi_tile(sK, nullptr, ct, n, nullptr, nullptr, sKc);
             grp_scale_rows(sP, ct, ish);
             fence_proxy_async_smem();
@@ -635,32 +639,30 @@ tc_bwd_reverse_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
             tc_fence_before();
             grp_sync();
             if (ct == 0) mbar_arrive(&bar->masks_ready);
-            // (d) dk = (dK~ + r_next) * phi'(k), dv; this thread's 64 columns of key row r
+            // (d) dk = (dK~ + r_next) * phi'(k) in place of phi(k) in Kc, dv into Rb; this
+            // thread's 64 columns of key row r; one TMA store each (rows past N are not written)
             if (!grp_all(mbar_wait(&bar->dkv_done, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
             tc_fence_after();
-            const bool valid = r < n;
 #pragma unroll
             for (int cb = 0; cb < 2; ++cb) {
                 uint32_t w[32];
                 tmem_ld32(tmem + lb + kRDK + 32 * cb, w);
                 tmem_ld_wait();
-                if (valid) {
-                    __nv_bfloat16* dkrow = dk + ((size_t)bh * N + c0 + r) * kD + 64 * h + 32 * cb;
 #pragma unroll
-                    for (int c4 = 0; c4 < 4; ++c4) {
-                        const uint4 kv = *reinterpret_cast<const uint4*>(sKc + chunk_off(r, 8 * h + 4 * cb + c4));
-                        const uint32_t* ku = reinterpret_cast<const uint32_t*>(&kv);
-                        uint4 o4;
-                        uint32_t* ou = reinterpret_cast<uint32_t*>(&o4);
+                for (int c4 = 0; c4 < 4; ++c4) {
+                    uint4* kp = reinterpret_cast<uint4*>(sKc + chunk_off(r, 8 * h + 4 * cb + c4));
+                    const uint4 kv = *kp;
+                    const uint32_t* ku = reinterpret_cast<const uint32_t*>(&kv);
+                    uint4 o4;
+                    uint32_t* ou = reinterpret_cast<uint32_t*>(&o4);
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int d = 64 * h + 32 * cb + 8 * c4 + 2 * e;
-                            ou[e] = pack_bf16x2((__uint_as_float(w[8 * c4 + 2 * e]) + rsh[d]) * dphi_from_phi(bf_lo(ku[e])),
-                                                (__uint_as_float(w[8 * c4 + 2 * e + 1]) + rsh[d + 1]) *
-                                                    dphi_from_phi(bf_hi(ku[e])));
-                        }
-                        *reinterpret_cast<uint4*>(dkrow + 8 * c4) = o4;
+                    for (int e = 0; e < 4; ++e) {
+                        const int d = 64 * h + 32 * cb + 8 * c4 + 2 * e;
+                        ou[e] = pack_bf16x2((__uint_as_float(w[8 * c4 + 2 * e]) + rsh[d]) * dphi_from_phi(bf_lo(ku[e])),
+                                            (__uint_as_float(w[8 * c4 + 2 * e + 1]) + rsh[d + 1]) *
+                                                dphi_from_phi(bf_hi(ku[e])));
                     }
+                    *kp = o4;
                 }
             }
 #pragma unroll
@@ -668,27 +670,22 @@ tc_bwd_reverse_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
                 uint32_t w[32];
                 tmem_ld32(tmem + lb + kRDV + 32 * cb, w);
                 tmem_ld_wait();
-                if (valid) {
-                    __nv_bfloat16* dvrow = dv + ((size_t)bh * N + c0 + r) * kD + 64 * h + 32 * cb;
-#pragma unroll
-                    for (int c4 = 0; c4 < 4; ++c4) {
-                        uint4 o4;
-                        o4.x = pack_bf16x2(__uint_as_float(w[8 * c4 + 0]), __uint_as_float(w[8 * c4 + 1]));
-                        o4.y = pack_bf16x2(__uint_as_float(w[8 * c4 + 2]), __uint_as_float(w[8 * c4 + 3]));
-                        o4.z = pack_bf16x2(__uint_as_float(w[8 * c4 + 4]), __uint_as_float(w[8 * c4 + 5]));
-                        o4.w = pack_bf16x2(__uint_as_float(w[8 * c4 + 6]), __uint_as_float(w[8 * c4 + 7]));
-                        *reinterpret_cast<uint4*>(dvrow + 8 * c4) = o4;
-                    }
-                }
+                row32_to_tile(w, sRb, r, 8 * h + 4 * cb);
             }
+            // (e) stores out; r_next += this chunk's sum of g phi(q) (every thread has used r_next)
+            fence_proxy_async_smem();
             tc_fence_before();
-            // (e) r_next += this chunk's sum of g phi(q) (after every thread has used r_next)
             grp_sync();
-            if (ct < 128) {
-                rsh[ct] += racc[ct];
-                racc[ct] = 0.f;
+            if (ct == 0) {
+                tma_store_3d(&tm_dk, sKc, 0, c0, bh);
+                tma_store_3d(&tm_dk, sKc + kBlockBytes, 64, c0, bh);
+                tma_store_3d(&tm_dv, sRb, 0, c0, bh);
+                tma_store_3d(&tm_dv, sRb + kBlockBytes, 64, c0, bh);
+                bulk_commit();
             }
+            if (ct < 128) rsh[ct] += grp_column_sum(rpart, ct);
         }
+        if (ct == 0) bulk_wait_all();
         tc_fence_before();
     }
     __syncthreads();
@@ -708,15 +705,17 @@ cudaError_t tc_bwd_forward_sweep(const void* q, const void* k, const void* v, co
                                  cudaStream_t st) {
     const int BH = s.B * s.H;
     CUtensorMap tq, tk, tv, td;
+    CUtensorMap tdq;
     if (!make_tmap_bf16_rows(&tq, q, BH, s.N, kD, kC) || !make_tmap_bf16_rows(&tk, k, BH, s.N, kD, kC) ||
-        !make_tmap_bf16_rows(&tv, v, BH, s.N, kD, kC) || !make_tmap_bf16_rows(&td, dout, BH, s.N, kD, kC))
+        !make_tmap_bf16_rows(&tv, v, BH, s.N, kD, kC) || !make_tmap_bf16_rows(&td, dout, BH, s.N, kD, kC) ||
+        !make_tmap_bf16_rows(&tdq, dq, BH, s.N, kD, kC))
         return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(tc_bwd_forward_sweep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kFwdSweepSmem);
     if (e != cudaSuccess) return e;
     launch_begin("tc_bwd_forward_sweep", st);
     tc_bwd_forward_sweep_kernel<<<dim3(p.P, BH), kThreads, kFwdSweepSmem, st>>>(
-        tq, tk, tv, td, (__nv_bfloat16*)dq, seg_S, seg_R, den_g, s.N, p.nchunks, p.cps, p.P, device_error_word());
+        tq, tk, tv, td, tdq, seg_S, seg_R, den_g, s.N, p.nchunks, p.cps, p.P, device_error_word());
     return launch_end("tc_bwd_forward_sweep", st);
 }
 
@@ -725,16 +724,17 @@ cudaError_t tc_bwd_reverse_sweep(const void* q, const void* k, const void* v, co
                                  cudaStream_t st) {
     const int BH = s.B * s.H;
     CUtensorMap tq, tk, tv, td;
+    CUtensorMap tdk, tdv;
     if (!make_tmap_bf16_rows(&tq, q, BH, s.N, kD, kC) || !make_tmap_bf16_rows(&tk, k, BH, s.N, kD, kC) ||
-        !make_tmap_bf16_rows(&tv, v, BH, s.N, kD, kC) || !make_tmap_bf16_rows(&td, dout, BH, s.N, kD, kC))
+        !make_tmap_bf16_rows(&tv, v, BH, s.N, kD, kC) || !make_tmap_bf16_rows(&td, dout, BH, s.N, kD, kC) ||
+        !make_tmap_bf16_rows(&tdk, dk, BH, s.N, kD, kC) || !make_tmap_bf16_rows(&tdv, dv, BH, s.N, kD, kC))
         return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(tc_bwd_reverse_sweep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kRevSweepSmem);
     if (e != cudaSuccess) return e;
     launch_begin("tc_bwd_reverse_sweep", st);
     tc_bwd_reverse_sweep_kernel<<<dim3(p.P, BH), kThreads, kRevSweepSmem, st>>>(
-        tq, tk, tv, td, (__nv_bfloat16*)dk, (__nv_bfloat16*)dv, seg_R, den_g, s.N, p.nchunks, p.cps, p.P,
-        device_error_word());
+        tq, tk, tv, td, tdk, tdv, seg_R, den_g, s.N, p.nchunks, p.cps, p.P, device_error_word());
     return launch_end("tc_bwd_reverse_sweep", st);
 }
 

@@ -256,8 +256,10 @@ __device__ __forceinline__ int grp_vec_lc(int ct) { return (ct & 7) ^ ((ct >> 3)
 
 // Column partial sums zp[block][e] (for columns 64*block + 8*lc + e of this
 // thread) summed over the four lanes of the warp that share lc (lanes l, l^9,
-// l^18, l^27) and added into dst[128] by lanes 0-7.
-__device__ __forceinline__ void grp_column_add(float (&zp)[2][8], float* dst, int ct) {
+// l^18, l^27) and stored by lanes 0-7 as this warp's row of part[8][128]
+// (no atomics: the eight warps' rows are added by grp_column_sum after a
+// group barrier).
+__device__ __forceinline__ void grp_column_part(float (&zp)[2][8], float* part, int ct) {
 #pragma unroll
     for (int b = 0; b < 2; ++b)
 #pragma unroll
@@ -268,20 +270,29 @@ __device__ __forceinline__ void grp_column_add(float (&zp)[2][8], float* dst, in
             zp[b][e] = x;
         }
     if ((ct & 31) < 8) {
-        const int lc = grp_vec_lc(ct);
+        float* row = part + (ct >> 5) * 128 + 8 * grp_vec_lc(ct);
 #pragma unroll
-        for (int b = 0; b < 2; ++b)
-#pragma unroll
-            for (int e = 0; e < 8; ++e) atomicAdd(dst + 64 * b + 8 * lc + e, zp[b][e]);
+        for (int b = 0; b < 2; ++b) {
+            *reinterpret_cast<float4*>(row + 64 * b) = make_float4(zp[b][0], zp[b][1], zp[b][2], zp[b][3]);
+            *reinterpret_cast<float4*>(row + 64 * b + 4) = make_float4(zp[b][4], zp[b][5], zp[b][6], zp[b][7]);
+        }
     }
 }
+// Column c (0..127) of part[8][128] summed over the eight warps.
+__device__ __forceinline__ float grp_column_sum(const float* part, int c) {
+    float s = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) s += part[128 * w + c];
+    return s;
+}
 
-// phi in place on a staged tile (rows >= n exactly 0) with the column sums of
-// the rounded values (weighted by w[row] when w is given) added into colsum.
-// With lo_tile, also writes lo = bf16(phi - hi) there; with copy_tile, a second
-// copy of the rounded phi.
+// phi in place on a staged tile (rows >= n exactly 0).  With colpart, the
+// column sums of the rounded values (weighted by w[row] when w is given) go to
+// colpart[8][128] as per-warp partials (see grp_column_part).  With lo_tile,
+// also writes lo = bf16(phi - hi) there; with copy_tile, a second copy of the
+// rounded phi.
 __device__ __forceinline__ void grp_phi_tile(uint8_t* tile, uint8_t* lo_tile, int ct, int n, const float* w,
-                                             float* colsum, uint8_t* copy_tile = nullptr) {
+                                             float* colpart, uint8_t* copy_tile = nullptr) {
     float zp[2][8];
 #pragma unroll
     for (int b = 0; b < 2; ++b)
@@ -303,7 +314,7 @@ __device__ __forceinline__ void grp_phi_tile(uint8_t* tile, uint8_t* lo_tile, in
             const float a = valid ? phi_f(bf_lo(u[e])) : 0.f, b = valid ? phi_f(bf_hi(u[e])) : 0.f;
             u[e] = pack_bf16x2(a, b);
             ul[e] = pack_bf16x2(a - bf_lo(u[e]), b - bf_hi(u[e]));
-            if (colsum) {
+            if (colpart) {
                 zp[j >> 2][2 * e] = fmaf(wr, bf_lo(u[e]), zp[j >> 2][2 * e]);
                 zp[j >> 2][2 * e + 1] = fmaf(wr, bf_hi(u[e]), zp[j >> 2][2 * e + 1]);
             }
@@ -312,7 +323,7 @@ __device__ __forceinline__ void grp_phi_tile(uint8_t* tile, uint8_t* lo_tile, in
         if (lo_tile) *reinterpret_cast<uint4*>(lo_tile + grp_vec_off(ct, j)) = l;
         if (copy_tile) *reinterpret_cast<uint4*>(copy_tile + grp_vec_off(ct, j)) = v[j];
     }
-    if (colsum) grp_column_add(zp, colsum, ct);
+    if (colpart) grp_column_part(zp, colpart, ct);
 }
 
 // Every row of a staged tile scaled by s[row], rounded to bf16, in place.
