@@ -17,7 +17,10 @@
 // enters as a hi + lo pair of bf16 operands and phi(K) as hi + lo in D K~.
 // Reverse sweep kernel: chunks in reverse order with R_next in TMEM; every
 // product is taken with the keys as the M (TMEM lane) dimension so dk and dv
-// come out row by row.
+// come out row by row.  1/den is folded into the query operand, Q' = phi(Q) /
+// den, so dO enters unscaled: A'^T = K~ Q'^T (= A^T / den), D'^T = tril(V dO^T
+// + (g den) 1^T), dK~ = V R_next^T + 1 r_next^T + D'^T Q', dV = K~ R_next +
+// A'^T dO, R_next += Q'^T dO, r_next += sum of (g den) Q'.
 //
 // Roles: warp 0 TMA, warp 1 TMEM owner and MMA issuer, warps 2-9 the 256-thread
 // compute group (each row's columns split between two warpgroups).  All waits
@@ -178,14 +181,14 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
                     mma_ss(tmem + kFX, desc_kmajor(aP, kk), desc_kmajor(aV, kk), id_kk, kk > 0);
                 mma_commit(&bar->pv_done);
 #pragma unroll
+                for (int kk = 0; kk < 8; ++kk)  // Y = P S_prev^T (Y is free: O was read before p_ready)
+                    mma_ss(tmem + kFY, desc_kmajor(aP, kk), desc_kmajor(aSb, kk), id_kk, kk > 0);
+#pragma unroll
                 for (int kk = 0; kk < 8; ++kk)  // R += Q~^T P
                     mma_ss(tmem + kFR, desc_mnmajor(aQ, kk), desc_mnmajor(aP, kk), id_mnmn, (i > 0 || kk > 0));
                 mma_commit(&bar->empty_qv);  // last MMA read of Q and V in this chunk
                 if (!mbar_wait(&bar->d_ready, ph, err, LA_ERR_TIMEOUT)) break;
                 tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)  // Y = P S_prev^T
-                    mma_ss(tmem + kFY, desc_kmajor(aP, kk), desc_kmajor(aSb, kk), id_kk, kk > 0);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {  // Y += D K~ as D_hi K_hi + D_lo K_hi + D_hi K_lo
                     mma_ts(tmem + kFY, tmem + kFX + xcol(kk), desc_mnmajor(aK, kk), id_kmn, 1);
@@ -453,7 +456,7 @@ struct RevSweepSmem {
     static constexpr int Kc = 5 * kTileBytes;
     static constexpr int rsh = 6 * kTileBytes;  // float[128] r_next
     static constexpr int rpart = rsh + 512;     // float[8][128] per-warp column sums of this chunk's g phi(q)
-    static constexpr int gsh = rpart + 4096;    // float[128] g of the chunk's rows
+    static constexpr int gsh = rpart + 4096;    // float[128] g den of the chunk's rows
     static constexpr int ish = gsh + 512;       // float[128] 1/den of the chunk's rows
     static constexpr int bars = ish + 512;
     static constexpr int tmem_slot = bars + 256;
@@ -476,7 +479,7 @@ tc_bwd_reverse_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
     uint8_t* sKc = base + RevSweepSmem::Kc;
     float* rsh = reinterpret_cast<float*>(base + RevSweepSmem::rsh);
     float* rpart = reinterpret_cast<float*>(base + RevSweepSmem::rpart);
-    float* gsh = reinterpret_cast<float*>(base + RevSweepSmem::gsh);
+    float* gsh = reinterpret_cast<float*>(base + RevSweepSmem::gsh);  // g den
     float* ish = reinterpret_cast<float*>(base + RevSweepSmem::ish);
     RevSweepBars* bar = reinterpret_cast<RevSweepBars*>(base + RevSweepSmem::bars);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + RevSweepSmem::tmem_slot);
@@ -537,30 +540,31 @@ tc_bwd_reverse_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
                 if (!mbar_wait(&bar->ready, ph, err, LA_ERR_TIMEOUT)) break;
                 tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)  // DV region = A^T = K~ Q~^T (rows = keys)
+                for (int kk = 0; kk < 8; ++kk)  // DV region = A'^T = K~ Q'^T (rows = keys)
                     mma_ss(tmem + kRDV, desc_kmajor(aK, kk), desc_kmajor(aQ, kk), id_kk, kk > 0);
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)  // DK region = V P^T (rows = keys)
+                for (int kk = 0; kk < 8; ++kk)  // DK region = V dO^T (rows = keys)
                     mma_ss(tmem + kRDK, desc_kmajor(aV, kk), desc_kmajor(aP, kk), id_kk, kk > 0);
                 mma_commit(&bar->at_dt_done);
                 if (!mbar_wait(&bar->rb_ready, ph, err, LA_ERR_TIMEOUT)) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)  // R_next += Q'^T dO (R_next of this chunk is already in Rb)
+                    mma_ss(tmem + kRR, desc_mnmajor(aQ, kk), desc_mnmajor(aP, kk), id_mnmn, 1);
                 if (!mbar_wait(&bar->masks_ready, ph, err, LA_ERR_TIMEOUT)) break;
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)  // dK~ = V R_next^T
                     mma_ss(tmem + kRDK, desc_kmajor(aV, kk), desc_kmajor(aRb, kk), id_kk, kk > 0);
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)  // dK~ += D^T Q~
+                for (int kk = 0; kk < 8; ++kk)  // dK~ += D'^T Q'
                     mma_ts(tmem + kRDK, tmem + kRX + 8 * kk, desc_mnmajor(aQ, kk), id_kmn, 1);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)  // dV = K~ R_next
                     mma_ss(tmem + kRDV, desc_kmajor(aK, kk), desc_mnmajor(aRb, kk), id_kmn, kk > 0);
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)  // dV += A^T P
+                for (int kk = 0; kk < 8; ++kk)  // dV += A'^T dO
                     mma_ts(tmem + kRDV, tmem + kRX + 64 + 8 * kk, desc_mnmajor(aP, kk), id_kmn, 1);
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)  // R_next += Q~^T P
-                    mma_ss(tmem + kRR, desc_mnmajor(aQ, kk), desc_mnmajor(aP, kk), id_mnmn, 1);
                 mma_commit(&bar->dkv_done);
                 mma_commit(&bar->empty);  // Q, K, V, P: no further read in this chunk
             }
@@ -579,22 +583,31 @@ tc_bwd_reverse_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
         tc_fence_before();
         bool ok = grp_all(true);
         const float* dgh = den_g + (size_t)bh * N * 2;
+        // (den, g) of row ct of chunk ii (rows past N: den 1, g 0); loaded one chunk ahead
+        auto load_dg = [&](int ii) {
+            const int cc = (cend - 1 - ii) * kC;
+            return ct < min(kC, N - cc) ? *reinterpret_cast<const float2*>(dgh + (size_t)(cc + ct) * 2)
+                                        : make_float2(1.f, 0.f);
+        };
+        float2 dg_next = make_float2(1.f, 0.f);
+        if (ct < 128 && nloc > 0) dg_next = load_dg(0);
         for (int i = 0; i < nloc && ok; ++i) {
             const uint32_t ph = i & 1;
             const int c0 = (cend - 1 - i) * kC, n = min(kC, N - c0);
-            // (a) per-row 1/den and g; phi on Q (with the chunk's sum of g phi(q)) and K; P = dO / den
+            const float2 dg = dg_next;
+            if (ct < 128 && i + 1 < nloc) dg_next = load_dg(i + 1);
+            // (a) per-row 1/den and g den; Q' = phi(Q) / den with the chunk's sum of (g den) Q';
+            // phi on K (and its copy)
             if (ct == 0) bulk_wait_read_all();  // the previous dk / dv stores have left Kc and Rb
             if (!grp_all(mbar_wait(&bar->full, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
             if (ct < 128) {
                 const bool v = ct < n;
-                const float2 dg = v ? *reinterpret_cast<const float2*>(dgh + (size_t)(c0 + ct) * 2) : make_float2(1.f, 0.f);
                 ish[ct] = v ? 1.f / dg.x : 0.f;
-                gsh[ct] = dg.y;
+                gsh[ct] = v ? dg.y * dg.x : 0.f;
             }
             grp_sync();
-            grp_phi_tile(sQ, nullptr, ct, n, gsh, rpart);
+            grp_phi_tile(sQ, nullptr, ct, n, gsh, rpart, nullptr, ish);
             grp_phi_tile(sK, nullptr, ct, n, nullptr, nullptr, sKc);
-            grp_scale_rows(sP, ct, ish);
             fence_proxy_async_smem();
             grp_sync();
             if (ct == 0) mbar_arrive(&bar->ready);

@@ -33,141 +33,8 @@ __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, int kk) {
 __device__ __forceinline__ int chunk_off(int row, int lc) {
     return (lc >> 3) * kBlockBytes + row * 128 + (((lc & 7) ^ (row & 7)) << 4);
 }
-// Byte offset of element (row, col).
-__device__ __forceinline__ int elem_off(int row, int col) { return chunk_off(row, col >> 3) + ((col & 7) << 1); }
-
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-__device__ __forceinline__ float bf_at(const uint8_t* tile, int row, int col) {
-    const uint16_t h = *reinterpret_cast<const uint16_t*>(tile + elem_off(row, col));
-    return __uint_as_float((uint32_t)h << 16);
-}
-
-// Barrier over the 128-thread compute warpgroup (named barrier 1) that ANDs a
-// predicate across it, so every thread takes the same branch after a bounded wait.
-__device__ __forceinline__ bool wg_all(bool v) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.and.pred q, 1, 128, p;\n\t"
-        "selp.u32 %0, 1, 0, q;\n\t}"
-        : "=r"(r)
-        : "r"((uint32_t)v)
-        : "memory");
-    return r != 0;
-}
-__device__ __forceinline__ void wg_sync() { named_barrier(1, 128); }
-
-// phi in place on a staged tile, rows >= n set to exactly 0.  Thread t
-// (0..127) handles the 16-byte vectors t + 128 j (block j / 8, row
-// ((t >> 3) + 16 j) & 127); the swizzle only permutes chunks within a row, so
-// an elementwise map ignores it.
-__device__ __forceinline__ void phi_tile(uint8_t* tile, int t, int n) {
-#pragma unroll 4
-    for (int j = 0; j < 16; ++j) {
-        const int row = ((t >> 3) + 16 * j) & 127;
-        uint4* p = reinterpret_cast<uint4*>(tile + (j >> 3) * kBlockBytes + row * 128 + (t & 7) * 16);
-        uint4 w = *p;
-        uint32_t* u = reinterpret_cast<uint32_t*>(&w);
-        const bool valid = row < n;
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-            u[e] = valid ? pack_bf16x2(phi_f(bf_lo(u[e])), phi_f(bf_hi(u[e]))) : 0u;
-        *p = w;
-    }
-}
-
-// phi in place as the bf16 "hi" part, plus lo = bf16(phi - hi) into `lo_tile`
-// (same layout), so that hi + lo carries phi to about 2^-17 relative.
-__device__ __forceinline__ void phi_tile_split(uint8_t* tile, uint8_t* lo_tile, int t, int n) {
-#pragma unroll 4
-    for (int j = 0; j < 16; ++j) {
-        const int row = ((t >> 3) + 16 * j) & 127;
-        const int off = (j >> 3) * kBlockBytes + row * 128 + (t & 7) * 16;
-        uint4 w = *reinterpret_cast<const uint4*>(tile + off);
-        uint32_t* u = reinterpret_cast<uint32_t*>(&w);
-        uint4 l;
-        uint32_t* ul = reinterpret_cast<uint32_t*>(&l);
-        const bool valid = row < n;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float a = valid ? phi_f(bf_lo(u[e])) : 0.f, b = valid ? phi_f(bf_hi(u[e])) : 0.f;
-            u[e] = pack_bf16x2(a, b);
-            ul[e] = pack_bf16x2(a - bf_lo(u[e]), b - bf_hi(u[e]));
-        }
-        *reinterpret_cast<uint4*>(tile + off) = w;
-        *reinterpret_cast<uint4*>(lo_tile + off) = l;
-    }
-}
-
-// Row `row` scaled by 1/den[row] in place (rows >= n are left as loaded: zero).
-__device__ __forceinline__ void scale_rows_tile(uint8_t* tile, int t, const float* inv_den) {
-#pragma unroll 4
-    for (int j = 0; j < 16; ++j) {
-        const int row = ((t >> 3) + 16 * j) & 127;
-        uint4* p = reinterpret_cast<uint4*>(tile + (j >> 3) * kBlockBytes + row * 128 + (t & 7) * 16);
-        uint4 w = *p;
-        uint32_t* u = reinterpret_cast<uint32_t*>(&w);
-        const float s = inv_den[row];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) u[e] = pack_bf16x2(bf_lo(u[e]) * s, bf_hi(u[e]) * s);
-        *p = w;
-    }
-}
-
-// Sum over rows 0..n-1 of column `col` of a tile, each row weighted by w[row] (or 1).
-__device__ __forceinline__ float column_sum(const uint8_t* tile, int col, int n, const float* w) {
-    float acc = 0.f;
-    for (int row = 0; row < n; ++row) acc = fmaf(w ? w[row] : 1.f, bf_at(tile, row, col), acc);
-    return acc;
-}
-
-// One TMEM row (32 lanes per warp) of 128 fp32 columns into a bf16 tile row
-// (rows = TMEM lanes), e.g. the fp32 state S -> its bf16 MMA operand copy.
-__device__ __forceinline__ void tmem_row_to_tile(uint32_t taddr, uint8_t* tile, int row) {
-#pragma unroll
-    for (int cb = 0; cb < 4; ++cb) {
-        uint32_t w[32];
-        tmem_ld32(taddr + 32 * cb, w);
-        tmem_ld_wait();
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-            uint4 v4;
-            v4.x = pack_bf16x2(__uint_as_float(w[8 * q4 + 0]), __uint_as_float(w[8 * q4 + 1]));
-            v4.y = pack_bf16x2(__uint_as_float(w[8 * q4 + 2]), __uint_as_float(w[8 * q4 + 3]));
-            v4.z = pack_bf16x2(__uint_as_float(w[8 * q4 + 4]), __uint_as_float(w[8 * q4 + 5]));
-            v4.w = pack_bf16x2(__uint_as_float(w[8 * q4 + 6]), __uint_as_float(w[8 * q4 + 7]));
-            *reinterpret_cast<uint4*>(tile + chunk_off(row, 4 * cb + q4)) = v4;
-        }
-    }
-}
-
-// The same row as a hi + lo pair of bf16 tiles, hi = bf16(x), lo = bf16(x - hi):
-// a product with (hi + lo) carries the fp32 state to about 2^-17 relative, which
-// the backward needs where two large inter-chunk terms cancel.
-__device__ __forceinline__ void tmem_row_to_tiles_split(uint32_t taddr, uint8_t* hi, uint8_t* lo, int row) {
-#pragma unroll
-    for (int cb = 0; cb < 4; ++cb) {
-        uint32_t w[32];
-        tmem_ld32(taddr + 32 * cb, w);
-        tmem_ld_wait();
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-            uint32_t h4[4], l4[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float x0 = __uint_as_float(w[8 * q4 + 2 * e]), x1 = __uint_as_float(w[8 * q4 + 2 * e + 1]);
-                h4[e] = pack_bf16x2(x0, x1);
-                l4[e] = pack_bf16x2(x0 - bf_lo(h4[e]), x1 - bf_hi(h4[e]));
-            }
-            const int off = chunk_off(row, 4 * cb + q4);
-            *reinterpret_cast<uint4*>(hi + off) = make_uint4(h4[0], h4[1], h4[2], h4[3]);
-            *reinterpret_cast<uint4*>(lo + off) = make_uint4(l4[0], l4[1], l4[2], l4[3]);
-        }
-    }
-}
-
 // kCols fp32 values of a row from global memory into TMEM columns (initial states).
 template <int kCols = 128>
 __device__ __forceinline__ void global_row_to_tmem(const float* src, uint32_t taddr) {
@@ -286,13 +153,14 @@ __device__ __forceinline__ float grp_column_sum(const float* part, int c) {
     return s;
 }
 
-// phi in place on a staged tile (rows >= n exactly 0).  With colpart, the
-// column sums of the rounded values (weighted by w[row] when w is given) go to
-// colpart[8][128] as per-warp partials (see grp_column_part).  With lo_tile,
-// also writes lo = bf16(phi - hi) there; with copy_tile, a second copy of the
-// rounded phi.
+// phi in place on a staged tile (rows >= n exactly 0), times scale[row] when
+// scale is given.  With colpart, the column sums of the rounded values
+// (weighted by w[row] when w is given) go to colpart[8][128] as per-warp
+// partials (see grp_column_part).  With lo_tile, also writes lo = bf16(phi -
+// hi) there; with copy_tile, a second copy of the rounded values.
 __device__ __forceinline__ void grp_phi_tile(uint8_t* tile, uint8_t* lo_tile, int ct, int n, const float* w,
-                                             float* colpart, uint8_t* copy_tile = nullptr) {
+                                             float* colpart, uint8_t* copy_tile = nullptr,
+                                             const float* scale = nullptr) {
     float zp[2][8];
 #pragma unroll
     for (int b = 0; b < 2; ++b)
@@ -309,9 +177,10 @@ __device__ __forceinline__ void grp_phi_tile(uint8_t* tile, uint8_t* lo_tile, in
         uint32_t* ul = reinterpret_cast<uint32_t*>(&l);
         const bool valid = row < n;
         const float wr = (w && valid) ? w[row] : 1.f;
+        const float sr = scale ? scale[row] : 1.f;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            const float a = valid ? phi_f(bf_lo(u[e])) : 0.f, b = valid ? phi_f(bf_hi(u[e])) : 0.f;
+            const float a = valid ? phi_f(bf_lo(u[e])) * sr : 0.f, b = valid ? phi_f(bf_hi(u[e])) * sr : 0.f;
             u[e] = pack_bf16x2(a, b);
             ul[e] = pack_bf16x2(a - bf_lo(u[e]), b - bf_hi(u[e]));
             if (colpart) {
@@ -324,21 +193,6 @@ __device__ __forceinline__ void grp_phi_tile(uint8_t* tile, uint8_t* lo_tile, in
         if (copy_tile) *reinterpret_cast<uint4*>(copy_tile + grp_vec_off(ct, j)) = v[j];
     }
     if (colpart) grp_column_part(zp, colpart, ct);
-}
-
-// Every row of a staged tile scaled by s[row], rounded to bf16, in place.
-__device__ __forceinline__ void grp_scale_rows(uint8_t* tile, int ct, const float* s) {
-    uint4 v[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) v[j] = *reinterpret_cast<const uint4*>(tile + grp_vec_off(ct, j));
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        uint32_t* u = reinterpret_cast<uint32_t*>(&v[j]);
-        const float f = s[grp_vec_row(ct, j)];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) u[e] = pack_bf16x2(bf_lo(u[e]) * f, bf_hi(u[e]) * f);
-        *reinterpret_cast<uint4*>(tile + grp_vec_off(ct, j)) = v[j];
-    }
 }
 
 }  // namespace tc
