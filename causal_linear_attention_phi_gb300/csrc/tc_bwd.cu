@@ -22,9 +22,11 @@
 // + (g den) 1^T), dK~ = V R_next^T + 1 r_next^T + D'^T Q', dV = K~ R_next +
 // A'^T dO, R_next += Q'^T dO, r_next += sum of (g den) Q'.
 //
-// Roles: warp 0 TMA, warp 1 TMEM owner and MMA issuer, warps 2-9 the 256-thread
-// compute group (each row's columns split between two warpgroups).  All waits
-// are bounded.
+// Roles: warp 0 TMA, warp 1 TMEM owner and MMA issuer, the other warps the
+// compute group: 8 warps in the forward sweep, 16 in the reverse sweep.  For
+// row-wise TMEM work warp w reads TMEM lanes 32 (w % 4) .. +31 (row r of a
+// 128-row tile) and its share of the columns: half h = (w - 2) / 4 with 8 warps,
+// quarter qt = (w - 2) / 4 with 16.  All waits are bounded.
 #include "tc_common.cuh"
 
 namespace la {
@@ -32,7 +34,9 @@ namespace {
 using namespace sm100;
 using namespace tc;
 
-constexpr int kThreads = 320;
+using FG = Grp<256>;  // forward sweep: 8 compute warps
+using RG = Grp<512>;  // reverse sweep: 16 compute warps (4 per SM sub-partition)
+constexpr int kThreadsFS = 64 + 256, kThreadsRS = 64 + 512;  // + the TMA and MMA warps
 
 // ------------------------------------------------------------------ forward sweep
 // TMEM: S [0,128) fp32 state; R [128,256) segment sum of phi(q) P^T;
@@ -63,15 +67,15 @@ struct FwdSweepSmem {
     static constexpr int racc = zpart + 4096;   // float[128] segment sum of g phi(q)
     static constexpr int drpart = racc + 512;   // float[8][128] per-warp column sums of this chunk's g phi(q)
     static constexpr int gsh = drpart + 4096;   // float[128] g of the chunk's rows
-    static constexpr int rpart = gsh + 512;     // float[2][128] row-sum halves of A
-    static constexpr int dpart = rpart + 1024;  // float[2][128] halves of phi(q) . z_prev
-    static constexpr int tpart = dpart + 1024;  // float[2][128] halves of P . num
+    static constexpr int rpart = gsh + 512;     // float[2][128] row sums of A, per column half
+    static constexpr int dpart = rpart + 1024;  // float[2][128] phi(q) . z_prev, per column half
+    static constexpr int tpart = dpart + 1024;  // float[2][128] P . num, per column half
     static constexpr int bars = tpart + 1024;
     static constexpr int tmem_slot = bars + 256;
     static constexpr int total = tmem_slot + 16;
 };
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreadsFS, 1)
 tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                             const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                             const __grid_constant__ CUtensorMap tm_dq, const float* __restrict__ seg_S,
@@ -213,7 +217,7 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
             racc[ct] = 0.f;
         }
         tc_fence_before();
-        bool ok = grp_all(true);
+        bool ok = FG::all(true);
         float* dgh = den_g + (size_t)bh * N * 2;
         for (int i = 0; i < nloc && ok; ++i) {
             const uint32_t ph = i & 1;
@@ -223,13 +227,13 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
             // columns).  S and Y are settled: the previous chunk's dq_done, which follows
             // every earlier MMA, has been awaited.
             if (ct == 0) bulk_wait_read_all();  // the previous dq store has left the Sb tile
-            if (!grp_all(mbar_wait(&bar->full_qv, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
+            if (!FG::all(mbar_wait(&bar->full_qv, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
             tc_fence_after();
-            grp_phi_tile(sQ, nullptr, ct, n, nullptr, nullptr);
+            FG::phi_tile(sQ, nullptr, ct, n, nullptr, nullptr);
             tmem_half_row_to_tile(tmem + lb + kFS, sSb, r, h);
             tc_fence_before();
             fence_proxy_async_smem();
-            grp_sync();
+            FG::sync();
             if (ct == 0) mbar_arrive(&bar->sb_ready);
             // phi(q_r) on this thread's 64 columns stays in registers for phi'(q) in the dq
             // epilogue (Q is released before it); phi(q_r) . z_prev
@@ -251,13 +255,13 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
                 dpart[128 * h + r] = di;
             }
             // (b) phi on K: hi in place, lo beside it, per-warp column sums of hi into zpart
-            if (!grp_all(mbar_wait(&bar->full_kp, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
-            grp_phi_tile(sK, sKLo, ct, n, nullptr, zpart);
+            if (!FG::all(mbar_wait(&bar->full_kp, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
+            FG::phi_tile(sK, sKLo, ct, n, nullptr, zpart);
             fence_proxy_async_smem();
-            grp_sync();
+            FG::sync();
             if (ct == 0) mbar_arrive(&bar->qk_ready);
             // (c) A = tril(QK^T) on this thread's keys [64h, 64h+64), in place (see the X layout)
-            if (!grp_all(mbar_wait(&bar->qk_done, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
+            if (!FG::all(mbar_wait(&bar->qk_done, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
             tc_fence_after();
             {
                 float rs = 0.f;
@@ -286,10 +290,10 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
                 tmem_st_wait();
             }
             tc_fence_before();
-            grp_sync();
+            FG::sync();
             if (ct == 0) mbar_arrive(&bar->a_ready);
             // (d) den; P = dO / den (in place, bf16); g = -P . num / den from that bf16 P
-            if (!grp_all(mbar_wait(&bar->o_done, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
+            if (!FG::all(mbar_wait(&bar->o_done, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
             tc_fence_after();
             const float den = valid ? rpart[r] + rpart[128 + r] + dpart[r] + dpart[128 + r] : 1.f;
             const float inv = 1.f / den;
@@ -317,14 +321,14 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
                 tpart[128 * h + r] = dot;
             }
             fence_proxy_async_smem();
-            grp_sync();
+            FG::sync();
             const float g = valid ? -(tpart[r] + tpart[128 + r]) * inv : 0.f;
             if (h == 0) {
                 gsh[r] = g;
                 if (valid) *reinterpret_cast<float2*>(dgh + (size_t)(c0 + r) * 2) = make_float2(den, g);
             }
             tc_fence_before();
-            grp_sync();
+            FG::sync();
             if (ct == 0) mbar_arrive(&bar->p_ready);
             {
                 // segment sum of g phi(q): weighted column sums of the Q tile
@@ -334,22 +338,22 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
 #pragma unroll
                     for (int e = 0; e < 8; ++e) zp[b][e] = 0.f;
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const uint4 qv = *reinterpret_cast<const uint4*>(sQ + grp_vec_off(ct, j));
+                for (int j = 0; j < FG::kJ; ++j) {
+                    const uint4 qv = *reinterpret_cast<const uint4*>(sQ + FG::vec_off(ct, j));
                     const uint32_t* u = reinterpret_cast<const uint32_t*>(&qv);
-                    const float wr = gsh[grp_vec_row(ct, j)];
+                    const float wr = gsh[FG::vec_row(ct, j)];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        zp[j >> 2][2 * e] = fmaf(wr, bf_lo(u[e]), zp[j >> 2][2 * e]);
-                        zp[j >> 2][2 * e + 1] = fmaf(wr, bf_hi(u[e]), zp[j >> 2][2 * e + 1]);
+                        zp[FG::vec_block(j)][2 * e] = fmaf(wr, bf_lo(u[e]), zp[FG::vec_block(j)][2 * e]);
+                        zp[FG::vec_block(j)][2 * e + 1] = fmaf(wr, bf_hi(u[e]), zp[FG::vec_block(j)][2 * e + 1]);
                     }
                 }
-                grp_column_part(zp, drpart, ct);
+                FG::column_part(zp, drpart, ct);
             }
-            grp_sync();  // every read of Q by the compute group is done
+            FG::sync();  // every read of Q by the compute group is done
             if (ct == 0) mbar_arrive(&bar->empty_qv);
             // (e) D = tril(P V^T + g) as bf16 hi + lo on this thread's keys, in place (see the X layout)
-            if (!grp_all(mbar_wait(&bar->pv_done, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
+            if (!FG::all(mbar_wait(&bar->pv_done, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
             tc_fence_after();
 #pragma unroll
             for (int cb = 0; cb < 2; ++cb) {
@@ -376,12 +380,12 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
             }
             tmem_st_wait();
             tc_fence_before();
-            grp_sync();
+            FG::sync();
             if (ct == 0) mbar_arrive(&bar->d_ready);
             // (f) dq = (dQ~ + g z_prev) * phi'(q), this thread's 64 columns, staged in the Sb
             // tile (free once the dq products are done) and written by one TMA store
             // (rows past N are not written)
-            if (!grp_all(mbar_wait(&bar->dq_done, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
+            if (!FG::all(mbar_wait(&bar->dq_done, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
             tc_fence_after();
 #pragma unroll
             for (int cb = 0; cb < 2; ++cb) {
@@ -406,20 +410,20 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
             }
             fence_proxy_async_smem();
             tc_fence_before();
-            grp_sync();  // the dq tile is complete and z_prev has been used by every thread
+            FG::sync();  // the dq tile is complete and z_prev has been used by every thread
             if (ct == 0) {
                 tma_store_3d(&tm_dq, sSb, 0, c0, bh);
                 tma_store_3d(&tm_dq, sSb + kBlockBytes, 64, c0, bh);
                 bulk_commit();
             }
             if (ct < 128) {
-                zsh[ct] += grp_column_sum(zpart, ct);
-                racc[ct] += grp_column_sum(drpart, ct);
+                zsh[ct] += FG::column_sum(zpart, ct);
+                racc[ct] += FG::column_sum(drpart, ct);
             }
         }
         if (ct == 0) bulk_wait_all();
         // segment sums of the reverse state out: R from TMEM, r from shared memory
-        if (ok && nloc > 0 && grp_all(mbar_wait(&bar->final_mma, 0, err, LA_ERR_TIMEOUT))) {
+        if (ok && nloc > 0 && FG::all(mbar_wait(&bar->final_mma, 0, err, LA_ERR_TIMEOUT))) {
             tc_fence_after();
             float* out = seg_R + ((size_t)bh * P + p) * E;
             tmem_row_to_global<64>(tmem + lb + kFR, out + (size_t)r * kD + 64 * h);
@@ -455,15 +459,15 @@ struct RevSweepSmem {
     static constexpr int Q = 0, K = kTileBytes, V = 2 * kTileBytes, P = 3 * kTileBytes, Rb = 4 * kTileBytes;
     static constexpr int Kc = 5 * kTileBytes;
     static constexpr int rsh = 6 * kTileBytes;  // float[128] r_next
-    static constexpr int rpart = rsh + 512;     // float[8][128] per-warp column sums of this chunk's g phi(q)
-    static constexpr int gsh = rpart + 4096;    // float[128] g den of the chunk's rows
+    static constexpr int rpart = rsh + 512;     // float[16][128] per-warp column sums of this chunk's (g den) Q'
+    static constexpr int gsh = rpart + 8192;    // float[128] g den of the chunk's rows
     static constexpr int ish = gsh + 512;       // float[128] 1/den of the chunk's rows
     static constexpr int bars = ish + 512;
     static constexpr int tmem_slot = bars + 256;
     static constexpr int total = tmem_slot + 16;
 };
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreadsRS, 1)
 tc_bwd_reverse_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                             const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                             const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
@@ -573,15 +577,15 @@ tc_bwd_reverse_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
         }
     } else {
         const int ct = tid - 64;
-        const int h = (warp - 2) >> 2;
+        const int qt = (warp - 2) >> 2;  // column quarter: columns [32 qt, 32 qt + 32)
         const int r = 32 * (warp & 3) + lane;
         const uint32_t lane0 = (uint32_t)(32 * (warp & 3)) << 16;
-        const uint32_t lb = lane0 + 64 * h;
+        const uint32_t lb = lane0 + 32 * qt;
         const float* suf = seg_R + ((size_t)bh * P + p) * E;
-        global_row_to_tmem<64>(suf + (size_t)r * kD + 64 * h, tmem + lb + kRR);  // R_next row r, this half
+        global_row_to_tmem<32>(suf + (size_t)r * kD + 32 * qt, tmem + lb + kRR);  // R_next row r, this quarter
         if (ct < 128) rsh[ct] = suf[(size_t)kD * kD + ct];
         tc_fence_before();
-        bool ok = grp_all(true);
+        bool ok = RG::all(true);
         const float* dgh = den_g + (size_t)bh * N * 2;
         // (den, g) of row ct of chunk ii (rows past N: den 1, g 0); loaded one chunk ahead
         auto load_dg = [&](int ii) {
@@ -599,42 +603,44 @@ tc_bwd_reverse_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
             // (a) per-row 1/den and g den; Q' = phi(Q) / den with the chunk's sum of (g den) Q';
             // phi on K (and its copy)
             if (ct == 0) bulk_wait_read_all();  // the previous dk / dv stores have left Kc and Rb
-            if (!grp_all(mbar_wait(&bar->full, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
+            if (!RG::all(mbar_wait(&bar->full, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
             if (ct < 128) {
                 const bool v = ct < n;
                 ish[ct] = v ? 1.f / dg.x : 0.f;
                 gsh[ct] = v ? dg.y * dg.x : 0.f;
             }
-            grp_sync();
-            grp_phi_tile(sQ, nullptr, ct, n, gsh, rpart, nullptr, ish);
-            grp_phi_tile(sK, nullptr, ct, n, nullptr, nullptr, sKc);
+            RG::sync();
+            RG::phi_tile(sQ, nullptr, ct, n, gsh, rpart, nullptr, ish);
+            RG::phi_tile(sK, nullptr, ct, n, nullptr, nullptr, sKc);
             fence_proxy_async_smem();
-            grp_sync();
+            RG::sync();
             if (ct == 0) mbar_arrive(&bar->ready);
-            // (b) R_next -> bf16 copy (rows = dk; this thread's 64 columns)
-            if (i > 0) {
-                if (!grp_all(mbar_wait(&bar->dkv_done, (i - 1) & 1, err, LA_ERR_TIMEOUT))) { ok = false; break; }
-                tc_fence_after();
+            // (b) R_next -> bf16 copy (rows = dk; this thread's 32 columns).  R is settled:
+            // the previous chunk's dkv_done follows its R update.
+            tc_fence_after();
+            {
+                uint32_t w[32];
+                tmem_ld32(tmem + lb + kRR, w);
+                tmem_ld_wait();
+                row32_to_tile(w, sRb, r, 4 * qt);
             }
-            tmem_half_row_to_tile(tmem + lb + kRR, sRb, r, h);
             tc_fence_before();
             fence_proxy_async_smem();
-            grp_sync();
+            RG::sync();
             if (ct == 0) mbar_arrive(&bar->rb_ready);
-            // (c) masks: row r is key j = r; columns [64h, 64h+64) are queries; keep j <= i
-            if (!grp_all(mbar_wait(&bar->at_dt_done, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
+            // (c) masks: row r is key j = r; columns [32 qt, 32 qt + 32) are queries; keep j <= i
+            if (!RG::all(mbar_wait(&bar->at_dt_done, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
             tc_fence_after();
-#pragma unroll
-            for (int cb = 0; cb < 2; ++cb) {
-                const int q0 = 64 * h + 32 * cb;  // first query of this block
+            {
+                const int q0 = 32 * qt;  // first query of this block
                 uint32_t pa[16], pd[16];
                 if (q0 + 31 < r) {  // every query here is before key r: all masked
 #pragma unroll
                     for (int x = 0; x < 16; ++x) pa[x] = pd[x] = 0u;
                 } else {
                     uint32_t wa[32], wd[32];
-                    tmem_ld32(tmem + lb + kRDV + 32 * cb, wa);
-                    tmem_ld32(tmem + lb + kRDK + 32 * cb, wd);
+                    tmem_ld32(tmem + lb + kRDV, wa);
+                    tmem_ld32(tmem + lb + kRDK, wd);
                     tmem_ld_wait();
 #pragma unroll
                     for (int x = 0; x < 16; ++x) {
@@ -645,32 +651,31 @@ tc_bwd_reverse_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
                                             r <= qi + 1 ? __uint_as_float(wd[2 * x + 1]) + gsh[qi + 1] : 0.f);
                     }
                 }
-                tmem_st16(lane0 + tmem + kRX + 64 + 32 * h + 16 * cb, pa);
-                tmem_st16(lane0 + tmem + kRX + 32 * h + 16 * cb, pd);
+                tmem_st16(lane0 + tmem + kRX + 64 + 16 * qt, pa);
+                tmem_st16(lane0 + tmem + kRX + 16 * qt, pd);
+                tmem_st_wait();
             }
-            tmem_st_wait();
             tc_fence_before();
-            grp_sync();
+            RG::sync();
             if (ct == 0) mbar_arrive(&bar->masks_ready);
             // (d) dk = (dK~ + r_next) * phi'(k) in place of phi(k) in Kc, dv into Rb; this
-            // thread's 64 columns of key row r; one TMA store each (rows past N are not written)
-            if (!grp_all(mbar_wait(&bar->dkv_done, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
+            // thread's 32 columns of key row r; one TMA store each (rows past N are not written)
+            if (!RG::all(mbar_wait(&bar->dkv_done, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
             tc_fence_after();
-#pragma unroll
-            for (int cb = 0; cb < 2; ++cb) {
+            {
                 uint32_t w[32];
-                tmem_ld32(tmem + lb + kRDK + 32 * cb, w);
+                tmem_ld32(tmem + lb + kRDK, w);
                 tmem_ld_wait();
 #pragma unroll
                 for (int c4 = 0; c4 < 4; ++c4) {
-                    uint4* kp = reinterpret_cast<uint4*>(sKc + chunk_off(r, 8 * h + 4 * cb + c4));
+                    uint4* kp = reinterpret_cast<uint4*>(sKc + chunk_off(r, 4 * qt + c4));
                     const uint4 kv = *kp;
                     const uint32_t* ku = reinterpret_cast<const uint32_t*>(&kv);
                     uint4 o4;
                     uint32_t* ou = reinterpret_cast<uint32_t*>(&o4);
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const int d = 64 * h + 32 * cb + 8 * c4 + 2 * e;
+                        const int d = 32 * qt + 8 * c4 + 2 * e;
                         ou[e] = pack_bf16x2((__uint_as_float(w[8 * c4 + 2 * e]) + rsh[d]) * dphi_from_phi(bf_lo(ku[e])),
                                             (__uint_as_float(w[8 * c4 + 2 * e + 1]) + rsh[d + 1]) *
                                                 dphi_from_phi(bf_hi(ku[e])));
@@ -678,17 +683,16 @@ tc_bwd_reverse_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
                     *kp = o4;
                 }
             }
-#pragma unroll
-            for (int cb = 0; cb < 2; ++cb) {
+            {
                 uint32_t w[32];
-                tmem_ld32(tmem + lb + kRDV + 32 * cb, w);
+                tmem_ld32(tmem + lb + kRDV, w);
                 tmem_ld_wait();
-                row32_to_tile(w, sRb, r, 8 * h + 4 * cb);
+                row32_to_tile(w, sRb, r, 4 * qt);
             }
             // (e) stores out; r_next += this chunk's sum of g phi(q) (every thread has used r_next)
             fence_proxy_async_smem();
             tc_fence_before();
-            grp_sync();
+            RG::sync();
             if (ct == 0) {
                 tma_store_3d(&tm_dk, sKc, 0, c0, bh);
                 tma_store_3d(&tm_dk, sKc + kBlockBytes, 64, c0, bh);
@@ -696,7 +700,7 @@ tc_bwd_reverse_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
                 tma_store_3d(&tm_dv, sRb + kBlockBytes, 64, c0, bh);
                 bulk_commit();
             }
-            if (ct < 128) rsh[ct] += grp_column_sum(rpart, ct);
+            if (ct < 128) rsh[ct] += RG::column_sum(rpart, ct);
         }
         if (ct == 0) bulk_wait_all();
         tc_fence_before();
@@ -727,7 +731,7 @@ cudaError_t tc_bwd_forward_sweep(const void* q, const void* k, const void* v, co
                                          (int)kFwdSweepSmem);
     if (e != cudaSuccess) return e;
     launch_begin("tc_bwd_forward_sweep", st);
-    tc_bwd_forward_sweep_kernel<<<dim3(p.P, BH), kThreads, kFwdSweepSmem, st>>>(
+    tc_bwd_forward_sweep_kernel<<<dim3(p.P, BH), kThreadsFS, kFwdSweepSmem, st>>>(
         tq, tk, tv, td, tdq, seg_S, seg_R, den_g, s.N, p.nchunks, p.cps, p.P, device_error_word());
     return launch_end("tc_bwd_forward_sweep", st);
 }
@@ -746,7 +750,7 @@ cudaError_t tc_bwd_reverse_sweep(const void* q, const void* k, const void* v, co
                                          (int)kRevSweepSmem);
     if (e != cudaSuccess) return e;
     launch_begin("tc_bwd_reverse_sweep", st);
-    tc_bwd_reverse_sweep_kernel<<<dim3(p.P, BH), kThreads, kRevSweepSmem, st>>>(
+    tc_bwd_reverse_sweep_kernel<<<dim3(p.P, BH), kThreadsRS, kRevSweepSmem, st>>>(
         tq, tk, tv, td, tdk, tdv, seg_R, den_g, s.N, p.nchunks, p.cps, p.P, device_error_word());
     return launch_end("tc_bwd_reverse_sweep", st);
 }

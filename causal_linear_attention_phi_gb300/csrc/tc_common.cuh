@@ -93,107 +93,114 @@ __device__ __forceinline__ void tmem_half_row_to_tile(uint32_t taddr, uint8_t* t
     }
 }
 
-// ------------------------------------------------------------------ 256-thread compute group
-// Warps 2-9 of a CTA: thread ct = tid - 64.  For row-wise TMEM work, warp w owns
-// TMEM lanes 32*(w%4) .. +31 and column half h = (w - 2) / 4 of those rows.  For
-// whole-tile elementwise work, thread ct owns the 16-byte vectors ct + 256 j
-// (j < 8): block j / 4, row ((ct >> 3) + 32 j) & 127, physical chunk ct & 7,
-// logical chunk lc = (ct & 7) ^ ((ct >> 3) & 7), i.e. columns 64*(j/4) + 8*lc + e.
-constexpr int kGroupThreads = 256;
+// ------------------------------------------------------------------ compute group
+// The compute warps of a CTA (G threads, G = 256 or 512): thread ct = tid - 64
+// (warps 0 and 1 are the TMA and MMA roles).  For whole-tile elementwise work,
+// thread ct owns the 16-byte vectors ct + G j (j < 2048 / G): block j / (J / 2),
+// row ((ct >> 3) + (G / 8) (j % (J / 2))) & 127, physical chunk ct & 7, logical
+// chunk lc = (ct & 7) ^ ((ct >> 3) & 7), i.e. columns 64 block + 8 lc + e.
+template <int G>
+struct Grp {
+    static_assert(G == 256 || G == 512, "compute group of 8 or 16 warps");
+    static constexpr int kJ = 2048 / G;  // 16-byte vectors of a 128 x 128 bf16 tile per thread
+    static constexpr int kWarps = G / 32;
 
-__device__ __forceinline__ bool grp_all(bool v) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.and.pred q, 1, 256, p;\n\t"
-        "selp.u32 %0, 1, 0, q;\n\t}"
-        : "=r"(r)
-        : "r"((uint32_t)v)
-        : "memory");
-    return r != 0;
-}
-__device__ __forceinline__ void grp_sync() { named_barrier(1, kGroupThreads); }
-
-__device__ __forceinline__ int grp_vec_row(int ct, int j) { return ((ct >> 3) + 32 * j) & 127; }
-__device__ __forceinline__ int grp_vec_off(int ct, int j) {
-    return (j >> 2) * kBlockBytes + grp_vec_row(ct, j) * 128 + (ct & 7) * 16;
-}
-__device__ __forceinline__ int grp_vec_lc(int ct) { return (ct & 7) ^ ((ct >> 3) & 7); }
-
-// Column partial sums zp[block][e] (for columns 64*block + 8*lc + e of this
-// thread) summed over the four lanes of the warp that share lc (lanes l, l^9,
-// l^18, l^27) and stored by lanes 0-7 as this warp's row of part[8][128]
-// (no atomics: the eight warps' rows are added by grp_column_sum after a
-// group barrier).
-__device__ __forceinline__ void grp_column_part(float (&zp)[2][8], float* part, int ct) {
-#pragma unroll
-    for (int b = 0; b < 2; ++b)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            float x = zp[b][e];
-            x += __shfl_xor_sync(0xffffffffu, x, 9);
-            x += __shfl_xor_sync(0xffffffffu, x, 18);
-            zp[b][e] = x;
-        }
-    if ((ct & 31) < 8) {
-        float* row = part + (ct >> 5) * 128 + 8 * grp_vec_lc(ct);
-#pragma unroll
-        for (int b = 0; b < 2; ++b) {
-            *reinterpret_cast<float4*>(row + 64 * b) = make_float4(zp[b][0], zp[b][1], zp[b][2], zp[b][3]);
-            *reinterpret_cast<float4*>(row + 64 * b + 4) = make_float4(zp[b][4], zp[b][5], zp[b][6], zp[b][7]);
-        }
+    // Barrier over the group (named barrier 1) that ANDs a predicate across it,
+    // so every thread takes the same branch after a bounded wait.
+    __device__ static __forceinline__ bool all(bool v) {
+        uint32_t r;
+        asm volatile(
+            "{\n\t.reg .pred p, q;\n\t"
+            "setp.ne.u32 p, %1, 0;\n\t"
+            "bar.red.and.pred q, 1, %2, p;\n\t"
+            "selp.u32 %0, 1, 0, q;\n\t}"
+            : "=r"(r)
+            : "r"((uint32_t)v), "n"(G)
+            : "memory");
+        return r != 0;
     }
-}
-// Column c (0..127) of part[8][128] summed over the eight warps.
-__device__ __forceinline__ float grp_column_sum(const float* part, int c) {
-    float s = 0.f;
-#pragma unroll
-    for (int w = 0; w < 8; ++w) s += part[128 * w + c];
-    return s;
-}
+    __device__ static __forceinline__ void sync() { named_barrier(1, G); }
 
-// phi in place on a staged tile (rows >= n exactly 0), times scale[row] when
-// scale is given.  With colpart, the column sums of the rounded values
-// (weighted by w[row] when w is given) go to colpart[8][128] as per-warp
-// partials (see grp_column_part).  With lo_tile, also writes lo = bf16(phi -
-// hi) there; with copy_tile, a second copy of the rounded values.
-__device__ __forceinline__ void grp_phi_tile(uint8_t* tile, uint8_t* lo_tile, int ct, int n, const float* w,
-                                             float* colpart, uint8_t* copy_tile = nullptr,
-                                             const float* scale = nullptr) {
-    float zp[2][8];
+    __device__ static __forceinline__ int vec_block(int j) { return j / (kJ / 2); }
+    __device__ static __forceinline__ int vec_row(int ct, int j) { return ((ct >> 3) + (G / 8) * (j % (kJ / 2))) & 127; }
+    __device__ static __forceinline__ int vec_off(int ct, int j) {
+        return vec_block(j) * kBlockBytes + vec_row(ct, j) * 128 + (ct & 7) * 16;
+    }
+    __device__ static __forceinline__ int vec_lc(int ct) { return (ct & 7) ^ ((ct >> 3) & 7); }
+
+    // Column partial sums zp[block][e] (for columns 64 block + 8 lc + e of this
+    // thread) summed over the four lanes of the warp that share lc (lanes l,
+    // l^9, l^18, l^27) and stored by lanes 0-7 as this warp's row of
+    // part[kWarps][128] (no atomics: column_sum adds the rows after a barrier).
+    __device__ static __forceinline__ void column_part(float (&zp)[2][8], float* part, int ct) {
 #pragma unroll
-    for (int b = 0; b < 2; ++b)
+        for (int b = 0; b < 2; ++b)
 #pragma unroll
-        for (int e = 0; e < 8; ++e) zp[b][e] = 0.f;
-    uint4 v[8];
+            for (int e = 0; e < 8; ++e) {
+                float x = zp[b][e];
+                x += __shfl_xor_sync(0xffffffffu, x, 9);
+                x += __shfl_xor_sync(0xffffffffu, x, 18);
+                zp[b][e] = x;
+            }
+        if ((ct & 31) < 8) {
+            float* row = part + (ct >> 5) * 128 + 8 * vec_lc(ct);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) v[j] = *reinterpret_cast<const uint4*>(tile + grp_vec_off(ct, j));
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const int row = grp_vec_row(ct, j);
-        uint32_t* u = reinterpret_cast<uint32_t*>(&v[j]);
-        uint4 l;
-        uint32_t* ul = reinterpret_cast<uint32_t*>(&l);
-        const bool valid = row < n;
-        const float wr = (w && valid) ? w[row] : 1.f;
-        const float sr = scale ? scale[row] : 1.f;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float a = valid ? phi_f(bf_lo(u[e])) * sr : 0.f, b = valid ? phi_f(bf_hi(u[e])) * sr : 0.f;
-            u[e] = pack_bf16x2(a, b);
-            ul[e] = pack_bf16x2(a - bf_lo(u[e]), b - bf_hi(u[e]));
-            if (colpart) {
-                zp[j >> 2][2 * e] = fmaf(wr, bf_lo(u[e]), zp[j >> 2][2 * e]);
-                zp[j >> 2][2 * e + 1] = fmaf(wr, bf_hi(u[e]), zp[j >> 2][2 * e + 1]);
+            for (int b = 0; b < 2; ++b) {
+                *reinterpret_cast<float4*>(row + 64 * b) = make_float4(zp[b][0], zp[b][1], zp[b][2], zp[b][3]);
+                *reinterpret_cast<float4*>(row + 64 * b + 4) = make_float4(zp[b][4], zp[b][5], zp[b][6], zp[b][7]);
             }
         }
-        *reinterpret_cast<uint4*>(tile + grp_vec_off(ct, j)) = v[j];
-        if (lo_tile) *reinterpret_cast<uint4*>(lo_tile + grp_vec_off(ct, j)) = l;
-        if (copy_tile) *reinterpret_cast<uint4*>(copy_tile + grp_vec_off(ct, j)) = v[j];
     }
-    if (colpart) grp_column_part(zp, colpart, ct);
-}
+    // Column c (0..127) of part[kWarps][128] summed over the warps.
+    __device__ static __forceinline__ float column_sum(const float* part, int c) {
+        float s = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) s += part[128 * w + c];
+        return s;
+    }
+
+    // phi in place on a staged tile (rows >= n exactly 0), times scale[row]
+    // when scale is given.  With colpart, the column sums of the rounded values
+    // (weighted by w[row] when w is given) go to colpart as per-warp partials
+    // (column_part).  With lo_tile, also writes lo = bf16(phi - hi) there; with
+    // copy_tile, a second copy of the rounded values.
+    __device__ static __forceinline__ void phi_tile(uint8_t* tile, uint8_t* lo_tile, int ct, int n, const float* w,
+                                                    float* colpart, uint8_t* copy_tile = nullptr,
+                                                    const float* scale = nullptr) {
+        float zp[2][8];
+#pragma unroll
+        for (int b = 0; b < 2; ++b)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) zp[b][e] = 0.f;
+        uint4 v[kJ];
+#pragma unroll
+        for (int j = 0; j < kJ; ++j) v[j] = *reinterpret_cast<const uint4*>(tile + vec_off(ct, j));
+#pragma unroll
+        for (int j = 0; j < kJ; ++j) {
+            const int row = vec_row(ct, j);
+            uint32_t* u = reinterpret_cast<uint32_t*>(&v[j]);
+            uint4 l;
+            uint32_t* ul = reinterpret_cast<uint32_t*>(&l);
+            const bool valid = row < n;
+            const float wr = (w && valid) ? w[row] : 1.f;
+            const float sr = scale ? scale[row] : 1.f;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float a = valid ? phi_f(bf_lo(u[e])) * sr : 0.f, b = valid ? phi_f(bf_hi(u[e])) * sr : 0.f;
+                u[e] = pack_bf16x2(a, b);
+                ul[e] = pack_bf16x2(a - bf_lo(u[e]), b - bf_hi(u[e]));
+                if (colpart) {
+                    zp[vec_block(j)][2 * e] = fmaf(wr, bf_lo(u[e]), zp[vec_block(j)][2 * e]);
+                    zp[vec_block(j)][2 * e + 1] = fmaf(wr, bf_hi(u[e]), zp[vec_block(j)][2 * e + 1]);
+                }
+            }
+            *reinterpret_cast<uint4*>(tile + vec_off(ct, j)) = v[j];
+            if (lo_tile) *reinterpret_cast<uint4*>(lo_tile + vec_off(ct, j)) = l;
+            if (copy_tile) *reinterpret_cast<uint4*>(copy_tile + vec_off(ct, j)) = v[j];
+        }
+        if (colpart) column_part(zp, colpart, ct);
+    }
+};
 
 }  // namespace tc
 

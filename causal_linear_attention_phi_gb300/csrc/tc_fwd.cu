@@ -36,7 +36,8 @@ using namespace sm100;
 using namespace tc;
 
 constexpr int kThreads = 320;  // warp 0 TMA, warp 1 MMA, warps 2-9 compute
-constexpr int kComputeThreads = kGroupThreads;
+constexpr int kComputeThreads = 256;
+using CG = Grp<kComputeThreads>;
 constexpr int kSmallBytes = 4096;  // a 16-row x 128-column bf16 K-major operand (two 2 KB blocks)
 
 // TMEM column map (512 columns allocated)
@@ -237,23 +238,23 @@ tc_causal_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             tmem_st_wait();
         }
         tc_fence_before();
-        bool ok = grp_all(true);
+        bool ok = CG::all(true);
         for (int i = 0; i < nloc && ok; ++i) {
             const int s = i & 1;
             const int c0 = (cbeg + i) * kC, n = min(kC, N - c0);
             // (a) phi on the K (and Q) tiles
             bool w = mbar_wait(&bar->kv_full[s], (i >> 1) & 1, err, LA_ERR_TIMEOUT);
             if (kOut) w = w && mbar_wait(&bar->q_full, i & 1, err, LA_ERR_TIMEOUT);
-            if (!grp_all(w)) { ok = false; break; }
-            grp_phi_tile(sK(s), nullptr, ct, n, nullptr, nullptr);
-            if (kOut) grp_phi_tile(sQ, nullptr, ct, n, nullptr, nullptr);
+            if (!CG::all(w)) { ok = false; break; }
+            CG::phi_tile(sK(s), nullptr, ct, n, nullptr, nullptr);
+            if (kOut) CG::phi_tile(sQ, nullptr, ct, n, nullptr, nullptr);
             fence_proxy_async_smem();
-            grp_sync();
+            CG::sync();
             if (ct == 0) mbar_arrive(&bar->qk_ready[s]);
             if (!kOut) continue;
             // (b) S_prev, z_prev -> bf16 operands (row r = dk, this thread's 64 dv columns = block h)
             if (i > 0) {
-                if (!grp_all(mbar_wait(&bar->s_done, (i - 1) & 1, err, LA_ERR_TIMEOUT))) { ok = false; break; }
+                if (!CG::all(mbar_wait(&bar->s_done, (i - 1) & 1, err, LA_ERR_TIMEOUT))) { ok = false; break; }
                 tc_fence_after();
             }
 #pragma unroll
@@ -279,10 +280,10 @@ tc_causal_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             }
             tc_fence_before();
             fence_proxy_async_smem();
-            grp_sync();
+            CG::sync();
             if (ct == 0) mbar_arrive(&bar->sb_ready);
             // (c) A = tril(QK^T) on keys [64 h, 64 h + 64) -> bf16 pairs into TMEM columns [32 h, 32 h + 32)
-            if (!grp_all(mbar_wait(&bar->qk_done, i & 1, err, LA_ERR_TIMEOUT))) { ok = false; break; }
+            if (!CG::all(mbar_wait(&bar->qk_done, i & 1, err, LA_ERR_TIMEOUT))) { ok = false; break; }
             tc_fence_after();
 #pragma unroll
             for (int cb = 0; cb < 2; ++cb) {
@@ -310,10 +311,10 @@ tc_causal_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             }
             tmem_st_wait();
             tc_fence_before();
-            grp_sync();
+            CG::sync();
             if (ct == 0) mbar_arrive(&bar->a_ready);
             // (d) o = O / den on this thread's 64 columns
-            if (!grp_all(mbar_wait(&bar->o_done, i & 1, err, LA_ERR_TIMEOUT))) { ok = false; break; }
+            if (!CG::all(mbar_wait(&bar->o_done, i & 1, err, LA_ERR_TIMEOUT))) { ok = false; break; }
             tc_fence_after();
             uint32_t dv[16];
             tmem_ld16(tmem + lane_base + kTmDen, dv);
@@ -342,7 +343,7 @@ tc_causal_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         if (!kOut && ok && nloc > 0) {
             // segment sums out: S row r (this thread's 64 columns) and z[r] from TMEM.  The MMA
             // thread's single-use drain barrier marks the last update done.
-            if (grp_all(mbar_wait(&bar->final_mma, 0, err, LA_ERR_TIMEOUT))) {
+            if (CG::all(mbar_wait(&bar->final_mma, 0, err, LA_ERR_TIMEOUT))) {
                 tc_fence_after();
                 float* out = segp + (size_t)r * kD + 64 * h;
 #pragma unroll
