@@ -2,9 +2,10 @@
 
 Default workload: causal forward + backward, bf16 inputs with fp32
 accumulation, B=2 H=16 N=65536 Dk=Dv=128 (Q, K ~ N(0,1)/sqrt(128), V, dO ~
-N(0,1), seed 5).  One step = la_causal_fwd + la_causal_bwd over that batch
-(feature map, intra-chunk products, chunk-state scan, backward with states
-recomputed).  The inputs (2.1 GB) are far larger than L2, so consecutive steps
+N(0,1), seed 5).  One step = la_causal_fwd + la_causal_bwd_after_fwd over that
+batch (feature map, intra-chunk products, chunk-state scan; the backward takes
+the per-segment forward states from the forward's workspace and recomputes
+everything per position).  The inputs (2.1 GB) are far larger than L2, so consecutive steps
 cannot reuse cached data.
 
 Printed on rank 0 as one JSON line:
@@ -206,7 +207,7 @@ def run_ours(args):
 
     def step():
         la.causal_fwd(qd, kd, vd, out=o, workspace=ws_f)
-        la.causal_bwd(qd, kd, vd, dOd, dq=dq, dk=dk, dv=dv, workspace=ws_b)
+        la.causal_bwd(qd, kd, vd, dOd, dq=dq, dk=dk, dv=dv, workspace=ws_b, fwd_workspace=ws_f)
 
     def barrier():
         if ws_n > 1:
@@ -479,7 +480,7 @@ def run_sweep(args):
 
         def step():
             la.causal_fwd(qd, kd, vd, out=o, workspace=wsf)
-            la.causal_bwd(qd, kd, vd, dOd, dq=dq, dk=dk, dv=dv, workspace=wsb)
+            la.causal_bwd(qd, kd, vd, dOd, dq=dq, dk=dk, dv=dv, workspace=wsb, fwd_workspace=wsf)
 
         for _ in range(args.warmup):
             step()

@@ -56,8 +56,10 @@ def _declare(lib):
     lib.la_noncausal_fwd.argtypes = [_vp, _vp, _vp, _vp, Shape, _vp, ctypes.c_size_t, _vp]
     lib.la_causal_fwd.argtypes = [_vp, _vp, _vp, _vp, Shape, _vp, ctypes.c_size_t, _vp]
     lib.la_causal_bwd.argtypes = [_vp] * 7 + [Shape, _vp, ctypes.c_size_t, _vp]
+    lib.la_causal_bwd_after_fwd.argtypes = [_vp] * 7 + [Shape, _vp, ctypes.c_size_t, _vp, ctypes.c_size_t, _vp]
     lib.la_recurrent_step.argtypes = [_vp] * 6 + [Shape, _vp]
-    for f in ("la_noncausal_fwd", "la_causal_fwd", "la_causal_bwd", "la_recurrent_step", "la_last_error",
+    for f in ("la_noncausal_fwd", "la_causal_fwd", "la_causal_bwd", "la_causal_bwd_after_fwd", "la_recurrent_step",
+              "la_last_error",
               "la_clear_error", "la_timing_enable", "la_timing_reset"):
         getattr(lib, f).restype = ctypes.c_int
     lib.la_last_error.argtypes = []
@@ -140,7 +142,9 @@ def workspace_bytes(op: int, B: int, H: int, N: int, Dk: int, Dv: int, dtype: to
 def _workspace(op, s: Shape, device, workspace):
     need = int(library().la_workspace_bytes(op, s))
     if workspace is not None:
-        return workspace, max(need, workspace.numel())
+        if not workspace.is_cuda:
+            raise ValueError("workspace must be a device tensor")
+        return workspace, workspace.numel() * workspace.element_size()  # its real size: the library checks it
     if need == 0:
         return None, 0
     return torch.empty(need, dtype=torch.uint8, device=device), need
@@ -170,8 +174,13 @@ def causal_fwd(q, k, v, out=None, workspace=None, stream=None):
     return out
 
 
-def causal_bwd(q, k, v, dout, dq=None, dk=None, dv=None, workspace=None, stream=None):
-    """Gradients (dq, dk, dv) of the causal form for upstream gradient dout; states are recomputed."""
+def causal_bwd(q, k, v, dout, dq=None, dk=None, dv=None, workspace=None, stream=None, fwd_workspace=None):
+    """Gradients (dq, dk, dv) of the causal form for upstream gradient dout.
+
+    With fwd_workspace (the workspace of the causal_fwd call on the same q, k,
+    v, unchanged since), the per-segment forward states are read from it
+    (la_causal_bwd_after_fwd); otherwise they are recomputed (la_causal_bwd).
+    """
     _need_cuda(q, k, v, dout)
     s = _shape4(q, k, v)
     if dout.shape != v.shape or dout.dtype != v.dtype:
@@ -180,8 +189,16 @@ def causal_bwd(q, k, v, dout, dq=None, dk=None, dv=None, workspace=None, stream=
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
     ws, nb = _workspace(OP_CAUSAL_BWD, s, q.device, workspace)
-    _check(library().la_causal_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), s, _ptr(ws),
-                                   nb, _stream_ptr(stream)), "la_causal_bwd")
+    if fwd_workspace is None:
+        _check(library().la_causal_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), s,
+                                       _ptr(ws), nb, _stream_ptr(stream)), "la_causal_bwd")
+    else:
+        if not fwd_workspace.is_cuda:
+            raise ValueError("fwd_workspace must be the device workspace of the forward call")
+        fnb = fwd_workspace.numel() * fwd_workspace.element_size()
+        _check(library().la_causal_bwd_after_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
+                                                 s, _ptr(fwd_workspace), fnb, _ptr(ws), nb, _stream_ptr(stream)),
+               "la_causal_bwd_after_fwd")
     return dq, dk, dv
 
 

@@ -286,6 +286,46 @@ void clear_detail() { t_detail.clear(); }
 
 using namespace la;
 
+namespace {
+
+// The two backward sweeps and the reverse scan between them; segS holds the
+// exclusive prefix state of every segment.
+static la_status causal_bwd_sweeps(const void* q, const void* k, const void* v, const void* dout, void* dq, void* dk,
+                                   void* dv, const la_shape& s, const Plan& p, const float* segS, char* base,
+                                   const WsLayout& w, cudaStream_t st) {
+    float* segR = reinterpret_cast<float*>(base + w.seg_states2);
+    float* den_g = reinterpret_cast<float*>(base + w.den_g);
+    if (p.tc) {
+        LA_TRY(cuda_status(tc_bwd_forward_sweep(q, k, v, dout, dq, segS, segR, den_g, s, p, st),
+                           "backward forward sweep"));
+        LA_TRY(cuda_status(scan_segments(segR, nullptr, s, p, SCAN_EXCLUSIVE_SUFFIX, st), "reverse scan"));
+        LA_TRY(cuda_status(tc_bwd_reverse_sweep(q, k, v, dout, dk, dv, segR, den_g, s, p, st),
+                           "backward reverse sweep"));
+    } else {
+        LA_TRY(cuda_status(simt_bwd_forward_sweep(q, k, v, dout, dq, segS, segR, den_g, s, p, st),
+                           "backward forward sweep"));
+        LA_TRY(cuda_status(scan_segments(segR, nullptr, s, p, SCAN_EXCLUSIVE_SUFFIX, st), "reverse scan"));
+        LA_TRY(cuda_status(simt_bwd_reverse_sweep(q, k, v, dout, dk, dv, segR, den_g, s, p, st),
+                           "backward reverse sweep"));
+    }
+    return LA_OK;
+}
+
+static la_status check_bwd_args(const void* q, const void* k, const void* v, const void* dout, const void* dq,
+                                const void* dk, const void* dv) {
+    LA_TRY(check_device());
+    LA_TRY(check_ptr(q, "q"));
+    LA_TRY(check_ptr(k, "k"));
+    LA_TRY(check_ptr(v, "v"));
+    LA_TRY(check_ptr(dout, "dout"));
+    LA_TRY(check_ptr(dq, "dq"));
+    LA_TRY(check_ptr(dk, "dk"));
+    LA_TRY(check_ptr(dv, "dv"));
+    return LA_OK;
+}
+
+}  // namespace
+
 extern "C" {
 
 size_t la_workspace_bytes(int op, la_shape s) {
@@ -354,22 +394,13 @@ la_status la_causal_bwd(const void* q, const void* k, const void* v, const void*
     t_detail.clear();
     LA_TRY(check_shape(s));
     if (empty(s)) return LA_OK;
-    LA_TRY(check_device());
-    LA_TRY(check_ptr(q, "q"));
-    LA_TRY(check_ptr(k, "k"));
-    LA_TRY(check_ptr(v, "v"));
-    LA_TRY(check_ptr(dout, "dout"));
-    LA_TRY(check_ptr(dq, "dq"));
-    LA_TRY(check_ptr(dk, "dk"));
-    LA_TRY(check_ptr(dv, "dv"));
+    LA_TRY(check_bwd_args(q, k, v, dout, dq, dk, dv));
     const Plan p = make_plan(s, LA_OP_CAUSAL_BWD);
     const WsLayout w = make_ws_layout(s, LA_OP_CAUSAL_BWD, p);
     LA_TRY(check_ws(ws, ws_bytes, w.bytes));
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     char* base = static_cast<char*>(ws);
     float* segS = reinterpret_cast<float*>(base + w.seg_states);
-    float* segR = reinterpret_cast<float*>(base + w.seg_states2);
-    float* den_g = reinterpret_cast<float*>(base + w.den_g);
     const size_t seg_bytes = (size_t)s.B * s.H * p.P * state_elems(s.Dk, s.Dv) * sizeof(float);
     if (p.P > 1) {
         if (p.tc)
@@ -380,20 +411,29 @@ la_status la_causal_bwd(const void* q, const void* k, const void* v, const void*
     } else {
         LA_TRY(cuda_status(cudaMemsetAsync(segS, 0, seg_bytes, st), "state clear"));
     }
-    if (p.tc) {
-        LA_TRY(cuda_status(tc_bwd_forward_sweep(q, k, v, dout, dq, segS, segR, den_g, s, p, st),
-                           "backward forward sweep"));
-        LA_TRY(cuda_status(scan_segments(segR, nullptr, s, p, SCAN_EXCLUSIVE_SUFFIX, st), "reverse scan"));
-        LA_TRY(cuda_status(tc_bwd_reverse_sweep(q, k, v, dout, dk, dv, segR, den_g, s, p, st),
-                           "backward reverse sweep"));
-    } else {
-        LA_TRY(cuda_status(simt_bwd_forward_sweep(q, k, v, dout, dq, segS, segR, den_g, s, p, st),
-                           "backward forward sweep"));
-        LA_TRY(cuda_status(scan_segments(segR, nullptr, s, p, SCAN_EXCLUSIVE_SUFFIX, st), "reverse scan"));
-        LA_TRY(cuda_status(simt_bwd_reverse_sweep(q, k, v, dout, dk, dv, segR, den_g, s, p, st),
-                           "backward reverse sweep"));
-    }
-    return LA_OK;
+    return causal_bwd_sweeps(q, k, v, dout, dq, dk, dv, s, p, segS, base, w, st);
+}
+
+la_status la_causal_bwd_after_fwd(const void* q, const void* k, const void* v, const void* dout, void* dq, void* dk,
+                                  void* dv, la_shape s, const void* fwd_ws, size_t fwd_ws_bytes, void* ws,
+                                  size_t ws_bytes, la_stream_t stream) {
+    t_detail.clear();
+    LA_TRY(check_shape(s));
+    if (empty(s)) return LA_OK;
+    LA_TRY(check_bwd_args(q, k, v, dout, dq, dk, dv));
+    const Plan p = make_plan(s, LA_OP_CAUSAL_BWD);
+    const Plan pf = make_plan(s, LA_OP_CAUSAL_FWD);
+    if (pf.P != p.P || pf.C != p.C)  // the forward's segments are the backward's (same planner)
+        return fail(LA_ERR_UNSUPPORTED, "forward and backward segmentations differ (P %d vs %d)", pf.P, p.P);
+    const WsLayout wf = make_ws_layout(s, LA_OP_CAUSAL_FWD, pf);
+    if (fwd_ws_bytes < wf.bytes)
+        return fail(LA_ERR_WORKSPACE, "forward workspace of %zu bytes, the forward needs %zu", fwd_ws_bytes, wf.bytes);
+    LA_TRY(check_ptr(fwd_ws, "fwd_ws"));
+    const WsLayout w = make_ws_layout(s, LA_OP_CAUSAL_BWD, p);
+    LA_TRY(check_ws(ws, ws_bytes, w.bytes));
+    const float* segS = reinterpret_cast<const float*>(static_cast<const char*>(fwd_ws) + wf.seg_states);
+    return causal_bwd_sweeps(q, k, v, dout, dq, dk, dv, s, p, segS, static_cast<char*>(ws), w,
+                             reinterpret_cast<cudaStream_t>(stream));
 }
 
 la_status la_recurrent_step(const void* q, const void* k, const void* v, float* S, float* z, void* out, la_shape s,

@@ -56,7 +56,7 @@ struct SmemLayout {
     static constexpr int Q = 0;
     static constexpr int K0 = Q + kTileBytes;       // K stages 0, 1
     static constexpr int V0 = K0 + 2 * kTileBytes;  // V stages 0, 1
-    static constexpr int Sb = V0 + 2 * kTileBytes;  // bf16 S_prev, rows = dk
+    static constexpr int Sb = V0 + 2 * kTileBytes;  // bf16 S_prev (rows = dk); once O is done, the o tile for its TMA store
     static constexpr int Ones = Sb + kTileBytes;    // 16 x 128: row 0 ones, rows 1-15 zero
     static constexpr int Zb = Ones + kSmallBytes;   // 16 x 128: row 0 bf16 z_prev, rows 1-15 zero
     static constexpr int bars = Zb + kSmallBytes;
@@ -77,7 +77,7 @@ __device__ __forceinline__ int small_row0_off(int col) {
 template <bool kOut>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_causal_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                     const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16* __restrict__ o,
+                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                      float* __restrict__ seg, int N, int nchunks, int cps, int P, int* err) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -103,7 +103,10 @@ tc_causal_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         fence_mbar_init();
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
-        if (kOut) tma_prefetch_desc(&tm_q);
+        if (kOut) {
+            tma_prefetch_desc(&tm_q);
+            tma_prefetch_desc(&tm_o);
+        }
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, 512);
@@ -243,6 +246,7 @@ tc_causal_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             const int s = i & 1;
             const int c0 = (cbeg + i) * kC, n = min(kC, N - c0);
             // (a) phi on the K (and Q) tiles
+            if (kOut && ct == 0) bulk_wait_read_all();  // the previous o store has left the Sb tile
             bool w = mbar_wait(&bar->kv_full[s], (i >> 1) & 1, err, LA_ERR_TIMEOUT);
             if (kOut) w = w && mbar_wait(&bar->q_full, i & 1, err, LA_ERR_TIMEOUT);
             if (!CG::all(w)) { ok = false; break; }
@@ -313,33 +317,39 @@ tc_causal_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             tc_fence_before();
             CG::sync();
             if (ct == 0) mbar_arrive(&bar->a_ready);
-            // (d) o = O / den on this thread's 64 columns
+            // (d) o = O / den on this thread's 64 columns, staged in the Sb tile (free once
+            // O is complete) and written by one TMA store (rows past N are not written)
             if (!CG::all(mbar_wait(&bar->o_done, i & 1, err, LA_ERR_TIMEOUT))) { ok = false; break; }
             tc_fence_after();
             uint32_t dv[16];
             tmem_ld16(tmem + lane_base + kTmDen, dv);
             tmem_ld_wait();
             const float inv = 1.f / __uint_as_float(dv[0]);
-            __nv_bfloat16* orow = o + ((size_t)bh * N + c0 + r) * kD + 64 * h;
 #pragma unroll
             for (int cb = 0; cb < 2; ++cb) {
                 uint32_t wv[32];
                 tmem_ld32(tmem + lane_base + kTmO + 64 * h + 32 * cb, wv);
                 tmem_ld_wait();
-                if (r < n) {
 #pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) {
-                        uint4 v4;
-                        v4.x = pack_bf16x2(__uint_as_float(wv[8 * q4 + 0]) * inv, __uint_as_float(wv[8 * q4 + 1]) * inv);
-                        v4.y = pack_bf16x2(__uint_as_float(wv[8 * q4 + 2]) * inv, __uint_as_float(wv[8 * q4 + 3]) * inv);
-                        v4.z = pack_bf16x2(__uint_as_float(wv[8 * q4 + 4]) * inv, __uint_as_float(wv[8 * q4 + 5]) * inv);
-                        v4.w = pack_bf16x2(__uint_as_float(wv[8 * q4 + 6]) * inv, __uint_as_float(wv[8 * q4 + 7]) * inv);
-                        *reinterpret_cast<uint4*>(orow + 32 * cb + 8 * q4) = v4;
-                    }
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    uint4 v4;
+                    v4.x = pack_bf16x2(__uint_as_float(wv[8 * q4 + 0]) * inv, __uint_as_float(wv[8 * q4 + 1]) * inv);
+                    v4.y = pack_bf16x2(__uint_as_float(wv[8 * q4 + 2]) * inv, __uint_as_float(wv[8 * q4 + 3]) * inv);
+                    v4.z = pack_bf16x2(__uint_as_float(wv[8 * q4 + 4]) * inv, __uint_as_float(wv[8 * q4 + 5]) * inv);
+                    v4.w = pack_bf16x2(__uint_as_float(wv[8 * q4 + 6]) * inv, __uint_as_float(wv[8 * q4 + 7]) * inv);
+                    *reinterpret_cast<uint4*>(sSb + chunk_off(r, 8 * h + 4 * cb + q4)) = v4;
                 }
             }
+            fence_proxy_async_smem();
             tc_fence_before();
+            CG::sync();
+            if (ct == 0) {
+                tma_store_3d(&tm_o, sSb, 0, c0, bh);
+                tma_store_3d(&tm_o, sSb + kBlockBytes, 64, c0, bh);
+                bulk_commit();
+            }
         }
+        if (kOut && ct == 0) bulk_wait_all();
         if (!kOut && ok && nloc > 0) {
             // segment sums out: S row r (this thread's 64 columns) and z[r] from TMEM.  The MMA
             // thread's single-use drain barrier marks the last update done.
@@ -408,9 +418,10 @@ bool make_tmap_bf16_rows(CUtensorMap* map, const void* ptr, int BH, int N, int D
 cudaError_t tc_causal_fwd(const void* q, const void* k, const void* v, void* o, float* seg, const la_shape& s,
                           const Plan& p, bool out_pass, cudaStream_t st) {
     const int BH = s.B * s.H;
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, to;
+    // the sums pass has no q and no o: it is given the k map in their place and never uses them
     if (!make_tmap_bf16_rows(&tk, k, BH, s.N, kD, kC) || !make_tmap_bf16_rows(&tv, v, BH, s.N, kD, kC) ||
-        !make_tmap_bf16_rows(&tq, q ? q : k, BH, s.N, kD, kC))
+        !make_tmap_bf16_rows(&tq, q ? q : k, BH, s.N, kD, kC) || !make_tmap_bf16_rows(&to, o ? o : k, BH, s.N, kD, kC))
         return cudaErrorInvalidValue;
     int* err = device_error_word();
     dim3 grid(p.P, BH);
@@ -421,14 +432,14 @@ cudaError_t tc_causal_fwd(const void* q, const void* k, const void* v, void* o, 
             cudaSuccess)
             return e;
         launch_begin("tc_causal_fwd_out", st);
-        kern<<<grid, kThreads, kSmemBytes, st>>>(tq, tk, tv, (__nv_bfloat16*)o, seg, s.N, p.nchunks, p.cps, p.P, err);
+        kern<<<grid, kThreads, kSmemBytes, st>>>(tq, tk, tv, to, seg, s.N, p.nchunks, p.cps, p.P, err);
         return launch_end("tc_causal_fwd_out", st);
     }
     auto kern = tc_causal_fwd_kernel<false>;
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes)) != cudaSuccess)
         return e;
     launch_begin("tc_segment_sums", st);
-    kern<<<grid, kThreads, kSmemBytes, st>>>(tq, tk, tv, nullptr, seg, s.N, p.nchunks, p.cps, p.P, err);
+    kern<<<grid, kThreads, kSmemBytes, st>>>(tq, tk, tv, to, seg, s.N, p.nchunks, p.cps, p.P, err);
     return launch_end("tc_segment_sums", st);
 }
 

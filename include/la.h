@@ -125,6 +125,25 @@ la_status la_causal_bwd(const void* q, const void* k, const void* v, const void*
                         void* ws, size_t ws_bytes, la_stream_t stream);
 
 /*
+ * The same gradient as la_causal_bwd, bit for bit, for the training step in
+ * which the forward has just run: the forward state entering each segment is
+ * taken from the workspace of that la_causal_fwd call instead of being summed
+ * again from k and v.  This keeps the memory bound of the cumulative-sum
+ * gradient (velog review 3.5): what is kept from the forward is one state per
+ * segment, not one per position.
+ * fwd_ws: the workspace (at least la_workspace_bytes(LA_OP_CAUSAL_FWD, s)
+ * bytes) of an la_causal_fwd call on the same q, k, v and shape, unchanged
+ * since and complete in stream order; it is read, not written.  ws: a
+ * backward workspace as for la_causal_bwd.  A forward workspace that is too
+ * small returns LA_ERR_WORKSPACE; one from another shape or other inputs gives
+ * wrong gradients (this is not detectable).
+ */
+la_status la_causal_bwd_after_fwd(const void* q, const void* k, const void* v, const void* dout,
+                                  void* dq, void* dk, void* dv, la_shape s,
+                                  const void* fwd_ws, size_t fwd_ws_bytes,
+                                  void* ws, size_t ws_bytes, la_stream_t stream);
+
+/*
  * One recurrent (decode) step for every head, the state updated first and then
  * read:  S <- S + phi(k) v^T,  z <- z + phi(k),  out = phi(q)^T S / phi(q)^T z.
  * ("Transformers은 RNN이다" digest, 핵심 구성요소 4; velog review 3.6; itwiki

@@ -35,6 +35,16 @@ def test_workspace_too_small(la):
     assert _raw_fwd(la, q, q, q, o, ws, need) == 0
 
 
+def test_binding_passes_real_workspace_size(la):
+    q = torch.randn(1, 2, 300, 32, device=DEV)
+    need = la.workspace_bytes(la.OP_CAUSAL_FWD, 1, 2, 300, 32, 32, torch.float32)
+    short = torch.empty(need - 1, dtype=torch.uint8, device=DEV)
+    with pytest.raises(la.LaError):
+        la.causal_fwd(q, q, q, workspace=short)
+    torch.cuda.synchronize()
+    assert la.last_error() == 0
+
+
 def test_bad_pointers(la):
     q = torch.randn(1, 2, 100, 32, device=DEV)
     o = torch.empty_like(q)

@@ -195,6 +195,25 @@ def test_bf16_d128_many_chunks_and_segments(la):
     _sampled_heads(la, None, [(0, 0), (2, 7), (3, 15)], tensors=t)
 
 
+@pytest.mark.parametrize("B,H,N,Dk,Dv,dtype", [
+    (1, 4, 4096, 128, 128, torch.bfloat16),   # tensor-core path, several segments
+    (1, 2, 100, 128, 128, torch.bfloat16),    # tensor-core path, one segment
+    (2, 3, 1500, 32, 64, torch.float32),      # CUDA-core path
+])
+def test_bwd_after_fwd_is_bit_identical(la, B, H, N, Dk, Dv, dtype):
+    """The backward that reads the forward's segment states gives exactly la_causal_bwd's gradients."""
+    q, k, v, dO = dev(*W.random_case(300 + N, B, H, N, Dk, Dv, dtype=dtype, scale=Dk ** -0.5, with_grad=True))
+    ws_f = torch.empty(la.workspace_bytes(la.OP_CAUSAL_FWD, B, H, N, Dk, Dv, dtype), dtype=torch.uint8, device=DEV)
+    la.causal_fwd(q, k, v, workspace=ws_f)
+    ref = la.causal_bwd(q, k, v, dO)
+    got = la.causal_bwd(q, k, v, dO, fwd_workspace=ws_f)
+    torch.cuda.synchronize()
+    for name, a, b in zip(("dq", "dk", "dv"), got, ref):
+        assert torch.equal(a, b), name
+    with pytest.raises(la.LaError):  # a forward workspace one byte short is refused
+        la.causal_bwd(q, k, v, dO, fwd_workspace=ws_f[:-1])
+
+
 def test_bf16_d128_single_position(la):
     q, k, v, dO = W.random_case(78, 1, 2, 1, 128, 128, dtype=torch.bfloat16, with_grad=True)
     qd, kd, vd, dOd = dev(q, k, v, dO)
