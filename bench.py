@@ -14,7 +14,7 @@ Printed on rank 0 as one JSON line:
               of q, k, v, dO in and o, dq, dk, dv out inside the timed region
   roofline    the dominant kernel against the measured HBM copy bandwidth
   decode      recurrent step at B=64 H=8 D=32, 3072 and 784 steps, CUDA graph
-  noncausal   the non-causal forward at B=4 H=8 N=1024 D=64 bf16
+  noncausal   the non-causal forward and backward at B=4 H=8 N=1024 D=64 bf16
   cpu_baseline  the fp64 oracle on a bounded sample of the same workload
 
 `--impl reference` times the fp64 CPU oracle on the same workload instead
@@ -373,9 +373,16 @@ def bench_noncausal(la, dev):
     oc = torch.empty_like(v)
     wsc = torch.empty(la.workspace_bytes(la.OP_CAUSAL_FWD, w.B, w.H, w.N, w.Dk, w.Dv, w.dtype),
                       dtype=torch.uint8, device=dev)
+    g = torch.Generator(device="cpu")
+    g.manual_seed(12)
+    dO = torch.randn(v.shape, generator=g).to(w.dtype).to(dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    wsb = torch.empty(la.workspace_bytes(la.OP_NONCAUSAL_BWD, w.B, w.H, w.N, w.Dk, w.Dv, w.dtype),
+                      dtype=torch.uint8, device=dev)
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
     res = {}
     for name, fn in (("noncausal_fwd", lambda: la.noncausal_fwd(q, k, v, out=o, workspace=ws)),
+                     ("noncausal_bwd", lambda: la.noncausal_bwd(q, k, v, dO, dq=dq, dk=dk, dv=dv, workspace=wsb)),
                      ("causal_fwd", lambda: la.causal_fwd(q, k, v, out=oc, workspace=wsc))):
         for _ in range(3):
             fn()

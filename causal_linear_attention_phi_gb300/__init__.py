@@ -18,7 +18,7 @@ import torch
 from . import build as _build
 
 __all__ = [
-    "LaError", "noncausal_fwd", "causal_fwd", "causal_bwd", "recurrent_step", "workspace_bytes",
+    "LaError", "noncausal_fwd", "noncausal_bwd", "causal_fwd", "causal_bwd", "recurrent_step", "workspace_bytes",
     "last_error", "clear_error", "timing_enable", "timing_reset", "timing_read", "library", "version",
     "OP_NONCAUSAL_FWD", "OP_CAUSAL_FWD", "OP_CAUSAL_BWD", "OP_NONCAUSAL_BWD",
 ]
@@ -56,9 +56,12 @@ def _declare(lib):
     lib.la_noncausal_fwd.argtypes = [_vp, _vp, _vp, _vp, Shape, _vp, ctypes.c_size_t, _vp]
     lib.la_causal_fwd.argtypes = [_vp, _vp, _vp, _vp, Shape, _vp, ctypes.c_size_t, _vp]
     lib.la_causal_bwd.argtypes = [_vp] * 7 + [Shape, _vp, ctypes.c_size_t, _vp]
+    lib.la_noncausal_bwd.argtypes = [_vp] * 7 + [Shape, _vp, ctypes.c_size_t, _vp]
+    lib.la_causal_fwd_with_state.argtypes = [_vp] * 6 + [Shape, _vp, ctypes.c_size_t, _vp]
     lib.la_causal_bwd_after_fwd.argtypes = [_vp] * 7 + [Shape, _vp, ctypes.c_size_t, _vp, ctypes.c_size_t, _vp]
     lib.la_recurrent_step.argtypes = [_vp] * 6 + [Shape, _vp]
-    for f in ("la_noncausal_fwd", "la_causal_fwd", "la_causal_bwd", "la_causal_bwd_after_fwd", "la_recurrent_step",
+    for f in ("la_noncausal_fwd", "la_noncausal_bwd", "la_causal_fwd", "la_causal_fwd_with_state", "la_causal_bwd", "la_causal_bwd_after_fwd",
+              "la_recurrent_step",
               "la_last_error",
               "la_clear_error", "la_timing_enable", "la_timing_reset"):
         getattr(lib, f).restype = ctypes.c_int
@@ -162,16 +165,27 @@ def noncausal_fwd(q, k, v, out=None, workspace=None, stream=None):
     return out
 
 
-def causal_fwd(q, k, v, out=None, workspace=None, stream=None):
-    """Causal linear attention (j <= i) in the chunked form; returns o [B,H,N,Dv]."""
+def causal_fwd(q, k, v, out=None, workspace=None, stream=None, return_state=False):
+    """Causal linear attention (j <= i) in the chunked form; returns o [B,H,N,Dv].
+
+    With return_state, returns (o, S, z): the fp32 state after the last position
+    (S [B,H,Dk,Dv], z [B,H,Dk]), from which recurrent_step continues.
+    """
     _need_cuda(q, k, v)
     s = _shape4(q, k, v)
     if out is None:
         out = torch.empty_like(v)
     ws, nb = _workspace(OP_CAUSAL_FWD, s, q.device, workspace)
-    _check(library().la_causal_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), s, _ptr(ws), nb, _stream_ptr(stream)),
-           "la_causal_fwd")
-    return out
+    if not return_state:
+        _check(library().la_causal_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), s, _ptr(ws), nb, _stream_ptr(stream)),
+               "la_causal_fwd")
+        return out
+    B, H, _, Dk = q.shape
+    S = torch.empty(B, H, Dk, v.shape[-1], dtype=torch.float32, device=q.device)
+    z = torch.empty(B, H, Dk, dtype=torch.float32, device=q.device)
+    _check(library().la_causal_fwd_with_state(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(S), _ptr(z), s, _ptr(ws),
+                                              nb, _stream_ptr(stream)), "la_causal_fwd_with_state")
+    return out, S, z
 
 
 def causal_bwd(q, k, v, dout, dq=None, dk=None, dv=None, workspace=None, stream=None, fwd_workspace=None):
@@ -199,6 +213,21 @@ def causal_bwd(q, k, v, dout, dq=None, dk=None, dv=None, workspace=None, stream=
         _check(library().la_causal_bwd_after_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
                                                  s, _ptr(fwd_workspace), fnb, _ptr(ws), nb, _stream_ptr(stream)),
                "la_causal_bwd_after_fwd")
+    return dq, dk, dv
+
+
+def noncausal_bwd(q, k, v, dout, dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """Gradients (dq, dk, dv) of the non-causal form for upstream gradient dout."""
+    _need_cuda(q, k, v, dout)
+    s = _shape4(q, k, v)
+    if dout.shape != v.shape or dout.dtype != v.dtype:
+        raise ValueError("dout must match v in shape and dtype")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    ws, nb = _workspace(OP_NONCAUSAL_BWD, s, q.device, workspace)
+    _check(library().la_noncausal_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), s,
+                                      _ptr(ws), nb, _stream_ptr(stream)), "la_noncausal_bwd")
     return dq, dk, dv
 
 

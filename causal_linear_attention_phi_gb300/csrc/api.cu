@@ -197,6 +197,10 @@ WsLayout make_ws_layout(const la_shape& s, int op, const Plan& p) {
         w.totals = off;
         off += align256(BH * E * sizeof(float));
     }
+    if (op == LA_OP_NONCAUSAL_BWD) {
+        w.totals2 = off;
+        off += align256(BH * E * sizeof(float));
+    }
     w.bytes = off;
     return w;
 }
@@ -324,6 +328,56 @@ static la_status check_bwd_args(const void* q, const void* k, const void* v, con
     return LA_OK;
 }
 
+static la_status causal_fwd_impl(const void* q, const void* k, const void* v, void* o, float* S_out, float* z_out,
+                                 la_shape s, void* ws, size_t ws_bytes, la_stream_t stream) {
+    t_detail.clear();
+    LA_TRY(check_shape(s));
+    if (empty(s)) {
+        if (!S_out || s.B == 0 || s.H == 0) return LA_OK;
+        // no position: the state after it is zero
+        LA_TRY(check_device());
+        LA_TRY(check_ptr(S_out, "S"));
+        LA_TRY(check_ptr(z_out, "z"));
+        cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+        const size_t BH = (size_t)s.B * s.H;
+        LA_TRY(cuda_status(cudaMemsetAsync(S_out, 0, BH * s.Dk * s.Dv * sizeof(float), st), "state clear"));
+        LA_TRY(cuda_status(cudaMemsetAsync(z_out, 0, BH * s.Dk * sizeof(float), st), "state clear"));
+        return LA_OK;
+    }
+    LA_TRY(check_device());
+    LA_TRY(check_ptr(q, "q"));
+    LA_TRY(check_ptr(k, "k"));
+    LA_TRY(check_ptr(v, "v"));
+    LA_TRY(check_ptr(o, "o"));
+    if (S_out) {
+        LA_TRY(check_ptr(S_out, "S"));
+        LA_TRY(check_ptr(z_out, "z"));
+    }
+    const Plan p = make_plan(s, LA_OP_CAUSAL_FWD);
+    const WsLayout w = make_ws_layout(s, LA_OP_CAUSAL_FWD, p);
+    LA_TRY(check_ws(ws, ws_bytes, w.bytes));
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    float* seg = reinterpret_cast<float*>(static_cast<char*>(ws) + w.seg_states);
+    const size_t seg_bytes = (size_t)s.B * s.H * p.P * state_elems(s.Dk, s.Dv) * sizeof(float);
+    if (p.P > 1 || S_out) {
+        if (p.tc)
+            LA_TRY(cuda_status(tc_causal_fwd(nullptr, k, v, nullptr, seg, s, p, false, st), "segment sums"));
+        else
+            LA_TRY(cuda_status(simt_segment_sums(k, v, seg, s, p, st), "segment sums"));
+        if (S_out)
+            LA_TRY(cuda_status(scan_segments_final_state(seg, S_out, z_out, s, p, st), "segment scan"));
+        else
+            LA_TRY(cuda_status(scan_segments(seg, nullptr, s, p, SCAN_EXCLUSIVE_PREFIX, st), "segment scan"));
+    } else {
+        LA_TRY(cuda_status(cudaMemsetAsync(seg, 0, seg_bytes, st), "state clear"));
+    }
+    if (p.tc)
+        LA_TRY(cuda_status(tc_causal_fwd(q, k, v, o, seg, s, p, true, st), "causal forward"));
+    else
+        LA_TRY(cuda_status(simt_causal_fwd_out(q, k, v, o, seg, s, p, st), "causal forward"));
+    return LA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -357,36 +411,20 @@ la_status la_noncausal_fwd(const void* q, const void* k, const void* v, void* o,
     return LA_OK;
 }
 
+// The causal forward; with S_out / z_out also the state after position N.
+
 la_status la_causal_fwd(const void* q, const void* k, const void* v, void* o, la_shape s, void* ws, size_t ws_bytes,
                         la_stream_t stream) {
-    t_detail.clear();
-    LA_TRY(check_shape(s));
-    if (empty(s)) return LA_OK;
-    LA_TRY(check_device());
-    LA_TRY(check_ptr(q, "q"));
-    LA_TRY(check_ptr(k, "k"));
-    LA_TRY(check_ptr(v, "v"));
-    LA_TRY(check_ptr(o, "o"));
-    const Plan p = make_plan(s, LA_OP_CAUSAL_FWD);
-    const WsLayout w = make_ws_layout(s, LA_OP_CAUSAL_FWD, p);
-    LA_TRY(check_ws(ws, ws_bytes, w.bytes));
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    float* seg = reinterpret_cast<float*>(static_cast<char*>(ws) + w.seg_states);
-    const size_t seg_bytes = (size_t)s.B * s.H * p.P * state_elems(s.Dk, s.Dv) * sizeof(float);
-    if (p.P > 1) {
-        if (p.tc)
-            LA_TRY(cuda_status(tc_causal_fwd(nullptr, k, v, nullptr, seg, s, p, false, st), "segment sums"));
-        else
-            LA_TRY(cuda_status(simt_segment_sums(k, v, seg, s, p, st), "segment sums"));
-        LA_TRY(cuda_status(scan_segments(seg, nullptr, s, p, SCAN_EXCLUSIVE_PREFIX, st), "segment scan"));
-    } else {
-        LA_TRY(cuda_status(cudaMemsetAsync(seg, 0, seg_bytes, st), "state clear"));
+    return causal_fwd_impl(q, k, v, o, nullptr, nullptr, s, ws, ws_bytes, stream);
+}
+
+la_status la_causal_fwd_with_state(const void* q, const void* k, const void* v, void* o, float* S, float* z,
+                                   la_shape s, void* ws, size_t ws_bytes, la_stream_t stream) {
+    if (!S || !z) {
+        t_detail.clear();
+        return fail(LA_ERR_INVALID_ARG, "S and z are required");
     }
-    if (p.tc)
-        LA_TRY(cuda_status(tc_causal_fwd(q, k, v, o, seg, s, p, true, st), "causal forward"));
-    else
-        LA_TRY(cuda_status(simt_causal_fwd_out(q, k, v, o, seg, s, p, st), "causal forward"));
-    return LA_OK;
+    return causal_fwd_impl(q, k, v, o, S, z, s, ws, ws_bytes, stream);
 }
 
 la_status la_causal_bwd(const void* q, const void* k, const void* v, const void* dout, void* dq, void* dk, void* dv,
@@ -434,6 +472,32 @@ la_status la_causal_bwd_after_fwd(const void* q, const void* k, const void* v, c
     const float* segS = reinterpret_cast<const float*>(static_cast<const char*>(fwd_ws) + wf.seg_states);
     return causal_bwd_sweeps(q, k, v, dout, dq, dk, dv, s, p, segS, static_cast<char*>(ws), w,
                              reinterpret_cast<cudaStream_t>(stream));
+}
+
+la_status la_noncausal_bwd(const void* q, const void* k, const void* v, const void* dout, void* dq, void* dk, void* dv,
+                           la_shape s, void* ws, size_t ws_bytes, la_stream_t stream) {
+    t_detail.clear();
+    LA_TRY(check_shape(s));
+    if (empty(s)) return LA_OK;
+    LA_TRY(check_bwd_args(q, k, v, dout, dq, dk, dv));
+    const Plan p = make_plan(s, LA_OP_NONCAUSAL_BWD);
+    const WsLayout w = make_ws_layout(s, LA_OP_NONCAUSAL_BWD, p);
+    LA_TRY(check_ws(ws, ws_bytes, w.bytes));
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    char* base = static_cast<char*>(ws);
+    float* seg = reinterpret_cast<float*>(base + w.seg_states);
+    float* segR = reinterpret_cast<float*>(base + w.seg_states2);
+    float* den_g = reinterpret_cast<float*>(base + w.den_g);
+    float* totS = reinterpret_cast<float*>(base + w.totals);
+    float* totR = reinterpret_cast<float*>(base + w.totals2);
+    LA_TRY(cuda_status(simt_segment_sums(k, v, seg, s, p, st), "noncausal segment sums"));
+    LA_TRY(cuda_status(scan_segments(seg, totS, s, p, SCAN_TOTAL, st), "noncausal totals"));
+    LA_TRY(cuda_status(simt_bwd_forward_sweep(q, k, v, dout, dq, totS, segR, den_g, s, p, st, false),
+                       "noncausal backward, query pass"));
+    LA_TRY(cuda_status(scan_segments(segR, totR, s, p, SCAN_TOTAL, st), "noncausal reverse totals"));
+    LA_TRY(cuda_status(simt_bwd_reverse_sweep(q, k, v, dout, dk, dv, totR, den_g, s, p, st, false),
+                       "noncausal backward, key pass"));
+    return LA_OK;
 }
 
 la_status la_recurrent_step(const void* q, const void* k, const void* v, float* S, float* z, void* out, la_shape s,

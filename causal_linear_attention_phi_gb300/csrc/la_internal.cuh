@@ -33,7 +33,8 @@ struct Plan {
 struct WsLayout {
     size_t seg_states;   // [BH][P][E] fp32: per-segment S/z sums, then scanned in place
     size_t seg_states2;  // [BH][P][E] fp32: backward reverse-state sums (R, r)
-    size_t totals;       // [BH][E] fp32: non-causal totals
+    size_t totals;       // [BH][E] fp32: non-causal totals (S, z)
+    size_t totals2;      // [BH][E] fp32: non-causal backward totals (R, r)
     size_t den_g;        // [BH][N][2] fp32: backward per-position den and g
     size_t bytes;        // total
 };
@@ -80,16 +81,20 @@ cudaError_t simt_segment_sums(const void* k, const void* v, float* seg, const la
                               cudaStream_t st);
 cudaError_t scan_segments(float* seg, float* totals, const la_shape& s, const Plan& p, int mode,
                           cudaStream_t st);
+// Exclusive prefix in place, and the sum over all segments (the state after
+// position N) split into S_out [BH][Dk][Dv] and z_out [BH][Dk].
+cudaError_t scan_segments_final_state(float* seg, float* S_out, float* z_out, const la_shape& s, const Plan& p,
+                                      cudaStream_t st);
 cudaError_t simt_causal_fwd_out(const void* q, const void* k, const void* v, void* o, const float* seg,
                                 const la_shape& s, const Plan& p, cudaStream_t st);
 cudaError_t simt_noncausal_apply(const void* q, void* o, const float* totals, const la_shape& s,
                                  cudaStream_t st);
 cudaError_t simt_bwd_forward_sweep(const void* q, const void* k, const void* v, const void* dout,
                                    void* dq, const float* seg_S, float* seg_R, float* den_g,
-                                   const la_shape& s, const Plan& p, cudaStream_t st);
+                                   const la_shape& s, const Plan& p, cudaStream_t st, bool causal = true);
 cudaError_t simt_bwd_reverse_sweep(const void* q, const void* k, const void* v, const void* dout,
                                    void* dk, void* dv, const float* seg_R, const float* den_g,
-                                   const la_shape& s, const Plan& p, cudaStream_t st);
+                                   const la_shape& s, const Plan& p, cudaStream_t st, bool causal = true);
 cudaError_t recurrent_step(const void* q, const void* k, const void* v, float* S, float* z, void* out,
                            const la_shape& s, cudaStream_t st);
 

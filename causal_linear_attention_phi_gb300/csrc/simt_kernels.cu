@@ -103,12 +103,15 @@ segment_sums_kernel(const T* __restrict__ k, const T* __restrict__ v, float* __r
 
 // ---------------------------------------------------------------- scan over segments
 // mode 0: exclusive prefix over p (in place); 1: exclusive suffix (in place);
-// 2: totals[bh][e] = sum over p (seg unchanged).  Each thread owns four
-// consecutive elements (one float4) of every segment record and walks the P
-// records in batches whose loads are all issued before any of them is used.
+// 2: totals only (seg unchanged).  With totS, the sum over p of each record is
+// also written: its S part (elements < DkDv) to totS + bh * sS, its z part to
+// totz + bh * sz.  Each thread owns four consecutive elements (one float4, never
+// across the S / z boundary) of every segment record and walks the P records
+// in batches whose loads are all issued before any of them is used.
 constexpr int kScanBatch = 8;
 
-__global__ void scan_kernel(float* __restrict__ seg, float* __restrict__ totals, int P, size_t E, int mode) {
+__global__ void scan_kernel(float* __restrict__ seg, float* __restrict__ totS, float* __restrict__ totz, size_t sS,
+                            size_t sz, int P, size_t E, size_t DkDv, int mode) {
     const size_t e4 = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
     if (e4 >= E) return;
     const size_t bh = blockIdx.y;
@@ -136,7 +139,10 @@ __global__ void scan_kernel(float* __restrict__ seg, float* __restrict__ totals,
             }
         }
     }
-    if (mode == SCAN_TOTAL) *reinterpret_cast<float4*>(totals + bh * E + e4) = run;
+    if (totS) {
+        float* dst = e4 < DkDv ? totS + bh * sS + e4 : totz + bh * sz + (e4 - DkDv);
+        *reinterpret_cast<float4*>(dst) = run;
+    }
 }
 
 // ---------------------------------------------------------------- causal forward
@@ -302,7 +308,7 @@ noncausal_apply_kernel(const T* __restrict__ q, T* __restrict__ o, const float* 
 // dq = (P S^T + g z^T + D K~) * phi'(q) with D = tril(P V^T + g 1^T), stores
 // (den, g) per position, and sums the segment's reverse-state contributions
 // (sum phi(q_i) P_i^T, sum g_i phi(q_i)) into seg_R.
-template <typename T>
+template <typename T, bool kCausal>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_forward_sweep_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
                          const T* __restrict__ dout, T* __restrict__ dq, const float* __restrict__ seg_S,
@@ -330,7 +336,8 @@ bwd_forward_sweep_kernel(const T* __restrict__ q, const T* __restrict__ k, const
     T* dqh = dq + bh * N * Dk;
     float* dgh = den_g + bh * N * 2;
     const size_t E = state_elems(Dk, Dv);
-    const float* init = seg_S + (bh * P + p) * E;
+    // causal: the segment's exclusive prefix state; non-causal: the total over the head (fixed)
+    const float* init = kCausal ? seg_S + (bh * P + p) * E : seg_S + bh * E;
 
     float s[kMaxT][kMaxT], r[kMaxT][kMaxT];
 #pragma unroll
@@ -360,15 +367,17 @@ bwd_forward_sweep_kernel(const T* __restrict__ q, const T* __restrict__ k, const
         load_tile(vs, ldv, vh, c0, n, Dv, false);
         load_tile(ps, ldv, doh, c0, n, Dv, false);
         __syncthreads();
+        if (kCausal) {
 #pragma unroll
-        for (int i = 0; i < kC / 16; ++i)
+            for (int i = 0; i < kC / 16; ++i)
 #pragma unroll
-            for (int j = 0; j < kC / 16; ++j) {
-                const int a = ty + 16 * i, b = tx + 16 * j;
-                float acc = 0.f;
-                for (int d = 0; d < Dk; ++d) acc = fmaf(qs[a * ldk + d], ks[b * ldk + d], acc);
-                AD[a * kC + b] = (b <= a) ? acc : 0.f;
-            }
+                for (int j = 0; j < kC / 16; ++j) {
+                    const int a = ty + 16 * i, b = tx + 16 * j;
+                    float acc = 0.f;
+                    for (int d = 0; d < Dk; ++d) acc = fmaf(qs[a * ldk + d], ks[b * ldk + d], acc);
+                    AD[a * kC + b] = (b <= a) ? acc : 0.f;
+                }
+        }
         __syncthreads();
         // den, o -> g and P (P overwrites dout in place: each thread touches only its own entries)
 #pragma unroll 1
@@ -378,7 +387,7 @@ bwd_forward_sweep_kernel(const T* __restrict__ q, const T* __restrict__ k, const
 #pragma unroll
             for (int j = 0; j < kMaxT; ++j) num[j] = 0.f;
             float den = 0.f;
-            for (int b = 0; b <= a; ++b) {
+            for (int b = 0; kCausal && b <= a; ++b) {
                 const float w = AD[a * kC + b];
                 den += w;
 #pragma unroll
@@ -417,17 +426,19 @@ bwd_forward_sweep_kernel(const T* __restrict__ q, const T* __restrict__ k, const
         }
         __syncthreads();
         // D = tril(P V^T + g 1^T), masked to valid columns
+        if (kCausal) {
 #pragma unroll
-        for (int i = 0; i < kC / 16; ++i)
+            for (int i = 0; i < kC / 16; ++i)
 #pragma unroll
-            for (int j = 0; j < kC / 16; ++j) {
-                const int a = ty + 16 * i, b = tx + 16 * j;
-                float acc = 0.f;
-                for (int m = 0; m < Dv; ++m) acc = fmaf(ps[a * ldv + m], vs[b * ldv + m], acc);
-                AD[a * kC + b] = (b <= a && b < n) ? acc + gs[a] : 0.f;
-            }
+                for (int j = 0; j < kC / 16; ++j) {
+                    const int a = ty + 16 * i, b = tx + 16 * j;
+                    float acc = 0.f;
+                    for (int m = 0; m < Dv; ++m) acc = fmaf(ps[a * ldv + m], vs[b * ldv + m], acc);
+                    AD[a * kC + b] = (b <= a && b < n) ? acc + gs[a] : 0.f;
+                }
+        }
         __syncthreads();
-        // dq = (P S^T + g z^T + D K~) * phi'(q)
+        // dq = (P S^T + g z^T + D K~) * phi'(q)  (no D K~ term without the mask: S, z are totals)
 #pragma unroll 1
         for (int i = 0; i < kC / 16; ++i) {
             const int a = ty + 16 * i;
@@ -440,7 +451,7 @@ bwd_forward_sweep_kernel(const T* __restrict__ q, const T* __restrict__ k, const
                 for (int j = 0; j < kMaxT; ++j)
                     if (j < nA) acc[j] = fmaf(pm, Ss[(tx + 16 * j) * lds + m], acc[j]);
             }
-            for (int b = 0; b <= a; ++b) {
+            for (int b = 0; kCausal && b <= a; ++b) {
                 const float w = AD[a * kC + b];
 #pragma unroll
                 for (int j = 0; j < kMaxT; ++j)
@@ -470,26 +481,28 @@ bwd_forward_sweep_kernel(const T* __restrict__ q, const T* __restrict__ k, const
         if (tid < Dk)
             for (int a = 0; a < n; ++a) rz = fmaf(gs[a], qs[a * ldk + tid], rz);
         __syncthreads();
-        // forward state update
-        for (int b = 0; b < n; ++b) {
-            float kd[kMaxT], vm[kMaxT];
+        if (kCausal) {  // without the mask the state is the total: no update
+            // forward state update
+            for (int b = 0; b < n; ++b) {
+                float kd[kMaxT], vm[kMaxT];
 #pragma unroll
-            for (int x = 0; x < kMaxT; ++x) kd[x] = (x < nA) ? ks[b * ldk + ty + 16 * x] : 0.f;
+                for (int x = 0; x < kMaxT; ++x) kd[x] = (x < nA) ? ks[b * ldk + ty + 16 * x] : 0.f;
 #pragma unroll
-            for (int j = 0; j < kMaxT; ++j) vm[j] = (j < nB) ? vs[b * ldv + tx + 16 * j] : 0.f;
+                for (int j = 0; j < kMaxT; ++j) vm[j] = (j < nB) ? vs[b * ldv + tx + 16 * j] : 0.f;
+#pragma unroll
+                for (int x = 0; x < kMaxT; ++x)
+#pragma unroll
+                    for (int j = 0; j < kMaxT; ++j) s[x][j] = fmaf(kd[x], vm[j], s[x][j]);
+            }
 #pragma unroll
             for (int x = 0; x < kMaxT; ++x)
 #pragma unroll
-                for (int j = 0; j < kMaxT; ++j) s[x][j] = fmaf(kd[x], vm[j], s[x][j]);
-        }
-#pragma unroll
-        for (int x = 0; x < kMaxT; ++x)
-#pragma unroll
-            for (int j = 0; j < kMaxT; ++j)
-                if (x < nA && j < nB) Ss[(ty + 16 * x) * lds + tx + 16 * j] = s[x][j];
-        if (tid < Dk) {
-            for (int b = 0; b < n; ++b) zreg += ks[b * ldk + tid];
-            zs[tid] = zreg;
+                for (int j = 0; j < kMaxT; ++j)
+                    if (x < nA && j < nB) Ss[(ty + 16 * x) * lds + tx + 16 * j] = s[x][j];
+            if (tid < Dk) {
+                for (int b = 0; b < n; ++b) zreg += ks[b * ldk + tid];
+                zs[tid] = zreg;
+            }
         }
     }
     float* out = seg_R + (bh * P + p) * E;
@@ -505,7 +518,7 @@ bwd_forward_sweep_kernel(const T* __restrict__ q, const T* __restrict__ k, const
 // Chunks of the segment in reverse order, R_next / r_next carried from the
 // scanned suffix:  dk = (V R_next^T + 1 r_next^T + D^T Q~) * phi'(k),
 // dv = K~ R_next + A^T P, then R_next += Q~^T P, r_next += Q~^T g.
-template <typename T>
+template <typename T, bool kCausal>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_reverse_sweep_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
                          const T* __restrict__ dout, T* __restrict__ dk, T* __restrict__ dv,
@@ -535,7 +548,8 @@ bwd_reverse_sweep_kernel(const T* __restrict__ q, const T* __restrict__ k, const
     T* dvh = dv + bh * N * Dv;
     const float* dgh = den_g + bh * N * 2;
     const size_t E = state_elems(Dk, Dv);
-    const float* init = seg_R + (bh * P + p) * E;
+    // causal: the segment's exclusive suffix; non-causal: the total over the head (fixed)
+    const float* init = kCausal ? seg_R + (bh * P + p) * E : seg_R + bh * E;
 
     float r[kMaxT][kMaxT];
 #pragma unroll
@@ -575,17 +589,19 @@ bwd_reverse_sweep_kernel(const T* __restrict__ q, const T* __restrict__ k, const
         }
         __syncthreads();
         // D = tril(P V^T + g 1^T), masked to valid columns
+        if (kCausal) {
 #pragma unroll
-        for (int i = 0; i < kC / 16; ++i)
+            for (int i = 0; i < kC / 16; ++i)
 #pragma unroll
-            for (int j = 0; j < kC / 16; ++j) {
-                const int a = ty + 16 * i, b = tx + 16 * j;
-                float acc = 0.f;
-                for (int m = 0; m < Dv; ++m) acc = fmaf(ps[a * ldv + m], vs[b * ldv + m], acc);
-                AD[a * kC + b] = (b <= a && b < n) ? acc + gs[a] : 0.f;
-            }
+                for (int j = 0; j < kC / 16; ++j) {
+                    const int a = ty + 16 * i, b = tx + 16 * j;
+                    float acc = 0.f;
+                    for (int m = 0; m < Dv; ++m) acc = fmaf(ps[a * ldv + m], vs[b * ldv + m], acc);
+                    AD[a * kC + b] = (b <= a && b < n) ? acc + gs[a] : 0.f;
+                }
+        }
         __syncthreads();
-        // dk = (V R^T + r + D^T Q~) * phi'(k)
+        // dk = (V R^T + r + D^T Q~) * phi'(k)  (no D^T Q~ term without the mask: R, r are totals)
 #pragma unroll 1
         for (int i = 0; i < kC / 16; ++i) {
             const int b = ty + 16 * i;
@@ -598,7 +614,7 @@ bwd_reverse_sweep_kernel(const T* __restrict__ q, const T* __restrict__ k, const
                 for (int j = 0; j < kMaxT; ++j)
                     if (j < nA) acc[j] = fmaf(vm, Rs[(tx + 16 * j) * lds + m], acc[j]);
             }
-            for (int a = b; a < kC; ++a) {
+            for (int a = b; kCausal && a < kC; ++a) {
                 const float w = AD[a * kC + b];
 #pragma unroll
                 for (int j = 0; j < kMaxT; ++j)
@@ -615,15 +631,17 @@ bwd_reverse_sweep_kernel(const T* __restrict__ q, const T* __restrict__ k, const
         }
         __syncthreads();
         // A = tril(Q~ K~^T)
+        if (kCausal) {
 #pragma unroll
-        for (int i = 0; i < kC / 16; ++i)
+            for (int i = 0; i < kC / 16; ++i)
 #pragma unroll
-            for (int j = 0; j < kC / 16; ++j) {
-                const int a = ty + 16 * i, b = tx + 16 * j;
-                float acc = 0.f;
-                for (int d = 0; d < Dk; ++d) acc = fmaf(qs[a * ldk + d], ks[b * ldk + d], acc);
-                AD[a * kC + b] = (b <= a) ? acc : 0.f;
-            }
+                for (int j = 0; j < kC / 16; ++j) {
+                    const int a = ty + 16 * i, b = tx + 16 * j;
+                    float acc = 0.f;
+                    for (int d = 0; d < Dk; ++d) acc = fmaf(qs[a * ldk + d], ks[b * ldk + d], acc);
+                    AD[a * kC + b] = (b <= a) ? acc : 0.f;
+                }
+        }
         __syncthreads();
         // dv = K~ R + A^T P
 #pragma unroll 1
@@ -638,7 +656,7 @@ bwd_reverse_sweep_kernel(const T* __restrict__ q, const T* __restrict__ k, const
                 for (int j = 0; j < kMaxT; ++j)
                     if (j < nB) acc[j] = fmaf(kd, Rs[d * lds + tx + 16 * j], acc[j]);
             }
-            for (int a = b; a < kC; ++a) {
+            for (int a = b; kCausal && a < kC; ++a) {
                 const float w = AD[a * kC + b];
 #pragma unroll
                 for (int j = 0; j < kMaxT; ++j)
@@ -651,26 +669,28 @@ bwd_reverse_sweep_kernel(const T* __restrict__ q, const T* __restrict__ k, const
             }
         }
         __syncthreads();
-        // R += Q~^T P, r += Q~^T g
-        for (int a = 0; a < n; ++a) {
-            float qd[kMaxT], pm[kMaxT];
+        if (kCausal) {  // without the mask R, r are the totals: no update
+            // R += Q~^T P, r += Q~^T g
+            for (int a = 0; a < n; ++a) {
+                float qd[kMaxT], pm[kMaxT];
 #pragma unroll
-            for (int x = 0; x < kMaxT; ++x) qd[x] = (x < nA) ? qs[a * ldk + ty + 16 * x] : 0.f;
+                for (int x = 0; x < kMaxT; ++x) qd[x] = (x < nA) ? qs[a * ldk + ty + 16 * x] : 0.f;
 #pragma unroll
-            for (int j = 0; j < kMaxT; ++j) pm[j] = (j < nB) ? ps[a * ldv + tx + 16 * j] : 0.f;
+                for (int j = 0; j < kMaxT; ++j) pm[j] = (j < nB) ? ps[a * ldv + tx + 16 * j] : 0.f;
+#pragma unroll
+                for (int x = 0; x < kMaxT; ++x)
+#pragma unroll
+                    for (int j = 0; j < kMaxT; ++j) r[x][j] = fmaf(qd[x], pm[j], r[x][j]);
+            }
 #pragma unroll
             for (int x = 0; x < kMaxT; ++x)
 #pragma unroll
-                for (int j = 0; j < kMaxT; ++j) r[x][j] = fmaf(qd[x], pm[j], r[x][j]);
-        }
-#pragma unroll
-        for (int x = 0; x < kMaxT; ++x)
-#pragma unroll
-            for (int j = 0; j < kMaxT; ++j)
-                if (x < nA && j < nB) Rs[(ty + 16 * x) * lds + tx + 16 * j] = r[x][j];
-        if (tid < Dk) {
-            for (int a = 0; a < n; ++a) rz = fmaf(gs[a], qs[a * ldk + tid], rz);
-            rs[tid] = rz;
+                for (int j = 0; j < kMaxT; ++j)
+                    if (x < nA && j < nB) Rs[(ty + 16 * x) * lds + tx + 16 * j] = r[x][j];
+            if (tid < Dk) {
+                for (int a = 0; a < n; ++a) rz = fmaf(gs[a], qs[a * ldk + tid], rz);
+                rs[tid] = rz;
+            }
         }
     }
 }
@@ -731,9 +751,20 @@ cudaError_t simt_segment_sums(const void* k, const void* v, float* seg, const la
 
 cudaError_t scan_segments(float* seg, float* totals, const la_shape& s, const Plan& p, int mode, cudaStream_t st) {
     const size_t E = state_elems(s.Dk, s.Dv);  // a multiple of 16 for the supported head sizes
+    const size_t DkDv = (size_t)s.Dk * s.Dv;
     dim3 grid((unsigned)((E / 4 + 127) / 128), s.B * s.H);
     launch_begin("scan_segments", st);
-    scan_kernel<<<grid, 128, 0, st>>>(seg, totals, p.P, E, mode);
+    scan_kernel<<<grid, 128, 0, st>>>(seg, totals, totals ? totals + DkDv : nullptr, E, E, p.P, E, DkDv, mode);
+    return launch_end("scan_segments", st);
+}
+
+cudaError_t scan_segments_final_state(float* seg, float* S_out, float* z_out, const la_shape& s, const Plan& p,
+                                      cudaStream_t st) {
+    const size_t E = state_elems(s.Dk, s.Dv);
+    const size_t DkDv = (size_t)s.Dk * s.Dv;
+    dim3 grid((unsigned)((E / 4 + 127) / 128), s.B * s.H);
+    launch_begin("scan_segments", st);
+    scan_kernel<<<grid, 128, 0, st>>>(seg, S_out, z_out, DkDv, (size_t)s.Dk, p.P, E, DkDv, SCAN_EXCLUSIVE_PREFIX);
     return launch_end("scan_segments", st);
 }
 
@@ -769,34 +800,34 @@ cudaError_t simt_noncausal_apply(const void* q, void* o, const float* totals, co
 
 cudaError_t simt_bwd_forward_sweep(const void* q, const void* k, const void* v, const void* dout, void* dq,
                                    const float* seg_S, float* seg_R, float* den_g, const la_shape& s, const Plan& p,
-                                   cudaStream_t st) {
+                                   cudaStream_t st, bool causal) {
     const size_t smem = smem_bytes_bwd(s.Dk, s.Dv);
     dim3 grid(p.P, s.B * s.H);
     cudaError_t err = cudaSuccess;
     LA_DISPATCH_DTYPE(s.dtype, T, {
-        auto kern = bwd_forward_sweep_kernel<T>;
+        auto kern = causal ? bwd_forward_sweep_kernel<T, true> : bwd_forward_sweep_kernel<T, false>;
         if ((err = allow_smem(kern, smem)) != cudaSuccess) return err;
-        launch_begin("simt_bwd_forward_sweep", st);
+        launch_begin(causal ? "simt_bwd_forward_sweep" : "simt_noncausal_bwd_query", st);
         kern<<<grid, kThreads, smem, st>>>((const T*)q, (const T*)k, (const T*)v, (const T*)dout, (T*)dq, seg_S,
                                            seg_R, den_g, s.N, s.Dk, s.Dv, p.nchunks, p.cps, p.P);
-        err = launch_end("simt_bwd_forward_sweep", st);
+        err = launch_end(causal ? "simt_bwd_forward_sweep" : "simt_noncausal_bwd_query", st);
     });
     return err;
 }
 
 cudaError_t simt_bwd_reverse_sweep(const void* q, const void* k, const void* v, const void* dout, void* dk, void* dv,
                                    const float* seg_R, const float* den_g, const la_shape& s, const Plan& p,
-                                   cudaStream_t st) {
+                                   cudaStream_t st, bool causal) {
     const size_t smem = smem_bytes_bwd(s.Dk, s.Dv) + 256;
     dim3 grid(p.P, s.B * s.H);
     cudaError_t err = cudaSuccess;
     LA_DISPATCH_DTYPE(s.dtype, T, {
-        auto kern = bwd_reverse_sweep_kernel<T>;
+        auto kern = causal ? bwd_reverse_sweep_kernel<T, true> : bwd_reverse_sweep_kernel<T, false>;
         if ((err = allow_smem(kern, smem)) != cudaSuccess) return err;
-        launch_begin("simt_bwd_reverse_sweep", st);
+        launch_begin(causal ? "simt_bwd_reverse_sweep" : "simt_noncausal_bwd_key", st);
         kern<<<grid, kThreads, smem, st>>>((const T*)q, (const T*)k, (const T*)v, (const T*)dout, (T*)dk, (T*)dv,
                                            seg_R, den_g, s.N, s.Dk, s.Dv, p.nchunks, p.cps, p.P);
-        err = launch_end("simt_bwd_reverse_sweep", st);
+        err = launch_end(causal ? "simt_bwd_reverse_sweep" : "simt_noncausal_bwd_key", st);
     });
     return err;
 }

@@ -109,6 +109,19 @@ la_status la_causal_fwd(const void* q, const void* k, const void* v, void* o, la
                         void* ws, size_t ws_bytes, la_stream_t stream);
 
 /*
+ * la_causal_fwd that also returns the state after the last position, the (S, z)
+ * from which la_recurrent_step continues the sequence (prefill, then one step
+ * per new token: the RNN view of the causal form, digest 핵심 구성요소 4 and
+ * velog review 3.6):  S = phi(K)^T V  [B,H,Dk,Dv] and  z = phi(K)^T 1  [B,H,Dk],
+ * summed over all N positions of each head, fp32, written (not accumulated).
+ * For N = 0 both are set to zero.  o and the workspace as for la_causal_fwd.
+ * Costs one more pass over k and v when the forward has a single segment.
+ */
+la_status la_causal_fwd_with_state(const void* q, const void* k, const void* v, void* o,
+                                   float* S, float* z, la_shape s,
+                                   void* ws, size_t ws_bytes, la_stream_t stream);
+
+/*
  * Gradient of the causal form for an upstream gradient dout = dL/do.  States
  * are recomputed from q, k, v (nothing from the forward call is needed), and
  * no per-position state is stored, so memory stays linear in N ("velog review"
@@ -142,6 +155,22 @@ la_status la_causal_bwd_after_fwd(const void* q, const void* k, const void* v, c
                                   void* dq, void* dk, void* dv, la_shape s,
                                   const void* fwd_ws, size_t fwd_ws_bytes,
                                   void* ws, size_t ws_bytes, la_stream_t stream);
+
+/*
+ * Gradient of the non-causal form (la_noncausal_fwd) for an upstream gradient
+ * dout.  With S = phi(K)^T V and z = phi(K)^T 1 over all positions,
+ * den_i = phi(q_i)^T z, P_i = dout_i / den_i, g_i = -(dout_i . o_i) / den_i,
+ * R = sum_i phi(q_i) P_i^T and r = sum_i g_i phi(q_i) (all i):
+ *   dq_i = (S P_i + g_i z) * phi'(q_i),  dk_j = (R v_j + r) * phi'(k_j),  dv_j = R^T phi(k_j).
+ * (The same state algebra as the causal gradient without the mask: velog
+ * review 3.2 and 3.5; digest 핵심 구성요소 2.)  A query pass computes dq and the
+ * sums of R and r, a key pass dk and dv; the pages print no formula for this
+ * gradient, it is derived from the definition by the chain rule.
+ * Shapes as for la_causal_bwd; workspace la_workspace_bytes(LA_OP_NONCAUSAL_BWD, s).
+ */
+la_status la_noncausal_bwd(const void* q, const void* k, const void* v, const void* dout,
+                           void* dq, void* dk, void* dv, la_shape s,
+                           void* ws, size_t ws_bytes, la_stream_t stream);
 
 /*
  * One recurrent (decode) step for every head, the state updated first and then

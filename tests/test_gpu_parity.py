@@ -134,6 +134,31 @@ def test_causal_bwd_cases(la, B, H, N, Dk, Dv, dtype):
     check_all([(n, a, b) for n, a, b in zip(("dq", "dk", "dv"), (dq, dk, dv), ref)], tol_for(dtype))
 
 
+@pytest.mark.parametrize("B,H,N,Dk,Dv,dtype", [
+    (1, 2, 64, 16, 16, torch.float32),
+    (2, 3, 1000, 32, 64, torch.float32),       # several chunks and segments, ragged tail
+    (4, 8, 1024, 64, 64, torch.bfloat16),      # the non-causal forward workload's shape
+    (1, 2, 300, 128, 128, torch.bfloat16),
+    (1, 1, 1, 32, 16, torch.float32),          # a single position
+])
+def test_noncausal_bwd_cases(la, B, H, N, Dk, Dv, dtype):
+    q, k, v, dO = W.random_case(500 + N, B, H, N, Dk, Dv, dtype=dtype, scale=Dk ** -0.5, with_grad=True)
+    dq, dk, dv = la.noncausal_bwd(*dev(q, k, v, dO))
+    ref = oracle.noncausal_bwd_direct(q, k, v, dO)
+    if N == 1:  # o = v: no dependence on q or k, dv = dO
+        assert float(dq.abs().max()) < 1e-5 and float(dk.abs().max()) < 1e-5
+        check("dv", dv, ref[2], tol_for(dtype))
+        return
+    check_all([(n, a, b) for n, a, b in zip(("dq", "dk", "dv"), (dq, dk, dv), ref)], tol_for(dtype))
+
+
+def test_noncausal_bwd_sums_match_forward_invariants(la):
+    """sum_j dv_j = sum_i dO_i per head and column (the weights of each o_i sum to one)."""
+    q, k, v, dO = W.random_case(77, 2, 2, 513, 32, 32, dtype=torch.float32, with_grad=True)
+    _, _, dv = la.noncausal_bwd(*dev(q, k, v, dO))
+    np.testing.assert_allclose(to_np(dv.sum(2).cpu()), to_np(dO.sum(2)), rtol=1e-4, atol=1e-4)
+
+
 def test_bwd_single_position(la):
     # N = 1: o_1 = v_1 whatever q and k are, so dq = dk = 0 exactly and dv = dO.
     q, k, v, dO = W.random_case(30, 2, 3, 1, 16, 32, dtype=torch.float32, with_grad=True)
@@ -260,6 +285,37 @@ def test_decode_resume_is_bit_exact(la):
         o = la.recurrent_step(qd[t], kd[t], vd[t], S3, z3)
         assert torch.equal(o, full[t])
     assert torch.equal(S3, S) and torch.equal(z3, z)
+
+
+@pytest.mark.parametrize("B,H,N,Dk,Dv,dtype", [
+    (1, 2, 4096, 128, 128, torch.bfloat16),   # tensor-core forward, several segments
+    (1, 3, 100, 128, 128, torch.bfloat16),    # tensor-core forward, one segment
+    (2, 3, 700, 32, 64, torch.float32),       # CUDA-core forward
+])
+def test_prefill_state_then_decode(la, B, H, N, Dk, Dv, dtype):
+    """The forward's final (S, z) is phi(K)^T V, phi(K)^T 1; decoding on from it continues the causal form."""
+    T = 12
+    q, k, v = W.random_case(400 + N, B, H, N + T, Dk, Dv, dtype=dtype, scale=Dk ** -0.5)
+    qd, kd, vd = dev(q, k, v)
+    pre = lambda x: x[:, :, :N].contiguous()
+    o, S, z = la.causal_fwd(pre(qd), pre(kd), pre(vd), return_state=True)
+    torch.cuda.synchronize()
+    tol = tol_for(dtype)
+    phk = oracle.phi(pre(k))
+    check("final S", S.cpu(), np.einsum("bhnd,bhnm->bhdm", phk, to_np(pre(v))), tol)
+    assert rel_per_head(z.cpu()[..., None], phk.sum(axis=2)[..., None]) < tol
+    assert torch.equal(o, la.causal_fwd(pre(qd), pre(kd), pre(vd)))  # same output as without the state
+    outs = [la.recurrent_step(qd[:, :, t].contiguous(), kd[:, :, t].contiguous(), vd[:, :, t].contiguous(), S, z)
+            for t in range(N, N + T)]
+    ref = oracle.causal_recurrent(q, k, v)[:, :, N:]
+    check("decode after prefill", torch.stack(outs, 2), ref, tol)
+
+
+def test_prefill_state_of_empty_sequence_is_zero(la):
+    q = torch.randn(2, 3, 0, 32, device=DEV)
+    o, S, z = la.causal_fwd(q, q, q, return_state=True)
+    torch.cuda.synchronize()
+    assert o.shape == (2, 3, 0, 32) and float(S.abs().max()) == 0.0 and float(z.abs().max()) == 0.0
 
 
 @pytest.mark.parametrize("Dk,Dv,dtype", [(16, 16, torch.float32), (64, 32, torch.float32), (128, 128, torch.float32),
