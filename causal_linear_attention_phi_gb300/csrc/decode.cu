@@ -111,12 +111,14 @@ recurrent_step_kernel(const T* __restrict__ q, const T* __restrict__ k, const T*
     }
 }
 
-// Fast path for heads with Dk*Dv <= 64*64: one warp per head, every global
-// load of the step issued before any arithmetic (one memory round trip), S
-// held in registers as float4s.  Lane layout: COLS = Dv/4 lanes across a row,
-// RPI = 32/COLS rows per warp instruction, ROWS = Dk/RPI rows per lane.
-// Launched with programmatic stream serialization: the grid may be scheduled
-// while the previous kernel in the stream drains, and it waits
+// Fast path for heads with Dk, Dv <= 64: one warp per head, every global load
+// of the step issued before any arithmetic (one memory round trip), S held in
+// registers as float4s.  Lane layout for S: COLS = Dv/4 lanes across a row,
+// RPI = 32/COLS rows per warp instruction, ROWS = Dk/RPI rows per lane.  q, k
+// and z are read once, element d by lane d % 32 (coalesced); phi is applied
+// there once and the value of row d reaches the lanes that update row d by a
+// shuffle.  Launched with programmatic stream serialization: the grid may be
+// scheduled while the previous kernel in the stream drains, and it waits
 // (griddepcontrol.wait) before touching any global memory, so the stream
 // order seen by memory is unchanged.
 template <typename T, int DK, int DV>
@@ -126,7 +128,7 @@ recurrent_step_small_kernel(const T* __restrict__ q, const T* __restrict__ k, co
     constexpr int COLS = DV / 4;
     constexpr int RPI = 32 / COLS;
     constexpr int ROWS = DK / RPI;
-    constexpr int ZPL = (DK + 31) / 32;  // z entries per lane
+    constexpr int ZPL = (DK + 31) / 32;  // q, k, z entries per lane
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -135,18 +137,11 @@ recurrent_step_small_kernel(const T* __restrict__ q, const T* __restrict__ k, co
     const int c4 = lane % COLS, rsub = lane / COLS;
     const int col = c4 * 4;
     float* Sh = S + (size_t)h * DK * DV;
-    const T* qh = q + (size_t)h * DK;
-    const T* kh = k + (size_t)h * DK;
     // ---- all loads first
     float4 s[ROWS];
-    float kt[ROWS], qt[ROWS];
 #pragma unroll
-    for (int x = 0; x < ROWS; ++x) {
-        const int d = rsub + RPI * x;
-        s[x] = *reinterpret_cast<const float4*>(Sh + (size_t)d * DV + col);
-        kt[x] = to_f32(kh[d]);
-        qt[x] = to_f32(qh[d]);
-    }
+    for (int x = 0; x < ROWS; ++x)
+        s[x] = *reinterpret_cast<const float4*>(Sh + (size_t)(rsub + RPI * x) * DV + col);
     const float4 vv = load4<T>(v + (size_t)h * DV + col);
     float zq[ZPL], zk[ZPL], zz[ZPL];
 #pragma unroll
@@ -154,28 +149,38 @@ recurrent_step_small_kernel(const T* __restrict__ q, const T* __restrict__ k, co
         const int d = lane + 32 * y;
         const bool in = d < DK;
         zz[y] = in ? z[(size_t)h * DK + d] : 0.f;
-        zk[y] = in ? to_f32(kh[d]) : 0.f;
-        zq[y] = in ? to_f32(qh[d]) : 0.f;
+        zk[y] = in ? to_f32(k[(size_t)h * DK + d]) : 0.f;
+        zq[y] = in ? to_f32(q[(size_t)h * DK + d]) : 0.f;
     }
-    // ---- z update and phi(q).z
+    // ---- phi once per element, z update and phi(q).z
     float den = 0.f;
 #pragma unroll
     for (int y = 0; y < ZPL; ++y) {
         const int d = lane + 32 * y;
+        zk[y] = phi_f(zk[y]);
+        zq[y] = phi_f(zq[y]);
         if (d < DK) {
-            const float zn = zz[y] + phi_f(zk[y]);
+            const float zn = zz[y] + zk[y];
             z[(size_t)h * DK + d] = zn;
-            den = fmaf(phi_f(zq[y]), zn, den);
+            den = fmaf(zq[y], zn, den);
         }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-    // ---- S update and phi(q)^T S
+    // ---- S update and phi(q)^T S; row d's phi(k), phi(q) come from lane d % 32
     float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int x = 0; x < ROWS; ++x) {
         const int d = rsub + RPI * x;
-        const float a = phi_f(kt[x]), b = phi_f(qt[x]);
+        float a = __shfl_sync(0xffffffffu, zk[0], d & 31), b = __shfl_sync(0xffffffffu, zq[0], d & 31);
+        if (ZPL > 1) {
+            const float a1 = __shfl_sync(0xffffffffu, zk[ZPL - 1], d & 31);
+            const float b1 = __shfl_sync(0xffffffffu, zq[ZPL - 1], d & 31);
+            if (d >= 32) {
+                a = a1;
+                b = b1;
+            }
+        }
         float4 t = s[x];
         t.x = fmaf(a, vv.x, t.x);
         t.y = fmaf(a, vv.y, t.y);
