@@ -44,7 +44,7 @@ import torch  # noqa: E402
 from causal_linear_attention_phi_gb300 import workloads as W  # noqa: E402
 
 PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
-TRAFFIC_PATH = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+TRAFFIC_PATH = os.path.join(ROOT, "profiles", "tc_kernels_B1_H16_N32768_D128_dram_traffic.json")
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 
@@ -426,6 +426,9 @@ def cpu_baseline(seconds_hint: float = 15.0):
     oracle.causal_bwd_recurrent(q, k, v, dO)
     dt = time.perf_counter() - t0
     n_pos = int(min(w.N, max(n_probe, n_probe * seconds_hint / max(dt, 1e-6))))
+    if n_pos == w.N:  # whole heads already: take more of them (up to all B*H) to fill the time
+        per_head = dt / n_probe * w.N
+        heads = int(min(w.B * w.H, max(heads, cores * round(seconds_hint / max(per_head, 1e-6)))))
     q, k, v, dO = W.make_inputs(w, with_grad=True, B=1, H=heads, N=n_pos)
     t0 = time.perf_counter()
     oracle.causal_recurrent(q, k, v)
@@ -512,7 +515,7 @@ def run_sweep(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
