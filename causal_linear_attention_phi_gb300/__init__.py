@@ -18,7 +18,8 @@ import torch
 from . import build as _build
 
 __all__ = [
-    "LaError", "noncausal_fwd", "noncausal_bwd", "causal_fwd", "causal_bwd", "recurrent_step", "workspace_bytes",
+    "LaError", "noncausal_fwd", "noncausal_bwd", "causal_fwd", "causal_bwd", "causal_step_host", "host_step_bytes",
+    "recurrent_step", "workspace_bytes",
     "last_error", "clear_error", "timing_enable", "timing_reset", "timing_read", "library", "version",
     "OP_NONCAUSAL_FWD", "OP_CAUSAL_FWD", "OP_CAUSAL_BWD", "OP_NONCAUSAL_BWD",
 ]
@@ -56,11 +57,14 @@ def _declare(lib):
     lib.la_noncausal_fwd.argtypes = [_vp, _vp, _vp, _vp, Shape, _vp, ctypes.c_size_t, _vp]
     lib.la_causal_fwd.argtypes = [_vp, _vp, _vp, _vp, Shape, _vp, ctypes.c_size_t, _vp]
     lib.la_causal_bwd.argtypes = [_vp] * 7 + [Shape, _vp, ctypes.c_size_t, _vp]
+    lib.la_host_step_bytes.argtypes = [Shape, ctypes.c_int]
+    lib.la_host_step_bytes.restype = ctypes.c_size_t
+    lib.la_causal_step_host.argtypes = [_vp] * 8 + [Shape, ctypes.c_int, _vp, ctypes.c_size_t, _vp]
     lib.la_noncausal_bwd.argtypes = [_vp] * 7 + [Shape, _vp, ctypes.c_size_t, _vp]
     lib.la_causal_fwd_with_state.argtypes = [_vp] * 6 + [Shape, _vp, ctypes.c_size_t, _vp]
     lib.la_causal_bwd_after_fwd.argtypes = [_vp] * 7 + [Shape, _vp, ctypes.c_size_t, _vp, ctypes.c_size_t, _vp]
     lib.la_recurrent_step.argtypes = [_vp] * 6 + [Shape, _vp]
-    for f in ("la_noncausal_fwd", "la_noncausal_bwd", "la_causal_fwd", "la_causal_fwd_with_state", "la_causal_bwd", "la_causal_bwd_after_fwd",
+    for f in ("la_causal_step_host", "la_noncausal_fwd", "la_noncausal_bwd", "la_causal_fwd", "la_causal_fwd_with_state", "la_causal_bwd", "la_causal_bwd_after_fwd",
               "la_recurrent_step",
               "la_last_error",
               "la_clear_error", "la_timing_enable", "la_timing_reset"):
@@ -229,6 +233,36 @@ def noncausal_bwd(q, k, v, dout, dq=None, dk=None, dv=None, workspace=None, stre
     _check(library().la_noncausal_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), s,
                                       _ptr(ws), nb, _stream_ptr(stream)), "la_noncausal_bwd")
     return dq, dk, dv
+
+
+def host_step_bytes(B: int, H: int, N: int, Dk: int, Dv: int, dtype: torch.dtype, group_heads: int) -> int:
+    code = LA_BF16 if dtype == torch.bfloat16 else LA_F32
+    return int(library().la_host_step_bytes(Shape(B, H, N, Dk, Dv, code), group_heads))
+
+
+def causal_step_host(q, k, v, dout, o, dq, dk, dv, group_heads=4, dev_buf=None, stream=None):
+    """One causal forward + backward on pinned host tensors (la_causal_step_host).
+
+    q, k, v, dout are read and o, dq, dk, dv written, all pinned CPU tensors of
+    the [B,H,N,D] shapes; transfers and kernels are pipelined over groups of
+    `group_heads` heads.  Returns after queueing: synchronise the stream before
+    reading the outputs.
+    """
+    for t in (q, k, v, dout, o, dq, dk, dv):
+        if t.is_cuda or not t.is_pinned():
+            raise ValueError("causal_step_host takes pinned host tensors")
+    s = _shape4(q, k, v)
+    if dout.shape != v.shape or o.shape != v.shape or dv.shape != v.shape or dq.shape != q.shape or \
+            dk.shape != k.shape:
+        raise ValueError("output and gradient shapes must match the inputs")
+    need = int(library().la_host_step_bytes(s, group_heads))
+    if dev_buf is None:
+        dev_buf = torch.empty(need, dtype=torch.uint8, device=torch.device("cuda", torch.cuda.current_device()))
+    nb = dev_buf.numel() * dev_buf.element_size()
+    _check(library().la_causal_step_host(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(o), _ptr(dq), _ptr(dk), _ptr(dv),
+                                         s, group_heads, _ptr(dev_buf), nb, _stream_ptr(stream)),
+           "la_causal_step_host")
+    return o, dq, dk, dv
 
 
 def recurrent_step(q, k, v, S, z, out=None, stream=None):

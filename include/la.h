@@ -173,6 +173,29 @@ la_status la_noncausal_bwd(const void* q, const void* k, const void* v, const vo
                            void* ws, size_t ws_bytes, la_stream_t stream);
 
 /*
+ * One training step of the causal form on host-resident data: o = the causal
+ * forward of (q, k, v), then (dq, dk, dv) = its gradient for dout, exactly as
+ * la_causal_fwd followed by la_causal_bwd_after_fwd on each group of heads.
+ * All eight tensors are pinned (page-locked) host buffers in the [B,H,N,D]
+ * layout of the device calls.  Heads are independent, so the call cuts the B*H
+ * heads into groups of `group_heads` consecutive heads and overlaps, on three
+ * internal streams, the host->device copies of one group, the kernels of the
+ * previous one and the device->host copies of the one before; the transfers,
+ * not the kernels, then bound the step.  dev_buf: device scratch of at least
+ * la_host_step_bytes(s, group_heads) bytes, owned by the caller (two slots of
+ * group buffers and the two workspaces).  The work starts after what is
+ * already queued on `stream`, and `stream` waits for all of it: read the
+ * outputs after synchronising it.  Concurrent calls on one device share the
+ * internal streams and must not overlap.  Pageable host memory is refused
+ * (LA_ERR_INVALID_ARG).  The internal streams and events are created on the
+ * first call on a device and kept.
+ */
+size_t la_host_step_bytes(la_shape s, int group_heads);
+la_status la_causal_step_host(const void* q, const void* k, const void* v, const void* dout,
+                              void* o, void* dq, void* dk, void* dv, la_shape s,
+                              int group_heads, void* dev_buf, size_t dev_bytes, la_stream_t stream);
+
+/*
  * One recurrent (decode) step for every head, the state updated first and then
  * read:  S <- S + phi(k) v^T,  z <- z + phi(k),  out = phi(q)^T S / phi(q)^T z.
  * ("Transformers은 RNN이다" digest, 핵심 구성요소 4; velog review 3.6; itwiki

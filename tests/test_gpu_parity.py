@@ -4,6 +4,8 @@ Every comparison is per (b, h) head slice, max|gpu - oracle| / max|oracle|,
 bounded by 1e-4 for fp32 inputs and 2e-2 for bf16 inputs (fp32 accumulation).
 The oracle consumes the same seeded inputs after the cast to the input dtype.
 """
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -157,6 +159,37 @@ def test_noncausal_bwd_sums_match_forward_invariants(la):
     q, k, v, dO = W.random_case(77, 2, 2, 513, 32, 32, dtype=torch.float32, with_grad=True)
     _, _, dv = la.noncausal_bwd(*dev(q, k, v, dO))
     np.testing.assert_allclose(to_np(dv.sum(2).cpu()), to_np(dO.sum(2)), rtol=1e-4, atol=1e-4)
+
+
+@pytest.mark.parametrize("B,H,N,Dk,Dv,dtype,G", [
+    (2, 3, 1000, 128, 128, torch.bfloat16, 4),   # tensor-core kernels; 6 heads in groups of 4 and 2
+    (1, 5, 700, 32, 64, torch.float32, 2),       # CUDA-core kernels; groups of 2, 2, 1
+    (1, 2, 300, 64, 64, torch.bfloat16, 8),      # one group
+])
+def test_step_host_matches_oracle(la, B, H, N, Dk, Dv, dtype, G):
+    q, k, v, dO = W.random_case(600 + N, B, H, N, Dk, Dv, dtype=dtype, scale=Dk ** -0.5, with_grad=True)
+    hin = [t.contiguous().pin_memory() for t in (q, k, v, dO)]
+    hout = [torch.empty(t.shape, dtype=dtype).pin_memory() for t in (v, q, k, v)]
+    la.causal_step_host(*hin, *hout, group_heads=G)
+    torch.cuda.synchronize()
+    o, dq, dk, dv = hout
+    tol = tol_for(dtype)
+    check("o", o, oracle.causal_recurrent(q, k, v), tol)
+    ref = oracle.causal_bwd_recurrent(q, k, v, dO)
+    check_all([(n, a, b) for n, a, b in zip(("dq", "dk", "dv"), (dq, dk, dv), ref)], tol)
+
+
+def test_step_host_refuses_pageable_memory(la):
+    q = torch.randn(1, 2, 64, 32)
+    with pytest.raises(ValueError):
+        la.causal_step_host(q, q, q, q, q.clone(), q.clone(), q.clone(), q.clone())
+    # through the C ABI directly: pageable buffers are refused before anything is queued
+    s = la.Shape(1, 2, 64, 32, 32, la.LA_F32)
+    dev_buf = torch.empty(la.host_step_bytes(1, 2, 64, 32, 32, torch.float32, 2), dtype=torch.uint8, device=DEV)
+    p = ctypes.c_void_p(q.data_ptr())
+    st = la.library().la_causal_step_host(p, p, p, p, p, p, p, p, s, 2, ctypes.c_void_p(dev_buf.data_ptr()),
+                                          dev_buf.numel(), None)
+    assert st == 1
 
 
 def test_bwd_single_position(la):
