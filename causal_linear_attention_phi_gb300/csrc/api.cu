@@ -135,8 +135,11 @@ static constexpr int kTcChunk = 128;
 static constexpr int kSms = 152;
 static constexpr int kMaxWaves = 8;
 
+// bf16 heads with Dk = Dv = 128, or 64 (padded to 128 on chip: the tile loads
+// zero-fill the upper columns, phi keeps them zero and their stores are skipped).
 bool tc_supported(const la_shape& s, int op) {
-    return s.dtype == LA_BF16 && s.Dk == 128 && s.Dv == 128 && (op == LA_OP_CAUSAL_FWD || op == LA_OP_CAUSAL_BWD);
+    return s.dtype == LA_BF16 && s.Dk == s.Dv && (s.Dk == 128 || s.Dk == 64) &&
+           (op == LA_OP_CAUSAL_FWD || op == LA_OP_CAUSAL_BWD);
 }
 
 static void finish_plan(Plan& p, int P) {
@@ -153,6 +156,8 @@ Plan make_plan(const la_shape& s, int op) {
     const int BH = s.B * s.H;
     p.tc = tc_supported(s, op);
     p.C = p.tc ? kTcChunk : kSimtChunk;
+    p.sk = p.tc ? 128 : s.Dk;
+    p.sv = p.tc ? 128 : s.Dv;
     p.nchunks = (s.N + p.C - 1) / p.C;
     if (!p.tc) {
         finish_plan(p, (kTargetCtas + BH - 1) / BH);
@@ -182,7 +187,7 @@ static size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 WsLayout make_ws_layout(const la_shape& s, int op, const Plan& p) {
     WsLayout w{};
     const size_t BH = (size_t)s.B * s.H;
-    const size_t E = state_elems(s.Dk, s.Dv);
+    const size_t E = plan_state_elems(p);
     const size_t seg = align256(BH * p.P * E * sizeof(float));
     size_t off = 0;
     w.seg_states = off;
@@ -358,7 +363,7 @@ static la_status causal_fwd_impl(const void* q, const void* k, const void* v, vo
     LA_TRY(check_ws(ws, ws_bytes, w.bytes));
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     float* seg = reinterpret_cast<float*>(static_cast<char*>(ws) + w.seg_states);
-    const size_t seg_bytes = (size_t)s.B * s.H * p.P * state_elems(s.Dk, s.Dv) * sizeof(float);
+    const size_t seg_bytes = (size_t)s.B * s.H * p.P * plan_state_elems(p) * sizeof(float);
     if (p.P > 1 || S_out) {
         if (p.tc)
             LA_TRY(cuda_status(tc_causal_fwd(nullptr, k, v, nullptr, seg, s, p, false, st), "segment sums"));
@@ -439,7 +444,7 @@ la_status la_causal_bwd(const void* q, const void* k, const void* v, const void*
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     char* base = static_cast<char*>(ws);
     float* segS = reinterpret_cast<float*>(base + w.seg_states);
-    const size_t seg_bytes = (size_t)s.B * s.H * p.P * state_elems(s.Dk, s.Dv) * sizeof(float);
+    const size_t seg_bytes = (size_t)s.B * s.H * p.P * plan_state_elems(p) * sizeof(float);
     if (p.P > 1) {
         if (p.tc)
             LA_TRY(cuda_status(tc_causal_fwd(nullptr, k, v, nullptr, segS, s, p, false, st), "segment sums"));

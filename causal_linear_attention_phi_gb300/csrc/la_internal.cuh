@@ -27,7 +27,10 @@ struct Plan {
     int P;        // segments per head
     int cps;      // chunks per segment
     bool tc;      // tensor-core (tcgen05) kernels, else CUDA-core kernels
+    int sk, sv;   // dimensions of the state records (Dk, Dv; 128 on the tensor-core path, which
+                  // pads a 64-wide head to 128 on chip)
 };
+inline size_t plan_state_elems(const Plan& p) { return state_elems(p.sk, p.sv); }
 
 // Byte offsets of the workspace regions of one call (all 256-byte aligned).
 struct WsLayout {
@@ -98,7 +101,7 @@ cudaError_t simt_bwd_reverse_sweep(const void* q, const void* k, const void* v, 
 cudaError_t recurrent_step(const void* q, const void* k, const void* v, float* S, float* z, void* out,
                            const la_shape& s, cudaStream_t st);
 
-// Tensor-core (tcgen05) kernels: bf16, Dk = Dv = 128, C = 128.
+// Tensor-core (tcgen05) kernels: bf16, Dk = Dv = 128 (or 64, zero-padded to 128 on chip), C = 128.
 // out_pass = false: per-segment sums (S, z) into seg; true: outputs from the scanned prefixes.
 cudaError_t tc_causal_fwd(const void* q, const void* k, const void* v, void* o, float* seg, const la_shape& s,
                           const Plan& p, bool out_pass, cudaStream_t st);

@@ -58,7 +58,7 @@ cudaError_t scratch_address(void** out) {
 // The regular plan, with fewer segments if its segment states would not fit.
 bool fit_plan(const la_shape& s, Plan* p) {
     *p = make_plan(s, LA_OP_CAUSAL_FWD);
-    const size_t per_seg = (size_t)s.B * s.H * state_elems(s.Dk, s.Dv) * sizeof(float);
+    const size_t per_seg = (size_t)s.B * s.H * plan_state_elems(*p) * sizeof(float);
     const size_t max_P = kNoallocScratchBytes / per_seg;
     if (max_P < 1) return false;
     if ((size_t)p->P > max_P) {
@@ -95,7 +95,7 @@ extern "C" la_status la_causal_fwd_noalloc(const void* q, const void* k, const v
         return failed(LA_ERR_CUDA, "la_causal_fwd_noalloc: cudaGetSymbolAddress of the static scratch failed");
     float* seg = static_cast<float*>(scratch);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    const size_t seg_bytes = (size_t)s.B * s.H * p.P * state_elems(s.Dk, s.Dv) * sizeof(float);
+    const size_t seg_bytes = (size_t)s.B * s.H * p.P * plan_state_elems(p) * sizeof(float);
     cudaError_t e;
     if (p.P > 1) {
         e = p.tc ? tc_causal_fwd(nullptr, k, v, nullptr, seg, s, p, false, st) : simt_segment_sums(k, v, seg, s, p, st);

@@ -104,14 +104,17 @@ segment_sums_kernel(const T* __restrict__ k, const T* __restrict__ v, float* __r
 // ---------------------------------------------------------------- scan over segments
 // mode 0: exclusive prefix over p (in place); 1: exclusive suffix (in place);
 // 2: totals only (seg unchanged).  With totS, the sum over p of each record is
-// also written: its S part (elements < DkDv) to totS + bh * sS, its z part to
-// totz + bh * sz.  Each thread owns four consecutive elements (one float4, never
-// across the S / z boundary) of every segment record and walks the P records
-// in batches whose loads are all issued before any of them is used.
+// also written.  A record is an sk x sv state (row length sv) followed by sk z
+// entries; of these, rows < Dk and columns < Dv of the state go to
+// totS + bh * sS (row length Dv) and z entries < Dk to totz + bh * sz (sk = Dk,
+// sv = Dv except on the padded tensor-core path).  Each thread owns four
+// consecutive elements (one float4, inside one row) of every segment record and
+// walks the P records in batches whose loads are all issued before any of them
+// is used.
 constexpr int kScanBatch = 8;
 
 __global__ void scan_kernel(float* __restrict__ seg, float* __restrict__ totS, float* __restrict__ totz, size_t sS,
-                            size_t sz, int P, size_t E, size_t DkDv, int mode) {
+                            size_t sz, int P, size_t E, int sk, int sv, int Dk, int Dv, int mode) {
     const size_t e4 = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
     if (e4 >= E) return;
     const size_t bh = blockIdx.y;
@@ -140,8 +143,13 @@ __global__ void scan_kernel(float* __restrict__ seg, float* __restrict__ totS, f
         }
     }
     if (totS) {
-        float* dst = e4 < DkDv ? totS + bh * sS + e4 : totz + bh * sz + (e4 - DkDv);
-        *reinterpret_cast<float4*>(dst) = run;
+        const size_t SkSv = (size_t)sk * sv;
+        if (e4 < SkSv) {
+            const int d = (int)(e4 / sv), m = (int)(e4 % sv);
+            if (d < Dk && m < Dv) *reinterpret_cast<float4*>(totS + bh * sS + (size_t)d * Dv + m) = run;
+        } else if (e4 - SkSv < (size_t)Dk) {
+            *reinterpret_cast<float4*>(totz + bh * sz + (e4 - SkSv)) = run;
+        }
     }
 }
 
@@ -749,22 +757,24 @@ cudaError_t simt_segment_sums(const void* k, const void* v, float* seg, const la
     return err;
 }
 
+// totals: [BH][E] records (the non-causal path, whose records are unpadded).
 cudaError_t scan_segments(float* seg, float* totals, const la_shape& s, const Plan& p, int mode, cudaStream_t st) {
-    const size_t E = state_elems(s.Dk, s.Dv);  // a multiple of 16 for the supported head sizes
-    const size_t DkDv = (size_t)s.Dk * s.Dv;
+    const size_t E = plan_state_elems(p);  // a multiple of 16 for the supported head sizes
+    const size_t SkSv = (size_t)p.sk * p.sv;
     dim3 grid((unsigned)((E / 4 + 127) / 128), s.B * s.H);
     launch_begin("scan_segments", st);
-    scan_kernel<<<grid, 128, 0, st>>>(seg, totals, totals ? totals + DkDv : nullptr, E, E, p.P, E, DkDv, mode);
+    scan_kernel<<<grid, 128, 0, st>>>(seg, totals, totals ? totals + SkSv : nullptr, E, E, p.P, E, p.sk, p.sv, p.sk,
+                                      p.sv, mode);
     return launch_end("scan_segments", st);
 }
 
 cudaError_t scan_segments_final_state(float* seg, float* S_out, float* z_out, const la_shape& s, const Plan& p,
                                       cudaStream_t st) {
-    const size_t E = state_elems(s.Dk, s.Dv);
-    const size_t DkDv = (size_t)s.Dk * s.Dv;
+    const size_t E = plan_state_elems(p);
     dim3 grid((unsigned)((E / 4 + 127) / 128), s.B * s.H);
     launch_begin("scan_segments", st);
-    scan_kernel<<<grid, 128, 0, st>>>(seg, S_out, z_out, DkDv, (size_t)s.Dk, p.P, E, DkDv, SCAN_EXCLUSIVE_PREFIX);
+    scan_kernel<<<grid, 128, 0, st>>>(seg, S_out, z_out, (size_t)s.Dk * s.Dv, (size_t)s.Dk, p.P, E, p.sk, p.sv, s.Dk,
+                                      s.Dv, SCAN_EXCLUSIVE_PREFIX);
     return launch_end("scan_segments", st);
 }
 

@@ -75,6 +75,9 @@ struct FwdSweepSmem {
     static constexpr int total = tmem_slot + 16;
 };
 
+// D: the head size, 128 or 64 (padded to the 128-wide tiles); a template
+// parameter so that the full-width kernels carry no column test.
+template <int D>
 __global__ void __launch_bounds__(kThreadsFS, 1)
 tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                             const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -229,7 +232,7 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
             if (ct == 0) bulk_wait_read_all();  // the previous dq store has left the Sb tile
             if (!FG::all(mbar_wait(&bar->full_qv, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
             tc_fence_after();
-            FG::phi_tile(sQ, nullptr, ct, n, nullptr, nullptr);
+            FG::phi_tile(sQ, nullptr, ct, n, D, nullptr, nullptr);
             tmem_half_row_to_tile(tmem + lb + kFS, sSb, r, h);
             tc_fence_before();
             fence_proxy_async_smem();
@@ -256,7 +259,7 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
             }
             // (b) phi on K: hi in place, lo beside it, per-warp column sums of hi into zpart
             if (!FG::all(mbar_wait(&bar->full_kp, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
-            FG::phi_tile(sK, sKLo, ct, n, nullptr, zpart);
+            FG::phi_tile(sK, sKLo, ct, n, D, nullptr, zpart);
             fence_proxy_async_smem();
             FG::sync();
             if (ct == 0) mbar_arrive(&bar->qk_ready);
@@ -413,7 +416,7 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
             FG::sync();  // the dq tile is complete and z_prev has been used by every thread
             if (ct == 0) {
                 tma_store_3d(&tm_dq, sSb, 0, c0, bh);
-                tma_store_3d(&tm_dq, sSb + kBlockBytes, 64, c0, bh);
+                if (D > 64) tma_store_3d(&tm_dq, sSb + kBlockBytes, 64, c0, bh);
                 bulk_commit();
             }
             if (ct < 128) {
@@ -467,6 +470,7 @@ struct RevSweepSmem {
     static constexpr int total = tmem_slot + 16;
 };
 
+template <int D>
 __global__ void __launch_bounds__(kThreadsRS, 1)
 tc_bwd_reverse_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                             const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -610,8 +614,8 @@ tc_bwd_reverse_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
                 gsh[ct] = v ? dg.y * dg.x : 0.f;
             }
             RG::sync();
-            RG::phi_tile(sQ, nullptr, ct, n, gsh, rpart, nullptr, ish);
-            RG::phi_tile(sK, nullptr, ct, n, nullptr, nullptr, sKc);
+            RG::phi_tile(sQ, nullptr, ct, n, D, gsh, rpart, nullptr, ish);
+            RG::phi_tile(sK, nullptr, ct, n, D, nullptr, nullptr, sKc);
             fence_proxy_async_smem();
             RG::sync();
             if (ct == 0) mbar_arrive(&bar->ready);
@@ -695,9 +699,11 @@ tc_bwd_reverse_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
             RG::sync();
             if (ct == 0) {
                 tma_store_3d(&tm_dk, sKc, 0, c0, bh);
-                tma_store_3d(&tm_dk, sKc + kBlockBytes, 64, c0, bh);
                 tma_store_3d(&tm_dv, sRb, 0, c0, bh);
-                tma_store_3d(&tm_dv, sRb + kBlockBytes, 64, c0, bh);
+                if (D > 64) {
+                    tma_store_3d(&tm_dk, sKc + kBlockBytes, 64, c0, bh);
+                    tma_store_3d(&tm_dv, sRb + kBlockBytes, 64, c0, bh);
+                }
                 bulk_commit();
             }
             if (ct < 128) rsh[ct] += RG::column_sum(rpart, ct);
@@ -723,16 +729,18 @@ cudaError_t tc_bwd_forward_sweep(const void* q, const void* k, const void* v, co
     const int BH = s.B * s.H;
     CUtensorMap tq, tk, tv, td;
     CUtensorMap tdq;
-    if (!make_tmap_bf16_rows(&tq, q, BH, s.N, kD, kC) || !make_tmap_bf16_rows(&tk, k, BH, s.N, kD, kC) ||
-        !make_tmap_bf16_rows(&tv, v, BH, s.N, kD, kC) || !make_tmap_bf16_rows(&td, dout, BH, s.N, kD, kC) ||
-        !make_tmap_bf16_rows(&tdq, dq, BH, s.N, kD, kC))
+    const int D = s.Dk;  // = s.Dv: 128, or 64 padded to the 128-wide tiles
+    if (!make_tmap_bf16_rows(&tq, q, BH, s.N, D, kC) || !make_tmap_bf16_rows(&tk, k, BH, s.N, D, kC) ||
+        !make_tmap_bf16_rows(&tv, v, BH, s.N, D, kC) || !make_tmap_bf16_rows(&td, dout, BH, s.N, D, kC) ||
+        !make_tmap_bf16_rows(&tdq, dq, BH, s.N, D, kC))
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(tc_bwd_forward_sweep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    auto kern = D == 128 ? tc_bwd_forward_sweep_kernel<128> : tc_bwd_forward_sweep_kernel<64>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kFwdSweepSmem);
     if (e != cudaSuccess) return e;
     launch_begin("tc_bwd_forward_sweep", st);
-    tc_bwd_forward_sweep_kernel<<<dim3(p.P, BH), kThreadsFS, kFwdSweepSmem, st>>>(
-        tq, tk, tv, td, tdq, seg_S, seg_R, den_g, s.N, p.nchunks, p.cps, p.P, device_error_word());
+    kern<<<dim3(p.P, BH), kThreadsFS, kFwdSweepSmem, st>>>(tq, tk, tv, td, tdq, seg_S, seg_R, den_g, s.N, p.nchunks,
+                                                           p.cps, p.P, device_error_word());
     return launch_end("tc_bwd_forward_sweep", st);
 }
 
@@ -742,16 +750,18 @@ cudaError_t tc_bwd_reverse_sweep(const void* q, const void* k, const void* v, co
     const int BH = s.B * s.H;
     CUtensorMap tq, tk, tv, td;
     CUtensorMap tdk, tdv;
-    if (!make_tmap_bf16_rows(&tq, q, BH, s.N, kD, kC) || !make_tmap_bf16_rows(&tk, k, BH, s.N, kD, kC) ||
-        !make_tmap_bf16_rows(&tv, v, BH, s.N, kD, kC) || !make_tmap_bf16_rows(&td, dout, BH, s.N, kD, kC) ||
-        !make_tmap_bf16_rows(&tdk, dk, BH, s.N, kD, kC) || !make_tmap_bf16_rows(&tdv, dv, BH, s.N, kD, kC))
+    const int D = s.Dk;  // = s.Dv: 128, or 64 padded to the 128-wide tiles
+    if (!make_tmap_bf16_rows(&tq, q, BH, s.N, D, kC) || !make_tmap_bf16_rows(&tk, k, BH, s.N, D, kC) ||
+        !make_tmap_bf16_rows(&tv, v, BH, s.N, D, kC) || !make_tmap_bf16_rows(&td, dout, BH, s.N, D, kC) ||
+        !make_tmap_bf16_rows(&tdk, dk, BH, s.N, D, kC) || !make_tmap_bf16_rows(&tdv, dv, BH, s.N, D, kC))
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(tc_bwd_reverse_sweep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    auto kern = D == 128 ? tc_bwd_reverse_sweep_kernel<128> : tc_bwd_reverse_sweep_kernel<64>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kRevSweepSmem);
     if (e != cudaSuccess) return e;
     launch_begin("tc_bwd_reverse_sweep", st);
-    tc_bwd_reverse_sweep_kernel<<<dim3(p.P, BH), kThreadsRS, kRevSweepSmem, st>>>(
-        tq, tk, tv, td, tdk, tdv, seg_R, den_g, s.N, p.nchunks, p.cps, p.P, device_error_word());
+    kern<<<dim3(p.P, BH), kThreadsRS, kRevSweepSmem, st>>>(tq, tk, tv, td, tdk, tdv, seg_R, den_g, s.N, p.nchunks,
+                                                           p.cps, p.P, device_error_word());
     return launch_end("tc_bwd_reverse_sweep", st);
 }
 

@@ -16,7 +16,7 @@ namespace tc {
 using namespace sm100;
 
 constexpr int kC = 128;             // chunk length
-constexpr int kD = 128;             // Dk = Dv
+constexpr int kD = 128;             // Dk = Dv of the tiles (a 64-wide head is zero-padded)
 constexpr int kTileBytes = 32768;   // one 128 x 128 bf16 tile
 constexpr int kBlockBytes = 16384;  // one 64-column block
 
@@ -159,13 +159,14 @@ struct Grp {
         return s;
     }
 
-    // phi in place on a staged tile (rows >= n exactly 0), times scale[row]
-    // when scale is given.  With colpart, the column sums of the rounded values
+    // phi in place on a staged tile (rows >= n and columns >= dcols exactly 0:
+    // a head narrower than the tile is zero-padded), times scale[row] when
+    // scale is given.  With colpart, the column sums of the rounded values
     // (weighted by w[row] when w is given) go to colpart as per-warp partials
     // (column_part).  With lo_tile, also writes lo = bf16(phi - hi) there; with
     // copy_tile, a second copy of the rounded values.
-    __device__ static __forceinline__ void phi_tile(uint8_t* tile, uint8_t* lo_tile, int ct, int n, const float* w,
-                                                    float* colpart, uint8_t* copy_tile = nullptr,
+    __device__ static __forceinline__ void phi_tile(uint8_t* tile, uint8_t* lo_tile, int ct, int n, int dcols,
+                                                    const float* w, float* colpart, uint8_t* copy_tile = nullptr,
                                                     const float* scale = nullptr) {
         float zp[2][8];
 #pragma unroll
@@ -181,7 +182,7 @@ struct Grp {
             uint32_t* u = reinterpret_cast<uint32_t*>(&v[j]);
             uint4 l;
             uint32_t* ul = reinterpret_cast<uint32_t*>(&l);
-            const bool valid = row < n;
+            const bool valid = row < n && 64 * vec_block(j) + 8 * vec_lc(ct) < dcols;
             const float wr = (w && valid) ? w[row] : 1.f;
             const float sr = scale ? scale[row] : 1.f;
 #pragma unroll

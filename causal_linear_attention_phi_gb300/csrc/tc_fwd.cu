@@ -74,7 +74,9 @@ __device__ __forceinline__ int small_row0_off(int col) {
     return (col >> 6) * 2048 + (((col & 63) >> 3) << 4) + ((col & 7) << 1);
 }
 
-template <bool kOut>
+// D: the head size, 128 or 64 (padded to the 128-wide tiles); a template
+// parameter so that the full-width kernel carries no column test.
+template <bool kOut, int D>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_causal_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -250,8 +252,8 @@ tc_causal_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             bool w = mbar_wait(&bar->kv_full[s], (i >> 1) & 1, err, LA_ERR_TIMEOUT);
             if (kOut) w = w && mbar_wait(&bar->q_full, i & 1, err, LA_ERR_TIMEOUT);
             if (!CG::all(w)) { ok = false; break; }
-            CG::phi_tile(sK(s), nullptr, ct, n, nullptr, nullptr);
-            if (kOut) CG::phi_tile(sQ, nullptr, ct, n, nullptr, nullptr);
+            CG::phi_tile(sK(s), nullptr, ct, n, D, nullptr, nullptr);
+            if (kOut) CG::phi_tile(sQ, nullptr, ct, n, D, nullptr, nullptr);
             fence_proxy_async_smem();
             CG::sync();
             if (ct == 0) mbar_arrive(&bar->qk_ready[s]);
@@ -345,7 +347,7 @@ tc_causal_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             CG::sync();
             if (ct == 0) {
                 tma_store_3d(&tm_o, sSb, 0, c0, bh);
-                tma_store_3d(&tm_o, sSb + kBlockBytes, 64, c0, bh);
+                if (D > 64) tma_store_3d(&tm_o, sSb + kBlockBytes, 64, c0, bh);
                 bulk_commit();
             }
         }
@@ -419,28 +421,21 @@ cudaError_t tc_causal_fwd(const void* q, const void* k, const void* v, void* o, 
                           const Plan& p, bool out_pass, cudaStream_t st) {
     const int BH = s.B * s.H;
     CUtensorMap tq, tk, tv, to;
+    const int D = s.Dk;  // = s.Dv: 128, or 64 padded to the 128-wide tiles
     // the sums pass has no q and no o: it is given the k map in their place and never uses them
-    if (!make_tmap_bf16_rows(&tk, k, BH, s.N, kD, kC) || !make_tmap_bf16_rows(&tv, v, BH, s.N, kD, kC) ||
-        !make_tmap_bf16_rows(&tq, q ? q : k, BH, s.N, kD, kC) || !make_tmap_bf16_rows(&to, o ? o : k, BH, s.N, kD, kC))
+    if (!make_tmap_bf16_rows(&tk, k, BH, s.N, D, kC) || !make_tmap_bf16_rows(&tv, v, BH, s.N, D, kC) ||
+        !make_tmap_bf16_rows(&tq, q ? q : k, BH, s.N, D, kC) || !make_tmap_bf16_rows(&to, o ? o : k, BH, s.N, D, kC))
         return cudaErrorInvalidValue;
     int* err = device_error_word();
     dim3 grid(p.P, BH);
-    cudaError_t e;
-    if (out_pass) {
-        auto kern = tc_causal_fwd_kernel<true>;
-        if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes)) !=
-            cudaSuccess)
-            return e;
-        launch_begin("tc_causal_fwd_out", st);
-        kern<<<grid, kThreads, kSmemBytes, st>>>(tq, tk, tv, to, seg, s.N, p.nchunks, p.cps, p.P, err);
-        return launch_end("tc_causal_fwd_out", st);
-    }
-    auto kern = tc_causal_fwd_kernel<false>;
-    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes)) != cudaSuccess)
-        return e;
-    launch_begin("tc_segment_sums", st);
+    auto kern = out_pass ? (D == 128 ? tc_causal_fwd_kernel<true, 128> : tc_causal_fwd_kernel<true, 64>)
+                         : (D == 128 ? tc_causal_fwd_kernel<false, 128> : tc_causal_fwd_kernel<false, 64>);
+    cudaError_t e = cudaFuncSetAttribute((const void*)kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const char* name = out_pass ? "tc_causal_fwd_out" : "tc_segment_sums";
+    launch_begin(name, st);
     kern<<<grid, kThreads, kSmemBytes, st>>>(tq, tk, tv, to, seg, s.N, p.nchunks, p.cps, p.P, err);
-    return launch_end("tc_segment_sums", st);
+    return launch_end(name, st);
 }
 
 }  // namespace la
