@@ -84,6 +84,9 @@ cudaError_t simt_segment_sums(const void* k, const void* v, float* seg, const la
                               cudaStream_t st);
 cudaError_t scan_segments(float* seg, float* totals, const la_shape& s, const Plan& p, int mode,
                           cudaStream_t st);
+// The sum over all segments as [BH][Dk*Dv + Dk] records without padding (seg unchanged).
+cudaError_t scan_segments_unpadded_totals(float* seg, float* totals, const la_shape& s, const Plan& p,
+                                          cudaStream_t st);
 // Exclusive prefix in place, and the sum over all segments (the state after
 // position N) split into S_out [BH][Dk][Dv] and z_out [BH][Dk].
 cudaError_t scan_segments_final_state(float* seg, float* S_out, float* z_out, const la_shape& s, const Plan& p,

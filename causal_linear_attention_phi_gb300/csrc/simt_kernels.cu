@@ -768,6 +768,16 @@ cudaError_t scan_segments(float* seg, float* totals, const la_shape& s, const Pl
     return launch_end("scan_segments", st);
 }
 
+cudaError_t scan_segments_unpadded_totals(float* seg, float* totals, const la_shape& s, const Plan& p,
+                                          cudaStream_t st) {
+    const size_t E = plan_state_elems(p), Eu = state_elems(s.Dk, s.Dv);
+    dim3 grid((unsigned)((E / 4 + 127) / 128), s.B * s.H);
+    launch_begin("scan_segments", st);
+    scan_kernel<<<grid, 128, 0, st>>>(seg, totals, totals + (size_t)s.Dk * s.Dv, Eu, Eu, p.P, E, p.sk, p.sv, s.Dk,
+                                      s.Dv, SCAN_TOTAL);
+    return launch_end("scan_segments", st);
+}
+
 cudaError_t scan_segments_final_state(float* seg, float* S_out, float* z_out, const la_shape& s, const Plan& p,
                                       cudaStream_t st) {
     const size_t E = plan_state_elems(p);

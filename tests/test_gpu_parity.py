@@ -102,6 +102,17 @@ def test_causal_fwd_cases(la, B, H, N, Dk, Dv, dtype):
         assert torch.allclose(o.cpu(), v, rtol=1e-6, atol=0)
 
 
+@pytest.mark.parametrize("B,H,N,Dk,Dv,dtype", [
+    (1, 2, 1000, 128, 128, torch.bfloat16),   # segment sums on the tensor cores
+    (2, 3, 777, 64, 64, torch.bfloat16),      # the same with a padded head
+    (1, 2, 300, 32, 16, torch.float32),       # CUDA cores throughout
+])
+def test_noncausal_fwd_cases(la, B, H, N, Dk, Dv, dtype):
+    q, k, v = W.random_case(700 + N, B, H, N, Dk, Dv, dtype=dtype, scale=Dk ** -0.5)
+    o = la.noncausal_fwd(*dev(q, k, v))
+    check("non-causal o", o, oracle.noncausal_assoc(q, k, v), tol_for(dtype))
+
+
 def test_constant_v_gives_constant_output(la):
     q, k, _ = W.random_case(5, 1, 2, 333, 64, 32, dtype=torch.float32)
     c = torch.linspace(-2, 2, 32)
@@ -256,6 +267,7 @@ def test_bf16_d128_many_chunks_and_segments(la):
 @pytest.mark.parametrize("B,H,N,Dk,Dv,dtype", [
     (1, 4, 4096, 128, 128, torch.bfloat16),   # tensor-core path, several segments
     (1, 2, 100, 128, 128, torch.bfloat16),    # tensor-core path, one segment
+    (2, 2, 3000, 64, 64, torch.bfloat16),     # tensor-core path, head of 64 padded on chip
     (2, 3, 1500, 32, 64, torch.float32),      # CUDA-core path
 ])
 def test_bwd_after_fwd_is_bit_identical(la, B, H, N, Dk, Dv, dtype):
@@ -323,6 +335,7 @@ def test_decode_resume_is_bit_exact(la):
 @pytest.mark.parametrize("B,H,N,Dk,Dv,dtype", [
     (1, 2, 4096, 128, 128, torch.bfloat16),   # tensor-core forward, several segments
     (1, 3, 100, 128, 128, torch.bfloat16),    # tensor-core forward, one segment
+    (2, 2, 1500, 64, 64, torch.bfloat16),     # tensor-core forward, padded state records
     (2, 3, 700, 32, 64, torch.float32),       # CUDA-core forward
 ])
 def test_prefill_state_then_decode(la, B, H, N, Dk, Dv, dtype):

@@ -35,6 +35,7 @@ def _noalloc(la, q, k, v, o):
 
 
 @pytest.mark.parametrize("B,H,N,D,dtype", [(2, 16, 8192, 128, torch.bfloat16),   # tensor-core path, segments capped
+                                           (2, 8, 5000, 64, torch.bfloat16),     # tensor-core path, padded head
                                            (1, 2, 1000, 64, torch.float32)])      # CUDA-core path
 def test_noalloc_matches_workspace_entry_twice(la, B, H, N, D, dtype):
     scale = 128 ** -0.5 if dtype == torch.bfloat16 else 1.0
