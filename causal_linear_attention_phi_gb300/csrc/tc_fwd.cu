@@ -244,15 +244,16 @@ tc_causal_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         }
         tc_fence_before();
         bool ok = CG::all(true);
+        bool k_applied = false;  // phi on this chunk's K was applied while the previous chunk's O was formed
         for (int i = 0; i < nloc && ok; ++i) {
             const int s = i & 1;
             const int c0 = (cbeg + i) * kC, n = min(kC, N - c0);
-            // (a) phi on the K (and Q) tiles
+            // (a) phi on the K (unless done already) and Q tiles
             if (kOut && ct == 0) bulk_wait_read_all();  // the previous o store has left the Sb tile
             bool w = mbar_wait(&bar->kv_full[s], (i >> 1) & 1, err, LA_ERR_TIMEOUT);
             if (kOut) w = w && mbar_wait(&bar->q_full, i & 1, err, LA_ERR_TIMEOUT);
             if (!CG::all(w)) { ok = false; break; }
-            CG::phi_tile(sK(s), nullptr, ct, n, D, nullptr, nullptr);
+            if (!k_applied) CG::phi_tile(sK(s), nullptr, ct, n, D, nullptr, nullptr);
             if (kOut) CG::phi_tile(sQ, nullptr, ct, n, D, nullptr, nullptr);
             fence_proxy_async_smem();
             CG::sync();
@@ -319,6 +320,14 @@ tc_causal_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             tc_fence_before();
             CG::sync();
             if (ct == 0) mbar_arrive(&bar->a_ready);
+            // (c') while O is formed: phi on the next chunk's K (the other K/V stage) if it
+            // has landed; that stage's previous chunk finished with it before it was reloaded
+            k_applied = false;
+            if (i + 1 < nloc && CG::all(mbar_try_wait(&bar->kv_full[s ^ 1], ((i + 1) >> 1) & 1))) {
+                CG::phi_tile(sK(s ^ 1), nullptr, ct, min(kC, N - (c0 + kC)), D, nullptr, nullptr);
+                fence_proxy_async_smem();
+                k_applied = true;
+            }
             // (d) o = O / den on this thread's 64 columns, staged in the Sb tile (free once
             // O is complete) and written by one TMA store (rows past N are not written)
             if (!CG::all(mbar_wait(&bar->o_done, i & 1, err, LA_ERR_TIMEOUT))) { ok = false; break; }
