@@ -229,7 +229,7 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
             // (a) phi on Q in place; S_prev -> its bf16 copy (rows = dk; this thread's 64
             // columns).  S and Y are settled: the previous chunk's dq_done, which follows
             // every earlier MMA, has been awaited.
-            if (ct == 0) bulk_wait_read_all();  // the previous dq store has left the Sb tile
+            if (ct == kStoreThread) bulk_wait_read_all();  // the previous dq store has left the Sb tile
             if (!FG::all(mbar_wait(&bar->full_qv, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
             tc_fence_after();
             FG::phi_tile(sQ, nullptr, ct, n, D, nullptr, nullptr);
@@ -414,7 +414,7 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
             fence_proxy_async_smem();
             tc_fence_before();
             FG::sync();  // the dq tile is complete and z_prev has been used by every thread
-            if (ct == 0) {
+            if (ct == kStoreThread) {
                 tma_store_3d(&tm_dq, sSb, 0, c0, bh);
                 if (D > 64) tma_store_3d(&tm_dq, sSb + kBlockBytes, 64, c0, bh);
                 bulk_commit();
@@ -424,7 +424,7 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
                 racc[ct] += FG::column_sum(drpart, ct);
             }
         }
-        if (ct == 0) bulk_wait_all();
+        if (ct == kStoreThread) bulk_wait_all();
         // segment sums of the reverse state out: R from TMEM, r from shared memory
         if (ok && nloc > 0 && FG::all(mbar_wait(&bar->final_mma, 0, err, LA_ERR_TIMEOUT))) {
             tc_fence_after();
@@ -606,7 +606,7 @@ tc_bwd_reverse_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
             if (ct < 128 && i + 1 < nloc) dg_next = load_dg(i + 1);
             // (a) per-row 1/den and g den; Q' = phi(Q) / den with the chunk's sum of (g den) Q';
             // phi on K (and its copy)
-            if (ct == 0) bulk_wait_read_all();  // the previous dk / dv stores have left Kc and Rb
+            if (ct == kStoreThread) bulk_wait_read_all();  // the previous dk / dv stores have left Kc and Rb
             if (!RG::all(mbar_wait(&bar->full, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
             if (ct < 128) {
                 const bool v = ct < n;
@@ -697,7 +697,7 @@ tc_bwd_reverse_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
             fence_proxy_async_smem();
             tc_fence_before();
             RG::sync();
-            if (ct == 0) {
+            if (ct == kStoreThread) {
                 tma_store_3d(&tm_dk, sKc, 0, c0, bh);
                 tma_store_3d(&tm_dv, sRb, 0, c0, bh);
                 if (D > 64) {
@@ -708,7 +708,7 @@ tc_bwd_reverse_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
             }
             if (ct < 128) rsh[ct] += RG::column_sum(rpart, ct);
         }
-        if (ct == 0) bulk_wait_all();
+        if (ct == kStoreThread) bulk_wait_all();
         tc_fence_before();
     }
     __syncthreads();

@@ -19,6 +19,9 @@ constexpr int kC = 128;             // chunk length
 constexpr int kD = 128;             // Dk = Dv of the tiles (a 64-wide head is zero-padded)
 constexpr int kTileBytes = 32768;   // one 128 x 128 bf16 tile
 constexpr int kBlockBytes = 16384;  // one 64-column block
+// The compute thread that issues a kernel's TMA stores and waits for them: one
+// that has no per-column work at the end of a chunk (compute threads 0-127 do).
+constexpr int kStoreThread = 128;
 
 // K-major operand, K step kk (16 elements): block kk / 4, +32 B inside the 128-B row.
 __device__ __forceinline__ uint64_t desc_kmajor(uint32_t tile, int kk) {

@@ -249,7 +249,7 @@ tc_causal_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             const int s = i & 1;
             const int c0 = (cbeg + i) * kC, n = min(kC, N - c0);
             // (a) phi on the K (unless done already) and Q tiles
-            if (kOut && ct == 0) bulk_wait_read_all();  // the previous o store has left the Sb tile
+            if (kOut && ct == kStoreThread) bulk_wait_read_all();  // the previous o store has left the Sb tile
             bool w = mbar_wait(&bar->kv_full[s], (i >> 1) & 1, err, LA_ERR_TIMEOUT);
             if (kOut) w = w && mbar_wait(&bar->q_full, i & 1, err, LA_ERR_TIMEOUT);
             if (!CG::all(w)) { ok = false; break; }
@@ -354,13 +354,13 @@ tc_causal_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             fence_proxy_async_smem();
             tc_fence_before();
             CG::sync();
-            if (ct == 0) {
+            if (ct == kStoreThread) {
                 tma_store_3d(&tm_o, sSb, 0, c0, bh);
                 if (D > 64) tma_store_3d(&tm_o, sSb + kBlockBytes, 64, c0, bh);
                 bulk_commit();
             }
         }
-        if (kOut && ct == 0) bulk_wait_all();
+        if (kOut && ct == kStoreThread) bulk_wait_all();
         if (!kOut && ok && nloc > 0) {
             // segment sums out: S row r (this thread's 64 columns) and z[r] from TMEM.  The MMA
             // thread's single-use drain barrier marks the last update done.
