@@ -191,6 +191,9 @@ def run_ours(args):
     la.build.build_library()
     la.library()
     la.clear_error()
+    # the decode step first, on a fresh device allocator (it is independent of the main
+    # workload, whose 8 GB of buffers would otherwise shape where its small buffers land)
+    decode = bench_decode(la, dev, peaks()[0]) if (rank == 0 and not args.skip_extras) else None
 
     w = W.LONG_BF16
     if args.workload == "profile":
@@ -306,7 +309,7 @@ def run_ours(args):
 
     # ---- decode and non-causal sub-measurements (rank 0 only, not part of value)
     if rank == 0 and not args.skip_extras:
-        result["decode"] = bench_decode(la, dev, hbm)
+        result["decode"] = decode
         result["noncausal"] = bench_noncausal(la, dev)
     if rank == 0 and not args.skip_cpu:
         result["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
