@@ -284,7 +284,7 @@ def run_ours(args):
         host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (v, q, k, v)]  # o, dq, dk, dv
         h2d = sum(t.numel() * t.element_size() for t in host_in)
         d2h = sum(t.numel() * t.element_size() for t in host_out)
-        group = 4
+        group = 2
         dev_buf = torch.empty(la.host_step_bytes(B, H, N, Dk, Dv, w.dtype, group), dtype=torch.uint8, device=dev)
 
         def e2e_step():
