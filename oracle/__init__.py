@@ -1,4 +1,5 @@
-"""fp64 CPU oracle for causal linear attention with phi(x) = elu(x) + 1.
+"""fp64 CPU oracle for causal linear attention with phi(x) = elu(x) + 1, and for
+its decayed variant, retention (a fixed decay per head, no feature map).
 
 TEST INFRASTRUCTURE ONLY.  The tests, the smoke check and the benchmark's
 CPU-baseline leg may import this package; the product library never does.  The
@@ -56,6 +57,13 @@ def _declare(lib):
         getattr(lib, name).restype = None
     lib.oracle_recurrent_step.argtypes = [_DP] * 6 + [i, i, i]
     lib.oracle_recurrent_step.restype = None
+    for name in ("oracle_retention_direct", "oracle_retention_recurrent"):
+        getattr(lib, name).argtypes = [_DP] * 5 + [i, i, i, i]
+        getattr(lib, name).restype = None
+    lib.oracle_retention_chunked.argtypes = [_DP] * 5 + [i, i, i, i, i]
+    lib.oracle_retention_chunked.restype = None
+    lib.oracle_retention_step.argtypes = [_DP] * 6 + [i, i, i]
+    lib.oracle_retention_step.restype = None
     for name in ("oracle_phi", "oracle_dphi"):
         getattr(lib, name).argtypes = [_DP, _DP, ctypes.c_long]
         getattr(lib, name).restype = None
@@ -156,6 +164,44 @@ class Oracle:
     def noncausal_bwd_direct(self, q, k, v, dO):
         return self._bwd("oracle_noncausal_bwd_direct", q, k, v, dO)
 
+    # ---- retention (decay gamma per head, no feature map, no normaliser)
+    @staticmethod
+    def _gamma(gamma, BH):
+        """gamma per flat head: given per head of one batch row ([H], tiled over B) or per flat head."""
+        g = np.atleast_1d(_f64(gamma)).ravel()
+        if g.size != BH and (g.size == 0 or BH % g.size != 0):
+            raise ValueError("gamma has %d entries for %d heads" % (g.size, BH))
+        return np.ascontiguousarray(np.tile(g, BH // g.size))
+
+    def _ret(self, name, q, k, v, gamma, *extra):
+        q, k, v, BH, N, Dk, Dv = _heads(q, k, v)
+        g = self._gamma(gamma, BH)
+        o = np.empty(v.shape, dtype=np.float64)
+        getattr(self.l, name)(_p(q), _p(k), _p(v), _p(g), _p(o), BH, N, Dk, Dv, *extra)
+        return o
+
+    def retention_direct(self, q, k, v, gamma):
+        return self._ret("oracle_retention_direct", q, k, v, gamma)
+
+    def retention_recurrent(self, q, k, v, gamma):
+        return self._ret("oracle_retention_recurrent", q, k, v, gamma)
+
+    def retention_chunked(self, q, k, v, gamma, C):
+        return self._ret("oracle_retention_chunked", q, k, v, gamma, int(C))
+
+    def retention_step(self, q, k, v, gamma, S):
+        """One retention decode step; returns (out, S') without touching the inputs."""
+        q, k, v = _f64(q), _f64(k), _f64(v)
+        S = _f64(S).copy()
+        Dk, Dv = q.shape[-1], v.shape[-1]
+        BH = q.size // Dk
+        if S.size != BH * Dk * Dv or v.size != BH * Dv:
+            raise ValueError("state shape mismatch")
+        g = self._gamma(gamma, BH)
+        out = np.empty(v.shape, dtype=np.float64)
+        self.l.oracle_retention_step(_p(q), _p(k), _p(v), _p(g), _p(S), _p(out), BH, Dk, Dv)
+        return out, S
+
     def recurrent_step(self, q, k, v, S, z):
         """One decode step; returns (out, S', z') without touching the inputs."""
         q, k, v = _f64(q), _f64(k), _f64(v)
@@ -181,3 +227,7 @@ causal_bwd_direct = default.causal_bwd_direct
 causal_bwd_recurrent = default.causal_bwd_recurrent
 noncausal_bwd_direct = default.noncausal_bwd_direct
 recurrent_step = default.recurrent_step
+retention_direct = default.retention_direct
+retention_recurrent = default.retention_recurrent
+retention_chunked = default.retention_chunked
+retention_step = default.retention_step

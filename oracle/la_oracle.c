@@ -456,3 +456,110 @@ void oracle_noncausal_bwd_direct(const double* q, const double* k, const double*
         free(qt); free(kt); free(den); free(oh); free(dqt); free(dkt);
     }
 }
+
+/* ------------------------------------------------------------------ retention
+ * The decayed variant in [WIKI] "발전: 감쇠, 게이트, 델타 규칙" (RetNet row):
+ * S_t = gamma S_{t-1} + v_t k_t^T with a fixed decay gamma per head, read as
+ * o_t = S_t q_t (column convention).  Here S is kept as Dk x Dv, so
+ * S_t = gamma S_{t-1} + k_t v_t^T and o_t = S_t^T q_t.  Per [WIKI] "항등 사상"
+ * the queries and keys enter as they are (no feature map) and there is no
+ * denominator (RetNet normalises the head output outside the attention).
+ * gamma[h] is the decay of flat head h (h = b*H + head), 0 <= gamma <= 1.
+ * 0^0 is taken as 1 (the j = i term always has weight 1).
+ */
+static double powi(double g, int m) {
+    double r = 1.0;
+    for (int i = 0; i < m; ++i) r *= g;
+    return r;
+}
+
+/* Direct form, O(N^2) per head: o_i = sum_{j <= i} gamma^(i-j) (q_i . k_j) v_j. */
+void oracle_retention_direct(const double* q, const double* k, const double* v, const double* gamma, double* o,
+                             int BH, int N, int Dk, int Dv) {
+#pragma omp parallel for schedule(dynamic)
+    for (int h = 0; h < BH; ++h) {
+        for (int i = 0; i < N; ++i) {
+            double* oi = o + IDX3(h, i, 0, N, Dv);
+            for (int m = 0; m < Dv; ++m) oi[m] = 0.0;
+            for (int j = 0; j <= i; ++j) {
+                const double w = powi(gamma[h], i - j) * dot(q + IDX3(h, i, 0, N, Dk), k + IDX3(h, j, 0, N, Dk), Dk);
+                const double* vj = v + IDX3(h, j, 0, N, Dv);
+                for (int m = 0; m < Dv; ++m) oi[m] += w * vj[m];
+            }
+        }
+    }
+}
+
+/* One recurrent step for every head: S <- gamma S + k v^T, then out = S^T q. */
+void oracle_retention_step(const double* q, const double* k, const double* v, const double* gamma, double* S,
+                           double* out, int BH, int Dk, int Dv) {
+    for (int h = 0; h < BH; ++h) {
+        const double* qh = q + (size_t)h * Dk;
+        const double* kh = k + (size_t)h * Dk;
+        const double* vh = v + (size_t)h * Dv;
+        double* Sh = S + (size_t)h * Dk * Dv;
+        for (int d = 0; d < Dk; ++d)
+            for (int m = 0; m < Dv; ++m) Sh[(size_t)d * Dv + m] = gamma[h] * Sh[(size_t)d * Dv + m] + kh[d] * vh[m];
+        for (int m = 0; m < Dv; ++m) {
+            double acc = 0.0;
+            for (int d = 0; d < Dk; ++d) acc += qh[d] * Sh[(size_t)d * Dv + m];
+            out[(size_t)h * Dv + m] = acc;
+        }
+    }
+}
+
+/* The recurrence from S = 0 over i = 1..N. */
+void oracle_retention_recurrent(const double* q, const double* k, const double* v, const double* gamma, double* o,
+                                int BH, int N, int Dk, int Dv) {
+#pragma omp parallel for schedule(dynamic)
+    for (int h = 0; h < BH; ++h) {
+        double* S = (double*)calloc((size_t)Dk * (size_t)Dv, sizeof(double));
+        for (int i = 0; i < N; ++i)
+            oracle_retention_step(q + IDX3(h, i, 0, N, Dk), k + IDX3(h, i, 0, N, Dk), v + IDX3(h, i, 0, N, Dv),
+                                  gamma + h, S, o + IDX3(h, i, 0, N, Dv), 1, Dk, Dv);
+        free(S);
+    }
+}
+
+/*
+ * Chunked form: inside a chunk of C positions starting at s, the product
+ * (Q_c K_c^T) weighted by gamma^(a-b) on its lower triangle, plus the carried
+ * state read as gamma^(a+1) q_a^T S; then S <- gamma^n S + sum_b gamma^(n-1-b)
+ * k_b v_b^T for a chunk of n positions (a, b counted from the chunk start).
+ */
+void oracle_retention_chunked(const double* q, const double* k, const double* v, const double* gamma, double* o,
+                              int BH, int N, int Dk, int Dv, int C) {
+#pragma omp parallel for schedule(dynamic)
+    for (int h = 0; h < BH; ++h) {
+        const double g = gamma[h];
+        double* S = (double*)calloc((size_t)Dk * (size_t)Dv, sizeof(double));
+        for (int s = 0; s < N; s += C) {
+            int n = (N - s) < C ? (N - s) : C;
+            for (int a = 0; a < n; ++a) {
+                const double* qa = q + IDX3(h, s + a, 0, N, Dk);
+                double* oa = o + IDX3(h, s + a, 0, N, Dv);
+                const double carry = powi(g, a + 1);
+                for (int m = 0; m < Dv; ++m) {
+                    double acc = 0.0;
+                    for (int d = 0; d < Dk; ++d) acc += qa[d] * S[(size_t)d * Dv + m];
+                    oa[m] = carry * acc;
+                }
+                for (int b = 0; b <= a; ++b) {
+                    const double w = powi(g, a - b) * dot(qa, k + IDX3(h, s + b, 0, N, Dk), Dk);
+                    const double* vb = v + IDX3(h, s + b, 0, N, Dv);
+                    for (int m = 0; m < Dv; ++m) oa[m] += w * vb[m];
+                }
+            }
+            const double gn = powi(g, n);
+            for (size_t e = 0; e < (size_t)Dk * Dv; ++e) S[e] *= gn;
+            for (int b = 0; b < n; ++b) {
+                const double w = powi(g, n - 1 - b);
+                const double* kb = k + IDX3(h, s + b, 0, N, Dk);
+                const double* vb = v + IDX3(h, s + b, 0, N, Dv);
+                for (int d = 0; d < Dk; ++d)
+                    for (int m = 0; m < Dv; ++m) S[(size_t)d * Dv + m] += w * kb[d] * vb[m];
+            }
+        }
+        free(S);
+    }
+}

@@ -258,4 +258,61 @@ def pin_bwd_invariants(orc):
         assert rel(dv, ref_dv) < 1e-12
 
 
+# ---------------------------------------------------------------- retention (decay per head, no phi, no normaliser)
+GAMMA = np.array([0.3, 0.9, 1.0])
+
+
+def pin_retention_forms_agree(orc):
+    q, k, v, _ = case(61, B=2, H=3, N=50)
+    ref = orc.retention_direct(q, k, v, GAMMA)
+    assert rel(orc.retention_recurrent(q, k, v, GAMMA), ref) < 1e-12
+    for C in (1, 7, 16, 64):
+        assert rel(orc.retention_chunked(q, k, v, GAMMA, C), ref) < 1e-12
+
+
+def pin_retention_gamma_one_is_masked_product(orc):
+    """gamma = 1: no decay, o = tril(Q K^T) V (the causal form without phi and without a denominator)."""
+    q, k, v, _ = case(62, B=1, H=2, N=40)
+    ref = np.tril(q @ np.swapaxes(k, -1, -2)) @ v
+    assert rel(orc.retention_direct(q, k, v, [1.0]), ref) < 1e-12
+    assert rel(orc.retention_chunked(q, k, v, [1.0], 16), ref) < 1e-12
+
+
+def pin_retention_gamma_zero_keeps_diagonal(orc):
+    """gamma = 0: everything before the current position is forgotten, o_i = (q_i . k_i) v_i."""
+    q, k, v, _ = case(63, B=1, H=2, N=30)
+    ref = np.einsum("bhnd,bhnd->bhn", q, k)[..., None] * v
+    assert rel(orc.retention_direct(q, k, v, [0.0]), ref) < 1e-12
+    assert rel(orc.retention_recurrent(q, k, v, [0.0]), ref) < 1e-12
+    assert rel(orc.retention_chunked(q, k, v, [0.0], 8), ref) < 1e-12
+
+
+def pin_retention_geometric_closed_form(orc):
+    """Constant q, k (q . k = c) and v = u: o_i = c u (1 - g^(i+1)) / (1 - g)."""
+    N, g = 37, 0.8
+    a, b, u = rnd(64, 8), rnd(65, 8), rnd(66, 5)
+    q = np.broadcast_to(a, (1, 1, N, 8)).copy()
+    k = np.broadcast_to(b, (1, 1, N, 8)).copy()
+    v = np.broadcast_to(u, (1, 1, N, 5)).copy()
+    c = float(a @ b)
+    i = np.arange(N)[:, None]
+    ref = (c * u[None, :] * (1.0 - g ** (i + 1)) / (1.0 - g))[None, None]
+    for o in (orc.retention_direct(q, k, v, [g]), orc.retention_chunked(q, k, v, [g], 10)):
+        assert rel(o, ref) < 1e-12
+
+
+def pin_retention_decode_state(orc):
+    """N decode steps from S = 0 give the recurrent outputs and S = sum_j g^(N-1-j) k_j v_j^T."""
+    q, k, v, _ = case(67, B=1, H=3, N=20, Dk=8, Dv=6)
+    S = np.zeros((1, 3, 8, 6))
+    outs = []
+    for t in range(20):
+        o, S = orc.retention_step(q[:, :, t], k[:, :, t], v[:, :, t], GAMMA, S)
+        outs.append(o)
+    assert rel(np.stack(outs, 2), orc.retention_recurrent(q, k, v, GAMMA)) < 1e-12
+    w = GAMMA[None, :, None] ** (19 - np.arange(20))[None, None, :]  # [1, H, N]
+    ref_S = np.einsum("bhn,bhnd,bhnm->bhdm", w, k, v)
+    assert rel(S, ref_S) < 1e-12
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
