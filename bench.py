@@ -311,6 +311,7 @@ def run_ours(args):
     if rank == 0 and not args.skip_extras:
         result["decode"] = decode
         result["noncausal"] = bench_noncausal(la, dev)
+        result["retention"] = bench_retention(la, dev)
     if rank == 0 and not args.skip_cpu:
         result["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     assert la.last_error() == 0
@@ -402,6 +403,54 @@ def bench_noncausal(la, dev):
             times.append(e0.elapsed_time(e1))
         ms = statistics.median(times)
         res[name] = {"ms": ms, "tokens_per_s": w.B * w.N / (ms / 1e3), "workload": w.name, "l2": "flushed"}
+    return res
+
+
+def bench_retention(la, dev):
+    """Retention (constant decay per head) forward at the long-context shape, and its decode step."""
+    w = W.RETENTION_BF16
+    q, k, v = (t.to(dev) for t in W.make_inputs(w))  # 805 MB of inputs: larger than L2
+    gam = W.retention_gammas(w.H).to(dev)
+    o = torch.empty_like(v)
+    ws = torch.empty(la.workspace_bytes(la.OP_RETENTION_FWD, w.B, w.H, w.N, w.Dk, w.Dv, w.dtype),
+                     dtype=torch.uint8, device=dev)
+    for _ in range(3):
+        la.retention_fwd(q, k, v, gam, out=o, workspace=ws)
+    times = []
+    la.timing_reset()
+    la.timing_enable(True)
+    for _ in range(5):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        la.retention_fwd(q, k, v, gam, out=o, workspace=ws)
+        e1.record()
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    la.timing_enable(False)
+    kern = {n: ms / c for n, (c, ms) in la.timing_read().items()}
+    ms = statistics.median(times)
+    res = {"fwd": {"ms": ms, "tokens_per_s": w.B * w.N / (ms / 1e3), "workload": w.name,
+                   "kernel_ms": kern, "l2": "inputs larger than L2"}}
+    del q, k, v, o, ws
+    # decode: S <- gamma S + k v^T, out = S^T q at the decode shape, eager launches
+    wd = W.DECODE_CIFAR
+    T = 200
+    qd, kd, vd = (t.to(dev) for t in W.make_decode_inputs(wd, steps=T))
+    gd = W.retention_gammas(wd.H).to(dev)
+    S = torch.zeros(wd.B, wd.H, wd.Dk, wd.Dv, device=dev)
+    outs = torch.empty(T, wd.B, wd.H, wd.Dv, device=dev)
+    for t in range(3):
+        la.retention_step(qd[t], kd[t], vd[t], gd, S, out=outs[t])
+    torch.cuda.synchronize()
+    la.timing_reset()
+    la.timing_enable(True)
+    for t in range(T):
+        la.retention_step(qd[t], kd[t], vd[t], gd, S, out=outs[t])
+    torch.cuda.synchronize()
+    la.timing_enable(False)
+    n_l, ms_l = la.timing_read()["retention_step"]
+    res["step"] = {"kernel_us": ms_l * 1e3 / n_l, "workload": "retention decode f32 B=%d H=%d Dk=Dv=%d" %
+                   (wd.B, wd.H, wd.Dk)}
     return res
 
 

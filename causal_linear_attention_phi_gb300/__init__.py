@@ -19,12 +19,12 @@ from . import build as _build
 
 __all__ = [
     "LaError", "noncausal_fwd", "noncausal_bwd", "causal_fwd", "causal_bwd", "causal_step_host", "host_step_bytes",
-    "recurrent_step", "workspace_bytes",
+    "recurrent_step", "retention_fwd", "retention_step", "workspace_bytes",
     "last_error", "clear_error", "timing_enable", "timing_reset", "timing_read", "library", "version",
-    "OP_NONCAUSAL_FWD", "OP_CAUSAL_FWD", "OP_CAUSAL_BWD", "OP_NONCAUSAL_BWD",
+    "OP_NONCAUSAL_FWD", "OP_CAUSAL_FWD", "OP_CAUSAL_BWD", "OP_NONCAUSAL_BWD", "OP_RETENTION_FWD",
 ]
 
-OP_NONCAUSAL_FWD, OP_CAUSAL_FWD, OP_CAUSAL_BWD, OP_NONCAUSAL_BWD = 0, 1, 2, 3
+OP_NONCAUSAL_FWD, OP_CAUSAL_FWD, OP_CAUSAL_BWD, OP_NONCAUSAL_BWD, OP_RETENTION_FWD = 0, 1, 2, 3, 4
 LA_F32, LA_BF16 = 0, 1
 _STATUS = {0: "LA_OK", 1: "LA_ERR_INVALID_ARG", 2: "LA_ERR_UNSUPPORTED", 3: "LA_ERR_WORKSPACE",
            4: "LA_ERR_CUDA", 5: "LA_ERR_TIMEOUT"}
@@ -64,6 +64,8 @@ def _declare(lib):
     lib.la_causal_fwd_with_state.argtypes = [_vp] * 6 + [Shape, _vp, ctypes.c_size_t, _vp]
     lib.la_causal_bwd_after_fwd.argtypes = [_vp] * 7 + [Shape, _vp, ctypes.c_size_t, _vp, ctypes.c_size_t, _vp]
     lib.la_recurrent_step.argtypes = [_vp] * 6 + [Shape, _vp]
+    lib.la_retention_fwd.argtypes = [_vp] * 6 + [Shape, _vp, ctypes.c_size_t, _vp]
+    lib.la_retention_step.argtypes = [_vp] * 6 + [Shape, _vp]
     for f in ("la_causal_step_host", "la_noncausal_fwd", "la_noncausal_bwd", "la_causal_fwd", "la_causal_fwd_with_state", "la_causal_bwd", "la_causal_bwd_after_fwd",
               "la_recurrent_step",
               "la_last_error",
@@ -279,6 +281,53 @@ def recurrent_step(q, k, v, S, z, out=None, stream=None):
     s = Shape(B, H, 1, Dk, Dv, _dtype_code(q))
     _check(library().la_recurrent_step(_ptr(q), _ptr(k), _ptr(v), _ptr(S), _ptr(z), _ptr(out), s, _stream_ptr(stream)),
            "la_recurrent_step")
+    return out
+
+
+def _gamma(gamma, H):
+    _need_cuda(gamma)
+    if gamma.dtype != torch.float32 or gamma.shape != (H,):
+        raise ValueError("gamma must be an fp32 CUDA tensor of shape [H] (one decay per head)")
+    return gamma
+
+
+def retention_fwd(q, k, v, gamma, out=None, workspace=None, stream=None, return_state=False):
+    """Retention with a constant decay per head: o_t = sum_{j<=t} gamma^(t-j) (q_t . k_j) v_j.
+
+    No feature map and no normaliser; gamma is fp32 [H] on the device.  With
+    return_state, returns (o, S): S [B,H,Dk,Dv] fp32 is the state after the
+    last position, from which retention_step continues.
+    """
+    _need_cuda(q, k, v)
+    s = _shape4(q, k, v)
+    _gamma(gamma, q.shape[1])
+    if out is None:
+        out = torch.empty_like(v)
+    S = None
+    if return_state:
+        B, H, _, Dk = q.shape
+        S = torch.empty(B, H, Dk, v.shape[-1], dtype=torch.float32, device=q.device)
+    ws, nb = _workspace(OP_RETENTION_FWD, s, q.device, workspace)
+    _check(library().la_retention_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(gamma), _ptr(out), _ptr(S), s, _ptr(ws), nb,
+                                      _stream_ptr(stream)), "la_retention_fwd")
+    return (out, S) if return_state else out
+
+
+def retention_step(q, k, v, gamma, S, out=None, stream=None):
+    """One retention decode step: S <- gamma S + k v^T (in place), out = S^T q."""
+    _need_cuda(q, k, v, S)
+    if q.dim() != 3 or k.shape != q.shape or v.shape[:2] != q.shape[:2]:
+        raise ValueError("expected q, k [B,H,Dk] and v [B,H,Dv]")
+    B, H, Dk = q.shape
+    Dv = v.shape[2]
+    _gamma(gamma, H)
+    if S.dtype != torch.float32 or S.shape != (B, H, Dk, Dv):
+        raise ValueError("S must be fp32 [B,H,Dk,Dv]")
+    if out is None:
+        out = torch.empty_like(v)
+    s = Shape(B, H, 1, Dk, Dv, _dtype_code(q))
+    _check(library().la_retention_step(_ptr(q), _ptr(k), _ptr(v), _ptr(gamma), _ptr(S), _ptr(out), s,
+                                       _stream_ptr(stream)), "la_retention_step")
     return out
 
 

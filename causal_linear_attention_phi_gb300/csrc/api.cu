@@ -188,7 +188,8 @@ static size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 WsLayout make_ws_layout(const la_shape& s, int op, const Plan& p) {
     WsLayout w{};
     const size_t BH = (size_t)s.B * s.H;
-    const size_t E = plan_state_elems(p);
+    // retention records hold S only (no normaliser)
+    const size_t E = op == LA_OP_RETENTION_FWD ? (size_t)s.Dk * s.Dv : plan_state_elems(p);
     const size_t seg = align256(BH * p.P * E * sizeof(float));
     size_t off = 0;
     w.seg_states = off;
@@ -246,12 +247,13 @@ la_status check_device() {
     return ok > 0 ? LA_OK : fail(LA_ERR_UNSUPPORTED, "device is not sm_103");
 }
 
-// A tensor argument must be a 16-byte aligned pointer to device (or managed)
-// memory of the current device.  Host pointers are refused here, before any
-// kernel could dereference them.
-la_status check_ptr(const void* p, const char* what) {
+// A tensor argument must be a 16-byte aligned (`align`) pointer to device (or
+// managed) memory of the current device.  Host pointers are refused here,
+// before any kernel could dereference them.
+la_status check_ptr(const void* p, const char* what, uintptr_t align = 16) {
     if (!p) return fail(LA_ERR_INVALID_ARG, "%s is NULL", what);
-    if (reinterpret_cast<uintptr_t>(p) & 15) return fail(LA_ERR_INVALID_ARG, "%s is not 16-byte aligned", what);
+    if (reinterpret_cast<uintptr_t>(p) & (align - 1))
+        return fail(LA_ERR_INVALID_ARG, "%s is not %d-byte aligned", what, (int)align);
     cudaPointerAttributes attr;
     cudaError_t e = cudaPointerGetAttributes(&attr, p);
     if (e != cudaSuccess) {
@@ -389,7 +391,7 @@ static la_status causal_fwd_impl(const void* q, const void* k, const void* v, vo
 extern "C" {
 
 size_t la_workspace_bytes(int op, la_shape s) {
-    if (op < LA_OP_NONCAUSAL_FWD || op > LA_OP_NONCAUSAL_BWD) return 0;
+    if (op < LA_OP_NONCAUSAL_FWD || op > LA_OP_RETENTION_FWD) return 0;
     if (check_shape(s) != LA_OK || empty(s)) return 0;
     const Plan p = make_plan(s, op);
     return make_ws_layout(s, op, p).bytes;
@@ -527,6 +529,59 @@ la_status la_recurrent_step(const void* q, const void* k, const void* v, float* 
     LA_TRY(check_ptr(out, "out"));
     LA_TRY(cuda_status(la::recurrent_step(q, k, v, S, z, out, s1, reinterpret_cast<cudaStream_t>(stream)),
                        "recurrent step"));
+    return LA_OK;
+}
+
+la_status la_retention_fwd(const void* q, const void* k, const void* v, const float* gamma, void* o, float* S,
+                           la_shape s, void* ws, size_t ws_bytes, la_stream_t stream) {
+    t_detail.clear();
+    LA_TRY(check_shape(s));
+    if (s.B == 0 || s.H == 0) return LA_OK;
+    LA_TRY(check_device());
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (s.N == 0) {  // no position: the state after it is zero
+        if (!S) return LA_OK;
+        LA_TRY(check_ptr(S, "S"));
+        LA_TRY(cuda_status(cudaMemsetAsync(S, 0, (size_t)s.B * s.H * s.Dk * s.Dv * sizeof(float), st), "state clear"));
+        return LA_OK;
+    }
+    LA_TRY(check_ptr(q, "q"));
+    LA_TRY(check_ptr(k, "k"));
+    LA_TRY(check_ptr(v, "v"));
+    LA_TRY(check_ptr(o, "o"));
+    LA_TRY(check_ptr(gamma, "gamma", 4));
+    if (S) LA_TRY(check_ptr(S, "S"));
+    const Plan p = make_plan(s, LA_OP_RETENTION_FWD);
+    const WsLayout w = make_ws_layout(s, LA_OP_RETENTION_FWD, p);
+    LA_TRY(check_ws(ws, ws_bytes, w.bytes));
+    float* seg = reinterpret_cast<float*>(static_cast<char*>(ws) + w.seg_states);
+    if (p.P > 1 || S) {
+        LA_TRY(cuda_status(retention_segment_sums(k, v, gamma, seg, s, p, st), "retention segment sums"));
+        LA_TRY(cuda_status(retention_scan(seg, S, gamma, s, p, st), "retention segment scan"));
+    } else {
+        const size_t seg_bytes = (size_t)s.B * s.H * s.Dk * s.Dv * sizeof(float);
+        LA_TRY(cuda_status(cudaMemsetAsync(seg, 0, seg_bytes, st), "state clear"));
+    }
+    LA_TRY(cuda_status(retention_out(q, k, v, gamma, o, seg, s, p, st), "retention forward"));
+    return LA_OK;
+}
+
+la_status la_retention_step(const void* q, const void* k, const void* v, const float* gamma, float* S, void* out,
+                            la_shape s, la_stream_t stream) {
+    t_detail.clear();
+    la_shape s1 = s;
+    s1.N = 1;  // N is ignored by the step
+    LA_TRY(check_shape(s1));
+    if (empty(s1)) return LA_OK;
+    LA_TRY(check_device());
+    LA_TRY(check_ptr(q, "q"));
+    LA_TRY(check_ptr(k, "k"));
+    LA_TRY(check_ptr(v, "v"));
+    LA_TRY(check_ptr(gamma, "gamma", 4));
+    LA_TRY(check_ptr(S, "S"));
+    LA_TRY(check_ptr(out, "out"));
+    LA_TRY(cuda_status(la::retention_step(q, k, v, gamma, S, out, s1, reinterpret_cast<cudaStream_t>(stream)),
+                       "retention step"));
     return LA_OK;
 }
 

@@ -114,6 +114,16 @@ cudaError_t tc_bwd_forward_sweep(const void* q, const void* k, const void* v, co
 cudaError_t tc_bwd_reverse_sweep(const void* q, const void* k, const void* v, const void* dout, void* dk, void* dv,
                                  const float* seg_R, const float* den_g, const la_shape& s, const Plan& p,
                                  cudaStream_t st);
+// Retention (constant decay per head), CUDA-core kernels, any dtype and head size;
+// segment records are Dk*Dv floats (no z).
+cudaError_t retention_segment_sums(const void* k, const void* v, const float* gamma, float* seg, const la_shape& s,
+                                   const Plan& p, cudaStream_t st);
+cudaError_t retention_scan(float* seg, float* S_out, const float* gamma, const la_shape& s, const Plan& p,
+                           cudaStream_t st);
+cudaError_t retention_out(const void* q, const void* k, const void* v, const float* gamma, void* o, const float* seg,
+                          const la_shape& s, const Plan& p, cudaStream_t st);
+cudaError_t retention_step(const void* q, const void* k, const void* v, const float* gamma, float* S, void* out,
+                           const la_shape& s, cudaStream_t st);
 bool tc_supported(const la_shape& s, int op);
 
 enum ScanMode { SCAN_EXCLUSIVE_PREFIX = 0, SCAN_EXCLUSIVE_SUFFIX = 1, SCAN_TOTAL = 2 };

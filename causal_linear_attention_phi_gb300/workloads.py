@@ -43,6 +43,18 @@ FWD_BF16 = Workload("causal+noncausal fwd bf16 B=4 H=8 N=1024 Dk=Dv=64", 4, 8, 1
 LONG_BF16 = Workload("causal fwd+bwd bf16 B=2 H=16 N=65536 Dk=Dv=128", 2, 16, 65536, 128, 128,
                      torch.bfloat16, 5, qk_scale=1 / math.sqrt(128), ops=("causal_fwd", "causal_bwd"))
 
+# Retention (constant decay per head) forward at the long-context shape: B=2 H=16 N=65536 D=128 bf16;
+# Q, K ~ N(0,1) * 128^-1/4 (so q . k ~ N(0,1)), V ~ N(0,1); decays from retention_gammas(16).
+RETENTION_BF16 = Workload("retention fwd bf16 B=2 H=16 N=65536 Dk=Dv=128", 2, 16, 65536, 128, 128,
+                          torch.bfloat16, 6, qk_scale=128 ** -0.25, ops=("retention_fwd",))
+
+
+def retention_gammas(H: int) -> torch.Tensor:
+    """Per-head decays (fp32 [H], CPU): 1 - gamma_h spaced evenly in log from 1/32 to 1/1024."""
+    e = torch.linspace(5.0, 10.0, H, dtype=torch.float64) if H > 1 else torch.tensor([5.0], dtype=torch.float64)
+    return (1.0 - torch.pow(2.0, -e)).float()
+
+
 # 3: length sweep of causal fwd+bwd, bf16, B=1 H=8 D=64, N = 2^9 .. 2^16, all N(0,1).
 SWEEP_NS = tuple(2 ** e for e in range(9, 17))
 

@@ -68,7 +68,8 @@ typedef enum {
     LA_OP_NONCAUSAL_FWD = 0,
     LA_OP_CAUSAL_FWD = 1,
     LA_OP_CAUSAL_BWD = 2,
-    LA_OP_NONCAUSAL_BWD = 3
+    LA_OP_NONCAUSAL_BWD = 3,
+    LA_OP_RETENTION_FWD = 4
 } la_op;
 
 /* Problem shape.  dtype is an la_dtype value. */
@@ -207,6 +208,41 @@ la_status la_causal_step_host(const void* q, const void* k, const void* v, const
  */
 la_status la_recurrent_step(const void* q, const void* k, const void* v, float* S, float* z,
                             void* out, la_shape s, la_stream_t stream);
+
+/*
+ * Retention: causal linear attention with a constant decay per head, the
+ * decayed update of itwiki 선형 어텐션, section 발전: 감쇠, 게이트, 델타 규칙
+ * (RetNet's gamma):
+ *   S_t = gamma_h S_(t-1) + k_t v_t^T  (S_(-1) = 0),   o_t = S_t^T q_t,
+ * i.e. o_t = sum_(j<=t) gamma_h^(t-j) (q_t . k_j) v_j.  The feature map is the
+ * identity and there is no normaliser (phi and z above do not enter), so
+ * gamma = 1 gives the plain masked product tril(Q K^T) V, and gamma = 0 gives
+ * o_t = (q_t . k_t) v_t (0^0 = 1).  Computed in the chunked form: a decay mask
+ * gamma^(a-b) inside a chunk of C = 64 positions, the carried state seen
+ * through gamma^(a+1), and a decayed prefix scan over segments of chunks.
+ * q, k: [B,H,N,Dk]; v, o: [B,H,N,Dv] in s.dtype; o written.
+ * gamma: DEVICE pointer to H fp32 values (one per head, shared by the B batch
+ *   entries), 4-byte aligned, read only.  Any real value is computed as
+ *   written; the method intends 0 <= gamma <= 1 (|gamma| > 1 grows without
+ *   bound).
+ * S: NULL, or a DEVICE fp32 [B,H,Dk,Dv] that receives the state after the
+ *   last position (written, not accumulated; zero for N = 0), from which
+ *   la_retention_step continues the sequence.
+ * Workspace: la_workspace_bytes(LA_OP_RETENTION_FWD, s).
+ */
+la_status la_retention_fwd(const void* q, const void* k, const void* v, const float* gamma,
+                           void* o, float* S, la_shape s,
+                           void* ws, size_t ws_bytes, la_stream_t stream);
+
+/*
+ * One decode step of retention for every head, the state updated first and
+ * then read:  S <- gamma_h S + k v^T,  out = S^T q.
+ * q, k: [B,H,Dk]; v, out: [B,H,Dv] in s.dtype; gamma as for la_retention_fwd;
+ * S: [B,H,Dk,Dv] fp32, read and updated in place (zero before the first step
+ * of a sequence, or the S of la_retention_fwd).  s.N is ignored.  No workspace.
+ */
+la_status la_retention_step(const void* q, const void* k, const void* v, const float* gamma,
+                            float* S, void* out, la_shape s, la_stream_t stream);
 
 /*
  * la_causal_fwd with no workspace argument: the same causal forward, with its

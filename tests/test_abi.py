@@ -33,6 +33,7 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for required in ("la_noncausal_fwd", "la_causal_fwd", "la_causal_bwd", "la_recurrent_step",
+                     "la_retention_fwd", "la_retention_step",
                      "la_workspace_bytes", "la_last_error", "la_status_string"):
         assert required in names
 
@@ -58,6 +59,9 @@ def test_workspace_bytes_is_pure(la):
     assert la.workspace_bytes(la.OP_CAUSAL_FWD, 2, 16, 0, 128, 128, torch.bfloat16) == 0
     assert la.workspace_bytes(la.OP_CAUSAL_FWD, 2, 16, 64, 48, 128, torch.bfloat16) == 0   # unsupported size
     assert la.workspace_bytes(99, 2, 16, 64, 64, 64, torch.bfloat16) == 0                   # bad op
+    # retention records hold S only: smaller than the CUDA-core causal forward's (S, z) records
+    rw = la.workspace_bytes(la.OP_RETENTION_FWD, 2, 16, 65536, 128, 128, torch.float32)
+    assert 0 < rw < la.workspace_bytes(la.OP_CAUSAL_FWD, 2, 16, 65536, 128, 128, torch.float32)
 
 
 def _call_fwd(la, shape, ptr=0):
