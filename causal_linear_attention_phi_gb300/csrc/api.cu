@@ -140,7 +140,8 @@ static constexpr int kMaxWaves = 8;
 // For the non-causal forward only its segment sums run on the tensor cores.
 bool tc_supported(const la_shape& s, int op) {
     return s.dtype == LA_BF16 && s.Dk == s.Dv && (s.Dk == 128 || s.Dk == 64) &&
-           (op == LA_OP_CAUSAL_FWD || op == LA_OP_CAUSAL_BWD || op == LA_OP_NONCAUSAL_FWD);
+           (op == LA_OP_CAUSAL_FWD || op == LA_OP_CAUSAL_BWD || op == LA_OP_NONCAUSAL_FWD ||
+            op == LA_OP_RETENTION_FWD);
 }
 
 static void finish_plan(Plan& p, int P) {
@@ -189,7 +190,7 @@ WsLayout make_ws_layout(const la_shape& s, int op, const Plan& p) {
     WsLayout w{};
     const size_t BH = (size_t)s.B * s.H;
     // retention records hold S only (no normaliser)
-    const size_t E = op == LA_OP_RETENTION_FWD ? (size_t)s.Dk * s.Dv : plan_state_elems(p);
+    const size_t E = op == LA_OP_RETENTION_FWD ? (size_t)p.sk * p.sv : plan_state_elems(p);
     const size_t seg = align256(BH * p.P * E * sizeof(float));
     size_t off = 0;
     w.seg_states = off;
@@ -556,13 +557,20 @@ la_status la_retention_fwd(const void* q, const void* k, const void* v, const fl
     LA_TRY(check_ws(ws, ws_bytes, w.bytes));
     float* seg = reinterpret_cast<float*>(static_cast<char*>(ws) + w.seg_states);
     if (p.P > 1 || S) {
-        LA_TRY(cuda_status(retention_segment_sums(k, v, gamma, seg, s, p, st), "retention segment sums"));
+        if (p.tc)
+            LA_TRY(cuda_status(tc_retention_fwd(nullptr, k, v, gamma, nullptr, seg, s, p, false, st),
+                               "retention segment sums"));
+        else
+            LA_TRY(cuda_status(retention_segment_sums(k, v, gamma, seg, s, p, st), "retention segment sums"));
         LA_TRY(cuda_status(retention_scan(seg, S, gamma, s, p, st), "retention segment scan"));
     } else {
-        const size_t seg_bytes = (size_t)s.B * s.H * s.Dk * s.Dv * sizeof(float);
+        const size_t seg_bytes = (size_t)s.B * s.H * p.sk * p.sv * sizeof(float);
         LA_TRY(cuda_status(cudaMemsetAsync(seg, 0, seg_bytes, st), "state clear"));
     }
-    LA_TRY(cuda_status(retention_out(q, k, v, gamma, o, seg, s, p, st), "retention forward"));
+    if (p.tc)
+        LA_TRY(cuda_status(tc_retention_fwd(q, k, v, gamma, o, seg, s, p, true, st), "retention forward"));
+    else
+        LA_TRY(cuda_status(retention_out(q, k, v, gamma, o, seg, s, p, st), "retention forward"));
     return LA_OK;
 }
 

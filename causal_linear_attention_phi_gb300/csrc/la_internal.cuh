@@ -114,14 +114,18 @@ cudaError_t tc_bwd_forward_sweep(const void* q, const void* k, const void* v, co
 cudaError_t tc_bwd_reverse_sweep(const void* q, const void* k, const void* v, const void* dout, void* dk, void* dv,
                                  const float* seg_R, const float* den_g, const la_shape& s, const Plan& p,
                                  cudaStream_t st);
-// Retention (constant decay per head), CUDA-core kernels, any dtype and head size;
-// segment records are Dk*Dv floats (no z).
+// Retention (constant decay per head).  Segment records are sk*sv floats (S only,
+// no z).  CUDA-core kernels for any dtype and head size; the scan serves both paths.
 cudaError_t retention_segment_sums(const void* k, const void* v, const float* gamma, float* seg, const la_shape& s,
                                    const Plan& p, cudaStream_t st);
 cudaError_t retention_scan(float* seg, float* S_out, const float* gamma, const la_shape& s, const Plan& p,
                            cudaStream_t st);
 cudaError_t retention_out(const void* q, const void* k, const void* v, const float* gamma, void* o, const float* seg,
                           const la_shape& s, const Plan& p, cudaStream_t st);
+// Tensor-core retention (bf16, Dk = Dv = 128 or 64, C = 128): out_pass = false forms
+// the segments' local states in seg, true the outputs from the scanned prefixes.
+cudaError_t tc_retention_fwd(const void* q, const void* k, const void* v, const float* gamma, void* o, float* seg,
+                             const la_shape& s, const Plan& p, bool out_pass, cudaStream_t st);
 cudaError_t retention_step(const void* q, const void* k, const void* v, const float* gamma, float* S, void* out,
                            const la_shape& s, cudaStream_t st);
 bool tc_supported(const la_shape& s, int op);

@@ -92,7 +92,7 @@ retention_sums_kernel(const T* __restrict__ k, const T* __restrict__ v, const fl
                 for (int j = 0; j < kMaxT; ++j) s[a][j] = fmaf(kd[a], vm[j], s[a][j]);
         }
     }
-    float* out = seg + (bh * P + p) * (size_t)Dk * Dv;
+    float* out = seg + (bh * P + p) * (size_t)Dk * Dv;  // unpadded records on this path
 #pragma unroll
     for (int a = 0; a < kMaxT; ++a)
 #pragma unroll
@@ -102,12 +102,15 @@ retention_sums_kernel(const T* __restrict__ k, const T* __restrict__ v, const fl
 
 // ---------------------------------------------------------------- decayed scan over segments
 // In place: seg[bh][p] <- R_p with R_0 = 0 and R_(p+1) = gamma^(L_p) R_p + seg[bh][p].
-// With S_out, R_P (the state after position N) is written to S_out[bh].  Each
-// thread owns four consecutive elements of every record (E = Dk * Dv).
+// A record is an sk x sv state (sk = Dk, sv = Dv, or 128 x 128 on the padded
+// tensor-core path).  With S_out, R_P (the state after position N) is written
+// to S_out[bh] as Dk x Dv.  Each thread owns four consecutive elements of every
+// record (E = sk * sv).
 constexpr int kScanBatch = 8;
 
 __global__ void retention_scan_kernel(float* __restrict__ seg, float* __restrict__ S_out,
-                                      const float* __restrict__ gamma, int H, int N, int P, int seg_len, size_t E) {
+                                      const float* __restrict__ gamma, int H, int N, int P, int seg_len, size_t E,
+                                      int sv, int Dk, int Dv) {
     const size_t e4 = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
     if (e4 >= E) return;
     const size_t bh = blockIdx.y;
@@ -135,7 +138,10 @@ __global__ void retention_scan_kernel(float* __restrict__ seg, float* __restrict
             }
         }
     }
-    if (S_out) *reinterpret_cast<float4*>(S_out + bh * E + e4) = run;
+    if (S_out) {
+        const int d = (int)(e4 / sv), m = (int)(e4 % sv);
+        if (d < Dk && m < Dv) *reinterpret_cast<float4*>(S_out + bh * Dk * Dv + (size_t)d * Dv + m) = run;
+    }
 }
 
 // ---------------------------------------------------------------- outputs
@@ -346,10 +352,10 @@ cudaError_t retention_segment_sums(const void* k, const void* v, const float* ga
 
 cudaError_t retention_scan(float* seg, float* S_out, const float* gamma, const la_shape& s, const Plan& p,
                            cudaStream_t st) {
-    const size_t E = (size_t)s.Dk * s.Dv;  // a multiple of 256 for the supported head sizes
+    const size_t E = (size_t)p.sk * p.sv;  // a multiple of 256 for the supported head sizes
     const dim3 grid((unsigned)((E / 4 + 127) / 128), s.B * s.H);
     launch_begin("retention_scan", st);
-    retention_scan_kernel<<<grid, 128, 0, st>>>(seg, S_out, gamma, s.H, s.N, p.P, p.cps * p.C, E);
+    retention_scan_kernel<<<grid, 128, 0, st>>>(seg, S_out, gamma, s.H, s.N, p.P, p.cps * p.C, E, p.sv, s.Dk, s.Dv);
     return launch_end("retention_scan", st);
 }
 

@@ -73,6 +73,40 @@ def test_retention_fwd_cases(la, B, H, N, Dk, Dv, dtype):
         check("retention S", S, Sref, 1e-4 if dtype == torch.float32 else 1e-3)
 
 
+# bf16 heads of 128 (or 64, padded on chip) run on the tensor-core kernels (chunks of 128)
+TC_CASES = [
+    (1, 3, 1, 128, 128),      # a single position
+    (1, 2, 127, 128, 128),    # one short chunk
+    (2, 3, 128, 128, 128),    # exactly one chunk
+    (1, 3, 129, 64, 64),      # one position past a chunk, padded head
+    (1, 6, 1000, 128, 128),   # several chunks and segments, ragged tail
+    (2, 6, 3001, 64, 64),
+    (1, 2, 8192, 128, 128),   # long segments: the reverse-walk sums over many chunks
+]
+
+
+@pytest.mark.parametrize("B,H,N,Dk,Dv", TC_CASES)
+def test_retention_tensor_core_cases(la, B, H, N, Dk, Dv):
+    q, k, v = W.random_case(1900 + N, B, H, N, Dk, Dv, dtype=torch.bfloat16, scale=Dk ** -0.25)
+    g = gammas(H)
+    la.timing_reset()
+    la.timing_enable(True)
+    try:
+        o, S = la.retention_fwd(q.to(DEV), k.to(DEV), v.to(DEV), g.to(DEV), return_state=True)
+        torch.cuda.synchronize()
+    finally:
+        la.timing_enable(False)
+    assert "tc_retention_out" in la.timing_read()
+    ref = oracle.retention_direct(q, k, v, g) if N <= 1000 else oracle.retention_chunked(q, k, v, g, 128)
+    check("retention o (tensor cores)", o, ref, 2e-2)
+    # the final state against the oracle's decode recurrence (bf16 K' and V products, fp32 sums)
+    if N <= 300:
+        Sref = np.zeros((B, H, Dk, Dv))
+        for t in range(N):
+            _, Sref = oracle.retention_step(q[:, :, t], k[:, :, t], v[:, :, t], g, Sref)
+        check("retention S (tensor cores)", S, Sref, 1e-2)
+
+
 def test_gamma_one_is_the_masked_product(la):
     """gamma = 1: o = tril(Q K^T) V, checked against a float64 matrix product."""
     q, k, v = W.random_case(31, 1, 2, 300, 64, 32, dtype=torch.float32, scale=64 ** -0.25)
