@@ -61,10 +61,10 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 // phi(x) = elu(x) + 1 (alpha = 1): x + 1 for x > 0, exp(x) = 2^(x log2 e) for x <= 0.
-// Branch-free: the exponential is taken of min(x, 0) and selected.
+// Branch-free and select-free: max(x, 0) + 2^(min(x, 0) log2 e) is x + 2^0 for
+// x > 0 and 0 + e^x otherwise.
 __device__ __forceinline__ float phi_f(float x) {
-    const float e = ex2_approx(fminf(x, 0.f) * 1.4426950408889634f);
-    return x > 0.f ? x + 1.f : e;
+    return fmaxf(x, 0.f) + ex2_approx(fminf(x, 0.f) * 1.4426950408889634f);
 }
 // phi'(x) = 1 for x > 0, exp(x) otherwise; equal to min(1, phi(x)).
 __device__ __forceinline__ float dphi_from_phi(float p) { return fminf(p, 1.f); }

@@ -251,9 +251,10 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
                     qrow[4 * c8 + 1] = qv.y;
                     qrow[4 * c8 + 2] = qv.z;
                     qrow[4 * c8 + 3] = qv.w;
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        di += bf_lo(qrow[4 * c8 + e]) * zsh[8 * lc + 2 * e] + bf_hi(qrow[4 * c8 + e]) * zsh[8 * lc + 2 * e + 1];
+                    const float4 za = *reinterpret_cast<const float4*>(zsh + 8 * lc);
+                    const float4 zb = *reinterpret_cast<const float4*>(zsh + 8 * lc + 4);
+                    di += bf_lo(qv.x) * za.x + bf_hi(qv.x) * za.y + bf_lo(qv.y) * za.z + bf_hi(qv.y) * za.w +
+                          bf_lo(qv.z) * zb.x + bf_hi(qv.z) * zb.y + bf_lo(qv.w) * zb.z + bf_hi(qv.w) * zb.w;
                 }
                 dpart[128 * h + r] = di;
             }
@@ -279,12 +280,20 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
                         uint32_t w[32];
                         tmem_ld32(tmem + lb + kFX + 32 * cb, w);
                         tmem_ld_wait();
+                        if (j0 + 31 < (r & ~31)) {  // below the diagonal for the whole warp: no mask
 #pragma unroll
-                        for (int x = 0; x < 16; ++x) {
-                            const int j = j0 + 2 * x;
-                            pk[x] = pack_bf16x2(j <= r ? __uint_as_float(w[2 * x]) : 0.f,
-                                                j + 1 <= r ? __uint_as_float(w[2 * x + 1]) : 0.f);
-                            rs += bf_lo(pk[x]) + bf_hi(pk[x]);
+                            for (int x = 0; x < 16; ++x) {
+                                pk[x] = pack_bf16x2(__uint_as_float(w[2 * x]), __uint_as_float(w[2 * x + 1]));
+                                rs += bf_lo(pk[x]) + bf_hi(pk[x]);
+                            }
+                        } else {
+#pragma unroll
+                            for (int x = 0; x < 16; ++x) {
+                                const int j = j0 + 2 * x;
+                                pk[x] = pack_bf16x2(j <= r ? __uint_as_float(w[2 * x]) : 0.f,
+                                                    j + 1 <= r ? __uint_as_float(w[2 * x + 1]) : 0.f);
+                                rs += bf_lo(pk[x]) + bf_hi(pk[x]);
+                            }
                         }
                     }
                     tmem_st16(tmem + lb + kFX + 32 * cb, pk);
@@ -369,13 +378,22 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
                     uint32_t w[32];
                     tmem_ld32(tmem + lb + kFX + 32 * cb, w);
                     tmem_ld_wait();
+                    if (j0 + 31 < (r & ~31)) {  // below the diagonal for the whole warp: no mask
 #pragma unroll
-                    for (int x = 0; x < 16; ++x) {
-                        const int j = j0 + 2 * x;
-                        const float d0 = j <= r ? __uint_as_float(w[2 * x]) + g : 0.f;
-                        const float d1 = j + 1 <= r ? __uint_as_float(w[2 * x + 1]) + g : 0.f;
-                        hi[x] = pack_bf16x2(d0, d1);
-                        lo[x] = pack_bf16x2(d0 - bf_lo(hi[x]), d1 - bf_hi(hi[x]));
+                        for (int x = 0; x < 16; ++x) {
+                            const float d0 = __uint_as_float(w[2 * x]) + g, d1 = __uint_as_float(w[2 * x + 1]) + g;
+                            hi[x] = pack_bf16x2(d0, d1);
+                            lo[x] = pack_bf16x2(d0 - bf_lo(hi[x]), d1 - bf_hi(hi[x]));
+                        }
+                    } else {
+#pragma unroll
+                        for (int x = 0; x < 16; ++x) {
+                            const int j = j0 + 2 * x;
+                            const float d0 = j <= r ? __uint_as_float(w[2 * x]) + g : 0.f;
+                            const float d1 = j + 1 <= r ? __uint_as_float(w[2 * x + 1]) + g : 0.f;
+                            hi[x] = pack_bf16x2(d0, d1);
+                            lo[x] = pack_bf16x2(d0 - bf_lo(hi[x]), d1 - bf_hi(hi[x]));
+                        }
                     }
                 }
                 tmem_st16(tmem + lb + kFX + 32 * cb, hi);
@@ -400,12 +418,15 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
                     const uint32_t* qu = &qrow[4 * (4 * cb + c4)];
                     uint4 o4;
                     uint32_t* ou = reinterpret_cast<uint32_t*>(&o4);
+                    float zr[8];
+                    *reinterpret_cast<float4*>(zr) = *reinterpret_cast<const float4*>(zsh + 64 * h + 32 * cb + 8 * c4);
+                    *reinterpret_cast<float4*>(zr + 4) =
+                        *reinterpret_cast<const float4*>(zsh + 64 * h + 32 * cb + 8 * c4 + 4);
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const int d = 64 * h + 32 * cb + 8 * c4 + 2 * e;
-                        const float a0 = (__uint_as_float(w[8 * c4 + 2 * e]) + g * zsh[d]) * dphi_from_phi(bf_lo(qu[e]));
+                        const float a0 = (__uint_as_float(w[8 * c4 + 2 * e]) + g * zr[2 * e]) * dphi_from_phi(bf_lo(qu[e]));
                         const float a1 =
-                            (__uint_as_float(w[8 * c4 + 2 * e + 1]) + g * zsh[d + 1]) * dphi_from_phi(bf_hi(qu[e]));
+                            (__uint_as_float(w[8 * c4 + 2 * e + 1]) + g * zr[2 * e + 1]) * dphi_from_phi(bf_hi(qu[e]));
                         ou[e] = pack_bf16x2(a0, a1);
                     }
                     *reinterpret_cast<uint4*>(sSb + chunk_off(r, 8 * h + 4 * cb + c4)) = o4;
@@ -641,6 +662,17 @@ tc_bwd_reverse_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
                 if (q0 + 31 < r) {  // every query here is before key r: all masked
 #pragma unroll
                     for (int x = 0; x < 16; ++x) pa[x] = pd[x] = 0u;
+                } else if ((r | 31) <= q0) {  // every query here is at or after every key of the warp
+                    uint32_t wa[32], wd[32];
+                    tmem_ld32(tmem + lb + kRDV, wa);
+                    tmem_ld32(tmem + lb + kRDK, wd);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int x = 0; x < 16; ++x) {
+                        const int qi = q0 + 2 * x;
+                        pa[x] = pack_bf16x2(__uint_as_float(wa[2 * x]), __uint_as_float(wa[2 * x + 1]));
+                        pd[x] = pack_bf16x2(__uint_as_float(wd[2 * x]) + gsh[qi], __uint_as_float(wd[2 * x + 1]) + gsh[qi + 1]);
+                    }
                 } else {
                     uint32_t wa[32], wd[32];
                     tmem_ld32(tmem + lb + kRDV, wa);

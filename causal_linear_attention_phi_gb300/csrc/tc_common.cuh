@@ -171,6 +171,17 @@ struct Grp {
     __device__ static __forceinline__ void phi_tile(uint8_t* tile, uint8_t* lo_tile, int ct, int n, int dcols,
                                                     const float* w, float* colpart, uint8_t* copy_tile = nullptr,
                                                     const float* scale = nullptr) {
+        // a whole tile (every row and column in range: all chunks but a short last one of a
+        // full-width head) takes the copy of the body without the per-element range test
+        if (n >= kC && dcols >= kD)
+            phi_tile_body<true>(tile, lo_tile, ct, n, dcols, w, colpart, copy_tile, scale);
+        else
+            phi_tile_body<false>(tile, lo_tile, ct, n, dcols, w, colpart, copy_tile, scale);
+    }
+    template <bool kWhole>
+    __device__ static __forceinline__ void phi_tile_body(uint8_t* tile, uint8_t* lo_tile, int ct, int n, int dcols,
+                                                         const float* w, float* colpart, uint8_t* copy_tile,
+                                                         const float* scale) {
         float zp[2][8];
 #pragma unroll
         for (int b = 0; b < 2; ++b)
@@ -185,7 +196,7 @@ struct Grp {
             uint32_t* u = reinterpret_cast<uint32_t*>(&v[j]);
             uint4 l;
             uint32_t* ul = reinterpret_cast<uint32_t*>(&l);
-            const bool valid = row < n && 64 * vec_block(j) + 8 * vec_lc(ct) < dcols;
+            const bool valid = kWhole || (row < n && 64 * vec_block(j) + 8 * vec_lc(ct) < dcols);
             const float wr = (w && valid) ? w[row] : 1.f;
             const float sr = scale ? scale[row] : 1.f;
 #pragma unroll

@@ -303,7 +303,7 @@ tc_causal_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                     uint32_t wv[32];
                     tmem_ld32(tmem + lane_base + kTmQK + j0, wv);
                     tmem_ld_wait();
-                    if (j0 + 31 <= r) {  // entirely on or below the diagonal
+                    if (j0 + 31 < (r & ~31)) {  // below the diagonal for every row of the warp
 #pragma unroll
                         for (int x = 0; x < 16; ++x)
                             pk[x] = pack_bf16x2(__uint_as_float(wv[2 * x]), __uint_as_float(wv[2 * x + 1]));

@@ -290,13 +290,22 @@ tc_retention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                     uint32_t wv[32];
                     tmem_ld32(tmem + lane_base + kTmQK + j0, wv);
                     tmem_ld_wait();
+                    if (j0 + 31 < (r & ~31)) {  // below the diagonal for every row of the warp
 #pragma unroll
-                    for (int x = 0; x < 16; ++x) {
-                        const int j = j0 + 2 * x;
-                        const float a0 = j <= r ? __uint_as_float(wv[2 * x]) * pw[j <= r ? r - j : 0] : 0.f;
-                        const float a1 =
-                            j + 1 <= r ? __uint_as_float(wv[2 * x + 1]) * pw[j + 1 <= r ? r - j - 1 : 0] : 0.f;
-                        pk[x] = pack_bf16x2(a0, a1);
+                        for (int x = 0; x < 16; ++x) {
+                            const int j = j0 + 2 * x;
+                            pk[x] = pack_bf16x2(__uint_as_float(wv[2 * x]) * pw[r - j],
+                                                __uint_as_float(wv[2 * x + 1]) * pw[r - j - 1]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int x = 0; x < 16; ++x) {
+                            const int j = j0 + 2 * x;
+                            const float a0 = j <= r ? __uint_as_float(wv[2 * x]) * pw[j <= r ? r - j : 0] : 0.f;
+                            const float a1 =
+                                j + 1 <= r ? __uint_as_float(wv[2 * x + 1]) * pw[j + 1 <= r ? r - j - 1 : 0] : 0.f;
+                            pk[x] = pack_bf16x2(a0, a1);
+                        }
                     }
                 }
                 tmem_st16(tmem + lane_base + kTmA + 32 * h + 16 * cb, pk);
