@@ -471,7 +471,7 @@ constexpr uint32_t kRR = 0, kRDK = 128, kRDV = 256, kRX = 384;
 struct RevSweepBars {
     uint64_t full, empty;
     uint64_t ready, rb_ready, masks_ready;
-    uint64_t at_dt_done, dkv_done;
+    uint64_t at_dt_done, dk_done, dkv_done;  // dk_done: the dK~ products; dkv_done: the dV products too
     uint64_t final_mma;
 };
 
@@ -588,6 +588,7 @@ tc_bwd_reverse_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)  // dK~ += D'^T Q'
                     mma_ts(tmem + kRDK, tmem + kRX + 8 * kk, desc_mnmajor(aQ, kk), id_kmn, 1);
+                mma_commit(&bar->dk_done);  // the dk epilogue runs during the dV products
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)  // dV = K~ R_next
                     mma_ss(tmem + kRDV, desc_kmajor(aK, kk), desc_mnmajor(aRb, kk), id_kmn, kk > 0);
@@ -694,9 +695,10 @@ tc_bwd_reverse_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
             tc_fence_before();
             RG::sync();
             if (ct == 0) mbar_arrive(&bar->masks_ready);
-            // (d) dk = (dK~ + r_next) * phi'(k) in place of phi(k) in Kc, dv into Rb; this
-            // thread's 32 columns of key row r; one TMA store each (rows past N are not written)
-            if (!RG::all(mbar_wait(&bar->dkv_done, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
+            // (d) dk = (dK~ + r_next) * phi'(k) in place of phi(k) in Kc once the dK~ products
+            // are done, then dv into Rb (free once the dV products are done); this thread's 32
+            // columns of key row r; one TMA store each (rows past N are not written)
+            if (!RG::all(mbar_wait(&bar->dk_done, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
             tc_fence_after();
             {
                 uint32_t w[32];
@@ -719,6 +721,8 @@ tc_bwd_reverse_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
                     *kp = o4;
                 }
             }
+            if (!RG::all(mbar_wait(&bar->dkv_done, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
+            tc_fence_after();
             {
                 uint32_t w[32];
                 tmem_ld32(tmem + lb + kRDV, w);
