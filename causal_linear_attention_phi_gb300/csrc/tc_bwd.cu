@@ -49,11 +49,12 @@ constexpr int kThreadsFS = 64 + 256, kThreadsRS = 64 + 512;  // + the TMA and MM
 constexpr uint32_t kFS = 0, kFR = 128, kFX = 256, kFY = 384;
 __device__ __forceinline__ uint32_t xcol(int kk) { return 32 * (kk >> 1) + 8 * (kk & 1); }
 
-// Q and V arrive (full_qv) and are released (empty_qv: the MMA's last read of
-// them and the compute group's last read of Q) apart from K and dO (full_kp,
-// empty_kp), so the next chunk's Q and V load during this chunk's D and dq work.
+// Q, V and dO arrive (full_qv) and are released (empty_qv: the MMA's last read of
+// them and the compute group's last read of Q) apart from K (full_k, empty_k:
+// the dq products read it last), so the next chunk's Q, V and dO load during
+// this chunk's D and dq work.
 struct FwdSweepBars {
-    uint64_t full_qv, empty_qv, full_kp, empty_kp;
+    uint64_t full_qv, empty_qv, full_k, empty_k;
     uint64_t qk_ready, sb_ready, a_ready, p_ready, d_ready;
     uint64_t qk_done, o_done, pv_done, dq_done;
     uint64_t final_mma;
@@ -130,27 +131,27 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
 
     if (warp == 0) {
         if (lane == 0) {
-            int armed_qv = -1, armed_kp = -1;
+            int armed_qv = -1, armed_k = -1;
             for (int i = 0; i < nloc; ++i) {
                 const int t0 = (cbeg + i) * kC;
                 if (!mbar_wait(&bar->empty_qv, (i & 1) ^ 1, err, LA_ERR_TIMEOUT)) break;
-                mbar_arrive_expect_tx(&bar->full_qv, 2 * kTileBytes);
+                mbar_arrive_expect_tx(&bar->full_qv, 3 * kTileBytes);
                 tma_load_3d(sQ, &tm_q, 0, t0, bh, &bar->full_qv);
                 tma_load_3d(sQ + kBlockBytes, &tm_q, 64, t0, bh, &bar->full_qv);
                 tma_load_3d(sV, &tm_v, 0, t0, bh, &bar->full_qv);
                 tma_load_3d(sV + kBlockBytes, &tm_v, 64, t0, bh, &bar->full_qv);
+                tma_load_3d(sP, &tm_do, 0, t0, bh, &bar->full_qv);
+                tma_load_3d(sP + kBlockBytes, &tm_do, 64, t0, bh, &bar->full_qv);
                 armed_qv = i;
-                if (!mbar_wait(&bar->empty_kp, (i & 1) ^ 1, err, LA_ERR_TIMEOUT)) break;
-                mbar_arrive_expect_tx(&bar->full_kp, 2 * kTileBytes);
-                tma_load_3d(sK, &tm_k, 0, t0, bh, &bar->full_kp);
-                tma_load_3d(sK + kBlockBytes, &tm_k, 64, t0, bh, &bar->full_kp);
-                tma_load_3d(sP, &tm_do, 0, t0, bh, &bar->full_kp);
-                tma_load_3d(sP + kBlockBytes, &tm_do, 64, t0, bh, &bar->full_kp);
-                armed_kp = i;
+                if (!mbar_wait(&bar->empty_k, (i & 1) ^ 1, err, LA_ERR_TIMEOUT)) break;
+                mbar_arrive_expect_tx(&bar->full_k, kTileBytes);
+                tma_load_3d(sK, &tm_k, 0, t0, bh, &bar->full_k);
+                tma_load_3d(sK + kBlockBytes, &tm_k, 64, t0, bh, &bar->full_k);
+                armed_k = i;
             }
             // no copy may still be landing when the CTA exits
             if (armed_qv >= 0) mbar_wait(&bar->full_qv, armed_qv & 1, err, LA_ERR_TIMEOUT);
-            if (armed_kp >= 0) mbar_wait(&bar->full_kp, armed_kp & 1, err, LA_ERR_TIMEOUT);
+            if (armed_k >= 0) mbar_wait(&bar->full_k, armed_k & 1, err, LA_ERR_TIMEOUT);
         }
     } else if (warp == 1) {
         if (lane == 0) {
@@ -193,7 +194,7 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)  // R += Q~^T P
                     mma_ss(tmem + kFR, desc_mnmajor(aQ, kk), desc_mnmajor(aP, kk), id_mnmn, (i > 0 || kk > 0));
-                mma_commit(&bar->empty_qv);  // last MMA read of Q and V in this chunk
+                mma_commit(&bar->empty_qv);  // last MMA read of Q, V and P in this chunk
                 if (!mbar_wait(&bar->d_ready, ph, err, LA_ERR_TIMEOUT)) break;
                 tc_fence_after();
 #pragma unroll
@@ -203,7 +204,7 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
                     mma_ts(tmem + kFY, tmem + kFX + xcol(kk), desc_mnmajor(aKLo, kk), id_kmn, 1);
                 }
                 mma_commit(&bar->dq_done);
-                mma_commit(&bar->empty_kp);  // last read of K, K_lo and P
+                mma_commit(&bar->empty_k);  // last read of K and K_lo
             }
             mma_commit(&bar->final_mma);
             mbar_wait(&bar->final_mma, 0, err, LA_ERR_TIMEOUT);
@@ -238,8 +239,14 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
             fence_proxy_async_smem();
             FG::sync();
             if (ct == 0) mbar_arrive(&bar->sb_ready);
-            // phi(q_r) on this thread's 64 columns stays in registers for phi'(q) in the dq
-            // epilogue (Q is released before it); phi(q_r) . z_prev
+            // (b) phi on K: hi in place, lo beside it, per-warp column sums of hi into zpart
+            if (!FG::all(mbar_wait(&bar->full_k, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
+            FG::phi_tile(sK, sKLo, ct, n, D, nullptr, zpart);
+            fence_proxy_async_smem();
+            FG::sync();
+            if (ct == 0) mbar_arrive(&bar->qk_ready);
+            // while Q K^T is formed: phi(q_r) on this thread's 64 columns stays in registers for
+            // phi'(q) in the dq epilogue (Q is released before it); phi(q_r) . z_prev
             uint32_t qrow[32];
             {
                 float di = 0.f;
@@ -258,12 +265,6 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
                 }
                 dpart[128 * h + r] = di;
             }
-            // (b) phi on K: hi in place, lo beside it, per-warp column sums of hi into zpart
-            if (!FG::all(mbar_wait(&bar->full_kp, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
-            FG::phi_tile(sK, sKLo, ct, n, D, nullptr, zpart);
-            fence_proxy_async_smem();
-            FG::sync();
-            if (ct == 0) mbar_arrive(&bar->qk_ready);
             // (c) A = tril(QK^T) on this thread's keys [64h, 64h+64), in place (see the X layout)
             if (!FG::all(mbar_wait(&bar->qk_done, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
             tc_fence_after();
@@ -304,11 +305,22 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
             tc_fence_before();
             FG::sync();
             if (ct == 0) mbar_arrive(&bar->a_ready);
-            // (d) den; P = dO / den (in place, bf16); g = -P . num / den from that bf16 P
-            if (!FG::all(mbar_wait(&bar->o_done, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
-            tc_fence_after();
+            // (d) den (the row sums of A and phi(q) . z_prev are in); P = dO / den in place (bf16)
+            // on this thread's 64 columns while A V is formed; then g = -P . num / den from
+            // that bf16 P
             const float den = valid ? rpart[r] + rpart[128 + r] + dpart[r] + dpart[128 + r] : 1.f;
             const float inv = 1.f / den;
+#pragma unroll
+            for (int c8 = 0; c8 < 8; ++c8) {
+                uint4* pp = reinterpret_cast<uint4*>(sP + chunk_off(r, 8 * h + c8));
+                uint4 v4 = *pp;
+                uint32_t* u = reinterpret_cast<uint32_t*>(&v4);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) u[e] = pack_bf16x2(bf_lo(u[e]) * inv, bf_hi(u[e]) * inv);
+                *pp = v4;
+            }
+            if (!FG::all(mbar_wait(&bar->o_done, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
+            tc_fence_after();
             {
                 float dot = 0.f;
 #pragma unroll
@@ -318,16 +330,12 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
                     tmem_ld_wait();
 #pragma unroll
                     for (int c4 = 0; c4 < 4; ++c4) {
-                        uint4* pp = reinterpret_cast<uint4*>(sP + chunk_off(r, 8 * h + 4 * cb + c4));
-                        uint4 v4 = *pp;
-                        uint32_t* u = reinterpret_cast<uint32_t*>(&v4);
+                        const uint4 v4 = *reinterpret_cast<const uint4*>(sP + chunk_off(r, 8 * h + 4 * cb + c4));
+                        const uint32_t* u = reinterpret_cast<const uint32_t*>(&v4);
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            u[e] = pack_bf16x2(bf_lo(u[e]) * inv, bf_hi(u[e]) * inv);
+                        for (int e = 0; e < 4; ++e)
                             dot += bf_lo(u[e]) * __uint_as_float(w[8 * c4 + 2 * e]) +
                                    bf_hi(u[e]) * __uint_as_float(w[8 * c4 + 2 * e + 1]);
-                        }
-                        *pp = v4;
                     }
                 }
                 tpart[128 * h + r] = dot;
