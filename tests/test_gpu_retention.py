@@ -107,6 +107,21 @@ def test_retention_tensor_core_cases(la, B, H, N, Dk, Dv):
         check("retention S (tensor cores)", S, Sref, 1e-2)
 
 
+@pytest.mark.parametrize("Dk,dtype", [(32, torch.float32), (64, torch.bfloat16), (128, torch.bfloat16)])
+def test_decay_outside_unit_interval(la, Dk, dtype):
+    """Any real gamma is computed as written: negative decays alternate the signs of older
+    terms (the powers come from repeated squaring, not a logarithm), and a decay above 1
+    grows them (here 1.01^300, about 20)."""
+    q, k, v = W.random_case(2300 + Dk, 1, 3, 300, Dk, Dk, dtype=dtype, scale=Dk ** -0.25)
+    g = torch.tensor([-0.5, 1.01, -1.0])
+    o, S = la.retention_fwd(q.to(DEV), k.to(DEV), v.to(DEV), g.to(DEV), return_state=True)
+    check("o", o, oracle.retention_direct(q, k, v, g), tol_for(dtype))
+    Sref = np.zeros((1, 3, Dk, Dk))
+    for t in range(300):
+        _, Sref = oracle.retention_step(q[:, :, t], k[:, :, t], v[:, :, t], g, Sref)
+    check("S", S, Sref, 1e-4 if dtype == torch.float32 else 1e-2)
+
+
 def test_gamma_one_is_the_masked_product(la):
     """gamma = 1: o = tril(Q K^T) V, checked against a float64 matrix product."""
     q, k, v = W.random_case(31, 1, 2, 300, 64, 32, dtype=torch.float32, scale=64 ** -0.25)
