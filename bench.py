@@ -194,6 +194,7 @@ def run_ours(args):
     # the decode step first, on a fresh device allocator (it is independent of the main
     # workload, whose 8 GB of buffers would otherwise shape where its small buffers land)
     decode = bench_decode(la, dev, peaks()[0]) if (rank == 0 and not args.skip_extras) else None
+    ret_step = bench_retention_step(la, dev) if (rank == 0 and not args.skip_extras) else None
 
     w = W.LONG_BF16
     if args.workload == "profile":
@@ -319,6 +320,7 @@ def run_ours(args):
         result["decode"] = decode
         result["noncausal"] = bench_noncausal(la, dev)
         result["retention"] = bench_retention(la, dev)
+        result["retention"]["step"] = ret_step
     if rank == 0 and not args.skip_cpu:
         result["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     assert la.last_error() == 0
@@ -413,8 +415,42 @@ def bench_noncausal(la, dev):
     return res
 
 
+def bench_retention_step(la, dev):
+    """Retention decode, S <- gamma S + k v^T and out = S^T q, at the decode shape: a CUDA
+    graph of single-step launches replayed as for the causal decode step."""
+    wd = W.DECODE_CIFAR
+    T = wd.steps
+    qd, kd, vd = (t.to(dev) for t in W.make_decode_inputs(wd))
+    gd = W.retention_gammas(wd.H).to(dev)
+    S = torch.zeros(wd.B, wd.H, wd.Dk, wd.Dv, device=dev)
+    outs = torch.empty(T, wd.B, wd.H, wd.Dv, device=dev)
+    s = torch.cuda.Stream(dev)
+    s.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(s):
+        for t in range(3):
+            la.retention_step(qd[t], kd[t], vd[t], gd, S, out=outs[t])
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for t in range(T):
+            la.retention_step(qd[t], kd[t], vd[t], gd, S, out=outs[t])
+    g.replay()
+    torch.cuda.synchronize()
+    reps = 5
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    us_step = e0.elapsed_time(e1) * 1e3 / (reps * T)
+    return {"us_per_step": us_step, "steps_per_s": 1e6 / us_step,
+            "workload": "retention decode f32 B=%d H=%d Dk=Dv=%d, CUDA graph of %d single-step launches" %
+            (wd.B, wd.H, wd.Dk, T)}
+
+
 def bench_retention(la, dev):
-    """Retention (constant decay per head) forward at the long-context shape, and its decode step."""
+    """Retention (constant decay per head) forward at the long-context shape."""
     w = W.RETENTION_BF16
     q, k, v = (t.to(dev) for t in W.make_inputs(w))  # 805 MB of inputs: larger than L2
     gam = W.retention_gammas(w.H).to(dev)
@@ -439,25 +475,6 @@ def bench_retention(la, dev):
     res = {"fwd": {"ms": ms, "tokens_per_s": w.B * w.N / (ms / 1e3), "workload": w.name,
                    "kernel_ms": kern, "l2": "inputs larger than L2"}}
     del q, k, v, o, ws
-    # decode: S <- gamma S + k v^T, out = S^T q at the decode shape, eager launches
-    wd = W.DECODE_CIFAR
-    T = 200
-    qd, kd, vd = (t.to(dev) for t in W.make_decode_inputs(wd, steps=T))
-    gd = W.retention_gammas(wd.H).to(dev)
-    S = torch.zeros(wd.B, wd.H, wd.Dk, wd.Dv, device=dev)
-    outs = torch.empty(T, wd.B, wd.H, wd.Dv, device=dev)
-    for t in range(3):
-        la.retention_step(qd[t], kd[t], vd[t], gd, S, out=outs[t])
-    torch.cuda.synchronize()
-    la.timing_reset()
-    la.timing_enable(True)
-    for t in range(T):
-        la.retention_step(qd[t], kd[t], vd[t], gd, S, out=outs[t])
-    torch.cuda.synchronize()
-    la.timing_enable(False)
-    n_l, ms_l = la.timing_read()["retention_step"]
-    res["step"] = {"kernel_us": ms_l * 1e3 / n_l, "workload": "retention decode f32 B=%d H=%d Dk=Dv=%d" %
-                   (wd.B, wd.H, wd.Dk)}
     return res
 
 

@@ -242,7 +242,7 @@ def host_step_bytes(B: int, H: int, N: int, Dk: int, Dv: int, dtype: torch.dtype
     return int(library().la_host_step_bytes(Shape(B, H, N, Dk, Dv, code), group_heads))
 
 
-def causal_step_host(q, k, v, dout, o, dq, dk, dv, group_heads=4, dev_buf=None, stream=None):
+def causal_step_host(q, k, v, dout, o, dq, dk, dv, group_heads=2, dev_buf=None, stream=None):
     """One causal forward + backward on pinned host tensors (la_causal_step_host).
 
     q, k, v, dout are read and o, dq, dk, dv written, all pinned CPU tensors of

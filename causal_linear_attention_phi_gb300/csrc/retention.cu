@@ -318,6 +318,123 @@ retention_step_kernel(const T* __restrict__ q, const T* __restrict__ k, const T*
     }
 }
 
+// Four consecutive elements as one vector access (16 bytes of fp32, 8 of bf16).
+__device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ float4 ld4(const __nv_bfloat16* p) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(p);
+    const float2 a = __bfloat1622float2(h[0]), b = __bfloat1622float2(h[1]);
+    return make_float4(a.x, a.y, b.x, b.y);
+}
+__device__ __forceinline__ void st4(float* p, float4 x) { *reinterpret_cast<float4*>(p) = x; }
+__device__ __forceinline__ void st4(__nv_bfloat16* p, float4 x) {
+    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(p);
+    h[0] = __floats2bfloat162_rn(x.x, x.y);
+    h[1] = __floats2bfloat162_rn(x.z, x.w);
+}
+
+// Heads with Dk, Dv <= 64: one warp per head with S held in registers as float4s
+// (COLS = Dv/4 lanes across a row, RPI = 32/COLS rows per instruction, ROWS = Dk/RPI
+// rows per lane), every global load of the step issued before any arithmetic (one
+// memory round trip), q and k read once per element (lane d % 32) and handed to the
+// lanes of row d by a shuffle.  Launched with programmatic stream serialization: the
+// grid may be scheduled while the previous kernel in the stream drains and waits
+// (griddepcontrol.wait) before its first global access, so the order memory sees is
+// the stream's.
+template <typename T, int DK, int DV>
+__global__ void __launch_bounds__(32 * kStepWarps)
+retention_step_small_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
+                            const float* __restrict__ gamma, float* __restrict__ S, T* __restrict__ out, int BH,
+                            int H) {
+    constexpr int COLS = DV / 4;
+    constexpr int RPI = 32 / COLS;
+    constexpr int ROWS = DK / RPI;
+    constexpr int QPL = (DK + 31) / 32;  // q, k entries per lane
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int h = blockIdx.x * kStepWarps + warp;
+    if (h >= BH) return;
+    const int c4 = lane % COLS, rsub = lane / COLS;
+    const int col = c4 * 4;
+    float* Sh = S + (size_t)h * DK * DV;
+    float4 st[ROWS];
+#pragma unroll
+    for (int x = 0; x < ROWS; ++x)
+        st[x] = *reinterpret_cast<const float4*>(Sh + (size_t)(rsub + RPI * x) * DV + col);
+    const float4 vv = ld4(v + (size_t)h * DV + col);
+    float qa[QPL], ka[QPL];
+#pragma unroll
+    for (int y = 0; y < QPL; ++y) {
+        const int d = lane + 32 * y;
+        qa[y] = d < DK ? to_f32(q[(size_t)h * DK + d]) : 0.f;
+        ka[y] = d < DK ? to_f32(k[(size_t)h * DK + d]) : 0.f;
+    }
+    const float g = gamma[h % H];
+    float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int x = 0; x < ROWS; ++x) {
+        const int d = rsub + RPI * x;
+        float kd = __shfl_sync(0xffffffffu, ka[0], d & 31), qd = __shfl_sync(0xffffffffu, qa[0], d & 31);
+        if (QPL > 1) {
+            const float k1 = __shfl_sync(0xffffffffu, ka[QPL - 1], d & 31);
+            const float q1 = __shfl_sync(0xffffffffu, qa[QPL - 1], d & 31);
+            if (d >= 32) {
+                kd = k1;
+                qd = q1;
+            }
+        }
+        float4 t = st[x];
+        t.x = fmaf(kd, vv.x, g * t.x);
+        t.y = fmaf(kd, vv.y, g * t.y);
+        t.z = fmaf(kd, vv.z, g * t.z);
+        t.w = fmaf(kd, vv.w, g * t.w);
+        *reinterpret_cast<float4*>(Sh + (size_t)d * DV + col) = t;
+        num.x = fmaf(qd, t.x, num.x);
+        num.y = fmaf(qd, t.y, num.y);
+        num.z = fmaf(qd, t.z, num.z);
+        num.w = fmaf(qd, t.w, num.w);
+    }
+#pragma unroll
+    for (int o = COLS; o < 32; o <<= 1) {
+        num.x += __shfl_xor_sync(0xffffffffu, num.x, o);
+        num.y += __shfl_xor_sync(0xffffffffu, num.y, o);
+        num.z += __shfl_xor_sync(0xffffffffu, num.z, o);
+        num.w += __shfl_xor_sync(0xffffffffu, num.w, o);
+    }
+    if (rsub == 0) st4(out + (size_t)h * DV + col, num);
+}
+
+template <typename T, int DK, int DV>
+cudaError_t launch_step_small(const void* q, const void* k, const void* v, const float* gamma, float* S, void* out,
+                              int BH, int H, cudaStream_t st) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((BH + kStepWarps - 1) / kStepWarps));
+    cfg.blockDim = dim3(32 * kStepWarps);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, retention_step_small_kernel<T, DK, DV>, (const T*)q, (const T*)k, (const T*)v,
+                              gamma, S, (T*)out, BH, H);
+}
+
+// The small-head fast path for (Dk, Dv) in {16, 32, 64}^2; *handled = false otherwise.
+template <typename T>
+cudaError_t step_small(const void* q, const void* k, const void* v, const float* gamma, float* S, void* out, int BH,
+                       int H, int Dk, int Dv, cudaStream_t st, bool* handled) {
+    *handled = true;
+#define LA_RET_SMALL(a, b) \
+    if (Dk == a && Dv == b) return launch_step_small<T, a, b>(q, k, v, gamma, S, out, BH, H, st);
+    LA_RET_SMALL(16, 16) LA_RET_SMALL(16, 32) LA_RET_SMALL(16, 64) LA_RET_SMALL(32, 16) LA_RET_SMALL(32, 32)
+    LA_RET_SMALL(32, 64) LA_RET_SMALL(64, 16) LA_RET_SMALL(64, 32) LA_RET_SMALL(64, 64)
+#undef LA_RET_SMALL
+    *handled = false;
+    return cudaSuccess;
+}
+
 size_t smem_bytes_sums(int Dk, int Dv) {
     return smem_floats((size_t)kC * (Dk + 1)) + smem_floats((size_t)kC * (Dv + 1)) + smem_floats(kC + 1);
 }
@@ -386,6 +503,14 @@ cudaError_t retention_step(const void* q, const void* k, const void* v, const fl
     const int BH = s.B * s.H;
     const unsigned blocks = (unsigned)((BH + kStepWarps - 1) / kStepWarps);
     launch_begin("retention_step", st);
+    bool handled = false;
+    cudaError_t e = s.dtype == LA_BF16
+                        ? step_small<__nv_bfloat16>(q, k, v, gamma, S, out, BH, s.H, s.Dk, s.Dv, st, &handled)
+                        : step_small<float>(q, k, v, gamma, S, out, BH, s.H, s.Dk, s.Dv, st, &handled);
+    if (handled) {
+        const cudaError_t e2 = launch_end("retention_step", st);
+        return e != cudaSuccess ? e : e2;
+    }
     if (s.dtype == LA_BF16)
         retention_step_kernel<__nv_bfloat16><<<blocks, 32 * kStepWarps, 0, st>>>(
             (const __nv_bfloat16*)q, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, gamma, S,
