@@ -106,7 +106,7 @@ retention_sums_kernel(const T* __restrict__ k, const T* __restrict__ v, const fl
 // tensor-core path).  With S_out, R_P (the state after position N) is written
 // to S_out[bh] as Dk x Dv.  Each thread owns four consecutive elements of every
 // record (E = sk * sv).
-constexpr int kScanBatch = 8;
+constexpr int kScanBatch = 24;  // covers the segment counts the planner picks for the long workloads (19)
 
 __global__ void retention_scan_kernel(float* __restrict__ seg, float* __restrict__ S_out,
                                       const float* __restrict__ gamma, int H, int N, int P, int seg_len, size_t E,

@@ -82,7 +82,7 @@ segment_sums_kernel(const T* __restrict__ k, const T* __restrict__ v, float* __r
 // consecutive elements (one float4, inside one row) of every segment record and
 // walks the P records in batches whose loads are all issued before any of them
 // is used.
-constexpr int kScanBatch = 8;
+constexpr int kScanBatch = 24;  // covers the segment counts the planner picks for the long workloads (19)
 
 __global__ void scan_kernel(float* __restrict__ seg, float* __restrict__ totS, float* __restrict__ totz, size_t sS,
                             size_t sz, int P, size_t E, int sk, int sv, int Dk, int Dv, int mode) {
