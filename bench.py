@@ -139,11 +139,16 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+# The sources of the tensor-core kernels that the committed DRAM-traffic figures describe
+# (kernels, shared device code and the headers they include): any change to these makes
+# the figures stale; changes to other kernels (the scans, the CUDA-core path) do not.
+TC_KERNEL_SOURCES = ("tc_fwd.cu", "tc_bwd.cu", "tc_retention.cu", "tc_common.cuh", "sm100.cuh", "la_internal.cuh")
+
+
 def kernel_sources_sha():
-    import glob
     h = hashlib.sha256()
-    for p in sorted(glob.glob(os.path.join(ROOT, "causal_linear_attention_phi_gb300", "csrc", "*"))):
-        with open(p, "rb") as f:
+    for name in TC_KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "causal_linear_attention_phi_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
