@@ -84,6 +84,35 @@ def test_host_side_rejections(la):
     assert b"head sizes" in lib.la_error_detail() or True
 
 
+def test_retention_host_side_rejections(la):
+    # shape checks come before any device call, so these run without a GPU
+    lib = la.library()
+    p = ctypes.c_void_p(0)
+
+    def fwd(shape):
+        return lib.la_retention_fwd(p, p, p, p, p, p, la.Shape(*shape), p, 0, None)
+
+    def step(shape):
+        return lib.la_retention_step(p, p, p, p, p, p, la.Shape(*shape), None)
+
+    assert fwd((-1, 1, 8, 16, 16, 0)) == 1      # negative size
+    assert fwd((1, 1, 8, 16, 16, 9)) == 1       # bad dtype
+    assert fwd((1, 1, 8, 48, 16, 0)) == 2       # head size not in {16, 32, 64, 128}
+    assert fwd((0, 4, 8, 16, 16, 1)) == 0       # no heads: a no-op
+    assert step((1, 1, 1, 16, 256, 0)) == 2
+    assert step((0, 2, 1, 16, 16, 0)) == 0
+    assert step((-2, 2, 1, 16, 16, 0)) == 1
+
+
+def test_retention_workspace_is_pure(la):
+    import torch
+    a = la.workspace_bytes(la.OP_RETENTION_FWD, 2, 16, 65536, 128, 128, torch.bfloat16)
+    assert a > 0 and a == la.workspace_bytes(la.OP_RETENTION_FWD, 2, 16, 65536, 128, 128, torch.bfloat16)
+    assert la.workspace_bytes(la.OP_RETENTION_FWD, 2, 16, 0, 128, 128, torch.bfloat16) == 0
+    # same planner as the causal forward, records of S only (no z): strictly smaller
+    assert a < la.workspace_bytes(la.OP_CAUSAL_FWD, 2, 16, 65536, 128, 128, torch.bfloat16)
+
+
 def test_product_path_fails_loudly_without_library(tmp_path):
     import causal_linear_attention_phi_gb300 as la
     saved = la._lib
