@@ -86,6 +86,7 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
                             float* __restrict__ seg_R, float* __restrict__ den_g, int N, int nchunks, int cps, int P,
                             int* err) {
     extern __shared__ uint8_t smem_raw[];
+    constexpr int kKd = D / 16;  // K steps of a product over a head dimension (a 64-wide head is zero above)
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sQ = base + FwdSweepSmem::Q;
     uint8_t* sK = base + FwdSweepSmem::K;
@@ -165,12 +166,12 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
                 if (!mbar_wait(&bar->sb_ready, ph, err, LA_ERR_TIMEOUT)) break;
                 tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)  // Y = Q~ S_prev (needs phi(Q) and S_prev only)
+                for (int kk = 0; kk < kKd; ++kk)  // Y = Q~ S_prev (needs phi(Q) and S_prev only)
                     mma_ss(tmem + kFY, desc_kmajor(aQ, kk), desc_mnmajor(aSb, kk), id_kmn, kk > 0);
                 if (!mbar_wait(&bar->qk_ready, ph, err, LA_ERR_TIMEOUT)) break;
                 tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)  // X = Q~ K~^T
+                for (int kk = 0; kk < kKd; ++kk)  // X = Q~ K~^T
                     mma_ss(tmem + kFX, desc_kmajor(aQ, kk), desc_kmajor(aK, kk), id_kk, kk > 0);
                 mma_commit(&bar->qk_done);
                 if (!mbar_wait(&bar->a_ready, ph, err, LA_ERR_TIMEOUT)) break;
@@ -185,11 +186,11 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
                 if (!mbar_wait(&bar->p_ready, ph, err, LA_ERR_TIMEOUT)) break;
                 tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)  // X = P V^T
+                for (int kk = 0; kk < kKd; ++kk)  // X = P V^T
                     mma_ss(tmem + kFX, desc_kmajor(aP, kk), desc_kmajor(aV, kk), id_kk, kk > 0);
                 mma_commit(&bar->pv_done);
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)  // Y = P S_prev^T (Y is free: O was read before p_ready)
+                for (int kk = 0; kk < kKd; ++kk)  // Y = P S_prev^T (Y is free: O was read before p_ready)
                     mma_ss(tmem + kFY, desc_kmajor(aP, kk), desc_kmajor(aSb, kk), id_kk, kk > 0);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)  // R += Q~^T P
@@ -219,6 +220,11 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
         if (ct < 128) {
             zsh[ct] = pre[(size_t)kD * kD + ct];
             racc[ct] = 0.f;
+        }
+        if (D <= 64) {  // phi leaves the lo tile's upper column block unwritten: keep it zero
+            for (int x = ct; x < kBlockBytes / 16; x += 256)
+                reinterpret_cast<uint4*>(sKLo + kBlockBytes)[x] = make_uint4(0u, 0u, 0u, 0u);
+            fence_proxy_async_smem();
         }
         tc_fence_before();
         bool ok = FG::all(true);
@@ -507,6 +513,7 @@ tc_bwd_reverse_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
                             const float* __restrict__ seg_R, const float* __restrict__ den_g, int N, int nchunks,
                             int cps, int P, int* err) {
     extern __shared__ uint8_t smem_raw[];
+    constexpr int kKd = D / 16;  // K steps of a product over a head dimension (a 64-wide head is zero above)
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sQ = base + RevSweepSmem::Q;
     uint8_t* sK = base + RevSweepSmem::K;
@@ -577,10 +584,10 @@ tc_bwd_reverse_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
                 if (!mbar_wait(&bar->ready, ph, err, LA_ERR_TIMEOUT)) break;
                 tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)  // DV region = A'^T = K~ Q'^T (rows = keys)
+                for (int kk = 0; kk < kKd; ++kk)  // DV region = A'^T = K~ Q'^T (rows = keys)
                     mma_ss(tmem + kRDV, desc_kmajor(aK, kk), desc_kmajor(aQ, kk), id_kk, kk > 0);
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)  // DK region = V dO^T (rows = keys)
+                for (int kk = 0; kk < kKd; ++kk)  // DK region = V dO^T (rows = keys)
                     mma_ss(tmem + kRDK, desc_kmajor(aV, kk), desc_kmajor(aP, kk), id_kk, kk > 0);
                 mma_commit(&bar->at_dt_done);
                 if (!mbar_wait(&bar->rb_ready, ph, err, LA_ERR_TIMEOUT)) break;
@@ -591,14 +598,14 @@ tc_bwd_reverse_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
                 if (!mbar_wait(&bar->masks_ready, ph, err, LA_ERR_TIMEOUT)) break;
                 tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)  // dK~ = V R_next^T
+                for (int kk = 0; kk < kKd; ++kk)  // dK~ = V R_next^T
                     mma_ss(tmem + kRDK, desc_kmajor(aV, kk), desc_kmajor(aRb, kk), id_kk, kk > 0);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)  // dK~ += D'^T Q'
                     mma_ts(tmem + kRDK, tmem + kRX + 8 * kk, desc_mnmajor(aQ, kk), id_kmn, 1);
                 mma_commit(&bar->dk_done);  // the dk epilogue runs during the dV products
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)  // dV = K~ R_next
+                for (int kk = 0; kk < kKd; ++kk)  // dV = K~ R_next
                     mma_ss(tmem + kRDV, desc_kmajor(aK, kk), desc_mnmajor(aRb, kk), id_kmn, kk > 0);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)  // dV += A'^T dO

@@ -172,13 +172,17 @@ struct Grp {
                                                     const float* w, float* colpart, uint8_t* copy_tile = nullptr,
                                                     const float* scale = nullptr) {
         // a whole tile (every row and column in range: all chunks but a short last one of a
-        // full-width head) takes the copy of the body without the per-element range test
+        // full-width head) takes the copy of the body without the per-element range test; a
+        // 64-wide head leaves the upper column block alone (its TMA zero fill stays in place,
+        // and the lo and copy tiles there feed only output columns that are never stored)
         if (n >= kC && dcols >= kD)
-            phi_tile_body<true>(tile, lo_tile, ct, n, dcols, w, colpart, copy_tile, scale);
+            phi_tile_body<true, false>(tile, lo_tile, ct, n, dcols, w, colpart, copy_tile, scale);
+        else if (dcols <= kD / 2)
+            phi_tile_body<false, true>(tile, lo_tile, ct, n, dcols, w, colpart, copy_tile, scale);
         else
-            phi_tile_body<false>(tile, lo_tile, ct, n, dcols, w, colpart, copy_tile, scale);
+            phi_tile_body<false, false>(tile, lo_tile, ct, n, dcols, w, colpart, copy_tile, scale);
     }
-    template <bool kWhole>
+    template <bool kWhole, bool kHalf>
     __device__ static __forceinline__ void phi_tile_body(uint8_t* tile, uint8_t* lo_tile, int ct, int n, int dcols,
                                                          const float* w, float* colpart, uint8_t* copy_tile,
                                                          const float* scale) {
@@ -189,14 +193,16 @@ struct Grp {
             for (int e = 0; e < 8; ++e) zp[b][e] = 0.f;
         uint4 v[kJ];
 #pragma unroll
-        for (int j = 0; j < kJ; ++j) v[j] = *reinterpret_cast<const uint4*>(tile + vec_off(ct, j));
+        for (int j = 0; j < kJ; ++j)
+            if (!kHalf || vec_block(j) == 0) v[j] = *reinterpret_cast<const uint4*>(tile + vec_off(ct, j));
 #pragma unroll
         for (int j = 0; j < kJ; ++j) {
+            if (kHalf && vec_block(j) != 0) continue;
             const int row = vec_row(ct, j);
             uint32_t* u = reinterpret_cast<uint32_t*>(&v[j]);
             uint4 l;
             uint32_t* ul = reinterpret_cast<uint32_t*>(&l);
-            const bool valid = kWhole || (row < n && 64 * vec_block(j) + 8 * vec_lc(ct) < dcols);
+            const bool valid = kWhole || (row < n && (kHalf || 64 * vec_block(j) + 8 * vec_lc(ct) < dcols));
             const float wr = (w && valid) ? w[row] : 1.f;
             const float sr = scale ? scale[row] : 1.f;
 #pragma unroll

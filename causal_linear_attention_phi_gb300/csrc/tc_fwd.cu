@@ -82,6 +82,7 @@ tc_causal_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                      float* __restrict__ seg, int N, int nchunks, int cps, int P, int* err) {
     extern __shared__ uint8_t smem_raw[];
+    constexpr int kKd = D / 16;  // K steps of a product over a head dimension (a 64-wide head is zero above)
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sQ = base + SmemLayout::Q;
     uint8_t* sSb = base + SmemLayout::Sb;
@@ -177,13 +178,13 @@ tc_causal_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                 tc_fence_after();
                 if (kOut) {
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)  // QK = Q~ K~^T
+                    for (int kk = 0; kk < kKd; ++kk)  // QK = Q~ K~^T
                         mma_ss(tmem + kTmQK, desc_kmajor(aQ, kk), desc_kmajor(aK, kk), id_kk, kk > 0);
                     mma_commit(&bar->qk_done);
                     if (!(ok = mbar_wait(&bar->sb_ready, i & 1, err, LA_ERR_TIMEOUT))) break;
                     tc_fence_after();
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {  // O = Q~ S_prev, den = Q~ z_prev
+                    for (int kk = 0; kk < kKd; ++kk) {  // O = Q~ S_prev, den = Q~ z_prev
                         mma_ss(tmem + kTmO, desc_kmajor(aQ, kk), desc_mnmajor(aSb, kk), id_kmn, kk > 0);
                         mma_ss(tmem + kTmDen, desc_kmajor(aQ, kk), desc_small(aZb, kk), id_k16, kk > 0);
                     }
