@@ -19,7 +19,7 @@ from . import build as _build
 
 __all__ = [
     "LaError", "noncausal_fwd", "noncausal_bwd", "causal_fwd", "causal_bwd", "causal_step_host", "host_step_bytes",
-    "recurrent_step", "retention_fwd", "retention_step", "workspace_bytes",
+    "recurrent_step", "retention_fwd", "retention_step", "selftest_bounded_wait", "workspace_bytes",
     "last_error", "clear_error", "timing_enable", "timing_reset", "timing_read", "library", "version",
     "OP_NONCAUSAL_FWD", "OP_CAUSAL_FWD", "OP_CAUSAL_BWD", "OP_NONCAUSAL_BWD", "OP_RETENTION_FWD",
 ]
@@ -66,6 +66,7 @@ def _declare(lib):
     lib.la_recurrent_step.argtypes = [_vp] * 6 + [Shape, _vp]
     lib.la_retention_fwd.argtypes = [_vp] * 6 + [Shape, _vp, ctypes.c_size_t, _vp]
     lib.la_retention_step.argtypes = [_vp] * 6 + [Shape, _vp]
+    lib.la_selftest_bounded_wait.argtypes = [_vp]
     for f in ("la_causal_step_host", "la_noncausal_fwd", "la_noncausal_bwd", "la_causal_fwd", "la_causal_fwd_with_state", "la_causal_bwd", "la_causal_bwd_after_fwd",
               "la_recurrent_step",
               "la_last_error",
@@ -329,6 +330,12 @@ def retention_step(q, k, v, gamma, S, out=None, stream=None):
     _check(library().la_retention_step(_ptr(q), _ptr(k), _ptr(v), _ptr(gamma), _ptr(S), _ptr(out), s,
                                        _stream_ptr(stream)), "la_retention_step")
     return out
+
+
+def selftest_bounded_wait(stream=None):
+    """Launch the bounded-wait self-test (a wait that runs out after about a second and
+    records LA_ERR_TIMEOUT in the sticky status word); read it with last_error()."""
+    _check(library().la_selftest_bounded_wait(_stream_ptr(stream)), "la_selftest_bounded_wait")
 
 
 def last_error() -> int:

@@ -276,6 +276,17 @@ la_status la_causal_fwd_noalloc(const void* q, const void* k, const void* v, voi
 la_status la_last_error(void);
 la_status la_clear_error(void);
 
+/*
+ * Self-test of the device-side failure detection, with no fault: launches one
+ * thread that waits on an mbarrier phase nothing completes.  Like every wait in
+ * the library's kernels, the wait is bounded (about one second of SM clock);
+ * it gives up, records LA_ERR_TIMEOUT in the sticky status word and the kernel
+ * ends normally.  After the stream has been synchronised, la_last_error()
+ * returns LA_ERR_TIMEOUT (unless an earlier error is already recorded); clear it
+ * with la_clear_error().  The device and context stay usable.
+ */
+la_status la_selftest_bounded_wait(la_stream_t stream);
+
 /* Static description of a status code. */
 const char* la_status_string(la_status st);
 

@@ -71,3 +71,18 @@ def test_timing_hooks(la):
         la.timing_enable(False)
     assert any(n.startswith("simt_causal_fwd") or n.startswith("tc_") for n in t)
     assert all(v[0] >= 1 and v[1] >= 0 for v in t.values())
+
+
+def test_bounded_wait_times_out_and_the_context_stays_usable(la):
+    """A device wait on a barrier that nothing completes gives up after its limit (about a
+    second), records LA_ERR_TIMEOUT in the sticky word and lets the kernel end; no fault."""
+    la.clear_error()
+    la.selftest_bounded_wait()
+    torch.cuda.synchronize()
+    assert la.last_error() == 5  # LA_ERR_TIMEOUT
+    la.clear_error()
+    assert la.last_error() == 0
+    q = torch.randn(1, 2, 200, 32, device=DEV)
+    o = la.causal_fwd(q, q, q)
+    torch.cuda.synchronize()
+    assert torch.isfinite(o).all() and la.last_error() == 0
