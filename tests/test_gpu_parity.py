@@ -376,3 +376,47 @@ def test_decode_head_sizes(la, Dk, Dv, dtype):
             for t in range(T)]
     o = torch.stack(outs, 2)
     check("decode", o, oracle.causal_recurrent(q, k, v), tol_for(dtype))
+
+
+# ---------------------------------------------------------------- maximum sizes
+SAMPLE_HEADS = [0, 1, 32767, 65534]
+
+
+@pytest.mark.parametrize("N,D,dtype", [(70, 16, torch.float32), (129, 64, torch.bfloat16)])
+def test_maximum_head_count(la, N, D, dtype):
+    """B*H = 65535 (the largest head count, one grid row per head): forward and backward
+    on the CUDA cores (fp32) and on the padded tensor-core path (bf16, D = 64); sampled
+    heads against the oracle."""
+    B = 65535
+    q, k, v, dO = W.random_case(4242 + N, B, 1, N, D, D, dtype=dtype, scale=D ** -0.5, with_grad=True)
+    qd, kd, vd, dOd = dev(q, k, v, dO)
+    o = la.causal_fwd(qd, kd, vd)
+    dq, dk, dv = la.causal_bwd(qd, kd, vd, dOd)
+    torch.cuda.synchronize()
+    idx = torch.tensor(SAMPLE_HEADS)
+    sq, sk, sv, sdo = (t[idx] for t in (q, k, v, dO))
+    tol = tol_for(dtype)
+    check("o", o.cpu()[idx], oracle.causal_recurrent(sq, sk, sv), tol)
+    ref = oracle.causal_bwd_recurrent(sq, sk, sv, sdo)
+    check_all([("dq", dq.cpu()[idx], ref[0]), ("dk", dk.cpu()[idx], ref[1]), ("dv", dv.cpu()[idx], ref[2])], tol)
+
+
+def test_maximum_head_count_decode(la):
+    B, Dk, Dv = 65535, 16, 32
+    q, k, v = W.random_case(4343, B, 1, 2, Dk, Dv)
+    S = torch.zeros(B, 1, Dk, Dv, device=DEV)
+    z = torch.zeros(B, 1, Dk, device=DEV)
+    for t in range(2):
+        out = la.recurrent_step(q[:, :, t].contiguous().to(DEV), k[:, :, t].contiguous().to(DEV),
+                                v[:, :, t].contiguous().to(DEV), S, z)
+    idx = torch.tensor(SAMPLE_HEADS)
+    ref = oracle.causal_recurrent(q[idx], k[idx], v[idx])[:, :, 1]
+    check("decode", out.cpu()[idx], ref, 1e-4)
+
+
+def test_long_single_head_bf16(la):
+    """One head of N = 2^19 positions (1216 segments of the tensor-core planner, a scan over
+    them, index arithmetic past 2^31 elements of work): the forward against the oracle."""
+    q, k, v = W.random_case(4444, 1, 1, 1 << 19, 64, 64, dtype=torch.bfloat16, scale=64 ** -0.5)
+    o = la.causal_fwd(*dev(q, k, v))
+    check("o", o, oracle.causal_recurrent(q, k, v), 2e-2)
