@@ -137,7 +137,7 @@ static constexpr int kMaxWaves = 8;
 
 // bf16 heads with Dk = Dv = 128, or 64 (padded to 128 on chip: the tile loads
 // zero-fill the upper columns, phi keeps them zero and their stores are skipped).
-// For the non-causal forward only its segment sums run on the tensor cores.
+// The non-causal forward runs its segment sums and its apply on the tensor cores.
 bool tc_supported(const la_shape& s, int op) {
     return s.dtype == LA_BF16 && s.Dk == s.Dv && (s.Dk == 128 || s.Dk == 64) &&
            (op == LA_OP_CAUSAL_FWD || op == LA_OP_CAUSAL_BWD || op == LA_OP_NONCAUSAL_FWD ||
@@ -421,7 +421,10 @@ la_status la_noncausal_fwd(const void* q, const void* k, const void* v, void* o,
         LA_TRY(cuda_status(simt_segment_sums(k, v, seg, s, p, st), "noncausal segment sums"));
         LA_TRY(cuda_status(scan_segments(seg, tot, s, p, SCAN_TOTAL, st), "noncausal totals"));
     }
-    LA_TRY(cuda_status(simt_noncausal_apply(q, o, tot, s, st), "noncausal apply"));
+    if (p.tc)
+        LA_TRY(cuda_status(tc_noncausal_apply(q, o, tot, s, p, st), "noncausal apply"));
+    else
+        LA_TRY(cuda_status(simt_noncausal_apply(q, o, tot, s, st), "noncausal apply"));
     return LA_OK;
 }
 

@@ -128,6 +128,10 @@ cudaError_t tc_retention_fwd(const void* q, const void* k, const void* v, const 
                              const la_shape& s, const Plan& p, bool out_pass, cudaStream_t st);
 cudaError_t retention_step(const void* q, const void* k, const void* v, const float* gamma, float* S, void* out,
                            const la_shape& s, cudaStream_t st);
+// Tensor-core non-causal apply (bf16, Dk = Dv = 128 or 64): o from the head totals
+// [BH][Dk*Dv + Dk] (unpadded S then z), over the chunks of Plan p.
+cudaError_t tc_noncausal_apply(const void* q, void* o, const float* totals, const la_shape& s, const Plan& p,
+                               cudaStream_t st);
 bool tc_supported(const la_shape& s, int op);
 
 enum ScanMode { SCAN_EXCLUSIVE_PREFIX = 0, SCAN_EXCLUSIVE_SUFFIX = 1, SCAN_TOTAL = 2 };

@@ -420,3 +420,14 @@ def test_long_single_head_bf16(la):
     q, k, v = W.random_case(4444, 1, 1, 1 << 19, 64, 64, dtype=torch.bfloat16, scale=64 ** -0.5)
     o = la.causal_fwd(*dev(q, k, v))
     check("o", o, oracle.causal_recurrent(q, k, v), 2e-2)
+
+
+def test_noncausal_fwd_long_sampled_heads(la):
+    """The non-causal forward at B=2 H=16 N=65536 D=128 bf16 (segment sums and apply on the
+    tensor cores): two heads against the oracle's associative form."""
+    w = W.LONG_BF16
+    q, k, v = W.make_inputs(w)
+    o = la.noncausal_fwd(*dev(q, k, v)).cpu()
+    for b, h in [(0, 0), (1, 15)]:
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        check("head (%d,%d)" % (b, h), o[sl], oracle.noncausal_assoc(q[sl], k[sl], v[sl]), 2e-2)
