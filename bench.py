@@ -417,6 +417,27 @@ def bench_noncausal(la, dev):
             times.append(e0.elapsed_time(e1))
         ms = statistics.median(times)
         res[name] = {"ms": ms, "tokens_per_s": w.B * w.N / (ms / 1e3), "workload": w.name, "l2": "flushed"}
+    del q, k, v, o, ws, oc, wsc, dO, dq, dk, dv, wsb, flush
+    # the non-causal forward at the long-context shape (inputs larger than L2)
+    wl = W.LONG_BF16
+    q, k, v = (t.to(dev) for t in W.make_inputs(wl))
+    o = torch.empty_like(v)
+    ws = torch.empty(la.workspace_bytes(la.OP_NONCAUSAL_FWD, wl.B, wl.H, wl.N, wl.Dk, wl.Dv, wl.dtype),
+                     dtype=torch.uint8, device=dev)
+    for _ in range(3):
+        la.noncausal_fwd(q, k, v, out=o, workspace=ws)
+    times = []
+    for _ in range(10):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        la.noncausal_fwd(q, k, v, out=o, workspace=ws)
+        e1.record()
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    ms = statistics.median(times)
+    res["noncausal_fwd_long"] = {"ms": ms, "tokens_per_s": wl.B * wl.N / (ms / 1e3),
+                                 "workload": "noncausal fwd bf16 B=2 H=16 N=65536 Dk=Dv=128",
+                                 "l2": "inputs larger than L2"}
     return res
 
 
