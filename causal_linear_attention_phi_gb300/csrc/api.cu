@@ -137,11 +137,11 @@ static constexpr int kMaxWaves = 8;
 
 // bf16 heads with Dk = Dv = 128, or 64 (padded to 128 on chip: the tile loads
 // zero-fill the upper columns, phi keeps them zero and their stores are skipped).
-// The non-causal forward runs its segment sums and its apply on the tensor cores.
+// The non-causal forward and gradient run entirely on the tensor cores as well.
 bool tc_supported(const la_shape& s, int op) {
     return s.dtype == LA_BF16 && s.Dk == s.Dv && (s.Dk == 128 || s.Dk == 64) &&
            (op == LA_OP_CAUSAL_FWD || op == LA_OP_CAUSAL_BWD || op == LA_OP_NONCAUSAL_FWD ||
-            op == LA_OP_RETENTION_FWD);
+            op == LA_OP_NONCAUSAL_BWD || op == LA_OP_RETENTION_FWD);
 }
 
 static void finish_plan(Plan& p, int P) {
@@ -507,6 +507,16 @@ la_status la_noncausal_bwd(const void* q, const void* k, const void* v, const vo
     float* den_g = reinterpret_cast<float*>(base + w.den_g);
     float* totS = reinterpret_cast<float*>(base + w.totals);
     float* totR = reinterpret_cast<float*>(base + w.totals2);
+    if (p.tc) {  // padded (S, z) and (R, r) records throughout; phi(K) split hi + lo in the sums
+        LA_TRY(cuda_status(tc_causal_fwd(nullptr, k, v, nullptr, seg, s, p, false, st, true),
+                           "noncausal segment sums"));
+        LA_TRY(cuda_status(scan_segments(seg, totS, s, p, SCAN_TOTAL, st), "noncausal totals"));
+        LA_TRY(cuda_status(tc_noncausal_bwd_query(q, dout, dq, totS, segR, s, p, st),
+                           "noncausal backward, query pass"));
+        LA_TRY(cuda_status(scan_segments(segR, totR, s, p, SCAN_TOTAL, st), "noncausal reverse totals"));
+        LA_TRY(cuda_status(tc_noncausal_bwd_key(k, v, dk, dv, totR, s, p, st), "noncausal backward, key pass"));
+        return LA_OK;
+    }
     LA_TRY(cuda_status(simt_segment_sums(k, v, seg, s, p, st), "noncausal segment sums"));
     LA_TRY(cuda_status(scan_segments(seg, totS, s, p, SCAN_TOTAL, st), "noncausal totals"));
     LA_TRY(cuda_status(simt_bwd_forward_sweep(q, k, v, dout, dq, totS, segR, den_g, s, p, st, false),

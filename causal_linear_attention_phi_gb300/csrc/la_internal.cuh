@@ -106,8 +106,9 @@ cudaError_t recurrent_step(const void* q, const void* k, const void* v, float* S
 
 // Tensor-core (tcgen05) kernels: bf16, Dk = Dv = 128 (or 64, zero-padded to 128 on chip), C = 128.
 // out_pass = false: per-segment sums (S, z) into seg; true: outputs from the scanned prefixes.
+// split_k (sums only): phi(K) enters the sums as hi + lo bf16 parts (the non-causal gradient).
 cudaError_t tc_causal_fwd(const void* q, const void* k, const void* v, void* o, float* seg, const la_shape& s,
-                          const Plan& p, bool out_pass, cudaStream_t st);
+                          const Plan& p, bool out_pass, cudaStream_t st, bool split_k = false);
 cudaError_t tc_bwd_forward_sweep(const void* q, const void* k, const void* v, const void* dout, void* dq,
                                  const float* seg_S, float* seg_R, float* den_g, const la_shape& s, const Plan& p,
                                  cudaStream_t st);
@@ -132,6 +133,13 @@ cudaError_t retention_step(const void* q, const void* k, const void* v, const fl
 // [BH][Dk*Dv + Dk] (unpadded S then z), over the chunks of Plan p.
 cudaError_t tc_noncausal_apply(const void* q, void* o, const float* totals, const la_shape& s, const Plan& p,
                                cudaStream_t st);
+// Tensor-core non-causal gradient (bf16, Dk = Dv = 128 or 64): the query pass writes dq
+// and the segments' (R, r) sums (padded records) from the padded totals (S, z); the key
+// pass writes dk, dv from the padded totals (R, r).
+cudaError_t tc_noncausal_bwd_query(const void* q, const void* dout, void* dq, const float* totS, float* seg_R,
+                                   const la_shape& s, const Plan& p, cudaStream_t st);
+cudaError_t tc_noncausal_bwd_key(const void* k, const void* v, void* dk, void* dv, const float* totR,
+                                 const la_shape& s, const Plan& p, cudaStream_t st);
 bool tc_supported(const la_shape& s, int op);
 
 enum ScanMode { SCAN_EXCLUSIVE_PREFIX = 0, SCAN_EXCLUSIVE_SUFFIX = 1, SCAN_TOTAL = 2 };

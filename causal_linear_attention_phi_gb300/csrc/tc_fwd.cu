@@ -16,7 +16,11 @@
 // every chunk.  phi is applied in place to the TMA-staged Q and K tiles.
 //
 // The same kernel with kOut = false only accumulates the segment's sums
-// (S, z) for the segment scan.
+// (S, z) for the segment scan.  With kSplit as well, phi(K) enters those sums as a
+// hi + lo pair of bf16 operands (S += K_hi^T V + K_lo^T V, and z likewise), the lo
+// tiles of the two K stages taking the Q and S_prev tiles that the sums pass leaves
+// unused: the non-causal gradient needs S and z to carry phi(K) beyond bf16, since
+// its dq is a small difference of terms built from them.
 //
 // Roles (320 threads): warp 0 issues TMA loads, warp 1 owns TMEM and issues
 // tcgen05.mma, warps 2-9 (two warpgroups) transform tiles, mask A, refresh
@@ -76,7 +80,7 @@ __device__ __forceinline__ int small_row0_off(int col) {
 
 // D: the head size, 128 or 64 (padded to the 128-wide tiles); a template
 // parameter so that the full-width kernel carries no column test.
-template <bool kOut, int D>
+template <bool kOut, int D, bool kSplit = false>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_causal_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -99,6 +103,9 @@ tc_causal_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     // K and V stage s live at K0 + s * kTileBytes and V0 + s * kTileBytes
     auto sK = [&](int s) { return base + SmemLayout::K0 + s * kTileBytes; };
     auto sV = [&](int s) { return base + SmemLayout::V0 + s * kTileBytes; };
+    // the lo part of phi(K) of stage s (kSplit only: the sums pass has no Q and no S_prev)
+    auto sKlo = [&](int s) { return s == 0 ? sQ : sSb; };
+    static_assert(!(kOut && kSplit), "the split sums are a sums-pass variant");
 
     if (tid == 0) {
         uint64_t* b = reinterpret_cast<uint64_t*>(bar);
@@ -125,6 +132,11 @@ tc_causal_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             reinterpret_cast<uint4*>(sOnes)[x] = v;
             reinterpret_cast<uint4*>(sZb)[x] = make_uint4(0u, 0u, 0u, 0u);
         }
+        if (kSplit)  // lo tiles zeroed once: a 64-wide head never writes their upper column block
+            for (int x = ct; x < kTileBytes / 16; x += kComputeThreads) {
+                reinterpret_cast<uint4*>(sQ)[x] = make_uint4(0u, 0u, 0u, 0u);
+                reinterpret_cast<uint4*>(sSb)[x] = make_uint4(0u, 0u, 0u, 0u);
+            }
         fence_proxy_async_smem();
     }
     tc_fence_before();
@@ -205,6 +217,14 @@ tc_causal_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                     mma_ss(tmem + kTmS, desc_mnmajor(aK, kk), desc_mnmajor(aV, kk), id_mnmn, acc);
                     mma_ss(tmem + kTmZ, desc_mnmajor(aK, kk), desc_small(aOnes, kk), id_mn16, acc);
                 }
+                if (kSplit) {
+                    const uint32_t aKlo = smem_u32(sKlo(s));
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        mma_ss(tmem + kTmS, desc_mnmajor(aKlo, kk), desc_mnmajor(aV, kk), id_mnmn, 1);
+                        mma_ss(tmem + kTmZ, desc_mnmajor(aKlo, kk), desc_small(aOnes, kk), id_mn16, 1);
+                    }
+                }
                 mma_commit(&bar->s_done);
                 mma_commit(&bar->kv_empty[s]);
             }
@@ -254,7 +274,9 @@ tc_causal_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             bool w = mbar_wait(&bar->kv_full[s], (i >> 1) & 1, err, LA_ERR_TIMEOUT);
             if (kOut) w = w && mbar_wait(&bar->q_full, i & 1, err, LA_ERR_TIMEOUT);
             if (!CG::all(w)) { ok = false; break; }
-            if (!k_applied) CG::phi_tile(sK(s), nullptr, ct, n, D, nullptr, nullptr);
+            // (a stage's lo tile is free here: its last reader, the previous chunk's MMAs on this
+            // stage, completed before the stage was reloaded)
+            if (!k_applied) CG::phi_tile(sK(s), kSplit ? sKlo(s) : nullptr, ct, n, D, nullptr, nullptr);
             if (kOut) CG::phi_tile(sQ, nullptr, ct, n, D, nullptr, nullptr);
             fence_proxy_async_smem();
             CG::sync();
@@ -428,7 +450,7 @@ bool make_tmap_bf16_rows(CUtensorMap* map, const void* ptr, int BH, int N, int D
 }
 
 cudaError_t tc_causal_fwd(const void* q, const void* k, const void* v, void* o, float* seg, const la_shape& s,
-                          const Plan& p, bool out_pass, cudaStream_t st) {
+                          const Plan& p, bool out_pass, cudaStream_t st, bool split_k) {
     const int BH = s.B * s.H;
     CUtensorMap tq, tk, tv, to;
     const int D = s.Dk;  // = s.Dv: 128, or 64 padded to the 128-wide tiles
@@ -438,11 +460,13 @@ cudaError_t tc_causal_fwd(const void* q, const void* k, const void* v, void* o, 
         return cudaErrorInvalidValue;
     int* err = device_error_word();
     dim3 grid(p.P, BH);
-    auto kern = out_pass ? (D == 128 ? tc_causal_fwd_kernel<true, 128> : tc_causal_fwd_kernel<true, 64>)
-                         : (D == 128 ? tc_causal_fwd_kernel<false, 128> : tc_causal_fwd_kernel<false, 64>);
+    if (out_pass && split_k) return cudaErrorInvalidValue;
+    auto kern = out_pass  ? (D == 128 ? tc_causal_fwd_kernel<true, 128> : tc_causal_fwd_kernel<true, 64>)
+                : split_k ? (D == 128 ? tc_causal_fwd_kernel<false, 128, true> : tc_causal_fwd_kernel<false, 64, true>)
+                          : (D == 128 ? tc_causal_fwd_kernel<false, 128> : tc_causal_fwd_kernel<false, 64>);
     cudaError_t e = cudaFuncSetAttribute((const void*)kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
-    const char* name = out_pass ? "tc_causal_fwd_out" : "tc_segment_sums";
+    const char* name = out_pass ? "tc_causal_fwd_out" : split_k ? "tc_segment_sums_split" : "tc_segment_sums";
     launch_begin(name, st);
     kern<<<grid, kThreads, kSmemBytes, st>>>(tq, tk, tv, to, seg, s.N, p.nchunks, p.cps, p.P, err);
     return launch_end(name, st);

@@ -152,6 +152,8 @@ def test_causal_bwd_cases(la, B, H, N, Dk, Dv, dtype):
     (2, 3, 1000, 32, 64, torch.float32),       # several chunks and segments, ragged tail
     (4, 8, 1024, 64, 64, torch.bfloat16),      # the non-causal forward workload's shape
     (1, 2, 300, 128, 128, torch.bfloat16),
+    (1, 2, 2049, 128, 128, torch.bfloat16),    # tensor cores: many chunks, a one-row tail
+    (2, 1, 1500, 64, 64, torch.bfloat16),      # tensor cores, padded head, several segments
     (1, 1, 1, 32, 16, torch.float32),          # a single position
 ])
 def test_noncausal_bwd_cases(la, B, H, N, Dk, Dv, dtype):
