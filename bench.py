@@ -15,7 +15,8 @@ Printed on rank 0 as one JSON line:
               region, transfers overlapped with the kernels over groups of heads
   roofline    the dominant kernel against the measured HBM copy bandwidth
   decode      recurrent step at B=64 H=8 D=32, 3072 and 784 steps, CUDA graph
-  noncausal   the non-causal forward and backward at B=4 H=8 N=1024 D=64 bf16
+  noncausal   the non-causal forward and backward at B=4 H=8 N=1024 D=64 bf16, and at
+              B=2 H=16 N=65536 D=128 bf16
   cpu_baseline  the fp64 oracle on a bounded sample of the same workload
 
 `--impl reference` times the fp64 CPU oracle on the same workload instead
@@ -142,7 +143,8 @@ class ClockSampler:
 # The sources of the tensor-core kernels that the committed DRAM-traffic figures describe
 # (kernels, shared device code and the headers they include): any change to these makes
 # the figures stale; changes to other kernels (the scans, the CUDA-core path) do not.
-TC_KERNEL_SOURCES = ("tc_fwd.cu", "tc_bwd.cu", "tc_retention.cu", "tc_common.cuh", "sm100.cuh", "la_internal.cuh")
+TC_KERNEL_SOURCES = ("tc_fwd.cu", "tc_bwd.cu", "tc_retention.cu", "tc_apply.cu", "tc_noncausal_bwd.cu",
+                     "tc_common.cuh", "sm100.cuh", "la_internal.cuh")
 
 
 def kernel_sources_sha():
@@ -245,11 +247,16 @@ def run_ours(args):
     la.timing_enable(False)
     ktimes = la.timing_read()
     if args.workload == "profile":
-        # two retention forwards at the same shape, outside the timed region, so that one
-        # small command also covers the retention kernels in an ncu capture
+        # two retention forwards, two non-causal forwards and two non-causal backwards at the
+        # same shape, outside the timed region, so that one small command also covers their
+        # kernels in an ncu capture
         gam = W.retention_gammas(H).to(dev)
         for _ in range(2):
             la.retention_fwd(qd, kd, vd, gam, out=o)
+        for _ in range(2):
+            la.noncausal_fwd(qd, kd, vd, out=o)
+        for _ in range(2):
+            la.noncausal_bwd(qd, kd, vd, dOd, dq=dq, dk=dk, dv=dv)
         torch.cuda.synchronize()
     ms_total = max_over_ranks(e0.elapsed_time(e1))
     ms_step = ms_total / args.steps
@@ -418,26 +425,32 @@ def bench_noncausal(la, dev):
         ms = statistics.median(times)
         res[name] = {"ms": ms, "tokens_per_s": w.B * w.N / (ms / 1e3), "workload": w.name, "l2": "flushed"}
     del q, k, v, o, ws, oc, wsc, dO, dq, dk, dv, wsb, flush
-    # the non-causal forward at the long-context shape (inputs larger than L2)
+    # the non-causal forward and backward at the long-context shape (inputs larger than L2)
     wl = W.LONG_BF16
-    q, k, v = (t.to(dev) for t in W.make_inputs(wl))
+    q, k, v, dO = (t.to(dev) for t in W.make_inputs(wl, with_grad=True))
     o = torch.empty_like(v)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     ws = torch.empty(la.workspace_bytes(la.OP_NONCAUSAL_FWD, wl.B, wl.H, wl.N, wl.Dk, wl.Dv, wl.dtype),
                      dtype=torch.uint8, device=dev)
-    for _ in range(3):
-        la.noncausal_fwd(q, k, v, out=o, workspace=ws)
-    times = []
-    for _ in range(10):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        la.noncausal_fwd(q, k, v, out=o, workspace=ws)
-        e1.record()
-        torch.cuda.synchronize()
-        times.append(e0.elapsed_time(e1))
-    ms = statistics.median(times)
-    res["noncausal_fwd_long"] = {"ms": ms, "tokens_per_s": wl.B * wl.N / (ms / 1e3),
-                                 "workload": "noncausal fwd bf16 B=2 H=16 N=65536 Dk=Dv=128",
-                                 "l2": "inputs larger than L2"}
+    wsb = torch.empty(la.workspace_bytes(la.OP_NONCAUSAL_BWD, wl.B, wl.H, wl.N, wl.Dk, wl.Dv, wl.dtype),
+                      dtype=torch.uint8, device=dev)
+    for name, fn in (("noncausal_fwd_long", lambda: la.noncausal_fwd(q, k, v, out=o, workspace=ws)),
+                     ("noncausal_bwd_long",
+                      lambda: la.noncausal_bwd(q, k, v, dO, dq=dq, dk=dk, dv=dv, workspace=wsb))):
+        for _ in range(3):
+            fn()
+        times = []
+        for _ in range(10):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1))
+        ms = statistics.median(times)
+        res[name] = {"ms": ms, "tokens_per_s": wl.B * wl.N / (ms / 1e3),
+                     "workload": "noncausal " + name.split("_")[1] + " bf16 B=2 H=16 N=65536 Dk=Dv=128",
+                     "l2": "inputs larger than L2"}
     return res
 
 
@@ -629,7 +642,8 @@ def main():
     ap.add_argument("--sweep", action="store_true", help="length sweep N=2^9..2^16 (time, peak memory)")
     ap.add_argument("--workload", choices=("long", "profile"), default="long",
                     help="long: B=2 H=16 N=65536 D=128 (the benchmark); profile: B=1 H=16 N=32768, plus two "
-                         "retention forwards of that shape after the timed steps (ncu captures)")
+                         "retention forwards, two non-causal forwards and two non-causal backwards of that "
+                         "shape after the timed steps (ncu captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
