@@ -15,13 +15,16 @@
 // dq_i = sum_j phi(k_j) P_i . (v_j - o_i) is a small difference of large terms when
 // phi(k) varies little, and here every row carries the whole sum: an error of relative
 // size e in o_i (through num and den) or in S reaches dq at about e / (the spread of
-// phi(k)).  So phi(Q) and S enter num as hi + lo pairs of bf16 operands
-// (num = Q_hi S_hi + Q_hi S_lo + Q_lo S_hi), den is summed in fp32 from hi + lo, and
-// dQ~ = P S_hi^T + P S_lo^T, with g formed from the bf16 P the products use (single
-// bf16 copies gave 2.1-2.6 % error in dq against a 2 % bound).  Roles (320 threads):
-// warp 0 TMA loads, warp 1 TMEM owner and MMA issuer, warps 2-9 the compute group
-// (warp w: TMEM lanes 32 (w % 4) .. +31, i.e. row r of the chunk, column half
-// (w - 2) / 4).  Every wait is bounded.
+// phi(k)).  So S (summed from phi(K) as hi + lo parts) enters as a hi + lo pair of
+// bf16 operands, num = Q S_hi + Q S_lo and dQ~ = P S_hi^T + P S_lo^T, with g formed
+// from the bf16 P the products use (single bf16 copies gave 2.1-2.6 % error in dq
+// against a 2 % bound).  phi(Q) stays one bf16 copy: its rounding scales every key's
+// weight w_ij alike, num and den see the same copy, and o_i barely moves.  Q is
+// double-buffered (the next chunk's tile lands while this one is worked on) and dO is
+// released apart from it, right after its last reads.  Roles (320 threads): warp 0
+// TMA loads, warp 1 TMEM owner and MMA issuer, warps 2-9 the compute group (warp w:
+// TMEM lanes 32 (w % 4) .. +31, i.e. row r of the chunk, column half (w - 2) / 4).
+// Every wait is bounded.
 #include <cudaTypedefs.h>
 
 #include "tc_common.cuh"
@@ -40,17 +43,18 @@ constexpr size_t kE = (size_t)kD * kD + kD;  // a padded (R, r) or (S, z) record
 // TMEM: Y [0,128) num, then dQ~; R [128,256) the segment's sum of phi(Q)^T P.
 constexpr uint32_t kQY = 0, kQR = 128;
 
+// full/empty pairs: the Q buffers (empty: the MMA's last read and the compute group's)
+// and the dO tile (likewise).
 struct QBars {
-    uint64_t full, empty;  // Q and dO of a chunk; empty: the MMA's last read and the compute group's
+    uint64_t full_q[2], empty_q[2], full_p, empty_p;
     uint64_t q_ready, num_done, p_ready, dq_done, y_free;
     uint64_t final_mma;
 };
 
 struct QSmem {
-    static constexpr int Q = 0, P = kTileBytes, Sb = 2 * kTileBytes;  // Sb: bf16 S (hi), rows = dk
-    static constexpr int SbLo = 3 * kTileBytes;  // bf16 S - hi
-    static constexpr int Ob = 4 * kTileBytes;    // dq tile for the TMA store
-    static constexpr int QLo = 5 * kTileBytes;   // bf16 phi(Q) - hi
+    static constexpr int Q0 = 0, P = 2 * kTileBytes, Sb = 3 * kTileBytes;  // Q buffers 0, 1; Sb: bf16 S (hi), rows = dk
+    static constexpr int SbLo = 4 * kTileBytes;  // bf16 S - hi
+    static constexpr int Ob = 5 * kTileBytes;    // dq tile for the TMA store
     static constexpr int zsh = 6 * kTileBytes;  // float[128] z
     static constexpr int dpart = zsh + 512;     // float[2][128] phi(q) . z per column half
     static constexpr int tpart = dpart + 1024;  // float[2][128] P . num per column half
@@ -71,12 +75,11 @@ tc_noncausal_bwd_query_kernel(const __grid_constant__ CUtensorMap tm_q, const __
     extern __shared__ uint8_t smem_raw[];
     constexpr int kKd = D / 16;  // K steps over a head dimension (a 64-wide head is zero above)
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* sQ = base + QSmem::Q;
+    auto sQb = [&](int b) { return base + QSmem::Q0 + b * kTileBytes; };
     uint8_t* sP = base + QSmem::P;
     uint8_t* sSb = base + QSmem::Sb;
     uint8_t* sSbLo = base + QSmem::SbLo;
     uint8_t* sOb = base + QSmem::Ob;
-    uint8_t* sQLo = base + QSmem::QLo;
     float* zsh = reinterpret_cast<float*>(base + QSmem::zsh);
     float* dpart = reinterpret_cast<float*>(base + QSmem::dpart);
     float* tpart = reinterpret_cast<float*>(base + QSmem::tpart);
@@ -94,7 +97,9 @@ tc_noncausal_bwd_query_kernel(const __grid_constant__ CUtensorMap tm_q, const __
     if (tid == 0) {
         uint64_t* b = reinterpret_cast<uint64_t*>(bar);
         for (int x = 0; x < (int)(sizeof(QBars) / 8); ++x) mbar_init(b + x, 1);
-        mbar_init(&bar->empty, 2);  // one MMA commit + one compute-group arrival
+        mbar_init(&bar->empty_q[0], 2);  // one MMA commit + one compute-group arrival each
+        mbar_init(&bar->empty_q[1], 2);
+        mbar_init(&bar->empty_p, 2);
         fence_mbar_init();
         tma_prefetch_desc(&tm_q);
         tma_prefetch_desc(&tm_do);
@@ -131,37 +136,42 @@ tc_noncausal_bwd_query_kernel(const __grid_constant__ CUtensorMap tm_q, const __
 
     if (warp == 0) {
         if (lane == 0) {
-            int armed = -1;
+            int armed_q[2] = {-1, -1}, armed_p = -1;
             for (int i = 0; i < nloc; ++i) {
-                const int t0 = (cbeg + i) * kC;
-                if (!mbar_wait(&bar->empty, (i & 1) ^ 1, err, LA_ERR_TIMEOUT)) break;
-                mbar_arrive_expect_tx(&bar->full, 2 * kTileBytes);
-                tma_load_3d(sQ, &tm_q, 0, t0, bh, &bar->full);
-                tma_load_3d(sQ + kBlockBytes, &tm_q, 64, t0, bh, &bar->full);
-                tma_load_3d(sP, &tm_do, 0, t0, bh, &bar->full);
-                tma_load_3d(sP + kBlockBytes, &tm_do, 64, t0, bh, &bar->full);
-                armed = i;
+                const int t0 = (cbeg + i) * kC, b = i & 1;
+                if (!mbar_wait(&bar->empty_q[b], ((i >> 1) & 1) ^ 1, err, LA_ERR_TIMEOUT)) break;
+                mbar_arrive_expect_tx(&bar->full_q[b], kTileBytes);
+                tma_load_3d(sQb(b), &tm_q, 0, t0, bh, &bar->full_q[b]);
+                tma_load_3d(sQb(b) + kBlockBytes, &tm_q, 64, t0, bh, &bar->full_q[b]);
+                armed_q[b] = i;
+                if (!mbar_wait(&bar->empty_p, (i & 1) ^ 1, err, LA_ERR_TIMEOUT)) break;
+                mbar_arrive_expect_tx(&bar->full_p, kTileBytes);
+                tma_load_3d(sP, &tm_do, 0, t0, bh, &bar->full_p);
+                tma_load_3d(sP + kBlockBytes, &tm_do, 64, t0, bh, &bar->full_p);
+                armed_p = i;
             }
-            if (armed >= 0) mbar_wait(&bar->full, armed & 1, err, LA_ERR_TIMEOUT);
+            // no copy may still be landing when the CTA exits
+            for (int b = 0; b < 2; ++b)
+                if (armed_q[b] >= 0) mbar_wait(&bar->full_q[b], (armed_q[b] >> 1) & 1, err, LA_ERR_TIMEOUT);
+            if (armed_p >= 0) mbar_wait(&bar->full_p, armed_p & 1, err, LA_ERR_TIMEOUT);
         }
     } else if (warp == 1) {
         if (lane == 0) {
             constexpr uint32_t id_kk = idesc_bf16_f32(128, 128, 0, 0);
             constexpr uint32_t id_kmn = idesc_bf16_f32(128, 128, 0, 1);
             constexpr uint32_t id_mnmn = idesc_bf16_f32(128, 128, 1, 1);
-            const uint32_t aQ = smem_u32(sQ), aP = smem_u32(sP), aSb = smem_u32(sSb), aSbLo = smem_u32(sSbLo),
-                           aQLo = smem_u32(sQLo);
+            const uint32_t aP = smem_u32(sP), aSb = smem_u32(sSb), aSbLo = smem_u32(sSbLo);
             for (int i = 0; i < nloc; ++i) {
                 const uint32_t ph = i & 1;
+                const uint32_t aQ = smem_u32(sQb(i & 1));
                 if (!mbar_wait(&bar->q_ready, ph, err, LA_ERR_TIMEOUT) ||
                     (i > 0 && !mbar_wait(&bar->y_free, ph ^ 1, err, LA_ERR_TIMEOUT)))
                     break;
                 tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < kKd; ++kk) {  // Y = Q_hi S_hi + Q_hi S_lo + Q_lo S_hi (num)
+                for (int kk = 0; kk < kKd; ++kk) {  // Y = Q S_hi + Q S_lo (num)
                     mma_ss(tmem + kQY, desc_kmajor(aQ, kk), desc_mnmajor(aSb, kk), id_kmn, kk > 0);
                     mma_ss(tmem + kQY, desc_kmajor(aQ, kk), desc_mnmajor(aSbLo, kk), id_kmn, 1);
-                    mma_ss(tmem + kQY, desc_kmajor(aQLo, kk), desc_mnmajor(aSb, kk), id_kmn, 1);
                 }
                 mma_commit(&bar->num_done);
                 if (!mbar_wait(&bar->p_ready, ph, err, LA_ERR_TIMEOUT)) break;
@@ -176,7 +186,8 @@ tc_noncausal_bwd_query_kernel(const __grid_constant__ CUtensorMap tm_q, const __
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)  // R += phi(Q)^T P
                     mma_ss(tmem + kQR, desc_mnmajor(aQ, kk), desc_mnmajor(aP, kk), id_mnmn, (i > 0 || kk > 0));
-                mma_commit(&bar->empty);  // last MMA read of Q and P in this chunk
+                mma_commit(&bar->empty_q[i & 1]);  // last MMA reads of this Q buffer and of P in this chunk
+                mma_commit(&bar->empty_p);
             }
             mma_commit(&bar->final_mma);
             mbar_wait(&bar->final_mma, 0, err, LA_ERR_TIMEOUT);
@@ -191,39 +202,30 @@ tc_noncausal_bwd_query_kernel(const __grid_constant__ CUtensorMap tm_q, const __
             const uint32_t ph = i & 1;
             const int c0 = (cbeg + i) * kC, n = min(kC, N - c0);
             const bool valid = r < n;
-            // (a) phi on Q in place (hi) with its lo part beside it; phi(q_r) on this thread's 64
-            // columns kept for phi'(q); (hi + lo) . z in fp32.  The lo tile is free: the num
-            // products of the previous chunk, its last reader, were awaited there.
-            if (!CG::all(mbar_wait(&bar->full, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
-            CG::phi_tile(sQ, sQLo, ct, n, D, nullptr, nullptr);
+            // (a) phi on Q in place (the buffer is held to the end of the chunk: the dq epilogue
+            // reads phi(q) again for phi'(q)); phi(q_r) . z in fp32 on this thread's 64 columns
+            uint8_t* sQ = sQb(i & 1);
+            if (!CG::all(mbar_wait(&bar->full_q[i & 1], (i >> 1) & 1, err, LA_ERR_TIMEOUT))) { ok = false; break; }
+            CG::phi_tile(sQ, nullptr, ct, n, D, nullptr, nullptr);
             fence_proxy_async_smem();
             CG::sync();
             if (ct == 0) mbar_arrive(&bar->q_ready);
-            uint32_t qrow[32];
             {
                 float di = 0.f;
 #pragma unroll
                 for (int c8 = 0; c8 < 8; ++c8) {
                     const int lc = 8 * h + c8;
                     const uint4 qv = *reinterpret_cast<const uint4*>(sQ + chunk_off(r, lc));
-                    qrow[4 * c8 + 0] = qv.x;
-                    qrow[4 * c8 + 1] = qv.y;
-                    qrow[4 * c8 + 2] = qv.z;
-                    qrow[4 * c8 + 3] = qv.w;
-                    // a 64-wide head leaves the lo tile's upper column block unwritten
-                    const uint4 lv = (D > 64 || h == 0) ? *reinterpret_cast<const uint4*>(sQLo + chunk_off(r, lc))
-                                                        : make_uint4(0u, 0u, 0u, 0u);
                     const float4 za = *reinterpret_cast<const float4*>(zsh + 8 * lc);
                     const float4 zb = *reinterpret_cast<const float4*>(zsh + 8 * lc + 4);
-                    di += (bf_lo(qv.x) + bf_lo(lv.x)) * za.x + (bf_hi(qv.x) + bf_hi(lv.x)) * za.y +
-                          (bf_lo(qv.y) + bf_lo(lv.y)) * za.z + (bf_hi(qv.y) + bf_hi(lv.y)) * za.w +
-                          (bf_lo(qv.z) + bf_lo(lv.z)) * zb.x + (bf_hi(qv.z) + bf_hi(lv.z)) * zb.y +
-                          (bf_lo(qv.w) + bf_lo(lv.w)) * zb.z + (bf_hi(qv.w) + bf_hi(lv.w)) * zb.w;
+                    di += bf_lo(qv.x) * za.x + bf_hi(qv.x) * za.y + bf_lo(qv.y) * za.z + bf_hi(qv.y) * za.w +
+                          bf_lo(qv.z) * zb.x + bf_hi(qv.z) * zb.y + bf_lo(qv.w) * zb.z + bf_hi(qv.w) * zb.w;
                 }
                 dpart[128 * h + r] = di;
             }
-            CG::sync();  // both halves of phi(q) . z are in
-            // (b) den; P = dO / den in place (bf16); g = -P . num / den from that bf16 P
+            // (b) den; P = dO / den in place (bf16); g = -P . num / den from that bf16 P.  The
+            // dO wait is also the barrier after which both halves of phi(q) . z are in.
+            if (!CG::all(mbar_wait(&bar->full_p, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
             const float den = valid ? dpart[r] + dpart[128 + r] : 1.f;
             const float inv = 1.f / den;
 #pragma unroll
@@ -262,7 +264,10 @@ tc_noncausal_bwd_query_kernel(const __grid_constant__ CUtensorMap tm_q, const __
             if (h == 0) gsh[r] = g;
             tc_fence_before();
             CG::sync();
-            if (ct == 0) mbar_arrive(&bar->p_ready);
+            if (ct == 0) {
+                mbar_arrive(&bar->p_ready);
+                mbar_arrive(&bar->empty_p);  // the compute group's last read of P in this chunk
+            }
             // (c) the chunk's column sums of g phi(q) (weighted column sums of the Q tile)
             {
                 float zp[2][8];
@@ -283,8 +288,7 @@ tc_noncausal_bwd_query_kernel(const __grid_constant__ CUtensorMap tm_q, const __
                 }
                 CG::column_part(zp, drpart, ct);
             }
-            CG::sync();  // every read of Q and P by the compute group is done
-            if (ct == 0) mbar_arrive(&bar->empty);
+            CG::sync();  // drpart is complete
             // (d) dq = (dQ~ + g z) * phi'(q) on this thread's 64 columns, staged for one TMA store
             if (ct == kStoreThread) bulk_wait_read_all();  // the previous dq store has left the staging tile
             if (!CG::all(mbar_wait(&bar->dq_done, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
@@ -296,7 +300,8 @@ tc_noncausal_bwd_query_kernel(const __grid_constant__ CUtensorMap tm_q, const __
                 tmem_ld_wait();
 #pragma unroll
                 for (int c4 = 0; c4 < 4; ++c4) {
-                    const uint32_t* qu = &qrow[4 * (4 * cb + c4)];
+                    const uint4 qv = *reinterpret_cast<const uint4*>(sQ + chunk_off(r, 8 * h + 4 * cb + c4));
+                    const uint32_t qu[4] = {qv.x, qv.y, qv.z, qv.w};
                     uint4 o4;
                     uint32_t* ou = reinterpret_cast<uint32_t*>(&o4);
                     const int c = 64 * h + 32 * cb + 8 * c4;
@@ -315,8 +320,11 @@ tc_noncausal_bwd_query_kernel(const __grid_constant__ CUtensorMap tm_q, const __
             }
             fence_proxy_async_smem();
             tc_fence_before();
-            CG::sync();
-            if (ct == 0) mbar_arrive(&bar->y_free);
+            CG::sync();  // every read of this Q buffer by the compute group is done
+            if (ct == 0) {
+                mbar_arrive(&bar->y_free);
+                mbar_arrive(&bar->empty_q[i & 1]);
+            }
             if (ct == kStoreThread) {
                 tma_store_3d(&tm_dq, sOb, 0, c0, bh);
                 if (D > 64) tma_store_3d(&tm_dq, sOb + kBlockBytes, 64, c0, bh);
@@ -342,24 +350,30 @@ tc_noncausal_bwd_query_kernel(const __grid_constant__ CUtensorMap tm_q, const __
 }
 
 // ------------------------------------------------------------------ key pass
-// TMEM: DK [0,128) dK~, DV [128,256) dV.
-constexpr uint32_t kKDK = 0, kKDV = 128;
+// TMEM: two accumulator sets at 0 and 256, each DK [+0,+128) dK~ and DV [+128,+256) dV.
+// K and V are double-buffered in shared memory and the accumulators in TMEM, and phi on
+// the next chunk's K tile runs while this chunk's products are formed, so the products
+// of chunk i + 1 overlap the epilogue of chunk i.  Every per-buffer barrier is used once
+// per two chunks and never runs a phase ahead of its waiter: a buffer is refilled only
+// after its previous chunk has been consumed.
+constexpr uint32_t kKDK = 0, kKDV = 128, kKAcc = 256;
 
 struct KBars {
-    uint64_t full, empty;  // K and V of a chunk; empty: the MMA's last read and the epilogue's
-    uint64_t k_ready, kv_done, acc_free;
+    uint64_t full[2], empty[2];  // K and V buffers; empty: the MMA's last read and the epilogue's
+    uint64_t k_ready[2], kv_done[2], acc_free[2];
     uint64_t final_mma;
 };
 
 struct KSmem {
-    static constexpr int K = 0, V = kTileBytes, Rb = 2 * kTileBytes;
-    static constexpr int Ok = 3 * kTileBytes, Ov = 4 * kTileBytes;  // dk, dv tiles for the TMA stores
-    static constexpr int rsh = 5 * kTileBytes;                       // float[128] r
+    static constexpr int K0 = 0, V0 = 2 * kTileBytes, Rb = 4 * kTileBytes;  // K, V buffers 0 and 1
+    static constexpr int Ok = 5 * kTileBytes, Ov = 6 * kTileBytes;          // dk, dv tiles for the TMA stores
+    static constexpr int rsh = 7 * kTileBytes;                              // float[128] r
     static constexpr int bars = rsh + 512;
     static constexpr int tmem_slot = bars + 256;
     static constexpr int total = tmem_slot + 16;
 };
 constexpr size_t kKSmemBytes = KSmem::total + 1024;
+static_assert(kKSmemBytes <= 232448, "key pass: shared memory above the per-CTA limit");
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -369,8 +383,8 @@ tc_noncausal_bwd_key_kernel(const __grid_constant__ CUtensorMap tm_k, const __gr
     extern __shared__ uint8_t smem_raw[];
     constexpr int kKd = D / 16;
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* sK = base + KSmem::K;
-    uint8_t* sV = base + KSmem::V;
+    auto sKb = [&](int b) { return base + KSmem::K0 + b * kTileBytes; };
+    auto sVb = [&](int b) { return base + KSmem::V0 + b * kTileBytes; };
     uint8_t* sRb = base + KSmem::Rb;
     uint8_t* sOk = base + KSmem::Ok;
     uint8_t* sOv = base + KSmem::Ov;
@@ -386,7 +400,8 @@ tc_noncausal_bwd_key_kernel(const __grid_constant__ CUtensorMap tm_k, const __gr
     if (tid == 0) {
         uint64_t* b = reinterpret_cast<uint64_t*>(bar);
         for (int x = 0; x < (int)(sizeof(KBars) / 8); ++x) mbar_init(b + x, 1);
-        mbar_init(&bar->empty, 2);  // one MMA commit + one compute-group arrival
+        mbar_init(&bar->empty[0], 2);  // one MMA commit + one compute-group arrival each
+        mbar_init(&bar->empty[1], 2);
         fence_mbar_init();
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
@@ -394,7 +409,7 @@ tc_noncausal_bwd_key_kernel(const __grid_constant__ CUtensorMap tm_k, const __gr
         tma_prefetch_desc(&tm_dv);
     }
     if (warp == 1) {
-        tmem_alloc(tmem_slot, 256);
+        tmem_alloc(tmem_slot, 512);
         tmem_relinquish();
     }
     if (warp >= 2) {  // R as the bf16 operand (row r = dk, this thread's 64 columns), r in fp32
@@ -416,38 +431,42 @@ tc_noncausal_bwd_key_kernel(const __grid_constant__ CUtensorMap tm_k, const __gr
 
     if (warp == 0) {
         if (lane == 0) {
-            int armed = -1;
+            int armed[2] = {-1, -1};
             for (int i = 0; i < nloc; ++i) {
-                const int t0 = (cbeg + i) * kC;
-                if (!mbar_wait(&bar->empty, (i & 1) ^ 1, err, LA_ERR_TIMEOUT)) break;
-                mbar_arrive_expect_tx(&bar->full, 2 * kTileBytes);
-                tma_load_3d(sK, &tm_k, 0, t0, bh, &bar->full);
-                tma_load_3d(sK + kBlockBytes, &tm_k, 64, t0, bh, &bar->full);
-                tma_load_3d(sV, &tm_v, 0, t0, bh, &bar->full);
-                tma_load_3d(sV + kBlockBytes, &tm_v, 64, t0, bh, &bar->full);
-                armed = i;
+                const int t0 = (cbeg + i) * kC, b = i & 1;
+                if (!mbar_wait(&bar->empty[b], ((i >> 1) & 1) ^ 1, err, LA_ERR_TIMEOUT)) break;
+                mbar_arrive_expect_tx(&bar->full[b], 2 * kTileBytes);
+                tma_load_3d(sKb(b), &tm_k, 0, t0, bh, &bar->full[b]);
+                tma_load_3d(sKb(b) + kBlockBytes, &tm_k, 64, t0, bh, &bar->full[b]);
+                tma_load_3d(sVb(b), &tm_v, 0, t0, bh, &bar->full[b]);
+                tma_load_3d(sVb(b) + kBlockBytes, &tm_v, 64, t0, bh, &bar->full[b]);
+                armed[b] = i;
             }
-            if (armed >= 0) mbar_wait(&bar->full, armed & 1, err, LA_ERR_TIMEOUT);
+            // no copy may still be landing when the CTA exits
+            for (int b = 0; b < 2; ++b)
+                if (armed[b] >= 0) mbar_wait(&bar->full[b], (armed[b] >> 1) & 1, err, LA_ERR_TIMEOUT);
         }
     } else if (warp == 1) {
         if (lane == 0) {
             constexpr uint32_t id_kk = idesc_bf16_f32(128, 128, 0, 0);
             constexpr uint32_t id_kmn = idesc_bf16_f32(128, 128, 0, 1);
-            const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aRb = smem_u32(sRb);
+            const uint32_t aRb = smem_u32(sRb);
             for (int i = 0; i < nloc; ++i) {
-                const uint32_t ph = i & 1;
-                if (!mbar_wait(&bar->k_ready, ph, err, LA_ERR_TIMEOUT) ||
-                    (i > 0 && !mbar_wait(&bar->acc_free, ph ^ 1, err, LA_ERR_TIMEOUT)))
+                const int b = i & 1;
+                const uint32_t use = (i >> 1) & 1;  // parity of this buffer's current use
+                if (!mbar_wait(&bar->k_ready[b], use, err, LA_ERR_TIMEOUT) ||
+                    !mbar_wait(&bar->acc_free[b], use ^ 1, err, LA_ERR_TIMEOUT))
                     break;
                 tc_fence_after();
+                const uint32_t aK = smem_u32(sKb(b)), aV = smem_u32(sVb(b)), acc = tmem + kKAcc * b;
 #pragma unroll
                 for (int kk = 0; kk < kKd; ++kk)  // dK~ = V R^T (rows = keys)
-                    mma_ss(tmem + kKDK, desc_kmajor(aV, kk), desc_kmajor(aRb, kk), id_kk, kk > 0);
+                    mma_ss(acc + kKDK, desc_kmajor(aV, kk), desc_kmajor(aRb, kk), id_kk, kk > 0);
 #pragma unroll
                 for (int kk = 0; kk < kKd; ++kk)  // dV = phi(K) R
-                    mma_ss(tmem + kKDV, desc_kmajor(aK, kk), desc_mnmajor(aRb, kk), id_kmn, kk > 0);
-                mma_commit(&bar->kv_done);
-                mma_commit(&bar->empty);  // last MMA read of K and V in this chunk
+                    mma_ss(acc + kKDV, desc_kmajor(aK, kk), desc_mnmajor(aRb, kk), id_kmn, kk > 0);
+                mma_commit(&bar->kv_done[b]);
+                mma_commit(&bar->empty[b]);  // last MMA read of this K and V buffer
             }
             mma_commit(&bar->final_mma);
             mbar_wait(&bar->final_mma, 0, err, LA_ERR_TIMEOUT);
@@ -458,24 +477,33 @@ tc_noncausal_bwd_key_kernel(const __grid_constant__ CUtensorMap tm_k, const __gr
         const int r = 32 * (warp & 3) + lane;
         const uint32_t lb = ((uint32_t)(32 * (warp & 3)) << 16) + 64 * h;
         bool ok = CG::all(true);
-        for (int i = 0; i < nloc && ok; ++i) {
-            const uint32_t ph = i & 1;
-            const int c0 = (cbeg + i) * kC, n = min(kC, N - c0);
-            // (a) phi on K in place
-            if (!CG::all(mbar_wait(&bar->full, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
-            CG::phi_tile(sK, nullptr, ct, n, D, nullptr, nullptr);
+        // phi on K in place for chunk j (buffer j & 1), then hand it to the MMA
+        auto phi_k = [&](int j) -> bool {
+            const int b = j & 1, n = min(kC, N - (cbeg + j) * kC);
+            if (!CG::all(mbar_wait(&bar->full[b], (j >> 1) & 1, err, LA_ERR_TIMEOUT))) return false;
+            CG::phi_tile(sKb(b), nullptr, ct, n, D, nullptr, nullptr);
             fence_proxy_async_smem();
             CG::sync();
-            if (ct == 0) mbar_arrive(&bar->k_ready);
+            if (ct == 0) mbar_arrive(&bar->k_ready[b]);
+            return true;
+        };
+        if (nloc > 0) ok = phi_k(0);
+        for (int i = 0; i < nloc && ok; ++i) {
+            const int b = i & 1;
+            const int c0 = (cbeg + i) * kC;
+            // (a) the next chunk's phi while this chunk's products are formed
+            if (i + 1 < nloc && !phi_k(i + 1)) { ok = false; break; }
             // (b) dk = (dK~ + r) * phi'(k) (phi(k) read back from the K tile) and dv, this
             // thread's 64 columns of key row r, staged for one TMA store each
             if (ct == kStoreThread) bulk_wait_read_all();  // the previous stores have left the staging tiles
-            if (!CG::all(mbar_wait(&bar->kv_done, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
+            if (!CG::all(mbar_wait(&bar->kv_done[b], (i >> 1) & 1, err, LA_ERR_TIMEOUT))) { ok = false; break; }
             tc_fence_after();
+            const uint8_t* sK = sKb(b);
+            const uint32_t acc = tmem + lb + kKAcc * b;
 #pragma unroll
             for (int cb = 0; cb < 2; ++cb) {
                 uint32_t w[32];
-                tmem_ld32(tmem + lb + kKDK + 32 * cb, w);
+                tmem_ld32(acc + kKDK + 32 * cb, w);
                 tmem_ld_wait();
 #pragma unroll
                 for (int c4 = 0; c4 < 4; ++c4) {
@@ -495,13 +523,13 @@ tc_noncausal_bwd_key_kernel(const __grid_constant__ CUtensorMap tm_k, const __gr
                     *reinterpret_cast<uint4*>(sOk + chunk_off(r, lc)) = o4;
                 }
             }
-            tmem_half_row_to_tile(tmem + lb + kKDV, sOv, r, h);
+            tmem_half_row_to_tile(acc + kKDV, sOv, r, h);
             fence_proxy_async_smem();
             tc_fence_before();
-            CG::sync();  // the accumulators are read and the K tile is no longer used
+            CG::sync();  // this accumulator set is read and this K buffer is no longer used
             if (ct == 0) {
-                mbar_arrive(&bar->acc_free);
-                mbar_arrive(&bar->empty);
+                mbar_arrive(&bar->acc_free[b]);
+                mbar_arrive(&bar->empty[b]);
             }
             if (ct == kStoreThread) {
                 tma_store_3d(&tm_dk, sOk, 0, c0, bh);
@@ -519,7 +547,7 @@ tc_noncausal_bwd_key_kernel(const __grid_constant__ CUtensorMap tm_k, const __gr
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, 256);
+        tmem_dealloc(tmem, 512);
     }
 }
 

@@ -8,9 +8,9 @@ the kernel rounds, and checks that the chosen scheme (D and phi(K) as hi + lo
 pairs in D K~, g taken from the rounded P) stays inside the 2e-2 bound while
 single bf16 copies do not.  The non-causal gradient has the same cancellation
 with the whole sequence in every row; its model checks the scheme of the
-non-causal kernels (phi(K) as hi + lo in the sums S and z, S and phi(Q) as
-hi + lo in num, den in fp32, g from the rounded P).  CPU only; no GPU code
-involved.
+non-causal kernels (phi(K) as hi + lo in the sums S and z, S as hi + lo in
+num and dQ~, phi(Q) one bf16 copy in num and den, den in fp32, g from the
+rounded P).  CPU only; no GPU code involved.
 """
 import numpy as np
 import pytest
@@ -117,14 +117,14 @@ def nc_data():
     return q, qt, kt, v, dO, dq
 
 
-def nc_modelled_dq(data, k_split, qs_split):
+def nc_modelled_dq(data, k_split, s_split, q_split):
     q, qt, kt, v, dO, _ = data
     Ks = split(kt) if k_split else bf(kt)          # phi(K) operand(s) of the sums
     S, z = Ks.T @ v, Ks.sum(0)                     # fp32-accumulated sums
     Sh = bf(S)
-    Sl = bf(S - Sh) if qs_split else 0 * S
+    Sl = bf(S - Sh) if s_split else 0 * S
     Qh = bf(qt)
-    Ql = bf(qt - Qh) if qs_split else 0 * qt
+    Ql = bf(qt - Qh) if q_split else 0 * qt
     num = Qh @ Sh + Qh @ Sl + Ql @ Sh
     den = (Qh + Ql) @ z                            # fp32, from the same parts
     P = bf(dO / den[:, None])                      # bf16 P
@@ -142,10 +142,19 @@ def test_noncausal_exact_gradient_is_the_state_form(nc_data):
     assert rel(ref, dq) < 1e-10
 
 
-@pytest.mark.parametrize("k_split,qs_split", [(False, False), (True, False), (False, True)])
-def test_noncausal_partial_schemes_exceed_the_bound(nc_data, k_split, qs_split):
-    assert rel(nc_modelled_dq(nc_data, k_split, qs_split), nc_data[-1]) > 2e-2
+@pytest.mark.parametrize("k_split,s_split,q_split", [(False, False, False), (True, False, False),
+                                                     (False, True, True)])
+def test_noncausal_partial_schemes_exceed_the_bound(nc_data, k_split, s_split, q_split):
+    assert rel(nc_modelled_dq(nc_data, k_split, s_split, q_split), nc_data[-1]) > 2e-2
 
 
 def test_noncausal_chosen_scheme_meets_the_bound(nc_data):
-    assert rel(nc_modelled_dq(nc_data, True, True), nc_data[-1]) < 5e-3
+    assert rel(nc_modelled_dq(nc_data, True, True, False), nc_data[-1]) < 5e-3
+
+
+def test_noncausal_splitting_phi_q_adds_nothing(nc_data):
+    # phi(q) rounding scales every key's weight alike and num, den share it: splitting it
+    # as well changes dq by far less than the bound
+    a = rel(nc_modelled_dq(nc_data, True, True, False), nc_data[-1])
+    b = rel(nc_modelled_dq(nc_data, True, True, True), nc_data[-1])
+    assert abs(a - b) < 5e-4
