@@ -243,7 +243,7 @@ la_status check_device() {
             return fail(LA_ERR_CUDA, "cannot query device %d", dev);
         ok = (major == 10 && minor == 3) ? 1 : -1;
         g_cc_ok[dev] = ok;
-        if (ok < 0) return fail(LA_ERR_UNSUPPORTED, "device %d is sm_%d%d; this build targets sm_103a", dev, major, minor);
+        if (ok < 0) return fail(LA_ERR_UNSUPPORTED, "device %d is sm_%d%d; the library is compiled for sm_103a", dev, major, minor);
     }
     return ok > 0 ? LA_OK : fail(LA_ERR_UNSUPPORTED, "device is not sm_103");
 }
