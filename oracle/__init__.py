@@ -52,7 +52,7 @@ def _declare(lib):
     lib.oracle_causal_chunked.argtypes = [_DP, _DP, _DP, _DP, i, i, i, i, i]
     lib.oracle_causal_chunked.restype = None
     for name in ("oracle_causal_bwd_direct", "oracle_causal_bwd_recurrent",
-                 "oracle_noncausal_bwd_direct"):
+                 "oracle_noncausal_bwd_direct", "oracle_noncausal_bwd_assoc"):
         getattr(lib, name).argtypes = [_DP] * 7 + [i, i, i, i]
         getattr(lib, name).restype = None
     lib.oracle_recurrent_step.argtypes = [_DP] * 6 + [i, i, i]
@@ -164,6 +164,9 @@ class Oracle:
     def noncausal_bwd_direct(self, q, k, v, dO):
         return self._bwd("oracle_noncausal_bwd_direct", q, k, v, dO)
 
+    def noncausal_bwd_assoc(self, q, k, v, dO):
+        return self._bwd("oracle_noncausal_bwd_assoc", q, k, v, dO)
+
     # ---- retention (decay gamma per head, no feature map, no normaliser)
     @staticmethod
     def _gamma(gamma, BH):
@@ -226,6 +229,7 @@ noncausal_assoc = default.noncausal_assoc
 causal_bwd_direct = default.causal_bwd_direct
 causal_bwd_recurrent = default.causal_bwd_recurrent
 noncausal_bwd_direct = default.noncausal_bwd_direct
+noncausal_bwd_assoc = default.noncausal_bwd_assoc
 recurrent_step = default.recurrent_step
 retention_direct = default.retention_direct
 retention_recurrent = default.retention_recurrent

@@ -32,8 +32,9 @@
  *
  * Parity pins (tests/test_oracle.py): direct == recurrence == chunked; N=1,
  * constant V, identical keys, Dk=1, non-causal == causal at i=N, convex hull,
- * affine covariance, decode vs numpy K^T V, finite differences for the
- * backward, gradient invariants, and phi against the library ELU.
+ * affine covariance, decode vs numpy K^T V, finite differences for every
+ * backward (the non-causal one in its direct and its associative form),
+ * gradient invariants, and phi against the library ELU.
  */
 #include <math.h>
 #include <stdlib.h>
@@ -454,6 +455,76 @@ void oracle_noncausal_bwd_direct(const double* q, const double* k, const double*
             dk[IDX3(h, 0, 0, N, Dk) + t] = dkt[t] * dphi(kh[t]);
         }
         free(qt); free(kt); free(den); free(oh); free(dqt); free(dkt);
+    }
+}
+
+/*
+ * Backward of the non-causal form through its totals, O(N Dk Dv) per head: the chain
+ * rule of oracle_noncausal_bwd_direct with the sums over keys (for q) and over queries
+ * (for k and v) taken once.  With S = sum_j phi(k_j) v_j^T and z = sum_j phi(k_j)
+ * ([KAT] 핵심 구성요소 2; [REV] 3.2), for every i: den_i = phi(q_i) . z,
+ * o_i = phi(q_i)^T S / den_i, P_i = dO_i / den_i, g_i = -P_i . o_i, so that
+ * dL/dw_ij = P_i . v_j + g_i and
+ *   dphi(q_i) = sum_j phi(k_j) (P_i . v_j + g_i) = S P_i + g_i z;
+ * then with R = sum_i phi(q_i) P_i^T and r = sum_i g_i phi(q_i):
+ *   dphi(k_j) = sum_i phi(q_i) (P_i . v_j + g_i) = R v_j + r,   dv_j = R^T phi(k_j).
+ */
+void oracle_noncausal_bwd_assoc(const double* q, const double* k, const double* v, const double* dO,
+                                double* dq, double* dk, double* dv, int BH, int N, int Dk, int Dv) {
+#pragma omp parallel for schedule(dynamic)
+    for (int h = 0; h < BH; ++h) {
+        double* qt = phi_slice(q, h, N, Dk);
+        double* kt = phi_slice(k, h, N, Dk);
+        const double* vh = v + IDX3(h, 0, 0, N, Dv);
+        const double* dOh = dO + IDX3(h, 0, 0, N, Dv);
+        const double* qh = q + IDX3(h, 0, 0, N, Dk);
+        const double* kh = k + IDX3(h, 0, 0, N, Dk);
+        double* S = (double*)calloc((size_t)Dk * Dv, sizeof(double));
+        double* z = (double*)calloc((size_t)Dk, sizeof(double));
+        double* R = (double*)calloc((size_t)Dk * Dv, sizeof(double));
+        double* r = (double*)calloc((size_t)Dk, sizeof(double));
+        double* P = (double*)malloc(sizeof(double) * (size_t)Dv);
+        double* num = (double*)malloc(sizeof(double) * (size_t)Dv);
+        for (int j = 0; j < N; ++j)
+            for (int d = 0; d < Dk; ++d) {
+                const double kd = kt[(size_t)j * Dk + d];
+                z[d] += kd;
+                for (int m = 0; m < Dv; ++m) S[(size_t)d * Dv + m] += kd * vh[(size_t)j * Dv + m];
+            }
+        for (int i = 0; i < N; ++i) {
+            const double* qi = qt + (size_t)i * Dk;
+            const double den = dot(qi, z, Dk);
+            for (int m = 0; m < Dv; ++m) num[m] = 0.0;
+            for (int d = 0; d < Dk; ++d)
+                for (int m = 0; m < Dv; ++m) num[m] += qi[d] * S[(size_t)d * Dv + m];
+            double g = 0.0;
+            for (int m = 0; m < Dv; ++m) {
+                P[m] = dOh[(size_t)i * Dv + m] / den;
+                g -= P[m] * num[m] / den;
+            }
+            for (int d = 0; d < Dk; ++d) {
+                double sp = 0.0;
+                for (int m = 0; m < Dv; ++m) sp += S[(size_t)d * Dv + m] * P[m];
+                dq[IDX3(h, i, d, N, Dk)] = (sp + g * z[d]) * dphi(qh[(size_t)i * Dk + d]);
+                r[d] += g * qi[d];
+                for (int m = 0; m < Dv; ++m) R[(size_t)d * Dv + m] += qi[d] * P[m];
+            }
+        }
+        for (int j = 0; j < N; ++j) {
+            const double* kj = kt + (size_t)j * Dk;
+            const double* vj = vh + (size_t)j * Dv;
+            for (int d = 0; d < Dk; ++d) {
+                double rv = r[d];
+                for (int m = 0; m < Dv; ++m) rv += R[(size_t)d * Dv + m] * vj[m];
+                dk[IDX3(h, j, d, N, Dk)] = rv * dphi(kh[(size_t)j * Dk + d]);
+            }
+            for (int m = 0; m < Dv; ++m) {
+                double s = 0.0;
+                for (int d = 0; d < Dk; ++d) s += R[(size_t)d * Dv + m] * kj[d];
+                dv[IDX3(h, j, m, N, Dv)] = s;
+            }
+        }
+        free(qt); free(kt); free(S); free(z); free(R); free(r); free(P); free(num);
     }
 }
 

@@ -229,19 +229,23 @@ def pin_bwd_finite_differences(orc):
             for a, b in zip(bwd(q, k, v, dO), fd):
                 assert np.max(np.abs(a - b)) <= 1e-6 * max(1.0, np.max(np.abs(b)))
         fdn = _fd_grads(orc.noncausal_direct, q, k, v, dO)
-        for a, b in zip(orc.noncausal_bwd_direct(q, k, v, dO), fdn):
-            assert np.max(np.abs(a - b)) <= 1e-6 * max(1.0, np.max(np.abs(b)))
+        for bwd in (orc.noncausal_bwd_direct, orc.noncausal_bwd_assoc):
+            for a, b in zip(bwd(q, k, v, dO), fdn):
+                assert np.max(np.abs(a - b)) <= 1e-6 * max(1.0, np.max(np.abs(b)))
 
 
 def pin_bwd_forms_agree(orc):
     q, k, v, dO = case(22, B=2, H=1, N=50, Dk=16, Dv=32)
     for a, b in zip(orc.causal_bwd_recurrent(q, k, v, dO), orc.causal_bwd_direct(q, k, v, dO)):
         assert rel(a, b) < 1e-11
+    for a, b in zip(orc.noncausal_bwd_assoc(q, k, v, dO), orc.noncausal_bwd_direct(q, k, v, dO)):
+        assert rel(a, b) < 1e-11
 
 
 def pin_bwd_invariants(orc):
     q, k, v, dO = case(23, B=1, H=2, N=24, Dk=5, Dv=3)
-    for bwd in (orc.causal_bwd_direct, orc.causal_bwd_recurrent, orc.noncausal_bwd_direct):
+    for bwd in (orc.causal_bwd_direct, orc.causal_bwd_recurrent, orc.noncausal_bwd_direct,
+                orc.noncausal_bwd_assoc):
         # sum_j dv_j = sum_i dO_i (the weights of each output sum to one)
         _, _, dv = bwd(q, k, v, dO)
         assert rel(dv.sum(axis=2), dO.sum(axis=2)) < 1e-12

@@ -433,3 +433,16 @@ def test_noncausal_fwd_long_sampled_heads(la):
     for b, h in [(0, 0), (1, 15)]:
         sl = (slice(b, b + 1), slice(h, h + 1))
         check("head (%d,%d)" % (b, h), o[sl], oracle.noncausal_assoc(q[sl], k[sl], v[sl]), 2e-2)
+
+
+def test_noncausal_bwd_long_sampled_heads(la):
+    """The non-causal gradient at B=2 H=16 N=65536 D=128 bf16 (split segment sums, query and
+    key passes on the tensor cores, the launch the bench times): two whole heads against the
+    oracle's associative form of the same gradient."""
+    w = W.LONG_BF16
+    q, k, v, dO = W.make_inputs(w, with_grad=True)
+    dq, dk, dv = (t.cpu() for t in la.noncausal_bwd(*dev(q, k, v, dO)))
+    heads = [(0, 0), (1, 15)]
+    sel = lambda t: torch.stack([t[b, h] for b, h in heads])[None]
+    ref = oracle.noncausal_bwd_assoc(sel(q), sel(k), sel(v), sel(dO))
+    check_all([(n, sel(a), b) for n, a, b in zip(("dq", "dk", "dv"), (dq, dk, dv), ref)], 2e-2)

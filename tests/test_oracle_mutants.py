@@ -29,6 +29,9 @@ MUTANTS = [
     ("bwd_dq_drops_gz", "double s = g[i] * z[d];", "double s = 0.0;"),
     ("noncausal_bwd_dk_uses_k", "dkt[(size_t)j * Dk + d] += gw * qt[(size_t)i * Dk + d];\n                }\n                for (int m = 0; m < Dv; ++m) dvh[(size_t)j * Dv + m] += w * dOi[m] / den[i];\n            }\n        }\n        const double* qh = q + IDX3(h, 0, 0, N, Dk);\n        const double* kh = k + IDX3(h, 0, 0, N, Dk);\n        for (size_t t = 0; t < (size_t)N * Dk; ++t) {\n            dq[IDX3(h, 0, 0, N, Dk) + t] = dqt[t] * dphi(qh[t]);\n            dk[IDX3(h, 0, 0, N, Dk) + t] = dkt[t] * dphi(kh[t]);\n        }\n        free(qt); free(kt); free(den); free(oh); free(dqt); free(dkt);\n    }\n}\n",
      "dkt[(size_t)j * Dk + d] += gw * kt[(size_t)j * Dk + d];\n                }\n                for (int m = 0; m < Dv; ++m) dvh[(size_t)j * Dv + m] += w * dOi[m] / den[i];\n            }\n        }\n        const double* qh = q + IDX3(h, 0, 0, N, Dk);\n        const double* kh = k + IDX3(h, 0, 0, N, Dk);\n        for (size_t t = 0; t < (size_t)N * Dk; ++t) {\n            dq[IDX3(h, 0, 0, N, Dk) + t] = dqt[t] * dphi(qh[t]);\n            dk[IDX3(h, 0, 0, N, Dk) + t] = dkt[t] * dphi(kh[t]);\n        }\n        free(qt); free(kt); free(den); free(oh); free(dqt); free(dkt);\n    }\n}\n"),
+    ("noncausal_assoc_bwd_g_sign", "g -= P[m] * num[m] / den;", "g += P[m] * num[m] / den;"),
+    ("noncausal_assoc_bwd_dk_drops_r", "double rv = r[d];", "double rv = 0.0;"),
+    ("noncausal_assoc_bwd_r_from_k", "r[d] += g * qi[d];", "r[d] += g * kt[(size_t)i * Dk + d];"),
     ("retention_decay_exponent_plus_one", "const double w = powi(gamma[h], i - j) * dot(",
      "const double w = powi(gamma[h], i - j + 1) * dot("),
     ("retention_step_decays_after_adding",
