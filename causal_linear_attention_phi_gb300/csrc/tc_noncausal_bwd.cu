@@ -6,7 +6,7 @@
 // R = sum_i phi(q_i) P_i^T and r = sum_i g_i phi(q_i) over all positions:
 //   dq_i = (S P_i + g_i z) * phi'(q_i),  dk_j = (R v_j + r) * phi'(k_j),  dv_j = R^T phi(k_j)
 // (the causal gradient's state algebra without the mask: velog review 3.2 and 3.5,
-// digest 핵심 구성요소 2).  There is no intra-chunk term, so each pass is a pair of
+// digest 핵심 구성요소 2).  There is no intra-chunk term, so each pass is a few
 // products per chunk against totals held in shared memory as bf16 operands:
 //   query pass:  num = phi(Q) S -> P, g (den in fp32 from phi(q) . z) -> dQ~ = P S^T,
 //                dq = (dQ~ + g z) * phi'(q); R += phi(Q)^T P and the column sums of
