@@ -403,6 +403,28 @@ def test_maximum_head_count(la, N, D, dtype):
     check_all([("dq", dq.cpu()[idx], ref[0]), ("dk", dk.cpu()[idx], ref[1]), ("dv", dv.cpu()[idx], ref[2])], tol)
 
 
+@pytest.mark.parametrize("N,D,dtype", [(70, 16, torch.float32), (129, 64, torch.bfloat16)])
+def test_maximum_head_count_noncausal_and_retention(la, N, D, dtype):
+    """B*H = 65535 for the non-causal forward and gradient and the retention forward (CUDA
+    cores for fp32, the padded tensor-core path for bf16 D = 64); sampled heads against the
+    oracle."""
+    B = 65535
+    q, k, v, dO = W.random_case(4545 + N, B, 1, N, D, D, dtype=dtype, scale=D ** -0.5, with_grad=True)
+    qd, kd, vd, dOd = dev(q, k, v, dO)
+    o = la.noncausal_fwd(qd, kd, vd).cpu()
+    dq, dk, dv = (t.cpu() for t in la.noncausal_bwd(qd, kd, vd, dOd))
+    del dOd
+    gam = torch.tensor([0.95])
+    orr = la.retention_fwd(qd, kd, vd, gam.to(DEV)).cpu()
+    idx = torch.tensor(SAMPLE_HEADS)
+    sq, sk, sv, sdo = (t[idx] for t in (q, k, v, dO))
+    tol = tol_for(dtype)
+    check("noncausal o", o[idx], oracle.noncausal_direct(sq, sk, sv), tol)
+    ref = oracle.noncausal_bwd_direct(sq, sk, sv, sdo)
+    check_all([("dq", dq[idx], ref[0]), ("dk", dk[idx], ref[1]), ("dv", dv[idx], ref[2])], tol)
+    check("retention o", orr[idx], oracle.retention_recurrent(sq, sk, sv, gam), tol)
+
+
 def test_maximum_head_count_decode(la):
     B, Dk, Dv = 65535, 16, 32
     q, k, v = W.random_case(4343, B, 1, 2, Dk, Dv)
