@@ -2,13 +2,15 @@
 
 Each ``pin_*`` function takes an oracle front end (``oracle.Oracle``) and raises
 AssertionError when the oracle disagrees with a closed form, an invariant, a
-library routine, brute-force finite differences or a hand-worked fixture.  The
+library routine, brute-force finite differences, exact symbolic derivatives of
+the definition or a hand-worked fixture.  The
 pins are chosen so that a plausible slip anywhere in the oracle (a dropped term,
 a wrong sign or index, a transposed operand) fails at least one of them; the
 mutation test plants such slips in a copy of the oracle and checks exactly that.
 """
 from __future__ import annotations
 
+import functools
 import os
 
 import numpy as np
@@ -232,6 +234,56 @@ def pin_bwd_finite_differences(orc):
         for bwd in (orc.noncausal_bwd_direct, orc.noncausal_bwd_assoc):
             for a, b in zip(bwd(q, k, v, dO), fdn):
                 assert np.max(np.abs(a - b)) <= 1e-6 * max(1.0, np.max(np.abs(b)))
+
+
+@functools.lru_cache(maxsize=1)
+def _exact_symbolic_grads():
+    """Gradients of L = sum_i dO_i . o_i taken exactly (sympy) from the definition
+    o_i = sum_j w_ij v_j / sum_j w_ij, w_ij = phi(q_i) . phi(k_j), on a 3-position case with
+    both branches of phi: (inputs, causal grads, non-causal grads), or None without sympy."""
+    try:
+        import sympy as sp
+    except ImportError:
+        return None
+    N, Dk, Dv = 3, 2, 2
+    R = sp.Rational
+    vals = {  # eighths, none zero, both signs (phi's two branches)
+        "q": [[5, -3], [-6, 2], [1, 7]], "k": [[-2, 4], [3, -5], [-7, 1]],
+        "v": [[3, -1], [-4, 6], [2, 5]], "dO": [[1, -2], [3, 1], [-2, 4]],
+    }
+    sym = {n: [[sp.Symbol("%s_%d_%d" % (n, i, d)) for d in range(2)] for i in range(N)] for n in ("q", "k", "v")}
+    at = {sym[n][i][d]: R(vals[n][i][d], 8) for n in sym for i in range(N) for d in range(2)}
+    # phi by the branch the concrete value lies in (no value is 0, where the branches meet)
+    ph = lambda s: s + 1 if at[s] > 0 else sp.exp(s)
+    qt = [[ph(x) for x in row] for row in sym["q"]]
+    kt = [[ph(x) for x in row] for row in sym["k"]]
+    dO = [[R(x, 8) for x in row] for row in vals["dO"]]
+    grads = []
+    for causal in (True, False):
+        L = 0
+        for i in range(N):
+            js = range(i + 1) if causal else range(N)
+            w = [sum(qt[i][d] * kt[j][d] for d in range(Dk)) for j in js]
+            den = sum(w)
+            for m in range(Dv):
+                L += dO[i][m] * sum(wj * sym["v"][j][m] for wj, j in zip(w, js)) / den
+        grads.append([np.array([[[[float(sp.N(sp.diff(L, sym[n][i][d]).subs(at), 30)) for d in range(2)]
+                                  for i in range(N)]]]) for n in ("q", "k", "v")])
+    args = tuple(np.array(vals[n], dtype=np.float64)[None, None] / 8 for n in ("q", "k", "v", "dO"))
+    return args, grads[0], grads[1]
+
+
+def pin_bwd_exact_symbolic(orc):
+    """Every backward form of the oracle against the exact gradients of the definition."""
+    ex = _exact_symbolic_grads()
+    if ex is None:  # sympy missing: finite differences still pin the backward
+        return
+    args, causal, noncausal = ex
+    for forms, exact in (((orc.causal_bwd_direct, orc.causal_bwd_recurrent), causal),
+                         ((orc.noncausal_bwd_direct, orc.noncausal_bwd_assoc), noncausal)):
+        for bwd in forms:
+            for a, b in zip(bwd(*args), exact):
+                assert rel(a, b) < 1e-12
 
 
 def pin_bwd_forms_agree(orc):
