@@ -67,9 +67,9 @@ def _declare(lib):
     lib.la_retention_fwd.argtypes = [_vp] * 6 + [Shape, _vp, ctypes.c_size_t, _vp]
     lib.la_retention_step.argtypes = [_vp] * 6 + [Shape, _vp]
     lib.la_selftest_bounded_wait.argtypes = [_vp]
-    for f in ("la_causal_step_host", "la_noncausal_fwd", "la_noncausal_bwd", "la_causal_fwd", "la_causal_fwd_with_state", "la_causal_bwd", "la_causal_bwd_after_fwd",
-              "la_recurrent_step",
-              "la_last_error",
+    for f in ("la_causal_step_host", "la_noncausal_fwd", "la_noncausal_bwd", "la_causal_fwd",
+              "la_causal_fwd_with_state", "la_causal_bwd", "la_causal_bwd_after_fwd", "la_recurrent_step",
+              "la_retention_fwd", "la_retention_step", "la_selftest_bounded_wait", "la_last_error",
               "la_clear_error", "la_timing_enable", "la_timing_reset"):
         getattr(lib, f).restype = ctypes.c_int
     lib.la_last_error.argtypes = []
@@ -145,6 +145,8 @@ def _shape4(q, k, v):
 
 
 def workspace_bytes(op: int, B: int, H: int, N: int, Dk: int, Dv: int, dtype: torch.dtype) -> int:
+    if dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("unsupported dtype %s (float32 or bfloat16)" % dtype)
     code = LA_BF16 if dtype == torch.bfloat16 else LA_F32
     return int(library().la_workspace_bytes(op, Shape(B, H, N, Dk, Dv, code)))
 
