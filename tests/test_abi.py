@@ -122,3 +122,32 @@ def test_product_path_fails_loudly_without_library(tmp_path):
             la.library(str(tmp_path / "missing.so"))
     finally:
         la._lib = saved
+
+
+def _segments(la, B, H, N, D=128):
+    """Segments per head of the tensor-core plan, read back from the causal forward's
+    workspace (one padded (S, z) record of (128 * 128 + 128) fp32 per segment and head)."""
+    import torch
+    rec = (128 * 128 + 128) * 4
+    ws = la.workspace_bytes(la.OP_CAUSAL_FWD, B, H, N, D, D, torch.bfloat16)
+    assert ws % (B * H * rec) == 0
+    return ws // (B * H * rec)
+
+
+@pytest.mark.parametrize("B,H,N", [(2, 16, 65536), (1, 16, 32768), (1, 8, 65536), (1, 1, 1 << 19),
+                                   (4, 8, 1024), (65535, 1, 129), (1, 1, 1)])
+def test_planner_segments(la, B, H, N):
+    # host logic only: every segment gets the same chunk count but possibly the last, none is
+    # empty, and the grid stays within 8 waves of the 152 SMs (one CTA per SM)
+    BH, nchunks = B * H, -(-N // 128)
+    P = _segments(la, B, H, N)
+    cps = -(-nchunks // P)
+    assert 1 <= P <= nchunks and -(-nchunks // cps) == P
+    assert BH * P <= 8 * 152 or P == 1
+
+
+def test_planner_fills_whole_waves_at_the_long_shape(la):
+    # B=2 H=16 N=65536: 512 chunks per head as 19 segments of 27 (the last 26), 608 CTAs,
+    # exactly 4 waves of 152; one head of 2^19 positions: 152 segments of 27, one wave
+    assert _segments(la, 2, 16, 65536) == 19
+    assert _segments(la, 1, 1, 1 << 19) == 152

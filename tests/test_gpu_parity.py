@@ -439,8 +439,9 @@ def test_maximum_head_count_decode(la):
 
 
 def test_long_single_head_bf16(la):
-    """One head of N = 2^19 positions (1216 segments of the tensor-core planner, a scan over
-    them, index arithmetic past 2^31 elements of work): the forward against the oracle."""
+    """One head of N = 2^19 positions (4096 chunks: the tensor-core planner gives 152
+    segments of 27 chunks, one wave, and the scan runs over 152 records of one head): the
+    forward against the oracle."""
     q, k, v = W.random_case(4444, 1, 1, 1 << 19, 64, 64, dtype=torch.bfloat16, scale=64 ** -0.5)
     o = la.causal_fwd(*dev(q, k, v))
     check("o", o, oracle.causal_recurrent(q, k, v), 2e-2)
