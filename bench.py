@@ -423,7 +423,9 @@ def bench_noncausal(la, dev):
             torch.cuda.synchronize()
             times.append(e0.elapsed_time(e1))
         ms = statistics.median(times)
-        res[name] = {"ms": ms, "tokens_per_s": w.B * w.N / (ms / 1e3), "workload": w.name, "l2": "flushed"}
+        res[name] = {"ms": ms, "tokens_per_s": w.B * w.N / (ms / 1e3),
+                     "workload": "%s bf16 B=%d H=%d N=%d Dk=Dv=%d" % (name.replace("_", " "), w.B, w.H, w.N, w.Dk),
+                     "l2": "flushed"}
     del q, k, v, o, ws, oc, wsc, dO, dq, dk, dv, wsb, flush
     # the non-causal forward and backward at the long-context shape (inputs larger than L2)
     wl = W.LONG_BF16
