@@ -9,14 +9,19 @@ everything per position).  The inputs (2.1 GB) are far larger than L2, so consec
 cannot reuse cached data.
 
 Printed on rank 0 as one JSON line:
-  value       tokens/s (B*N*ranks / step time), inputs resident in HBM
+  value       tokens/s (B*N*ranks / step time), inputs resident in HBM; the timed
+              region holds the K steps and two CUDA events, nothing else
   e2e         the same through the C ABI with host buffers (la_causal_step_host):
               pinned-host q, k, v, dO in and o, dq, dk, dv out inside the timed
               region, transfers overlapped with the kernels over groups of heads
-  roofline    the dominant kernel against the measured HBM copy bandwidth
-  decode      recurrent step at B=64 H=8 D=32, 3072 and 784 steps, CUDA graph
+  roofline    the dominant kernel against the measured HBM copy bandwidth, its
+              duration from a separate instrumented pass of the same steps
+  decode      recurrent step at B=64 H=8 D=32, 3072 and 784 steps, and at B=8192
+              (state larger than L2), CUDA graphs of single-step launches
   noncausal   the non-causal forward and backward at B=4 H=8 N=1024 D=64 bf16, and at
               B=2 H=16 N=65536 D=128 bf16
+  sweep       causal fwd+bwd at B=1 H=8 D=64 bf16 for N = 2^9 .. 2^16: time,
+              tokens/s and peak device memory per N
   cpu_baseline  the fp64 oracle on a bounded sample of the same workload
 
 `--impl reference` times the fp64 CPU oracle on the same workload instead
@@ -94,13 +99,21 @@ class ClockSampler:
     def __init__(self, index: int):
         self.index = index
         self.proc = None
-        self.lines = []
+        self.lines = []   # (arrival time, csv line)
+        self.t_start = None
+        self.t_stop = None
+
+    def mark_start(self):
+        self.t_start = time.perf_counter()
+
+    def mark_stop(self):
+        self.t_stop = time.perf_counter()
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
         except Exception:
@@ -109,7 +122,7 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.perf_counter(), line.strip()))
 
     def __exit__(self, *a):
         if self.proc is not None:
@@ -122,7 +135,13 @@ class ClockSampler:
     def summary(self):
         sm, mx, reasons = [], [], set()
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        for l in self.lines:
+        lines = self.lines
+        if self.t_start is not None and self.t_stop is not None:
+            # the samples taken while the timed region ran (plus the one just after it, which
+            # covers its last 20 ms); all of them if none arrived in that window
+            inside = [x for x in lines if self.t_start <= x[0] <= self.t_stop + 0.03]
+            lines = inside or lines
+        for _, l in lines:
             parts = [x.strip() for x in l.split(",")]
             if len(parts) < 9:
                 continue
@@ -231,19 +250,29 @@ def run_ours(args):
     torch.cuda.synchronize()
     assert la.last_error() == 0
 
-    # ---- timed region (device events on the launch stream; per-kernel events inside)
-    la.timing_reset()
-    la.timing_enable(True)
+    # ---- timed region: device events on the launch stream around K steps, nothing else
+    # recorded inside it
     barrier()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
+        time.sleep(0.1)  # the sampler's first reading lands before the timed region starts
+        clk.mark_start()
         e0.record(stream)
         for _ in range(args.steps):
             step()
         e1.record(stream)
         torch.cuda.synchronize()
+        clk.mark_stop()
     barrier()
+    # ---- per-kernel split from a separate pass of the same steps with the library's
+    # per-launch events on (outside the timed region)
+    inst_steps = min(args.steps, 10)
+    la.timing_reset()
+    la.timing_enable(True)
+    for _ in range(inst_steps):
+        step()
+    torch.cuda.synchronize()
     la.timing_enable(False)
     ktimes = la.timing_read()
     if args.workload == "profile":
@@ -262,7 +291,8 @@ def run_ours(args):
     ms_step = ms_total / args.steps
     tokens_per_step = B * N * ws_n
     value = weak_scaling_value(B * N, ws_n, ms_step)
-    launches = sum(c for c, _ in ktimes.values())
+    launches_per_step = sum(c for c, _ in ktimes.values()) / inst_steps
+    launches = int(round(launches_per_step * args.steps))
     assert la.last_error() == 0
 
     # ---- roofline of the dominant kernel
@@ -290,7 +320,10 @@ def run_ours(args):
         "config": {"workload": w.name, "B": B, "H": H, "N": N, "Dk": Dk, "Dv": Dv,
                    "global_batch": B * ws_n, "seq_len": N, "parallelism": "replicas over heads/batch (dp%d)" % ws_n,
                    "l2": "inputs (2.1 GB) larger than L2; no flush needed"},
-        "kernel_times_ms": {n: {"launches": c, "total_ms": round(t, 4)} for n, (c, t) in ktimes.items()},
+        "kernel_times_ms": {n: {"launches": c, "total_ms": round(t, 4), "avg_ms": round(t / c, 5)}
+                            for n, (c, t) in ktimes.items()},
+        "kernel_times_from": "a separate pass of %d steps with per-launch CUDA events, after the timed region "
+                             "(the timed region itself carries no instrumentation)" % inst_steps,
         "gpu_launches": launches,
         "roofline": roofline,
         "step_roofline": step_roof,
@@ -333,6 +366,10 @@ def run_ours(args):
         result["noncausal"] = bench_noncausal(la, dev)
         result["retention"] = bench_retention(la, dev)
         result["retention"]["step"] = ret_step
+        result["sweep"] = {"workload": "causal fwd+bwd bf16 B=1 H=8 Dk=Dv=64, N = 2^9 .. 2^16 (seed 3)",
+                           "l2": "flushed before every timed step", "steps_per_n": 10,
+                           "peak": "torch.cuda.max_memory_allocated above the flush buffer: inputs, outputs, "
+                                   "workspaces", "rows": length_sweep(la, dev, 10, 3)}
     if rank == 0 and not args.skip_cpu:
         result["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     assert la.last_error() == 0
@@ -343,51 +380,68 @@ def run_ours(args):
         print(json.dumps(result))
 
 
-def bench_decode(la, dev, hbm):
-    out = {}
-    for wd in (W.DECODE_CIFAR, W.DECODE_MNIST):
-        T = wd.steps
-        q, k, v = (t.to(dev) for t in W.make_decode_inputs(wd))
-        S = torch.zeros(wd.B, wd.H, wd.Dk, wd.Dv, device=dev)
-        z = torch.zeros(wd.B, wd.H, wd.Dk, device=dev)
-        outs = torch.empty(T, wd.B, wd.H, wd.Dv, device=dev)
-        s = torch.cuda.Stream(dev)
-        s.wait_stream(torch.cuda.current_stream(dev))
-        with torch.cuda.stream(s):
-            for t in range(3):  # warm-up outside capture
-                la.recurrent_step(q[t], k[t], v[t], S, z, out=outs[t])
-        torch.cuda.synchronize()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=s):
-            for t in range(T):
-                la.recurrent_step(q[t], k[t], v[t], S, z, out=outs[t])
-        g.replay()
-        torch.cuda.synchronize()
-        reps = 5
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for _ in range(reps):
-            g.replay()
-        e1.record()
-        torch.cuda.synchronize()
-        us_step = e0.elapsed_time(e1) * 1e3 / (reps * T)
-        # kernel-only duration: eager launches bracketed by the library's per-launch events
-        la.timing_reset()
-        la.timing_enable(True)
-        for t in range(min(T, 200)):
+def _decode_graph_us(la, wd, B, T, dev, reps=5):
+    """CUDA graph of T single-step launches of the recurrent step at batch B (heads H, D of
+    the decode workload), replayed `reps` times: microseconds per step."""
+    g_in = torch.Generator(device="cpu")
+    g_in.manual_seed(wd.seed)
+    q, k, v = (torch.randn(T, B, wd.H, d, generator=g_in).to(dev) for d in (wd.Dk, wd.Dk, wd.Dv))
+    S = torch.zeros(B, wd.H, wd.Dk, wd.Dv, device=dev)
+    z = torch.zeros(B, wd.H, wd.Dk, device=dev)
+    outs = torch.empty(T, B, wd.H, wd.Dv, device=dev)
+    s = torch.cuda.Stream(dev)
+    s.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(s):
+        for t in range(3):  # warm-up outside capture
             la.recurrent_step(q[t], k[t], v[t], S, z, out=outs[t])
-        torch.cuda.synchronize()
-        la.timing_enable(False)
-        n_l, ms_l = la.timing_read()["recurrent_step"]
-        kern_us = ms_l * 1e3 / n_l
-        bytes_step = wd.B * wd.H * (2 * wd.Dk * wd.Dv * 4 + 2 * wd.Dk * 4 + (2 * wd.Dk + 2 * wd.Dv) * 4)
-        out["steps_%d" % T] = {
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for t in range(T):
+            la.recurrent_step(q[t], k[t], v[t], S, z, out=outs[t])
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / (reps * T)
+    del q, k, v, S, z, outs, g
+    return us
+
+
+def bench_decode(la, dev, hbm):
+    """Steps/s of the recurrent step (CUDA-graph replay of single-step launches): at the decode
+    workload (B=64 H=8 D=32, whose 2 MiB state stays in L2 between steps), and at B=8192,
+    where the state (268 MB) is larger than L2 and every step moves it through HBM."""
+    out = {}
+    wd0 = W.DECODE_CIFAR
+    bytes_per_head = 2 * wd0.Dk * wd0.Dv * 4 + 2 * wd0.Dk * 4 + (2 * wd0.Dk + 2 * wd0.Dv) * 4
+    for wd in (W.DECODE_CIFAR, W.DECODE_MNIST):
+        us_step = _decode_graph_us(la, wd, wd.B, wd.steps, dev)
+        bytes_step = wd.B * wd.H * bytes_per_head
+        out["steps_%d" % wd.steps] = {
             "steps_per_s": 1e6 / us_step, "us_per_step": us_step, "tokens_per_s": wd.B * 1e6 / us_step,
-            "kernel_us": kern_us, "bytes_per_step": bytes_step,
-            "achieved_gbs_graph": bytes_step / (us_step * 1e-6) / 1e9,
-            "achieved_gbs_kernel": bytes_step / (kern_us * 1e-6) / 1e9,
-            "frac_graph": bytes_step / (us_step * 1e-6) / 1e9 / hbm,
-            "note": "S (2 MiB) stays in L2 across steps; graph replay of %d single-step launches" % T}
+            "bytes_per_step": bytes_step,
+            "achieved_gbs": bytes_step / (us_step * 1e-6) / 1e9,
+            "frac_of_hbm": bytes_step / (us_step * 1e-6) / 1e9 / hbm,
+            "launch_floor_us": 0.51,
+            "note": "S (2 MiB) stays in L2 across steps, so the step is bound by launch and L2 latency, not HBM; "
+                    "launch_floor_us is a CUDA-graph replay of an empty kernel of the same grid with "
+                    "programmatic dependent launch, measured on this GPU type; graph of %d single-step launches"
+                    % wd.steps}
+    B_big, T_big = 8192, 64
+    us_big = _decode_graph_us(la, wd0, B_big, T_big, dev)
+    bytes_big = B_big * wd0.H * bytes_per_head
+    out["large_batch"] = {
+        "workload": "recurrent decode f32 B=%d H=%d Dk=Dv=%d, CUDA graph of %d single-step launches"
+                    % (B_big, wd0.H, wd0.Dk, T_big),
+        "us_per_step": us_big, "steps_per_s": 1e6 / us_big, "tokens_per_s": B_big * 1e6 / us_big,
+        "bytes_per_step": bytes_big, "achieved_gbs": bytes_big / (us_big * 1e-6) / 1e9,
+        "frac_of_hbm": bytes_big / (us_big * 1e-6) / 1e9 / hbm,
+        "note": "S is 268 MB, larger than L2: each step reads and writes it from HBM"}
     return out
 
 
@@ -585,13 +639,11 @@ def run_reference(args):
     print(json.dumps(res))
 
 
-def run_sweep(args):
-    """fwd+bwd time and peak device memory per N for the length sweep
-    (bf16, B=1 H=8 D=64, N = 2^9 .. 2^16); one JSON line per N."""
-    import causal_linear_attention_phi_gb300 as la
-    torch.cuda.set_device(0)
-    dev = torch.device("cuda", 0)
-    la.build.build_library()
+def length_sweep(la, dev, steps: int, warmup: int):
+    """fwd+bwd time, tokens/s and peak device memory per N for the length sweep (bf16,
+    B=1 H=8 D=64, N = 2^9 .. 2^16), L2 flushed before every timed step; a list of dicts."""
+    rows = []
+    hbm = peaks()[0]
     for N in W.SWEEP_NS:
         w = W.sweep(N)
         q, k, v, dO = W.make_inputs(w, with_grad=True)
@@ -611,10 +663,10 @@ def run_sweep(args):
             la.causal_fwd(qd, kd, vd, out=o, workspace=wsf)
             la.causal_bwd(qd, kd, vd, dOd, dq=dq, dk=dk, dv=dv, workspace=wsb, fwd_workspace=wsf)
 
-        for _ in range(args.warmup):
+        for _ in range(warmup):
             step()
         times = []
-        for _ in range(args.steps):
+        for _ in range(steps):
             flush.zero_()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record()
@@ -624,11 +676,42 @@ def run_sweep(args):
             times.append(e0.elapsed_time(e1))
         ms = statistics.median(times)
         peak = torch.cuda.max_memory_allocated() - base - flush.numel()
-        print(json.dumps({"sweep": "causal fwd+bwd bf16 B=1 H=8 D=64", "N": N, "ms": ms,
-                          "tokens_per_s": w.B * N / (ms / 1e3), "peak_bytes": int(peak),
-                          "workspace_bytes": int(wsf.numel() + wsb.numel()),
-                          "io_bytes": int(8 * w.B * w.H * N * w.Dk * 2), "l2": "flushed between steps"}))
+        alg = w.B * w.H * N * ((2 * w.Dk + 2 * w.Dv) + (4 * w.Dk + 3 * w.Dv)) * 2
+        rows.append({"N": N, "ms": ms, "tokens_per_s": w.B * N / (ms / 1e3), "peak_bytes": int(peak),
+                     "workspace_bytes": int(wsf.numel() + wsb.numel()),
+                     "io_bytes": int(8 * w.B * w.H * N * w.Dk * 2),
+                     "frac_of_hbm": alg / (ms / 1e3) / 1e9 / hbm})
         del qd, kd, vd, dOd, o, dq, dk, dv, wsf, wsb, flush
+    return rows
+
+
+def run_sweep(args):
+    """The length sweep alone, one JSON line per N."""
+    import causal_linear_attention_phi_gb300 as la
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    la.build.build_library()
+    for row in length_sweep(la, dev, args.steps, args.warmup):
+        print(json.dumps(dict(sweep="causal fwd+bwd bf16 B=1 H=8 D=64", l2="flushed between steps", **row)))
+
+
+def run_decode_profile(args):
+    """Five eager decode steps at B=64 H=8 D=32 (state in L2) and five at B=8192 (state in
+    HBM): a short, fixed launch sequence for ncu captures of the recurrent step."""
+    import causal_linear_attention_phi_gb300 as la
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    la.build.build_library()
+    wd = W.DECODE_CIFAR
+    for B in (wd.B, 8192):
+        q, k, v = (torch.randn(B, wd.H, d, device=dev) for d in (wd.Dk, wd.Dk, wd.Dv))
+        S = torch.zeros(B, wd.H, wd.Dk, wd.Dv, device=dev)
+        z = torch.zeros(B, wd.H, wd.Dk, device=dev)
+        for _ in range(5):
+            la.recurrent_step(q, k, v, S, z)
+        torch.cuda.synchronize()
+    assert la.last_error() == 0
+    print(json.dumps({"decode_profile": "5 steps at B=64 and 5 at B=8192, H=8 Dk=Dv=32 fp32"}))
 
 
 def main():
@@ -642,6 +725,8 @@ def main():
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--skip-extras", action="store_true")
     ap.add_argument("--sweep", action="store_true", help="length sweep N=2^9..2^16 (time, peak memory)")
+    ap.add_argument("--decode-profile", action="store_true",
+                    help="only 5 decode steps at B=64 and 5 at B=8192 (H=8 D=32), for ncu captures")
     ap.add_argument("--workload", choices=("long", "profile"), default="long",
                     help="long: B=2 H=16 N=65536 D=128 (the benchmark); profile: B=1 H=16 N=32768, plus two "
                          "retention forwards, two non-causal forwards and two non-causal backwards of that "
@@ -649,7 +734,15 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.sweep:
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.gpus != world:
+        # one process per GPU: N GPUs need N ranks, started by torch.distributed.run
+        sys.exit("bench.py --gpus %d needs %d ranks (python -m torch.distributed.run --nproc-per-node %d "
+                 "bench.py --gpus %d); this launch has WORLD_SIZE=%d" % (args.gpus, args.gpus, args.gpus,
+                                                                         args.gpus, world))
+    if args.decode_profile:
+        run_decode_profile(args)
+    elif args.sweep:
         run_sweep(args)
     elif args.impl == "reference":
         run_reference(args)

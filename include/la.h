@@ -256,10 +256,16 @@ la_status la_retention_step(const void* q, const void* k, const void* v, const f
  * no cudaMalloc, cudaFree or other allocating routine.  The array is static:
  * every GPU that loads the library holds the 16 MiB until the process exits.
  * The first call on a device looks up the array's address on that device
- * (that device must be current); make that first call before any stream
- * capture.  Sizes needing more than the array, i.e. B*H*(Dk*Dv + Dk)*4 bytes
- * > 16 MiB (at Dk = Dv = 128: B*H > 254), return LA_ERR_WORKSPACE before
- * anything is launched.  Every call shares the array, so calls whose work
+ * (that device must be current) and caches it with the current CUDA context;
+ * a call under another context of the device (after cudaDeviceReset, say)
+ * looks it up again.  Make the first call on a device, and the first after a
+ * reset, before any stream capture.  The array holds one state record per
+ * head and segment, and needs room for at least one segment: B*H records of
+ * (Dk*Dv + Dk)*4 bytes on the CUDA-core path, and of (128*128 + 128)*4 bytes
+ * on the tensor-core path (bf16 heads of 64 or 128 keep the padded 128-wide
+ * record), so B*H may be at most 254 for bf16 heads of 64 or 128.  Larger
+ * sizes return LA_ERR_WORKSPACE before anything is launched; where the usual
+ * segment count does not fit, fewer, longer segments are used.  Every call shares the array, so calls whose work
  * overlaps on the GPU (other streams or host threads) race on it and corrupt
  * each other's results: serialise them.  Each call rewrites every part of the
  * array it reads, so what a previous call left there does not matter.

@@ -151,3 +151,15 @@ def test_planner_fills_whole_waves_at_the_long_shape(la):
     # exactly 4 waves of 152; one head of 2^19 positions: 152 segments of 27, one wave
     assert _segments(la, 2, 16, 65536) == 19
     assert _segments(la, 1, 1, 1 << 19) == 152
+
+
+def test_bench_refuses_a_gpu_count_it_was_not_launched_with():
+    """bench.py --gpus N runs one process per GPU: without N ranks it exits non-zero
+    instead of timing one GPU under another GPU count."""
+    import subprocess
+    import sys
+    env = dict(os.environ)
+    env.pop("WORLD_SIZE", None)
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "2", "--steps", "1"],
+                       capture_output=True, text=True, env=env, timeout=300)
+    assert r.returncode != 0 and "WORLD_SIZE=1" in r.stderr

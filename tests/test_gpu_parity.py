@@ -225,7 +225,7 @@ def test_bwd_invariants(la):
 
 
 # ---------------------------------------------------------------- length sweep, bf16 B=1 H=8 D=64
-@pytest.mark.parametrize("N", [512, 1024, 4096])
+@pytest.mark.parametrize("N", [n for n in W.SWEEP_NS if n <= 4096])
 def test_sweep_fwd_bwd_full(la, N):
     w = W.sweep(N)
     q, k, v, dO = W.make_inputs(w, with_grad=True)
@@ -251,8 +251,11 @@ def _sampled_heads(la, w, heads, tensors=None):
               [(n, sel(a.cpu()), b) for n, a, b in zip(("dq", "dk", "dv"), (dq, dk, dv), ref)], 2e-2)
 
 
-def test_sweep_65536_sampled_heads(la):
-    _sampled_heads(la, W.sweep(65536), [(0, 0), (0, 5)])
+@pytest.mark.parametrize("N", [n for n in W.SWEEP_NS if n > 4096])
+def test_sweep_long_sampled_heads(la, N):
+    """Every length of the sweep above 4096 (8192 .. 65536): the whole batch on the GPU,
+    two whole heads against the oracle."""
+    _sampled_heads(la, W.sweep(N), [(0, 0), (0, 5)])
 
 
 def test_long_bf16_full_size_sampled_heads(la):
@@ -314,6 +317,43 @@ def test_decode_mnist_shape_all_steps(la):
     phk = oracle.phi(to_seq(k))
     check("final S", S.cpu(), np.einsum("bhnd,bhnm->bhdm", phk, to_np(to_seq(v))), 1e-4)
     assert rel_per_head(z.cpu()[..., None], phk.sum(axis=2)[..., None]) < 1e-4
+
+
+def _graph_decode(la, w, q, k, v):
+    """All steps of the decode workload captured in one CUDA graph of single-step launches
+    and replayed once, as the benchmark runs them; returns (outputs [T,B,H,Dv], S, z)."""
+    qd, kd, vd = dev(q, k, v)
+    S = torch.zeros(w.B, w.H, w.Dk, w.Dv, device=DEV)
+    z = torch.zeros(w.B, w.H, w.Dk, device=DEV)
+    outs = torch.empty(w.steps, w.B, w.H, w.Dv, device=DEV)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):  # first launch outside the capture
+        la.recurrent_step(qd[0], kd[0], vd[0], S, z, out=outs[0])
+    torch.cuda.synchronize()
+    S.zero_()
+    z.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for t in range(w.steps):
+            la.recurrent_step(qd[t], kd[t], vd[t], S, z, out=outs[t])
+    g.replay()
+    torch.cuda.synchronize()
+    return outs.cpu(), S.cpu(), z.cpu()
+
+
+def test_decode_cifar_shape_all_steps_graph(la):
+    """The 3072-step decode at B=64 H=8 D=32 (CIFAR-shaped pixel sequences), every step's
+    output and the final (S, z) against the oracle, through the graph replay the bench times."""
+    w = W.DECODE_CIFAR
+    q, k, v = W.make_decode_inputs(w)
+    outs, S, z = _graph_decode(la, w, q, k, v)
+    to_seq = lambda x: x.permute(1, 2, 0, 3).contiguous()
+    ref = oracle.causal_recurrent(to_seq(q), to_seq(k), to_seq(v))
+    check("decode outputs, 3072 steps", to_seq(outs), ref, 1e-4)
+    phk = oracle.phi(to_seq(k))
+    check("final S", S, np.einsum("bhnd,bhnm->bhdm", phk, to_np(to_seq(v))), 1e-4)
+    assert rel_per_head(z[..., None], phk.sum(axis=2)[..., None]) < 1e-4
 
 
 def test_decode_resume_is_bit_exact(la):

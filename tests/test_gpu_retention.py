@@ -175,6 +175,36 @@ def test_decode_from_zero_matches_oracle_steps(la):
     check("final S", S, Sref, 1e-4)
 
 
+def test_decode_cifar_shape_all_steps_graph(la):
+    """The retention step over all 3072 steps of the CIFAR-shaped decode workload (B=64 H=8
+    D=32 fp32), captured in one CUDA graph as the bench runs it: every output and the final
+    state against the oracle's recurrence."""
+    w = W.DECODE_CIFAR
+    q, k, v = W.make_decode_inputs(w)
+    g = W.retention_gammas(w.H)
+    qd, kd, vd, gd = (t.to(DEV) for t in (q, k, v, g))
+    S = torch.zeros(w.B, w.H, w.Dk, w.Dv, device=DEV)
+    outs = torch.empty(w.steps, w.B, w.H, w.Dv, device=DEV)
+    st = torch.cuda.Stream()
+    st.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(st):
+        la.retention_step(qd[0], kd[0], vd[0], gd, S, out=outs[0])
+    torch.cuda.synchronize()
+    S.zero_()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=st):
+        for t in range(w.steps):
+            la.retention_step(qd[t], kd[t], vd[t], gd, S, out=outs[t])
+    graph.replay()
+    torch.cuda.synchronize()
+    to_seq = lambda x: x.permute(1, 2, 0, 3).contiguous()
+    ref = oracle.retention_recurrent(to_seq(q), to_seq(k), to_seq(v), g)
+    check("retention decode, 3072 steps", to_seq(outs.cpu()), ref, 1e-4)
+    decay = g.double().numpy()[:, None] ** np.arange(w.steps - 1, -1, -1, dtype=np.float64)[None, :]  # [H, T]
+    Sref = np.einsum("hn,bhnd,bhnm->bhdm", decay, to_np(to_seq(k)), to_np(to_seq(v)))
+    check("final S", S.cpu(), Sref, 1e-4)
+
+
 @pytest.mark.parametrize("Dk,Dv", [(16, 128), (128, 16), (64, 32)])
 def test_decode_head_sizes(la, Dk, Dv):
     B, H, T = 3, 2, 20

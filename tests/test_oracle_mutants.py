@@ -62,4 +62,6 @@ def test_planted_mistake_is_caught(name, old, new, tmp_path):
             pin(orc)
         except (AssertionError, FloatingPointError, ValueError):
             failed.append(pin.__name__)
+        except pytest.skip.Exception:  # a pin that cannot run here (sympy missing) catches nothing
+            pass
     assert failed, "planted mistake %s passed every pin" % name
