@@ -16,7 +16,7 @@ Printed on rank 0 as one JSON line:
               region, transfers overlapped with the kernels over groups of heads
   roofline    the dominant kernel against the measured HBM copy bandwidth, its
               duration from a separate instrumented pass of the same steps
-  decode      recurrent step at B=64 H=8 D=32, 3072 and 784 steps, and at B=8192
+  decode      recurrent step at B=64 H=8 D=32, 3072 and 784 steps, and at B=8000
               (state larger than L2), CUDA graphs of single-step launches
   noncausal   the non-causal forward and backward at B=4 H=8 N=1024 D=64 bf16, and at
               B=2 H=16 N=65536 D=128 bf16
@@ -414,8 +414,8 @@ def _decode_graph_us(la, wd, B, T, dev, reps=5):
 
 def bench_decode(la, dev, hbm):
     """Steps/s of the recurrent step (CUDA-graph replay of single-step launches): at the decode
-    workload (B=64 H=8 D=32, whose 2 MiB state stays in L2 between steps), and at B=8192,
-    where the state (268 MB) is larger than L2 and every step moves it through HBM."""
+    workload (B=64 H=8 D=32, whose 2 MiB state stays in L2 between steps), and at
+    B=8000, where the state (262 MB) is larger than L2 and every step moves it through HBM."""
     out = {}
     wd0 = W.DECODE_CIFAR
     bytes_per_head = 2 * wd0.Dk * wd0.Dv * 4 + 2 * wd0.Dk * 4 + (2 * wd0.Dk + 2 * wd0.Dv) * 4
@@ -432,7 +432,7 @@ def bench_decode(la, dev, hbm):
                     "launch_floor_us is a CUDA-graph replay of an empty kernel of the same grid with "
                     "programmatic dependent launch, measured on this GPU type; graph of %d single-step launches"
                     % wd.steps}
-    B_big, T_big = 8192, 64
+    B_big, T_big = 8000, 64  # B*H = 64000 heads (the library takes up to 65535)
     us_big = _decode_graph_us(la, wd0, B_big, T_big, dev)
     bytes_big = B_big * wd0.H * bytes_per_head
     out["large_batch"] = {
@@ -441,7 +441,7 @@ def bench_decode(la, dev, hbm):
         "us_per_step": us_big, "steps_per_s": 1e6 / us_big, "tokens_per_s": B_big * 1e6 / us_big,
         "bytes_per_step": bytes_big, "achieved_gbs": bytes_big / (us_big * 1e-6) / 1e9,
         "frac_of_hbm": bytes_big / (us_big * 1e-6) / 1e9 / hbm,
-        "note": "S is 268 MB, larger than L2: each step reads and writes it from HBM"}
+        "note": "S is 262 MB, larger than L2: each step reads and writes it from HBM"}
     return out
 
 
@@ -696,14 +696,14 @@ def run_sweep(args):
 
 
 def run_decode_profile(args):
-    """Five eager decode steps at B=64 H=8 D=32 (state in L2) and five at B=8192 (state in
+    """Five eager decode steps at B=64 H=8 D=32 (state in L2) and five at B=8000 (state in
     HBM): a short, fixed launch sequence for ncu captures of the recurrent step."""
     import causal_linear_attention_phi_gb300 as la
     torch.cuda.set_device(0)
     dev = torch.device("cuda", 0)
     la.build.build_library()
     wd = W.DECODE_CIFAR
-    for B in (wd.B, 8192):
+    for B in (wd.B, 8000):
         q, k, v = (torch.randn(B, wd.H, d, device=dev) for d in (wd.Dk, wd.Dk, wd.Dv))
         S = torch.zeros(B, wd.H, wd.Dk, wd.Dv, device=dev)
         z = torch.zeros(B, wd.H, wd.Dk, device=dev)
@@ -711,7 +711,7 @@ def run_decode_profile(args):
             la.recurrent_step(q, k, v, S, z)
         torch.cuda.synchronize()
     assert la.last_error() == 0
-    print(json.dumps({"decode_profile": "5 steps at B=64 and 5 at B=8192, H=8 Dk=Dv=32 fp32"}))
+    print(json.dumps({"decode_profile": "5 steps at B=64 and 5 at B=8000, H=8 Dk=Dv=32 fp32"}))
 
 
 def main():
@@ -726,7 +726,7 @@ def main():
     ap.add_argument("--skip-extras", action="store_true")
     ap.add_argument("--sweep", action="store_true", help="length sweep N=2^9..2^16 (time, peak memory)")
     ap.add_argument("--decode-profile", action="store_true",
-                    help="only 5 decode steps at B=64 and 5 at B=8192 (H=8 D=32), for ncu captures")
+                    help="only 5 decode steps at B=64 and 5 at B=8000 (H=8 D=32), for ncu captures")
     ap.add_argument("--workload", choices=("long", "profile"), default="long",
                     help="long: B=2 H=16 N=65536 D=128 (the benchmark); profile: B=1 H=16 N=32768, plus two "
                          "retention forwards, two non-causal forwards and two non-causal backwards of that "

@@ -27,7 +27,7 @@ __all__ = [
 OP_NONCAUSAL_FWD, OP_CAUSAL_FWD, OP_CAUSAL_BWD, OP_NONCAUSAL_BWD, OP_RETENTION_FWD = 0, 1, 2, 3, 4
 LA_F32, LA_BF16 = 0, 1
 _STATUS = {0: "LA_OK", 1: "LA_ERR_INVALID_ARG", 2: "LA_ERR_UNSUPPORTED", 3: "LA_ERR_WORKSPACE",
-           4: "LA_ERR_CUDA", 5: "LA_ERR_TIMEOUT"}
+           4: "LA_ERR_CUDA", 5: "LA_ERR_TIMEOUT", 6: "LA_ERR_BOUNDS"}
 
 
 class LaError(RuntimeError):
@@ -88,11 +88,14 @@ def _declare(lib):
 
 
 def library(path: str | None = None):
-    """The loaded libla (ctypes.CDLL).  Raises RuntimeError if it is not built."""
+    """The loaded libla (ctypes.CDLL).  Raises RuntimeError if it is not built.
+
+    With LA_DEBUG=1 in the environment the debug build (device-side index checks,
+    _lib/libla_debug.so) is loaded instead of the regular one."""
     global _lib
     with _lock:
         if _lib is None:
-            p = path or _build.LIB_PATH
+            p = path or _build.lib_path(os.environ.get("LA_DEBUG", "0") == "1")
             if not os.path.exists(p):
                 raise RuntimeError("libla.so is not built (%s); run causal_linear_attention_phi_gb300.build."
                                    "build_library() or __graft_entry__.build()" % p)

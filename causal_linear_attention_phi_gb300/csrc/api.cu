@@ -15,6 +15,9 @@ namespace la {
 
 // ------------------------------------------------------------------ sticky error word
 __device__ int g_error_word = 0;
+#ifdef LA_DEBUG
+__device__ unsigned int g_debug_site = 0;  // (file tag << 16) | line of the first failed index check
+#endif
 
 namespace {
 thread_local std::string t_detail;
@@ -610,6 +613,21 @@ la_status la_last_error(void) {
     int v = 0;
     if (cudaMemcpyFromSymbol(&v, g_error_word, sizeof(int)) != cudaSuccess)
         return fail(LA_ERR_CUDA, "cannot read the device error word");
+#ifdef LA_DEBUG
+    if (v == LA_ERR_BOUNDS) {
+        unsigned site = 0;
+        if (cudaMemcpyFromSymbol(&site, g_debug_site, sizeof(site)) == cudaSuccess) {
+            static const char* const kFiles[] = {"api.cu", "decode.cu", "host_step.cu", "noalloc.cu", "retention.cu",
+                                                 "selftest.cu", "simt_kernels.cu", "tc_apply.cu", "tc_bwd.cu",
+                                                 "tc_fwd.cu", "tc_noncausal_bwd.cu", "tc_retention.cu",
+                                                 "la_internal.cuh", "simt_common.cuh", "tc_common.cuh", "sm100.cuh"};
+            const char* file = "unknown file";
+            for (const char* f : kFiles)
+                if (dbg::file_tag(f) == (site >> 16)) file = f;
+            fail(LA_ERR_BOUNDS, "index check failed at %s:%u", file, site & 0xFFFFu);
+        }
+    }
+#endif
     return static_cast<la_status>(v);
 }
 
@@ -617,6 +635,11 @@ la_status la_clear_error(void) {
     const int zero = 0;
     if (cudaMemcpyToSymbol(g_error_word, &zero, sizeof(int)) != cudaSuccess)
         return fail(LA_ERR_CUDA, "cannot clear the device error word");
+#ifdef LA_DEBUG
+    const unsigned zs = 0;
+    if (cudaMemcpyToSymbol(g_debug_site, &zs, sizeof(zs)) != cudaSuccess)
+        return fail(LA_ERR_CUDA, "cannot clear the device error site");
+#endif
     return LA_OK;
 }
 
@@ -628,13 +651,18 @@ const char* la_status_string(la_status st) {
         case LA_ERR_WORKSPACE: return "LA_ERR_WORKSPACE: workspace missing or too small";
         case LA_ERR_CUDA: return "LA_ERR_CUDA: CUDA runtime or launch failure";
         case LA_ERR_TIMEOUT: return "LA_ERR_TIMEOUT: a bounded device wait ran out";
+        case LA_ERR_BOUNDS: return "LA_ERR_BOUNDS: a device-side index check of the debug build failed";
     }
     return "unknown la_status";
 }
 
 const char* la_error_detail(void) { return t_detail.c_str(); }
 
-const char* la_version(void) { return "0.1.0"; }
+#ifdef LA_DEBUG
+const char* la_version(void) { return "0.1.1-debug"; }
+#else
+const char* la_version(void) { return "0.1.1"; }
+#endif
 
 la_status la_timing_enable(int on) {
     std::lock_guard<std::mutex> g(g_t_mu);

@@ -69,6 +69,43 @@ __device__ __forceinline__ float phi_f(float x) {
 // phi'(x) = 1 for x > 0, exp(x) otherwise; equal to min(1, phi(x)).
 __device__ __forceinline__ float dphi_from_phi(float p) { return fminf(p, 1.f); }
 
+// ------------------------------------------------------------------ debug-build index checks
+// LA_DCHECK(cond) is `true` in the regular build (the condition is not even
+// evaluated).  In the debug build (compiled with -DLA_DEBUG and relocatable
+// device code, so every translation unit sees the one sticky error word) it
+// evaluates the condition; if it is false it records LA_ERR_BOUNDS in the
+// sticky word and the site (a 16-bit tag of the source file's name and the
+// line) in g_debug_site, both first-failure-wins, and yields false so that the
+// caller skips the access.  Nothing traps.
+namespace dbg {
+constexpr uint32_t file_tag(const char* path) {  // FNV-1a of the base name, 16 bits
+    const char* b = path;
+    for (const char* c = path; *c; ++c)
+        if (*c == '/') b = c + 1;
+    uint32_t h = 2166136261u;
+    for (; *b; ++b) h = (h ^ (uint32_t)(unsigned char)*b) * 16777619u;
+    return (h ^ (h >> 16)) & 0xFFFFu;
+}
+template <uint32_t V> struct Const { static constexpr uint32_t value = V; };
+}  // namespace dbg
+
+#ifdef LA_DEBUG
+extern __device__ int g_error_word;
+extern __device__ unsigned int g_debug_site;
+namespace dbg {
+__device__ __forceinline__ bool check(bool ok, uint32_t tag, uint32_t line) {
+    if (!ok) {
+        atomicCAS(&g_error_word, 0, (int)LA_ERR_BOUNDS);
+        atomicCAS(&g_debug_site, 0u, (tag << 16) | (line & 0xFFFFu));
+    }
+    return ok;
+}
+}  // namespace dbg
+#define LA_DCHECK(cond) (::la::dbg::check((cond), ::la::dbg::Const<::la::dbg::file_tag(__FILE__)>::value, __LINE__))
+#else
+#define LA_DCHECK(cond) (true)
+#endif
+
 // ------------------------------------------------------------------ launch bookkeeping
 // Every launch goes through launch_begin/launch_end so the optional per-kernel
 // timing (la_timing_enable) can bracket it with events on the launch stream.

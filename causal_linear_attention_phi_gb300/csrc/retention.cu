@@ -68,8 +68,11 @@ retention_sums_kernel(const T* __restrict__ k, const T* __restrict__ v, const fl
         for (int j = 0; j < kMaxT; ++j) s[a][j] = 0.f;
 
     const int cbeg = p * cps, cend = min(nchunks, cbeg + cps);
+
+    LA_DCHECK(p < (int)gridDim.x && cbeg < cend && cend <= nchunks && (long long)nchunks * kC < (long long)N + kC);
     for (int c = cbeg; c < cend; ++c) {
         const int c0 = c * kC, n = min(kC, N - c0);
+        LA_DCHECK(c0 >= 0 && n >= 1 && c0 + n <= N && blockIdx.y < gridDim.y);
         __syncthreads();
         load_tile(ks, ldk, kh, c0, n, Dk, false);
         load_tile(vs, ldv, vh, c0, n, Dv, false);
@@ -186,8 +189,11 @@ retention_out_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* 
         }
 
     const int cbeg = p * cps, cend = min(nchunks, cbeg + cps);
+
+    LA_DCHECK(p < (int)gridDim.x && cbeg < cend && cend <= nchunks && (long long)nchunks * kC < (long long)N + kC);
     for (int c = cbeg; c < cend; ++c) {
         const int c0 = c * kC, n = min(kC, N - c0);
+        LA_DCHECK(c0 >= 0 && n >= 1 && c0 + n <= N && blockIdx.y < gridDim.y);
         __syncthreads();
         load_tile(qs, ldk, qh, c0, n, Dk, false);
         load_tile(ks, ldk, kh, c0, n, Dk, false);

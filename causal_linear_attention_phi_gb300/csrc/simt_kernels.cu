@@ -43,8 +43,11 @@ segment_sums_kernel(const T* __restrict__ k, const T* __restrict__ v, float* __r
     float zacc = 0.f;
 
     const int cbeg = p * cps, cend = min(nchunks, cbeg + cps);
+
+    LA_DCHECK(p < (int)gridDim.x && cbeg < cend && cend <= nchunks && (long long)nchunks * kC < (long long)N + kC);
     for (int c = cbeg; c < cend; ++c) {
         const int c0 = c * kC, n = min(kC, N - c0);
+        LA_DCHECK(c0 >= 0 && n >= 1 && c0 + n <= N && blockIdx.y < gridDim.y);
         __syncthreads();
         load_tile(ks, ldk, kh, c0, n, Dk, true);
         load_tile(vs, ldv, vh, c0, n, Dv, false);
@@ -89,6 +92,7 @@ __global__ void scan_kernel(float* __restrict__ seg, float* __restrict__ totS, f
     const size_t e4 = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
     if (e4 >= E) return;
     const size_t bh = blockIdx.y;
+    if (!LA_DCHECK((E & 3) == 0 && (sv & 3) == 0 && e4 + 3 < E && P >= 1)) return;
     float* base = seg + bh * P * E + e4;
     float4 run = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int b0 = 0; b0 < P; b0 += kScanBatch) {
@@ -169,8 +173,11 @@ causal_fwd_out_kernel(const T* __restrict__ q, const T* __restrict__ k, const T*
     }
 
     const int cbeg = p * cps, cend = min(nchunks, cbeg + cps);
+
+    LA_DCHECK(p < (int)gridDim.x && cbeg < cend && cend <= nchunks && (long long)nchunks * kC < (long long)N + kC);
     for (int c = cbeg; c < cend; ++c) {
         const int c0 = c * kC, n = min(kC, N - c0);
+        LA_DCHECK(c0 >= 0 && n >= 1 && c0 + n <= N && blockIdx.y < gridDim.y);
         __syncthreads();
         load_tile(qs, ldk, qh, c0, n, Dk, true);
         load_tile(ks, ldk, kh, c0, n, Dk, true);
@@ -259,6 +266,7 @@ noncausal_apply_kernel(const T* __restrict__ q, T* __restrict__ o, const float* 
     for (int e = tid; e < Dk * Dv; e += kThreads) Ss[e] = tot[e];
     if (tid < Dk) zs[tid] = tot[(size_t)Dk * Dv + tid];
     const int c0 = blockIdx.x * kC, n = min(kC, N - c0);
+    LA_DCHECK(c0 >= 0 && n >= 1 && c0 + n <= N && blockIdx.y < gridDim.y);
     load_tile(qs, ldk, q + bh * N * Dk, c0, n, Dk, true);
     __syncthreads();
     for (int i = 0; i < kC / 16; ++i) {
@@ -338,8 +346,11 @@ bwd_forward_sweep_kernel(const T* __restrict__ q, const T* __restrict__ k, const
     }
 
     const int cbeg = p * cps, cend = min(nchunks, cbeg + cps);
+
+    LA_DCHECK(p < (int)gridDim.x && cbeg < cend && cend <= nchunks && (long long)nchunks * kC < (long long)N + kC);
     for (int c = cbeg; c < cend; ++c) {
         const int c0 = c * kC, n = min(kC, N - c0);
+        LA_DCHECK(c0 >= 0 && n >= 1 && c0 + n <= N && blockIdx.y < gridDim.y);
         __syncthreads();
         load_tile(qs, ldk, qh, c0, n, Dk, true);
         load_tile(ks, ldk, kh, c0, n, Dk, true);
@@ -549,8 +560,11 @@ bwd_reverse_sweep_kernel(const T* __restrict__ q, const T* __restrict__ k, const
     }
 
     const int cbeg = p * cps, cend = min(nchunks, cbeg + cps);
+
+    LA_DCHECK(p < (int)gridDim.x && cbeg < cend && cend <= nchunks && (long long)nchunks * kC < (long long)N + kC);
     for (int c = cend - 1; c >= cbeg; --c) {
         const int c0 = c * kC, n = min(kC, N - c0);
+        LA_DCHECK(c0 >= 0 && n >= 1 && c0 + n <= N && blockIdx.y < gridDim.y);
         __syncthreads();
         if (tid < kC) {
             const bool valid = tid < n;

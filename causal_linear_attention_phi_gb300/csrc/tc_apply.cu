@@ -76,6 +76,7 @@ tc_noncausal_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int p = blockIdx.x, bh = blockIdx.y;
     const int cbeg = p * cps, cend = min(nchunks, cbeg + cps), nloc = cend - cbeg;
+    check_plan(p, (int)gridDim.x, cbeg, cend, nchunks, N);
     const float* tot = totals + (size_t)bh * (D * D + D);  // unpadded record: S [D][D], then z [D]
 
     if (tid == 0) {
@@ -123,8 +124,8 @@ tc_noncausal_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid
                 const int s = i & 1, t0 = (cbeg + i) * kC;
                 if (!mbar_wait(&bar->q_empty[s], ((i >> 1) & 1) ^ 1, err, LA_ERR_TIMEOUT)) break;
                 mbar_arrive_expect_tx(&bar->q_full[s], kTileBytes);
-                tma_load_3d(sQ(s), &tm_q, 0, t0, bh, &bar->q_full[s]);
-                tma_load_3d(sQ(s) + kBlockBytes, &tm_q, 64, t0, bh, &bar->q_full[s]);
+                check_tile(0, t0, bh, N), tma_load_3d(sQ(s), &tm_q, 0, t0, bh, &bar->q_full[s]);
+                check_tile(64, t0, bh, N), tma_load_3d(sQ(s) + kBlockBytes, &tm_q, 64, t0, bh, &bar->q_full[s]);
                 armed[s] = i;
             }
             // never leave with copies in flight
@@ -199,8 +200,8 @@ tc_noncausal_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid
                 CG::sync();
                 if (ct == 0) mbar_arrive(&bar->o_free[sj]);
                 if (ct == kStoreThread) {
-                    tma_store_3d(&tm_out, sO(sj), 0, c0, bh);
-                    if (D > 64) tma_store_3d(&tm_out, sO(sj) + kBlockBytes, 64, c0, bh);
+                    check_tile(0, c0, bh, N), tma_store_3d(&tm_out, sO(sj), 0, c0, bh);
+                    if (D > 64) check_tile(64, c0, bh, N), tma_store_3d(&tm_out, sO(sj) + kBlockBytes, 64, c0, bh);
                     bulk_commit();
                 }
             }

@@ -109,6 +109,8 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
     const int p = blockIdx.x, bh = blockIdx.y;
     const int cbeg = p * cps, cend = min(nchunks, cbeg + cps), nloc = cend - cbeg;
     const size_t E = state_elems(kD, kD);
+    check_plan(p, P, cbeg, cend, nchunks, N);
+    record_ok(bh, p, P, E - 1, E);
 
     if (tid == 0) {
         uint64_t* b = reinterpret_cast<uint64_t*>(bar);
@@ -137,6 +139,7 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
                 const int t0 = (cbeg + i) * kC;
                 if (!mbar_wait(&bar->empty_qv, (i & 1) ^ 1, err, LA_ERR_TIMEOUT)) break;
                 mbar_arrive_expect_tx(&bar->full_qv, 3 * kTileBytes);
+                check_tile(64, t0, bh, N);
                 tma_load_3d(sQ, &tm_q, 0, t0, bh, &bar->full_qv);
                 tma_load_3d(sQ + kBlockBytes, &tm_q, 64, t0, bh, &bar->full_qv);
                 tma_load_3d(sV, &tm_v, 0, t0, bh, &bar->full_qv);
@@ -218,7 +221,7 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
         const float* pre = seg_S + ((size_t)bh * P + p) * E;
         global_row_to_tmem<64>(pre + (size_t)r * kD + 64 * h, tmem + lb + kFS);  // S_prev row r, this half
         if (ct < 128) {
-            zsh[ct] = pre[(size_t)kD * kD + ct];
+            zsh[ct] = record_ok(bh, p, P, (size_t)kD * kD + ct, E) ? pre[(size_t)kD * kD + ct] : 0.f;
             racc[ct] = 0.f;
         }
         if (D <= 64) {  // phi leaves the lo tile's upper column block unwritten: keep it zero
@@ -351,7 +354,8 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
             const float g = valid ? -(tpart[r] + tpart[128 + r]) * inv : 0.f;
             if (h == 0) {
                 gsh[r] = g;
-                if (valid) *reinterpret_cast<float2*>(dgh + (size_t)(c0 + r) * 2) = make_float2(den, g);
+                if (valid && LA_DCHECK(c0 + r < N))
+                    *reinterpret_cast<float2*>(dgh + (size_t)(c0 + r) * 2) = make_float2(den, g);
             }
             tc_fence_before();
             FG::sync();
@@ -450,6 +454,7 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
             tc_fence_before();
             FG::sync();  // the dq tile is complete and z_prev has been used by every thread
             if (ct == kStoreThread) {
+                check_tile(D > 64 ? 64 : 0, c0, bh, N);
                 tma_store_3d(&tm_dq, sSb, 0, c0, bh);
                 if (D > 64) tma_store_3d(&tm_dq, sSb + kBlockBytes, 64, c0, bh);
                 bulk_commit();
@@ -465,7 +470,7 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
             tc_fence_after();
             float* out = seg_R + ((size_t)bh * P + p) * E;
             tmem_row_to_global<64>(tmem + lb + kFR, out + (size_t)r * kD + 64 * h);
-            if (ct < 128) out[(size_t)kD * kD + ct] = racc[ct];
+            if (ct < 128 && record_ok(bh, p, P, (size_t)kD * kD + ct, E)) out[(size_t)kD * kD + ct] = racc[ct];
         }
         tc_fence_before();
     }
@@ -532,6 +537,8 @@ tc_bwd_reverse_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
     const int p = blockIdx.x, bh = blockIdx.y;
     const int cbeg = p * cps, cend = min(nchunks, cbeg + cps), nloc = cend - cbeg;
     const size_t E = state_elems(kD, kD);
+    check_plan(p, P, cbeg, cend, nchunks, N);
+    record_ok(bh, p, P, E - 1, E);
 
     if (tid == 0) {
         uint64_t* b = reinterpret_cast<uint64_t*>(bar);
@@ -560,6 +567,7 @@ tc_bwd_reverse_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
                 const int t0 = (cend - 1 - i) * kC;
                 if (!mbar_wait(&bar->empty, (i & 1) ^ 1, err, LA_ERR_TIMEOUT)) break;
                 mbar_arrive_expect_tx(&bar->full, 4 * kTileBytes);
+                check_tile(64, t0, bh, N);
                 tma_load_3d(sQ, &tm_q, 0, t0, bh, &bar->full);
                 tma_load_3d(sQ + kBlockBytes, &tm_q, 64, t0, bh, &bar->full);
                 tma_load_3d(sK, &tm_k, 0, t0, bh, &bar->full);
@@ -624,15 +632,16 @@ tc_bwd_reverse_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
         const uint32_t lb = lane0 + 32 * qt;
         const float* suf = seg_R + ((size_t)bh * P + p) * E;
         global_row_to_tmem<32>(suf + (size_t)r * kD + 32 * qt, tmem + lb + kRR);  // R_next row r, this quarter
-        if (ct < 128) rsh[ct] = suf[(size_t)kD * kD + ct];
+        if (ct < 128) rsh[ct] = record_ok(bh, p, P, (size_t)kD * kD + ct, E) ? suf[(size_t)kD * kD + ct] : 0.f;
         tc_fence_before();
         bool ok = RG::all(true);
         const float* dgh = den_g + (size_t)bh * N * 2;
         // (den, g) of row ct of chunk ii (rows past N: den 1, g 0); loaded one chunk ahead
         auto load_dg = [&](int ii) {
             const int cc = (cend - 1 - ii) * kC;
-            return ct < min(kC, N - cc) ? *reinterpret_cast<const float2*>(dgh + (size_t)(cc + ct) * 2)
-                                        : make_float2(1.f, 0.f);
+            return ct < min(kC, N - cc) && LA_DCHECK(cc + ct < N && cc >= 0)
+                       ? *reinterpret_cast<const float2*>(dgh + (size_t)(cc + ct) * 2)
+                       : make_float2(1.f, 0.f);
         };
         float2 dg_next = make_float2(1.f, 0.f);
         if (ct < 128 && nloc > 0) dg_next = load_dg(0);
@@ -749,6 +758,7 @@ tc_bwd_reverse_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
             tc_fence_before();
             RG::sync();
             if (ct == kStoreThread) {
+                check_tile(D > 64 ? 64 : 0, c0, bh, N);
                 tma_store_3d(&tm_dk, sKc, 0, c0, bh);
                 tma_store_3d(&tm_dv, sRb, 0, c0, bh);
                 if (D > 64) {

@@ -34,7 +34,25 @@ __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, int kk) {
 
 // Byte offset of logical 16-byte chunk lc (0..15, 8 columns each) of `row`.
 __device__ __forceinline__ int chunk_off(int row, int lc) {
+    LA_DCHECK(row >= 0 && row < kC && lc >= 0 && lc < 16);
     return (lc >> 3) * kBlockBytes + row * 128 + (((lc & 7) ^ (row & 7)) << 4);
+}
+
+// Debug build: the work split of a chunked kernel launched on a (P, BH) grid: this CTA's
+// segment p holds chunks [cbeg, cend) of a head, all starting inside the sequence.
+__device__ __forceinline__ void check_plan(int p, int P, int cbeg, int cend, int nchunks, int N) {
+    LA_DCHECK(p >= 0 && p < P && (int)gridDim.x == P && blockIdx.y < gridDim.y && cbeg >= 0 && cbeg < cend &&
+              cend <= nchunks && (long long)(cend - 1) * kC < N && (long long)nchunks * kC < (long long)N + kC);
+}
+// Debug build: a TMA tile (x, row) of head bh of a [BH][N][D] map: x a multiple of 8
+// elements (16 bytes) inside the 128-wide tile, the first row inside the sequence.  TMA
+// clips rows past N by itself; the check catches a wrong coordinate.
+__device__ __forceinline__ void check_tile(int x, int row, int bh, int N) {
+    LA_DCHECK(x >= 0 && (x & 7) == 0 && x < kD && row >= 0 && row < N && bh >= 0 && bh < (int)gridDim.y);
+}
+// Debug build: a state record index (head bh, segment p of P) and an element offset in it.
+__device__ __forceinline__ bool record_ok(int bh, int p, int P, size_t off, size_t E) {
+    return LA_DCHECK(bh >= 0 && bh < (int)gridDim.y && p >= 0 && p < P && off < E);
 }
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
@@ -127,6 +145,7 @@ struct Grp {
     __device__ static __forceinline__ int vec_block(int j) { return j / (kJ / 2); }
     __device__ static __forceinline__ int vec_row(int ct, int j) { return ((ct >> 3) + (G / 8) * (j % (kJ / 2))) & 127; }
     __device__ static __forceinline__ int vec_off(int ct, int j) {
+        LA_DCHECK(ct >= 0 && ct < G && j >= 0 && j < kJ);
         return vec_block(j) * kBlockBytes + vec_row(ct, j) * 128 + (ct & 7) * 16;
     }
     __device__ static __forceinline__ int vec_lc(int ct) { return (ct & 7) ^ ((ct >> 3) & 7); }

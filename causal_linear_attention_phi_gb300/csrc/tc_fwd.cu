@@ -100,6 +100,8 @@ tc_causal_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     const int cbeg = p * cps, cend = min(nchunks, cbeg + cps), nloc = cend - cbeg;
     const size_t E = state_elems(kD, kD);
     float* segp = seg + ((size_t)bh * P + p) * E;
+    check_plan(p, P, cbeg, cend, nchunks, N);
+    record_ok(bh, p, P, E - 1, E);
     // K and V stage s live at K0 + s * kTileBytes and V0 + s * kTileBytes
     auto sK = [&](int s) { return base + SmemLayout::K0 + s * kTileBytes; };
     auto sV = [&](int s) { return base + SmemLayout::V0 + s * kTileBytes; };
@@ -154,6 +156,7 @@ tc_causal_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                 ok = mbar_wait(&bar->kv_empty[s], ((i >> 1) & 1) ^ 1, err, LA_ERR_TIMEOUT);
                 if (!ok) break;
                 mbar_arrive_expect_tx(&bar->kv_full[s], 2 * kTileBytes);
+                check_tile(64, t0, bh, N);
                 tma_load_3d(sK(s), &tm_k, 0, t0, bh, &bar->kv_full[s]);
                 tma_load_3d(sK(s) + kBlockBytes, &tm_k, 64, t0, bh, &bar->kv_full[s]);
                 tma_load_3d(sV(s), &tm_v, 0, t0, bh, &bar->kv_full[s]);
@@ -256,7 +259,7 @@ tc_causal_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             }
             if (h == 0) {
                 uint32_t zw[16];
-                const uint32_t zv = __float_as_uint(segp[(size_t)kD * kD + r]);
+                const uint32_t zv = record_ok(bh, p, P, (size_t)kD * kD + r, E) ? __float_as_uint(segp[(size_t)kD * kD + r]) : 0u;
 #pragma unroll
                 for (int x = 0; x < 16; ++x) zw[x] = zv;
                 tmem_st16(tmem + lane_base + kTmZ, zw);
@@ -378,6 +381,7 @@ tc_causal_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             tc_fence_before();
             CG::sync();
             if (ct == kStoreThread) {
+                check_tile(D > 64 ? 64 : 0, c0, bh, N);
                 tma_store_3d(&tm_o, sSb, 0, c0, bh);
                 if (D > 64) tma_store_3d(&tm_o, sSb + kBlockBytes, 64, c0, bh);
                 bulk_commit();
@@ -405,7 +409,7 @@ tc_causal_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                     uint32_t zv[16];
                     tmem_ld16(tmem + lane_base + kTmZ, zv);
                     tmem_ld_wait();
-                    segp[(size_t)kD * kD + r] = __uint_as_float(zv[0]);
+                    if (record_ok(bh, p, P, (size_t)kD * kD + r, E)) segp[(size_t)kD * kD + r] = __uint_as_float(zv[0]);
                 }
             }
         }

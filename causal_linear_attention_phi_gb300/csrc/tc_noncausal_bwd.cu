@@ -92,6 +92,7 @@ tc_noncausal_bwd_query_kernel(const __grid_constant__ CUtensorMap tm_q, const __
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int p = blockIdx.x, bh = blockIdx.y;
     const int cbeg = p * cps, cend = min(nchunks, cbeg + cps), nloc = cend - cbeg;
+    check_plan(p, (int)gridDim.x, cbeg, cend, nchunks, N);
     const float* tot = totS + (size_t)bh * kE;
 
     if (tid == 0) {
@@ -141,13 +142,13 @@ tc_noncausal_bwd_query_kernel(const __grid_constant__ CUtensorMap tm_q, const __
                 const int t0 = (cbeg + i) * kC, b = i & 1;
                 if (!mbar_wait(&bar->empty_q[b], ((i >> 1) & 1) ^ 1, err, LA_ERR_TIMEOUT)) break;
                 mbar_arrive_expect_tx(&bar->full_q[b], kTileBytes);
-                tma_load_3d(sQb(b), &tm_q, 0, t0, bh, &bar->full_q[b]);
-                tma_load_3d(sQb(b) + kBlockBytes, &tm_q, 64, t0, bh, &bar->full_q[b]);
+                check_tile(0, t0, bh, N), tma_load_3d(sQb(b), &tm_q, 0, t0, bh, &bar->full_q[b]);
+                check_tile(64, t0, bh, N), tma_load_3d(sQb(b) + kBlockBytes, &tm_q, 64, t0, bh, &bar->full_q[b]);
                 armed_q[b] = i;
                 if (!mbar_wait(&bar->empty_p, (i & 1) ^ 1, err, LA_ERR_TIMEOUT)) break;
                 mbar_arrive_expect_tx(&bar->full_p, kTileBytes);
-                tma_load_3d(sP, &tm_do, 0, t0, bh, &bar->full_p);
-                tma_load_3d(sP + kBlockBytes, &tm_do, 64, t0, bh, &bar->full_p);
+                check_tile(0, t0, bh, N), tma_load_3d(sP, &tm_do, 0, t0, bh, &bar->full_p);
+                check_tile(64, t0, bh, N), tma_load_3d(sP + kBlockBytes, &tm_do, 64, t0, bh, &bar->full_p);
                 armed_p = i;
             }
             // no copy may still be landing when the CTA exits
@@ -326,8 +327,8 @@ tc_noncausal_bwd_query_kernel(const __grid_constant__ CUtensorMap tm_q, const __
                 mbar_arrive(&bar->empty_q[i & 1]);
             }
             if (ct == kStoreThread) {
-                tma_store_3d(&tm_dq, sOb, 0, c0, bh);
-                if (D > 64) tma_store_3d(&tm_dq, sOb + kBlockBytes, 64, c0, bh);
+                check_tile(0, c0, bh, N), tma_store_3d(&tm_dq, sOb, 0, c0, bh);
+                if (D > 64) check_tile(64, c0, bh, N), tma_store_3d(&tm_dq, sOb + kBlockBytes, 64, c0, bh);
                 bulk_commit();
             }
             if (ct < kD) racc[ct] += CG::column_sum(drpart, ct);
@@ -395,6 +396,7 @@ tc_noncausal_bwd_key_kernel(const __grid_constant__ CUtensorMap tm_k, const __gr
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int p = blockIdx.x, bh = blockIdx.y;
     const int cbeg = p * cps, cend = min(nchunks, cbeg + cps), nloc = cend - cbeg;
+    check_plan(p, (int)gridDim.x, cbeg, cend, nchunks, N);
     const float* tot = totR + (size_t)bh * kE;
 
     if (tid == 0) {
@@ -436,10 +438,10 @@ tc_noncausal_bwd_key_kernel(const __grid_constant__ CUtensorMap tm_k, const __gr
                 const int t0 = (cbeg + i) * kC, b = i & 1;
                 if (!mbar_wait(&bar->empty[b], ((i >> 1) & 1) ^ 1, err, LA_ERR_TIMEOUT)) break;
                 mbar_arrive_expect_tx(&bar->full[b], 2 * kTileBytes);
-                tma_load_3d(sKb(b), &tm_k, 0, t0, bh, &bar->full[b]);
-                tma_load_3d(sKb(b) + kBlockBytes, &tm_k, 64, t0, bh, &bar->full[b]);
-                tma_load_3d(sVb(b), &tm_v, 0, t0, bh, &bar->full[b]);
-                tma_load_3d(sVb(b) + kBlockBytes, &tm_v, 64, t0, bh, &bar->full[b]);
+                check_tile(0, t0, bh, N), tma_load_3d(sKb(b), &tm_k, 0, t0, bh, &bar->full[b]);
+                check_tile(64, t0, bh, N), tma_load_3d(sKb(b) + kBlockBytes, &tm_k, 64, t0, bh, &bar->full[b]);
+                check_tile(0, t0, bh, N), tma_load_3d(sVb(b), &tm_v, 0, t0, bh, &bar->full[b]);
+                check_tile(64, t0, bh, N), tma_load_3d(sVb(b) + kBlockBytes, &tm_v, 64, t0, bh, &bar->full[b]);
                 armed[b] = i;
             }
             // no copy may still be landing when the CTA exits
@@ -532,11 +534,11 @@ tc_noncausal_bwd_key_kernel(const __grid_constant__ CUtensorMap tm_k, const __gr
                 mbar_arrive(&bar->empty[b]);
             }
             if (ct == kStoreThread) {
-                tma_store_3d(&tm_dk, sOk, 0, c0, bh);
-                tma_store_3d(&tm_dv, sOv, 0, c0, bh);
+                check_tile(0, c0, bh, N), tma_store_3d(&tm_dk, sOk, 0, c0, bh);
+                check_tile(0, c0, bh, N), tma_store_3d(&tm_dv, sOv, 0, c0, bh);
                 if (D > 64) {
-                    tma_store_3d(&tm_dk, sOk + kBlockBytes, 64, c0, bh);
-                    tma_store_3d(&tm_dv, sOv + kBlockBytes, 64, c0, bh);
+                    check_tile(64, c0, bh, N), tma_store_3d(&tm_dk, sOk + kBlockBytes, 64, c0, bh);
+                    check_tile(64, c0, bh, N), tma_store_3d(&tm_dv, sOv + kBlockBytes, 64, c0, bh);
                 }
                 bulk_commit();
             }

@@ -116,6 +116,7 @@ tc_retention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int p = blockIdx.x, bh = blockIdx.y;
     const int cbeg = p * cps, cend = min(nchunks, cbeg + cps), nloc = cend - cbeg;
+    check_plan(p, (int)gridDim.x, cbeg, cend, nchunks, N);
     float* segp = seg + ((size_t)bh * P + p) * (size_t)(kD * kD);
     auto sK = [&](int s) { return base + SmemLayout::K0 + s * kTileBytes; };
     auto sV = [&](int s) { return base + SmemLayout::V0 + s * kTileBytes; };
@@ -156,17 +157,17 @@ tc_retention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 ok = mbar_wait(&bar->kv_empty[s], ((i >> 1) & 1) ^ 1, err, LA_ERR_TIMEOUT);
                 if (!ok) break;
                 mbar_arrive_expect_tx(&bar->kv_full[s], 2 * kTileBytes);
-                tma_load_3d(sK(s), &tm_k, 0, t0, bh, &bar->kv_full[s]);
-                tma_load_3d(sK(s) + kBlockBytes, &tm_k, 64, t0, bh, &bar->kv_full[s]);
-                tma_load_3d(sV(s), &tm_v, 0, t0, bh, &bar->kv_full[s]);
-                tma_load_3d(sV(s) + kBlockBytes, &tm_v, 64, t0, bh, &bar->kv_full[s]);
+                check_tile(0, t0, bh, N), tma_load_3d(sK(s), &tm_k, 0, t0, bh, &bar->kv_full[s]);
+                check_tile(64, t0, bh, N), tma_load_3d(sK(s) + kBlockBytes, &tm_k, 64, t0, bh, &bar->kv_full[s]);
+                check_tile(0, t0, bh, N), tma_load_3d(sV(s), &tm_v, 0, t0, bh, &bar->kv_full[s]);
+                check_tile(64, t0, bh, N), tma_load_3d(sV(s) + kBlockBytes, &tm_v, 64, t0, bh, &bar->kv_full[s]);
                 armed_kv[s] = i;
                 if (kOut) {
                     ok = mbar_wait(&bar->q_empty, (i & 1) ^ 1, err, LA_ERR_TIMEOUT);
                     if (!ok) break;
                     mbar_arrive_expect_tx(&bar->q_full, kTileBytes);
-                    tma_load_3d(sQ, &tm_q, 0, t0, bh, &bar->q_full);
-                    tma_load_3d(sQ + kBlockBytes, &tm_q, 64, t0, bh, &bar->q_full);
+                    check_tile(0, t0, bh, N), tma_load_3d(sQ, &tm_q, 0, t0, bh, &bar->q_full);
+                    check_tile(64, t0, bh, N), tma_load_3d(sQ + kBlockBytes, &tm_q, 64, t0, bh, &bar->q_full);
                     armed_q = i;
                 }
             }
@@ -338,8 +339,8 @@ tc_retention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             CG::sync();
             if (ct == 0) mbar_arrive(&bar->o_free);
             if (ct == kStoreThread) {
-                tma_store_3d(&tm_o, sSb, 0, c0, bh);
-                if (D > 64) tma_store_3d(&tm_o, sSb + kBlockBytes, 64, c0, bh);
+                check_tile(0, c0, bh, N), tma_store_3d(&tm_o, sSb, 0, c0, bh);
+                if (D > 64) check_tile(64, c0, bh, N), tma_store_3d(&tm_o, sSb + kBlockBytes, 64, c0, bh);
                 bulk_commit();
             }
         }

@@ -59,7 +59,9 @@ typedef enum {
     LA_ERR_UNSUPPORTED = 2,  /* Dk or Dv not in {16, 32, 64, 128}, B*H > 65535, or not an sm_103 device */
     LA_ERR_WORKSPACE = 3,    /* ws_bytes smaller than la_workspace_bytes(), or ws NULL */
     LA_ERR_CUDA = 4,         /* a CUDA runtime call or kernel launch failed */
-    LA_ERR_TIMEOUT = 5       /* a bounded device-side wait ran out (read via la_last_error) */
+    LA_ERR_TIMEOUT = 5,      /* a bounded device-side wait ran out (read via la_last_error) */
+    LA_ERR_BOUNDS = 6        /* debug builds only: a device-side index check failed and the access
+                                was skipped (read via la_last_error; la_error_detail names the site) */
 } la_status;
 
 typedef enum { LA_F32 = 0, LA_BF16 = 1 } la_dtype;
@@ -275,7 +277,9 @@ la_status la_causal_fwd_noalloc(const void* q, const void* k, const void* v, voi
 
 /*
  * Sticky device-side status: LA_OK, or the first error a kernel recorded since
- * the last la_clear_error() (LA_ERR_TIMEOUT for a bounded wait that ran out).
+ * the last la_clear_error() (LA_ERR_TIMEOUT for a bounded wait that ran out;
+ * LA_ERR_BOUNDS for a failed index check of the debug build, whose source file
+ * and line la_error_detail() then gives).
  * It reads device memory synchronously (the current device is synchronised);
  * call it after the stream work has finished.  la_clear_error() resets it.
  */
@@ -299,7 +303,13 @@ const char* la_status_string(la_status st);
 /* Text of the most recent host-side failure on the calling thread ("" if none). */
 const char* la_error_detail(void);
 
-/* Library version, e.g. "0.1.0". */
+/*
+ * Library version, e.g. "0.1.1".  A build with device-side bounds checks (the
+ * debug build: every plain global-memory access, segment record, TMA tile
+ * coordinate and shared-memory tile offset of the kernels is checked against
+ * the extents of its tensor, and a failed check records LA_ERR_BOUNDS and skips
+ * the access instead of trapping) reports "<version>-debug".
+ */
 const char* la_version(void);
 
 /*

@@ -163,3 +163,22 @@ def test_bench_refuses_a_gpu_count_it_was_not_launched_with():
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "2", "--steps", "1"],
                        capture_output=True, text=True, env=env, timeout=300)
     assert r.returncode != 0 and "WORLD_SIZE=1" in r.stderr
+
+
+def test_debug_build_flag_reaches_nvcc_and_the_library():
+    """build_library(debug=True) compiles with -DLA_DEBUG (and relocatable device code, so the
+    checks of every translation unit reach one error word) into a library that reports a
+    '-debug' version; the regular library does not."""
+    from causal_linear_attention_phi_gb300 import build
+    cmd = build.nvcc_command("x.cu", "x.o", debug=True)
+    assert "-DLA_DEBUG" in cmd and "-rdc=true" in cmd
+    assert "-DLA_DEBUG" not in build.nvcc_command("x.cu", "x.o")
+    path = build.build_library(debug=True)
+    lib = ctypes.CDLL(path)
+    lib.la_version.restype = ctypes.c_char_p
+    assert lib.la_version().decode().endswith("-debug")
+    reg = ctypes.CDLL(build.build_library())
+    reg.la_version.restype = ctypes.c_char_p
+    assert not reg.la_version().decode().endswith("-debug")
+    lib.la_status_string.restype = ctypes.c_char_p
+    assert b"LA_ERR_BOUNDS" in lib.la_status_string(6)
