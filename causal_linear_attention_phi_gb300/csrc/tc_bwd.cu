@@ -13,8 +13,12 @@
 // Forward sweep kernel: chunks in order, S and the segment's R contribution in
 // TMEM; recomputes num and den as the forward does, derives P and g (g from the
 // bf16 P the products use), writes dq and the per-position (den, g).  dq is the
-// difference of two terms that nearly cancel when phi(k) varies little, so D
-// enters as a hi + lo pair of bf16 operands and phi(K) as hi + lo in D K~.
+// difference of two terms that nearly cancel when phi(k) varies little, so two
+// products carry more than bf16: A = tril(Q~ K~^T), whose entries sit near the
+// head size (so a bf16 copy loses their variation), enters A V as a hi + lo pair,
+// and D K~ is formed as rowsum(D) 1^T + D (K~ - 1): the row sums exact in fp32,
+// the product on a bf16 copy of D and a bf16 copy of phi(K) - 1, which is small
+// where phi(k) is near 1 and so keeps its low bits.
 // Reverse sweep kernel: chunks in reverse order with R_next in TMEM; every
 // product is taken with the keys as the M (TMEM lane) dimension so dk and dv
 // come out row by row.  1/den is folded into the query operand, Q' = phi(Q) /
@@ -40,11 +44,11 @@ constexpr int kThreadsFS = 64 + 256, kThreadsRS = 64 + 512;  // + the TMA and MM
 
 // ------------------------------------------------------------------ forward sweep
 // TMEM: S [0,128) fp32 state; R [128,256) segment sum of phi(q) P^T;
-// X [256,384): QK^T fp32 -> A bf16 -> P V^T fp32 -> D as bf16 hi + lo.  Each 32-key
+// X [256,384): QK^T fp32 -> A as bf16 hi + lo -> P V^T fp32 -> D bf16.  Each 32-key
 // block b of fp32 columns X[32b, 32b+32) is rewritten in place by the thread that
-// read it: A (bf16 pairs) in X[32b, 32b+16), D_hi there and D_lo in X[32b+16, 32b+32);
-// so the MMA's A operand for K step kk (keys 16kk..16kk+15) sits at column
-// 32 (kk / 2) + 8 (kk % 2) (+16 for D_lo).
+// read it: A_hi (bf16 pairs) in X[32b, 32b+16) and A_lo in X[32b+16, 32b+32), later
+// D in X[32b, 32b+16); so the MMA's A operand for K step kk (keys 16kk..16kk+15)
+// sits at column 32 (kk / 2) + 8 (kk % 2) (+16 for A_lo).
 // Y [384,512): O = phi(Q) S_prev + A V (numerator) -> dQ~.
 constexpr uint32_t kFS = 0, kFR = 128, kFX = 256, kFY = 384;
 __device__ __forceinline__ uint32_t xcol(int kk) { return 32 * (kk >> 1) + 8 * (kk & 1); }
@@ -61,6 +65,7 @@ struct FwdSweepBars {
 };
 
 struct FwdSweepSmem {
+    // KLo: bf16(phi(K) - 1), the operand of D (K~ - 1)
     static constexpr int Q = 0, K = kTileBytes, KLo = 2 * kTileBytes, V = 3 * kTileBytes, P = 4 * kTileBytes;
     static constexpr int Sb = 5 * kTileBytes;   // bf16 S_prev; after the dq products, the dq tile for the TMA store
     static constexpr int zsh = 6 * kTileBytes;  // float[128] z_prev
@@ -68,7 +73,7 @@ struct FwdSweepSmem {
     static constexpr int racc = zpart + 4096;   // float[128] segment sum of g phi(q)
     static constexpr int drpart = racc + 512;   // float[8][128] per-warp column sums of this chunk's g phi(q)
     static constexpr int gsh = drpart + 4096;   // float[128] g of the chunk's rows
-    static constexpr int rpart = gsh + 512;     // float[2][128] row sums of A, per column half
+    static constexpr int rpart = gsh + 512;     // float[2][128] row sums of A, later of D, per column half
     static constexpr int dpart = rpart + 1024;  // float[2][128] phi(q) . z_prev, per column half
     static constexpr int tpart = dpart + 1024;  // float[2][128] P . num, per column half
     static constexpr int bars = tpart + 1024;
@@ -180,8 +185,10 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
                 if (!mbar_wait(&bar->a_ready, ph, err, LA_ERR_TIMEOUT)) break;
                 tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)  // Y += A V
+                for (int kk = 0; kk < 8; ++kk) {  // Y += A V as A_hi V + A_lo V
                     mma_ts(tmem + kFY, tmem + kFX + xcol(kk), desc_mnmajor(aV, kk), id_kmn, 1);
+                    mma_ts(tmem + kFY, tmem + kFX + xcol(kk) + 16, desc_mnmajor(aV, kk), id_kmn, 1);
+                }
                 mma_commit(&bar->o_done);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)  // S += K~^T V
@@ -202,13 +209,10 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
                 if (!mbar_wait(&bar->d_ready, ph, err, LA_ERR_TIMEOUT)) break;
                 tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {  // Y += D K~ as D_hi K_hi + D_lo K_hi + D_hi K_lo
-                    mma_ts(tmem + kFY, tmem + kFX + xcol(kk), desc_mnmajor(aK, kk), id_kmn, 1);
-                    mma_ts(tmem + kFY, tmem + kFX + xcol(kk) + 16, desc_mnmajor(aK, kk), id_kmn, 1);
+                for (int kk = 0; kk < 8; ++kk)  // Y += D (K~ - 1); the rowsum(D) 1^T part is added in fp32
                     mma_ts(tmem + kFY, tmem + kFX + xcol(kk), desc_mnmajor(aKLo, kk), id_kmn, 1);
-                }
                 mma_commit(&bar->dq_done);
-                mma_commit(&bar->empty_k);  // last read of K and K_lo
+                mma_commit(&bar->empty_k);  // last read of K and K~ - 1
             }
             mma_commit(&bar->final_mma);
             mbar_wait(&bar->final_mma, 0, err, LA_ERR_TIMEOUT);
@@ -248,9 +252,10 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
             fence_proxy_async_smem();
             FG::sync();
             if (ct == 0) mbar_arrive(&bar->sb_ready);
-            // (b) phi on K: hi in place, lo beside it, per-warp column sums of hi into zpart
+            // (b) phi on K: bf16 phi(K) in place, bf16(phi(K) - 1) beside it, per-warp column
+            // sums of the bf16 phi(K) into zpart
             if (!FG::all(mbar_wait(&bar->full_k, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
-            FG::phi_tile(sK, sKLo, ct, n, D, nullptr, zpart);
+            FG::phi_tile<true>(sK, sKLo, ct, n, D, nullptr, zpart);
             fence_proxy_async_smem();
             FG::sync();
             if (ct == 0) mbar_arrive(&bar->qk_ready);
@@ -274,7 +279,8 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
                 }
                 dpart[128 * h + r] = di;
             }
-            // (c) A = tril(QK^T) on this thread's keys [64h, 64h+64), in place (see the X layout)
+            // (c) A = tril(QK^T) as bf16 hi + lo on this thread's keys [64h, 64h+64), in place
+            // (see the X layout); the row sums of hi + lo (the operands A V uses) go to den
             if (!FG::all(mbar_wait(&bar->qk_done, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
             tc_fence_after();
             {
@@ -282,10 +288,10 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
 #pragma unroll
                 for (int cb = 0; cb < 2; ++cb) {
                     const int j0 = 64 * h + 32 * cb;
-                    uint32_t pk[16];
+                    uint32_t hi[16], lo[16];
                     if (j0 > r) {
 #pragma unroll
-                        for (int x = 0; x < 16; ++x) pk[x] = 0u;
+                        for (int x = 0; x < 16; ++x) hi[x] = lo[x] = 0u;
                     } else {
                         uint32_t w[32];
                         tmem_ld32(tmem + lb + kFX + 32 * cb, w);
@@ -293,20 +299,25 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
                         if (j0 + 31 < (r & ~31)) {  // below the diagonal for the whole warp: no mask
 #pragma unroll
                             for (int x = 0; x < 16; ++x) {
-                                pk[x] = pack_bf16x2(__uint_as_float(w[2 * x]), __uint_as_float(w[2 * x + 1]));
-                                rs += bf_lo(pk[x]) + bf_hi(pk[x]);
+                                const float a0 = __uint_as_float(w[2 * x]), a1 = __uint_as_float(w[2 * x + 1]);
+                                hi[x] = pack_bf16x2(a0, a1);
+                                lo[x] = pack_bf16x2(a0 - bf_lo(hi[x]), a1 - bf_hi(hi[x]));
+                                rs += (bf_lo(hi[x]) + bf_lo(lo[x])) + (bf_hi(hi[x]) + bf_hi(lo[x]));
                             }
                         } else {
 #pragma unroll
                             for (int x = 0; x < 16; ++x) {
                                 const int j = j0 + 2 * x;
-                                pk[x] = pack_bf16x2(j <= r ? __uint_as_float(w[2 * x]) : 0.f,
-                                                    j + 1 <= r ? __uint_as_float(w[2 * x + 1]) : 0.f);
-                                rs += bf_lo(pk[x]) + bf_hi(pk[x]);
+                                const float a0 = j <= r ? __uint_as_float(w[2 * x]) : 0.f;
+                                const float a1 = j + 1 <= r ? __uint_as_float(w[2 * x + 1]) : 0.f;
+                                hi[x] = pack_bf16x2(a0, a1);
+                                lo[x] = pack_bf16x2(a0 - bf_lo(hi[x]), a1 - bf_hi(hi[x]));
+                                rs += (bf_lo(hi[x]) + bf_lo(lo[x])) + (bf_hi(hi[x]) + bf_hi(lo[x]));
                             }
                         }
                     }
-                    tmem_st16(tmem + lb + kFX + 32 * cb, pk);
+                    tmem_st16(tmem + lb + kFX + 32 * cb, hi);
+                    tmem_st16(tmem + lb + kFX + 32 * cb + 16, lo);
                 }
                 rpart[128 * h + r] = rs;
                 tmem_st_wait();
@@ -382,50 +393,55 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
             }
             FG::sync();  // every read of Q by the compute group is done
             if (ct == 0) mbar_arrive(&bar->empty_qv);
-            // (e) D = tril(P V^T + g) as bf16 hi + lo on this thread's keys, in place (see the X layout)
+            // (e) D = tril(P V^T + g) as one bf16 copy on this thread's keys, in place (see the X
+            // layout); its fp32 row sums (this half) into rpart for the rowsum(D) 1^T part of D K~
             if (!FG::all(mbar_wait(&bar->pv_done, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
             tc_fence_after();
+            {
+                float ds = 0.f;
 #pragma unroll
-            for (int cb = 0; cb < 2; ++cb) {
-                const int j0 = 64 * h + 32 * cb;
-                uint32_t hi[16], lo[16];
-                if (j0 > r) {
+                for (int cb = 0; cb < 2; ++cb) {
+                    const int j0 = 64 * h + 32 * cb;
+                    uint32_t hi[16];
+                    if (j0 > r) {
 #pragma unroll
-                    for (int x = 0; x < 16; ++x) hi[x] = lo[x] = 0u;
-                } else {
-                    uint32_t w[32];
-                    tmem_ld32(tmem + lb + kFX + 32 * cb, w);
-                    tmem_ld_wait();
-                    if (j0 + 31 < (r & ~31)) {  // below the diagonal for the whole warp: no mask
-#pragma unroll
-                        for (int x = 0; x < 16; ++x) {
-                            const float d0 = __uint_as_float(w[2 * x]) + g, d1 = __uint_as_float(w[2 * x + 1]) + g;
-                            hi[x] = pack_bf16x2(d0, d1);
-                            lo[x] = pack_bf16x2(d0 - bf_lo(hi[x]), d1 - bf_hi(hi[x]));
-                        }
+                        for (int x = 0; x < 16; ++x) hi[x] = 0u;
                     } else {
+                        uint32_t w[32];
+                        tmem_ld32(tmem + lb + kFX + 32 * cb, w);
+                        tmem_ld_wait();
+                        if (j0 + 31 < (r & ~31)) {  // below the diagonal for the whole warp: no mask
 #pragma unroll
-                        for (int x = 0; x < 16; ++x) {
-                            const int j = j0 + 2 * x;
-                            const float d0 = j <= r ? __uint_as_float(w[2 * x]) + g : 0.f;
-                            const float d1 = j + 1 <= r ? __uint_as_float(w[2 * x + 1]) + g : 0.f;
-                            hi[x] = pack_bf16x2(d0, d1);
-                            lo[x] = pack_bf16x2(d0 - bf_lo(hi[x]), d1 - bf_hi(hi[x]));
+                            for (int x = 0; x < 16; ++x) {
+                                const float d0 = __uint_as_float(w[2 * x]) + g, d1 = __uint_as_float(w[2 * x + 1]) + g;
+                                hi[x] = pack_bf16x2(d0, d1);
+                                ds += d0 + d1;
+                            }
+                        } else {
+#pragma unroll
+                            for (int x = 0; x < 16; ++x) {
+                                const int j = j0 + 2 * x;
+                                const float d0 = j <= r ? __uint_as_float(w[2 * x]) + g : 0.f;
+                                const float d1 = j + 1 <= r ? __uint_as_float(w[2 * x + 1]) + g : 0.f;
+                                hi[x] = pack_bf16x2(d0, d1);
+                                ds += d0 + d1;
+                            }
                         }
                     }
+                    tmem_st16(tmem + lb + kFX + 32 * cb, hi);
                 }
-                tmem_st16(tmem + lb + kFX + 32 * cb, hi);
-                tmem_st16(tmem + lb + kFX + 32 * cb + 16, lo);
+                rpart[128 * h + r] = ds;
             }
             tmem_st_wait();
             tc_fence_before();
             FG::sync();
             if (ct == 0) mbar_arrive(&bar->d_ready);
-            // (f) dq = (dQ~ + g z_prev) * phi'(q), this thread's 64 columns, staged in the Sb
-            // tile (free once the dq products are done) and written by one TMA store
+            // (f) dq = (dQ~ + rowsum(D) + g z_prev) * phi'(q), this thread's 64 columns, staged in
+            // the Sb tile (free once the dq products are done) and written by one TMA store
             // (rows past N are not written)
             if (!FG::all(mbar_wait(&bar->dq_done, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
             tc_fence_after();
+            const float dsum = rpart[r] + rpart[128 + r];
 #pragma unroll
             for (int cb = 0; cb < 2; ++cb) {
                 uint32_t w[32];
@@ -442,9 +458,10 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
                         *reinterpret_cast<const float4*>(zsh + 64 * h + 32 * cb + 8 * c4 + 4);
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const float a0 = (__uint_as_float(w[8 * c4 + 2 * e]) + g * zr[2 * e]) * dphi_from_phi(bf_lo(qu[e]));
-                        const float a1 =
-                            (__uint_as_float(w[8 * c4 + 2 * e + 1]) + g * zr[2 * e + 1]) * dphi_from_phi(bf_hi(qu[e]));
+                        const float a0 = (__uint_as_float(w[8 * c4 + 2 * e]) + fmaf(g, zr[2 * e], dsum)) *
+                                         dphi_from_phi(bf_lo(qu[e]));
+                        const float a1 = (__uint_as_float(w[8 * c4 + 2 * e + 1]) + fmaf(g, zr[2 * e + 1], dsum)) *
+                                         dphi_from_phi(bf_hi(qu[e]));
                         ou[e] = pack_bf16x2(a0, a1);
                     }
                     *reinterpret_cast<uint4*>(sSb + chunk_off(r, 8 * h + 4 * cb + c4)) = o4;

@@ -185,8 +185,10 @@ struct Grp {
     // a head narrower than the tile is zero-padded), times scale[row] when
     // scale is given.  With colpart, the column sums of the rounded values
     // (weighted by w[row] when w is given) go to colpart as per-warp partials
-    // (column_part).  With lo_tile, also writes lo = bf16(phi - hi) there; with
-    // copy_tile, a second copy of the rounded values.
+    // (column_part).  With lo_tile, also writes lo = bf16(phi - hi) there, or,
+    // with kMinusOne, bf16(phi - 1) (0 outside the rows and columns in range);
+    // with copy_tile, a second copy of the rounded values.
+    template <bool kMinusOne = false>
     __device__ static __forceinline__ void phi_tile(uint8_t* tile, uint8_t* lo_tile, int ct, int n, int dcols,
                                                     const float* w, float* colpart, uint8_t* copy_tile = nullptr,
                                                     const float* scale = nullptr) {
@@ -195,13 +197,13 @@ struct Grp {
         // 64-wide head leaves the upper column block alone (its TMA zero fill stays in place,
         // and the lo and copy tiles there feed only output columns that are never stored)
         if (n >= kC && dcols >= kD)
-            phi_tile_body<true, false>(tile, lo_tile, ct, n, dcols, w, colpart, copy_tile, scale);
+            phi_tile_body<true, false, kMinusOne>(tile, lo_tile, ct, n, dcols, w, colpart, copy_tile, scale);
         else if (dcols <= kD / 2)
-            phi_tile_body<false, true>(tile, lo_tile, ct, n, dcols, w, colpart, copy_tile, scale);
+            phi_tile_body<false, true, kMinusOne>(tile, lo_tile, ct, n, dcols, w, colpart, copy_tile, scale);
         else
-            phi_tile_body<false, false>(tile, lo_tile, ct, n, dcols, w, colpart, copy_tile, scale);
+            phi_tile_body<false, false, kMinusOne>(tile, lo_tile, ct, n, dcols, w, colpart, copy_tile, scale);
     }
-    template <bool kWhole, bool kHalf>
+    template <bool kWhole, bool kHalf, bool kMinusOne = false>
     __device__ static __forceinline__ void phi_tile_body(uint8_t* tile, uint8_t* lo_tile, int ct, int n, int dcols,
                                                          const float* w, float* colpart, uint8_t* copy_tile,
                                                          const float* scale) {
@@ -228,7 +230,10 @@ struct Grp {
             for (int e = 0; e < 4; ++e) {
                 const float a = valid ? phi_f(bf_lo(u[e])) * sr : 0.f, b = valid ? phi_f(bf_hi(u[e])) * sr : 0.f;
                 u[e] = pack_bf16x2(a, b);
-                ul[e] = pack_bf16x2(a - bf_lo(u[e]), b - bf_hi(u[e]));
+                if (kMinusOne)
+                    ul[e] = valid ? pack_bf16x2(a - 1.f, b - 1.f) : 0u;
+                else
+                    ul[e] = pack_bf16x2(a - bf_lo(u[e]), b - bf_hi(u[e]));
                 if (colpart) {
                     zp[vec_block(j)][2 * e] = fmaf(wr, bf_lo(u[e]), zp[vec_block(j)][2 * e]);
                     zp[vec_block(j)][2 * e + 1] = fmaf(wr, bf_hi(u[e]), zp[vec_block(j)][2 * e + 1]);
