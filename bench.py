@@ -194,6 +194,8 @@ def kernel_algorithmic_bytes(name: str, B, H, N, Dk, Dv, sz):
     table = {
         "segment_sums": T * (Dk + Dv) * sz,                       # read k, v
         "causal_fwd_out": T * (2 * Dk + 2 * Dv) * sz,             # read q, k, v; write o
+        "causal_fwd_fused": T * (2 * Dk + 2 * Dv) * sz,           # read q, k, v; write o (the second read of
+                                                                  # k, v for the segment sums is not counted)
         "bwd_forward_sweep": T * ((2 * Dk + 2 * Dv) * sz + Dk * sz + 8),   # read q,k,v,dO; write dq, (den,g)
         "bwd_reverse_sweep": T * ((2 * Dk + 2 * Dv) * sz + 8 + (Dk + Dv) * sz),  # read q,k,v,dO,(den,g); write dk,dv
     }

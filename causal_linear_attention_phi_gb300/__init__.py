@@ -67,9 +67,11 @@ def _declare(lib):
     lib.la_retention_fwd.argtypes = [_vp] * 6 + [Shape, _vp, ctypes.c_size_t, _vp]
     lib.la_retention_step.argtypes = [_vp] * 6 + [Shape, _vp]
     lib.la_selftest_bounded_wait.argtypes = [_vp]
+    lib.la_selftest_lookback_timeout.argtypes = [_vp] * 4 + [Shape, _vp, ctypes.c_size_t, _vp]
     for f in ("la_causal_step_host", "la_noncausal_fwd", "la_noncausal_bwd", "la_causal_fwd",
               "la_causal_fwd_with_state", "la_causal_bwd", "la_causal_bwd_after_fwd", "la_recurrent_step",
-              "la_retention_fwd", "la_retention_step", "la_selftest_bounded_wait", "la_last_error",
+              "la_retention_fwd", "la_retention_step", "la_selftest_bounded_wait", "la_selftest_lookback_timeout",
+              "la_last_error",
               "la_clear_error", "la_timing_enable", "la_timing_reset"):
         getattr(lib, f).restype = ctypes.c_int
     lib.la_last_error.argtypes = []
@@ -341,6 +343,20 @@ def selftest_bounded_wait(stream=None):
     """Launch the bounded-wait self-test (a wait that runs out after about a second and
     records LA_ERR_TIMEOUT in the sticky status word); read it with last_error()."""
     _check(library().la_selftest_bounded_wait(_stream_ptr(stream)), "la_selftest_bounded_wait")
+
+
+def selftest_lookback_timeout(q, k, v, out=None, workspace=None, stream=None):
+    """The one-launch causal forward with segment 0 of head 0 withholding its sums: the
+    later segments of that head time out (about a second) and record LA_ERR_TIMEOUT; read
+    it with last_error().  Other heads' outputs are complete."""
+    _need_cuda(q, k, v)
+    s = _shape4(q, k, v)
+    if out is None:
+        out = torch.empty_like(v)
+    ws, nb = _workspace(OP_CAUSAL_FWD, s, q.device, workspace)
+    _check(library().la_selftest_lookback_timeout(_ptr(q), _ptr(k), _ptr(v), _ptr(out), s, _ptr(ws), nb,
+                                                  _stream_ptr(stream)), "la_selftest_lookback_timeout")
+    return out
 
 
 def last_error() -> int:

@@ -212,6 +212,12 @@ WsLayout make_ws_layout(const la_shape& s, int op, const Plan& p) {
         w.totals2 = off;
         off += align256(BH * E * sizeof(float));
     }
+    if (op == LA_OP_CAUSAL_FWD && p.tc) {  // the one-launch forward's chained scan
+        w.agg = off;
+        off += seg;
+        w.flags = off;
+        off += align256((BH * p.P + 1) * sizeof(unsigned));
+    }
     w.bytes = off;
     return w;
 }
@@ -311,10 +317,9 @@ static la_status causal_bwd_sweeps(const void* q, const void* k, const void* v, 
                                    const WsLayout& w, cudaStream_t st) {
     float* segR = reinterpret_cast<float*>(base + w.seg_states2);
     float* den_g = reinterpret_cast<float*>(base + w.den_g);
-    if (p.tc) {
+    if (p.tc) {  // the reverse sweep adds the later segments' (R, r) sums itself: no scan launch
         LA_TRY(cuda_status(tc_bwd_forward_sweep(q, k, v, dout, dq, segS, segR, den_g, s, p, st),
                            "backward forward sweep"));
-        LA_TRY(cuda_status(scan_segments(segR, nullptr, s, p, SCAN_EXCLUSIVE_SUFFIX, st), "reverse scan"));
         LA_TRY(cuda_status(tc_bwd_reverse_sweep(q, k, v, dout, dk, dv, segR, den_g, s, p, st),
                            "backward reverse sweep"));
     } else {
@@ -341,7 +346,8 @@ static la_status check_bwd_args(const void* q, const void* k, const void* v, con
 }
 
 static la_status causal_fwd_impl(const void* q, const void* k, const void* v, void* o, float* S_out, float* z_out,
-                                 la_shape s, void* ws, size_t ws_bytes, la_stream_t stream) {
+                                 la_shape s, void* ws, size_t ws_bytes, la_stream_t stream,
+                                 bool withhold_first = false) {
     t_detail.clear();
     LA_TRY(check_shape(s));
     if (empty(s)) {
@@ -369,7 +375,15 @@ static la_status causal_fwd_impl(const void* q, const void* k, const void* v, vo
     const WsLayout w = make_ws_layout(s, LA_OP_CAUSAL_FWD, p);
     LA_TRY(check_ws(ws, ws_bytes, w.bytes));
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    float* seg = reinterpret_cast<float*>(static_cast<char*>(ws) + w.seg_states);
+    char* base = static_cast<char*>(ws);
+    float* seg = reinterpret_cast<float*>(base + w.seg_states);
+    if (p.tc) {  // one kernel: segment sums, chained scan and outputs (plus a memset of its flags)
+        LA_TRY(cuda_status(tc_causal_fwd_fused(q, k, v, o, seg, reinterpret_cast<float*>(base + w.agg),
+                                               reinterpret_cast<unsigned*>(base + w.flags), S_out, z_out, s, p, st,
+                                               withhold_first),
+                           "causal forward"));
+        return LA_OK;
+    }
     const size_t seg_bytes = (size_t)s.B * s.H * p.P * plan_state_elems(p) * sizeof(float);
     if (p.P > 1 || S_out) {
         if (p.tc)
@@ -445,6 +459,17 @@ la_status la_causal_fwd_with_state(const void* q, const void* k, const void* v, 
         return fail(LA_ERR_INVALID_ARG, "S and z are required");
     }
     return causal_fwd_impl(q, k, v, o, S, z, s, ws, ws_bytes, stream);
+}
+
+la_status la_selftest_lookback_timeout(const void* q, const void* k, const void* v, void* o, la_shape s, void* ws,
+                                       size_t ws_bytes, la_stream_t stream) {
+    t_detail.clear();
+    LA_TRY(check_shape(s));
+    const Plan p = make_plan(s, LA_OP_CAUSAL_FWD);
+    if (empty(s) || !p.tc || p.P < 2)
+        return fail(LA_ERR_INVALID_ARG, "the look-back self-test needs a tensor-core shape with two or more segments "
+                                        "(bf16, Dk = Dv = 64 or 128; this one has %d)", empty(s) ? 0 : p.P);
+    return causal_fwd_impl(q, k, v, o, nullptr, nullptr, s, ws, ws_bytes, stream, true);
 }
 
 la_status la_causal_bwd(const void* q, const void* k, const void* v, const void* dout, void* dq, void* dk, void* dv,

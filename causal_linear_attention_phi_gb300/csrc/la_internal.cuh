@@ -39,6 +39,8 @@ struct WsLayout {
     size_t totals;       // [BH][E] fp32: non-causal totals (S, z)
     size_t totals2;      // [BH][E] fp32: non-causal backward totals (R, r)
     size_t den_g;        // [BH][N][2] fp32: backward per-position den and g
+    size_t agg;          // [BH][P][E] fp32: the one-launch causal forward's per-segment own sums
+    size_t flags;        // [BH][P] + 1 uint32: their publication flags and the ticket counter
     size_t bytes;        // total
 };
 
@@ -103,7 +105,10 @@ __device__ __forceinline__ bool check(bool ok, uint32_t tag, uint32_t line) {
 }  // namespace dbg
 #define LA_DCHECK(cond) (::la::dbg::check((cond), ::la::dbg::Const<::la::dbg::file_tag(__FILE__)>::value, __LINE__))
 #else
-#define LA_DCHECK(cond) (true)
+namespace dbg {
+__host__ __device__ constexpr bool pass() { return true; }
+}  // namespace dbg
+#define LA_DCHECK(cond) (::la::dbg::pass())
 #endif
 
 // ------------------------------------------------------------------ launch bookkeeping
@@ -146,6 +151,15 @@ cudaError_t recurrent_step(const void* q, const void* k, const void* v, float* S
 // split_k (sums only): phi(K) enters the sums as hi + lo bf16 parts (the non-causal gradient).
 cudaError_t tc_causal_fwd(const void* q, const void* k, const void* v, void* o, float* seg, const la_shape& s,
                           const Plan& p, bool out_pass, cudaStream_t st, bool split_k = false);
+// The causal forward in one kernel launch (after a memset of the flags): each CTA
+// forms and publishes its segment's own sums, adds the earlier segments' in order
+// (a chained scan with bounded waits), writes that exclusive prefix to seg and runs
+// the output pass; with S_out / z_out also the state after position N.
+// withhold_first (tests only): segment 0 of head 0 never publishes, so the later
+// segments of that head time out with LA_ERR_TIMEOUT.
+cudaError_t tc_causal_fwd_fused(const void* q, const void* k, const void* v, void* o, float* seg, float* agg,
+                                unsigned* flags, float* S_out, float* z_out, const la_shape& s, const Plan& p,
+                                cudaStream_t st, bool withhold_first = false);
 cudaError_t tc_bwd_forward_sweep(const void* q, const void* k, const void* v, const void* dout, void* dq,
                                  const float* seg_S, float* seg_R, float* den_g, const la_shape& s, const Plan& p,
                                  cudaStream_t st);

@@ -19,7 +19,9 @@
 // and D K~ is formed as rowsum(D) 1^T + D (K~ - 1): the row sums exact in fp32,
 // the product on a bf16 copy of D and a bf16 copy of phi(K) - 1, which is small
 // where phi(k) is near 1 and so keeps its low bits.
-// Reverse sweep kernel: chunks in reverse order with R_next in TMEM; every
+// Reverse sweep kernel: starts from the sum of the later segments' (R, r) records
+// (added from the last segment down, as an exclusive suffix scan would); chunks
+// in reverse order with R_next in TMEM; every
 // product is taken with the keys as the M (TMEM lane) dimension so dk and dv
 // come out row by row.  1/den is folded into the query operand, Q' = phi(Q) /
 // den, so dO enters unscaled: A'^T = K~ Q'^T (= A^T / den), D'^T = tril(V dO^T
@@ -647,9 +649,33 @@ tc_bwd_reverse_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
         const int r = 32 * (warp & 3) + lane;
         const uint32_t lane0 = (uint32_t)(32 * (warp & 3)) << 16;
         const uint32_t lb = lane0 + 32 * qt;
-        const float* suf = seg_R + ((size_t)bh * P + p) * E;
-        global_row_to_tmem<32>(suf + (size_t)r * kD + 32 * qt, tmem + lb + kRR);  // R_next row r, this quarter
-        if (ct < 128) rsh[ct] = record_ok(bh, p, P, (size_t)kD * kD + ct, E) ? suf[(size_t)kD * kD + ct] : 0.f;
+        {
+            // R_next, r_next at the segment's end: the later segments' (R, r) sums added from the
+            // last segment down (the order of the exclusive suffix scan); R row r, this quarter
+            float run[32];
+            float run_r = 0.f;
+#pragma unroll
+            for (int x = 0; x < 32; ++x) run[x] = 0.f;
+            for (int q2 = P - 1; q2 > p; --q2) {
+                const float* rec = seg_R + ((size_t)bh * P + q2) * E;
+                const float4* src = reinterpret_cast<const float4*>(rec + (size_t)r * kD + 32 * qt);
+#pragma unroll
+                for (int x = 0; x < 8; ++x) {
+                    const float4 f = src[x];
+                    run[4 * x] += f.x;
+                    run[4 * x + 1] += f.y;
+                    run[4 * x + 2] += f.z;
+                    run[4 * x + 3] += f.w;
+                }
+                if (ct < 128 && record_ok(bh, q2, P, (size_t)kD * kD + ct, E)) run_r += rec[(size_t)kD * kD + ct];
+            }
+            uint32_t w32[32];
+#pragma unroll
+            for (int x = 0; x < 32; ++x) w32[x] = __float_as_uint(run[x]);
+            tmem_st32(tmem + lb + kRR, w32);
+            tmem_st_wait();
+            if (ct < 128) rsh[ct] = run_r;
+        }
         tc_fence_before();
         bool ok = RG::all(true);
         const float* dgh = den_g + (size_t)bh * N * 2;

@@ -47,8 +47,9 @@ __device__ __forceinline__ void check_plan(int p, int P, int cbeg, int cend, int
 // Debug build: a TMA tile (x, row) of head bh of a [BH][N][D] map: x a multiple of 8
 // elements (16 bytes) inside the 128-wide tile, the first row inside the sequence.  TMA
 // clips rows past N by itself; the check catches a wrong coordinate.
-__device__ __forceinline__ void check_tile(int x, int row, int bh, int N) {
-    LA_DCHECK(x >= 0 && (x & 7) == 0 && x < kD && row >= 0 && row < N && bh >= 0 && bh < (int)gridDim.y);
+__device__ __forceinline__ void check_tile(int x, int row, int bh, int N, int BH = -1) {
+    LA_DCHECK(x >= 0 && (x & 7) == 0 && x < kD && row >= 0 && row < N && bh >= 0 &&
+              bh < (BH < 0 ? (int)gridDim.y : BH));
 }
 // Debug build: a state record index (head bh, segment p of P) and an element offset in it.
 __device__ __forceinline__ bool record_ok(int bh, int p, int P, size_t off, size_t E) {

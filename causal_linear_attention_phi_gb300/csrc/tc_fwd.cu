@@ -53,6 +53,7 @@ struct __align__(8) Barriers {
     uint64_t qk_ready[2], sb_ready, a_ready;  // qk_ready per K/V stage: its producer may run one chunk ahead
     uint64_t qk_done, o_done, s_done;
     uint64_t final_mma;
+    uint64_t agg_done;  // fused mode: the segment's own sums are complete in TMEM
 };
 
 struct SmemLayout {
@@ -78,13 +79,35 @@ __device__ __forceinline__ int small_row0_off(int col) {
     return (col >> 6) * 2048 + (((col & 63) >> 3) << 4) + ((col & 7) << 1);
 }
 
+// The fused causal forward's extra arguments: the chained scan over segments.
+struct FusedArgs {
+    float* agg;         // [BH][P][E]: each segment's own (S, z) sums, published for later segments
+    unsigned* flags;    // [BH][P] publication flags, then the ticket counter; zero at launch
+    float* S_out;       // optional [BH][Dk][Dv]: the state after position N (with z_out)
+    float* z_out;       // optional [BH][Dk]
+    int BH;
+    int withhold;       // test only: segment 0 of head 0 never publishes when this is 1
+};
+
 // D: the head size, 128 or 64 (padded to the 128-wide tiles); a template
 // parameter so that the full-width kernel carries no column test.
-template <bool kOut, int D, bool kSplit = false>
+//
+// kFused (with kOut): one launch for the whole causal forward.  CTAs take their
+// (segment, head) from a ticket counter in segment-major order, so a CTA only
+// ever waits on CTAs that started before it.  A CTA first forms its segment's
+// own sums (S, z) exactly as the sums pass does (same products, same order) and
+// publishes them (record, then a release flag); it then waits for the flags of
+// the earlier segments of its head and adds their records in segment order
+// (the order of the separate exclusive scan, so the prefixes are bit-identical
+// to it), writes that exclusive prefix to `seg` for the backward, loads it as
+// its starting state and runs the output pass.  The last segment skips its own
+// sums unless the state after position N is asked for (prefix + own sums, again
+// the scan's order).  Every wait is bounded.
+template <bool kOut, int D, bool kSplit = false, bool kFused = false>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_causal_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-                     float* __restrict__ seg, int N, int nchunks, int cps, int P, int* err) {
+                     float* __restrict__ seg, int N, int nchunks, int cps, int P, int* err, FusedArgs fa) {
     extern __shared__ uint8_t smem_raw[];
     constexpr int kKd = D / 16;  // K steps of a product over a head dimension (a 64-wide head is zero above)
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -94,14 +117,32 @@ tc_causal_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     uint8_t* sZb = base + SmemLayout::Zb;
     Barriers* bar = reinterpret_cast<Barriers*>(base + SmemLayout::bars);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + SmemLayout::tmem_slot);
+    static_assert(!kFused || kOut, "the fused forward is an output pass");
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int p = blockIdx.x, bh = blockIdx.y;
+    int p = blockIdx.x, bh = blockIdx.y;
+    if (kFused) {  // (segment, head) from the ticket counter, segment-major
+        if (tid == 0) tmem_slot[1] = atomicAdd(fa.flags + (size_t)fa.BH * P, 1u);
+        __syncthreads();
+        const int t = (int)tmem_slot[1];
+        LA_DCHECK(t >= 0 && t < fa.BH * P && (int)gridDim.x == fa.BH * P);
+        p = t / fa.BH;
+        bh = t - p * fa.BH;
+    }
     const int cbeg = p * cps, cend = min(nchunks, cbeg + cps), nloc = cend - cbeg;
     const size_t E = state_elems(kD, kD);
     float* segp = seg + ((size_t)bh * P + p) * E;
-    check_plan(p, P, cbeg, cend, nchunks, N);
-    record_ok(bh, p, P, E - 1, E);
+    if (kFused) {
+        LA_DCHECK(bh >= 0 && bh < fa.BH && p >= 0 && p < P && cbeg < cend && cend <= nchunks &&
+                  (long long)(cend - 1) * kC < N);
+    } else {
+        check_plan(p, P, cbeg, cend, nchunks, N);
+        record_ok(bh, p, P, E - 1, E);
+    }
+    const int nBH = kFused ? fa.BH : (int)gridDim.y;  // heads, for the tile checks
+    // fused: iterations [0, pre) form the segment's own sums, [pre, pre + nloc) the outputs
+    const int npre = kFused && (p < P - 1 || fa.S_out) ? nloc : 0;
+    (void)nBH;
     // K and V stage s live at K0 + s * kTileBytes and V0 + s * kTileBytes
     auto sK = [&](int s) { return base + SmemLayout::K0 + s * kTileBytes; };
     auto sV = [&](int s) { return base + SmemLayout::V0 + s * kTileBytes; };
@@ -151,18 +192,20 @@ tc_causal_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         if (lane == 0) {
             int armed_kv[2] = {-1, -1}, armed_q = -1;
             bool ok = true;
-            for (int i = 0; i < nloc && ok; ++i) {
-                const int s = i & 1, t0 = (cbeg + i) * kC;
-                ok = mbar_wait(&bar->kv_empty[s], ((i >> 1) & 1) ^ 1, err, LA_ERR_TIMEOUT);
+            // it: K/V stage iterations (own sums, then outputs, in the fused mode); i: output chunk
+            for (int it = 0; it < npre + nloc && ok; ++it) {
+                const int i = it - npre;
+                const int s = it & 1, t0 = (cbeg + (i < 0 ? it : i)) * kC;
+                ok = mbar_wait(&bar->kv_empty[s], ((it >> 1) & 1) ^ 1, err, LA_ERR_TIMEOUT);
                 if (!ok) break;
                 mbar_arrive_expect_tx(&bar->kv_full[s], 2 * kTileBytes);
-                check_tile(64, t0, bh, N);
+                check_tile(64, t0, bh, N, nBH);
                 tma_load_3d(sK(s), &tm_k, 0, t0, bh, &bar->kv_full[s]);
                 tma_load_3d(sK(s) + kBlockBytes, &tm_k, 64, t0, bh, &bar->kv_full[s]);
                 tma_load_3d(sV(s), &tm_v, 0, t0, bh, &bar->kv_full[s]);
                 tma_load_3d(sV(s) + kBlockBytes, &tm_v, 64, t0, bh, &bar->kv_full[s]);
-                armed_kv[s] = i;
-                if (kOut) {
+                armed_kv[s] = it;
+                if (kOut && i >= 0) {
                     ok = mbar_wait(&bar->q_empty, (i & 1) ^ 1, err, LA_ERR_TIMEOUT);
                     if (!ok) break;
                     mbar_arrive_expect_tx(&bar->q_full, kTileBytes);
@@ -186,11 +229,23 @@ tc_causal_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             constexpr uint32_t id_mn16 = idesc_bf16_f32(128, 16, 1, 0);  // N = 16, A MN-major
             const uint32_t aQ = smem_u32(sQ), aSb = smem_u32(sSb), aOnes = smem_u32(sOnes), aZb = smem_u32(sZb);
             bool ok = true;
-            for (int i = 0; i < nloc && ok; ++i) {
-                const int s = i & 1;
+            for (int it = 0; it < npre + nloc && ok; ++it) {
+                const int i = it - npre, s = it & 1;
                 const uint32_t aK = smem_u32(sK(s)), aV = smem_u32(sV(s));
-                if (!(ok = mbar_wait(&bar->qk_ready[s], (i >> 1) & 1, err, LA_ERR_TIMEOUT))) break;
+                if (!(ok = mbar_wait(&bar->qk_ready[s], (it >> 1) & 1, err, LA_ERR_TIMEOUT))) break;
                 tc_fence_after();
+                if (kFused && i < 0) {
+                    // the segment's own sums: the products and order of the sums pass
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
+                        mma_ss(tmem + kTmS, desc_mnmajor(aK, kk), desc_mnmajor(aV, kk), id_mnmn, acc);
+                        mma_ss(tmem + kTmZ, desc_mnmajor(aK, kk), desc_small(aOnes, kk), id_mn16, acc);
+                    }
+                    mma_commit(&bar->kv_empty[s]);
+                    if (it == npre - 1) mma_commit(&bar->agg_done);
+                    continue;
+                }
                 if (kOut) {
 #pragma unroll
                     for (int kk = 0; kk < kKd; ++kk)  // QK = Q~ K~^T
@@ -241,7 +296,7 @@ tc_causal_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         const int h = (warp - 2) >> 2;                 // column half of the rows this thread serves
         const int r = 32 * (warp & 3) + lane;          // TMEM lane / tile row
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-        if (kOut) {
+        if (kOut && !kFused) {
             // initial state from the scanned segment prefix: S row r (this thread's 64 columns), z[r]
             const float* pre = segp + (size_t)r * kD + 64 * h;
 #pragma unroll
@@ -268,13 +323,118 @@ tc_causal_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         }
         tc_fence_before();
         bool ok = CG::all(true);
+        if (kFused) {
+            // (own sums) phi on this segment's K tiles for the sums products
+            for (int it = 0; it < npre && ok; ++it) {
+                const int s = it & 1;
+                const int c0 = (cbeg + it) * kC, n = min(kC, N - c0);
+                if (!CG::all(mbar_wait(&bar->kv_full[s], (it >> 1) & 1, err, LA_ERR_TIMEOUT))) { ok = false; break; }
+                CG::phi_tile(sK(s), nullptr, ct, n, D, nullptr, nullptr);
+                fence_proxy_async_smem();
+                CG::sync();
+                if (ct == 0) mbar_arrive(&bar->qk_ready[s]);
+            }
+            // publish them: S row r (this thread's 64 columns) and z[r] to this segment's record,
+            // then the flag (release, after every thread's stores and fences)
+            if (ok && npre > 0) {
+                ok = CG::all(mbar_wait(&bar->agg_done, 0, err, LA_ERR_TIMEOUT));
+                if (ok) {
+                    tc_fence_after();
+                    float* own = fa.agg + ((size_t)bh * P + p) * E;
+                    tmem_row_to_global<64>(tmem + lane_base + kTmS + 64 * h, own + (size_t)r * kD + 64 * h);
+                    if (h == 0) {
+                        uint32_t zv[16];
+                        tmem_ld16(tmem + lane_base + kTmZ, zv);
+                        tmem_ld_wait();
+                        own[(size_t)kD * kD + r] = __uint_as_float(zv[0]);
+                    }
+                    __threadfence();
+                    CG::sync();
+                    if (ct == 0 && !(fa.withhold && p == 0 && bh == 0))
+                        flag_release(fa.flags + (size_t)bh * P + p, 1u);
+                }
+            }
+            // exclusive prefix: the records of segments 0 .. p-1 of this head added in segment order
+            float run[64];
+            float run_z = 0.f;
+#pragma unroll
+            for (int x = 0; x < 64; ++x) run[x] = 0.f;
+            if (ok && p > 0) {
+                bool w = true;
+                if (ct == 0)
+                    for (int q2 = 0; q2 < p && w; ++q2) w = flag_wait(fa.flags + (size_t)bh * P + q2, err, LA_ERR_TIMEOUT);
+                ok = CG::all(w);  // a barrier: thread 0's acquire precedes every thread's record loads
+                for (int q2 = 0; q2 < p && ok; ++q2) {
+                    const float* rec = fa.agg + ((size_t)bh * P + q2) * E;
+                    const float4* src = reinterpret_cast<const float4*>(rec + (size_t)r * kD + 64 * h);
+#pragma unroll
+                    for (int x = 0; x < 16; ++x) {
+                        const float4 f = __ldcg(src + x);
+                        run[4 * x] += f.x;
+                        run[4 * x + 1] += f.y;
+                        run[4 * x + 2] += f.z;
+                        run[4 * x + 3] += f.w;
+                    }
+                    if (h == 0) run_z += __ldcg(rec + (size_t)kD * kD + r);
+                }
+            }
+            if (ok) {
+                // the prefix record for the backward
+                float4* dst = reinterpret_cast<float4*>(segp + (size_t)r * kD + 64 * h);
+#pragma unroll
+                for (int x = 0; x < 16; ++x)
+                    dst[x] = make_float4(run[4 * x], run[4 * x + 1], run[4 * x + 2], run[4 * x + 3]);
+                if (h == 0) segp[(size_t)kD * kD + r] = run_z;
+                // the state after position N: prefix + own sums (still in TMEM), the scan's order
+                if (fa.S_out && p == P - 1) {
+#pragma unroll
+                    for (int cb = 0; cb < 2; ++cb) {
+                        uint32_t w32[32];
+                        tmem_ld32(tmem + lane_base + kTmS + 64 * h + 32 * cb, w32);
+                        tmem_ld_wait();
+                        if (r < D && 64 * h < D) {
+                            float4* so = reinterpret_cast<float4*>(fa.S_out + ((size_t)bh * D + r) * D + 64 * h + 32 * cb);
+#pragma unroll
+                            for (int x = 0; x < 8; ++x)
+                                so[x] = make_float4(run[32 * cb + 4 * x] + __uint_as_float(w32[4 * x]),
+                                                    run[32 * cb + 4 * x + 1] + __uint_as_float(w32[4 * x + 1]),
+                                                    run[32 * cb + 4 * x + 2] + __uint_as_float(w32[4 * x + 2]),
+                                                    run[32 * cb + 4 * x + 3] + __uint_as_float(w32[4 * x + 3]));
+                        }
+                    }
+                    if (h == 0) {
+                        uint32_t zv[16];
+                        tmem_ld16(tmem + lane_base + kTmZ, zv);
+                        tmem_ld_wait();
+                        if (r < D) fa.z_out[(size_t)bh * D + r] = run_z + __uint_as_float(zv[0]);
+                    }
+                }
+                // the prefix as the starting state in TMEM
+#pragma unroll
+                for (int cb = 0; cb < 2; ++cb) {
+                    uint32_t w32[32];
+#pragma unroll
+                    for (int x = 0; x < 32; ++x) w32[x] = __float_as_uint(run[32 * cb + x]);
+                    tmem_st32(tmem + lane_base + kTmS + 64 * h + 32 * cb, w32);
+                }
+                if (h == 0) {
+                    uint32_t zw[16];
+#pragma unroll
+                    for (int x = 0; x < 16; ++x) zw[x] = __float_as_uint(run_z);
+                    tmem_st16(tmem + lane_base + kTmZ, zw);
+                }
+                tmem_st_wait();
+            }
+            tc_fence_before();
+            ok = CG::all(ok);
+        }
         bool k_applied = false;  // phi on this chunk's K was applied while the previous chunk's O was formed
         for (int i = 0; i < nloc && ok; ++i) {
-            const int s = i & 1;
+            const int it = npre + i, s = it & 1;  // it: K/V stage iteration (own sums came first)
             const int c0 = (cbeg + i) * kC, n = min(kC, N - c0);
             // (a) phi on the K (unless done already) and Q tiles
             if (kOut && ct == kStoreThread) bulk_wait_read_all();  // the previous o store has left the Sb tile
-            bool w = mbar_wait(&bar->kv_full[s], (i >> 1) & 1, err, LA_ERR_TIMEOUT);
+            bool w = mbar_wait(&bar->kv_full[s], (it >> 1) & 1, err, LA_ERR_TIMEOUT);
             if (kOut) w = w && mbar_wait(&bar->q_full, i & 1, err, LA_ERR_TIMEOUT);
             if (!CG::all(w)) { ok = false; break; }
             // (a stage's lo tile is free here: its last reader, the previous chunk's MMAs on this
@@ -349,7 +509,7 @@ tc_causal_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             // (c') while O is formed: phi on the next chunk's K (the other K/V stage) if it
             // has landed; that stage's previous chunk finished with it before it was reloaded
             k_applied = false;
-            if (i + 1 < nloc && CG::all(mbar_try_wait(&bar->kv_full[s ^ 1], ((i + 1) >> 1) & 1))) {
+            if (i + 1 < nloc && CG::all(mbar_try_wait(&bar->kv_full[s ^ 1], ((it + 1) >> 1) & 1))) {
                 CG::phi_tile(sK(s ^ 1), nullptr, ct, min(kC, N - (c0 + kC)), D, nullptr, nullptr);
                 fence_proxy_async_smem();
                 k_applied = true;
@@ -472,8 +632,31 @@ cudaError_t tc_causal_fwd(const void* q, const void* k, const void* v, void* o, 
     if (e != cudaSuccess) return e;
     const char* name = out_pass ? "tc_causal_fwd_out" : split_k ? "tc_segment_sums_split" : "tc_segment_sums";
     launch_begin(name, st);
-    kern<<<grid, kThreads, kSmemBytes, st>>>(tq, tk, tv, to, seg, s.N, p.nchunks, p.cps, p.P, err);
+    kern<<<grid, kThreads, kSmemBytes, st>>>(tq, tk, tv, to, seg, s.N, p.nchunks, p.cps, p.P, err, FusedArgs{});
     return launch_end(name, st);
+}
+
+cudaError_t tc_causal_fwd_fused(const void* q, const void* k, const void* v, void* o, float* seg, float* agg,
+                                unsigned* flags, float* S_out, float* z_out, const la_shape& s, const Plan& p,
+                                cudaStream_t st, bool withhold_first) {
+    const int BH = s.B * s.H;
+    CUtensorMap tq, tk, tv, to;
+    const int D = s.Dk;  // = s.Dv: 128, or 64 padded to the 128-wide tiles
+    if (!make_tmap_bf16_rows(&tk, k, BH, s.N, D, kC) || !make_tmap_bf16_rows(&tv, v, BH, s.N, D, kC) ||
+        !make_tmap_bf16_rows(&tq, q, BH, s.N, D, kC) || !make_tmap_bf16_rows(&to, o, BH, s.N, D, kC))
+        return cudaErrorInvalidValue;
+    if ((long long)BH * p.P > 0x7FFFFFFFll) return cudaErrorInvalidValue;
+    auto kern = D == 128 ? tc_causal_fwd_kernel<true, 128, false, true> : tc_causal_fwd_kernel<true, 64, false, true>;
+    cudaError_t e = cudaFuncSetAttribute((const void*)kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    // the publication flags and the ticket counter start at zero
+    e = cudaMemsetAsync(flags, 0, ((size_t)BH * p.P + 1) * sizeof(unsigned), st);
+    if (e != cudaSuccess) return e;
+    const FusedArgs fa{agg, flags, S_out, z_out, BH, withhold_first ? 1 : 0};
+    launch_begin("tc_causal_fwd_fused", st);
+    kern<<<dim3((unsigned)(BH * p.P)), kThreads, kSmemBytes, st>>>(tq, tk, tv, to, seg, s.N, p.nchunks, p.cps, p.P,
+                                                                   device_error_word(), fa);
+    return launch_end("tc_causal_fwd_fused", st);
 }
 
 }  // namespace la

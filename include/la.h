@@ -107,6 +107,13 @@ la_status la_noncausal_fwd(const void* q, const void* k, const void* v, void* o,
  * than the chunk size is masked.  (Digest, 핵심 구성요소 3; velog review 3.4;
  * itwiki 계산 형태 비교, chunked row, and 구현.)
  * q, k: [B,H,N,Dk]; v: [B,H,N,Dv]; o: [B,H,N,Dv] (written).
+ * bf16 heads of 64 or 128 run as one kernel launch (after a memset of a few KB
+ * of flags in the workspace): each block forms its segment's own sums, publishes
+ * them, adds the earlier segments' in segment order (a chained scan whose waits
+ * are bounded: a wait that runs out records LA_ERR_TIMEOUT in the sticky word)
+ * and writes the outputs.  Other shapes run the sums, a scan and the output pass
+ * as three launches.  Either way the workspace keeps every segment's starting
+ * state for la_causal_bwd_after_fwd.
  */
 la_status la_causal_fwd(const void* q, const void* k, const void* v, void* o, la_shape s,
                         void* ws, size_t ws_bytes, la_stream_t stream);
@@ -118,7 +125,7 @@ la_status la_causal_fwd(const void* q, const void* k, const void* v, void* o, la
  * velog review 3.6):  S = phi(K)^T V  [B,H,Dk,Dv] and  z = phi(K)^T 1  [B,H,Dk],
  * summed over all N positions of each head, fp32, written (not accumulated).
  * For N = 0 both are set to zero.  o and the workspace as for la_causal_fwd.
- * Costs one more pass over k and v when the forward has a single segment.
+ * Costs one more pass over k and v of the last segment of each head.
  */
 la_status la_causal_fwd_with_state(const void* q, const void* k, const void* v, void* o,
                                    float* S, float* z, la_shape s,
@@ -296,6 +303,20 @@ la_status la_clear_error(void);
  * with la_clear_error().  The device and context stay usable.
  */
 la_status la_selftest_bounded_wait(la_stream_t stream);
+
+/*
+ * Self-test of the one-launch causal forward's chained scan, with no fault:
+ * la_causal_fwd on the given buffers (same arguments and checks), except that
+ * the block of segment 0 of head 0 never publishes its sums.  The later blocks
+ * of that head wait for it; each wait gives up after about one second, records
+ * LA_ERR_TIMEOUT in the sticky status word and the block ends; all other heads
+ * complete normally.  Needs a shape that runs the one-launch forward with at
+ * least two segments per head (bf16, Dk = Dv = 64 or 128), else returns
+ * LA_ERR_INVALID_ARG before anything is launched.  o (head 0) and the workspace
+ * are left unspecified.  The device and context stay usable.
+ */
+la_status la_selftest_lookback_timeout(const void* q, const void* k, const void* v, void* o, la_shape s,
+                                       void* ws, size_t ws_bytes, la_stream_t stream);
 
 /* Static description of a status code. */
 const char* la_status_string(la_status st);

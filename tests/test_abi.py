@@ -125,13 +125,24 @@ def test_product_path_fails_loudly_without_library(tmp_path):
 
 
 def _segments(la, B, H, N, D=128):
-    """Segments per head of the tensor-core plan, read back from the causal forward's
-    workspace (one padded (S, z) record of (128 * 128 + 128) fp32 per segment and head)."""
+    """Segments per head of the tensor-core plan, read back from the retention forward's
+    workspace (the same planner; one padded 128 x 128 fp32 state record per segment and head)."""
     import torch
-    rec = (128 * 128 + 128) * 4
-    ws = la.workspace_bytes(la.OP_CAUSAL_FWD, B, H, N, D, D, torch.bfloat16)
+    rec = 128 * 128 * 4
+    ws = la.workspace_bytes(la.OP_RETENTION_FWD, B, H, N, D, D, torch.bfloat16)
     assert ws % (B * H * rec) == 0
     return ws // (B * H * rec)
+
+
+def test_causal_forward_workspace_holds_the_chained_scan(la):
+    """The one-launch forward's workspace: the segment prefixes, the segments' own sums (both
+    B*H*P padded records) and B*H*P + 1 flag words, each region 256-byte aligned."""
+    import torch
+    for B, H, N in [(2, 16, 65536), (1, 8, 1024), (65535, 1, 129)]:
+        P = _segments(la, B, H, N)
+        seg = -(-(B * H * P * (128 * 128 + 128) * 4) // 256) * 256
+        flags = -(-((B * H * P + 1) * 4) // 256) * 256
+        assert la.workspace_bytes(la.OP_CAUSAL_FWD, B, H, N, 128, 128, torch.bfloat16) == 2 * seg + flags
 
 
 @pytest.mark.parametrize("B,H,N", [(2, 16, 65536), (1, 16, 32768), (1, 8, 65536), (1, 1, 1 << 19),

@@ -86,3 +86,48 @@ def test_bounded_wait_times_out_and_the_context_stays_usable(la):
     o = la.causal_fwd(q, q, q)
     torch.cuda.synchronize()
     assert torch.isfinite(o).all() and la.last_error() == 0
+
+
+def test_chained_scan_wait_times_out_and_the_context_stays_usable(la):
+    """The one-launch causal forward with segment 0 of head 0 withholding its sums (a
+    test-only switch of the self-test entry point): the later segments of head 0 give up
+    waiting after about a second and record LA_ERR_TIMEOUT; head 1 is complete and right;
+    after clearing the word the same call without the switch is right for both heads."""
+    import oracle
+    from causal_linear_attention_phi_gb300 import workloads as W
+    q, k, v = W.random_case(61, 1, 2, 1024, 128, 128, dtype=torch.bfloat16, scale=128 ** -0.5)
+    qd, kd, vd = (t.to(DEV) for t in (q, k, v))
+    la.clear_error()
+    o = la.selftest_lookback_timeout(qd, kd, vd)
+    torch.cuda.synchronize()
+    assert la.last_error() == 5  # LA_ERR_TIMEOUT
+    ref = oracle.causal_recurrent(q, k, v)
+    from util import rel_per_head
+    assert rel_per_head(o.cpu()[:, 1:], ref[:, 1:]) < 2e-2
+    la.clear_error()
+    o = la.causal_fwd(qd, kd, vd)
+    torch.cuda.synchronize()
+    assert la.last_error() == 0 and rel_per_head(o.cpu(), ref) < 2e-2
+
+
+def test_lookback_selftest_refuses_shapes_without_a_chained_scan(la):
+    q = torch.randn(1, 2, 1024, 64, device=DEV)          # fp32: the three-launch CUDA-core path
+    with pytest.raises(la.LaError):
+        la.selftest_lookback_timeout(q, q, q)
+    qb = torch.randn(1, 2, 100, 128, device=DEV).bfloat16()  # one chunk: a single segment
+    with pytest.raises(la.LaError):
+        la.selftest_lookback_timeout(qb, qb, qb)
+
+
+def test_tensor_core_causal_forward_is_one_kernel(la):
+    """bf16 heads of 64 and 128: la_causal_fwd launches one kernel (after a memset of its flags)."""
+    for D in (64, 128):
+        q = torch.randn(2, 3, 3000, D, device=DEV).bfloat16()
+        la.timing_reset()
+        la.timing_enable(True)
+        try:
+            la.causal_fwd(q, q, q)
+            t = la.timing_read()
+        finally:
+            la.timing_enable(False)
+        assert list(t) == ["tc_causal_fwd_fused"] and t["tc_causal_fwd_fused"][0] == 1, t
