@@ -317,9 +317,10 @@ static la_status causal_bwd_sweeps(const void* q, const void* k, const void* v, 
                                    const WsLayout& w, cudaStream_t st) {
     float* segR = reinterpret_cast<float*>(base + w.seg_states2);
     float* den_g = reinterpret_cast<float*>(base + w.den_g);
-    if (p.tc) {  // the reverse sweep adds the later segments' (R, r) sums itself: no scan launch
+    if (p.tc) {
         LA_TRY(cuda_status(tc_bwd_forward_sweep(q, k, v, dout, dq, segS, segR, den_g, s, p, st),
                            "backward forward sweep"));
+        LA_TRY(cuda_status(scan_segments(segR, nullptr, s, p, SCAN_EXCLUSIVE_SUFFIX, st), "reverse scan"));
         LA_TRY(cuda_status(tc_bwd_reverse_sweep(q, k, v, dout, dk, dv, segR, den_g, s, p, st),
                            "backward reverse sweep"));
     } else {

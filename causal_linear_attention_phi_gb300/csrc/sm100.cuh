@@ -86,20 +86,6 @@ __device__ __forceinline__ unsigned flag_acquire(const unsigned* f) {
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
     return v;
 }
-// Wait until *f is non-zero.  Gives up after kWaitLimitCycles, records `code` in
-// the sticky error word and returns false (the caller abandons its work).
-__device__ __forceinline__ bool flag_wait(const unsigned* f, int* err, int code) {
-    if (flag_acquire(f)) return true;
-    const long long t0 = clock64();
-    while (!flag_acquire(f)) {
-        if (clock64() - t0 > kWaitLimitCycles) {
-            if (err) atomicCAS(err, 0, code);
-            return false;
-        }
-        __nanosleep(256);
-    }
-    return true;
-}
 
 // ------------------------------------------------------------------ proxies and fences
 // Generic-proxy shared-memory writes become visible to the async proxy (TMA, tcgen05.mma).

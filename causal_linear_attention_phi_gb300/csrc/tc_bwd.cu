@@ -19,9 +19,7 @@
 // and D K~ is formed as rowsum(D) 1^T + D (K~ - 1): the row sums exact in fp32,
 // the product on a bf16 copy of D and a bf16 copy of phi(K) - 1, which is small
 // where phi(k) is near 1 and so keeps its low bits.
-// Reverse sweep kernel: starts from the sum of the later segments' (R, r) records
-// (added from the last segment down, as an exclusive suffix scan would); chunks
-// in reverse order with R_next in TMEM; every
+// Reverse sweep kernel: chunks in reverse order with R_next in TMEM; every
 // product is taken with the keys as the M (TMEM lane) dimension so dk and dv
 // come out row by row.  1/den is folded into the query operand, Q' = phi(Q) /
 // den, so dO enters unscaled: A'^T = K~ Q'^T (= A^T / den), D'^T = tril(V dO^T
@@ -506,8 +504,11 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
 // X[0,64), A^T bf16 in X[64,128).
 constexpr uint32_t kRR = 0, kRDK = 128, kRDV = 256, kRX = 384;
 
+// Q and V (last read by the dK~ products) arrive and are released apart from K and
+// dO (last read by the dV products), so the next chunk's Q and V load while the dV
+// products run.
 struct RevSweepBars {
-    uint64_t full, empty;
+    uint64_t full_qv, empty_qv, full_kd, empty_kd;
     uint64_t ready, rb_ready, masks_ready;
     uint64_t at_dt_done, dk_done, dkv_done;  // dk_done: the dK~ products; dkv_done: the dV products too
     uint64_t final_mma;
@@ -581,23 +582,28 @@ tc_bwd_reverse_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
 
     if (warp == 0) {
         if (lane == 0) {
-            int armed = -1;
+            int armed_qv = -1, armed_kd = -1;
             for (int i = 0; i < nloc; ++i) {
                 const int t0 = (cend - 1 - i) * kC;
-                if (!mbar_wait(&bar->empty, (i & 1) ^ 1, err, LA_ERR_TIMEOUT)) break;
-                mbar_arrive_expect_tx(&bar->full, 4 * kTileBytes);
+                if (!mbar_wait(&bar->empty_qv, (i & 1) ^ 1, err, LA_ERR_TIMEOUT)) break;
+                mbar_arrive_expect_tx(&bar->full_qv, 2 * kTileBytes);
                 check_tile(64, t0, bh, N);
-                tma_load_3d(sQ, &tm_q, 0, t0, bh, &bar->full);
-                tma_load_3d(sQ + kBlockBytes, &tm_q, 64, t0, bh, &bar->full);
-                tma_load_3d(sK, &tm_k, 0, t0, bh, &bar->full);
-                tma_load_3d(sK + kBlockBytes, &tm_k, 64, t0, bh, &bar->full);
-                tma_load_3d(sV, &tm_v, 0, t0, bh, &bar->full);
-                tma_load_3d(sV + kBlockBytes, &tm_v, 64, t0, bh, &bar->full);
-                tma_load_3d(sP, &tm_do, 0, t0, bh, &bar->full);
-                tma_load_3d(sP + kBlockBytes, &tm_do, 64, t0, bh, &bar->full);
-                armed = i;
+                tma_load_3d(sQ, &tm_q, 0, t0, bh, &bar->full_qv);
+                tma_load_3d(sQ + kBlockBytes, &tm_q, 64, t0, bh, &bar->full_qv);
+                tma_load_3d(sV, &tm_v, 0, t0, bh, &bar->full_qv);
+                tma_load_3d(sV + kBlockBytes, &tm_v, 64, t0, bh, &bar->full_qv);
+                armed_qv = i;
+                if (!mbar_wait(&bar->empty_kd, (i & 1) ^ 1, err, LA_ERR_TIMEOUT)) break;
+                mbar_arrive_expect_tx(&bar->full_kd, 2 * kTileBytes);
+                tma_load_3d(sK, &tm_k, 0, t0, bh, &bar->full_kd);
+                tma_load_3d(sK + kBlockBytes, &tm_k, 64, t0, bh, &bar->full_kd);
+                tma_load_3d(sP, &tm_do, 0, t0, bh, &bar->full_kd);
+                tma_load_3d(sP + kBlockBytes, &tm_do, 64, t0, bh, &bar->full_kd);
+                armed_kd = i;
             }
-            if (armed >= 0) mbar_wait(&bar->full, armed & 1, err, LA_ERR_TIMEOUT);
+            // no copy may still be landing when the CTA exits
+            if (armed_qv >= 0) mbar_wait(&bar->full_qv, armed_qv & 1, err, LA_ERR_TIMEOUT);
+            if (armed_kd >= 0) mbar_wait(&bar->full_kd, armed_kd & 1, err, LA_ERR_TIMEOUT);
         }
     } else if (warp == 1) {
         if (lane == 0) {
@@ -631,6 +637,7 @@ tc_bwd_reverse_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
                 for (int kk = 0; kk < 8; ++kk)  // dK~ += D'^T Q'
                     mma_ts(tmem + kRDK, tmem + kRX + 8 * kk, desc_mnmajor(aQ, kk), id_kmn, 1);
                 mma_commit(&bar->dk_done);  // the dk epilogue runs during the dV products
+                mma_commit(&bar->empty_qv);  // Q, V: no further read in this chunk
 #pragma unroll
                 for (int kk = 0; kk < kKd; ++kk)  // dV = K~ R_next
                     mma_ss(tmem + kRDV, desc_kmajor(aK, kk), desc_mnmajor(aRb, kk), id_kmn, kk > 0);
@@ -638,7 +645,7 @@ tc_bwd_reverse_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
                 for (int kk = 0; kk < 8; ++kk)  // dV += A'^T dO
                     mma_ts(tmem + kRDV, tmem + kRX + 64 + 8 * kk, desc_mnmajor(aP, kk), id_kmn, 1);
                 mma_commit(&bar->dkv_done);
-                mma_commit(&bar->empty);  // Q, K, V, P: no further read in this chunk
+                mma_commit(&bar->empty_kd);  // K, P: no further read in this chunk
             }
             mma_commit(&bar->final_mma);
             mbar_wait(&bar->final_mma, 0, err, LA_ERR_TIMEOUT);
@@ -649,33 +656,9 @@ tc_bwd_reverse_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
         const int r = 32 * (warp & 3) + lane;
         const uint32_t lane0 = (uint32_t)(32 * (warp & 3)) << 16;
         const uint32_t lb = lane0 + 32 * qt;
-        {
-            // R_next, r_next at the segment's end: the later segments' (R, r) sums added from the
-            // last segment down (the order of the exclusive suffix scan); R row r, this quarter
-            float run[32];
-            float run_r = 0.f;
-#pragma unroll
-            for (int x = 0; x < 32; ++x) run[x] = 0.f;
-            for (int q2 = P - 1; q2 > p; --q2) {
-                const float* rec = seg_R + ((size_t)bh * P + q2) * E;
-                const float4* src = reinterpret_cast<const float4*>(rec + (size_t)r * kD + 32 * qt);
-#pragma unroll
-                for (int x = 0; x < 8; ++x) {
-                    const float4 f = src[x];
-                    run[4 * x] += f.x;
-                    run[4 * x + 1] += f.y;
-                    run[4 * x + 2] += f.z;
-                    run[4 * x + 3] += f.w;
-                }
-                if (ct < 128 && record_ok(bh, q2, P, (size_t)kD * kD + ct, E)) run_r += rec[(size_t)kD * kD + ct];
-            }
-            uint32_t w32[32];
-#pragma unroll
-            for (int x = 0; x < 32; ++x) w32[x] = __float_as_uint(run[x]);
-            tmem_st32(tmem + lb + kRR, w32);
-            tmem_st_wait();
-            if (ct < 128) rsh[ct] = run_r;
-        }
+        const float* suf = seg_R + ((size_t)bh * P + p) * E;
+        global_row_to_tmem<32>(suf + (size_t)r * kD + 32 * qt, tmem + lb + kRR);  // R_next row r, this quarter
+        if (ct < 128) rsh[ct] = record_ok(bh, p, P, (size_t)kD * kD + ct, E) ? suf[(size_t)kD * kD + ct] : 0.f;
         tc_fence_before();
         bool ok = RG::all(true);
         const float* dgh = den_g + (size_t)bh * N * 2;
@@ -696,7 +679,7 @@ tc_bwd_reverse_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
             // (a) per-row 1/den and g den; Q' = phi(Q) / den with the chunk's sum of (g den) Q';
             // phi on K (and its copy)
             if (ct == kStoreThread) bulk_wait_read_all();  // the previous dk / dv stores have left Kc and Rb
-            if (!RG::all(mbar_wait(&bar->full, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
+            if (!RG::all(mbar_wait(&bar->full_qv, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
             if (ct < 128) {
                 const bool v = ct < n;
                 ish[ct] = v ? 1.f / dg.x : 0.f;
@@ -704,6 +687,7 @@ tc_bwd_reverse_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
             }
             RG::sync();
             RG::phi_tile(sQ, nullptr, ct, n, D, gsh, rpart, nullptr, ish);
+            if (!RG::all(mbar_wait(&bar->full_kd, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
             RG::phi_tile(sK, nullptr, ct, n, D, nullptr, nullptr, sKc);
             fence_proxy_async_smem();
             RG::sync();

@@ -96,13 +96,16 @@ struct FusedArgs {
 // (segment, head) from a ticket counter in segment-major order, so a CTA only
 // ever waits on CTAs that started before it.  A CTA first forms its segment's
 // own sums (S, z) exactly as the sums pass does (same products, same order) and
-// publishes them (record, then a release flag); it then waits for the flags of
-// the earlier segments of its head and adds their records in segment order
-// (the order of the separate exclusive scan, so the prefixes are bit-identical
-// to it), writes that exclusive prefix to `seg` for the backward, loads it as
-// its starting state and runs the output pass.  The last segment skips its own
-// sums unless the state after position N is asked for (prefix + own sums, again
-// the scan's order).  Every wait is bounded.
+// publishes them (record in `agg`, flag 1).  It then looks back over the earlier
+// segments of its head to the nearest one whose inclusive prefix is published
+// (flag 2) and adds, left to right, that prefix and the own sums after it: the
+// additions of a sequential exclusive scan, in its order, so the prefixes are
+// bit-identical to the separate scan's.  It publishes its own inclusive prefix
+// (prefix + own sums) as the next segment's record in `seg` (flag 2), which is
+// also what the backward reads, loads its prefix as the starting state and runs
+// the output pass.  The last segment skips its own sums unless the state after
+// position N is asked for (prefix + own sums, again the scan's order).  Every
+// wait is bounded.
 template <bool kOut, int D, bool kSplit = false, bool kFused = false>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_causal_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -334,12 +337,15 @@ tc_causal_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                 CG::sync();
                 if (ct == 0) mbar_arrive(&bar->qk_ready[s]);
             }
-            // publish them: S row r (this thread's 64 columns) and z[r] to this segment's record,
-            // then the flag (release, after every thread's stores and fences)
+            // publish them (segments with a successor): S row r (this thread's 64 columns) and z[r]
+            // to this segment's record, then its flag = 1 (release, after every thread's stores and
+            // fences).  The withheld segment (self-test) never publishes anything.
+            const bool withheld = fa.withhold && p == 0 && bh == 0;
+            unsigned* fl = fa.flags + (size_t)bh * P;
             if (ok && npre > 0) {
                 ok = CG::all(mbar_wait(&bar->agg_done, 0, err, LA_ERR_TIMEOUT));
-                if (ok) {
-                    tc_fence_after();
+                tc_fence_after();
+                if (ok && p < P - 1) {
                     float* own = fa.agg + ((size_t)bh * P + p) * E;
                     tmem_row_to_global<64>(tmem + lane_base + kTmS + 64 * h, own + (size_t)r * kD + 64 * h);
                     if (h == 0) {
@@ -350,21 +356,57 @@ tc_causal_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                     }
                     __threadfence();
                     CG::sync();
-                    if (ct == 0 && !(fa.withhold && p == 0 && bh == 0))
-                        flag_release(fa.flags + (size_t)bh * P + p, 1u);
+                    if (ct == 0 && !withheld) flag_release(fl + p, 1u);
                 }
             }
-            // exclusive prefix: the records of segments 0 .. p-1 of this head added in segment order
+            // exclusive prefix.  Thread 0 walks back from segment p - 1 to the nearest segment b
+            // whose inclusive prefix is published (flag 2: it sits in record b + 1 of seg), past
+            // segments whose own sums are published (flag 1); every thread then adds, left to
+            // right, that inclusive prefix (or zero when there is none, b = -1) and the own sums of
+            // segments b + 1 .. p - 1.  Each addition is the one a sequential scan over the
+            // segments makes, in its order, so the prefix is bit-identical to it whatever b is.
             float run[64];
             float run_z = 0.f;
 #pragma unroll
             for (int x = 0; x < 64; ++x) run[x] = 0.f;
             if (ok && p > 0) {
                 bool w = true;
-                if (ct == 0)
-                    for (int q2 = 0; q2 < p && w; ++q2) w = flag_wait(fa.flags + (size_t)bh * P + q2, err, LA_ERR_TIMEOUT);
-                ok = CG::all(w);  // a barrier: thread 0's acquire precedes every thread's record loads
-                for (int q2 = 0; q2 < p && ok; ++q2) {
+                if (ct == 0) {
+                    int b = p - 1;
+                    const long long t0 = clock64();
+                    for (;;) {  // bounded: gives up after kWaitLimitCycles in all
+                        const unsigned f = flag_acquire(fl + b);
+                        if (f == 2u) break;
+                        if (f == 1u) {
+                            if (b == 0) { b = -1; break; }
+                            --b;
+                            continue;
+                        }
+                        if (clock64() - t0 > kWaitLimitCycles) {
+                            atomicCAS(err, 0, LA_ERR_TIMEOUT);
+                            w = false;
+                            break;
+                        }
+                        __nanosleep(128);
+                    }
+                    tmem_slot[2] = (uint32_t)(b + 1);
+                }
+                ok = CG::all(w);  // a barrier: thread 0's acquires precede every thread's record loads
+                const int b = (int)tmem_slot[2] - 1;
+                if (ok && b >= 0) {
+                    const float* rec = segp - ((size_t)(p - 1 - b)) * E;  // seg record b + 1 of this head
+                    const float4* src = reinterpret_cast<const float4*>(rec + (size_t)r * kD + 64 * h);
+#pragma unroll
+                    for (int x = 0; x < 16; ++x) {
+                        const float4 f = __ldcg(src + x);
+                        run[4 * x] = f.x;
+                        run[4 * x + 1] = f.y;
+                        run[4 * x + 2] = f.z;
+                        run[4 * x + 3] = f.w;
+                    }
+                    if (h == 0) run_z = __ldcg(rec + (size_t)kD * kD + r);
+                }
+                for (int q2 = b + 1; q2 < p && ok; ++q2) {
                     const float* rec = fa.agg + ((size_t)bh * P + q2) * E;
                     const float4* src = reinterpret_cast<const float4*>(rec + (size_t)r * kD + 64 * h);
 #pragma unroll
@@ -379,12 +421,40 @@ tc_causal_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                 }
             }
             if (ok) {
-                // the prefix record for the backward
-                float4* dst = reinterpret_cast<float4*>(segp + (size_t)r * kD + 64 * h);
+                // the first segment's prefix record (zero) for the backward; every other segment's
+                // record b + 1 is written by segment b as its inclusive prefix
+                if (p == 0) {
+                    float4* dst = reinterpret_cast<float4*>(segp + (size_t)r * kD + 64 * h);
 #pragma unroll
-                for (int x = 0; x < 16; ++x)
-                    dst[x] = make_float4(run[4 * x], run[4 * x + 1], run[4 * x + 2], run[4 * x + 3]);
-                if (h == 0) segp[(size_t)kD * kD + r] = run_z;
+                    for (int x = 0; x < 16; ++x) dst[x] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (h == 0) segp[(size_t)kD * kD + r] = 0.f;
+                }
+                // the inclusive prefix (prefix + own sums, still in TMEM; the scan's order): the next
+                // segment's prefix record, then flag 2
+                if (p < P - 1 && npre > 0) {
+                    float4* dst = reinterpret_cast<float4*>(segp + E + (size_t)r * kD + 64 * h);
+#pragma unroll
+                    for (int cb = 0; cb < 2; ++cb) {
+                        uint32_t w32[32];
+                        tmem_ld32(tmem + lane_base + kTmS + 64 * h + 32 * cb, w32);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int x = 0; x < 8; ++x)
+                            dst[8 * cb + x] = make_float4(run[32 * cb + 4 * x] + __uint_as_float(w32[4 * x]),
+                                                          run[32 * cb + 4 * x + 1] + __uint_as_float(w32[4 * x + 1]),
+                                                          run[32 * cb + 4 * x + 2] + __uint_as_float(w32[4 * x + 2]),
+                                                          run[32 * cb + 4 * x + 3] + __uint_as_float(w32[4 * x + 3]));
+                    }
+                    if (h == 0) {
+                        uint32_t zv[16];
+                        tmem_ld16(tmem + lane_base + kTmZ, zv);
+                        tmem_ld_wait();
+                        segp[E + (size_t)kD * kD + r] = run_z + __uint_as_float(zv[0]);
+                    }
+                    __threadfence();
+                    CG::sync();
+                    if (ct == 0 && !withheld) flag_release(fl + p, 2u);
+                }
                 // the state after position N: prefix + own sums (still in TMEM), the scan's order
                 if (fa.S_out && p == P - 1) {
 #pragma unroll
@@ -541,7 +611,7 @@ tc_causal_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             tc_fence_before();
             CG::sync();
             if (ct == kStoreThread) {
-                check_tile(D > 64 ? 64 : 0, c0, bh, N);
+                check_tile(D > 64 ? 64 : 0, c0, bh, N, nBH);
                 tma_store_3d(&tm_o, sSb, 0, c0, bh);
                 if (D > 64) tma_store_3d(&tm_o, sSb + kBlockBytes, 64, c0, bh);
                 bulk_commit();
