@@ -278,10 +278,12 @@ def run_ours(args):
     la.timing_enable(False)
     ktimes = la.timing_read()
     if args.workload == "profile":
-        # two retention forwards, two non-causal forwards and two non-causal backwards at the
-        # same shape, outside the timed region, so that one small command also covers their
-        # kernels in an ncu capture
+        # two one-launch causal forwards, two retention forwards, two non-causal forwards and two
+        # non-causal backwards at the same shape, outside the timed region, so that one small
+        # command also covers their kernels in an ncu capture
         gam = W.retention_gammas(H).to(dev)
+        for _ in range(2):
+            la.causal_fwd(qd, kd, vd, out=o, one_launch=True)
         for _ in range(2):
             la.retention_fwd(qd, kd, vd, gam, out=o)
         for _ in range(2):
@@ -368,6 +370,7 @@ def run_ours(args):
         result["noncausal"] = bench_noncausal(la, dev)
         result["retention"] = bench_retention(la, dev)
         result["retention"]["step"] = ret_step
+        result["forward_forms"] = bench_forward_forms(la, dev)
         result["sweep"] = {"workload": "causal fwd+bwd bf16 B=1 H=8 Dk=Dv=64, N = 2^9 .. 2^16 (seed 3)",
                            "l2": "flushed before every timed step", "steps_per_n": 10,
                            "peak": "torch.cuda.max_memory_allocated above the flush buffer: inputs, outputs, "
@@ -510,6 +513,40 @@ def bench_noncausal(la, dev):
                      "workload": "noncausal " + name.split("_")[1] + " bf16 B=2 H=16 N=65536 Dk=Dv=128",
                      "l2": "inputs larger than L2"}
     return res
+
+
+def bench_forward_forms(la, dev):
+    """The causal forward as three launches (la_causal_fwd: segment sums, scan, outputs) and as
+    one launch with a chained scan (la_causal_fwd_fused), median of 10 calls each, at the
+    long-context shape (inputs larger than L2) and at shorter shapes (L2 flushed before each
+    call)."""
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    shapes = [(W.LONG_BF16, None), (W.FWD_BF16, None), (W.sweep(512), None), (W.sweep(2048), None)]
+    out = {}
+    for w, _ in shapes:
+        q, k, v = (t.to(dev) for t in W.make_inputs(w))
+        o = torch.empty_like(v)
+        ws = torch.empty(la.workspace_bytes(la.OP_CAUSAL_FWD, w.B, w.H, w.N, w.Dk, w.Dv, w.dtype),
+                         dtype=torch.uint8, device=dev)
+        row = {}
+        for form, one in (("three_launches", False), ("one_launch", True)):
+            for _ in range(3):
+                la.causal_fwd(q, k, v, out=o, workspace=ws, one_launch=one)
+            times = []
+            for _ in range(10):
+                if w.N < 65536:
+                    flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                la.causal_fwd(q, k, v, out=o, workspace=ws, one_launch=one)
+                e1.record()
+                torch.cuda.synchronize()
+                times.append(e0.elapsed_time(e1))
+            row[form + "_ms"] = statistics.median(times)
+        out["causal fwd bf16 B=%d H=%d N=%d Dk=Dv=%d" % (w.B, w.H, w.N, w.Dk)] = row
+        del q, k, v, o, ws
+    del flush
+    return out
 
 
 def bench_retention_step(la, dev):
@@ -731,8 +768,8 @@ def main():
                     help="only 5 decode steps at B=64 and 5 at B=8000 (H=8 D=32), for ncu captures")
     ap.add_argument("--workload", choices=("long", "profile"), default="long",
                     help="long: B=2 H=16 N=65536 D=128 (the benchmark); profile: B=1 H=16 N=32768, plus two "
-                         "retention forwards, two non-causal forwards and two non-causal backwards of that "
-                         "shape after the timed steps (ncu captures)")
+                         "one-launch causal forwards, two retention forwards, two non-causal forwards and two "
+                         "non-causal backwards of that shape after the timed steps (ncu captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -56,6 +56,7 @@ def _declare(lib):
     lib.la_workspace_bytes.restype = ctypes.c_size_t
     lib.la_noncausal_fwd.argtypes = [_vp, _vp, _vp, _vp, Shape, _vp, ctypes.c_size_t, _vp]
     lib.la_causal_fwd.argtypes = [_vp, _vp, _vp, _vp, Shape, _vp, ctypes.c_size_t, _vp]
+    lib.la_causal_fwd_fused.argtypes = [_vp, _vp, _vp, _vp, Shape, _vp, ctypes.c_size_t, _vp]
     lib.la_causal_bwd.argtypes = [_vp] * 7 + [Shape, _vp, ctypes.c_size_t, _vp]
     lib.la_host_step_bytes.argtypes = [Shape, ctypes.c_int]
     lib.la_host_step_bytes.restype = ctypes.c_size_t
@@ -71,7 +72,7 @@ def _declare(lib):
     for f in ("la_causal_step_host", "la_noncausal_fwd", "la_noncausal_bwd", "la_causal_fwd",
               "la_causal_fwd_with_state", "la_causal_bwd", "la_causal_bwd_after_fwd", "la_recurrent_step",
               "la_retention_fwd", "la_retention_step", "la_selftest_bounded_wait", "la_selftest_lookback_timeout",
-              "la_last_error",
+              "la_last_error", "la_causal_fwd_fused",
               "la_clear_error", "la_timing_enable", "la_timing_reset"):
         getattr(lib, f).restype = ctypes.c_int
     lib.la_last_error.argtypes = []
@@ -179,11 +180,13 @@ def noncausal_fwd(q, k, v, out=None, workspace=None, stream=None):
     return out
 
 
-def causal_fwd(q, k, v, out=None, workspace=None, stream=None, return_state=False):
+def causal_fwd(q, k, v, out=None, workspace=None, stream=None, return_state=False, one_launch=False):
     """Causal linear attention (j <= i) in the chunked form; returns o [B,H,N,Dv].
 
     With return_state, returns (o, S, z): the fp32 state after the last position
-    (S [B,H,Dk,Dv], z [B,H,Dk]), from which recurrent_step continues.
+    (S [B,H,Dk,Dv], z [B,H,Dk]), from which recurrent_step continues.  With
+    one_launch, runs la_causal_fwd_fused (the same results from one kernel launch
+    with a chained scan; bf16 heads of 64 or 128).
     """
     _need_cuda(q, k, v)
     s = _shape4(q, k, v)
@@ -191,8 +194,9 @@ def causal_fwd(q, k, v, out=None, workspace=None, stream=None, return_state=Fals
         out = torch.empty_like(v)
     ws, nb = _workspace(OP_CAUSAL_FWD, s, q.device, workspace)
     if not return_state:
-        _check(library().la_causal_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), s, _ptr(ws), nb, _stream_ptr(stream)),
-               "la_causal_fwd")
+        fn = library().la_causal_fwd_fused if one_launch else library().la_causal_fwd
+        _check(fn(_ptr(q), _ptr(k), _ptr(v), _ptr(out), s, _ptr(ws), nb, _stream_ptr(stream)),
+               "la_causal_fwd_fused" if one_launch else "la_causal_fwd")
         return out
     B, H, _, Dk = q.shape
     S = torch.empty(B, H, Dk, v.shape[-1], dtype=torch.float32, device=q.device)

@@ -346,9 +346,14 @@ static la_status check_bwd_args(const void* q, const void* k, const void* v, con
     return LA_OK;
 }
 
+// The causal forward.  one_launch selects the single-kernel form (segment sums, chained scan
+// and outputs in one launch) where the tensor-core path runs; otherwise the segment sums, the
+// scan and the output pass are three launches, which measure faster at every size timed (the
+// chained scan's look-back reads the earlier segments' records one L2 round trip at a time
+// whenever their inclusive prefixes are not yet published, as in a first wave).
 static la_status causal_fwd_impl(const void* q, const void* k, const void* v, void* o, float* S_out, float* z_out,
                                  la_shape s, void* ws, size_t ws_bytes, la_stream_t stream,
-                                 bool withhold_first = false) {
+                                 bool one_launch = false, bool withhold_first = false) {
     t_detail.clear();
     LA_TRY(check_shape(s));
     if (empty(s)) {
@@ -378,7 +383,7 @@ static la_status causal_fwd_impl(const void* q, const void* k, const void* v, vo
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     char* base = static_cast<char*>(ws);
     float* seg = reinterpret_cast<float*>(base + w.seg_states);
-    if (p.tc) {  // one kernel: segment sums, chained scan and outputs (plus a memset of its flags)
+    if (p.tc && one_launch) {  // one kernel: segment sums, chained scan and outputs (after a memset of its flags)
         LA_TRY(cuda_status(tc_causal_fwd_fused(q, k, v, o, seg, reinterpret_cast<float*>(base + w.agg),
                                                reinterpret_cast<unsigned*>(base + w.flags), S_out, z_out, s, p, st,
                                                withhold_first),
@@ -453,6 +458,11 @@ la_status la_causal_fwd(const void* q, const void* k, const void* v, void* o, la
     return causal_fwd_impl(q, k, v, o, nullptr, nullptr, s, ws, ws_bytes, stream);
 }
 
+la_status la_causal_fwd_fused(const void* q, const void* k, const void* v, void* o, la_shape s, void* ws,
+                              size_t ws_bytes, la_stream_t stream) {
+    return causal_fwd_impl(q, k, v, o, nullptr, nullptr, s, ws, ws_bytes, stream, true);
+}
+
 la_status la_causal_fwd_with_state(const void* q, const void* k, const void* v, void* o, float* S, float* z,
                                    la_shape s, void* ws, size_t ws_bytes, la_stream_t stream) {
     if (!S || !z) {
@@ -470,7 +480,7 @@ la_status la_selftest_lookback_timeout(const void* q, const void* k, const void*
     if (empty(s) || !p.tc || p.P < 2)
         return fail(LA_ERR_INVALID_ARG, "the look-back self-test needs a tensor-core shape with two or more segments "
                                         "(bf16, Dk = Dv = 64 or 128; this one has %d)", empty(s) ? 0 : p.P);
-    return causal_fwd_impl(q, k, v, o, nullptr, nullptr, s, ws, ws_bytes, stream, true);
+    return causal_fwd_impl(q, k, v, o, nullptr, nullptr, s, ws, ws_bytes, stream, true, true);
 }
 
 la_status la_causal_bwd(const void* q, const void* k, const void* v, const void* dout, void* dq, void* dk, void* dv,

@@ -280,7 +280,8 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
                 dpart[128 * h + r] = di;
             }
             // (c) A = tril(QK^T) as bf16 hi + lo on this thread's keys [64h, 64h+64), in place
-            // (see the X layout); the row sums of hi + lo (the operands A V uses) go to den
+            // (see the X layout); its fp32 row sums (equal to those of hi + lo, the operands A V
+            // uses, to about 2^-17) go to den
             if (!FG::all(mbar_wait(&bar->qk_done, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
             tc_fence_after();
             {
@@ -302,7 +303,7 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
                                 const float a0 = __uint_as_float(w[2 * x]), a1 = __uint_as_float(w[2 * x + 1]);
                                 hi[x] = pack_bf16x2(a0, a1);
                                 lo[x] = pack_bf16x2(a0 - bf_lo(hi[x]), a1 - bf_hi(hi[x]));
-                                rs += (bf_lo(hi[x]) + bf_lo(lo[x])) + (bf_hi(hi[x]) + bf_hi(lo[x]));
+                                rs += a0 + a1;
                             }
                         } else {
 #pragma unroll
@@ -312,7 +313,7 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
                                 const float a1 = j + 1 <= r ? __uint_as_float(w[2 * x + 1]) : 0.f;
                                 hi[x] = pack_bf16x2(a0, a1);
                                 lo[x] = pack_bf16x2(a0 - bf_lo(hi[x]), a1 - bf_hi(hi[x]));
-                                rs += (bf_lo(hi[x]) + bf_lo(lo[x])) + (bf_hi(hi[x]) + bf_hi(lo[x]));
+                                rs += a0 + a1;
                             }
                         }
                     }

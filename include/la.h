@@ -107,16 +107,28 @@ la_status la_noncausal_fwd(const void* q, const void* k, const void* v, void* o,
  * than the chunk size is masked.  (Digest, 핵심 구성요소 3; velog review 3.4;
  * itwiki 계산 형태 비교, chunked row, and 구현.)
  * q, k: [B,H,N,Dk]; v: [B,H,N,Dv]; o: [B,H,N,Dv] (written).
- * bf16 heads of 64 or 128 run as one kernel launch (after a memset of a few KB
- * of flags in the workspace): each block forms its segment's own sums, publishes
- * them, adds the earlier segments' in segment order (a chained scan whose waits
- * are bounded: a wait that runs out records LA_ERR_TIMEOUT in the sticky word)
- * and writes the outputs.  Other shapes run the sums, a scan and the output pass
- * as three launches.  Either way the workspace keeps every segment's starting
- * state for la_causal_bwd_after_fwd.
+ * Runs as three launches: the segments' own sums, their exclusive scan and the
+ * output pass.  The workspace keeps every segment's starting state for
+ * la_causal_bwd_after_fwd.
  */
 la_status la_causal_fwd(const void* q, const void* k, const void* v, void* o, la_shape s,
                         void* ws, size_t ws_bytes, la_stream_t stream);
+
+/*
+ * la_causal_fwd as one kernel launch (after a memset of a few KB of flags in the
+ * workspace) for bf16 heads of 64 or 128; other shapes run la_causal_fwd.
+ * Arguments, workspace and results are those of la_causal_fwd, bit for bit: each
+ * block forms its segment's own sums, publishes them, adds the earlier segments'
+ * (a chained scan in segment order, the separate scan's additions exactly) and
+ * writes the outputs.  Every wait is bounded: one that runs out records
+ * LA_ERR_TIMEOUT in the sticky word and the block ends.  Blocks take their work
+ * from a ticket counter, so a block only waits on blocks already running.  It
+ * saves two launches; it is not faster at the sizes measured, because a block
+ * adds the earlier segments' published sums one L2 round trip at a time while
+ * their prefixes are not yet complete.
+ */
+la_status la_causal_fwd_fused(const void* q, const void* k, const void* v, void* o, la_shape s,
+                              void* ws, size_t ws_bytes, la_stream_t stream);
 
 /*
  * la_causal_fwd that also returns the state after the last position, the (S, z)

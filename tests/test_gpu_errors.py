@@ -119,15 +119,32 @@ def test_lookback_selftest_refuses_shapes_without_a_chained_scan(la):
         la.selftest_lookback_timeout(qb, qb, qb)
 
 
-def test_tensor_core_causal_forward_is_one_kernel(la):
-    """bf16 heads of 64 and 128: la_causal_fwd launches one kernel (after a memset of its flags)."""
+def test_tensor_core_fused_forward_is_one_kernel(la):
+    """bf16 heads of 64 and 128: la_causal_fwd_fused launches one kernel (after a memset of its
+    flags) and gives la_causal_fwd's outputs and segment records bit for bit."""
     for D in (64, 128):
-        q = torch.randn(2, 3, 3000, D, device=DEV).bfloat16()
+        q, k, v = (torch.randn(2, 3, 3000, D, device=DEV).bfloat16() * 0.1 for _ in range(3))
+        wsf = torch.empty(la.workspace_bytes(la.OP_CAUSAL_FWD, 2, 3, 3000, D, D, torch.bfloat16), dtype=torch.uint8,
+                          device=DEV)
+        ws3 = torch.empty_like(wsf)
         la.timing_reset()
         la.timing_enable(True)
         try:
-            la.causal_fwd(q, q, q)
+            o1 = la.causal_fwd(q, k, v, workspace=wsf, one_launch=True)
             t = la.timing_read()
         finally:
             la.timing_enable(False)
         assert list(t) == ["tc_causal_fwd_fused"] and t["tc_causal_fwd_fused"][0] == 1, t
+        o3 = la.causal_fwd(q, k, v, workspace=ws3)
+        torch.cuda.synchronize()
+        assert torch.equal(o1, o3)
+        # the segment prefix records (the first region of the workspace) match bit for bit
+        rec = _segment_records_bytes(la, 2, 3, 3000, D)
+        assert torch.equal(wsf[:rec], ws3[:rec])
+
+
+def _segment_records_bytes(la, B, H, N, D):
+    """Bytes of the forward workspace's prefix records: B*H*P padded (128 x 128 + 128) fp32
+    records, P read back from the retention workspace (same planner)."""
+    P = la.workspace_bytes(la.OP_RETENTION_FWD, B, H, N, D, D, torch.bfloat16) // (B * H * 128 * 128 * 4)
+    return B * H * P * (128 * 128 + 128) * 4

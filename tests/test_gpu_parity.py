@@ -509,3 +509,33 @@ def test_noncausal_bwd_long_sampled_heads(la):
     sel = lambda t: torch.stack([t[b, h] for b, h in heads])[None]
     ref = oracle.noncausal_bwd_assoc(sel(q), sel(k), sel(v), sel(dO))
     check_all([(n, sel(a), b) for n, a, b in zip(("dq", "dk", "dv"), (dq, dk, dv), ref)], 2e-2)
+
+
+# ---------------------------------------------------------------- one-launch forward (chained scan)
+@pytest.mark.parametrize("B,H,N,D", [(1, 3, 4097, 128), (2, 2, 3000, 64), (1, 2, 1000, 128), (4, 8, 1024, 64),
+                                     (1, 1, 1 << 16, 128)])
+def test_one_launch_forward_matches_oracle_and_feeds_the_backward(la, B, H, N, D):
+    """la_causal_fwd_fused against the oracle; the backward that reads its workspace gives
+    la_causal_bwd's gradients bit for bit (its segment prefixes are the scan's exactly)."""
+    q, k, v, dO = W.random_case(800 + N, B, H, N, D, D, dtype=torch.bfloat16, scale=D ** -0.5, with_grad=True)
+    qd, kd, vd, dOd = dev(q, k, v, dO)
+    ws_f = torch.empty(la.workspace_bytes(la.OP_CAUSAL_FWD, B, H, N, D, D, torch.bfloat16), dtype=torch.uint8,
+                       device=DEV)
+    o = la.causal_fwd(qd, kd, vd, workspace=ws_f, one_launch=True)
+    got = la.causal_bwd(qd, kd, vd, dOd, fwd_workspace=ws_f)
+    ref_b = la.causal_bwd(qd, kd, vd, dOd)
+    torch.cuda.synchronize()
+    check("o", o, oracle.causal_recurrent(q, k, v), 2e-2)
+    for name, a, b in zip(("dq", "dk", "dv"), got, ref_b):
+        assert torch.equal(a, b), name
+
+
+def test_one_launch_forward_long_sampled_heads(la):
+    """The one-launch forward at B=2 H=16 N=65536 D=128 (19 segments per head, four waves):
+    two whole heads against the oracle."""
+    w = W.LONG_BF16
+    q, k, v = W.make_inputs(w)
+    o = la.causal_fwd(*dev(q, k, v), one_launch=True).cpu()
+    for b, h in [(0, 0), (1, 15)]:
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        check("head (%d,%d)" % (b, h), o[sl], oracle.causal_recurrent(q[sl], k[sl], v[sl]), 2e-2)
