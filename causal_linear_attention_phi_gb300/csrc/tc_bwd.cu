@@ -74,7 +74,7 @@ struct FwdSweepSmem {
     static constexpr int drpart = racc + 512;   // float[8][128] per-warp column sums of this chunk's g phi(q)
     static constexpr int gsh = drpart + 4096;   // float[128] g of the chunk's rows
     static constexpr int rpart = gsh + 512;     // float[2][128] row sums of A, later of D, per column half
-    static constexpr int dpart = rpart + 1024;  // float[128] phi(q) . z_prev (the rest of this slot unused)
+    static constexpr int dpart = rpart + 1024;  // float[2][128] phi(q) . z_prev, per column half
     static constexpr int tpart = dpart + 1024;  // float[2][128] P . num, per column half
     static constexpr int bars = tpart + 1024;
     static constexpr int tmem_slot = bars + 256;
@@ -89,7 +89,7 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
                             const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                             const __grid_constant__ CUtensorMap tm_dq, const float* __restrict__ seg_S,
                             float* __restrict__ seg_R, float* __restrict__ den_g, int N, int nchunks, int cps, int P,
-                            int* err, const __nv_bfloat16* __restrict__ qg) {
+                            int* err) {
     extern __shared__ uint8_t smem_raw[];
     constexpr int kKd = D / 16;  // K steps of a product over a head dimension (a 64-wide head is zero above)
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -246,8 +246,7 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
             if (ct == kStoreThread) bulk_wait_read_all();  // the previous dq store has left the Sb tile
             if (!FG::all(mbar_wait(&bar->full_qv, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
             tc_fence_after();
-            // phi(Q) in place, and each row's phi(q_r) . z_prev (into dpart[r]) on the way
-            FG::phi_tile(sQ, nullptr, ct, n, D, nullptr, nullptr, nullptr, nullptr, zsh, dpart);
+            FG::phi_tile(sQ, nullptr, ct, n, D, nullptr, nullptr);
             tmem_half_row_to_tile(tmem + lb + kFS, sSb, r, h);
             tc_fence_before();
             fence_proxy_async_smem();
@@ -260,6 +259,26 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
             fence_proxy_async_smem();
             FG::sync();
             if (ct == 0) mbar_arrive(&bar->qk_ready);
+            // while Q K^T is formed: phi(q_r) on this thread's 64 columns stays in registers for
+            // phi'(q) in the dq epilogue (Q is released before it); phi(q_r) . z_prev
+            uint32_t qrow[32];
+            {
+                float di = 0.f;
+#pragma unroll
+                for (int c8 = 0; c8 < 8; ++c8) {
+                    const int lc = 8 * h + c8;
+                    const uint4 qv = *reinterpret_cast<const uint4*>(sQ + chunk_off(r, lc));
+                    qrow[4 * c8 + 0] = qv.x;
+                    qrow[4 * c8 + 1] = qv.y;
+                    qrow[4 * c8 + 2] = qv.z;
+                    qrow[4 * c8 + 3] = qv.w;
+                    const float4 za = *reinterpret_cast<const float4*>(zsh + 8 * lc);
+                    const float4 zb = *reinterpret_cast<const float4*>(zsh + 8 * lc + 4);
+                    di += bf_lo(qv.x) * za.x + bf_hi(qv.x) * za.y + bf_lo(qv.y) * za.z + bf_hi(qv.y) * za.w +
+                          bf_lo(qv.z) * zb.x + bf_hi(qv.z) * zb.y + bf_lo(qv.w) * zb.z + bf_hi(qv.w) * zb.w;
+                }
+                dpart[128 * h + r] = di;
+            }
             // (c) A = tril(QK^T) as bf16 hi + lo on this thread's keys [64h, 64h+64), in place
             // (see the X layout); its fp32 row sums (equal to those of hi + lo, the operands A V
             // uses, to about 2^-17) go to den
@@ -310,7 +329,7 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
             // (d) den (the row sums of A and phi(q) . z_prev are in); P = dO / den in place (bf16)
             // on this thread's 64 columns while A V is formed; then g = -P . num / den from
             // that bf16 P
-            const float den = valid ? rpart[r] + rpart[128 + r] + dpart[r] : 1.f;
+            const float den = valid ? rpart[r] + rpart[128 + r] + dpart[r] + dpart[128 + r] : 1.f;
             const float inv = 1.f / den;
 #pragma unroll
             for (int c8 = 0; c8 < 8; ++c8) {
@@ -420,17 +439,7 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
             if (ct == 0) mbar_arrive(&bar->d_ready);
             // (f) dq = (dQ~ + rowsum(D) + g z_prev) * phi'(q), this thread's 64 columns, staged in
             // the Sb tile (free once the dq products are done) and written by one TMA store
-            // (rows past N are not written).  phi'(q) comes from this row's q, read again from
-            // global memory (L2) while the dq products run: the Q tile is gone by now.
-            uint4 qraw[8];
-            if (valid && 64 * h < D && LA_DCHECK(c0 + r < N)) {
-                const uint4* src = reinterpret_cast<const uint4*>(qg + ((size_t)bh * N + c0 + r) * D + 64 * h);
-#pragma unroll
-                for (int x = 0; x < 8; ++x) qraw[x] = __ldg(src + x);
-            } else {
-#pragma unroll
-                for (int x = 0; x < 8; ++x) qraw[x] = make_uint4(0u, 0u, 0u, 0u);
-            }
+            // (rows past N are not written)
             if (!FG::all(mbar_wait(&bar->dq_done, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
             tc_fence_after();
             const float dsum = rpart[r] + rpart[128 + r];
@@ -441,7 +450,7 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
                 tmem_ld_wait();
 #pragma unroll
                 for (int c4 = 0; c4 < 4; ++c4) {
-                    const uint32_t* qu = reinterpret_cast<const uint32_t*>(&qraw[4 * cb + c4]);
+                    const uint32_t* qu = &qrow[4 * (4 * cb + c4)];
                     uint4 o4;
                     uint32_t* ou = reinterpret_cast<uint32_t*>(&o4);
                     float zr[8];
@@ -451,9 +460,9 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const float a0 = (__uint_as_float(w[8 * c4 + 2 * e]) + fmaf(g, zr[2 * e], dsum)) *
-                                         dphi_from_phi(phi_f(bf_lo(qu[e])));
+                                         dphi_from_phi(bf_lo(qu[e]));
                         const float a1 = (__uint_as_float(w[8 * c4 + 2 * e + 1]) + fmaf(g, zr[2 * e + 1], dsum)) *
-                                         dphi_from_phi(phi_f(bf_hi(qu[e])));
+                                         dphi_from_phi(bf_hi(qu[e]));
                         ou[e] = pack_bf16x2(a0, a1);
                     }
                     *reinterpret_cast<uint4*>(sSb + chunk_off(r, 8 * h + 4 * cb + c4)) = o4;
@@ -820,8 +829,7 @@ cudaError_t tc_bwd_forward_sweep(const void* q, const void* k, const void* v, co
     if (e != cudaSuccess) return e;
     launch_begin("tc_bwd_forward_sweep", st);
     kern<<<dim3(p.P, BH), kThreadsFS, kFwdSweepSmem, st>>>(tq, tk, tv, td, tdq, seg_S, seg_R, den_g, s.N, p.nchunks,
-                                                           p.cps, p.P, device_error_word(),
-                                                           static_cast<const __nv_bfloat16*>(q));
+                                                           p.cps, p.P, device_error_word());
     return launch_end("tc_bwd_forward_sweep", st);
 }
 

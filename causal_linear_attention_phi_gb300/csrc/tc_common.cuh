@@ -189,43 +189,25 @@ struct Grp {
     // (column_part).  With lo_tile, also writes lo = bf16(phi - hi) there, or,
     // with kMinusOne, bf16(phi - 1) (0 outside the rows and columns in range);
     // with copy_tile, a second copy of the rounded values.
-    // With rowdot_w, also the dot of each row's rounded values with rowdot_w[0..127] (fp32,
-    // shared memory), written to rowdot[row] (one thread per row).
     template <bool kMinusOne = false>
     __device__ static __forceinline__ void phi_tile(uint8_t* tile, uint8_t* lo_tile, int ct, int n, int dcols,
                                                     const float* w, float* colpart, uint8_t* copy_tile = nullptr,
-                                                    const float* scale = nullptr, const float* rowdot_w = nullptr,
-                                                    float* rowdot = nullptr) {
+                                                    const float* scale = nullptr) {
         // a whole tile (every row and column in range: all chunks but a short last one of a
         // full-width head) takes the copy of the body without the per-element range test; a
         // 64-wide head leaves the upper column block alone (its TMA zero fill stays in place,
         // and the lo and copy tiles there feed only output columns that are never stored)
         if (n >= kC && dcols >= kD)
-            phi_tile_body<true, false, kMinusOne>(tile, lo_tile, ct, n, dcols, w, colpart, copy_tile, scale,
-                                                  rowdot_w, rowdot);
+            phi_tile_body<true, false, kMinusOne>(tile, lo_tile, ct, n, dcols, w, colpart, copy_tile, scale);
         else if (dcols <= kD / 2)
-            phi_tile_body<false, true, kMinusOne>(tile, lo_tile, ct, n, dcols, w, colpart, copy_tile, scale,
-                                                  rowdot_w, rowdot);
+            phi_tile_body<false, true, kMinusOne>(tile, lo_tile, ct, n, dcols, w, colpart, copy_tile, scale);
         else
-            phi_tile_body<false, false, kMinusOne>(tile, lo_tile, ct, n, dcols, w, colpart, copy_tile, scale,
-                                                   rowdot_w, rowdot);
+            phi_tile_body<false, false, kMinusOne>(tile, lo_tile, ct, n, dcols, w, colpart, copy_tile, scale);
     }
     template <bool kWhole, bool kHalf, bool kMinusOne = false>
     __device__ static __forceinline__ void phi_tile_body(uint8_t* tile, uint8_t* lo_tile, int ct, int n, int dcols,
                                                          const float* w, float* colpart, uint8_t* copy_tile,
-                                                         const float* scale, const float* rowdot_w, float* rowdot) {
-        // row dots: this thread's vectors j and j + kJ / 2 lie in the same row (one per column
-        // block), and the eight lanes with equal ct >> 3 cover that row's 16 vectors
-        float rd[kJ / 2];
-        float dw[2][8];
-#pragma unroll
-        for (int j = 0; j < kJ / 2; ++j) rd[j] = 0.f;
-        if (rowdot_w) {
-#pragma unroll
-            for (int b = 0; b < 2; ++b)
-#pragma unroll
-                for (int e = 0; e < 8; ++e) dw[b][e] = rowdot_w[64 * b + 8 * vec_lc(ct) + e];
-        }
+                                                         const float* scale) {
         float zp[2][8];
 #pragma unroll
         for (int b = 0; b < 2; ++b)
@@ -257,27 +239,12 @@ struct Grp {
                     zp[vec_block(j)][2 * e] = fmaf(wr, bf_lo(u[e]), zp[vec_block(j)][2 * e]);
                     zp[vec_block(j)][2 * e + 1] = fmaf(wr, bf_hi(u[e]), zp[vec_block(j)][2 * e + 1]);
                 }
-                if (rowdot_w) {
-                    float& acc = rd[j % (kJ / 2)];
-                    acc = fmaf(dw[vec_block(j)][2 * e], bf_lo(u[e]), acc);
-                    acc = fmaf(dw[vec_block(j)][2 * e + 1], bf_hi(u[e]), acc);
-                }
             }
             *reinterpret_cast<uint4*>(tile + vec_off(ct, j)) = v[j];
             if (lo_tile) *reinterpret_cast<uint4*>(lo_tile + vec_off(ct, j)) = l;
             if (copy_tile) *reinterpret_cast<uint4*>(copy_tile + vec_off(ct, j)) = v[j];
         }
         if (colpart) column_part(zp, colpart, ct);
-        if (rowdot_w) {
-#pragma unroll
-            for (int j = 0; j < kJ / 2; ++j) {
-                float x = rd[j];
-                x += __shfl_xor_sync(0xffffffffu, x, 1);
-                x += __shfl_xor_sync(0xffffffffu, x, 2);
-                x += __shfl_xor_sync(0xffffffffu, x, 4);
-                if ((ct & 7) == 0) rowdot[vec_row(ct, j)] = x;
-            }
-        }
     }
 };
 
