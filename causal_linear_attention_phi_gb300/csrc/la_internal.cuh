@@ -111,6 +111,34 @@ __host__ __device__ constexpr bool pass() { return true; }
 #define LA_DCHECK(cond) (::la::dbg::pass())
 #endif
 
+// ------------------------------------------------------------------ programmatic dependent launch
+// Kernels launched with launch_pdl may be scheduled while the previous kernel in
+// the stream finishes its last blocks.  Each such kernel calls pdl_enter() after its
+// prologue (barrier init, TMEM allocation, tensor-map prefetch) and before any
+// global-memory access: it waits until the previous grid has completed and its
+// writes are visible, and lets the next kernel be scheduled (which happens once
+// every block of this grid has reached this point, so a waiting dependent block
+// never holds an SM that a block of this grid still needs).
+__device__ __forceinline__ void pdl_enter() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
 // ------------------------------------------------------------------ launch bookkeeping
 // Every launch goes through launch_begin/launch_end so the optional per-kernel
 // timing (la_timing_enable) can bracket it with events on the launch stream.

@@ -89,6 +89,7 @@ constexpr int kScanBatch = 24;  // covers the segment counts the planner picks f
 
 __global__ void scan_kernel(float* __restrict__ seg, float* __restrict__ totS, float* __restrict__ totz, size_t sS,
                             size_t sz, int P, size_t E, int sk, int sv, int Dk, int Dv, int mode) {
+    pdl_enter();  // launched with programmatic dependent launch: the records are visible from here on
     const size_t e4 = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
     if (e4 >= E) return;
     const size_t bh = blockIdx.y;
@@ -748,9 +749,11 @@ cudaError_t scan_segments(float* seg, float* totals, const la_shape& s, const Pl
     const size_t SkSv = (size_t)p.sk * p.sv;
     dim3 grid((unsigned)((E / 4 + 127) / 128), s.B * s.H);
     launch_begin("scan_segments", st);
-    scan_kernel<<<grid, 128, 0, st>>>(seg, totals, totals ? totals + SkSv : nullptr, E, E, p.P, E, p.sk, p.sv, p.sk,
-                                      p.sv, mode);
-    return launch_end("scan_segments", st);
+    const cudaError_t e = launch_pdl(scan_kernel, grid, dim3(128), 0, st, seg, totals,
+                                     totals ? totals + SkSv : (float*)nullptr, E, E, p.P, E, p.sk, p.sv, p.sk, p.sv,
+                                     mode);
+    const cudaError_t e2 = launch_end("scan_segments", st);
+    return e != cudaSuccess ? e : e2;
 }
 
 cudaError_t scan_segments_unpadded_totals(float* seg, float* totals, const la_shape& s, const Plan& p,

@@ -136,6 +136,7 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    pdl_enter();  // the previous kernel's outputs (segment records, (den, g)) are visible from here on
 
     if (warp == 0) {
         if (lane == 0) {
@@ -580,6 +581,7 @@ tc_bwd_reverse_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    pdl_enter();  // the previous kernel's outputs (segment records, (den, g)) are visible from here on
 
     if (warp == 0) {
         if (lane == 0) {
@@ -828,9 +830,10 @@ cudaError_t tc_bwd_forward_sweep(const void* q, const void* k, const void* v, co
                                          (int)kFwdSweepSmem);
     if (e != cudaSuccess) return e;
     launch_begin("tc_bwd_forward_sweep", st);
-    kern<<<dim3(p.P, BH), kThreadsFS, kFwdSweepSmem, st>>>(tq, tk, tv, td, tdq, seg_S, seg_R, den_g, s.N, p.nchunks,
-                                                           p.cps, p.P, device_error_word());
-    return launch_end("tc_bwd_forward_sweep", st);
+    e = launch_pdl(kern, dim3(p.P, BH), dim3(kThreadsFS), kFwdSweepSmem, st, tq, tk, tv, td, tdq, seg_S, seg_R, den_g,
+                   s.N, p.nchunks, p.cps, p.P, device_error_word());
+    cudaError_t e2 = launch_end("tc_bwd_forward_sweep", st);
+    return e != cudaSuccess ? e : e2;
 }
 
 cudaError_t tc_bwd_reverse_sweep(const void* q, const void* k, const void* v, const void* dout, void* dk, void* dv,
@@ -849,9 +852,10 @@ cudaError_t tc_bwd_reverse_sweep(const void* q, const void* k, const void* v, co
                                          (int)kRevSweepSmem);
     if (e != cudaSuccess) return e;
     launch_begin("tc_bwd_reverse_sweep", st);
-    kern<<<dim3(p.P, BH), kThreadsRS, kRevSweepSmem, st>>>(tq, tk, tv, td, tdk, tdv, seg_R, den_g, s.N, p.nchunks,
-                                                           p.cps, p.P, device_error_word());
-    return launch_end("tc_bwd_reverse_sweep", st);
+    e = launch_pdl(kern, dim3(p.P, BH), dim3(kThreadsRS), kRevSweepSmem, st, tq, tk, tv, td, tdk, tdv, seg_R, den_g,
+                   s.N, p.nchunks, p.cps, p.P, device_error_word());
+    cudaError_t e2 = launch_end("tc_bwd_reverse_sweep", st);
+    return e != cudaSuccess ? e : e2;
 }
 
 }  // namespace la

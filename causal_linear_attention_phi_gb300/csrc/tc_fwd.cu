@@ -189,6 +189,7 @@ tc_causal_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    pdl_enter();  // the previous kernel's outputs (segment records) are visible from here on
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
@@ -702,8 +703,10 @@ cudaError_t tc_causal_fwd(const void* q, const void* k, const void* v, void* o, 
     if (e != cudaSuccess) return e;
     const char* name = out_pass ? "tc_causal_fwd_out" : split_k ? "tc_segment_sums_split" : "tc_segment_sums";
     launch_begin(name, st);
-    kern<<<grid, kThreads, kSmemBytes, st>>>(tq, tk, tv, to, seg, s.N, p.nchunks, p.cps, p.P, err, FusedArgs{});
-    return launch_end(name, st);
+    e = launch_pdl(kern, grid, dim3(kThreads), kSmemBytes, st, tq, tk, tv, to, seg, s.N, p.nchunks, p.cps, p.P, err,
+                   FusedArgs{});
+    cudaError_t e2 = launch_end(name, st);
+    return e != cudaSuccess ? e : e2;
 }
 
 cudaError_t tc_causal_fwd_fused(const void* q, const void* k, const void* v, void* o, float* seg, float* agg,
