@@ -114,6 +114,7 @@ constexpr int kScanBatch = 24;  // covers the segment counts the planner picks f
 __global__ void retention_scan_kernel(float* __restrict__ seg, float* __restrict__ S_out,
                                       const float* __restrict__ gamma, int H, int N, int P, int seg_len, size_t E,
                                       int sv, int Dk, int Dv) {
+    pdl_enter();  // launched with programmatic dependent launch
     const size_t e4 = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
     if (e4 >= E) return;
     const size_t bh = blockIdx.y;
@@ -478,8 +479,10 @@ cudaError_t retention_scan(float* seg, float* S_out, const float* gamma, const l
     const size_t E = (size_t)p.sk * p.sv;  // a multiple of 256 for the supported head sizes
     const dim3 grid((unsigned)((E / 4 + 127) / 128), s.B * s.H);
     launch_begin("retention_scan", st);
-    retention_scan_kernel<<<grid, 128, 0, st>>>(seg, S_out, gamma, s.H, s.N, p.P, p.cps * p.C, E, p.sv, s.Dk, s.Dv);
-    return launch_end("retention_scan", st);
+    const cudaError_t le = launch_pdl(retention_scan_kernel, grid, dim3(128), 0, st, seg, S_out, gamma, s.H, s.N, p.P,
+                                      p.cps * p.C, E, p.sv, s.Dk, s.Dv);
+    const cudaError_t le2 = launch_end("retention_scan", st);
+    return le != cudaSuccess ? le : le2;
 }
 
 cudaError_t retention_out(const void* q, const void* k, const void* v, const float* gamma, void* o, const float* seg,

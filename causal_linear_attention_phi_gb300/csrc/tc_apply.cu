@@ -64,6 +64,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 tc_noncausal_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_out,
                           const float* __restrict__ totals, int N, int nchunks, int cps, int* err) {
     extern __shared__ uint8_t smem_raw[];
+    pdl_enter();  // launched with programmatic dependent launch
     constexpr int kKd = D / 16;  // K steps over dk (a 64-wide head is zero above)
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sSb = base + SmemLayout::Sb;
@@ -230,8 +231,9 @@ cudaError_t tc_noncausal_apply(const void* q, void* o, const float* totals, cons
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
     launch_begin("tc_noncausal_apply", st);
-    kern<<<dim3(p.P, BH), kThreads, kSmemBytes, st>>>(tq, to, totals, s.N, p.nchunks, p.cps, device_error_word());
-    return launch_end("tc_noncausal_apply", st);
+    const cudaError_t le = launch_pdl(kern, dim3(p.P, BH), dim3(kThreads), kSmemBytes, st, tq, to, totals, s.N, p.nchunks, p.cps, device_error_word());
+    const cudaError_t le2 = launch_end("tc_noncausal_apply", st);
+    return le != cudaSuccess ? le : le2;
 }
 
 }  // namespace la

@@ -73,6 +73,7 @@ tc_noncausal_bwd_query_kernel(const __grid_constant__ CUtensorMap tm_q, const __
                               const __grid_constant__ CUtensorMap tm_dq, const float* __restrict__ totS,
                               float* __restrict__ seg_R, int N, int nchunks, int cps, int P, int* err) {
     extern __shared__ uint8_t smem_raw[];
+    pdl_enter();  // launched with programmatic dependent launch
     constexpr int kKd = D / 16;  // K steps over a head dimension (a 64-wide head is zero above)
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     auto sQb = [&](int b) { return base + QSmem::Q0 + b * kTileBytes; };
@@ -382,6 +383,7 @@ tc_noncausal_bwd_key_kernel(const __grid_constant__ CUtensorMap tm_k, const __gr
                             const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
                             const float* __restrict__ totR, int N, int nchunks, int cps, int* err) {
     extern __shared__ uint8_t smem_raw[];
+    pdl_enter();  // launched with programmatic dependent launch
     constexpr int kKd = D / 16;
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     auto sKb = [&](int b) { return base + KSmem::K0 + b * kTileBytes; };
@@ -567,9 +569,10 @@ cudaError_t tc_noncausal_bwd_query(const void* q, const void* dout, void* dq, co
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kQSmemBytes);
     if (e != cudaSuccess) return e;
     launch_begin("tc_noncausal_bwd_query", st);
-    kern<<<dim3(p.P, BH), kThreads, kQSmemBytes, st>>>(tq, td, tdq, totS, seg_R, s.N, p.nchunks, p.cps, p.P,
+    const cudaError_t le = launch_pdl(kern, dim3(p.P, BH), dim3(kThreads), kQSmemBytes, st, tq, td, tdq, totS, seg_R, s.N, p.nchunks, p.cps, p.P,
                                                        device_error_word());
-    return launch_end("tc_noncausal_bwd_query", st);
+    const cudaError_t le2 = launch_end("tc_noncausal_bwd_query", st);
+    return le != cudaSuccess ? le : le2;
 }
 
 cudaError_t tc_noncausal_bwd_key(const void* k, const void* v, void* dk, void* dv, const float* totR,
@@ -584,9 +587,10 @@ cudaError_t tc_noncausal_bwd_key(const void* k, const void* v, void* dk, void* d
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kKSmemBytes);
     if (e != cudaSuccess) return e;
     launch_begin("tc_noncausal_bwd_key", st);
-    kern<<<dim3(p.P, BH), kThreads, kKSmemBytes, st>>>(tk, tv, tdk, tdv, totR, s.N, p.nchunks, p.cps,
+    const cudaError_t le = launch_pdl(kern, dim3(p.P, BH), dim3(kThreads), kKSmemBytes, st, tk, tv, tdk, tdv, totR, s.N, p.nchunks, p.cps,
                                                        device_error_word());
-    return launch_end("tc_noncausal_bwd_key", st);
+    const cudaError_t le2 = launch_end("tc_noncausal_bwd_key", st);
+    return le != cudaSuccess ? le : le2;
 }
 
 }  // namespace la

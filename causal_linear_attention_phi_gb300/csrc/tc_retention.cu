@@ -105,6 +105,7 @@ tc_retention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                     const float* __restrict__ gamma, int H, float* __restrict__ seg, int N, int nchunks, int cps,
                     int P, int* err) {
     extern __shared__ uint8_t smem_raw[];
+    pdl_enter();  // launched with programmatic dependent launch
     constexpr int kKd = D / 16;  // K steps of a product over a head dimension (a 64-wide head is zero above)
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sQ = base + SmemLayout::Q;
@@ -382,8 +383,9 @@ cudaError_t tc_retention_fwd(const void* q, const void* k, const void* v, const 
     if (e != cudaSuccess) return e;
     const char* name = out_pass ? "tc_retention_out" : "tc_retention_sums";
     launch_begin(name, st);
-    kern<<<grid, kThreads, kSmemBytes, st>>>(tq, tk, tv, to, gamma, s.H, seg, s.N, p.nchunks, p.cps, p.P, err);
-    return launch_end(name, st);
+    const cudaError_t le = launch_pdl(kern, grid, dim3(kThreads), kSmemBytes, st, tq, tk, tv, to, gamma, s.H, seg, s.N, p.nchunks, p.cps, p.P, err);
+    const cudaError_t le2 = launch_end(name, st);
+    return le != cudaSuccess ? le : le2;
 }
 
 }  // namespace la
