@@ -506,11 +506,8 @@ tc_bwd_forward_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
 // X[0,64), A^T bf16 in X[64,128).
 constexpr uint32_t kRR = 0, kRDK = 128, kRDV = 256, kRX = 384;
 
-// Q and V (last read by the dK~ products) arrive and are released apart from K and
-// dO (last read by the dV products), so the next chunk's Q and V load while the dV
-// products run.
 struct RevSweepBars {
-    uint64_t full_qv, empty_qv, full_kd, empty_kd;
+    uint64_t full, empty;
     uint64_t ready, rb_ready, masks_ready;
     uint64_t at_dt_done, dk_done, dkv_done;  // dk_done: the dK~ products; dkv_done: the dV products too
     uint64_t final_mma;
@@ -585,28 +582,24 @@ tc_bwd_reverse_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
 
     if (warp == 0) {
         if (lane == 0) {
-            int armed_qv = -1, armed_kd = -1;
+            int armed = -1;
             for (int i = 0; i < nloc; ++i) {
                 const int t0 = (cend - 1 - i) * kC;
-                if (!mbar_wait(&bar->empty_qv, (i & 1) ^ 1, err, LA_ERR_TIMEOUT)) break;
-                mbar_arrive_expect_tx(&bar->full_qv, 2 * kTileBytes);
+                if (!mbar_wait(&bar->empty, (i & 1) ^ 1, err, LA_ERR_TIMEOUT)) break;
+                mbar_arrive_expect_tx(&bar->full, 4 * kTileBytes);
                 check_tile(64, t0, bh, N);
-                tma_load_3d(sQ, &tm_q, 0, t0, bh, &bar->full_qv);
-                tma_load_3d(sQ + kBlockBytes, &tm_q, 64, t0, bh, &bar->full_qv);
-                tma_load_3d(sV, &tm_v, 0, t0, bh, &bar->full_qv);
-                tma_load_3d(sV + kBlockBytes, &tm_v, 64, t0, bh, &bar->full_qv);
-                armed_qv = i;
-                if (!mbar_wait(&bar->empty_kd, (i & 1) ^ 1, err, LA_ERR_TIMEOUT)) break;
-                mbar_arrive_expect_tx(&bar->full_kd, 2 * kTileBytes);
-                tma_load_3d(sK, &tm_k, 0, t0, bh, &bar->full_kd);
-                tma_load_3d(sK + kBlockBytes, &tm_k, 64, t0, bh, &bar->full_kd);
-                tma_load_3d(sP, &tm_do, 0, t0, bh, &bar->full_kd);
-                tma_load_3d(sP + kBlockBytes, &tm_do, 64, t0, bh, &bar->full_kd);
-                armed_kd = i;
+                tma_load_3d(sQ, &tm_q, 0, t0, bh, &bar->full);
+                tma_load_3d(sQ + kBlockBytes, &tm_q, 64, t0, bh, &bar->full);
+                tma_load_3d(sK, &tm_k, 0, t0, bh, &bar->full);
+                tma_load_3d(sK + kBlockBytes, &tm_k, 64, t0, bh, &bar->full);
+                tma_load_3d(sV, &tm_v, 0, t0, bh, &bar->full);
+                tma_load_3d(sV + kBlockBytes, &tm_v, 64, t0, bh, &bar->full);
+                tma_load_3d(sP, &tm_do, 0, t0, bh, &bar->full);
+                tma_load_3d(sP + kBlockBytes, &tm_do, 64, t0, bh, &bar->full);
+                armed = i;
             }
             // no copy may still be landing when the CTA exits
-            if (armed_qv >= 0) mbar_wait(&bar->full_qv, armed_qv & 1, err, LA_ERR_TIMEOUT);
-            if (armed_kd >= 0) mbar_wait(&bar->full_kd, armed_kd & 1, err, LA_ERR_TIMEOUT);
+            if (armed >= 0) mbar_wait(&bar->full, armed & 1, err, LA_ERR_TIMEOUT);
         }
     } else if (warp == 1) {
         if (lane == 0) {
@@ -640,7 +633,6 @@ tc_bwd_reverse_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
                 for (int kk = 0; kk < 8; ++kk)  // dK~ += D'^T Q'
                     mma_ts(tmem + kRDK, tmem + kRX + 8 * kk, desc_mnmajor(aQ, kk), id_kmn, 1);
                 mma_commit(&bar->dk_done);  // the dk epilogue runs during the dV products
-                mma_commit(&bar->empty_qv);  // Q, V: no further read in this chunk
 #pragma unroll
                 for (int kk = 0; kk < kKd; ++kk)  // dV = K~ R_next
                     mma_ss(tmem + kRDV, desc_kmajor(aK, kk), desc_mnmajor(aRb, kk), id_kmn, kk > 0);
@@ -648,7 +640,7 @@ tc_bwd_reverse_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
                 for (int kk = 0; kk < 8; ++kk)  // dV += A'^T dO
                     mma_ts(tmem + kRDV, tmem + kRX + 64 + 8 * kk, desc_mnmajor(aP, kk), id_kmn, 1);
                 mma_commit(&bar->dkv_done);
-                mma_commit(&bar->empty_kd);  // K, P: no further read in this chunk
+                mma_commit(&bar->empty);  // Q, K, V, P: no further read in this chunk
             }
             mma_commit(&bar->final_mma);
             mbar_wait(&bar->final_mma, 0, err, LA_ERR_TIMEOUT);
@@ -682,7 +674,7 @@ tc_bwd_reverse_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
             // (a) per-row 1/den and g den; Q' = phi(Q) / den with the chunk's sum of (g den) Q';
             // phi on K (and its copy)
             if (ct == kStoreThread) bulk_wait_read_all();  // the previous dk / dv stores have left Kc and Rb
-            if (!RG::all(mbar_wait(&bar->full_qv, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
+            if (!RG::all(mbar_wait(&bar->full, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
             if (ct < 128) {
                 const bool v = ct < n;
                 ish[ct] = v ? 1.f / dg.x : 0.f;
@@ -690,7 +682,6 @@ tc_bwd_reverse_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
             }
             RG::sync();
             RG::phi_tile(sQ, nullptr, ct, n, D, gsh, rpart, nullptr, ish);
-            if (!RG::all(mbar_wait(&bar->full_kd, ph, err, LA_ERR_TIMEOUT))) { ok = false; break; }
             RG::phi_tile(sK, nullptr, ct, n, D, nullptr, nullptr, sKc);
             fence_proxy_async_smem();
             RG::sync();
