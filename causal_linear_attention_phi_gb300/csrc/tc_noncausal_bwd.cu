@@ -116,11 +116,16 @@ tc_noncausal_bwd_query_kernel(const __grid_constant__ CUtensorMap tm_q, const __
 #pragma unroll
         for (int cb = 0; cb < 2; ++cb) {
             uint32_t w[32], wl[32];
+            const float4* src = reinterpret_cast<const float4*>(tot + (size_t)r * kD + 64 * h + 32 * cb);
 #pragma unroll
-            for (int x = 0; x < 32; ++x) {
-                const float val = tot[(size_t)r * kD + 64 * h + 32 * cb + x];
-                w[x] = __float_as_uint(val);
-                wl[x] = __float_as_uint(val - __bfloat162float(__float2bfloat16_rn(val)));
+            for (int x4 = 0; x4 < 8; ++x4) {  // 16-byte loads: the workspace and each record row are 16-byte aligned
+                const float4 f = src[x4];
+                const float vals[4] = {f.x, f.y, f.z, f.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    w[4 * x4 + e] = __float_as_uint(vals[e]);
+                    wl[4 * x4 + e] = __float_as_uint(vals[e] - __bfloat162float(__float2bfloat16_rn(vals[e])));
+                }
             }
             row32_to_tile(w, sSb, r, 8 * h + 4 * cb);
             row32_to_tile(wl, sSbLo, r, 8 * h + 4 * cb);
@@ -421,8 +426,15 @@ tc_noncausal_bwd_key_kernel(const __grid_constant__ CUtensorMap tm_k, const __gr
 #pragma unroll
         for (int cb = 0; cb < 2; ++cb) {
             uint32_t w[32];
+            const float4* src = reinterpret_cast<const float4*>(tot + (size_t)r * kD + 64 * h + 32 * cb);
 #pragma unroll
-            for (int x = 0; x < 32; ++x) w[x] = __float_as_uint(tot[(size_t)r * kD + 64 * h + 32 * cb + x]);
+            for (int x4 = 0; x4 < 8; ++x4) {  // 16-byte loads: the workspace and each record row are 16-byte aligned
+                const float4 f = src[x4];
+                w[4 * x4] = __float_as_uint(f.x);
+                w[4 * x4 + 1] = __float_as_uint(f.y);
+                w[4 * x4 + 2] = __float_as_uint(f.z);
+                w[4 * x4 + 3] = __float_as_uint(f.w);
+            }
             row32_to_tile(w, sRb, r, 8 * h + 4 * cb);
         }
         if (ct < kD) rsh[ct] = tot[(size_t)kD * kD + ct];
