@@ -98,10 +98,21 @@ tc_noncausal_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid
 #pragma unroll
         for (int cb = 0; cb < 2; ++cb) {
             uint32_t w[32];
+            const int c0 = 64 * h + 32 * cb;  // a 32-column block lies wholly inside or outside D
+            if (r < D && c0 < D) {
+                // 16-byte loads: the workspace is 16-byte aligned, and so is every record and row
+                const float4* src = reinterpret_cast<const float4*>(tot + (size_t)r * D + c0);
 #pragma unroll
-            for (int x = 0; x < 32; ++x) {
-                const int col = 64 * h + 32 * cb + x;
-                w[x] = __float_as_uint(r < D && col < D ? tot[(size_t)r * D + col] : 0.f);
+                for (int x4 = 0; x4 < 8; ++x4) {
+                    const float4 f = src[x4];
+                    w[4 * x4] = __float_as_uint(f.x);
+                    w[4 * x4 + 1] = __float_as_uint(f.y);
+                    w[4 * x4 + 2] = __float_as_uint(f.z);
+                    w[4 * x4 + 3] = __float_as_uint(f.w);
+                }
+            } else {
+#pragma unroll
+                for (int x = 0; x < 32; ++x) w[x] = 0u;
             }
             row32_to_tile(w, sSb, r, 8 * h + 4 * cb);
         }
