@@ -508,6 +508,7 @@ constexpr uint32_t kRR = 0, kRDK = 128, kRDV = 256, kRX = 384;
 
 struct RevSweepBars {
     uint64_t full, empty;
+    uint64_t dk_free;  // every compute warp has read this chunk's dK~ from TMEM
     uint64_t ready, rb_ready, masks_ready;
     uint64_t at_dt_done, dk_done, dkv_done;  // dk_done: the dK~ products; dkv_done: the dV products too
     uint64_t final_mma;
@@ -562,6 +563,7 @@ tc_bwd_reverse_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
     if (tid == 0) {
         uint64_t* b = reinterpret_cast<uint64_t*>(bar);
         for (int x = 0; x < (int)(sizeof(RevSweepBars) / 8); ++x) mbar_init(b + x, 1);
+        mbar_init(&bar->dk_free, RG::kWarps);  // one arrival per compute warp
         fence_mbar_init();
         tma_prefetch_desc(&tm_q);
         tma_prefetch_desc(&tm_k);
@@ -610,14 +612,19 @@ tc_bwd_reverse_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
                            aRb = smem_u32(sRb);
             for (int i = 0; i < nloc; ++i) {
                 const uint32_t ph = i & 1;
+                // V dO^T needs only the tiles as loaded: it runs while phi is applied, once the
+                // previous chunk's dK~ has been read out of the DK region
+                if (!mbar_wait(&bar->full, ph, err, LA_ERR_TIMEOUT)) break;
+                if (i > 0 && !mbar_wait(&bar->dk_free, (i - 1) & 1, err, LA_ERR_TIMEOUT)) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < kKd; ++kk)  // DK region = V dO^T (rows = keys)
+                    mma_ss(tmem + kRDK, desc_kmajor(aV, kk), desc_kmajor(aP, kk), id_kk, kk > 0);
                 if (!mbar_wait(&bar->ready, ph, err, LA_ERR_TIMEOUT)) break;
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < kKd; ++kk)  // DV region = A'^T = K~ Q'^T (rows = keys)
                     mma_ss(tmem + kRDV, desc_kmajor(aK, kk), desc_kmajor(aQ, kk), id_kk, kk > 0);
-#pragma unroll
-                for (int kk = 0; kk < kKd; ++kk)  // DK region = V dO^T (rows = keys)
-                    mma_ss(tmem + kRDK, desc_kmajor(aV, kk), desc_kmajor(aP, kk), id_kk, kk > 0);
                 mma_commit(&bar->at_dt_done);
                 if (!mbar_wait(&bar->rb_ready, ph, err, LA_ERR_TIMEOUT)) break;
                 tc_fence_after();
@@ -749,6 +756,9 @@ tc_bwd_reverse_sweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __gr
                 uint32_t w[32];
                 tmem_ld32(tmem + lb + kRDK, w);
                 tmem_ld_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar->dk_free);  // the next chunk's V dO^T may overwrite DK
 #pragma unroll
                 for (int c4 = 0; c4 < 4; ++c4) {
                     uint4* kp = reinterpret_cast<uint4*>(sKc + chunk_off(r, 4 * qt + c4));
