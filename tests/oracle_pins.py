@@ -20,8 +20,11 @@ GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
 
 
 def rel(x, y):
-    """max|x - y| / max|y| (max-normalised relative error)."""
+    """max|x - y| / max|y| (max-normalised relative error); inf when either side holds a
+    non-finite value, so that every `rel(...) < tol` check fails on it."""
     x, y = np.asarray(x, np.float64), np.asarray(y, np.float64)
+    if not (np.all(np.isfinite(x)) and np.all(np.isfinite(y))):
+        return float("inf")
     den = np.max(np.abs(y))
     return float(np.max(np.abs(x - y)) / (den if den > 0 else 1.0))
 
