@@ -115,12 +115,18 @@ __global__ void retention_scan_kernel(float* __restrict__ seg, float* __restrict
                                       const float* __restrict__ gamma, int H, int N, int P, int seg_len, size_t E,
                                       int sv, int Dk, int Dv) {
     pdl_enter();  // launched with programmatic dependent launch
+    const size_t bh = blockIdx.y;
+    // the segment decays, once per block (fp64 square-and-multiply is slow; every thread needs them)
+    __shared__ float decay[2];
+    if (threadIdx.x == 0) {
+        const double g = gamma[bh % H];
+        decay[0] = (float)pow_int(g, seg_len);
+        decay[1] = (float)pow_int(g, N - (P - 1) * seg_len);
+    }
+    __syncthreads();
+    const float d_full = decay[0], d_last = decay[1];
     const size_t e4 = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
     if (e4 >= E) return;
-    const size_t bh = blockIdx.y;
-    const double g = gamma[bh % H];
-    const float d_full = (float)pow_int(g, seg_len);
-    const float d_last = (float)pow_int(g, N - (P - 1) * seg_len);
     float* base = seg + bh * P * E + e4;
     float4 run = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int b0 = 0; b0 < P; b0 += kScanBatch) {
